@@ -1,0 +1,377 @@
+"""CPU oracle for one DSA decode layer (k-pooled indexer + sparse latent MLA).
+
+TEST INFRASTRUCTURE. Only the tests, the package smoke check and the benchmark's
+CPU-baseline leg may import or run this module. The product path never does: it
+runs CUDA kernels or fails.
+
+Plain float64 numpy, single-threaded where the BLAS is held to one thread,
+written for a reader to check against the pages by eye. Library primitives
+(a matrix product, a sort) serve as steps; there is no blocking, fusion or
+reordering beyond what the definitions state. bf16 rounding (nearest even) is
+applied only where the layer stores bf16: the normalised indexer keys, the pooled
+keys, and the output ``y``.
+
+Sources (page title, section):
+
+* ``metrale_model_arch/glm5next_dsa/mod.rs``, module doc, "Shape of the pipeline"
+  and "Checkpoint and kernel facts the code depends on"; ``Glm5NextDsaConfig``
+  methods ``select_k`` and ``out_width``.
+* ``metrale_model_arch/glm5next_dsa/tp.rs``, module doc, "Why the indexer is
+  replicated" (the index-score formula).
+* ``metrale_model_arch/glm5next_dsa/build.rs``, module doc "The transforms, each
+  done once at load", ``absorb_q`` and ``absorb_o``.
+
+Every function here is pinned by a CPU test against values or identities fixed
+independently of it (tests/test_oracle_pins.py, tests/golden/); none is "parity
+unpinned".
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+
+F64 = np.float64
+
+
+# ---------------------------------------------------------------------------
+# bf16 storage rounding
+
+
+def bf16_round(x) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 value, ties to even.
+
+    bfloat16 has 8 significant bits and float32's exponent range (normal numbers
+    down to 2^-126, subnormal spacing 2^-133, largest finite 65280 * 2^112).
+    The host uploads of the layer round this way (``build.rs``, ``up_bf16``:
+    ``half::bf16::from_f32``).
+    """
+    x = np.asarray(x, dtype=F64)
+    out = np.array(x, dtype=F64, copy=True)
+    fin = np.isfinite(x) & (x != 0)
+    xs = x[fin]
+    _, e = np.frexp(xs)  # xs = m * 2**e, 0.5 <= |m| < 1
+    # quantum = 2**(exponent of leading bit - 7); subnormals share 2**-133.
+    q_exp = np.maximum(e - 1, -126) - 7
+    q = np.ldexp(np.ones_like(xs), q_exp)
+    r = np.rint(xs / q) * q  # rint: round half to even; xs/q is exact
+    big = np.ldexp(F64(255.0), 120)  # largest finite bf16 = 255 * 2^120
+    r = np.where(np.abs(r) > big, np.copysign(np.inf, r), r)
+    out[fin] = r
+    return out
+
+
+# ---------------------------------------------------------------------------
+# (a1) k_norm + kpool_compress
+
+
+def layernorm_bias(x, gamma, beta, eps: float) -> np.ndarray:
+    """``indexer.k_norm``: a LayerNorm with a bias over the last axis.
+
+    ``(x - mean) / sqrt(var + eps) * gamma + beta`` with the biased variance.
+    mod.rs, "Checkpoint and kernel facts": k_norm is a LayerNorm with a bias (an
+    RMSNorm would drop the mean and the bias). Returns float64, before the bf16
+    store.
+    """
+    x = np.asarray(x, dtype=F64)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + F64(eps)) * np.asarray(gamma, F64) + np.asarray(beta, F64)
+
+
+def kpool_compress(k_tok, gate_tok, valid_tok, ape, gamma, beta, eps: float,
+                   first_key: int, kpool: int):
+    """Pool one sequence's indexer keys (``dsa_kpool_compress`` after ``k_norm``).
+
+    Inputs are token-major for ONE sequence in logical order: ``k_tok`` and
+    ``gate_tok`` ``[S, ihd]``, ``valid_tok [S]``, ``ape [kpool, ihd]``.
+
+    mod.rs "Shape of the pipeline": ``k, gate, valid, ape -> kpool_compress ->
+    pool keys/indices/valid``. mod.rs "Checkpoint and kernel facts": the pool
+    softmax runs over the pool-slot axis, per channel; pooling starts at
+    ``first_key``; a pool counts only if every one of its slots is valid, so a
+    trailing partial pool is not a pool.
+
+    Pool ``p`` holds tokens ``t_s = first_key + p*kpool + s``, ``s < kpool``:
+    ``kn = bf16(LN(k))``; logit ``l_s[c] = gate[t_s, c] + ape[s, c]``;
+    ``kpool[p, c] = bf16(sum_s softmax_s(l[:, c])_s * kn[t_s, c])``.
+    Invalid pools are written as zeros (only their flag is read downstream).
+
+    Returns ``(keys [P, ihd] float64 of bf16 values, pool_valid [P] uint8,
+    pool_idx [P, kpool] int64)``.
+    """
+    k_tok = np.asarray(k_tok, dtype=F64)
+    gate_tok = np.asarray(gate_tok, dtype=F64)
+    valid_tok = np.asarray(valid_tok)
+    S, ihd = k_tok.shape
+    P = max(0, (S - first_key) // kpool)
+    keys = np.zeros((P, ihd), dtype=F64)
+    pool_valid = np.zeros(P, dtype=np.uint8)
+    pool_idx = first_key + np.arange(P)[:, None] * kpool + np.arange(kpool)[None, :]
+    if P == 0:
+        return keys, pool_valid, pool_idx.astype(np.int64)
+    toks = pool_idx  # [P, kpool]
+    kn = bf16_round(layernorm_bias(k_tok[toks], gamma, beta, eps))  # [P, kpool, ihd]
+    logits = gate_tok[toks] + np.asarray(ape, dtype=F64)[None, :, :]  # [P, kpool, ihd]
+    m = logits.max(axis=1, keepdims=True)
+    e = np.exp(logits - m)
+    alpha = e / e.sum(axis=1, keepdims=True)  # softmax over the slot axis
+    pooled = bf16_round((alpha * kn).sum(axis=1))
+    ok = np.all(valid_tok[toks] != 0, axis=1)
+    keys[ok] = pooled[ok]
+    pool_valid[ok] = 1
+    return keys, pool_valid, pool_idx.astype(np.int64)
+
+
+# ---------------------------------------------------------------------------
+# (a2) index_scores
+
+
+def index_scores(qidx_row, w_row, keys, pool_valid, ctx_len: int, first_key: int,
+                 kpool: int, scale: float, p_stride: Optional[int] = None) -> np.ndarray:
+    """Scores of one query row over one sequence's pools (``dsa_index_scores``).
+
+    tp.rs, "Why the indexer is replicated": ``index_scores`` adds
+    ``weights[h] * relu(scale * dot)`` over the indexer heads; scores are
+    ``[q_rows, n_pools]``. build.rs, transform 2: the kernel does not apply
+    ``index_heads^-0.5``; ``w`` arrives with it folded in.
+
+    ``score[p] = sum_h w[h] * relu(scale * <qidx[h], keys[p]>)`` when pool p is a
+    candidate: flagged valid, and visible to this row (its last slot
+    ``first_key + (p+1)*kpool - 1`` is before ``ctx_len``). Every other entry of
+    the ``p_stride``-wide row is ``-inf``.
+    """
+    q = np.asarray(qidx_row, dtype=F64)  # [Hi, ihd]
+    w = np.asarray(w_row, dtype=F64)  # [Hi]
+    keys = np.asarray(keys, dtype=F64)  # [P, ihd]
+    P = keys.shape[0]
+    if p_stride is None:
+        p_stride = P
+    out = np.full(p_stride, -np.inf, dtype=F64)
+    n_vis = max(0, (ctx_len - first_key) // kpool)
+    n = min(P, n_vis, p_stride)
+    if n == 0:
+        return out
+    dots = keys[:n] @ q.T  # [n, Hi]
+    s = (np.maximum(F64(scale) * dots, 0.0) * w[None, :]).sum(axis=1)
+    cand = np.asarray(pool_valid[:n]) != 0
+    out[:n] = np.where(cand, s, -np.inf)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# (a3) topk_pools, (a4) expand_selection
+
+
+def select_k(index_topk: int, kpool: int, n_pools: int) -> int:
+    """Pools selected per query, capped by how many pools exist
+    (mod.rs, ``Glm5NextDsaConfig::select_k``)."""
+    return min(index_topk // kpool, n_pools)
+
+
+def topk_pools(scores_row, sk: int) -> np.ndarray:
+    """``dsa_topk_pools`` for one row: ``[P]`` scores -> ``[sk]`` pool ids.
+
+    mod.rs "Shape of the pipeline": ``topk_pools -> [Q, select_k] pool ids``.
+    Reading taken where the pages are silent: the chosen pools are the first
+    ``k' = min(sk, #finite)`` in the order (score descending, pool id ascending),
+    with -0.0 equal to +0.0; non-candidates (-inf) are never chosen; the chosen
+    ids are emitted in ascending order and the row is padded with -1.
+    """
+    s = np.asarray(scores_row, dtype=F64)
+    if np.isnan(s).any():
+        raise ValueError("topk_pools: NaN score")
+    ids = np.arange(s.shape[0])
+    fin = np.isfinite(s)
+    kk = min(sk, int(fin.sum()))
+    order = np.lexsort((ids[fin], -s[fin]))  # primary: -score; secondary: id
+    chosen = np.sort(ids[fin][order[:kk]])
+    out = np.full(sk, -1, dtype=np.int64)
+    out[:kk] = chosen
+    return out
+
+
+def out_width(index_topk: int, kpool: int, always_select_tail: bool = False) -> int:
+    """Width of the emitted index row (mod.rs, ``Glm5NextDsaConfig::out_width``)."""
+    return index_topk + (kpool - 1 if always_select_tail else 0)
+
+
+def expand_selection(pool_ids_row, first_key: int, kpool: int, width: int) -> np.ndarray:
+    """``dsa_expand_selection`` for one row: pool ids -> token ids.
+
+    mod.rs "Checkpoint and kernel facts": ``dsa_expand_selection`` writes -1 over
+    the whole index row before it stores any index, so every slot is written.
+    Pool id ``p`` at position ``j`` becomes tokens ``first_key + p*kpool + s`` at
+    positions ``j*kpool + s``.
+    """
+    row = np.full(width, -1, dtype=np.int64)
+    for j, p in enumerate(np.asarray(pool_ids_row)):
+        if p < 0:
+            continue
+        for s in range(kpool):
+            row[j * kpool + s] = first_key + int(p) * kpool + s
+    return row
+
+
+# ---------------------------------------------------------------------------
+# (a5) NoPE MLA restricted to the selected tokens, in latent space
+
+
+def sparse_mla_decode_row(qlat_row, ckv_seq, token_ids_row, softmax_scale: float,
+                          o_absorb=None):
+    """Attention of one query row over its selected tokens, then ``o_absorb``.
+
+    mod.rs "Shape of the pipeline": NoPE MLA restricted to the expanded tokens
+    (-1 = invalid). build.rs transforms 1 and 3: Q is absorbed through
+    ``kv_b_proj``'s K half, so scores are taken against the latent row itself,
+    and ``o_proj`` is absorbed through the V half, so the latent row is also the
+    value and the output projection maps ``[heads, kv_lora_rank]`` back to
+    hidden. NoPE: no rope section (mod.rs, ``is_nope``).
+
+    ``logit[h, t] = softmax_scale * <qlat[h], ckv[t]>`` over ``t`` in the row's
+    token ids ``>= 0``; ``olat[h] = sum_t softmax(logit[h])_t * ckv[t]``;
+    ``y[i] = sum_{h,c} o_absorb[i, h*kvl + c] * olat[h, c]``. An empty selection
+    gives ``olat = 0``.
+
+    Returns ``(olat [H, kvl], y_exact [hidden] or None, y_bf16 or None)``.
+    """
+    q = np.asarray(qlat_row, dtype=F64)  # [H, kvl]
+    ids = np.asarray(token_ids_row)
+    ids = ids[ids >= 0]
+    H, kvl = q.shape
+    if ids.size == 0:
+        olat = np.zeros((H, kvl), dtype=F64)
+    else:
+        kv = np.asarray(ckv_seq[ids], dtype=F64)  # [T, kvl]
+        logits = F64(softmax_scale) * (q @ kv.T)  # [H, T]
+        m = logits.max(axis=1, keepdims=True)
+        p = np.exp(logits - m)
+        p /= p.sum(axis=1, keepdims=True)
+        olat = p @ kv
+    if o_absorb is None:
+        return olat, None, None
+    A = np.asarray(o_absorb, dtype=F64)  # [hidden, H*kvl]
+    y = A @ olat.reshape(-1)
+    return olat, y, bf16_round(y)
+
+
+# ---------------------------------------------------------------------------
+# Load-time absorptions (build.rs) and the two unabsorbed/dense references the
+# equivalence checks compare against.
+
+
+def absorb_q(q_b, kv_b, heads: int, nope: int, vd: int, kvl: int, ql: int) -> np.ndarray:
+    """build.rs ``absorb_q``:
+    ``q_absorb[h*kvl + c][k] = sum_r kv_b[h*(nope+vd) + r][c] * q_b[h*nope + r][k]``.
+
+    ``q_b [heads*nope, ql]`` (NoPE: ``qk_head_dim == nope``), ``kv_b
+    [heads*(nope+vd), kvl]``. Returns ``[heads*kvl, ql]``.
+    """
+    q_b = np.asarray(q_b, dtype=F64).reshape(heads, nope, ql)
+    kv_b = np.asarray(kv_b, dtype=F64).reshape(heads, nope + vd, kvl)
+    out = np.zeros((heads, kvl, ql), dtype=F64)
+    for h in range(heads):
+        k_half = kv_b[h, :nope, :]  # [nope, kvl]: rows r < nope of head h's block
+        out[h] = k_half.T @ q_b[h]  # [kvl, ql]: sum over r
+    return out.reshape(heads * kvl, ql)
+
+
+def absorb_o(o_proj, kv_b, heads: int, nope: int, vd: int, kvl: int, hidden: int) -> np.ndarray:
+    """build.rs ``absorb_o``:
+    ``o_absorb[i][h*kvl + c] = sum_r o_proj[i][h*vd + r] * kv_b[h*(nope+vd) + nope + r][c]``.
+
+    ``o_proj [hidden, heads*vd]``; each head's V half starts at row ``nope`` of
+    its ``kv_b`` block. Returns ``[hidden, heads*kvl]``.
+    """
+    o = np.asarray(o_proj, dtype=F64).reshape(hidden, heads, vd)
+    kv_b = np.asarray(kv_b, dtype=F64).reshape(heads, nope + vd, kvl)
+    out = np.zeros((hidden, heads, kvl), dtype=F64)
+    for h in range(heads):
+        v_half = kv_b[h, nope:, :]  # [vd, kvl]
+        out[:, h, :] = o[:, h, :] @ v_half
+    return out.reshape(hidden, heads * kvl)
+
+
+def mla_unabsorbed(q_lora, q_b, kv_b, o_proj, ckv_sel, heads: int, nope: int, vd: int,
+                   kvl: int, softmax_scale: float) -> np.ndarray:
+    """Standard (unabsorbed) NoPE MLA for one query over the given latent rows:
+    decompress the latent through ``kv_b_proj`` into per-head keys and values,
+    attend per head with ``qk_head_dim^-0.5`` scaling, project with ``o_proj``.
+    The reference that ``absorb_q``/``absorb_o`` must reproduce (build.rs module
+    doc: Q moves into the latent space; ``o_proj`` takes ``[heads, v_head_dim]``).
+    """
+    q_lora = np.asarray(q_lora, dtype=F64)
+    ql = q_lora.shape[0]
+    q = (np.asarray(q_b, dtype=F64) @ q_lora).reshape(heads, nope)
+    kv_b = np.asarray(kv_b, dtype=F64).reshape(heads, nope + vd, kvl)
+    c = np.asarray(ckv_sel, dtype=F64)  # [T, kvl]
+    outs = []
+    for h in range(heads):
+        k = c @ kv_b[h, :nope, :].T  # [T, nope]
+        v = c @ kv_b[h, nope:, :].T  # [T, vd]
+        logit = F64(softmax_scale) * (k @ q[h])
+        p = np.exp(logit - logit.max())
+        p /= p.sum()
+        outs.append(p @ v)
+    return np.asarray(o_proj, dtype=F64) @ np.concatenate(outs)
+
+
+def dense_masked_attention(qlat_row, ckv_seq, mask, softmax_scale: float) -> np.ndarray:
+    """Dense latent attention over ALL tokens of the sequence, with masked tokens'
+    logits set to -inf: the role of the pages' oracle kernels
+    (``dsa_topk_to_mask`` -> ``dsa_mla_masked_attn``, mod.rs
+    ``Glm5NextDsaKernels``)."""
+    q = np.asarray(qlat_row, dtype=F64)
+    kv = np.asarray(ckv_seq, dtype=F64)
+    logits = F64(softmax_scale) * (q @ kv.T)  # [H, S]
+    logits = np.where(np.asarray(mask, dtype=bool)[None, :], logits, -np.inf)
+    m = logits.max(axis=1, keepdims=True)
+    p = np.exp(logits - m)
+    p /= p.sum(axis=1, keepdims=True)
+    return p @ kv
+
+
+# ---------------------------------------------------------------------------
+# Cache addressing (the oracle's own, independent of the kernels')
+
+
+def sequence_tokens(cache, b: int, n_tokens: int, block_table=None, block_size: int = 0):
+    """Logical ``[n_tokens, ...]`` view of sequence ``b`` of a token cache:
+    contiguous ``[B, Smax, ...]`` or paged ``[NB, block_size, ...]`` through
+    ``block_table [B, max_blocks]``."""
+    cache = np.asarray(cache)
+    if block_table is None:
+        return cache[b, :n_tokens]
+    t = np.arange(n_tokens)
+    blk = np.asarray(block_table)[b, t // block_size]
+    return cache[blk, t % block_size]
+
+
+def sequence_pools(pcache, b: int, n_pools: int, block_table=None, pools_per_block: int = 0):
+    """Logical ``[n_pools, ...]`` view of sequence ``b`` of a pooled-key cache:
+    contiguous ``[B, Pcap, ...]`` or paged ``[NB, pools_per_block, ...]`` through
+    the same block table."""
+    pcache = np.asarray(pcache)
+    if block_table is None:
+        return pcache[b, :n_pools]
+    p = np.arange(n_pools)
+    blk = np.asarray(block_table)[b, p // pools_per_block]
+    return pcache[blk, p % pools_per_block]
+
+
+# ---------------------------------------------------------------------------
+# One query row end to end (a2..a5) on a pooled cache
+
+
+def decode_row(qidx_row, w_row, keys, pool_valid, ctx_len: int, first_key: int, kpool: int,
+               index_scale: float, index_topk: int, p_stride: int, qlat_row, ckv_seq,
+               softmax_scale: float, o_absorb=None):
+    """score -> top-k -> expand -> sparse latent MLA (-> o_absorb) for one row."""
+    s = index_scores(qidx_row, w_row, keys, pool_valid, ctx_len, first_key, kpool,
+                     index_scale, p_stride)
+    sk = select_k(index_topk, kpool, p_stride)
+    ids = topk_pools(s, sk)
+    tok = expand_selection(ids, first_key, kpool, out_width(index_topk, kpool))
+    olat, y, yb = sparse_mla_decode_row(qlat_row, ckv_seq, tok, softmax_scale, o_absorb)
+    return dict(scores=s, pool_ids=ids, token_ids=tok, olat=olat, y=y, y_bf16=yb)
