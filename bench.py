@@ -1,0 +1,476 @@
+"""Benchmark: DSA decode queries/s at 262,144-token context on one GB300 (or N
+independent replicas), with the HBM roofline fraction of the dominant stage.
+
+One step = one decode query per sequence for the whole batch: score -> select ->
+expand -> sparse latent MLA (split attention, combine, o_absorb projection), as a
+CUDA-graph replay of the four C-ABI calls. Inputs are resident in HBM; L2 is
+flushed (a 256 MiB write) between timed steps, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload 3] [--no-cpu-baseline] [--no-e2e]
+
+--impl reference times the CPU oracle (the plain float64 restatement of the
+method) on the host, one query row per step, single-threaded.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU oracle is timed single-threaded: hold numpy's BLAS to one thread before
+# numpy loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import ctypes
+import json
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_attention_decode_kpool_gb300 import workloads as W  # noqa: E402
+
+METRIC = "DSA decode queries/s (select + sparse MLA) at 262K ctx; % of HBM roofline"
+FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: no data-path collective)
+
+
+def dist_init(gpus: int):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (NVML read-only queries)
+
+
+class ClockSampler:
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+    def __init__(self, device: torch.device, period_s: float = 0.005):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.period = period_s
+        self._stop = threading.Event()
+        self._nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            p = torch.cuda.get_device_properties(device)
+            bus = "%08x:%02x:%02x.0" % (getattr(p, "pci_domain_id", 0), p.pci_bus_id,
+                                        p.pci_device_id)
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle for " + bus)
+            self._nvml, self._h = nv, h
+            self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+                self.max_mhz = int(mx.value)
+        except (OSError, AttributeError):
+            self._nvml = None
+
+    def _run(self):
+        nv, h = self._nvml, self._h
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(int(clk.value))
+            if self._reasons_fn(h, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self._nvml is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self._nvml is not None:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (the roofline numerator)
+
+
+def algorithmic_bytes(wl, layer) -> dict:
+    """Per step: pooled keys of candidate pools + pool flags, indexer q and w,
+    selected latent rows, absorbed Q, o_absorb once, the output."""
+    g = wl.geom
+    pv = layer.pool_valid
+    # candidate pools of each row = valid pools among those visible to the row
+    cand = 0
+    if wl.paged:
+        cand = int(pv.sum().item())  # decode rows see all their complete pools
+    else:
+        for r in range(wl.rows):
+            b = int(wl.row_seq[r])
+            nvis = max(0, (int(wl.row_ctx[r]) - g.first_key) // g.index_kpool)
+            cand += int(pv[b, :nvis].sum().item())
+    flags = sum(max(0, (int(wl.row_ctx[r]) - g.first_key) // g.index_kpool) for r in range(wl.rows))
+    keys = cand * g.index_head_dim * 2
+    q = wl.rows * g.index_heads * (g.index_head_dim * 2 + 4)
+    sel_tokens = int((layer.token_ids >= 0).sum().item())
+    latent = sel_tokens * g.kv_lora_rank * 2
+    qlat = wl.rows * g.heads * g.kv_lora_rank * 2
+    oabs = g.hidden * g.heads * g.kv_lora_rank * 2 if layer.o_absorb is not None else 0
+    y = wl.rows * g.hidden * 2 if layer.o_absorb is not None else 0
+    return {"score": keys + flags + q, "attend": latent + qlat + oabs + y,
+            "total": keys + flags + q + latent + qlat + oabs + y, "selected_tokens": sel_tokens,
+            "candidate_pools": cand}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm)
+
+
+class OracleRunner:
+    """Times the oracle's decode_row on rows of the workload. The oracle's own
+    pooled-key cache of a sequence is built once, untimed (it is layer state)."""
+
+    def __init__(self, wl):
+        from oracle import dsa_oracle as O
+
+        self.O, self.wl = O, wl
+        self._pools = {}
+        self._A = None
+
+    def _tokens(self, t: torch.Tensor, b: int) -> np.ndarray:
+        """Logical rows of sequence b of a cache, gathered on the raw bits and only
+        then widened (the whole 262K-token latent cache would be 4 GiB as f32)."""
+        wl = self.wl
+        bt = None if wl.block_table is None else wl.block_table.numpy()
+        raw = t.view(torch.int16).numpy() if t.dtype == torch.bfloat16 else t.numpy()
+        rows = self.O.sequence_tokens(raw, b, int(wl.seq_lens[b]), bt, wl.block_size or 0)
+        if t.dtype == torch.bfloat16:
+            return torch.from_numpy(np.ascontiguousarray(rows)).view(torch.bfloat16).float().numpy()
+        return rows
+
+    def _prep(self, r: int):
+        O, wl, g = self.O, self.wl, self.wl.geom
+        b = int(wl.row_seq[r])
+        if b not in self._pools:
+            f = lambda t: t.float().numpy().astype(np.float64)
+            keys, pv, _ = O.kpool_compress(self._tokens(wl.k_raw, b), self._tokens(wl.gate, b),
+                                           self._tokens(wl.valid, b), wl.ape.numpy(), f(wl.ln_w),
+                                           f(wl.ln_b), g.eps, g.first_key, g.index_kpool)
+            self._pools[b] = (keys, pv, self._tokens(wl.ckv, b))
+        if self._A is None and wl.o_absorb is not None:
+            self._A = wl.o_absorb.float().numpy()
+        return b
+
+    def run_row(self, r: int) -> float:
+        """Seconds for one query row (score, top-k, expand, attention, o_absorb)."""
+        O, wl, g = self.O, self.wl, self.wl.geom
+        b = self._prep(r)
+        keys, pv, ckv = self._pools[b]
+        q = wl.qidx[r].float().numpy()
+        w = wl.w[r].numpy()
+        ql = wl.qlat[r].float().numpy()
+        t0 = time.perf_counter()
+        O.decode_row(q, w, keys, pv, int(wl.row_ctx[r]), g.first_key, g.index_kpool,
+                     g.index_scale, g.index_topk, wl.p_stride, ql, ckv, g.softmax_scale, self._A)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, budget_s: float = 12.0, max_rows: int = 2) -> dict:
+    runner = OracleRunner(wl)
+    times, rows = [], []
+    for r in range(min(max_rows, wl.rows)):
+        runner._prep(r)
+        rows.append(r)
+        times.append(runner.run_row(r))
+        if sum(times) > budget_s:
+            break
+    # Repeat the prepared rows until the time budget is used.
+    i = 0
+    while sum(times) < budget_s and i < 50:
+        times.append(runner.run_row(rows[i % len(rows)]))
+        i += 1
+    v = len(times) / sum(times)
+    return {"value": v, "unit": "queries/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(times)} decode rows (sequences {rows}) of {wl.name}: score over all "
+                      f"{wl.p_stride} pools, top-k, expand, attention over the selected tokens, "
+                      f"o_absorb; float64 numpy, one thread; pooled-key cache built untimed",
+            "seconds": sum(times)}
+
+
+# ---------------------------------------------------------------------------
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    wl = W.WORKLOADS[args.workload]()
+    runner = OracleRunner(wl)
+    rows = [r % wl.rows for r in range(min(2, wl.rows))]
+    for r in rows:
+        runner._prep(r)
+    for i in range(args.warmup):
+        runner.run_row(rows[i % len(rows)])
+    ts = [runner.run_row(rows[i % len(rows)]) for i in range(args.steps)]
+    total = sum(ts)
+    v = args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "queries/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(wl, args),
+        "cpu_baseline": {"value": v, "unit": "queries/s", "cores": 1, "kind": "oracle",
+                         "sample": f"one decode query row per step (rows {rows}) of {wl.name}"},
+        "e2e": {"value": v, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl, args) -> dict:
+    g = wl.geom
+    return {"workload": wl.name, "sequences": wl.batch, "seq_len": int(wl.max_seq_len),
+            "query_rows": wl.rows, "index_kpool": g.index_kpool, "index_heads": g.index_heads,
+            "index_head_dim": g.index_head_dim, "index_topk": g.index_topk, "heads": g.heads,
+            "kv_lora_rank": g.kv_lora_rank, "hidden": g.hidden,
+            "paged_block": wl.block_size, "seed": wl.seed,
+            "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        barrier(ws)
+        return
+
+    import __graft_entry__ as ge
+    from sparse_attention_decode_kpool_gb300.pipeline import DsaDecodeLayer
+
+    if rank == 0 or ws == 1:
+        ge.build()
+    barrier(ws)
+    ge.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    wl = W.WORKLOADS[args.workload]()
+    layer = DsaDecodeLayer(wl, device=str(dev))
+    layer.compress()
+    torch.cuda.synchronize()
+
+    # compress alone (setup stage, reported on its own)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ct = []
+    for _ in range(3):
+        flush.zero_()
+        e0.record()
+        layer.compress()
+        e1.record()
+        torch.cuda.synchronize()
+        ct.append(e0.elapsed_time(e1))
+
+    layer.step()
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0, "device status flagged during the first step"
+
+    # Graph with stage-boundary timing events (external event nodes when supported).
+    stage_names = ["score", "select", "expand", "attend"]
+    try:
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+        graph_events = True
+    except TypeError:
+        ev, graph_events = None, False
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        layer.step()
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        if graph_events:
+            ev[0].record()
+            layer.score(); ev[1].record()
+            layer.select(); ev[2].record()
+            layer.expand(); ev[3].record()
+            layer.attend(); ev[4].record()
+        else:
+            layer.step()
+
+    launches = layer.launches_per_step()
+    for _ in range(args.warmup):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stage_ms = {k: 0.0 for k in stage_names}
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record()
+            graph.replay()
+            ends[i].record()
+            if graph_events:
+                ends[i].synchronize()
+                for j, k in enumerate(stage_names):
+                    stage_ms[k] += ev[j].elapsed_time(ev[j + 1])
+        torch.cuda.synchronize()
+    barrier(ws)
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = sum(step_ms) / args.steps
+    ms = max_over_ranks(ms, ws)
+    if not graph_events:  # eager per-stage timing pass (same stream, same kernels)
+        for i in range(args.steps):
+            flush.zero_()
+            ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev2[0].record(); layer.score(); ev2[1].record(); layer.select(); ev2[2].record()
+            layer.expand(); ev2[3].record(); layer.attend(); ev2[4].record()
+            ev2[4].synchronize()
+            for j, k in enumerate(stage_names):
+                stage_ms[k] += ev2[j].elapsed_time(ev2[j + 1])
+    stage_ms = {k: v / args.steps for k, v in stage_ms.items()}
+
+    queries = wl.rows * ws
+    value = queries / (ms * 1e-3)
+
+    # e2e: per-step query inputs from pinned host memory, result read back.
+    e2e = None
+    if not args.no_e2e:
+        h_qidx = wl.qidx.pin_memory()
+        h_w = wl.w.pin_memory()
+        h_qlat = wl.qlat.pin_memory()
+        h_ctx = torch.from_numpy(wl.row_ctx).pin_memory()
+        h_y = torch.empty_like(layer.y, device="cpu").pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (h_qidx, h_w, h_qlat, h_ctx))
+        d2h = h_y.numel() * h_y.element_size()
+        for _ in range(3):
+            layer.qidx.copy_(h_qidx, non_blocking=True)
+            graph.replay()
+        torch.cuda.synchronize()
+        t_e2e = []
+        for _ in range(args.steps):
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            layer.qidx.copy_(h_qidx, non_blocking=True)
+            layer.w.copy_(h_w, non_blocking=True)
+            layer.qlat.copy_(h_qlat, non_blocking=True)
+            layer.row_ctx.copy_(h_ctx, non_blocking=True)
+            graph.replay()
+            h_y.copy_(layer.y, non_blocking=True)
+            torch.cuda.synchronize()
+            t_e2e.append(time.perf_counter() - t0)
+        e2e_ms = max_over_ranks(1e3 * sum(t_e2e) / len(t_e2e), ws)
+        e2e = {"value": queries / (e2e_ms * 1e-3), "unit": "queries/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "path": "pinned host qidx/w/qlat/row_ctx -> device, graph replay, y -> host"}
+
+    if rank != 0:
+        return
+
+    peaks = {}
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        peaks = json.load(open(pk))
+    hbm = peaks.get("hbm_gbs")
+    peak_src = "measured" if hbm else "fallback"
+    hbm = hbm or 6800.0
+    ab = algorithmic_bytes(wl, layer)
+    dom = max(("score", "attend"), key=lambda k: stage_ms[k])
+    dom_bytes = ab[dom]
+    achieved = dom_bytes / (stage_ms[dom] * 1e-3) / 1e9
+    total_gbs = ab["total"] / (ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None, "peak_source": peak_src,
+                "kernel": {"attend": "dsa_sparse_mla_decode (split attention + combine + "
+                                     "o_absorb GEMV + sum)",
+                           "score": "dsa_score"}[dom],
+                "algorithmic_bytes_per_launch": dom_bytes,
+                "step_algorithmic_bytes": ab["total"], "step_achieved_gbs": total_gbs,
+                "step_frac": total_gbs / hbm}
+    line = {
+        "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(wl, args),
+        "roofline": roofline,
+        "stages_ms": stage_ms, "stage_timing": "graph event nodes" if graph_events else "eager pass",
+        "compress_ms": min(ct),
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

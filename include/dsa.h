@@ -1,0 +1,219 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DSA decode library, libdsa.so.
+ *
+ * One DeepSeek-Sparse-Attention decode step of a GLM-5.3-style layer, in the
+ * order of the pipeline in metrale_model_arch/glm5next_dsa/mod.rs, "Shape of the
+ * pipeline":
+ *
+ *   k, gate, valid, ape -> dsa_compress          -> pooled keys / pool flags
+ *                        -> dsa_score             -> [rows, p_stride] f32 scores
+ *                        -> dsa_select            -> [rows, select_k] pool ids
+ *                        -> dsa_expand            -> [rows, out_width] token ids
+ *                        -> dsa_sparse_mla_decode -> [rows, hidden] bf16 output
+ *
+ * Conventions shared by every entry point:
+ *
+ *  - Pointers to tensors are DEVICE pointers owned by the caller; the library
+ *    never frees or retains them past the call's stream work. Pointers to
+ *    dsa_paging structs and to size_t results are HOST pointers, read during
+ *    the call only.
+ *  - Tensors are dense row-major. bf16 values are passed as their 16-bit
+ *    patterns (dsa_bf16); the library rounds every bf16 it stores to nearest,
+ *    ties to even.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Every call only
+ *    enqueues work on it: no host synchronisation, no allocation. Calls that
+ *    need scratch take a caller-owned device `workspace` of at least the size
+ *    the matching *_workspace query reports.
+ *  - Return value: DSA_OK, or an error code with a message from
+ *    dsa_last_error(). Argument errors are found on the host before anything
+ *    is enqueued; nothing is launched then.
+ *  - `status` (nullable): a device int32 word the kernels OR DSA_STATUS_* bits
+ *    into when they meet an out-of-range token id or block-table entry. Such
+ *    entries are skipped (treated as absent); kernels never trap. The caller
+ *    clears the word and reads it after synchronising.
+ *  - Device-side values the host cannot see (sequence lengths, block-table
+ *    entries, token ids) are range-checked on the device against the sizes
+ *    given here.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_OK 0
+#define DSA_ERR_INVALID_ARG 1 /* null, negative, inconsistent or mis-sized argument */
+#define DSA_ERR_UNSUPPORTED 2 /* a size outside what the kernels are built for     */
+#define DSA_ERR_CONFIG 3      /* a layer-geometry rule of the pages is violated     */
+#define DSA_ERR_CUDA 4        /* a CUDA runtime error while enqueueing              */
+
+#define DSA_STATUS_BAD_TOKEN 1 /* token id < -1, or >= its sequence's length  */
+#define DSA_STATUS_BAD_BLOCK 2 /* block-table entry outside [0, num_blocks)    */
+
+#define DSA_KV_LORA_RANK 512 /* latent width the attention kernels are built for */
+#define DSA_MAX_KPOOL 16     /* most slots per pool dsa_compress handles         */
+
+typedef uint16_t dsa_bf16;
+
+/*
+ * Where a sequence's tokens (and pooled keys) live.
+ *
+ * Contiguous (block_table == NULL): a token cache is [batch, max_seq_len, D]
+ * and a pooled-key cache is [batch, max_seq_len / kpool, D]; pool p of
+ * sequence b is row b * (max_seq_len / kpool) + p.
+ *
+ * Paged (block_table != NULL): a token cache is [num_blocks, block_size, D];
+ * token t of sequence b is slot t % block_size of physical block
+ * block_table[b * max_blocks + t / block_size]. The pooled-key cache is
+ * [num_blocks, block_size / kpool, D] through the same table: pool p of
+ * sequence b is slot p % (block_size / kpool) of block
+ * block_table[b * max_blocks + p / (block_size / kpool)].
+ *
+ * seq_lens[b] (device) is the number of tokens sequence b holds; it must not
+ * exceed max_seq_len (contiguous) or max_blocks * block_size (paged).
+ * max_seq_len is a host-side upper bound used to size grids.
+ */
+typedef struct dsa_paging {
+    int32_t batch;
+    int32_t max_seq_len;
+    const int32_t* seq_lens;    /* device [batch]                          */
+    const int32_t* block_table; /* device [batch, max_blocks], or NULL     */
+    int32_t max_blocks;
+    int32_t block_size;
+    int64_t num_blocks;
+} dsa_paging;
+
+/* Message for the last error returned on this host thread ("" if none). */
+const char* dsa_last_error(void);
+
+/* ABI version of this header (bumped on any signature change). */
+int dsa_abi_version(void);
+#define DSA_ABI_VERSION 1
+
+/*
+ * Layer-geometry rules (mod.rs, Glm5NextDsaConfig::validate): index_kpool and
+ * index_topk positive (DSA_ERR_CONFIG), index_topk a multiple of index_kpool
+ * (DSA_ERR_CONFIG), index_kpool <= DSA_MAX_KPOOL (DSA_ERR_UNSUPPORTED; the
+ * pages' 8-slot register bound is replaced by ours, refused rather than
+ * truncated), kv_lora_rank == DSA_KV_LORA_RANK (0: DSA_ERR_CONFIG; other:
+ * DSA_ERR_UNSUPPORTED), local_heads > 0 (DSA_ERR_CONFIG).
+ */
+int dsa_validate_config(int index_kpool, int index_topk, int kv_lora_rank, int local_heads);
+
+/* Pools selected per row: min(index_topk / kpool, n_pools)
+ * (mod.rs, Glm5NextDsaConfig::select_k). Returns -1 on invalid input. */
+int dsa_select_k(int index_topk, int kpool, int n_pools);
+
+/*
+ * dsa_compress -- indexer k_norm fused with dsa_kpool_compress.
+ * mod.rs, "Checkpoint and kernel facts": k_norm is a LayerNorm with a bias; the
+ * pool softmax runs over the slot axis, per channel; pooling starts at
+ * first_key; a pool counts only if all its slots are valid, so a trailing
+ * partial pool is not a pool. build.rs transform 4: ape is f32.
+ *
+ *   kn[t, c]       = bf16((k[t,c] - mean_t) / sqrt(var_t + eps) * ln_w[c] + ln_b[c])
+ *   logit_s[c]     = gate[t_s, c] + ape[s, c],   t_s = first_key + p*kpool + s
+ *   kpool_out[p,c] = bf16(sum_s softmax_s(logit[c]) * kn[t_s, c])
+ *   pool_valid[p]  = all_s token_valid[t_s] != 0   (invalid pools: zero keys)
+ *   pool_idx[p,s]  = t_s                            (optional)
+ *
+ * k_raw, gate: token caches of width ihd (bf16); token_valid: token cache of
+ * width 1 (u8); ape [kpool, ihd] f32; ln_w, ln_b [ihd] bf16. Outputs are
+ * pooled-key caches (see dsa_paging): kpool_out width ihd (bf16), pool_valid
+ * width 1 (u8), pool_idx width kpool (i32, nullable). For each sequence b the
+ * pools p < floor((seq_lens[b] - first_key) / kpool) are written; other rows
+ * are not touched.
+ * Limits: ihd in {64, 128}; 1 <= kpool <= DSA_MAX_KPOOL; first_key >= 0.
+ * Paged: block_size % kpool == 0 and first_key % kpool == 0.
+ */
+int dsa_compress(const dsa_bf16* k_raw, const dsa_bf16* gate, const uint8_t* token_valid,
+                 const float* ape, const dsa_bf16* ln_w, const dsa_bf16* ln_b, float eps,
+                 const dsa_paging* pg, int first_key, int kpool, int ihd,
+                 dsa_bf16* kpool_out, uint8_t* pool_valid, int32_t* pool_idx,
+                 int32_t* status, void* stream);
+
+/*
+ * dsa_score -- dsa_index_scores. tp.rs, "Why the indexer is replicated": the
+ * score adds weights[h] * relu(scale * dot) over the indexer heads; build.rs
+ * transform 2: w arrives already multiplied by index_heads^-0.5.
+ *
+ *   scores[r, p] = sum_h w[r,h] * relu(scale * <qidx[r,h,:], kpool[p,:]>)
+ *
+ * when pool p of row r's sequence is a candidate: pool_valid[p] != 0 and its
+ * last slot first_key + (p+1)*kpool - 1 < row_ctx[r]; every other entry of the
+ * p_stride-wide row, up to p_stride, is -inf.
+ *
+ * qidx [rows, index_heads, ihd] bf16; w [rows, index_heads] f32; row_seq [rows]
+ * i32 (device, nullable: row r -> sequence r); row_ctx [rows] i32 (device,
+ * nullable: seq_lens[row_seq[r]]); kpool / pool_valid: pooled-key caches laid
+ * out as pg says; scores [rows, p_stride] f32.
+ * Limits: ihd in {64, 128}; 1 <= index_heads <= 64; p_stride >= 0.
+ */
+int dsa_score(const dsa_bf16* qidx, const float* w, int rows, int index_heads, int ihd,
+              const int32_t* row_seq, const int32_t* row_ctx,
+              const dsa_bf16* kpool, const uint8_t* pool_valid, const dsa_paging* pg,
+              int first_key, int kpool_size, float scale,
+              float* scores, int p_stride, int32_t* status, void* stream);
+
+/*
+ * dsa_select -- dsa_topk_pools. mod.rs "Shape of the pipeline": [Q, P] scores
+ * -> [Q, select_k] pool ids, select_k = min(index_topk / kpool, p_stride).
+ * Per row, k' = min(select_k, number of finite scores); the k' pools first in
+ * the order (score descending, pool id ascending; -0.0 equals +0.0) are
+ * written in ascending pool id, then -1 up to select_k. -inf is never chosen.
+ * NaN scores give unspecified (but in-bounds) results.
+ *
+ * scores [rows, p_stride] f32; pool_ids [rows, select_k] i32.
+ * Limits: p_stride <= 393,216.
+ */
+int dsa_select(const float* scores, int rows, int p_stride, int index_topk, int kpool,
+               int32_t* pool_ids, void* stream);
+
+/*
+ * dsa_expand -- dsa_expand_selection. mod.rs, "Checkpoint and kernel facts":
+ * the whole index row is -1 except the expanded tokens, so every slot is
+ * written: token_ids[r, j*kpool + s] = first_key + pool_ids[r, j]*kpool + s for
+ * pool_ids[r, j] >= 0, else -1; positions >= sk*kpool are -1.
+ *
+ * pool_ids [rows, sk] i32; token_ids [rows, out_width] i32; out_width >= sk*kpool.
+ */
+int dsa_expand(const int32_t* pool_ids, int rows, int sk, int first_key, int kpool,
+               int out_width, int32_t* token_ids, void* stream);
+
+/*
+ * dsa_sparse_mla_decode -- NoPE MLA restricted to the selected tokens, in the
+ * latent space (mod.rs "Shape of the pipeline", last stage; build.rs module
+ * doc, transforms 1 and 3: Q is absorbed through kv_b_proj's K half, o_proj
+ * through its V half, so each latent row is both key and value).
+ *
+ *   logit[r,h,t] = softmax_scale * <qlat[r,h,:], ckv[t,:]>, t in token_ids[r] (>= 0)
+ *   olat[r,h,:]  = sum_t softmax_t(logit[r,h]) * ckv[t,:]   (0 if no token)
+ *   y[r,i]       = bf16(sum_{h,c} o_absorb[i, h*kv_lora_rank + c] * olat[r,h,c])
+ *
+ * qlat [rows, heads, kv_lora_rank] bf16; row_seq [rows] (device, nullable:
+ * row r -> sequence r); ckv: token cache of width kv_lora_rank (bf16) laid out
+ * as pg says; token_ids [rows, out_width] i32 (-1 = empty; ids must be below
+ * seq_lens of the row's sequence); o_absorb [hidden, heads*kv_lora_rank] bf16
+ * (nullable: then y must be NULL and only olat is produced); y [rows, hidden]
+ * bf16; olat [rows, heads, kv_lora_rank] f32 (nullable).
+ * Limits: kv_lora_rank == 512; hidden % 32 == 0; heads >= 1.
+ */
+int dsa_sparse_mla_decode_workspace(int rows, int heads, int kv_lora_rank, int out_width,
+                                    int hidden, int with_o_absorb, size_t* bytes);
+
+int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, int kv_lora_rank,
+                          const int32_t* row_seq, const dsa_bf16* ckv, const dsa_paging* pg,
+                          const int32_t* token_ids, int out_width, float softmax_scale,
+                          const dsa_bf16* o_absorb, int hidden, dsa_bf16* y, float* olat,
+                          int32_t* status, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -48,18 +48,13 @@ def bf16_round(x) -> np.ndarray:
     ``half::bf16::from_f32``).
     """
     x = np.asarray(x, dtype=F64)
-    out = np.array(x, dtype=F64, copy=True)
-    fin = np.isfinite(x) & (x != 0)
-    xs = x[fin]
-    _, e = np.frexp(xs)  # xs = m * 2**e, 0.5 <= |m| < 1
-    # quantum = 2**(exponent of leading bit - 7); subnormals share 2**-133.
-    q_exp = np.maximum(e - 1, -126) - 7
-    q = np.ldexp(np.ones_like(xs), q_exp)
-    r = np.rint(xs / q) * q  # rint: round half to even; xs/q is exact
+    _, e = np.frexp(x)  # x = m * 2**e, 0.5 <= |m| < 1 (e = 0 for 0, inf, nan)
+    # quantum = 2**(exponent of the leading bit - 7); subnormals share 2**-133.
+    q = np.ldexp(1.0, np.maximum(e - 1, -126) - 7)
+    r = np.rint(x / q) * q  # rint: round half to even; x/q is exact
     big = np.ldexp(F64(255.0), 120)  # largest finite bf16 = 255 * 2^120
     r = np.where(np.abs(r) > big, np.copysign(np.inf, r), r)
-    out[fin] = r
-    return out
+    return np.where(np.isfinite(x), r, x)
 
 
 # ---------------------------------------------------------------------------
@@ -75,9 +70,9 @@ def layernorm_bias(x, gamma, beta, eps: float) -> np.ndarray:
     store.
     """
     x = np.asarray(x, dtype=F64)
-    mu = x.mean(axis=-1, keepdims=True)
-    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
-    return (x - mu) / np.sqrt(var + F64(eps)) * np.asarray(gamma, F64) + np.asarray(beta, F64)
+    d = x - x.mean(axis=-1, keepdims=True)
+    var = (d * d).mean(axis=-1, keepdims=True)
+    return d / np.sqrt(var + F64(eps)) * np.asarray(gamma, F64) + np.asarray(beta, F64)
 
 
 def kpool_compress(k_tok, gate_tok, valid_tok, ape, gamma, beta, eps: float,

@@ -1,0 +1,149 @@
+"""Python binding of libdsa: the C-ABI entry points with the same names, taking
+torch CUDA tensors. Argument marshalling only: shape/dtype/device checks, then
+``data_ptr()`` and the current stream go to the C call. Every computation runs in
+the library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import DsaPaging, check
+
+__all__ = ["paging", "dsa_compress", "dsa_score", "dsa_select", "dsa_expand",
+           "dsa_sparse_mla_decode_workspace", "dsa_sparse_mla_decode", "dsa_select_k",
+           "dsa_validate_config", "DsaPaging"]
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "tensor") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def paging(seq_lens: torch.Tensor, max_seq_len: int, block_table: Optional[torch.Tensor] = None,
+           block_size: int = 0, num_blocks: int = 0) -> DsaPaging:
+    """Describe where sequences live (see ``dsa_paging`` in include/dsa.h).
+
+    The tensors must outlive every call that uses the returned descriptor."""
+    pg = DsaPaging()
+    pg.batch = int(seq_lens.numel())
+    pg.max_seq_len = int(max_seq_len)
+    pg.seq_lens = _ptr(seq_lens, torch.int32, "seq_lens")
+    if block_table is not None:
+        pg.block_table = _ptr(block_table, torch.int32, "block_table")
+        pg.max_blocks = int(block_table.shape[1])
+        pg.block_size = int(block_size)
+        pg.num_blocks = int(num_blocks)
+    else:
+        pg.block_table = None
+        pg.max_blocks = 0
+        pg.block_size = 0
+        pg.num_blocks = 0
+    return pg
+
+
+def dsa_validate_config(index_kpool: int, index_topk: int, kv_lora_rank: int,
+                        local_heads: int) -> None:
+    check(_lib.load().dsa_validate_config(index_kpool, index_topk, kv_lora_rank, local_heads))
+
+
+def dsa_select_k(index_topk: int, kpool: int, n_pools: int) -> int:
+    return _lib.load().dsa_select_k(index_topk, kpool, n_pools)
+
+
+def dsa_compress(k_raw, gate, token_valid, ape, ln_w, ln_b, eps: float, pg: DsaPaging,
+                 first_key: int, kpool: int, kpool_out, pool_valid, pool_idx=None, status=None,
+                 stream=None) -> None:
+    ihd = int(k_raw.shape[-1])
+    check(_lib.load().dsa_compress(
+        _ptr(k_raw, torch.bfloat16, "k_raw"), _ptr(gate, torch.bfloat16, "gate"),
+        _ptr(token_valid, torch.uint8, "token_valid"), _ptr(ape, torch.float32, "ape"),
+        _ptr(ln_w, torch.bfloat16, "ln_w"), _ptr(ln_b, torch.bfloat16, "ln_b"), float(eps),
+        ctypes.byref(pg), int(first_key), int(kpool), ihd,
+        _ptr(kpool_out, torch.bfloat16, "kpool_out"), _ptr(pool_valid, torch.uint8, "pool_valid"),
+        _ptr(pool_idx, torch.int32, "pool_idx"), _ptr(status, torch.int32, "status"),
+        _stream(stream)))
+
+
+def dsa_score(qidx, w, row_seq, row_ctx, kpool, pool_valid, pg: DsaPaging, first_key: int,
+              kpool_size: int, scale: float, scores, status=None, stream=None) -> None:
+    rows, heads, ihd = (int(x) for x in qidx.shape)
+    if tuple(w.shape) != (rows, heads):
+        raise ValueError(f"w must be [{rows}, {heads}]")
+    if scores.dim() != 2 or scores.shape[0] != rows:
+        raise ValueError("scores must be [rows, p_stride]")
+    check(_lib.load().dsa_score(
+        _ptr(qidx, torch.bfloat16, "qidx"), _ptr(w, torch.float32, "w"), rows, heads, ihd,
+        _ptr(row_seq, torch.int32, "row_seq"), _ptr(row_ctx, torch.int32, "row_ctx"),
+        _ptr(kpool, torch.bfloat16, "kpool"), _ptr(pool_valid, torch.uint8, "pool_valid"),
+        ctypes.byref(pg), int(first_key), int(kpool_size), float(scale),
+        _ptr(scores, torch.float32, "scores"), int(scores.shape[1]),
+        _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def dsa_select(scores, index_topk: int, kpool: int, pool_ids, stream=None) -> None:
+    rows, p_stride = (int(x) for x in scores.shape)
+    sk = dsa_select_k(index_topk, kpool, p_stride)
+    if tuple(pool_ids.shape) != (rows, max(sk, 0)):
+        raise ValueError(f"pool_ids must be [{rows}, {sk}]")
+    check(_lib.load().dsa_select(
+        _ptr(scores, torch.float32, "scores"), rows, p_stride, int(index_topk), int(kpool),
+        _ptr(pool_ids, torch.int32, "pool_ids"), _stream(stream)))
+
+
+def dsa_expand(pool_ids, first_key: int, kpool: int, token_ids, stream=None) -> None:
+    rows, sk = (int(x) for x in pool_ids.shape)
+    if token_ids.dim() != 2 or token_ids.shape[0] != rows:
+        raise ValueError("token_ids must be [rows, out_width]")
+    check(_lib.load().dsa_expand(
+        _ptr(pool_ids, torch.int32, "pool_ids"), rows, sk, int(first_key), int(kpool),
+        int(token_ids.shape[1]), _ptr(token_ids, torch.int32, "token_ids"), _stream(stream)))
+
+
+def dsa_sparse_mla_decode_workspace(rows: int, heads: int, out_width: int, hidden: int,
+                                    with_o_absorb: bool, kv_lora_rank: int = 512) -> int:
+    n = ctypes.c_size_t(0)
+    check(_lib.load().dsa_sparse_mla_decode_workspace(
+        int(rows), int(heads), int(kv_lora_rank), int(out_width), int(hidden),
+        1 if with_o_absorb else 0, ctypes.byref(n)))
+    return int(n.value)
+
+
+def dsa_sparse_mla_decode(qlat, row_seq, ckv, pg: DsaPaging, token_ids, softmax_scale: float,
+                          o_absorb=None, y=None, olat=None, status=None, workspace=None,
+                          stream=None) -> None:
+    rows, heads, kvl = (int(x) for x in qlat.shape)
+    ow = int(token_ids.shape[1])
+    hidden = int(o_absorb.shape[0]) if o_absorb is not None else 0
+    if o_absorb is not None and tuple(o_absorb.shape) != (hidden, heads * kvl):
+        raise ValueError(f"o_absorb must be [hidden, {heads * kvl}]")
+    if y is not None and tuple(y.shape) != (rows, hidden):
+        raise ValueError(f"y must be [{rows}, {hidden}]")
+    if olat is not None and tuple(olat.shape) != (rows, heads, kvl):
+        raise ValueError(f"olat must be [{rows}, {heads}, {kvl}]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check(_lib.load().dsa_sparse_mla_decode(
+        _ptr(qlat, torch.bfloat16, "qlat"), rows, heads, kvl,
+        _ptr(row_seq, torch.int32, "row_seq"), _ptr(ckv, torch.bfloat16, "ckv"),
+        ctypes.byref(pg), _ptr(token_ids, torch.int32, "token_ids"), ow, float(softmax_scale),
+        _ptr(o_absorb, torch.bfloat16, "o_absorb"), hidden, _ptr(y, torch.bfloat16, "y"),
+        _ptr(olat, torch.float32, "olat"), _ptr(status, torch.int32, "status"),
+        _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)))

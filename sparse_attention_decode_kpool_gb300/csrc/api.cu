@@ -1,0 +1,173 @@
+// Host-side core of libdsa: error reporting, geometry rules, paging checks, and
+// dsa_expand (expand_selection).
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <atomic>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "common.cuh"
+
+namespace dsa {
+
+static thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(DSA_ERR_CUDA, "%s: CUDA error %d (%s)", what, (int)e, cudaGetErrorString(e));
+}
+
+int sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) {
+        int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+int set_max_smem(const void* kernel, int bytes) {
+    static std::mutex mu;
+    static std::set<std::pair<int, std::pair<const void*, int>>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_pair(dev, std::make_pair(kernel, bytes));
+    if (done.count(key)) return DSA_OK;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    done.insert(key);
+    return DSA_OK;
+}
+
+int check_paging(const dsa_paging* pg, int kpool, Paging* out) {
+    if (!pg) return fail(DSA_ERR_INVALID_ARG, "paging descriptor is NULL");
+    if (pg->batch < 1) return fail(DSA_ERR_INVALID_ARG, "paging: batch %d < 1", pg->batch);
+    if (pg->max_seq_len < 0)
+        return fail(DSA_ERR_INVALID_ARG, "paging: max_seq_len %d < 0", pg->max_seq_len);
+    if (!pg->seq_lens) return fail(DSA_ERR_INVALID_ARG, "paging: seq_lens is NULL");
+    if (pg->block_table) {
+        if (pg->block_size < 1 || pg->max_blocks < 1 || pg->num_blocks < 1)
+            return fail(DSA_ERR_INVALID_ARG,
+                        "paging: block_size %d, max_blocks %d, num_blocks %lld must be >= 1",
+                        pg->block_size, pg->max_blocks, (long long)pg->num_blocks);
+        if ((long long)pg->max_blocks * pg->block_size < pg->max_seq_len)
+            return fail(DSA_ERR_INVALID_ARG,
+                        "paging: max_blocks*block_size %lld < max_seq_len %d",
+                        (long long)pg->max_blocks * pg->block_size, pg->max_seq_len);
+        if (kpool > 0 && pg->block_size % kpool != 0)
+            return fail(DSA_ERR_UNSUPPORTED, "paging: block_size %d is not a multiple of kpool %d",
+                        pg->block_size, kpool);
+    }
+    out->seq_lens = pg->seq_lens;
+    out->block_table = pg->block_table;
+    out->num_blocks = pg->num_blocks;
+    out->batch = pg->batch;
+    out->max_seq_len = pg->max_seq_len;
+    out->max_blocks = pg->max_blocks;
+    out->block_size = pg->block_size;
+    return DSA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// dsa_expand: one thread per output slot; each slot written exactly once.
+
+__global__ void expand_kernel(const int32_t* __restrict__ pool_ids, int rows, int sk,
+                              int first_key, int kpool, int out_width,
+                              int32_t* __restrict__ token_ids) {
+    long long n = (long long)rows * out_width;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        int r = (int)(i / out_width);
+        int j = (int)(i % out_width);
+        int slot = j / kpool;
+        int v = -1;
+        if (slot < sk) {
+            int p = __ldg(pool_ids + (long long)r * sk + slot);
+            if (p >= 0) v = first_key + p * kpool + (j - slot * kpool);
+        }
+        token_ids[i] = v;
+    }
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+const char* dsa_last_error(void) { return g_err; }
+
+int dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+int dsa_validate_config(int index_kpool, int index_topk, int kv_lora_rank, int local_heads) {
+    if (index_kpool <= 0 || index_topk <= 0)
+        return fail(DSA_ERR_CONFIG, "DSA needs index_kpool > 0 and index_topk > 0 (got %d, %d)",
+                    index_kpool, index_topk);
+    if (index_topk % index_kpool != 0)
+        return fail(DSA_ERR_CONFIG,
+                    "index_topk %d is not a multiple of index_kpool %d: the pool budget is "
+                    "index_topk / index_kpool",
+                    index_topk, index_kpool);
+    if (index_kpool > DSA_MAX_KPOOL)
+        return fail(DSA_ERR_UNSUPPORTED,
+                    "index_kpool %d exceeds the %d slots dsa_compress pools; refused instead of "
+                    "pooling only the first slots",
+                    index_kpool, DSA_MAX_KPOOL);
+    if (kv_lora_rank == 0) return fail(DSA_ERR_CONFIG, "MLA needs kv_lora_rank > 0");
+    if (kv_lora_rank != DSA_KV_LORA_RANK)
+        return fail(DSA_ERR_UNSUPPORTED,
+                    "kv_lora_rank %d: the attention kernels are built for a %d-wide latent",
+                    kv_lora_rank, DSA_KV_LORA_RANK);
+    if (local_heads <= 0) return fail(DSA_ERR_CONFIG, "zero attention heads (local_heads %d)",
+                                      local_heads);
+    return DSA_OK;
+}
+
+int dsa_select_k(int index_topk, int kpool, int n_pools) {
+    if (index_topk <= 0 || kpool <= 0 || n_pools < 0) return -1;
+    int k = index_topk / kpool;
+    return k < n_pools ? k : n_pools;
+}
+
+int dsa_expand(const int32_t* pool_ids, int rows, int sk, int first_key, int kpool,
+               int out_width, int32_t* token_ids, void* stream) {
+    if (rows < 0 || sk < 0 || first_key < 0 || kpool < 1 || out_width < 0)
+        return fail(DSA_ERR_INVALID_ARG,
+                    "dsa_expand: rows %d, sk %d, first_key %d, kpool %d, out_width %d", rows, sk,
+                    first_key, kpool, out_width);
+    if ((long long)sk * kpool > out_width)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_expand: out_width %d < sk*kpool %lld", out_width,
+                    (long long)sk * kpool);
+    if (rows == 0 || out_width == 0) return DSA_OK;
+    if (!token_ids || (sk > 0 && !pool_ids))
+        return fail(DSA_ERR_INVALID_ARG, "dsa_expand: NULL tensor");
+    long long n = (long long)rows * out_width;
+    int threads = 256;
+    long long blocks = (n + threads - 1) / threads;
+    int cap = sm_count() * 8;
+    if (cap < 1) cap = 1024;
+    if (blocks > cap) blocks = cap;
+    expand_kernel<<<(int)blocks, threads, 0, (cudaStream_t)stream>>>(
+        pool_ids, rows, sk, first_key, kpool, out_width, token_ids);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_expand launch");
+    return DSA_OK;
+}
+
+}  // extern "C"

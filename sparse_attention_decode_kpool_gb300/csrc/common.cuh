@@ -1,0 +1,127 @@
+// Shared device and host helpers of libdsa (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dsa.h"
+
+namespace dsa {
+
+// ---------------------------------------------------------------------------
+// Host side: error state and launch bookkeeping (defined in api.cu).
+
+int fail(int code, const char* fmt, ...);  // records the message, returns code
+int cuda_fail(cudaError_t e, const char* what);
+int sm_count();                            // SMs of the current device (cached)
+int set_max_smem(const void* kernel, int bytes);  // once per (device, kernel)
+
+// Kernel-side copy of dsa_paging.
+struct Paging {
+    const int32_t* seq_lens;
+    const int32_t* block_table;
+    long long num_blocks;
+    int batch;
+    int max_seq_len;
+    int max_blocks;
+    int block_size;
+};
+
+int check_paging(const dsa_paging* pg, int kpool, Paging* out);
+
+// ---------------------------------------------------------------------------
+// Device side.
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float round_bf16(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ uint4 ldg16(const void* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// 16-byte load that bypasses L1 allocation: for data streamed exactly once.
+__device__ __forceinline__ uint4 ldg16_stream(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// D += A * B, m16n8k16, bf16 inputs, f32 accumulate (warp-wide).
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// 16-byte async copy global -> shared; src_bytes == 0 zero-fills without reading.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void flag_status(int32_t* status, int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// Physical row of token t of sequence b in a token cache (-1: bad block entry).
+__device__ __forceinline__ long long token_row(const Paging& pg, int b, int t) {
+    if (pg.block_table == nullptr) return (long long)b * pg.max_seq_len + t;
+    int blk = __ldg(pg.block_table + (long long)b * pg.max_blocks + t / pg.block_size);
+    if (blk < 0 || blk >= pg.num_blocks) return -1;
+    return (long long)blk * pg.block_size + t % pg.block_size;
+}
+
+// Physical row of pool p of sequence b in a pooled-key cache (-1: bad block entry).
+__device__ __forceinline__ long long pool_row(const Paging& pg, int b, int p, int kpool) {
+    if (pg.block_table == nullptr) return (long long)b * (pg.max_seq_len / kpool) + p;
+    int ppb = pg.block_size / kpool;
+    int blk = __ldg(pg.block_table + (long long)b * pg.max_blocks + p / ppb);
+    if (blk < 0 || blk >= pg.num_blocks) return -1;
+    return (long long)blk * ppb + p % ppb;
+}
+
+// Tokens a sequence can hold in its cache.
+__device__ __forceinline__ int seq_capacity(const Paging& pg) {
+    return pg.block_table == nullptr ? pg.max_seq_len : pg.max_blocks * pg.block_size;
+}
+
+}  // namespace dsa

@@ -1,0 +1,247 @@
+// dsa_compress: indexer k_norm (LayerNorm with bias) fused with k-pool compression.
+//
+// Page: metrale_model_arch/glm5next_dsa/mod.rs, "Checkpoint and kernel facts the code
+// depends on" (k_norm is a LayerNorm with a bias; the pool softmax runs over the slot
+// axis per channel; pooling starts at first_key; a pool counts only if every slot is
+// valid) and build.rs, transform 4 (ape is f32).
+//
+// Layout of the work: a pool of KP tokens x IHD channels is handled by IHD/8 lanes,
+// each lane owning 8 consecutive channels (one 16-byte vector per token row). All
+// KP rows of keys and gate logits are issued as 16-byte streaming loads before any
+// arithmetic, so a warp keeps 2 * KP * 512 bytes in flight. The per-token LayerNorm
+// reduces over the pool's lane group with xor shuffles (two passes: mean, then the
+// centred second moment); the normalised key is rounded to bf16 in registers, the
+// storage point of the unfused pipeline, and pooled with the slot softmax in f32.
+#include "common.cuh"
+
+namespace dsa {
+namespace {
+
+struct CompressArgs {
+    const uint16_t* k_raw;
+    const uint16_t* gate;
+    const uint8_t* valid;
+    const float* ape;
+    const uint16_t* ln_w;
+    const uint16_t* ln_b;
+    uint16_t* kout;
+    uint8_t* pvalid;
+    int32_t* pidx;
+    int32_t* status;
+    Paging pg;
+    float eps;
+    int first_key;
+    int kpool;
+};
+
+constexpr int kThreads = 256;
+
+template <int IHD, int KPMAX>
+__global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
+    constexpr int LPP = IHD / 8;     // lanes per pool
+    constexpr int PPW = 32 / LPP;    // pools per warp
+    constexpr int PPC = PPW * (kThreads / 32);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int sub = lane % LPP;
+    const int c0 = sub * 8;
+    const int b = blockIdx.y;
+    const int p = blockIdx.x * PPC + warp * PPW + lane / LPP;
+    const int KP = a.kpool;
+
+    int L = __ldg(a.pg.seq_lens + b);
+    L = min(L, seq_capacity(a.pg));
+    const int P = L > a.first_key ? (L - a.first_key) / KP : 0;
+    bool active = p < P;
+    const int t0 = a.first_key + p * KP;
+    long long trow = -1, orow = -1;
+    if (active) {
+        trow = token_row(a.pg, b, t0);  // all slots of a pool share one block
+        orow = pool_row(a.pg, b, p, KP);
+        if (trow < 0 || orow < 0) {
+            if (sub == 0) flag_status(a.status, DSA_STATUS_BAD_BLOCK);
+            active = false;
+        }
+    }
+
+    uint4 kr[KPMAX], gr[KPMAX];
+    bool ok = true;
+#pragma unroll
+    for (int s = 0; s < KPMAX; ++s) {
+        kr[s] = make_uint4(0, 0, 0, 0);
+        gr[s] = make_uint4(0, 0, 0, 0);
+        if (s < KP && active) {
+            const long long row = trow + s;
+            kr[s] = ldg16_stream(a.k_raw + row * IHD + c0);
+            gr[s] = ldg16_stream(a.gate + row * IHD + c0);
+            ok = ok && (__ldg(a.valid + row) != 0);
+        }
+    }
+
+    float lw[8], lb[8];
+    {
+        const uint4 w4 = ldg16(a.ln_w + c0);
+        const uint4 b4 = ldg16(a.ln_b + c0);
+        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+        const uint32_t bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lw[2 * i] = bf16_lo(wv[i]);
+            lw[2 * i + 1] = bf16_hi(wv[i]);
+            lb[2 * i] = bf16_lo(bv[i]);
+            lb[2 * i + 1] = bf16_hi(bv[i]);
+        }
+    }
+
+    // Pass 1: per-channel max of the slot logits.
+    float mx[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < KPMAX; ++s) {
+        if (s < KP) {
+            const float4 ap0 = __ldg(reinterpret_cast<const float4*>(a.ape + s * IHD + c0));
+            const float4 ap1 = __ldg(reinterpret_cast<const float4*>(a.ape + s * IHD + c0 + 4));
+            const float ap[8] = {ap0.x, ap0.y, ap0.z, ap0.w, ap1.x, ap1.y, ap1.z, ap1.w};
+            const uint32_t gv[4] = {gr[s].x, gr[s].y, gr[s].z, gr[s].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                mx[2 * i] = fmaxf(mx[2 * i], bf16_lo(gv[i]) + ap[2 * i]);
+                mx[2 * i + 1] = fmaxf(mx[2 * i + 1], bf16_hi(gv[i]) + ap[2 * i + 1]);
+            }
+        }
+    }
+
+    // Pass 2: LayerNorm each slot, round to bf16, accumulate the softmax-weighted sum.
+    float num[8], den[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) num[i] = den[i] = 0.f;
+#pragma unroll
+    for (int s = 0; s < KPMAX; ++s) {
+        if (s < KP) {  // KP is warp-uniform: the shuffles below see the whole warp
+            const uint32_t kv[4] = {kr[s].x, kr[s].y, kr[s].z, kr[s].w};
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[2 * i] = bf16_lo(kv[i]);
+                x[2 * i + 1] = bf16_hi(kv[i]);
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sum += x[i];
+#pragma unroll
+            for (int off = LPP / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            const float mean = sum * (1.0f / IHD);
+            float sq = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                x[i] -= mean;
+                sq += x[i] * x[i];
+            }
+#pragma unroll
+            for (int off = LPP / 2; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+            const float rstd = 1.0f / sqrtf(sq * (1.0f / IHD) + a.eps);
+
+            const float4 ap0 = __ldg(reinterpret_cast<const float4*>(a.ape + s * IHD + c0));
+            const float4 ap1 = __ldg(reinterpret_cast<const float4*>(a.ape + s * IHD + c0 + 4));
+            const float ap[8] = {ap0.x, ap0.y, ap0.z, ap0.w, ap1.x, ap1.y, ap1.z, ap1.w};
+            const uint32_t gv[4] = {gr[s].x, gr[s].y, gr[s].z, gr[s].w};
+            float gl[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                gl[2 * i] = bf16_lo(gv[i]);
+                gl[2 * i + 1] = bf16_hi(gv[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float kn = round_bf16(x[i] * rstd * lw[i] + lb[i]);
+                const float e = expf(gl[i] + ap[i] - mx[i]);
+                den[i] += e;
+                num[i] += e * kn;
+            }
+        }
+    }
+
+    if (!active) return;
+    const bool pv = ok;
+    uint4 o;
+    if (pv) {
+        o.x = pack_bf16x2(num[0] / den[0], num[1] / den[1]);
+        o.y = pack_bf16x2(num[2] / den[2], num[3] / den[3]);
+        o.z = pack_bf16x2(num[4] / den[4], num[5] / den[5]);
+        o.w = pack_bf16x2(num[6] / den[6], num[7] / den[7]);
+    } else {
+        o = make_uint4(0, 0, 0, 0);
+    }
+    *reinterpret_cast<uint4*>(a.kout + orow * IHD + c0) = o;
+    if (sub == 0) {
+        a.pvalid[orow] = pv ? 1 : 0;
+        if (a.pidx) {
+            for (int s = 0; s < KP; ++s) a.pidx[orow * KP + s] = t0 + s;
+        }
+    }
+}
+
+template <int IHD, int KPMAX>
+int launch(const CompressArgs& a, int pmax, cudaStream_t st) {
+    constexpr int PPC = (32 / (IHD / 8)) * (kThreads / 32);
+    dim3 grid((pmax + PPC - 1) / PPC, a.pg.batch);
+    if (grid.x == 0) return DSA_OK;
+    if (grid.x > 0x7fffffffu || grid.y > 65535u)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_compress: grid too large");
+    compress_kernel<IHD, KPMAX><<<grid, kThreads, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_compress launch");
+    return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" int dsa_compress(const dsa_bf16* k_raw, const dsa_bf16* gate,
+                            const uint8_t* token_valid, const float* ape, const dsa_bf16* ln_w,
+                            const dsa_bf16* ln_b, float eps, const dsa_paging* pg,
+                            int first_key, int kpool, int ihd, dsa_bf16* kpool_out,
+                            uint8_t* pool_valid, int32_t* pool_idx, int32_t* status,
+                            void* stream) {
+    if (kpool < 1 || kpool > DSA_MAX_KPOOL)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_compress: kpool %d outside [1, %d]", kpool,
+                    DSA_MAX_KPOOL);
+    if (ihd != 64 && ihd != 128)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_compress: index_head_dim %d not in {64, 128}", ihd);
+    if (first_key < 0) return fail(DSA_ERR_INVALID_ARG, "dsa_compress: first_key %d < 0", first_key);
+    if (!(eps >= 0.f)) return fail(DSA_ERR_INVALID_ARG, "dsa_compress: eps must be >= 0");
+    Paging P;
+    int rc = check_paging(pg, kpool, &P);
+    if (rc) return rc;
+    if (P.block_table && first_key % kpool != 0)
+        return fail(DSA_ERR_UNSUPPORTED,
+                    "dsa_compress: paged layout needs first_key %% kpool == 0 (got %d, %d)",
+                    first_key, kpool);
+    if (!k_raw || !gate || !token_valid || !ape || !ln_w || !ln_b || !kpool_out || !pool_valid)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_compress: NULL tensor");
+    if ((((uintptr_t)k_raw) | ((uintptr_t)gate) | ((uintptr_t)kpool_out) | ((uintptr_t)ape) |
+         ((uintptr_t)ln_w) | ((uintptr_t)ln_b)) & 15)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_compress: tensors must be 16-byte aligned");
+    const int pmax = P.max_seq_len > first_key ? (P.max_seq_len - first_key) / kpool : 0;
+    CompressArgs a;
+    a.k_raw = k_raw;
+    a.gate = gate;
+    a.valid = token_valid;
+    a.ape = ape;
+    a.ln_w = ln_w;
+    a.ln_b = ln_b;
+    a.kout = kpool_out;
+    a.pvalid = pool_valid;
+    a.pidx = pool_idx;
+    a.status = status;
+    a.pg = P;
+    a.eps = eps;
+    a.first_key = first_key;
+    a.kpool = kpool;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (ihd == 128) return kpool <= 4 ? launch<128, 4>(a, pmax, st) : launch<128, 16>(a, pmax, st);
+    return kpool <= 4 ? launch<64, 4>(a, pmax, st) : launch<64, 16>(a, pmax, st);
+}

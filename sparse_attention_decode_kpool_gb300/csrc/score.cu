@@ -1,0 +1,248 @@
+// dsa_score: index scores of query rows against their sequence's pooled keys.
+//
+// Page: metrale_model_arch/glm5next_dsa/tp.rs, "Why the indexer is replicated": the
+// score adds weights[h] * relu(scale * dot) over the indexer heads; scores are
+// [q_rows, n_pools]. build.rs, transform 2: weights already carry index_heads^-0.5.
+//
+// Per pooled key (ihd bf16 = 256 B at ihd 128) the row does index_heads * ihd MACs:
+// 16 MAC per byte at 32 x 128, more than the f32 pipes sustain at HBM speed. So the
+// contraction [16 pools x ihd] x [ihd x 8 heads] runs on the tensor cores as
+// m16n8k16 bf16 MMAs with f32 accumulation, and the head reduction
+// sum_h w[h] * relu(scale * acc) happens in the accumulator registers: each thread
+// holds 2 pools x 2 heads per 8-head tile, so the sum over heads is a local sum plus
+// two xor shuffles inside the lane quad.
+//
+// Keys are streamed straight from HBM into the MMA A-fragments, without shared
+// memory. The dot product does not depend on the order of the ihd axis, so the
+// same permutation of that axis is applied to keys and queries: lane quad q owns
+// physical elements [32v + 8q, 32v + 8q + 8) of each row, loaded as one 16-byte
+// vector per v, which makes every warp load 8 rows x 64 contiguous bytes.
+#include "common.cuh"
+
+namespace dsa {
+namespace {
+
+struct ScoreArgs {
+    const uint16_t* qidx;
+    const float* w;
+    const int32_t* row_seq;
+    const int32_t* row_ctx;
+    const uint16_t* kp;
+    const uint8_t* pv;
+    float* scores;
+    int32_t* status;
+    Paging pg;
+    int rows;
+    int heads;
+    int first_key;
+    int kpool;
+    int p_stride;
+    int tiles_per_warp;
+    float scale;
+};
+
+constexpr int kWarps = 4;
+
+template <int IHD, int NT>
+__global__ void __launch_bounds__(kWarps * 32) score_kernel(ScoreArgs a) {
+    constexpr int NV = IHD / 32;  // 16-byte vectors per row per lane
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int g = lane >> 2;
+    const int q = lane & 3;
+    const int r = blockIdx.y;
+    const int ntiles = (a.p_stride + 15) >> 4;
+    const int t_begin = (blockIdx.x * kWarps + warp) * a.tiles_per_warp;
+    if (t_begin >= ntiles) return;
+    const int t_end = min(ntiles, t_begin + a.tiles_per_warp);
+    float* srow = a.scores + (long long)r * a.p_stride;
+
+    int seq = a.row_seq ? __ldg(a.row_seq + r) : r;
+    int nvis = 0;
+    if (seq >= 0 && seq < a.pg.batch) {
+        int L = min(__ldg(a.pg.seq_lens + seq), seq_capacity(a.pg));
+        int ctx = a.row_ctx ? min(__ldg(a.row_ctx + r), L) : L;
+        nvis = ctx > a.first_key ? (ctx - a.first_key) / a.kpool : 0;
+    } else if (lane == 0 && blockIdx.x == 0 && warp == 0) {
+        flag_status(a.status, DSA_STATUS_BAD_TOKEN);
+    }
+
+    // Query fragments (B operand): head 8*nt + g, this quad's permuted elements.
+    uint32_t bq[NT][NV][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int h = nt * 8 + g;
+        const uint16_t* qp = a.qidx + ((long long)r * a.heads + h) * IHD + 8 * q;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            uint4 x = make_uint4(0, 0, 0, 0);
+            if (h < a.heads) x = ldg16(qp + 32 * v);
+            bq[nt][v][0] = x.x;
+            bq[nt][v][1] = x.y;
+            bq[nt][v][2] = x.z;
+            bq[nt][v][3] = x.w;
+        }
+    }
+    float wv[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int h = nt * 8 + 2 * q + j;
+            wv[nt][j] = h < a.heads ? __ldg(a.w + (long long)r * a.heads + h) : 0.f;
+        }
+
+    for (int t = t_begin; t < t_end; t += 2) {
+        const bool two = (t + 1) < t_end;
+        if ((t << 4) >= nvis) {  // nothing visible from here on in this warp's range
+            const int p0 = t << 4;
+            const int p1 = min(a.p_stride, (t_end << 4));
+            for (int p = p0 + lane; p < p1; p += 32) srow[p] = -INFINITY;
+            break;
+        }
+        // This thread's 4 pools: tile t rows g, g+8; tile t+1 rows g, g+8.
+        int pool[4];
+        pool[0] = (t << 4) + g;
+        pool[1] = pool[0] + 8;
+        pool[2] = pool[0] + 16;
+        pool[3] = pool[0] + 24;
+        long long prow[4];
+        bool cand[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            prow[i] = -1;
+            if (pool[i] < nvis && (i < 2 || two)) {
+                prow[i] = pool_row(a.pg, seq, pool[i], a.kpool);
+                if (prow[i] < 0) flag_status(a.status, DSA_STATUS_BAD_BLOCK);
+            }
+        }
+        uint4 kr[4][NV];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                kr[i][v] = make_uint4(0, 0, 0, 0);
+                if (prow[i] >= 0) kr[i][v] = ldg16_stream(a.kp + prow[i] * IHD + 8 * q + 32 * v);
+            }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cand[i] = prow[i] >= 0 && __ldg(a.pv + prow[i]) != 0;
+
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+            if (tt == 1 && !two) break;
+            float acc[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const uint32_t ra[4] = {kr[2 * tt][v].x, kr[2 * tt][v].y, kr[2 * tt][v].z,
+                                        kr[2 * tt][v].w};
+                const uint32_t rb[4] = {kr[2 * tt + 1][v].x, kr[2 * tt + 1][v].y,
+                                        kr[2 * tt + 1][v].z, kr[2 * tt + 1][v].w};
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_16816(acc[nt], ra[2 * h2], rb[2 * h2], ra[2 * h2 + 1], rb[2 * h2 + 1],
+                                  bq[nt][v][2 * h2], bq[nt][v][2 * h2 + 1]);
+            }
+            float s0 = 0.f, s1 = 0.f;  // rows g and g+8 of this tile
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                s0 += wv[nt][0] * fmaxf(a.scale * acc[nt][0], 0.f) +
+                      wv[nt][1] * fmaxf(a.scale * acc[nt][1], 0.f);
+                s1 += wv[nt][0] * fmaxf(a.scale * acc[nt][2], 0.f) +
+                      wv[nt][1] * fmaxf(a.scale * acc[nt][3], 0.f);
+            }
+            s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+            s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+            if (q < 2) {
+                const int p = (t << 4) + g + 8 * (2 * tt + q);
+                const bool c = q == 0 ? cand[2 * tt] : cand[2 * tt + 1];
+                if (p < a.p_stride) srow[p] = c ? (q == 0 ? s0 : s1) : -INFINITY;
+            }
+        }
+    }
+}
+
+template <int IHD, int NT>
+int launch(const ScoreArgs& a0, cudaStream_t st) {
+    ScoreArgs a = a0;
+    const int ntiles = (a.p_stride + 15) / 16;
+    // Enough warps to cover the GPU a few times over; at least 2 tiles per warp.
+    const long long want_warps = (long long)sm_count() * 48;
+    long long per = ((long long)ntiles * a.rows + want_warps - 1) / want_warps;
+    if (per < 2) per = 2;
+    if (per > 64) per = 64;
+    a.tiles_per_warp = (int)((per + 1) & ~1LL);
+    const long long warps_per_row = (ntiles + a.tiles_per_warp - 1) / a.tiles_per_warp;
+    dim3 grid((unsigned)((warps_per_row + kWarps - 1) / kWarps), a.rows);
+    if (grid.y > 65535u) return fail(DSA_ERR_UNSUPPORTED, "dsa_score: rows %d > 65535", a.rows);
+    score_kernel<IHD, NT><<<grid, kWarps * 32, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_score launch");
+    return DSA_OK;
+}
+
+template <int IHD>
+int dispatch_heads(const ScoreArgs& a, cudaStream_t st) {
+    const int nt = (a.heads + 7) / 8;
+    switch (nt) {
+        case 1: return launch<IHD, 1>(a, st);
+        case 2: return launch<IHD, 2>(a, st);
+        case 3:
+        case 4: return launch<IHD, 4>(a, st);
+        default: return launch<IHD, 8>(a, st);
+    }
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" int dsa_score(const dsa_bf16* qidx, const float* w, int rows, int index_heads,
+                         int ihd, const int32_t* row_seq, const int32_t* row_ctx,
+                         const dsa_bf16* kpool, const uint8_t* pool_valid, const dsa_paging* pg,
+                         int first_key, int kpool_size, float scale, float* scores,
+                         int p_stride, int32_t* status, void* stream) {
+    if (rows < 0 || p_stride < 0 || first_key < 0)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_score: rows %d, p_stride %d, first_key %d", rows,
+                    p_stride, first_key);
+    if (kpool_size < 1 || kpool_size > DSA_MAX_KPOOL)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_score: kpool %d outside [1, %d]", kpool_size,
+                    DSA_MAX_KPOOL);
+    if (ihd != 64 && ihd != 128)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_score: index_head_dim %d not in {64, 128}", ihd);
+    if (index_heads < 1 || index_heads > 64)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_score: index_heads %d outside [1, 64]", index_heads);
+    Paging P;
+    int rc = check_paging(pg, kpool_size, &P);
+    if (rc) return rc;
+    if (rows == 0 || p_stride == 0) return DSA_OK;
+    if (!qidx || !w || !kpool || !pool_valid || !scores)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_score: NULL tensor");
+    if ((((uintptr_t)qidx) | ((uintptr_t)kpool)) & 15)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_score: qidx and kpool must be 16-byte aligned");
+    ScoreArgs a;
+    a.qidx = qidx;
+    a.w = w;
+    a.row_seq = row_seq;
+    a.row_ctx = row_ctx;
+    a.kp = kpool;
+    a.pv = pool_valid;
+    a.scores = scores;
+    a.status = status;
+    a.pg = P;
+    a.rows = rows;
+    a.heads = index_heads;
+    a.first_key = first_key;
+    a.kpool = kpool_size;
+    a.p_stride = p_stride;
+    a.tiles_per_warp = 2;
+    a.scale = scale;
+    cudaStream_t st = (cudaStream_t)stream;
+    return ihd == 128 ? dispatch_heads<128>(a, st) : dispatch_heads<64>(a, st);
+}

@@ -1,0 +1,138 @@
+"""One DSA decode layer on one GPU: device-resident caches plus the per-step chain
+score -> select -> expand -> sparse latent MLA, all through the C ABI.
+
+``DsaDecodeLayer`` uploads a workload's caches once (the latent KV cache, the raw
+indexer keys, o_absorb), builds the pooled-key cache with ``dsa_compress``, and
+owns every step buffer, so a step allocates nothing and can be captured in a
+CUDA graph.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import api
+from .workloads import Workload
+
+
+class DsaDecodeLayer:
+    def __init__(self, wl: Workload, device: str = "cuda", keep_olat: bool = False,
+                 with_o_absorb: bool = True, use_drawn_kpool: bool = False):
+        g = wl.geom
+        self.wl = wl
+        self.geom = g
+        dev = torch.device(device)
+        self.device = dev
+        up = lambda t: None if t is None else t.to(dev, non_blocking=False).contiguous()
+
+        self.seq_lens = torch.from_numpy(wl.seq_lens).to(dev)
+        self.block_table = up(wl.block_table)
+        self.pg = api.paging(self.seq_lens, wl.max_seq_len, self.block_table,
+                             wl.block_size or 0, wl.num_blocks)
+        self.row_seq = torch.from_numpy(wl.row_seq).to(dev)
+        self.row_ctx = torch.from_numpy(wl.row_ctx).to(dev)
+
+        # Resident state.
+        self.ckv = up(wl.ckv)
+        self.o_absorb = up(wl.o_absorb) if with_o_absorb else None
+        KP, ihd = g.index_kpool, g.index_head_dim
+        if wl.paged:
+            pshape = (wl.num_blocks, wl.block_size // KP)
+        else:
+            pshape = (wl.batch, wl.max_seq_len // KP)
+        if use_drawn_kpool:
+            self.kpool = up(wl.kpool_keys)
+            self.pool_valid = up(wl.kpool_valid)
+            self.k_raw = self.gate = self.valid = None
+        else:
+            self.kpool = torch.zeros(pshape + (ihd,), dtype=torch.bfloat16, device=dev)
+            self.pool_valid = torch.zeros(pshape, dtype=torch.uint8, device=dev)
+            self.k_raw, self.gate, self.valid = up(wl.k_raw), up(wl.gate), up(wl.valid)
+        self.ape, self.ln_w, self.ln_b = up(wl.ape), up(wl.ln_w), up(wl.ln_b)
+
+        # Per-step inputs (device copies) and buffers.
+        self.qidx = up(wl.qidx)
+        self.w = up(wl.w)
+        self.qlat = up(wl.qlat)
+        R = wl.rows
+        self.p_stride = wl.p_stride
+        self.sk = api.dsa_select_k(g.index_topk, KP, self.p_stride)
+        self.scores = torch.empty((R, self.p_stride), dtype=torch.float32, device=dev)
+        self.pool_ids = torch.empty((R, self.sk), dtype=torch.int32, device=dev)
+        self.token_ids = torch.empty((R, g.out_width), dtype=torch.int32, device=dev)
+        hidden = g.hidden if self.o_absorb is not None else 0
+        self.y = torch.empty((R, hidden), dtype=torch.bfloat16, device=dev) if hidden else None
+        self.olat = (torch.empty((R, g.heads, g.kv_lora_rank), dtype=torch.float32, device=dev)
+                     if (keep_olat or self.o_absorb is None) else None)
+        ws = api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, hidden,
+                                                 self.o_absorb is not None)
+        self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.graph: Optional[torch.cuda.CUDAGraph] = None
+
+    # -- stages ------------------------------------------------------------
+    def compress(self, stream=None) -> None:
+        g = self.geom
+        api.dsa_compress(self.k_raw, self.gate, self.valid, self.ape, self.ln_w, self.ln_b, g.eps,
+                         self.pg, g.first_key, g.index_kpool, self.kpool, self.pool_valid,
+                         status=self.status, stream=stream)
+
+    def score(self, stream=None) -> None:
+        g = self.geom
+        api.dsa_score(self.qidx, self.w, self.row_seq, self.row_ctx, self.kpool, self.pool_valid,
+                      self.pg, g.first_key, g.index_kpool, g.index_scale, self.scores,
+                      status=self.status, stream=stream)
+
+    def select(self, stream=None) -> None:
+        api.dsa_select(self.scores, self.geom.index_topk, self.geom.index_kpool, self.pool_ids,
+                       stream=stream)
+
+    def expand(self, stream=None) -> None:
+        api.dsa_expand(self.pool_ids, self.geom.first_key, self.geom.index_kpool, self.token_ids,
+                       stream=stream)
+
+    def attend(self, stream=None) -> None:
+        api.dsa_sparse_mla_decode(self.qlat, self.row_seq, self.ckv, self.pg, self.token_ids,
+                                  self.geom.softmax_scale, self.o_absorb, self.y, self.olat,
+                                  self.status, self.workspace, stream=stream)
+
+    def step(self, stream=None) -> None:
+        """One decode step over the whole batch: score, select, expand, attend."""
+        self.score(stream)
+        self.select(stream)
+        self.expand(stream)
+        self.attend(stream)
+
+    # Kernel launches one step() makes (score, select, expand, split attention,
+    # [combine], [gemv, ysum]).
+    def launches_per_step(self) -> int:
+        from . import api as _a  # noqa: F401
+        n = 4
+        R, g = self.wl.rows, self.geom
+        hidden = g.hidden if self.o_absorb is not None else 0
+        ws_split = api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, 0, False)
+        if ws_split > 0:
+            n += 1  # combine
+        if self.o_absorb is not None:
+            n += 1 + (R + 63) // 64  # gemv launches + ysum
+        return n
+
+    # -- graphs ------------------------------------------------------------
+    def capture(self) -> torch.cuda.CUDAGraph:
+        """Capture step() into a CUDA graph (run step() once eagerly first)."""
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            self.step()
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        torch.cuda.synchronize(self.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step()
+        self.graph = g
+        return g
+
+    def replay(self) -> None:
+        assert self.graph is not None
+        self.graph.replay()

@@ -26,8 +26,11 @@ nearest even, ``ape`` kept in f32, index weights pre-multiplied by
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
 import math
+import os
+import threading
 from typing import Optional, Sequence
 
 import numpy as np
@@ -39,8 +42,63 @@ _T_QIDX, _T_W, _T_QLAT, _T_CKV, _T_OABS, _T_LENS, _T_PERM = 7, 8, 9, 10, 11, 12,
 _T_KPOOL = 14
 
 
-def _rng(seed: int, tensor: int, seq: int = 0) -> np.random.Generator:
-    return np.random.Generator(np.random.PCG64([seed, tensor, seq]))
+def _rng(seed: int, tensor: int, seq: int = 0, chunk: Optional[int] = None) -> np.random.Generator:
+    key = [seed, tensor, seq] if chunk is None else [seed, tensor, seq, chunk]
+    return np.random.Generator(np.random.PCG64(key))
+
+
+_CHUNK = 1 << 22  # elements per independently seeded stream of a large tensor
+_POOL = cf.ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1)))
+_TLS = threading.local()
+
+
+def _tls_buffers():
+    if getattr(_TLS, "f32", None) is None:
+        _TLS.f32 = np.empty(_CHUNK, dtype=np.float32)
+        _TLS.bf16 = torch.empty(_CHUNK, dtype=torch.bfloat16)
+    return _TLS.f32, _TLS.bf16
+
+
+def _fill_normal(dst: torch.Tensor, seed: int, tensor: int, seq: int, width: int,
+                 mean: float, std: float, row_index: Optional[np.ndarray] = None,
+                 nrows: Optional[int] = None) -> None:
+    """Fill ``nrows`` rows of ``width`` bf16 values ~ N(mean, std^2) into the 2-D bf16
+    tensor ``dst``: rows 0.. in order, or rows ``row_index[i]`` when given. Values are
+    drawn in fixed chunks of _CHUNK elements, chunk i from stream (seed, tensor, seq,
+    i); numpy releases the GIL, so chunks run in parallel threads and the result does
+    not depend on the thread count."""
+    assert _CHUNK % width == 0
+    if nrows is None:
+        nrows = dst.shape[0] if row_index is None else len(row_index)
+    n = nrows * width
+
+    def one(i: int) -> None:
+        lo, hi = i * _CHUNK, min(n, (i + 1) * _CHUNK)
+        f32, b16 = _tls_buffers()
+        x = f32[: hi - lo]
+        _rng(seed, tensor, seq, i).standard_normal(out=x, dtype=np.float32)
+        if std != 1.0:
+            x *= np.float32(std)
+        if mean != 0.0:
+            x += np.float32(mean)
+        r0, r1 = lo // width, hi // width
+        src = torch.from_numpy(x).view(r1 - r0, width)
+        if row_index is None:
+            dst[r0:r1].copy_(src)  # float32 -> bf16, nearest even
+        else:
+            tmp = b16[: hi - lo].view(r1 - r0, width)
+            tmp.copy_(src)
+            dst.index_copy_(0, torch.from_numpy(row_index[r0:r1]), tmp)
+
+    list(_POOL.map(one, range((n + _CHUNK - 1) // _CHUNK)))
+
+
+def _normal_bf16(seed: int, tensor: int, seq: int, n: int, mean: float, std: float) -> torch.Tensor:
+    """n bf16 values ~ N(mean, std^2) (see ``_fill_normal``)."""
+    out = torch.empty(n, dtype=torch.bfloat16)
+    width = 64 if n % 64 == 0 else 1
+    _fill_normal(out.view(-1, width), seed, tensor, seq, width, mean, std)
+    return out
 
 
 def _normal_f32(rng: np.random.Generator, shape, mean: float, std: float) -> np.ndarray:
@@ -225,8 +283,11 @@ def make_workload(
         out = torch.zeros((n_tok_rows, width), dtype=torch.bfloat16)
         for b in sorted(want):
             L = int(seq_lens[b])
-            x = _normal_f32(_rng(seed, tensor_id, b), (L, width), mean, std)
-            out[torch.from_numpy(token_rows(b))] = _to_bf16(x)
+            if block_size is None:
+                _fill_normal(out[b * smax: b * smax + L], seed, tensor_id, b, width, mean, std)
+            else:
+                _fill_normal(out, seed, tensor_id, b, width, mean, std,
+                             row_index=token_rows(b).astype(np.int64))
         return out.view(tok_shape(width))
 
     k_raw = gate = valid = None
@@ -240,7 +301,8 @@ def make_workload(
             if invalid_tail:
                 vb[max(0, L - invalid_tail) :] = 0
             if invalid_per_seq:
-                bad = _rng(seed, _T_VALID, b).choice(L, size=invalid_per_seq, replace=False)
+                bad = _rng(seed, _T_VALID, b).choice(L, size=min(L, invalid_per_seq),
+                                                     replace=False)
                 vb[bad] = 0
             v[token_rows(b)] = vb
         valid = torch.from_numpy(v).view(tok_shape())
@@ -249,15 +311,17 @@ def make_workload(
     ln_b = _to_bf16(_normal_f32(_rng(seed, _T_LNB), (ihd,), 0.0, 0.1))
     ape = torch.from_numpy(_normal_f32(_rng(seed, _T_APE), (KP, ihd), 0.0, 0.1))
 
-    qidx = _to_bf16(_normal_f32(_rng(seed, _T_QIDX), (rows, g.index_heads, ihd), 0.0, 1.0))
+    qidx = _normal_bf16(seed, _T_QIDX, 0, rows * g.index_heads * ihd, 0.0, 1.0).view(
+        rows, g.index_heads, ihd)
     w_np = _rng(seed, _T_W).random(size=(rows, g.index_heads), dtype=np.float32)
     w_np *= np.float32(g.index_heads ** -0.5)
     w = torch.from_numpy(w_np)
-    qlat = _to_bf16(_normal_f32(_rng(seed, _T_QLAT), (rows, g.heads, kvl), 0.0, 1.0))
+    qlat = _normal_bf16(seed, _T_QLAT, 0, rows * g.heads * kvl, 0.0, 1.0).view(rows, g.heads, kvl)
     ckv = fill_tokens(_T_CKV, kvl, 0.0, ckv_std)
     o_absorb = None
     if with_o_absorb:
-        o_absorb = _to_bf16(_normal_f32(_rng(seed, _T_OABS), (g.hidden, g.heads * kvl), 0.0, 0.02))
+        o_absorb = _normal_bf16(seed, _T_OABS, 0, g.hidden * g.heads * kvl, 0.0, 0.02).view(
+            g.hidden, g.heads * kvl)
 
     kpool_keys = kpool_valid = None
     if direct_kpool:
@@ -271,7 +335,7 @@ def make_workload(
         for b in sorted(want):
             P = max(0, (int(seq_lens[b]) - g.first_key) // KP)
             r = _rng(seed, _T_KPOOL, b)
-            x = _to_bf16(_normal_f32(r, (P, ihd), 0.0, 0.5))
+            x = _normal_bf16(seed, _T_KPOOL, b, P * ihd, 0.0, 0.5).view(P, ihd)
             vv = (r.random(P) >= 0.002).astype(np.uint8)
             p = np.arange(P)
             if block_size is None:

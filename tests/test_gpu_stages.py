@@ -1,0 +1,302 @@
+"""Stage-by-stage parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Each stage is fed the oracle's (or the generator's) previous-stage output, so one
+stage's rounding never reaches the next stage's check."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import dsa_oracle as O
+from sparse_attention_decode_kpool_gb300 import api, workloads as W
+from sparse_attention_decode_kpool_gb300.pipeline import DsaDecodeLayer
+from tests import _harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    torch.cuda.init()
+
+
+def _geom(**kw):
+    base = dict(index_kpool=4, index_heads=32, index_head_dim=128, index_topk=256, heads=8,
+                hidden=256)
+    base.update(kw)
+    return W.Geometry(**base)
+
+
+# ---------------------------------------------------------------------------
+# dsa_compress
+
+
+COMPRESS_CASES = [
+    # (name, geometry kwargs, seq_lens, block_size, first_key, invalid_per_seq)
+    ("tiny", None, None, None, 0, 0),
+    ("ihd128-kp4-ragged", dict(), [1000, 37, 513], None, 0, 9),
+    ("ihd128-kp1", dict(index_kpool=1, index_topk=64), [301, 64], None, 0, 3),
+    ("ihd64-kp2-fk5", dict(index_head_dim=64, index_kpool=2, index_topk=64), [333, 90], None, 5, 4),
+    ("ihd128-kp3", dict(index_kpool=3, index_topk=48), [400, 11], None, 1, 5),
+    ("ihd128-kp8", dict(index_kpool=8, index_topk=64), [777, 64], None, 0, 6),
+    ("ihd64-kp16", dict(index_head_dim=64, index_kpool=16, index_topk=64), [999, 15], None, 0, 6),
+    ("paged-kp4", dict(), [1000, 300, 64, 5], 64, 0, 7),
+    ("paged-kp4-fk8", dict(), [900, 130], 64, 8, 2),
+]
+
+
+@pytest.mark.parametrize("case", COMPRESS_CASES, ids=[c[0] for c in COMPRESS_CASES])
+def test_compress_parity(case):
+    name, gkw, lens, bs, fk, inval = case
+    if gkw is None:
+        wl = W.tiny()
+    else:
+        g = _geom(first_key=fk, **gkw)
+        wl = W.make_workload(name, 100, g, lens, block_size=bs, invalid_per_seq=inval,
+                             with_o_absorb=False)
+    layer = DsaDecodeLayer(wl, with_o_absorb=False)
+    g = wl.geom
+    KP, ihd = g.index_kpool, g.index_head_dim
+    layer.kpool.fill_(7.0)  # sentinel: rows not written must keep it
+    layer.pool_valid.fill_(9)
+    pidx = torch.full(layer.pool_valid.shape + (KP,), -7, dtype=torch.int32, device="cuda")
+    api.dsa_compress(layer.k_raw, layer.gate, layer.valid, layer.ape, layer.ln_w, layer.ln_b,
+                     g.eps, layer.pg, g.first_key, KP, layer.kpool, layer.pool_valid, pidx,
+                     layer.status)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    oq = H.OracleSeq(wl)
+    kp = layer.kpool.float().cpu().numpy()
+    pv = layer.pool_valid.cpu().numpy()
+    pi = pidx.cpu().numpy()
+    bt = None if wl.block_table is None else wl.block_table.numpy()
+    ppb = (wl.block_size or 0) // KP
+    touched = np.zeros(pv.shape, dtype=bool)
+    for b in range(wl.batch):
+        keys, rpv, ridx = oq.pools(b)
+        P = keys.shape[0]
+        gk = O.sequence_pools(kp, b, P, bt, ppb)
+        gv = O.sequence_pools(pv, b, P, bt, ppb)
+        gi = O.sequence_pools(pi, b, P, bt, ppb)
+        np.testing.assert_array_equal(gv, rpv)
+        np.testing.assert_array_equal(gi, ridx)
+        H.check_kpool(gk, keys, oq.kn_ulp(b), f"{name} seq {b}")
+        if bt is None:
+            touched[b, :P] = True
+        else:
+            p = np.arange(P)
+            touched[bt[b, p // ppb], p % ppb] = True
+    assert (pv[~touched] == 9).all() and (kp[~touched] == 7.0).all(), "rows past P written"
+
+
+# ---------------------------------------------------------------------------
+# dsa_score (fed the drawn pooled-key cache)
+
+
+SCORE_CASES = [
+    ("h32-d128", dict(), [3000, 517, 64], None, None, 0),
+    ("h4-d64", dict(index_heads=4, index_head_dim=64), [2048], None, None, 0),
+    ("h20-d128", dict(index_heads=20), [1234, 99], None, None, 0),
+    ("h32-paged", dict(), [4000, 1000, 65], 64, None, 0),
+    ("h32-prefill-ctx", dict(), [2000], None, [1, 3, 4, 5, 1999, 2000, 1500, 17], 0),
+    ("h32-fk3", dict(first_key=3), [701, 40], None, None, 0),
+    ("h8-kp8", dict(index_heads=8, index_kpool=8, index_topk=64), [1601, 3], None, None, 0),
+]
+
+
+@pytest.mark.parametrize("case", SCORE_CASES, ids=[c[0] for c in SCORE_CASES])
+def test_score_parity(case):
+    name, gkw, lens, bs, rows_ctx, _ = case
+    g = _geom(**gkw)
+    wl = W.make_workload(name, 200, g, lens, block_size=bs, rows_ctx=rows_ctx,
+                         with_raw=False, with_o_absorb=False, direct_kpool=True)
+    layer = DsaDecodeLayer(wl, with_o_absorb=False, use_drawn_kpool=True)
+    sc = H.Guarded(layer.scores.shape, torch.float32, 12345.0)
+    api.dsa_score(layer.qidx, layer.w, layer.row_seq, layer.row_ctx, layer.kpool,
+                  layer.pool_valid, layer.pg, g.first_key, g.index_kpool, g.index_scale, sc.t,
+                  status=layer.status)
+    torch.cuda.synchronize()
+    sc.check()
+    assert int(layer.status.item()) == 0
+    got = sc.t.cpu().numpy().astype(np.float64)
+    oq = H.OracleSeq(wl, use_drawn_kpool=True)
+    for r in range(wl.rows):
+        H.check_scores(got[r], oq.scores(r, wl.p_stride), f"{name} row {r}")
+
+
+# ---------------------------------------------------------------------------
+# dsa_select (fed oracle-side f32 score rows) and dsa_expand
+
+
+def _tie_rows(rng, rows, P, kind):
+    if kind == "ties":
+        vals = np.array([-np.inf, -1.0, -0.0, 0.0, 0.5, 1.0, 2.0], dtype=np.float32)
+        return vals[rng.integers(0, len(vals), (rows, P))]
+    if kind == "normal":
+        x = rng.standard_normal((rows, P)).astype(np.float32)
+        x[rng.random((rows, P)) < 0.05] = -np.inf
+        return x
+    if kind == "sparse":
+        x = np.full((rows, P), -np.inf, dtype=np.float32)
+        m = rng.random((rows, P)) < 0.01
+        x[m] = rng.random(m.sum()).astype(np.float32)
+        return x
+    if kind == "allinf":
+        return np.full((rows, P), -np.inf, dtype=np.float32)
+    if kind == "positive":
+        return (rng.random((rows, P)) * 3).astype(np.float32)
+    raise ValueError(kind)
+
+
+SELECT_CASES = [
+    (1, 1, 4, 4, "normal"), (3, 5, 8, 4, "ties"), (2, 512, 256, 4, "ties"), (4, 511, 256, 4, "normal"),
+    (1, 8192, 2048, 4, "positive"), (8, 65536, 2048, 4, "positive"), (2, 65536, 2048, 4, "ties"),
+    (3, 100003, 2048, 4, "normal"), (2, 3000, 2048, 4, "sparse"), (2, 700, 256, 4, "allinf"),
+    (5, 16384, 2048, 4, "positive"), (64, 16384, 2048, 4, "normal"), (300, 2048, 512, 4, "ties"),
+    (1, 393216, 2048, 4, "positive"), (2, 40000, 64, 1, "ties"),
+]
+
+
+@pytest.mark.parametrize("case", SELECT_CASES, ids=[f"{c[0]}x{c[1]}-k{c[2]}/{c[3]}-{c[4]}" for c in SELECT_CASES])
+def test_select_parity(case):
+    rows, P, topk, kp, kind = case
+    rng = np.random.default_rng(rows * 7919 + P)
+    s = _tie_rows(rng, rows, P, kind)
+    sk = O.select_k(topk, kp, P)
+    scores = torch.from_numpy(s).cuda()
+    out = H.Guarded((rows, sk), torch.int32, -77)
+    api.dsa_select(scores, topk, kp, out.t)
+    torch.cuda.synchronize()
+    out.check()
+    got = out.t.cpu().numpy()
+    for r in range(rows):
+        np.testing.assert_array_equal(got[r], O.topk_pools(s[r].astype(np.float64), sk),
+                                      err_msg=f"row {r}")
+
+
+def test_expand_parity():
+    rng = np.random.default_rng(3)
+    for kp, fk, sk, width, rows in [(4, 0, 64, 256, 5), (4, 3, 512, 2048, 3), (1, 0, 7, 9, 2),
+                                    (16, 16, 4, 70, 4), (3, 1, 10, 31, 6)]:
+        ids = np.full((rows, sk), -1, dtype=np.int32)
+        for r in range(rows):
+            k = int(rng.integers(0, sk + 1))
+            ids[r, :k] = np.sort(rng.choice(10 * sk + 10, k, replace=False))
+        out = H.Guarded((rows, width), torch.int32, -99)
+        api.dsa_expand(torch.from_numpy(ids).cuda(), fk, kp, out.t)
+        torch.cuda.synchronize()
+        out.check()
+        got = out.t.cpu().numpy()
+        for r in range(rows):
+            np.testing.assert_array_equal(got[r], O.expand_selection(ids[r], fk, kp, width))
+
+
+# ---------------------------------------------------------------------------
+# dsa_sparse_mla_decode (fed oracle-side token ids)
+
+
+MLA_CASES = [
+    # name, heads, hidden, lens, block_size, out_width, o_absorb
+    ("h4-tiny", 4, 1024, [2048], None, 256, True),
+    ("h64-b1", 64, 512, [5000], None, 2048, True),
+    ("h64-b3-paged", 64, 256, [3000, 700, 4097], 64, 512, True),
+    ("h20-ragged", 20, 128, [999, 400], None, 300, True),
+    ("h16-olat-only", 16, 0, [1500, 1500], None, 700, False),
+    ("h96-two-groups", 96, 64, [800], None, 200, True),
+    ("h64-b70-rows", 64, 64, [300] * 70, None, 64, True),
+]
+
+
+def _token_rows(rng, wl, ow, empty_row=True):
+    ids = np.full((wl.rows, ow), -1, dtype=np.int32)
+    for r in range(wl.rows):
+        L = int(wl.seq_lens[int(wl.row_seq[r])])
+        if empty_row and r == 1:
+            continue
+        k = int(rng.integers(1, min(ow, L) + 1))
+        pos = np.sort(rng.choice(ow, k, replace=False))
+        ids[r, pos] = rng.choice(L, k, replace=False)
+    return ids
+
+
+@pytest.mark.parametrize("case", MLA_CASES, ids=[c[0] for c in MLA_CASES])
+def test_mla_parity(case):
+    name, heads, hidden, lens, bs, ow, with_o = case
+    g = _geom(heads=heads, hidden=max(hidden, 32), index_topk=ow)
+    wl = W.make_workload(name, 300, g, lens, block_size=bs, with_raw=False,
+                         with_o_absorb=with_o)
+    layer = DsaDecodeLayer(wl, with_o_absorb=with_o, keep_olat=True, use_drawn_kpool=False)
+    rng = np.random.default_rng(heads + ow)
+    ids = _token_rows(rng, wl, ow)
+    tok = torch.from_numpy(ids).cuda()
+    olat = H.Guarded((wl.rows, heads, 512), torch.float32, 555.0)
+    y = H.Guarded((wl.rows, g.hidden), torch.bfloat16, 3.0) if with_o else None
+    api.dsa_sparse_mla_decode(layer.qlat, layer.row_seq, layer.ckv, layer.pg, tok,
+                              g.softmax_scale, layer.o_absorb, None if y is None else y.t,
+                              olat.t, layer.status, layer.workspace)
+    torch.cuda.synchronize()
+    olat.check()
+    if y is not None:
+        y.check()
+    assert int(layer.status.item()) == 0
+    oq = H.OracleSeq(wl)
+    A = H.f(wl.o_absorb) if with_o else None
+    ro, ry = [], []
+    for r in range(wl.rows):
+        o_, y_, _ = O.sparse_mla_decode_row(H.f(wl.qlat[r]), oq.ckv(int(wl.row_seq[r])), ids[r],
+                                            g.softmax_scale, A)
+        ro.append(o_.reshape(-1))
+        if with_o:
+            ry.append(y_)
+    H.check_attention(olat.t.cpu().numpy().reshape(wl.rows, -1), np.array(ro), f"{name} olat")
+    if with_o:
+        H.check_attention(y.t.float().cpu().numpy(), np.array(ry), f"{name} y")
+
+
+def test_mla_bad_ids_set_status_and_are_skipped():
+    g = _geom(heads=8, hidden=64, index_topk=128)
+    wl = W.make_workload("bad", 301, g, [500, 200], block_size=64, with_raw=False)
+    layer = DsaDecodeLayer(wl, keep_olat=True)
+    rng = np.random.default_rng(5)
+    ids = _token_rows(rng, wl, 128, empty_row=False)
+    bad = ids.copy()
+    bad[0, 3] = 500        # == seq_len: out of range
+    bad[1, 5] = -5         # < -1
+    bad[1, 6] = 10 ** 6    # far out of range
+    clean = bad.copy()
+    clean[0, 3] = clean[1, 5] = clean[1, 6] = -1
+    layer.status.zero_()
+    api.dsa_sparse_mla_decode(layer.qlat, layer.row_seq, layer.ckv, layer.pg,
+                              torch.from_numpy(bad).cuda(), g.softmax_scale, layer.o_absorb,
+                              layer.y, layer.olat, layer.status, layer.workspace)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) & api._lib.DSA_STATUS_BAD_TOKEN
+    got = layer.olat.cpu().numpy().reshape(wl.rows, -1)
+    assert np.isfinite(got).all()
+    oq = H.OracleSeq(wl)
+    ref = [O.sparse_mla_decode_row(H.f(wl.qlat[r]), oq.ckv(r), clean[r], g.softmax_scale)[0]
+           .reshape(-1) for r in range(wl.rows)]
+    H.check_attention(got, np.array(ref), "olat with bad ids")
+
+
+def test_bad_block_table_entry_sets_status():
+    g = _geom(heads=8, hidden=64, index_topk=128)
+    wl = W.make_workload("badblk", 302, g, [300, 300], block_size=64, with_raw=False,
+                         direct_kpool=True)
+    layer = DsaDecodeLayer(wl, keep_olat=True, use_drawn_kpool=True)
+    bt = layer.block_table.clone()
+    bt[1, 2] = wl.num_blocks + 5  # corrupt one entry of sequence 1
+    pg = api.paging(layer.seq_lens, wl.max_seq_len, bt, 64, wl.num_blocks)
+    layer.status.zero_()
+    api.dsa_score(layer.qidx, layer.w, layer.row_seq, layer.row_ctx, layer.kpool,
+                  layer.pool_valid, pg, 0, 4, g.index_scale, layer.scores, status=layer.status)
+    ids = torch.full((2, 128), -1, dtype=torch.int32)
+    ids[1, :10] = torch.arange(128, 138)  # tokens in block 2 of sequence 1
+    api.dsa_sparse_mla_decode(layer.qlat, layer.row_seq, layer.ckv, pg, ids.cuda(),
+                              g.softmax_scale, layer.o_absorb, layer.y, layer.olat, layer.status,
+                              layer.workspace)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) & api._lib.DSA_STATUS_BAD_BLOCK
+    s = layer.scores.cpu().numpy()
+    assert np.isneginf(s[1, 32:48]).all()  # pools of the bad block are not candidates
+    assert (layer.olat[1].abs().sum().item() == 0.0)  # all of row 1's tokens skipped
