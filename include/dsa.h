@@ -212,6 +212,37 @@ int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, int kv_lora
                           int32_t* status, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/*
+ * dsa_sparse_mla_decode_noalloc -- dsa_sparse_mla_decode for callers that cannot
+ * allocate device memory. The pages have no counterpart: this is an interface
+ * convenience of this library, not a step of the method.
+ *
+ * Who needs it: code hosted inside a framework that owns every device
+ * allocation and gives plug-ins no allocator, or a latency-critical loop that
+ * must never call cudaMalloc/cudaFree (both can synchronise the whole device).
+ * Such a caller still passes its inputs and outputs, but no workspace.
+ *
+ * Arguments, results and errors are those of dsa_sparse_mla_decode, without the
+ * workspace pair. The scratch is a fixed array of DSA_NOALLOC_SCRATCH_BYTES
+ * compiled into the library; every GPU that loads the library holds one copy
+ * until the process exits. A problem whose workspace (as reported by
+ * dsa_sparse_mla_decode_workspace) exceeds it is refused with
+ * DSA_ERR_UNSUPPORTED before anything is enqueued. No allocation of any kind
+ * happens in the call.
+ *
+ * The first call on each device (with that device current) looks up the
+ * array's device address and caches it; make that first call before any stream
+ * capture. All calls share the one array and it keeps the last call's
+ * contents; nothing in it needs clearing, but calls whose GPU work overlaps in
+ * time (other streams, other host threads) race on it: serialise them.
+ */
+#define DSA_NOALLOC_SCRATCH_BYTES ((size_t)48 << 20)
+int dsa_sparse_mla_decode_noalloc(const dsa_bf16* qlat, int rows, int heads, int kv_lora_rank,
+                                  const int32_t* row_seq, const dsa_bf16* ckv,
+                                  const dsa_paging* pg, const int32_t* token_ids, int out_width,
+                                  float softmax_scale, const dsa_bf16* o_absorb, int hidden,
+                                  dsa_bf16* y, float* olat, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

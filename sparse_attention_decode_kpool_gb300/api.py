@@ -14,7 +14,8 @@ from . import _lib
 from ._lib import DsaPaging, check
 
 __all__ = ["paging", "dsa_compress", "dsa_score", "dsa_select", "dsa_expand",
-           "dsa_sparse_mla_decode_workspace", "dsa_sparse_mla_decode", "dsa_select_k",
+           "dsa_sparse_mla_decode_workspace", "dsa_sparse_mla_decode",
+           "dsa_sparse_mla_decode_noalloc", "dsa_select_k",
            "dsa_validate_config", "DsaPaging"]
 
 
@@ -147,3 +148,21 @@ def dsa_sparse_mla_decode(qlat, row_seq, ckv, pg: DsaPaging, token_ids, softmax_
         _ptr(o_absorb, torch.bfloat16, "o_absorb"), hidden, _ptr(y, torch.bfloat16, "y"),
         _ptr(olat, torch.float32, "olat"), _ptr(status, torch.int32, "status"),
         _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)))
+
+
+def dsa_sparse_mla_decode_noalloc(qlat, row_seq, ckv, pg: DsaPaging, token_ids,
+                                  softmax_scale: float, o_absorb=None, y=None, olat=None,
+                                  status=None, stream=None) -> None:
+    """dsa_sparse_mla_decode without a workspace: the library's fixed scratch array
+    is used instead (for hosts that cannot allocate device memory; see
+    include/dsa.h). Calls whose GPU work overlaps in time must be serialised."""
+    rows, heads, kvl = (int(x) for x in qlat.shape)
+    ow = int(token_ids.shape[1])
+    hidden = int(o_absorb.shape[0]) if o_absorb is not None else 0
+    check(_lib.load().dsa_sparse_mla_decode_noalloc(
+        _ptr(qlat, torch.bfloat16, "qlat"), rows, heads, kvl,
+        _ptr(row_seq, torch.int32, "row_seq"), _ptr(ckv, torch.bfloat16, "ckv"),
+        ctypes.byref(pg), _ptr(token_ids, torch.int32, "token_ids"), ow, float(softmax_scale),
+        _ptr(o_absorb, torch.bfloat16, "o_absorb"), hidden, _ptr(y, torch.bfloat16, "y"),
+        _ptr(olat, torch.float32, "olat"), _ptr(status, torch.int32, "status"),
+        _stream(stream)))
