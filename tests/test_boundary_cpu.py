@@ -1,0 +1,147 @@
+"""The C ABI on the host, without a GPU: the library loads and exports every symbol
+include/dsa.h declares, host-visible argument errors come back as the documented
+codes before anything touches CUDA, the paging struct matches the C layout, and the
+product path refuses to run without the library."""
+import ctypes
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+from sparse_attention_decode_kpool_gb300 import _build, _lib
+from sparse_attention_decode_kpool_gb300._lib import (DSA_ERR_CONFIG, DSA_ERR_INVALID_ARG,
+                                                       DSA_ERR_UNSUPPORTED, DSA_OK, DsaPaging)
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000  # a non-NULL device address the host never dereferences
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return _lib.load()
+
+
+def _err(lib):
+    return lib.dsa_last_error().decode()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _lib.header_functions()
+    assert len(names) >= 11
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(_lib.SIGNATURES) == set(names)
+    assert lib.dsa_abi_version() == _lib.DSA_ABI_VERSION
+
+
+@pytest.mark.parametrize("args,code", [
+    ((4, 2048, 512, 64), DSA_OK),
+    ((0, 2048, 512, 64), DSA_ERR_CONFIG),
+    ((4, 0, 512, 64), DSA_ERR_CONFIG),
+    ((4, 2050, 512, 64), DSA_ERR_CONFIG),
+    ((32, 64, 512, 64), DSA_ERR_UNSUPPORTED),
+    ((16, 64, 512, 64), DSA_OK),
+    ((4, 2048, 0, 64), DSA_ERR_CONFIG),
+    ((4, 2048, 576, 64), DSA_ERR_UNSUPPORTED),
+    ((4, 2048, 512, 0), DSA_ERR_CONFIG),
+])
+def test_validate_config_rules(lib, args, code):
+    rc = lib.dsa_validate_config(*args)
+    assert rc == code
+    if code:
+        assert _err(lib)
+
+
+def test_select_k(lib):
+    assert lib.dsa_select_k(2048, 4, 65536) == 512
+    assert lib.dsa_select_k(256, 4, 50) == 50
+    assert lib.dsa_select_k(0, 4, 50) == -1
+
+
+def _paging(batch=1, max_seq_len=1024, block_table=None, max_blocks=0, block_size=0, nb=0):
+    pg = DsaPaging()
+    pg.batch, pg.max_seq_len, pg.seq_lens = batch, max_seq_len, FAKE
+    pg.block_table, pg.max_blocks, pg.block_size, pg.num_blocks = block_table, max_blocks, block_size, nb
+    return pg
+
+
+def test_compress_argument_errors(lib):
+    pg = _paging()
+    call = lambda kp, ihd, pgp=ctypes.byref(pg), fk=0: lib.dsa_compress(
+        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1e-6, pgp, fk, kp, ihd, FAKE, FAKE, None, None, None)
+    assert call(17, 128) == DSA_ERR_UNSUPPORTED
+    assert call(0, 128) == DSA_ERR_UNSUPPORTED
+    assert call(4, 96) == DSA_ERR_UNSUPPORTED
+    assert call(4, 128, None) == DSA_ERR_INVALID_ARG
+    assert call(4, 128, ctypes.byref(pg), -1) == DSA_ERR_INVALID_ARG
+    paged = _paging(block_table=FAKE, max_blocks=16, block_size=64, nb=8)
+    assert call(3, 128, ctypes.byref(paged)) == DSA_ERR_UNSUPPORTED  # 64 % 3 != 0
+    assert call(4, 128, ctypes.byref(paged), 2) == DSA_ERR_UNSUPPORTED  # first_key % kpool
+    short = _paging(max_seq_len=2048, block_table=FAKE, max_blocks=16, block_size=64, nb=8)
+    assert call(4, 128, ctypes.byref(short)) == DSA_ERR_INVALID_ARG  # 16*64 < 2048
+    assert "paging" in _err(lib)
+
+
+def test_score_select_expand_argument_errors(lib):
+    pg = _paging()
+    score = lambda heads, ihd, kp=4: lib.dsa_score(FAKE, FAKE, 1, heads, ihd, None, None, FAKE,
+                                                   FAKE, ctypes.byref(pg), 0, kp, 0.1, FAKE, 16,
+                                                   None, None)
+    assert score(65, 128) == DSA_ERR_UNSUPPORTED
+    assert score(32, 96) == DSA_ERR_UNSUPPORTED
+    assert score(32, 128, 0) == DSA_ERR_UNSUPPORTED
+    assert lib.dsa_score(FAKE, FAKE, 0, 32, 128, None, None, FAKE, FAKE, ctypes.byref(pg), 0, 4,
+                         0.1, FAKE, 16, None, None) == DSA_OK  # nothing to do
+    assert lib.dsa_select(FAKE, 1, 100, 0, 4, FAKE, None) == DSA_ERR_CONFIG
+    assert lib.dsa_select(FAKE, 1, 393217, 2048, 4, FAKE, None) == DSA_ERR_UNSUPPORTED
+    assert lib.dsa_select(FAKE, 0, 100, 2048, 4, FAKE, None) == DSA_OK
+    assert lib.dsa_select(None, 1, 100, 2048, 4, FAKE, None) == DSA_ERR_INVALID_ARG
+    assert lib.dsa_expand(FAKE, 2, 64, 0, 4, 255, FAKE, None) == DSA_ERR_INVALID_ARG
+    assert lib.dsa_expand(FAKE, 0, 64, 0, 4, 256, FAKE, None) == DSA_OK
+    assert lib.dsa_expand(FAKE, 2, 64, -1, 4, 256, FAKE, None) == DSA_ERR_INVALID_ARG
+
+
+def test_sparse_mla_argument_errors(lib):
+    pg = _paging()
+
+    def mla(kvl=512, hidden=4096, oabs=FAKE, y=FAKE, heads=64):
+        return lib.dsa_sparse_mla_decode(FAKE, 1, heads, kvl, None, FAKE, ctypes.byref(pg), FAKE,
+                                         2048, 0.0625, oabs, hidden, y, None, None, FAKE, 1 << 20,
+                                         None)
+
+    assert mla(kvl=576) == DSA_ERR_UNSUPPORTED
+    assert mla(kvl=0) == DSA_ERR_CONFIG
+    assert mla(hidden=100) == DSA_ERR_UNSUPPORTED
+    assert mla(y=None) == DSA_ERR_INVALID_ARG
+    assert mla(heads=0) == DSA_ERR_INVALID_ARG
+    n = ctypes.c_size_t()
+    assert lib.dsa_sparse_mla_decode_workspace(1, 64, 576, 2048, 4096, 1, ctypes.byref(n)) == \
+        DSA_ERR_UNSUPPORTED
+    assert lib.dsa_sparse_mla_decode_noalloc(FAKE, 1, 64, 576, None, FAKE, ctypes.byref(pg), FAKE,
+                                             2048, 0.0625, FAKE, 4096, FAKE, None, None,
+                                             None) == DSA_ERR_UNSUPPORTED
+
+
+def test_paging_struct_matches_c_layout(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "dsa.h"\nint main(void){'
+                   'printf("%zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(dsa_paging),'
+                   'offsetof(dsa_paging,batch),offsetof(dsa_paging,max_seq_len),'
+                   'offsetof(dsa_paging,seq_lens),offsetof(dsa_paging,block_table),'
+                   'offsetof(dsa_paging,max_blocks),offsetof(dsa_paging,block_size),'
+                   'offsetof(dsa_paging,num_blocks));return 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    c = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
+    py = [ctypes.sizeof(DsaPaging)] + [getattr(DsaPaging, f).offset for f, _ in DsaPaging._fields_]
+    assert c == py
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", "/nonexistent/libdsa.so")
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        _lib.load()
