@@ -168,7 +168,8 @@ def algorithmic_bytes(wl, layer) -> dict:
     qlat = wl.rows * g.heads * g.kv_lora_rank * 2
     oabs = g.hidden * g.heads * g.kv_lora_rank * 2 if layer.o_absorb is not None else 0
     y = wl.rows * g.hidden * 2 if layer.o_absorb is not None else 0
-    return {"score": keys + flags + q, "attend": latent + qlat + oabs + y,
+    olat = wl.rows * g.heads * g.kv_lora_rank * 4 if layer.o_absorb is not None else 0
+    return {"score": keys + flags + q, "attend": latent + qlat, "project": oabs + olat + y,
             "total": keys + flags + q + latent + qlat + oabs + y, "selected_tokens": sel_tokens,
             "candidate_pools": cand}
 
@@ -284,7 +285,8 @@ def workload_config(wl, args) -> dict:
             "index_head_dim": g.index_head_dim, "index_topk": g.index_topk, "heads": g.heads,
             "kv_lora_rank": g.kv_lora_rank, "hidden": g.hidden,
             "paged_block": wl.block_size, "seed": wl.seed,
-            "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+            "l2": "flushed between timed steps (256 MiB write, then a 256 MiB read so the dirty "
+                  "lines are written back; both outside the timed events)",
             "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
 
 
@@ -297,6 +299,8 @@ def main():
     ap.add_argument("--workload", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="shrink the 262K workload's sequences (profiling runs only)")
     args = ap.parse_args()
     ws, rank, local = dist_init(args.gpus)
     if args.impl == "reference":
@@ -314,14 +318,26 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
-    wl = W.WORKLOADS[args.workload]()
+    wl = (W.long_262k(seq_len=args.seq_len) if (args.seq_len and args.workload == 3)
+          else W.WORKLOADS[args.workload]())
     layer = DsaDecodeLayer(wl, device=str(dev))
     layer.compress()
     torch.cuda.synchronize()
 
     # compress alone (setup stage, reported on its own)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    class _Flush:
+        """Write 256 MiB (evicts L2), then read another 256 MiB so the dirty lines
+        are written back before the timed region instead of inside it."""
+
+        def zero_(self):
+            flush_w.zero_()
+            flush_r.sum()
+
+    flush = _Flush()
     ct = []
     for _ in range(3):
         flush.zero_()
@@ -335,13 +351,7 @@ def main():
     torch.cuda.synchronize()
     assert int(layer.status.item()) == 0, "device status flagged during the first step"
 
-    # Graph with stage-boundary timing events (external event nodes when supported).
-    stage_names = ["score", "select", "expand", "attend"]
-    try:
-        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
-        graph_events = True
-    except TypeError:
-        ev, graph_events = None, False
+    # The timed graph: the step's library calls only.
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(s):
@@ -350,14 +360,25 @@ def main():
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        if graph_events:
+        layer.step()
+    # A second graph with timing event nodes at the stage boundaries (external
+    # events when the installed torch supports them): per-stage times.
+    stage_names = ["score", "select", "expand", "attend", "project"]
+    try:
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+        graph_events = True
+    except TypeError:
+        ev, graph_events = None, False
+    sgraph = None
+    if graph_events:
+        sgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(sgraph):
             ev[0].record()
             layer.score(); ev[1].record()
             layer.select(); ev[2].record()
             layer.expand(); ev[3].record()
             layer.attend(); ev[4].record()
-        else:
-            layer.step()
+            layer.project(); ev[5].record()
 
     launches = layer.launches_per_step()
     for _ in range(args.warmup):
@@ -367,7 +388,6 @@ def main():
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stage_ms = {k: 0.0 for k in stage_names}
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(dev) as clocks:
@@ -376,22 +396,26 @@ def main():
             starts[i].record()
             graph.replay()
             ends[i].record()
-            if graph_events:
-                ends[i].synchronize()
-                for j, k in enumerate(stage_names):
-                    stage_ms[k] += ev[j].elapsed_time(ev[j + 1])
         torch.cuda.synchronize()
     barrier(ws)
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     ms = sum(step_ms) / args.steps
     ms = max_over_ranks(ms, ws)
-    if not graph_events:  # eager per-stage timing pass (same stream, same kernels)
-        for i in range(args.steps):
-            flush.zero_()
-            ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    # Per-stage times (separate pass; event nodes add a little time of their own).
+    stage_ms = {k: 0.0 for k in stage_names}
+    for i in range(args.steps):
+        flush.zero_()
+        if graph_events:
+            sgraph.replay()
+            ev[5].synchronize()
+            for j, k in enumerate(stage_names):
+                stage_ms[k] += ev[j].elapsed_time(ev[j + 1])
+        else:
+            ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
             ev2[0].record(); layer.score(); ev2[1].record(); layer.select(); ev2[2].record()
             layer.expand(); ev2[3].record(); layer.attend(); ev2[4].record()
-            ev2[4].synchronize()
+            layer.project(); ev2[5].record()
+            ev2[5].synchronize()
             for j, k in enumerate(stage_names):
                 stage_ms[k] += ev2[j].elapsed_time(ev2[j + 1])
     stage_ms = {k: v / args.steps for k, v in stage_ms.items()}
@@ -442,14 +466,15 @@ def main():
     peak_src = "measured" if hbm else "fallback"
     hbm = hbm or 6800.0
     ab = algorithmic_bytes(wl, layer)
-    dom = max(("score", "attend"), key=lambda k: stage_ms[k])
+    dom = max(("score", "attend", "project"), key=lambda k: stage_ms[k])
     dom_bytes = ab[dom]
     achieved = dom_bytes / (stage_ms[dom] * 1e-3) / 1e9
     total_gbs = ab["total"] / (ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "traffic": None, "peak_source": peak_src,
-                "kernel": {"attend": "dsa_sparse_mla_decode (split attention + combine + "
-                                     "o_absorb GEMV + sum)",
+                "kernel": {"attend": "dsa_sparse_mla_decode (split attention + combine)",
+                           "project": "dsa_latent_project (TMA-pipelined o_absorb GEMM + "
+                                      "partial sum)",
                            "score": "dsa_score"}[dom],
                 "algorithmic_bytes_per_launch": dom_bytes,
                 "step_algorithmic_bytes": ab["total"], "step_achieved_gbs": total_gbs,
@@ -460,7 +485,9 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(wl, args),
         "roofline": roofline,
-        "stages_ms": stage_ms, "stage_timing": "graph event nodes" if graph_events else "eager pass",
+        "stages_ms": stage_ms,
+        "stage_timing": ("separate pass, graph with event nodes" if graph_events
+                         else "separate eager pass"),
         "compress_ms": min(ct),
         "gpu_launches": launches * args.steps,
         "clocks": clocks.summary(),

@@ -53,6 +53,7 @@ extern "C" {
 
 #define DSA_STATUS_BAD_TOKEN 1 /* token id < -1, or >= its sequence's length  */
 #define DSA_STATUS_BAD_BLOCK 2 /* block-table entry outside [0, num_blocks)    */
+#define DSA_STATUS_TIMEOUT 4   /* a pipeline wait gave up after ~1 s (results invalid) */
 
 #define DSA_KV_LORA_RANK 512 /* latent width the attention kernels are built for */
 #define DSA_MAX_KPOOL 16     /* most slots per pool dsa_compress handles         */
@@ -168,7 +169,7 @@ int dsa_score(const dsa_bf16* qidx, const float* w, int rows, int index_heads, i
  * NaN scores give unspecified (but in-bounds) results.
  *
  * scores [rows, p_stride] f32; pool_ids [rows, select_k] i32.
- * Limits: p_stride <= 393,216.
+ * Limits: p_stride <= 327,680.
  */
 int dsa_select(const float* scores, int rows, int p_stride, int index_topk, int kpool,
                int32_t* pool_ids, void* stream);
@@ -211,6 +212,26 @@ int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, int kv_lora
                           const dsa_bf16* o_absorb, int hidden, dsa_bf16* y, float* olat,
                           int32_t* status, void* workspace, size_t workspace_bytes,
                           void* stream);
+
+/*
+ * dsa_latent_project -- the absorbed output projection on its own (build.rs,
+ * module doc, transform 3 and absorb_o: o_proj is multiplied through kv_b_proj's V
+ * half, so the decode output [heads, kv_lora_rank] maps back to hidden):
+ *
+ *   y[r, i] = bf16(sum_k o_absorb[i, k] * bf16(olat[r, k])),  k < heads*kv_lora_rank
+ *
+ * This is the last step of dsa_sparse_mla_decode, callable separately so that the
+ * attention (o_absorb = NULL, olat output) and the projection can be scheduled and
+ * timed apart; the two-call form gives results identical to the one-call form.
+ * olat [rows, heads*kv_lora_rank] f32 (rounded to bf16 as the MMA operand);
+ * o_absorb [hidden, heads*kv_lora_rank] bf16; y [rows, hidden] bf16; status as
+ * above (DSA_STATUS_TIMEOUT only). Limits: kv_lora_rank == 512; hidden % 64 == 0.
+ */
+int dsa_latent_project_workspace(int rows, int heads, int kv_lora_rank, int hidden,
+                                 size_t* bytes);
+int dsa_latent_project(const float* olat, int rows, int heads, int kv_lora_rank,
+                       const dsa_bf16* o_absorb, int hidden, dsa_bf16* y, int32_t* status,
+                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * dsa_sparse_mla_decode_noalloc -- dsa_sparse_mla_decode for callers that cannot

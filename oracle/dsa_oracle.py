@@ -246,9 +246,17 @@ def sparse_mla_decode_row(qlat_row, ckv_seq, token_ids_row, softmax_scale: float
         olat = p @ kv
     if o_absorb is None:
         return olat, None, None
+    y, yb = latent_project(olat, o_absorb)
+    return olat, y, yb
+
+
+def latent_project(olat, o_absorb):
+    """The absorbed output projection (build.rs, transform 3 and ``absorb_o``):
+    ``y[i] = sum_{h,c} o_absorb[i, h*kvl + c] * olat[h, c]``; y is stored bf16.
+    Returns ``(y_exact, y_bf16)``."""
     A = np.asarray(o_absorb, dtype=F64)  # [hidden, H*kvl]
-    y = A @ olat.reshape(-1)
-    return olat, y, bf16_round(y)
+    y = A @ np.asarray(olat, dtype=F64).reshape(-1)
+    return y, bf16_round(y)
 
 
 # ---------------------------------------------------------------------------

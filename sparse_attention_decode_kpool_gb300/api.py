@@ -15,7 +15,8 @@ from ._lib import DsaPaging, check
 
 __all__ = ["paging", "dsa_compress", "dsa_score", "dsa_select", "dsa_expand",
            "dsa_sparse_mla_decode_workspace", "dsa_sparse_mla_decode",
-           "dsa_sparse_mla_decode_noalloc", "dsa_select_k",
+           "dsa_sparse_mla_decode_noalloc", "dsa_latent_project_workspace",
+           "dsa_latent_project", "dsa_select_k",
            "dsa_validate_config", "DsaPaging"]
 
 
@@ -147,6 +148,27 @@ def dsa_sparse_mla_decode(qlat, row_seq, ckv, pg: DsaPaging, token_ids, softmax_
         ctypes.byref(pg), _ptr(token_ids, torch.int32, "token_ids"), ow, float(softmax_scale),
         _ptr(o_absorb, torch.bfloat16, "o_absorb"), hidden, _ptr(y, torch.bfloat16, "y"),
         _ptr(olat, torch.float32, "olat"), _ptr(status, torch.int32, "status"),
+        _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)))
+
+
+def dsa_latent_project_workspace(rows: int, heads: int, hidden: int,
+                                 kv_lora_rank: int = 512) -> int:
+    n = ctypes.c_size_t(0)
+    check(_lib.load().dsa_latent_project_workspace(int(rows), int(heads), int(kv_lora_rank),
+                                                   int(hidden), ctypes.byref(n)))
+    return int(n.value)
+
+
+def dsa_latent_project(olat, o_absorb, y, status=None, workspace=None, stream=None) -> None:
+    """y = bf16(o_absorb @ bf16(olat)) per row; olat [rows, heads, 512] f32."""
+    rows, heads, kvl = (int(x) for x in olat.shape)
+    hidden = int(o_absorb.shape[0])
+    if tuple(o_absorb.shape) != (hidden, heads * kvl) or tuple(y.shape) != (rows, hidden):
+        raise ValueError("o_absorb must be [hidden, heads*kvl] and y [rows, hidden]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check(_lib.load().dsa_latent_project(
+        _ptr(olat, torch.float32, "olat"), rows, heads, kvl, _ptr(o_absorb, torch.bfloat16, "o_absorb"),
+        hidden, _ptr(y, torch.bfloat16, "y"), _ptr(status, torch.int32, "status"),
         _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)))
 
 

@@ -493,6 +493,7 @@ struct Plan {
     int gemv_nt;
     int KS;
     int n_mg;
+    bool tma_proj;  // the TMA-pipelined projection (project.cu) handles o_absorb
     size_t off_part_o, off_part_ml, off_xbf, off_ypart, bytes;
 };
 
@@ -530,7 +531,11 @@ Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms)
     p.off_xbf = off;
     if (with_oabs) off += align256((size_t)rows * heads * KVL * 2);
     p.off_ypart = off;
-    if (with_oabs) off += align256((size_t)p.KS * rows * hidden * 4);
+    p.tma_proj = with_oabs && project_supported(heads * KVL, hidden);
+    if (p.tma_proj)
+        off += align256(project_workspace_bytes(rows, heads * KVL, hidden, sms));
+    else if (with_oabs)
+        off += align256((size_t)p.KS * rows * hidden * 4);
     p.bytes = off;
     return p;
 }
@@ -647,6 +652,10 @@ extern "C" int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, 
                                                               olat, a.xbf);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_mla_decode combine launch");
+    }
+    if (p.tma_proj) {
+        return project_launch(a.xbf, false, rows, heads * KVL, o_absorb, hidden, y, status,
+                              ws + p.off_ypart, workspace_bytes - p.off_ypart, st);
     }
     if (with_oabs) {
         GemvArgs g;

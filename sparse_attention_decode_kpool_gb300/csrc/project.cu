@@ -1,0 +1,354 @@
+// The absorbed output projection y = o_absorb . olat (dsa_latent_project, and the last
+// step of dsa_sparse_mla_decode).
+//
+// Page: metrale_model_arch/glm5next_dsa/build.rs, module doc, transform 3 and
+// absorb_o: o_proj is multiplied through kv_b_proj's V half at load, so the decode
+// kernel's latent output [heads, kv_lora_rank] maps back to hidden through
+// o_absorb [hidden, heads * kv_lora_rank].
+//
+// At decode sizes this is a skinny GEMM: every element of o_absorb (268 MB at
+// 4096 x 64 x 512) is used by only the few query rows of the step, so the kernel is
+// an HBM stream. It is built so the number of bytes in flight does not depend on
+// registers: one producer warp per CTA issues bulk async copies (the TMA engine's
+// non-tensor form, one 512-byte row segment per copy) into a ring of shared-memory
+// stages guarded by mbarriers; four consumer warps turn each stage into m16n8k16
+// MMAs (o_absorb rows on M, query rows on N, f32 accumulation). The grid is one CTA
+// per SM and the (row block, k block) units are split evenly over the CTAs in
+// row-block-major order ("stream-K"), so every SM streams the same number of bytes;
+// a CTA whose range crosses a row block writes one partial per row block, and a
+// small reduction adds the partials of each row block in a fixed order.
+//
+// All waits are bounded (about 1 s); a wait that gives up sets DSA_STATUS_TIMEOUT in
+// the status word and the CTA winds down after its own copies have landed.
+#include "common.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int KT = 256;               // k per stage (one 512-byte box row of o_absorb)
+constexpr int MROWS = 64;             // o_absorb rows per CTA tile: 4 consumer warps x 16
+constexpr int kConsumers = 4;
+constexpr int kThreads = (kConsumers + 1) * 32;
+
+// CTAs per SM: two for the decode sizes (<= 16 query rows), so that every scheduler
+// has two consumer warps; one with the larger query-row tiles.
+__host__ __device__ constexpr int ctas_per_sm(int nt) { return nt <= 2 ? 2 : 1; }
+
+template <int NT, bool XF32>
+struct Cfg {
+    static constexpr int XB = XF32 ? 4 : 2;
+    static constexpr int A_BYTES = MROWS * KT * 2;        // one 256 x 64 box
+    static constexpr int X_BYTES = 8 * NT * KT * XB;      // one 256 x (8*NT) box
+    static constexpr int STAGE = A_BYTES + X_BYTES;       // multiple of 1 KiB
+    static constexpr int S_FIT = (200 * 1024) / ctas_per_sm(NT) / STAGE;
+    static constexpr int S = S_FIT > 6 ? 6 : (S_FIT < 2 ? 2 : S_FIT);
+    static constexpr int SMEM = S * STAGE + 2 * S * 8;
+};
+
+struct ProjArgs {
+    const uint16_t* A;  // [hidden, K] bf16
+    const void* X;      // [R, K] bf16 or f32
+    float* ypart;       // [G, J, R, 64]
+    int32_t* status;
+    long long U;        // units = (hidden / 64) * KB
+    int K;
+    int KB;             // K / KT
+    int R;
+    int n0;
+    int nrows;
+    int J;
+};
+
+__host__ __device__ inline long long unit_begin(long long c, long long U, long long G) {
+    return c * U / G;
+}
+
+template <int NT, bool XF32>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(NT))
+    project_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmX,
+                   ProjArgs a) {
+    using C = Cfg<NT, XF32>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::S * C::STAGE);
+    uint64_t* empty = full + C::S;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const long long G = gridDim.x;
+    const long long u0 = unit_begin(blockIdx.x, a.U, G);
+    const long long u1 = unit_begin(blockIdx.x + 1, a.U, G);
+
+    if (tid == 0) {
+        for (int s = 0; s < C::S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumers);
+        }
+        fence_mbar_init();
+    }
+    if ((smem_u32(smem) & 127u) != 0u) {  // tensor copies need an aligned destination
+        if (tid == 0) flag_status(a.status, DSA_STATUS_TIMEOUT);
+        return;
+    }
+    __syncthreads();
+
+    if (warp == kConsumers) {
+        // ---------------- producer warp: one elected lane issues two tensor copies per stage
+        const uint32_t bytes = (uint32_t)C::STAGE;  // full boxes (zero fill counts too)
+        long long i = 0;
+        bool ok = true;
+        if (lane == 0) {
+            for (long long u = u0; u < u1; ++u, ++i) {
+                const int s = (int)(i % C::S);
+                const uint32_t ph = (uint32_t)((i / C::S) & 1);
+                if (!mbar_wait(&empty[s], ph ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                const int mb = (int)(u / a.KB);
+                const int kb = (int)(u % a.KB);
+                mbar_arrive_expect_tx(&full[s], bytes);
+                const uint32_t dst = smem_u32(smem + s * C::STAGE);
+                tma_load_2d(dst, &tmA, kb * KT, mb * MROWS, &full[s]);
+                tma_load_2d(dst + C::A_BYTES, &tmX, kb * KT, a.n0, &full[s]);
+            }
+        }
+        if (lane == 0) {
+            if (!ok) flag_status(a.status, DSA_STATUS_TIMEOUT);
+            // Let the copies already issued land before the CTA may exit.
+            const long long first = i > C::S ? i - C::S : 0;
+            for (long long j = first; j < i; ++j)
+                if (!mbar_wait(&full[j % C::S], (uint32_t)((j / C::S) & 1))) break;
+        }
+        return;
+    }
+
+    // ---------------- consumer warps: rows 16*warp .. +15 of the 64-row tile
+    const int g = lane >> 2, q = lane & 3;
+    const int rA = 16 * warp + g;
+    float acc[NT][4];
+    long long cur_mb = -1;
+    const int J = a.J;
+    auto flush = [&](long long mb) {
+        const int j = (int)(mb - u0 / a.KB);
+        float* base = a.ypart + (((long long)blockIdx.x * J + j) * a.R + a.n0) * MROWS;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int n = nt * 8 + 2 * q + jj;
+                if (n < a.nrows) {
+                    base[(long long)n * MROWS + rA] = acc[nt][jj];
+                    base[(long long)n * MROWS + rA + 8] = acc[nt][2 + jj];
+                }
+            }
+    };
+    long long i = 0;
+    for (long long u = u0; u < u1; ++u, ++i) {
+        const int s = (int)(i % C::S);
+        const uint32_t ph = (uint32_t)((i / C::S) & 1);
+        const long long mb = u / a.KB;
+        if (mb != cur_mb) {
+            if (cur_mb >= 0) flush(cur_mb);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+            cur_mb = mb;
+        }
+        if (!mbar_wait(&full[s], ph)) {
+            if (lane == 0) flag_status(a.status, DSA_STATUS_TIMEOUT);
+            break;
+        }
+        const uint32_t sa = smem_u32(smem + s * C::STAGE);
+        const uint32_t sx = sa + C::A_BYTES;
+#pragma unroll
+        for (int kc = 0; kc < KT / 128; ++kc) {
+            uint4 ra0[4], ra1[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int e = kc * 128 + 32 * v + 8 * q;
+                ra0[v] = lds16(sa + rA * (KT * 2) + e * 2);
+                ra1[v] = lds16(sa + (rA + 8) * (KT * 2) + e * 2);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int n = nt * 8 + g;
+                uint4 xv[4];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int e = kc * 128 + 32 * v + 8 * q;
+                    if (XF32) {
+                        const uint32_t ad = sx + n * (KT * 4) + e * 4;
+                        const uint4 f0 = lds16(ad), f1 = lds16(ad + 16);
+                        xv[v].x = pack_bf16x2(__uint_as_float(f0.x), __uint_as_float(f0.y));
+                        xv[v].y = pack_bf16x2(__uint_as_float(f0.z), __uint_as_float(f0.w));
+                        xv[v].z = pack_bf16x2(__uint_as_float(f1.x), __uint_as_float(f1.y));
+                        xv[v].w = pack_bf16x2(__uint_as_float(f1.z), __uint_as_float(f1.w));
+                    } else {
+                        xv[v] = lds16(sx + n * (KT * 2) + e * 2);
+                    }
+                }
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    mma_16816(acc[nt], ra0[v].x, ra1[v].x, ra0[v].y, ra1[v].y, xv[v].x, xv[v].y);
+                    mma_16816(acc[nt], ra0[v].z, ra1[v].z, ra0[v].w, ra1[v].w, xv[v].z, xv[v].w);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (cur_mb >= 0) flush(cur_mb);
+}
+
+// y[r, col] = bf16(sum over the CTAs that covered row block col/64 of their partial).
+__global__ void project_reduce_kernel(const float* __restrict__ ypart, long long U, int KB, int G,
+                                      int J, int R, int hidden, uint16_t* __restrict__ y) {
+    const long long n = (long long)R * hidden;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(i / hidden);
+        const int col = (int)(i % hidden);
+        const long long mb = col / MROWS;
+        const long long lo = mb * KB, hi = lo + KB;
+        long long c = lo * G / U;
+        while (c > 0 && unit_begin(c, U, G) > lo) --c;
+        float s = 0.f;
+        for (; c < G; ++c) {
+            const long long b0 = unit_begin(c, U, G), b1 = unit_begin(c + 1, U, G);
+            if (b0 >= hi) break;
+            if (b1 <= lo || b1 == b0) continue;
+            const int j = (int)(mb - b0 / KB);
+            s += __ldg(ypart + (((long long)c * J + j) * R + r) * MROWS + (col % MROWS));
+        }
+        y[i] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+    }
+}
+
+struct ProjPlan {
+    long long U;
+    int KB, G, J, nt;
+    size_t bytes;
+};
+
+ProjPlan plan_for(int rows, int K, int hidden, int sms) {
+    ProjPlan p;
+    const int nr = rows < 64 ? rows : 64;
+    p.nt = nr <= 8 ? 1 : nr <= 16 ? 2 : nr <= 32 ? 4 : 8;
+    p.KB = K / KT;
+    p.U = (long long)(hidden / MROWS) * p.KB;
+    const long long slots = (long long)sms * ctas_per_sm(p.nt);
+    p.G = (int)(p.U < slots ? p.U : slots);
+    if (p.G < 1) p.G = 1;
+    const long long per = (p.U + p.G - 1) / p.G;
+    p.J = (int)((per + p.KB - 1) / p.KB) + 1;
+    p.bytes = (size_t)p.G * p.J * rows * MROWS * sizeof(float);
+    return p;
+}
+
+template <int NT, bool XF32>
+int launch_proj(const ProjArgs& a, int G, cudaStream_t st) {
+    using C = Cfg<NT, XF32>;
+    int rc = set_max_smem((const void*)project_kernel<NT, XF32>, C::SMEM);
+    if (rc) return rc;
+    CUtensorMap tmA, tmX;
+    rc = make_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, (uint64_t)a.K,
+                      (uint64_t)(a.U / a.KB) * MROWS, (uint64_t)a.K * 2, KT, MROWS);
+    if (rc) return rc;
+    rc = make_tmap_2d(&tmX, XF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      a.X, (uint64_t)a.K, (uint64_t)a.R, (uint64_t)a.K * C::XB, KT, 8 * NT);
+    if (rc) return rc;
+    project_kernel<NT, XF32><<<G, kThreads, C::SMEM, st>>>(tmA, tmX, a);
+    return DSA_OK;
+}
+
+template <bool XF32>
+int dispatch(const ProjArgs& a, int nt, int G, cudaStream_t st) {
+    switch (nt) {
+        case 1: return launch_proj<1, XF32>(a, G, st);
+        case 2: return launch_proj<2, XF32>(a, G, st);
+        case 4: return launch_proj<4, XF32>(a, G, st);
+        default: return launch_proj<8, XF32>(a, G, st);
+    }
+}
+
+}  // namespace
+
+bool project_supported(int K, int hidden) { return hidden > 0 && hidden % MROWS == 0 && K % KT == 0; }
+
+size_t project_workspace_bytes(int rows, int K, int hidden, int sms) {
+    return plan_for(rows, K, hidden, sms).bytes;
+}
+
+int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A, int hidden,
+                   uint16_t* y, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st) {
+    const int sms = sm_count();
+    if (sms <= 0) return fail(DSA_ERR_CUDA, "projection: no CUDA device");
+    const ProjPlan p = plan_for(rows, K, hidden, sms);
+    if (ws_bytes < p.bytes) return fail(DSA_ERR_INVALID_ARG, "projection: workspace too small");
+    ProjArgs a;
+    a.A = A;
+    a.X = x;
+    a.ypart = static_cast<float*>(ws);
+    a.status = status;
+    a.U = p.U;
+    a.K = K;
+    a.KB = p.KB;
+    a.R = rows;
+    a.J = p.J;
+    for (int n0 = 0; n0 < rows; n0 += 64) {
+        a.n0 = n0;
+        a.nrows = rows - n0 < 64 ? rows - n0 : 64;
+        int rc = x_f32 ? dispatch<true>(a, p.nt, p.G, st) : dispatch<false>(a, p.nt, p.G, st);
+        if (rc) return rc;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+    const long long n = (long long)rows * hidden;
+    long long blocks = (n + 255) / 256;
+    if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+    project_reduce_kernel<<<(int)blocks, 256, 0, st>>>(static_cast<float*>(ws), p.U, p.KB, p.G,
+                                                       p.J, rows, hidden, y);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "projection reduce launch");
+    return DSA_OK;
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" int dsa_latent_project_workspace(int rows, int heads, int kv_lora_rank, int hidden,
+                                            size_t* bytes) {
+    if (!bytes) return fail(DSA_ERR_INVALID_ARG, "dsa_latent_project_workspace: bytes is NULL");
+    if (rows < 0 || heads < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_latent_project: rows/heads");
+    if (kv_lora_rank != DSA_KV_LORA_RANK)
+        return fail(kv_lora_rank == 0 ? DSA_ERR_CONFIG : DSA_ERR_UNSUPPORTED,
+                    "dsa_latent_project: kv_lora_rank %d, built for %d", kv_lora_rank,
+                    DSA_KV_LORA_RANK);
+    if (!project_supported(heads * kv_lora_rank, hidden))
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_latent_project: hidden %d must be a multiple of 64",
+                    hidden);
+    const int sms = sm_count();
+    if (sms <= 0) return fail(DSA_ERR_CUDA, "dsa_latent_project_workspace: no CUDA device");
+    *bytes = project_workspace_bytes(rows, heads * kv_lora_rank, hidden, sms);
+    return DSA_OK;
+}
+
+extern "C" int dsa_latent_project(const float* olat, int rows, int heads, int kv_lora_rank,
+                                  const dsa_bf16* o_absorb, int hidden, dsa_bf16* y,
+                                  int32_t* status, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+    if (rows < 0 || heads < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_latent_project: rows/heads");
+    if (kv_lora_rank != DSA_KV_LORA_RANK)
+        return fail(kv_lora_rank == 0 ? DSA_ERR_CONFIG : DSA_ERR_UNSUPPORTED,
+                    "dsa_latent_project: kv_lora_rank %d, built for %d", kv_lora_rank,
+                    DSA_KV_LORA_RANK);
+    if (!project_supported(heads * kv_lora_rank, hidden))
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_latent_project: hidden %d must be a multiple of 64",
+                    hidden);
+    if (rows == 0) return DSA_OK;
+    if (!olat || !o_absorb || !y) return fail(DSA_ERR_INVALID_ARG, "dsa_latent_project: NULL tensor");
+    if ((((uintptr_t)olat) | ((uintptr_t)o_absorb) | ((uintptr_t)workspace)) & 15)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_latent_project: tensors must be 16-byte aligned");
+    return project_launch(olat, true, rows, heads * kv_lora_rank, o_absorb, hidden, y, status,
+                          workspace, workspace_bytes, (cudaStream_t)stream);
+}

@@ -38,6 +38,7 @@ struct ScoreArgs {
     int kpool;
     int p_stride;
     int tiles_per_warp;
+    int flags_tma;  // pool flags arrive with the keys (alignment allows 16-byte copies)
     float scale;
 };
 
@@ -167,6 +168,256 @@ __global__ void __launch_bounds__(kWarps * 32) score_kernel(ScoreArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// TMA-fed variant: one producer warp streams runs of 64 pooled keys (16 KiB at
+// ihd 128) per stage with bulk async copies into an 8-stage shared-memory ring;
+// four consumer warps each turn one 16-pool tile of the stage into MMAs and the
+// head reduction. Work units are (row, 64-pool stage) pairs split evenly over one
+// CTA per SM. Pool flags are read by the consumers while the keys are in flight.
+
+constexpr int kStagePools = 64;
+constexpr int kStages = 4;
+constexpr int kCtasPerSm = 3;  // 12 consumer warps per SM hide the MMA and shuffle latency
+constexpr int kTmaThreads = 5 * 32;
+
+struct RowInfo {
+    int seq;
+    int nvis;
+};
+
+__device__ __forceinline__ RowInfo row_info(const ScoreArgs& a, int r) {
+    RowInfo ri;
+    ri.seq = a.row_seq ? __ldg(a.row_seq + r) : r;
+    ri.nvis = 0;
+    if (ri.seq >= 0 && ri.seq < a.pg.batch) {
+        const int L = min(__ldg(a.pg.seq_lens + ri.seq), seq_capacity(a.pg));
+        const int ctx = a.row_ctx ? min(__ldg(a.row_ctx + r), L) : L;
+        ri.nvis = ctx > a.first_key ? (ctx - a.first_key) / a.kpool : 0;
+    } else {
+        ri.seq = -1;
+    }
+    return ri;
+}
+
+template <int IHD, int NT>
+__global__ void __launch_bounds__(kTmaThreads, kCtasPerSm) score_tma_kernel(ScoreArgs a) {
+    constexpr int NV = IHD / 32;
+    constexpr int ROWB = IHD * 2;                    // bytes per pooled key
+    constexpr int STAGE = kStagePools * ROWB;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t* flags = smem + kStages * STAGE;                                  // [stage][64]
+    unsigned long long* bad = reinterpret_cast<unsigned long long*>(flags + kStages * kStagePools);
+    uint64_t* full = reinterpret_cast<uint64_t*>(bad + kStages);
+    uint64_t* empty = full + kStages;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int spr = (a.p_stride + kStagePools - 1) / kStagePools;  // stages per row
+    const long long U = (long long)a.rows * spr;
+    const long long G = gridDim.x;
+    const long long u0 = blockIdx.x * U / G, u1 = (blockIdx.x + 1) * U / G;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 4);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == 4) {
+        // ---------------- producer
+        if (lane == 0) {
+            int cur_r = -1;
+            RowInfo ri{};
+            long long i = 0;
+            bool ok = true;
+            int r = (int)(u0 / spr), st = (int)(u0 % spr);
+            for (long long u = u0; u < u1; ++u, ++i) {
+                const int s = (int)(i % kStages);
+                const uint32_t ph = (uint32_t)((i / kStages) & 1);
+                if (!mbar_wait(&empty[s], ph ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                if (st == spr) {
+                    st = 0;
+                    ++r;
+                }
+                const int p0 = st++ * kStagePools;
+                if (r != cur_r) {
+                    ri = row_info(a, r);
+                    if (ri.seq < 0 && u == u0) flag_status(a.status, DSA_STATUS_BAD_TOKEN);
+                    cur_r = r;
+                }
+                const int nvalid = ri.seq < 0 ? 0 : max(0, min(kStagePools, ri.nvis - p0));
+                const uint32_t dst = smem_u32(smem + s * STAGE);
+                const uint32_t fdst = smem_u32(flags + s * kStagePools);
+                if (a.pg.block_table == nullptr) {
+                    const long long prow0 = (long long)ri.seq * (a.pg.max_seq_len / a.kpool) + p0;
+                    const uint32_t kbytes = (uint32_t)(nvalid * ROWB);
+                    const uint32_t fbytes = a.flags_tma ? (uint32_t)((nvalid + 15) & ~15) : 0u;
+                    bad[s] = 0ull;
+                    mbar_arrive_expect_tx(&full[s], kbytes + fbytes);
+                    if (kbytes) bulk_g2s(dst, a.kp + prow0 * IHD, kbytes, &full[s]);
+                    if (fbytes) bulk_g2s(fdst, a.pv + prow0, fbytes, &full[s]);
+                } else {
+                    // Pools of one block are contiguous: one copy per block run.
+                    const int ppb = a.pg.block_size / a.kpool;
+                    uint32_t bytes = 0;
+                    unsigned long long badm = 0ull;
+                    for (int p = p0; p < p0 + nvalid;) {
+                        const int run = min(ppb - p % ppb, p0 + nvalid - p);
+                        const long long row = pool_row(a.pg, ri.seq, p, a.kpool);
+                        if (row >= 0) {
+                            bytes += (uint32_t)(run * ROWB);
+                            if (a.flags_tma) bytes += (uint32_t)((run + 15) & ~15);
+                        } else {
+                            badm |= ((run >= 64) ? ~0ull : ((1ull << run) - 1ull)) << (p - p0);
+                            flag_status(a.status, DSA_STATUS_BAD_BLOCK);
+                        }
+                        p += run;
+                    }
+                    bad[s] = badm;
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                    for (int p = p0; p < p0 + nvalid;) {
+                        const int run = min(ppb - p % ppb, p0 + nvalid - p);
+                        const long long row = pool_row(a.pg, ri.seq, p, a.kpool);
+                        if (row >= 0) {
+                            bulk_g2s(dst + (p - p0) * ROWB, a.kp + row * IHD, (uint32_t)(run * ROWB),
+                                     &full[s]);
+                            if (a.flags_tma)
+                                bulk_g2s(fdst + (p - p0), a.pv + row, (uint32_t)((run + 15) & ~15),
+                                         &full[s]);
+                        }
+                        p += run;
+                    }
+                }
+            }
+            if (!ok) flag_status(a.status, DSA_STATUS_TIMEOUT);
+            const long long first = i > kStages ? i - kStages : 0;
+            for (long long j = first; j < i; ++j)
+                if (!mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1))) break;
+        }
+        return;
+    }
+
+    // ---------------- consumers: warp w takes pools p0 + 16w .. +15 of each stage
+    const int g = lane >> 2, q = lane & 3;
+    uint32_t bq[NT][NV][4];
+    float wv[NT][2];
+    int cur_r = -1;
+    RowInfo ri{};
+    long long i = 0;
+    int r = (int)(u0 / spr), st = (int)(u0 % spr);
+    for (long long u = u0; u < u1; ++u, ++i) {
+        const int s = (int)(i % kStages);
+        const uint32_t ph = (uint32_t)((i / kStages) & 1);
+        if (st == spr) {
+            st = 0;
+            ++r;
+        }
+        const int p0 = st++ * kStagePools + 16 * warp;
+        if (r != cur_r) {
+            ri = row_info(a, r);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int h = nt * 8 + g;
+                const uint16_t* qp = a.qidx + ((long long)r * a.heads + h) * IHD + 8 * q;
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    uint4 x = make_uint4(0, 0, 0, 0);
+                    if (h < a.heads) x = ldg16(qp + 32 * v);
+                    bq[nt][v][0] = x.x;
+                    bq[nt][v][1] = x.y;
+                    bq[nt][v][2] = x.z;
+                    bq[nt][v][3] = x.w;
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int hh = nt * 8 + 2 * q + j;
+                    wv[nt][j] = hh < a.heads ? __ldg(a.w + (long long)r * a.heads + hh) : 0.f;
+                }
+            }
+            cur_r = r;
+        }
+        const int pA = p0 + g, pB = pA + 8;
+        bool cA = false, cB = false;
+        if (!a.flags_tma && ri.seq >= 0) {  // flags not copied with the keys: load them
+            if (pA < ri.nvis) {
+                const long long rw = pool_row(a.pg, ri.seq, pA, a.kpool);
+                cA = rw >= 0 && __ldg(a.pv + rw) != 0;
+            }
+            if (pB < ri.nvis) {
+                const long long rw = pool_row(a.pg, ri.seq, pB, a.kpool);
+                cB = rw >= 0 && __ldg(a.pv + rw) != 0;
+            }
+        }
+        if (!mbar_wait(&full[s], ph)) {
+            if (lane == 0) flag_status(a.status, DSA_STATUS_TIMEOUT);
+            break;
+        }
+        if (a.flags_tma && ri.seq >= 0) {
+            const uint8_t* fl = flags + s * kStagePools + 16 * warp;
+            const unsigned long long bm = bad[s] >> (16 * warp);
+            cA = pA < ri.nvis && !((bm >> g) & 1ull) && fl[g] != 0;
+            cB = pB < ri.nvis && !((bm >> (g + 8)) & 1ull) && fl[g + 8] != 0;
+        }
+        float sA = 0.f, sB = 0.f;
+        if (p0 < ri.nvis) {  // warp-uniform: the tile has visible pools
+            const uint32_t base = smem_u32(smem + s * STAGE) + (16 * warp) * ROWB;
+            float acc[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const uint4 ra = lds16(base + g * ROWB + 64 * v + 16 * q);
+                const uint4 rb = lds16(base + (g + 8) * ROWB + 64 * v + 16 * q);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_16816(acc[nt], ra.x, rb.x, ra.y, rb.y, bq[nt][v][0], bq[nt][v][1]);
+                    mma_16816(acc[nt], ra.z, rb.z, ra.w, rb.w, bq[nt][v][2], bq[nt][v][3]);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                sA += wv[nt][0] * fmaxf(a.scale * acc[nt][0], 0.f) +
+                      wv[nt][1] * fmaxf(a.scale * acc[nt][1], 0.f);
+                sB += wv[nt][0] * fmaxf(a.scale * acc[nt][2], 0.f) +
+                      wv[nt][1] * fmaxf(a.scale * acc[nt][3], 0.f);
+            }
+            sA += __shfl_xor_sync(0xffffffffu, sA, 1);
+            sB += __shfl_xor_sync(0xffffffffu, sB, 1);
+            sA += __shfl_xor_sync(0xffffffffu, sA, 2);
+            sB += __shfl_xor_sync(0xffffffffu, sB, 2);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        float* srow = a.scores + (long long)r * a.p_stride;
+        if (q == 0 && pA < a.p_stride) srow[pA] = cA ? sA : -INFINITY;
+        if (q == 1 && pB < a.p_stride) srow[pB] = cB ? sB : -INFINITY;
+    }
+}
+
+template <int IHD, int NT>
+int launch_tma(const ScoreArgs& a0, cudaStream_t st) {
+    constexpr int smem = kStages * kStagePools * IHD * 2 + kStages * kStagePools + 3 * kStages * 8;
+    ScoreArgs a = a0;
+    // 16-byte flag copies need 16-byte aligned runs: whole 16-pool groups per row.
+    const bool al = (reinterpret_cast<uintptr_t>(a.pv) & 15u) == 0u;
+    a.flags_tma = al && (a.pg.block_table == nullptr
+                             ? (a.pg.max_seq_len / a.kpool) % 16 == 0
+                             : (a.pg.block_size / a.kpool) % 16 == 0);
+    int rc = set_max_smem((const void*)score_tma_kernel<IHD, NT>, smem);
+    if (rc) return rc;
+    const int spr = (a.p_stride + kStagePools - 1) / kStagePools;
+    const long long U = (long long)a.rows * spr;
+    const long long slots = (long long)sm_count() * kCtasPerSm;
+    const int G = (int)(U < slots ? U : slots);
+    score_tma_kernel<IHD, NT><<<G, kTmaThreads, smem, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_score launch");
+    return DSA_OK;
+}
+
 template <int IHD, int NT>
 int launch(const ScoreArgs& a0, cudaStream_t st) {
     ScoreArgs a = a0;
@@ -189,11 +440,12 @@ int launch(const ScoreArgs& a0, cudaStream_t st) {
 template <int IHD>
 int dispatch_heads(const ScoreArgs& a, cudaStream_t st) {
     const int nt = (a.heads + 7) / 8;
+    // Paged caches need whole 16-byte runs per block (always true for kpool | block).
     switch (nt) {
-        case 1: return launch<IHD, 1>(a, st);
-        case 2: return launch<IHD, 2>(a, st);
+        case 1: return launch_tma<IHD, 1>(a, st);
+        case 2: return launch_tma<IHD, 2>(a, st);
         case 3:
-        case 4: return launch<IHD, 4>(a, st);
+        case 4: return launch_tma<IHD, 4>(a, st);
         default: return launch<IHD, 8>(a, st);
     }
 }

@@ -6,16 +6,20 @@
 // Order: score descending, ties to the lower pool id; -0.0 == +0.0; -inf is never
 // chosen. The chosen ids are written in ascending order and padded with -1.
 //
-// Each row is split over a thread-block cluster of C CTAs (C in {1,2,4,8}); each CTA
-// keeps its slice of the row in shared memory as order-preserving u32 keys (0 for
-// -inf). An exact radix select finds the k'-th largest key T in four 8-bit passes:
-// every pass builds per-CTA histograms of the next digit among keys that match the
-// prefix found so far (warp-aggregated with match.any), merges them across the
-// cluster through distributed shared memory, and picks the digit where the running
-// count from the top reaches the remaining rank. Then every key > T is selected,
-// plus the first (in pool order) keys == T needed to reach k'. Positions come from
-// a cluster prefix over the CTAs' counts and warp-ballot prefixes inside each
-// CTA, so ids are written already in ascending order with no sort.
+// A row is split over a thread-block cluster of C CTAs (C in {1,2,4,8}, chosen so
+// that rows x C covers the GPU). Scores become order-preserving u32 keys (0 for
+// -inf) in shared memory. Each CTA finds the exact threshold of its slice's top-k:
+// the key range [kmin, kmax] gives a monotone 4096-bin index (kmax - key) >> shift; a
+// histogram locates the bin holding the k-th key; only that bin's keys are
+// collected, and a radix select over the bits that vary inside it (per-warp
+// shared-memory histograms) resolves the exact key and how many equal keys to take.
+// A ballot-prefix pass then emits the chosen positions in ascending order.
+//
+// With C > 1 every CTA pushes its chosen (key, id) pairs through distributed shared
+// memory into its own slot of CTA 0's merge area (unused slot entries get key 0),
+// one cluster barrier publishes them, and CTA 0 selects the row's top-k among the
+// C x k candidates the same way: the row's top-k is contained in the union of the
+// slices' top-k, and slot order keeps the ids ascending.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -27,8 +31,10 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxChunk = 49152;  // keys per CTA (192 KiB of shared memory)
+constexpr int kMaxChunk = 40960;      // keys per CTA slice
 constexpr int kMaxCluster = 8;
+constexpr int kMaxSmem = 200 * 1024;  // dynamic shared memory per CTA
+constexpr int kBins = 4096;
 
 struct SelectArgs {
     const float* scores;
@@ -37,6 +43,9 @@ struct SelectArgs {
     int p_stride;
     int sk;
     int chunk;
+    int merge_off;  // byte offsets in dynamic shared memory: merge keys, then ids
+    int tbuf_off;   // the threshold bin's scratch list
+    int tcap;       // its capacity (keys)
 };
 
 __device__ __forceinline__ uint32_t score_key(float f) {
@@ -46,48 +55,89 @@ __device__ __forceinline__ uint32_t score_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
-    cg::cluster_group cluster = cg::this_cluster();
-    const int C = (int)cluster.num_blocks();
-    const int crank = (int)cluster.block_rank();
-    const int r = blockIdx.x / C;
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
+struct BlockScratch {
+    uint32_t hist[kBins];  // 4096-bin histogram, or 16 per-warp 256-bin histograms
+    uint32_t tot[256];
+    int pick[4];
+    int wgt[kWarps], weq[kWarps], weqb[kWarps], wselb[kWarps];
+    uint32_t wmax[kWarps], wmin[kWarps];
+    int wcnt[kWarps];
+    int tcount;
+};
 
-    extern __shared__ uint32_t keys[];
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t tot[256];
-    __shared__ int s_gt[kWarps], s_eq[kWarps], s_eqb[kWarps], s_selb[kWarps];
-    __shared__ int s_cta[2];
-    __shared__ int s_pick[3];
+// Chosen keys: every key > T plus the first need_eq keys == T in position order;
+// kk keys in all.
+struct Thr {
+    uint32_t T;
+    int need_eq;
+    int kk;
+};
 
-    const int begin = crank * a.chunk;
-    const int n = max(0, min(a.chunk, a.p_stride - begin));
-    const int n32 = (n + 31) & ~31;
-    const float* srow = a.scores + (long long)r * a.p_stride + begin;
-    for (int i = threadIdx.x; i < n; i += kThreads) keys[i] = score_key(__ldg(srow + i));
+struct MinMax {
+    uint32_t kmin, kmax;
+    int count;
+};
 
-    uint32_t prefix = 0u, pmask = 0u;
-    int krem = 0, kk = 0;
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        if (threadIdx.x < 256) hist[threadIdx.x] = 0u;
+// Combine per-thread (min, max, count) of nonzero keys over the block.
+__device__ MinMax block_minmax(uint32_t mn, uint32_t mx, int cnt, BlockScratch& sc) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+    }
+    if (lane == 0) {
+        sc.wmax[warp] = mx;
+        sc.wmin[warp] = mn;
+        sc.wcnt[warp] = cnt;
+    }
+    __syncthreads();
+    MinMax r{0xffffffffu, 0u, 0};
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        r.kmax = max(r.kmax, sc.wmax[w]);
+        r.kmin = min(r.kmin, sc.wmin[w]);
+        r.count += sc.wcnt[w];
+    }
+    __syncthreads();  // w* arrays are reused by the caller
+    return r;
+}
+
+// Exact k-th largest key of the nonzero keys in keys[0..n), whose min, max and
+// count are mm. Radix passes of 8 bits over v = key - kmin, only over the bits
+// v can have. With allow_all, k >= count means "take every nonzero key".
+__device__ Thr radix_threshold(const uint32_t* keys, int n, int k, const MinMax& mm,
+                               BlockScratch& sc, bool allow_all) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (mm.count == 0) return Thr{0xffffffffu, 0, 0};
+    const int kk = min(k, mm.count);
+    if (allow_all && mm.count <= k) return Thr{1u, 0, kk};
+    if (mm.kmin == mm.kmax) return Thr{mm.kmax, kk, kk};
+    const uint32_t range = mm.kmax - mm.kmin;
+    const int bits = 32 - __clz(range);
+    const int passes = (bits + 7) >> 3;
+    uint32_t prefix = 0u;  // over v, bits above the current digit
+    int krem = kk;
+    for (int p = passes - 1; p >= 0; --p) {
+        const int shift = 8 * p;
+        const uint32_t hmask = (shift + 8 >= 32) ? 0u : ~((1u << (shift + 8)) - 1u);
+        for (int b = threadIdx.x; b < kBins; b += kThreads) sc.hist[b] = 0u;
         __syncthreads();
-        for (int i = threadIdx.x; i < n32; i += kThreads) {
-            const uint32_t k = i < n ? keys[i] : 0u;
-            const bool take = k != 0u && (k & pmask) == prefix;
-            const unsigned act = __ballot_sync(0xffffffffu, take);
-            if (take) {
-                const uint32_t bin = (k >> shift) & 255u;
-                const unsigned peers = __match_any_sync(act, bin);
-                if ((__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+        uint32_t* wh = sc.hist + warp * 256;
+        for (int i = threadIdx.x; i < n; i += kThreads) {
+            const uint32_t key = keys[i];
+            if (key) {
+                const uint32_t v = key - mm.kmin;
+                if ((v & hmask) == prefix) atomicAdd(&wh[(v >> shift) & 255u], 1u);
             }
         }
-        cluster.sync();
+        __syncthreads();
         if (threadIdx.x < 256) {
-            uint32_t s = 0u;
-            for (int c = 0; c < C; ++c) s += cluster.map_shared_rank(hist, c)[threadIdx.x];
-            tot[threadIdx.x] = s;
+            uint32_t t = 0u;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) t += sc.hist[w * 256 + threadIdx.x];
+            sc.tot[threadIdx.x] = t;
         }
         __syncthreads();
         if (warp == 0) {
@@ -96,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
             uint32_t local = 0u;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                cnt[j] = tot[8 * (31 - lane) + 7 - j];
+                cnt[j] = sc.tot[8 * (31 - lane) + 7 - j];
                 local += cnt[j];
             }
             uint32_t incl = local;
@@ -106,19 +156,13 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
                 if (lane >= off) incl += v;
             }
             const uint32_t excl = incl - local;
-            int want = krem;
-            if (pass == 0) {
-                const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
-                want = min(a.sk, (int)total);
-                if (lane == 0) s_pick[2] = want;
-            }
-            if (want > 0 && excl < (uint32_t)want && (uint32_t)want <= incl) {
+            if (excl < (uint32_t)krem && (uint32_t)krem <= incl) {
                 uint32_t above = excl;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    if (above + cnt[j] >= (uint32_t)want) {
-                        s_pick[0] = 8 * (31 - lane) + 7 - j;
-                        s_pick[1] = (int)above;
+                    if (above + cnt[j] >= (uint32_t)krem) {
+                        sc.pick[0] = 8 * (31 - lane) + 7 - j;
+                        sc.pick[1] = (int)above;
                         break;
                     }
                     above += cnt[j];
@@ -126,77 +170,245 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
             }
         }
         __syncthreads();
-        if (pass == 0) {
-            kk = s_pick[2];
-            krem = kk;
-        }
-        if (kk == 0) break;  // uniform across the cluster: same merged counts everywhere
-        krem -= s_pick[1];
-        prefix |= (uint32_t)s_pick[0] << shift;
-        pmask |= 255u << shift;
-        cluster.sync();  // all remote reads of hist done before it is cleared
+        krem -= sc.pick[1];
+        prefix |= (uint32_t)sc.pick[0] << shift;
+        __syncthreads();  // pick[] and hist are rewritten by the next pass
     }
+    return Thr{prefix + mm.kmin, krem, kk};
+}
+
+// Exact threshold of the top-k of keys[0..n) (see the file comment).
+__device__ Thr bin_threshold(const uint32_t* keys, int n, int k, BlockScratch& sc,
+                             uint32_t* tbuf, int tcap) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t mx = 0u, mn = 0xffffffffu;
+    int cnt = 0;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint32_t key = keys[i];
+        if (key) {
+            mx = max(mx, key);
+            mn = min(mn, key);
+            ++cnt;
+        }
+    }
+    const MinMax mm = block_minmax(mn, mx, cnt, sc);
+    if (mm.count == 0) return Thr{0xffffffffu, 0, 0};
+    const int kk = min(k, mm.count);
+    if (mm.count <= k) return Thr{1u, 0, kk};          // every nonzero key is chosen
+    if (mm.kmax == mm.kmin) return Thr{mm.kmax, kk, kk};  // all equal: lowest positions
+    const uint32_t range = mm.kmax - mm.kmin;
+    const int bits = 32 - __clz(range);
+    const int shift = bits > 12 ? bits - 12 : 0;
+
+    for (int b = threadIdx.x; b < kBins; b += kThreads) sc.hist[b] = 0u;
+    if (threadIdx.x == 0) sc.tcount = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint32_t key = keys[i];
+        if (key) atomicAdd(&sc.hist[(mm.kmax - key) >> shift], 1u);
+    }
+    __syncthreads();
+    // Thread t owns bins 8t .. 8t+7 (bin 0 holds the largest keys).
+    constexpr int BPT = kBins / kThreads;
+    uint32_t c[BPT];
+    uint32_t local = 0u;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+        c[j] = sc.hist[BPT * threadIdx.x + j];
+        local += c[j];
+    }
+    uint32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) sc.wcnt[warp] = (int)incl;
+    __syncthreads();
+    uint32_t wbase = 0u;
+    for (int w = 0; w < warp; ++w) wbase += (uint32_t)sc.wcnt[w];
+    const uint32_t excl = wbase + incl - local;
+    if (excl < (uint32_t)kk && (uint32_t)kk <= excl + local) {
+        uint32_t before = excl;
+#pragma unroll
+        for (int j = 0; j < BPT; ++j) {
+            if (before + c[j] >= (uint32_t)kk) {
+                sc.pick[0] = BPT * threadIdx.x + j;
+                sc.pick[1] = (int)before;
+                break;
+            }
+            before += c[j];
+        }
+    }
+    __syncthreads();
+    const uint32_t bstar = (uint32_t)sc.pick[0];
+    const int before = sc.pick[1];
+    const int nb = (int)sc.hist[bstar];
+    const int need = kk - before;  // 1 <= need <= nb
+    __syncthreads();                // pick[] and wcnt[] are reused below
+    if (nb > tcap) return radix_threshold(keys, n, k, mm, sc, true);
+    uint32_t bmx = 0u, bmn = 0xffffffffu;
+    const int n32 = (n + 31) & ~31;
+    for (int i = threadIdx.x; i < n32; i += kThreads) {
+        const uint32_t key = i < n ? keys[i] : 0u;
+        const bool in = key != 0u && ((mm.kmax - key) >> shift) == bstar;
+        const unsigned m = __ballot_sync(0xffffffffu, in);
+        if (m) {
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&sc.tcount, __popc(m));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (in) {
+                tbuf[base + __popc(m & ((1u << lane) - 1u))] = key;
+                bmx = max(bmx, key);
+                bmn = min(bmn, key);
+            }
+        }
+    }
+    const MinMax bm = block_minmax(bmn, bmx, 0, sc);  // syncs: tbuf complete after it
+    const Thr t = radix_threshold(tbuf, nb, need, MinMax{bm.kmin, bm.kmax, nb}, sc, false);
+    return Thr{t.T, t.need_eq, kk};
+}
+
+// emit(rank, position) for every chosen position, ranks ascending with position.
+template <class Emit>
+__device__ void ordered_emit(const uint32_t* keys, int n, const Thr& t, BlockScratch& sc,
+                             Emit emit) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t T = t.T;
+    const int need_eq = t.need_eq;
+    const int seg = (((n + kWarps - 1) / kWarps) + 31) & ~31;
+    const int w0 = warp * seg;
+    const int w1 = min(n, w0 + seg);
+    int gt = 0, eq = 0;
+    for (int i = w0 + lane; i < w0 + seg; i += 32) {
+        const uint32_t key = i < w1 ? keys[i] : 0u;
+        gt += __popc(__ballot_sync(0xffffffffu, key > T));
+        eq += __popc(__ballot_sync(0xffffffffu, key == T));
+    }
+    if (lane == 0) {
+        sc.wgt[warp] = gt;
+        sc.weq[warp] = eq;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int eqb = 0, selb = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            sc.weqb[w] = eqb;
+            sc.wselb[w] = selb;
+            selb += sc.wgt[w] + max(0, min(need_eq - eqb, sc.weq[w]));
+            eqb += sc.weq[w];
+        }
+    }
+    __syncthreads();
+    int eqr = sc.weqb[warp], pos = sc.wselb[warp];
+    const unsigned lt = (1u << lane) - 1u;
+    for (int i = w0 + lane; i < w0 + seg; i += 32) {
+        const uint32_t key = i < w1 ? keys[i] : 0u;
+        const unsigned beq = __ballot_sync(0xffffffffu, key == T);
+        const bool sel = key > T || (key == T && eqr + __popc(beq & lt) < need_eq);
+        const unsigned bsel = __ballot_sync(0xffffffffu, sel);
+        const int at = pos + __popc(bsel & lt);
+        if (sel && at < t.kk) emit(at, i);
+        eqr += __popc(beq);
+        pos += __popc(bsel);
+    }
+    __syncthreads();
+}
+
+// Exact top-k of keys[0..n) (key desc, position asc; key 0 never chosen): emits
+// the chosen positions ascending and returns how many, min(k, #nonzero keys).
+template <class Emit>
+__device__ int block_topk(const uint32_t* keys, int n, int k, BlockScratch& sc, uint32_t* tbuf,
+                          int tcap, Emit emit) {
+    const Thr t = bin_threshold(keys, n, k, sc, tbuf, tcap);
+    if (t.kk == 0) return 0;
+    ordered_emit(keys, n, t, sc, emit);
+    return t.kk;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int crank = (int)cluster.block_rank();
+    const int r = blockIdx.x / C;
+
+    extern __shared__ __align__(16) uint32_t keys[];
+    __shared__ BlockScratch sc;
+    uint8_t* dyn = reinterpret_cast<uint8_t*>(keys);
+    uint32_t* tbuf = reinterpret_cast<uint32_t*>(dyn + a.tbuf_off);
+
+    const int begin = crank * a.chunk;
+    const int n = max(0, min(a.chunk, a.p_stride - begin));
+    const float* srow = a.scores + (long long)r * a.p_stride + begin;
+    if ((reinterpret_cast<uintptr_t>(srow) & 15u) == 0u) {
+        // 16-byte loads, eight per thread in flight before any is converted.
+        const float4* s4 = reinterpret_cast<const float4*>(srow);
+        const int nv = n >> 2;
+        for (int base = 0; base < nv; base += 8 * kThreads) {
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = base + j * kThreads + threadIdx.x;
+                v[j] = i < nv ? __ldg(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = base + j * kThreads + threadIdx.x;
+                if (i < nv) {
+                    keys[4 * i] = score_key(v[j].x);
+                    keys[4 * i + 1] = score_key(v[j].y);
+                    keys[4 * i + 2] = score_key(v[j].z);
+                    keys[4 * i + 3] = score_key(v[j].w);
+                }
+            }
+        }
+        for (int i = (nv << 2) + threadIdx.x; i < n; i += kThreads) keys[i] = score_key(__ldg(srow + i));
+    } else {
+        for (int i = threadIdx.x; i < n; i += kThreads) keys[i] = score_key(__ldg(srow + i));
+    }
+    __syncthreads();
 
     int32_t* out = a.pool_ids + (long long)r * a.sk;
-    if (kk > 0) {
-        const uint32_t T = prefix;
-        const int need_eq = krem;  // keys equal to T still to take, lowest ids first
-        const int seg = (((n + kWarps - 1) / kWarps) + 31) & ~31;
-        const int w0 = warp * seg;
-        const int w1 = min(n, w0 + seg);
-        int gt = 0, eq = 0;
-        for (int i = w0 + lane; i < w0 + seg; i += 32) {
-            const uint32_t k = i < w1 ? keys[i] : 0u;
-            gt += __popc(__ballot_sync(0xffffffffu, k > T));
-            eq += __popc(__ballot_sync(0xffffffffu, k == T));
-        }
-        if (lane == 0) {
-            s_gt[warp] = gt;
-            s_eq[warp] = eq;
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int cg_ = 0, ce = 0;
-            for (int w = 0; w < kWarps; ++w) {
-                cg_ += s_gt[w];
-                ce += s_eq[w];
-            }
-            s_cta[0] = cg_;
-            s_cta[1] = ce;
-        }
-        cluster.sync();
-        if (threadIdx.x == 0) {
-            int eqb = 0, selb = 0;
-            for (int c = 0; c < crank; ++c) {
-                const int* rc = cluster.map_shared_rank(s_cta, c);
-                const int e = rc[1];
-                selb += rc[0] + max(0, min(need_eq - eqb, e));
-                eqb += e;
-            }
-            for (int w = 0; w < kWarps; ++w) {
-                s_eqb[w] = eqb;
-                s_selb[w] = selb;
-                selb += s_gt[w] + max(0, min(need_eq - eqb, s_eq[w]));
-                eqb += s_eq[w];
-            }
-        }
-        __syncthreads();
-        int eqr = s_eqb[warp], pos = s_selb[warp];
-        const unsigned lt = (1u << lane) - 1u;
-        for (int i = w0 + lane; i < w0 + seg; i += 32) {
-            const uint32_t k = i < w1 ? keys[i] : 0u;
-            const unsigned beq = __ballot_sync(0xffffffffu, k == T);
-            const bool sel = k > T || (k == T && eqr + __popc(beq & lt) < need_eq);
-            const unsigned bsel = __ballot_sync(0xffffffffu, sel);
-            const int at = pos + __popc(bsel & lt);
-            if (sel && at < kk) out[at] = begin + i;
-            eqr += __popc(beq);
-            pos += __popc(bsel);
-        }
-    }
-    if (crank == 0)
+    if (C == 1) {
+        const int kk = block_topk(keys, n, a.sk, sc, tbuf, a.tcap,
+                                  [&](int at, int i) { out[at] = begin + i; });
         for (int j = kk + threadIdx.x; j < a.sk; j += kThreads) out[j] = -1;
-    cluster.sync();  // keep this CTA's shared memory alive for remote readers
+        return;
+    }
+
+    // This slice's top-k, pushed into slot crank of CTA 0's merge area.
+    uint32_t* mkeys0 = cluster.map_shared_rank(reinterpret_cast<uint32_t*>(dyn + a.merge_off), 0);
+    uint32_t* rkeys = mkeys0 + crank * a.sk;
+    uint32_t* rids = mkeys0 + C * a.sk + crank * a.sk;
+    const int kc = block_topk(keys, n, a.sk, sc, tbuf, a.tcap, [&](int at, int i) {
+        rkeys[at] = keys[i];
+        rids[at] = (uint32_t)(begin + i);
+    });
+    for (int j = kc + threadIdx.x; j < a.sk; j += kThreads) rkeys[j] = 0u;
+    cluster.sync();  // publishes the pushed lists; no remote access happens after it
+    if (crank != 0) return;
+
+    const uint32_t* mkeys = reinterpret_cast<const uint32_t*>(dyn + a.merge_off);
+    const uint32_t* mids = mkeys + C * a.sk;
+    const int kk = block_topk(mkeys, C * a.sk, a.sk, sc, tbuf, a.tcap,
+                              [&](int at, int i) { out[at] = (int)mids[i]; });
+    for (int j = kk + threadIdx.x; j < a.sk; j += kThreads) out[j] = -1;
+}
+
+// Dynamic shared memory: the slice's keys (4 B each); with C > 1 the merge area
+// (C x select_k keys and ids, used in CTA 0); the threshold bin's list.
+struct SmemPlan {
+    long long merge_off, tbuf_off, tcap, bytes;
+};
+SmemPlan smem_plan(int p_stride, int sk, int C) {
+    const long long chunk = (p_stride + C - 1) / C;
+    SmemPlan p;
+    p.merge_off = (chunk * 4 + 15) & ~15LL;
+    p.tbuf_off = p.merge_off + (C > 1 ? (long long)C * sk * 8 : 0);
+    const long long room = (kMaxSmem - p.tbuf_off) / 4;
+    p.tcap = room > 2048 ? 2048 : room;
+    p.bytes = p.tbuf_off + 4 * (p.tcap > 0 ? p.tcap : 0);
+    return p;
 }
 
 }  // namespace
@@ -218,14 +430,22 @@ extern "C" int dsa_select(const float* scores, int rows, int p_stride, int index
         return fail(DSA_ERR_UNSUPPORTED, "dsa_select: p_stride %d > %d", p_stride,
                     kMaxChunk * kMaxCluster);
     const int sms = sm_count() > 0 ? sm_count() : 148;
+    auto fits = [&](int C) {
+        const SmemPlan sp = smem_plan(p_stride, sk, C);
+        return (p_stride + C - 1) / C <= kMaxChunk && sp.tcap >= 256 && sp.bytes <= kMaxSmem;
+    };
     int C = 1;
     while (C < kMaxCluster) {
-        const int chunk = (p_stride + C - 1) / C;
-        const bool too_big = chunk > kMaxChunk;
+        const long long chunk = (p_stride + C - 1) / C;
         const bool underfilled = (long long)rows * C < 2LL * sms && chunk > 2048;
-        if (!too_big && !underfilled) break;
+        if (fits(C) && !underfilled) break;
+        if (fits(C) && !fits(2 * C)) break;
         C *= 2;
     }
+    if (!fits(C))
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_select: p_stride %d with select_k %d does not fit",
+                    p_stride, sk);
+    const SmemPlan sp = smem_plan(p_stride, sk, C);
     SelectArgs a;
     a.scores = scores;
     a.pool_ids = pool_ids;
@@ -233,14 +453,16 @@ extern "C" int dsa_select(const float* scores, int rows, int p_stride, int index
     a.p_stride = p_stride;
     a.sk = sk;
     a.chunk = (p_stride + C - 1) / C;
-    const int smem = a.chunk * (int)sizeof(uint32_t);
-    int rc = set_max_smem((const void*)select_kernel, kMaxChunk * (int)sizeof(uint32_t));
+    a.merge_off = (int)sp.merge_off;
+    a.tbuf_off = (int)sp.tbuf_off;
+    a.tcap = (int)sp.tcap;
+    int rc = set_max_smem((const void*)select_kernel, kMaxSmem);
     if (rc) return rc;
     if ((long long)rows * C > 0x7fffffffLL) return fail(DSA_ERR_UNSUPPORTED, "dsa_select: too many rows");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(rows * C));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.dynamicSmemBytes = (size_t)sp.bytes;
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

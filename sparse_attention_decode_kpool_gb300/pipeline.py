@@ -63,13 +63,29 @@ class DsaDecodeLayer:
         self.token_ids = torch.empty((R, g.out_width), dtype=torch.int32, device=dev)
         hidden = g.hidden if self.o_absorb is not None else 0
         self.y = torch.empty((R, hidden), dtype=torch.bfloat16, device=dev) if hidden else None
+        # olat feeds the projection, so it always exists when o_absorb does.
         self.olat = (torch.empty((R, g.heads, g.kv_lora_rank), dtype=torch.float32, device=dev)
-                     if (keep_olat or self.o_absorb is None) else None)
-        ws = api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, hidden,
-                                                 self.o_absorb is not None)
+                     if (keep_olat or self.o_absorb is not None) else None)
+        ws = api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, 0, False)
         self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+        # Two-call form (attention, then dsa_latent_project) where the projection
+        # kernel supports the shape (hidden % 64 == 0); else the one-call form.
+        self.two_call = bool(hidden) and hidden % 64 == 0
+        pws = api.dsa_latent_project_workspace(R, g.heads, hidden) if self.two_call else 0
+        self.proj_workspace = torch.empty(max(pws, 1), dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.graph: Optional[torch.cuda.CUDAGraph] = None
+        self._fused_ws: Optional[torch.Tensor] = None
+
+    def fused_workspace(self) -> torch.Tensor:
+        """Workspace for the one-call form dsa_sparse_mla_decode(..., o_absorb, y)."""
+        if self._fused_ws is None:
+            g, R = self.geom, self.wl.rows
+            hidden = g.hidden if self.o_absorb is not None else 0
+            n = api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, hidden,
+                                                    self.o_absorb is not None)
+            self._fused_ws = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
+        return self._fused_ws
 
     # -- stages ------------------------------------------------------------
     def compress(self, stream=None) -> None:
@@ -93,29 +109,39 @@ class DsaDecodeLayer:
                        stream=stream)
 
     def attend(self, stream=None) -> None:
+        """Sparse latent attention over the selected tokens -> olat (f32); in the
+        one-call form also y."""
+        if self.o_absorb is not None and not self.two_call:
+            api.dsa_sparse_mla_decode(self.qlat, self.row_seq, self.ckv, self.pg, self.token_ids,
+                                      self.geom.softmax_scale, self.o_absorb, self.y, self.olat,
+                                      self.status, self.fused_workspace(), stream=stream)
+            return
         api.dsa_sparse_mla_decode(self.qlat, self.row_seq, self.ckv, self.pg, self.token_ids,
-                                  self.geom.softmax_scale, self.o_absorb, self.y, self.olat,
-                                  self.status, self.workspace, stream=stream)
+                                  self.geom.softmax_scale, None, None, self.olat, self.status,
+                                  self.workspace, stream=stream)
+
+    def project(self, stream=None) -> None:
+        """y = o_absorb . olat (the absorbed output projection)."""
+        if self.o_absorb is not None and self.two_call:
+            api.dsa_latent_project(self.olat, self.o_absorb, self.y, self.status,
+                                   self.proj_workspace, stream=stream)
 
     def step(self, stream=None) -> None:
-        """One decode step over the whole batch: score, select, expand, attend."""
+        """One decode step over the whole batch: score, select, expand, attend, project."""
         self.score(stream)
         self.select(stream)
         self.expand(stream)
         self.attend(stream)
+        self.project(stream)
 
-    # Kernel launches one step() makes (score, select, expand, split attention,
-    # [combine], [gemv, ysum]).
     def launches_per_step(self) -> int:
-        from . import api as _a  # noqa: F401
-        n = 4
+        """Library kernel launches one step() makes."""
         R, g = self.wl.rows, self.geom
-        hidden = g.hidden if self.o_absorb is not None else 0
-        ws_split = api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, 0, False)
-        if ws_split > 0:
-            n += 1  # combine
+        n = 4  # score, select, expand, split attention
+        if api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, 0, False) > 0:
+            n += 1  # split combine
         if self.o_absorb is not None:
-            n += 1 + (R + 63) // 64  # gemv launches + ysum
+            n += (R + 63) // 64 + 1  # projection kernel(s) + reduction (either form)
         return n
 
     # -- graphs ------------------------------------------------------------

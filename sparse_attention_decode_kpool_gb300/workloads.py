@@ -386,10 +386,13 @@ def paged_batch(seed: int = 2, **kw) -> Workload:
                          block_size=64, max_seq_len=65536, **kw)
 
 
-def long_262k(seed: int = 3, **kw) -> Workload:
-    """8 sequences at S=262,144, 1 % of token positions invalid (2,621 per sequence)."""
-    return make_workload("decode-S262144-b8", seed, Geometry(**GLM53), [262144] * 8,
-                         invalid_per_seq=2621, **kw)
+def long_262k(seed: int = 3, seq_len: Optional[int] = None, **kw) -> Workload:
+    """8 sequences at S=262,144, 1 % of token positions invalid (2,621 per sequence).
+    ``seq_len`` shrinks the sequences (same rows, heads and top-k) for profiling."""
+    S = seq_len or 262144
+    name = "decode-S262144-b8" if seq_len is None else f"decode-S{S}-b8"
+    return make_workload(name, seed, Geometry(**GLM53), [S] * 8,
+                         invalid_per_seq=(S * 2621 + 131072) // 262144, **kw)
 
 
 def prefill_chunk(seed: int = 4, **kw) -> Workload:

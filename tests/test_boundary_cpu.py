@@ -96,7 +96,7 @@ def test_score_select_expand_argument_errors(lib):
     assert lib.dsa_score(FAKE, FAKE, 0, 32, 128, None, None, FAKE, FAKE, ctypes.byref(pg), 0, 4,
                          0.1, FAKE, 16, None, None) == DSA_OK  # nothing to do
     assert lib.dsa_select(FAKE, 1, 100, 0, 4, FAKE, None) == DSA_ERR_CONFIG
-    assert lib.dsa_select(FAKE, 1, 393217, 2048, 4, FAKE, None) == DSA_ERR_UNSUPPORTED
+    assert lib.dsa_select(FAKE, 1, 327681, 2048, 4, FAKE, None) == DSA_ERR_UNSUPPORTED
     assert lib.dsa_select(FAKE, 0, 100, 2048, 4, FAKE, None) == DSA_OK
     assert lib.dsa_select(None, 1, 100, 2048, 4, FAKE, None) == DSA_ERR_INVALID_ARG
     assert lib.dsa_expand(FAKE, 2, 64, 0, 4, 255, FAKE, None) == DSA_ERR_INVALID_ARG

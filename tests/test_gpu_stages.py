@@ -153,7 +153,7 @@ SELECT_CASES = [
     (1, 8192, 2048, 4, "positive"), (8, 65536, 2048, 4, "positive"), (2, 65536, 2048, 4, "ties"),
     (3, 100003, 2048, 4, "normal"), (2, 3000, 2048, 4, "sparse"), (2, 700, 256, 4, "allinf"),
     (5, 16384, 2048, 4, "positive"), (64, 16384, 2048, 4, "normal"), (300, 2048, 512, 4, "ties"),
-    (1, 393216, 2048, 4, "positive"), (2, 40000, 64, 1, "ties"),
+    (1, 327680, 2048, 4, "positive"), (2, 40000, 64, 1, "ties"),
 ]
 
 
@@ -204,6 +204,7 @@ MLA_CASES = [
     ("h16-olat-only", 16, 0, [1500, 1500], None, 700, False),
     ("h96-two-groups", 96, 64, [800], None, 200, True),
     ("h64-b70-rows", 64, 64, [300] * 70, None, 64, True),
+    ("h8-hidden96-fallback", 8, 96, [600, 333], None, 128, True),
 ]
 
 
@@ -233,7 +234,7 @@ def test_mla_parity(case):
     y = H.Guarded((wl.rows, g.hidden), torch.bfloat16, 3.0) if with_o else None
     api.dsa_sparse_mla_decode(layer.qlat, layer.row_seq, layer.ckv, layer.pg, tok,
                               g.softmax_scale, layer.o_absorb, None if y is None else y.t,
-                              olat.t, layer.status, layer.workspace)
+                              olat.t, layer.status, layer.fused_workspace())
     torch.cuda.synchronize()
     olat.check()
     if y is not None:
@@ -268,7 +269,7 @@ def test_mla_bad_ids_set_status_and_are_skipped():
     layer.status.zero_()
     api.dsa_sparse_mla_decode(layer.qlat, layer.row_seq, layer.ckv, layer.pg,
                               torch.from_numpy(bad).cuda(), g.softmax_scale, layer.o_absorb,
-                              layer.y, layer.olat, layer.status, layer.workspace)
+                              layer.y, layer.olat, layer.status, layer.fused_workspace())
     torch.cuda.synchronize()
     assert int(layer.status.item()) & api._lib.DSA_STATUS_BAD_TOKEN
     got = layer.olat.cpu().numpy().reshape(wl.rows, -1)
@@ -294,9 +295,31 @@ def test_bad_block_table_entry_sets_status():
     ids[1, :10] = torch.arange(128, 138)  # tokens in block 2 of sequence 1
     api.dsa_sparse_mla_decode(layer.qlat, layer.row_seq, layer.ckv, pg, ids.cuda(),
                               g.softmax_scale, layer.o_absorb, layer.y, layer.olat, layer.status,
-                              layer.workspace)
+                              layer.fused_workspace())
     torch.cuda.synchronize()
     assert int(layer.status.item()) & api._lib.DSA_STATUS_BAD_BLOCK
     s = layer.scores.cpu().numpy()
     assert np.isneginf(s[1, 32:48]).all()  # pools of the bad block are not candidates
     assert (layer.olat[1].abs().sum().item() == 0.0)  # all of row 1's tokens skipped
+
+
+PROJECT_CASES = [(8, 64, 4096), (1, 64, 4096), (3, 4, 1024), (70, 16, 256), (20, 8, 128)]
+
+
+@pytest.mark.parametrize("rows,heads,hidden", PROJECT_CASES)
+def test_latent_project_parity(rows, heads, hidden):
+    rng = np.random.default_rng(rows * 100 + heads)
+    olat = torch.from_numpy(rng.standard_normal((rows, heads, 512)).astype(np.float32))
+    A = torch.from_numpy((rng.standard_normal((hidden, heads * 512)) * 0.02).astype(np.float32)
+                         ).to(torch.bfloat16)
+    ws = torch.empty(max(1, api.dsa_latent_project_workspace(rows, heads, hidden)),
+                     dtype=torch.uint8, device="cuda")
+    y = H.Guarded((rows, hidden), torch.bfloat16, 5.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.dsa_latent_project(olat.cuda(), A.cuda(), y.t, status, ws)
+    torch.cuda.synchronize()
+    y.check()
+    assert int(status.item()) == 0
+    ref = np.array([O.latent_project(olat[r].numpy().astype(np.float64), H.f(A))[0]
+                    for r in range(rows)])
+    H.check_attention(y.t.float().cpu().numpy(), ref, "y")

@@ -40,7 +40,7 @@ def _problem(seed, rows, heads, lens, ow, block_size=None):
 def _with_workspace(wl, layer):
     api.dsa_sparse_mla_decode(layer.qlat, layer.row_seq, layer.ckv, layer.pg, layer.token_ids,
                               wl.geom.softmax_scale, layer.o_absorb, layer.y, layer.olat,
-                              layer.status, layer.workspace)
+                              layer.status, layer.fused_workspace())
     torch.cuda.synchronize()
     return layer.y.float().cpu().numpy(), layer.olat.cpu().numpy().reshape(wl.rows, -1)
 
