@@ -35,6 +35,7 @@ constexpr int kMaxChunk = 40960;      // keys per CTA slice
 constexpr int kMaxCluster = 8;
 constexpr int kMaxSmem = 200 * 1024;  // dynamic shared memory per CTA
 constexpr int kBins = 4096;
+constexpr int kRankMax = 128;        // threshold bins up to this size are ranked directly
 
 struct SelectArgs {
     const float* scores;
@@ -59,7 +60,6 @@ struct BlockScratch {
     uint32_t hist[kBins];  // 4096-bin histogram, or 16 per-warp 256-bin histograms
     uint32_t tot[256];
     int pick[4];
-    int wgt[kWarps], weq[kWarps], weqb[kWarps], wselb[kWarps];
     uint32_t wmax[kWarps], wmin[kWarps];
     int wcnt[kWarps];
     int tcount;
@@ -79,7 +79,7 @@ struct MinMax {
 };
 
 // Combine per-thread (min, max, count) of nonzero keys over the block.
-__device__ MinMax block_minmax(uint32_t mn, uint32_t mx, int cnt, BlockScratch& sc) {
+__device__ __noinline__ MinMax block_minmax(uint32_t mn, uint32_t mx, int cnt, BlockScratch& sc) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -107,12 +107,12 @@ __device__ MinMax block_minmax(uint32_t mn, uint32_t mx, int cnt, BlockScratch& 
 // Exact k-th largest key of the nonzero keys in keys[0..n), whose min, max and
 // count are mm. Radix passes of 8 bits over v = key - kmin, only over the bits
 // v can have. With allow_all, k >= count means "take every nonzero key".
-__device__ Thr radix_threshold(const uint32_t* keys, int n, int k, const MinMax& mm,
-                               BlockScratch& sc, bool allow_all) {
+__device__ __noinline__ Thr radix_threshold(const uint32_t* keys, int n, int k, MinMax mm,
+                                            BlockScratch& sc, bool allow_all) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (mm.count == 0) return Thr{0xffffffffu, 0, 0};
     const int kk = min(k, mm.count);
-    if (allow_all && mm.count <= k) return Thr{1u, 0, kk};
+    if (allow_all && mm.count <= k) return Thr{0u, 0, kk};
     if (mm.kmin == mm.kmax) return Thr{mm.kmax, kk, kk};
     const uint32_t range = mm.kmax - mm.kmin;
     const int bits = 32 - __clz(range);
@@ -177,24 +177,15 @@ __device__ Thr radix_threshold(const uint32_t* keys, int n, int k, const MinMax&
     return Thr{prefix + mm.kmin, krem, kk};
 }
 
-// Exact threshold of the top-k of keys[0..n) (see the file comment).
-__device__ Thr bin_threshold(const uint32_t* keys, int n, int k, BlockScratch& sc,
-                             uint32_t* tbuf, int tcap) {
+// Exact threshold of the top-k of keys[0..n) whose nonzero keys have min, max and
+// count mm (see the file comment). The k-th key's bin usually holds a handful of
+// keys: up to 64 are ranked by one warp with shuffles; more go through radix passes.
+__device__ __noinline__ Thr bin_threshold(const uint32_t* keys, int n, int k, MinMax mm,
+                                          BlockScratch& sc, uint32_t* tbuf, int tcap) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t mx = 0u, mn = 0xffffffffu;
-    int cnt = 0;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-        const uint32_t key = keys[i];
-        if (key) {
-            mx = max(mx, key);
-            mn = min(mn, key);
-            ++cnt;
-        }
-    }
-    const MinMax mm = block_minmax(mn, mx, cnt, sc);
     if (mm.count == 0) return Thr{0xffffffffu, 0, 0};
     const int kk = min(k, mm.count);
-    if (mm.count <= k) return Thr{1u, 0, kk};          // every nonzero key is chosen
+    if (mm.count <= k) return Thr{0u, 0, kk};          // every nonzero key is chosen
     if (mm.kmax == mm.kmin) return Thr{mm.kmax, kk, kk};  // all equal: lowest positions
     const uint32_t range = mm.kmax - mm.kmin;
     const int bits = 32 - __clz(range);
@@ -242,87 +233,134 @@ __device__ Thr bin_threshold(const uint32_t* keys, int n, int k, BlockScratch& s
     }
     __syncthreads();
     const uint32_t bstar = (uint32_t)sc.pick[0];
-    const int before = sc.pick[1];
+    const int need = kk - sc.pick[1];  // 1 <= need <= nb
     const int nb = (int)sc.hist[bstar];
-    const int need = kk - before;  // 1 <= need <= nb
-    __syncthreads();                // pick[] and wcnt[] are reused below
-    if (nb > tcap) return radix_threshold(keys, n, k, mm, sc, true);
+    if (nb > tcap) {
+        __syncthreads();
+        return radix_threshold(keys, n, k, mm, sc, true);
+    }
+    // Collect the bin's keys (order is irrelevant to ranking). Exactly nb keys match,
+    // so the slot index stays below nb <= tcap.
     uint32_t bmx = 0u, bmn = 0xffffffffu;
-    const int n32 = (n + 31) & ~31;
-    for (int i = threadIdx.x; i < n32; i += kThreads) {
-        const uint32_t key = i < n ? keys[i] : 0u;
-        const bool in = key != 0u && ((mm.kmax - key) >> shift) == bstar;
-        const unsigned m = __ballot_sync(0xffffffffu, in);
-        if (m) {
-            int base = 0;
-            if (lane == 0) base = atomicAdd(&sc.tcount, __popc(m));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if (in) {
-                tbuf[base + __popc(m & ((1u << lane) - 1u))] = key;
-                bmx = max(bmx, key);
-                bmn = min(bmn, key);
-            }
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint32_t key = keys[i];
+        if (key != 0u && ((mm.kmax - key) >> shift) == bstar) {
+            const int at = atomicAdd(&sc.tcount, 1);
+            if (at < tcap) tbuf[at] = key;
+            bmx = max(bmx, key);
+            bmn = min(bmn, key);
         }
     }
-    const MinMax bm = block_minmax(bmn, bmx, 0, sc);  // syncs: tbuf complete after it
-    const Thr t = radix_threshold(tbuf, nb, need, MinMax{bm.kmin, bm.kmax, nb}, sc, false);
-    return Thr{t.T, t.need_eq, kk};
+    if (nb > kRankMax) {
+        const MinMax bm = block_minmax(bmn, bmx, 0, sc);  // syncs: tbuf complete after it
+        const Thr t = radix_threshold(tbuf, nb, need, MinMax{bm.kmin, bm.kmax, nb}, sc, false);
+        return Thr{t.T, t.need_eq, kk};
+    }
+    __syncthreads();  // tbuf complete
+    if (threadIdx.x < nb) {
+        // Rank this thread's key against the bin by broadcast reads: the need-th
+        // largest is T, and need - (#greater) of the keys equal to T are taken.
+        const uint32_t mine = tbuf[threadIdx.x];
+        int gt = 0, eq = 0;
+        for (int j = 0; j < nb; ++j) {
+            const uint32_t a = tbuf[j];
+            gt += a > mine;
+            eq += a == mine;
+        }
+        if (gt < need && need <= gt + eq) {  // equal keys write equal values
+            sc.pick[2] = (int)mine;
+            sc.pick[3] = need - gt;
+        }
+    }
+    __syncthreads();
+    return Thr{(uint32_t)sc.pick[2], sc.pick[3], kk};
 }
 
-// emit(rank, position) for every chosen position, ranks ascending with position.
-template <class Emit>
-__device__ void ordered_emit(const uint32_t* keys, int n, const Thr& t, BlockScratch& sc,
-                             Emit emit) {
+// Where the chosen positions go (one code path for all three uses keeps the kernel
+// small: it runs once per CTA, so instruction fetch matters).
+struct EmitTo {
+    int mode;               // 0: out[rank] = base + pos
+                            // 1: rkeys[rank] = keys[pos], rids[rank] = base + pos
+                            // 2: out[rank] = ids[pos]
+    int base;
+    int32_t* out;
+    uint32_t* rkeys;
+    uint32_t* rids;
+    const uint32_t* ids;
+};
+
+__device__ __forceinline__ void emit_one(const EmitTo& e, const uint32_t* keys, int at, int i) {
+    if (e.mode == 0) {
+        e.out[at] = e.base + i;
+    } else if (e.mode == 1) {
+        e.rkeys[at] = keys[i];
+        e.rids[at] = (uint32_t)(e.base + i);
+    } else {
+        e.out[at] = (int)e.ids[i];
+    }
+}
+
+// Emits every chosen position, ranks ascending with position. Thread t owns the
+// contiguous run [t*per, (t+1)*per), per = 4 x an odd number so that the 16-byte
+// loads of a quarter warp hit distinct banks; one block scan of its (#greater,
+// #equal) counts, packed in 16-bit halves (n <= 65535), gives the rank of its first
+// chosen key.
+__device__ __noinline__ void ordered_emit(const uint32_t* keys, int n, Thr t, BlockScratch& sc,
+                                          EmitTo e) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t T = t.T;
-    const int need_eq = t.need_eq;
-    const int seg = (((n + kWarps - 1) / kWarps) + 31) & ~31;
-    const int w0 = warp * seg;
-    const int w1 = min(n, w0 + seg);
-    int gt = 0, eq = 0;
-    for (int i = w0 + lane; i < w0 + seg; i += 32) {
-        const uint32_t key = i < w1 ? keys[i] : 0u;
-        gt += __popc(__ballot_sync(0xffffffffu, key > T));
-        eq += __popc(__ballot_sync(0xffffffffu, key == T));
-    }
-    if (lane == 0) {
-        sc.wgt[warp] = gt;
-        sc.weq[warp] = eq;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int eqb = 0, selb = 0;
-        for (int w = 0; w < kWarps; ++w) {
-            sc.weqb[w] = eqb;
-            sc.wselb[w] = selb;
-            selb += sc.wgt[w] + max(0, min(need_eq - eqb, sc.weq[w]));
-            eqb += sc.weq[w];
+    const int per = 4 * (((n + 4 * kThreads - 1) / (4 * kThreads)) | 1);
+    const int i0 = threadIdx.x * per;
+    const int i1 = min(n, i0 + per);
+    uint32_t gt = 0u, eq = 0u;
+    for (int i = i0; i < i1; i += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
+        const uint32_t k4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t key = i + j < i1 ? k4[j] : 0u;
+            gt += key > T;
+            eq += key == T;
         }
     }
+    const uint32_t packed = (eq << 16) | gt;
+    uint32_t incl = packed;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) sc.wcnt[warp] = (int)incl;
     __syncthreads();
-    int eqr = sc.weqb[warp], pos = sc.wselb[warp];
-    const unsigned lt = (1u << lane) - 1u;
-    for (int i = w0 + lane; i < w0 + seg; i += 32) {
-        const uint32_t key = i < w1 ? keys[i] : 0u;
-        const unsigned beq = __ballot_sync(0xffffffffu, key == T);
-        const bool sel = key > T || (key == T && eqr + __popc(beq & lt) < need_eq);
-        const unsigned bsel = __ballot_sync(0xffffffffu, sel);
-        const int at = pos + __popc(bsel & lt);
-        if (sel && at < t.kk) emit(at, i);
-        eqr += __popc(beq);
-        pos += __popc(bsel);
+    uint32_t excl = incl - packed;
+    for (int w = 0; w < warp; ++w) excl += (uint32_t)sc.wcnt[w];
+    int eqr = (int)(excl >> 16);
+    int pos = (int)(excl & 0xffffu) + min(eqr, t.need_eq);
+    for (int i = i0; i < i1 && pos < t.kk; i += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
+        const uint32_t k4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t key = i + j < i1 ? k4[j] : 0u;
+            bool sel = key > T;
+            if (key == T) sel = eqr++ < t.need_eq;
+            if (sel && pos < t.kk) emit_one(e, keys, pos++, i + j);
+        }
     }
     __syncthreads();
 }
 
-// Exact top-k of keys[0..n) (key desc, position asc; key 0 never chosen): emits
-// the chosen positions ascending and returns how many, min(k, #nonzero keys).
-template <class Emit>
-__device__ int block_topk(const uint32_t* keys, int n, int k, BlockScratch& sc, uint32_t* tbuf,
-                          int tcap, Emit emit) {
-    const Thr t = bin_threshold(keys, n, k, sc, tbuf, tcap);
+// Exact top-k of keys[0..n) (key desc, position asc; key 0 never chosen) whose
+// nonzero keys have min, max and count mm (bounds may be loose): emits the chosen
+// positions ascending and returns how many, min(k, #nonzero keys); *thr gets the
+// threshold (every chosen key is >= thr->T).
+__device__ __noinline__ int block_topk(const uint32_t* keys, int n, int k, MinMax mm,
+                                       BlockScratch& sc, uint32_t* tbuf, int tcap, EmitTo e,
+                                       Thr* thr) {
+    const Thr t = bin_threshold(keys, n, k, mm, sc, tbuf, tcap);
+    *thr = t;
     if (t.kk == 0) return 0;
-    ordered_emit(keys, n, t, sc, emit);
+    ordered_emit(keys, n, t, sc, e);
     return t.kk;
 }
 
@@ -340,6 +378,17 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
     const int begin = crank * a.chunk;
     const int n = max(0, min(a.chunk, a.p_stride - begin));
     const float* srow = a.scores + (long long)r * a.p_stride + begin;
+    uint32_t kmx = 0u, kmn = 0xffffffffu;
+    int kcnt = 0;
+    auto put = [&](int i, float f) {
+        const uint32_t key = score_key(f);
+        keys[i] = key;
+        if (key) {
+            kmx = max(kmx, key);
+            kmn = min(kmn, key);
+            ++kcnt;
+        }
+    };
     if ((reinterpret_cast<uintptr_t>(srow) & 15u) == 0u) {
         // 16-byte loads, eight per thread in flight before any is converted.
         const float4* s4 = reinterpret_cast<const float4*>(srow);
@@ -355,48 +404,68 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
             for (int j = 0; j < 8; ++j) {
                 const int i = base + j * kThreads + threadIdx.x;
                 if (i < nv) {
-                    keys[4 * i] = score_key(v[j].x);
-                    keys[4 * i + 1] = score_key(v[j].y);
-                    keys[4 * i + 2] = score_key(v[j].z);
-                    keys[4 * i + 3] = score_key(v[j].w);
+                    put(4 * i, v[j].x);
+                    put(4 * i + 1, v[j].y);
+                    put(4 * i + 2, v[j].z);
+                    put(4 * i + 3, v[j].w);
                 }
             }
         }
-        for (int i = (nv << 2) + threadIdx.x; i < n; i += kThreads) keys[i] = score_key(__ldg(srow + i));
+        for (int i = (nv << 2) + threadIdx.x; i < n; i += kThreads) put(i, __ldg(srow + i));
     } else {
-        for (int i = threadIdx.x; i < n; i += kThreads) keys[i] = score_key(__ldg(srow + i));
+        for (int i = threadIdx.x; i < n; i += kThreads) put(i, __ldg(srow + i));
     }
-    __syncthreads();
+    const MinMax mm = block_minmax(kmn, kmx, kcnt, sc);  // also publishes keys[]
 
     int32_t* out = a.pool_ids + (long long)r * a.sk;
+    EmitTo e;
+    e.base = begin;
+    e.out = out;
+    e.rkeys = e.rids = nullptr;
+    e.ids = nullptr;
+    Thr t;
     if (C == 1) {
-        const int kk = block_topk(keys, n, a.sk, sc, tbuf, a.tcap,
-                                  [&](int at, int i) { out[at] = begin + i; });
+        e.mode = 0;
+        const int kk = block_topk(keys, n, a.sk, mm, sc, tbuf, a.tcap, e, &t);
         for (int j = kk + threadIdx.x; j < a.sk; j += kThreads) out[j] = -1;
         return;
     }
 
-    // This slice's top-k, pushed into slot crank of CTA 0's merge area.
-    uint32_t* mkeys0 = cluster.map_shared_rank(reinterpret_cast<uint32_t*>(dyn + a.merge_off), 0);
-    uint32_t* rkeys = mkeys0 + crank * a.sk;
-    uint32_t* rids = mkeys0 + C * a.sk + crank * a.sk;
-    const int kc = block_topk(keys, n, a.sk, sc, tbuf, a.tcap, [&](int at, int i) {
-        rkeys[at] = keys[i];
-        rids[at] = (uint32_t)(begin + i);
-    });
-    for (int j = kc + threadIdx.x; j < a.sk; j += kThreads) rkeys[j] = 0u;
+    // This slice's top-k, pushed into slot crank of CTA 0's merge area, with bounds
+    // (chosen keys are >= the slice threshold and <= the slice maximum) and count.
+    uint32_t* m0 = cluster.map_shared_rank(reinterpret_cast<uint32_t*>(dyn + a.merge_off), 0);
+    e.mode = 1;
+    e.rkeys = m0 + crank * a.sk;
+    e.rids = m0 + C * a.sk + crank * a.sk;
+    const int kc = block_topk(keys, n, a.sk, mm, sc, tbuf, a.tcap, e, &t);
+    for (int j = kc + threadIdx.x; j < a.sk; j += kThreads) e.rkeys[j] = 0u;
+    if (threadIdx.x == 0) {
+        uint32_t* st = m0 + 2 * C * a.sk + 3 * crank;
+        st[0] = kc > 0 ? t.T : 0xffffffffu;
+        st[1] = kc > 0 ? mm.kmax : 0u;
+        st[2] = (uint32_t)kc;
+    }
     cluster.sync();  // publishes the pushed lists; no remote access happens after it
     if (crank != 0) return;
 
     const uint32_t* mkeys = reinterpret_cast<const uint32_t*>(dyn + a.merge_off);
-    const uint32_t* mids = mkeys + C * a.sk;
-    const int kk = block_topk(mkeys, C * a.sk, a.sk, sc, tbuf, a.tcap,
-                              [&](int at, int i) { out[at] = (int)mids[i]; });
+    const uint32_t* st = mkeys + 2 * C * a.sk;
+    MinMax mg{0xffffffffu, 0u, 0};
+    for (int c = 0; c < C; ++c) {
+        mg.kmin = min(mg.kmin, st[3 * c]);
+        mg.kmax = max(mg.kmax, st[3 * c + 1]);
+        mg.count += (int)st[3 * c + 2];
+    }
+    e.mode = 2;
+    e.base = 0;
+    e.ids = mkeys + C * a.sk;
+    const int kk = block_topk(mkeys, C * a.sk, a.sk, mg, sc, tbuf, a.tcap, e, &t);
     for (int j = kk + threadIdx.x; j < a.sk; j += kThreads) out[j] = -1;
 }
 
 // Dynamic shared memory: the slice's keys (4 B each); with C > 1 the merge area
-// (C x select_k keys and ids, used in CTA 0); the threshold bin's list.
+// (C x select_k keys and ids plus 3 words of bounds per slice, used in CTA 0); the
+// threshold bin's list.
 struct SmemPlan {
     long long merge_off, tbuf_off, tcap, bytes;
 };
@@ -404,7 +473,7 @@ SmemPlan smem_plan(int p_stride, int sk, int C) {
     const long long chunk = (p_stride + C - 1) / C;
     SmemPlan p;
     p.merge_off = (chunk * 4 + 15) & ~15LL;
-    p.tbuf_off = p.merge_off + (C > 1 ? (long long)C * sk * 8 : 0);
+    p.tbuf_off = p.merge_off + (C > 1 ? ((long long)C * sk * 8 + 12LL * C + 15) & ~15LL : 0);
     const long long room = (kMaxSmem - p.tbuf_off) / 4;
     p.tcap = room > 2048 ? 2048 : room;
     p.bytes = p.tbuf_off + 4 * (p.tcap > 0 ? p.tcap : 0);
