@@ -161,6 +161,36 @@ int dsa_score(const dsa_bf16* qidx, const float* w, int rows, int index_heads, i
               float* scores, int p_stride, int32_t* status, void* stream);
 
 /*
+ * dsa_score_prefill -- dsa_index_scores for a chunk of query rows of ONE sequence
+ * (chunked prefill), as a dense [rows * index_heads, ihd] x [ihd, P] contraction on
+ * the tensor cores (tcgen05, accumulators in tensor memory). Same equation and
+ * candidate rule as dsa_score (tp.rs, "Why the indexer is replicated"), with every
+ * row reading sequence `seq`:
+ *
+ *   scores[r, p] = sum_h w[r,h] * relu(scale * <qidx[r,h,:], kpool[seq, p, :]>)
+ *
+ * when pool_valid[seq, p] != 0 and first_key + (p+1)*kpool - 1 < min(row_ctx[r],
+ * seq_lens[seq]); every other entry up to p_stride is -inf. The products are bf16 x
+ * bf16 accumulated in f32; the head sum is f32 and takes w[r,h] * |scale| once.
+ *
+ * qidx [rows, index_heads, ihd] bf16 (16-byte aligned); w [rows, index_heads] f32;
+ * row_ctx [rows] i32 (device, nullable: seq_lens[seq]); kpool / pool_valid: the
+ * contiguous pooled-key caches [batch, max_seq_len / kpool, ihd] and
+ * [batch, max_seq_len / kpool] (pg->block_table must be NULL; dsa_score takes paged
+ * caches); seq in [0, pg->batch) (host value); scores [rows, p_stride] f32.
+ * Limits: ihd in {64, 128}; index_heads in {32, 64, 128}; 1 <= kpool <= 16.
+ * Errors: DSA_ERR_UNSUPPORTED outside the limits or for a paged cache;
+ * DSA_ERR_INVALID_ARG for a bad seq, NULL or misaligned tensors. `status` gets
+ * DSA_STATUS_TIMEOUT if a pipeline wait inside the kernel gives up (about 1 s); the
+ * scores are then incomplete.
+ */
+int dsa_score_prefill(const dsa_bf16* qidx, const float* w, int rows, int index_heads, int ihd,
+                      int seq, const int32_t* row_ctx,
+                      const dsa_bf16* kpool, const uint8_t* pool_valid, const dsa_paging* pg,
+                      int first_key, int kpool_size, float scale,
+                      float* scores, int p_stride, int32_t* status, void* stream);
+
+/*
  * dsa_select -- dsa_topk_pools. mod.rs "Shape of the pipeline": [Q, P] scores
  * -> [Q, select_k] pool ids, select_k = min(index_topk / kpool, p_stride).
  * Per row, k' = min(select_k, number of finite scores); the k' pools first in

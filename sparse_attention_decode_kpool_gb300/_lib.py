@@ -49,6 +49,8 @@ SIGNATURES = {
     "dsa_select_k": (_I, [_I, _I, _I]),
     "dsa_compress": (_I, [_P, _P, _P, _P, _P, _P, _F, _PG, _I, _I, _I, _P, _P, _P, _P, _P]),
     "dsa_score": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _PG, _I, _I, _F, _P, _I, _P, _P]),
+    "dsa_score_prefill": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _PG, _I, _I, _F, _P, _I, _P,
+                               _P]),
     "dsa_select": (_I, [_P, _I, _I, _I, _I, _P, _P]),
     "dsa_expand": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "dsa_sparse_mla_decode_workspace": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),

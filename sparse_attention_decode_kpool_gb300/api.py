@@ -13,7 +13,7 @@ import torch
 from . import _lib
 from ._lib import DsaPaging, check
 
-__all__ = ["paging", "dsa_compress", "dsa_score", "dsa_select", "dsa_expand",
+__all__ = ["paging", "dsa_compress", "dsa_score", "dsa_score_prefill", "dsa_select", "dsa_expand",
            "dsa_sparse_mla_decode_workspace", "dsa_sparse_mla_decode",
            "dsa_sparse_mla_decode_noalloc", "dsa_latent_project_workspace",
            "dsa_latent_project", "dsa_select_k",
@@ -95,6 +95,25 @@ def dsa_score(qidx, w, row_seq, row_ctx, kpool, pool_valid, pg: DsaPaging, first
     check(_lib.load().dsa_score(
         _ptr(qidx, torch.bfloat16, "qidx"), _ptr(w, torch.float32, "w"), rows, heads, ihd,
         _ptr(row_seq, torch.int32, "row_seq"), _ptr(row_ctx, torch.int32, "row_ctx"),
+        _ptr(kpool, torch.bfloat16, "kpool"), _ptr(pool_valid, torch.uint8, "pool_valid"),
+        ctypes.byref(pg), int(first_key), int(kpool_size), float(scale),
+        _ptr(scores, torch.float32, "scores"), int(scores.shape[1]),
+        _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def dsa_score_prefill(qidx, w, seq: int, row_ctx, kpool, pool_valid, pg: DsaPaging,
+                      first_key: int, kpool_size: int, scale: float, scores, status=None,
+                      stream=None) -> None:
+    """Index scores of a chunk of query rows of sequence ``seq`` on the tensor cores
+    (contiguous pooled-key cache; index_heads in {32, 64, 128})."""
+    rows, heads, ihd = (int(x) for x in qidx.shape)
+    if tuple(w.shape) != (rows, heads):
+        raise ValueError(f"w must be [{rows}, {heads}]")
+    if scores.dim() != 2 or scores.shape[0] != rows:
+        raise ValueError("scores must be [rows, p_stride]")
+    check(_lib.load().dsa_score_prefill(
+        _ptr(qidx, torch.bfloat16, "qidx"), _ptr(w, torch.float32, "w"), rows, heads, ihd,
+        int(seq), _ptr(row_ctx, torch.int32, "row_ctx"),
         _ptr(kpool, torch.bfloat16, "kpool"), _ptr(pool_valid, torch.uint8, "pool_valid"),
         ctypes.byref(pg), int(first_key), int(kpool_size), float(scale),
         _ptr(scores, torch.float32, "scores"), int(scores.shape[1]),

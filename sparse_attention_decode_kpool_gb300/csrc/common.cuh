@@ -31,10 +31,12 @@ struct Paging {
 
 int check_paging(const dsa_paging* pg, int kpool, Paging* out);
 
-// 2-D tiled tensor map over a row-major [outer, inner] array (no swizzle, zero fill
-// out of bounds), boxes of box_inner x box_outer elements.
+// 2-D tiled tensor map over a row-major [outer, inner] array (zero fill out of
+// bounds), boxes of box_inner x box_outer elements, stored in shared memory with the
+// given swizzle (128-byte swizzle: box_inner x element size must be 128 bytes).
 int make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
-                 uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+                 uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
 // The o_absorb projection (project.cu): y[r] = bf16(o_absorb . x[r]), x bf16 or f32.
 bool project_supported(int K, int hidden);

@@ -1,0 +1,542 @@
+// dsa_score_prefill: index scores of many query rows of one sequence (chunked
+// prefill) as a dense contraction on the tensor cores.
+//
+// Page: metrale_model_arch/glm5next_dsa/tp.rs, "Why the indexer is replicated"
+// (score[q, p] = sum_h w[q,h] * relu(scale * <qidx[q,h,:], kpool[p,:]>)); the dense
+// [Q * index_heads, ihd] x [ihd, P] form is the chunked-prefill case of the same
+// equation, with the candidate rule of dsa_score (pool flag set, last slot before the
+// row's context length).
+//
+// Tile: D[p, (q,h)] = <kpool[p,:], qidx[q,h,:]> for 128 pools (the MMA's M, one
+// tensor-memory lane each) by 256 (query, head) columns (N), K = ihd, bf16 operands,
+// f32 accumulation in tensor memory. A pool's row of D holds every head of the
+// tile's queries, so the head sum stays in one thread:
+//   score[q, p] = sum_h (w[q,h] * |scale|) * relu(sign(scale) * D[p, (q,h)]).
+//
+// Roles (one CTA per SM, persistent over work units of one query tile x 32 pool
+// tiles):
+//   warp 0      TMA producer: the unit's query tile once, pool tiles through a ring
+//               of shared-memory stages (128-byte swizzled K-major boxes);
+//   warp 1      owns the 512 tensor-memory columns (two 256-column accumulators) and
+//               issues tcgen05.mma from one thread;
+//   warps 2..9  epilogue: tcgen05.ld of their lane quarter and column half, the
+//               relu-weighted head sum, masking, and the f32 score stores.
+// Every wait is bounded: a wait that runs out sets DSA_STATUS_TIMEOUT and a CTA-wide
+// abort flag, every role then leaves its loop, copies and MMAs in flight are drained,
+// and tensor memory is released.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kTileP = 128;        // pools per tile
+constexpr int kTileN = 256;        // (query, head) columns per tile
+constexpr int kEpiWarps = 8;       // two per tensor-memory lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kTilesPerUnit = 32;  // pool tiles per work unit
+constexpr uint32_t kTmemCols = 2 * kTileN;
+
+struct PrefillArgs {
+    const float* w;
+    const int32_t* row_ctx;
+    const int32_t* seq_lens;
+    const uint8_t* pv;  // this sequence's pool flags
+    float* scores;
+    int32_t* status;
+    int rows;
+    int p_stride;
+    int first_key;
+    int kpool;
+    int seq;
+    int cap;   // token capacity of a sequence
+    int pcap;  // pool capacity of a sequence
+    long long prow0;  // this sequence's first pool row in the pooled-key tensor
+    int qtiles, ptiles, pchunks;
+    float wscale;  // |scale|
+    int neg;       // scale < 0
+};
+
+// ---- tcgen05 / tensor-memory helpers ---------------------------------------
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+// Shared-memory matrix descriptor: K-major operand in 128-byte swizzle atoms (8
+// rows x 128 bytes, rows 128 bytes apart, atoms 1024 bytes apart).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation this thread issued so far is done.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+// 32 consecutive f32 columns of this thread's lane.
+__device__ __forceinline__ void tc_ld32(uint32_t (&v)[32], uint32_t taddr) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+          "=r"(v[31])
+        : "r"(taddr));
+}
+// Waits for this thread's tensor-memory loads; v is tied in so that no use of it is
+// scheduled before the wait.
+__device__ __forceinline__ void tc_wait_ld(uint32_t (&v)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                   "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                   "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]),
+                   "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                   "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]),
+                   "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+                 :
+                 : "memory");
+}
+
+// Bounded wait that also gives up once another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort_flag, int32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > 1000000000ull) {
+                *abort_flag = 1;
+                flag_status(status, DSA_STATUS_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+template <int KA>
+struct Layout {
+    static constexpr int kStages = KA == 2 ? 4 : 8;
+    static constexpr uint32_t kRowBytes = 128;                      // one swizzle row
+    static constexpr uint32_t kABox = kTileP * kRowBytes;           // one K atom of a pool tile
+    static constexpr uint32_t kBBox = kTileN * kRowBytes;           // one K atom of a query tile
+    static constexpr uint32_t kABytes = KA * kABox;                 // a stage
+    static constexpr uint32_t kBBytes = KA * kBBox;
+    static constexpr uint32_t kOffA = kBBytes;
+    static constexpr uint32_t kOffW = kOffA + kStages * kABytes;    // [warp][128] f32
+    static constexpr uint32_t kOffN = kOffW + kEpiWarps * 128 * 4;  // [warp][8] i32
+    static constexpr uint32_t kOffBar = kOffN + kEpiWarps * 8 * 4;
+    static constexpr int kBars = 2 * kStages + 2 + 4 + 1;
+    static constexpr uint32_t kOffMisc = kOffBar + kBars * 8;
+    static constexpr uint32_t kBytes = kOffMisc + 16;
+    static constexpr uint32_t kDynBytes = kBytes + 1024;  // room to align the base to 1024
+};
+
+template <int KA, int HI>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_score_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB, PrefillArgs a) {
+    using L = Layout<KA>;
+    constexpr int S = L::kStages;
+    constexpr int QPT = kTileN / HI;    // queries per tile
+    constexpr int QPW = QPT / 2;        // queries per epilogue warp
+    constexpr int KSTEPS = KA * 4;      // MMAs of K = 16 per tile
+    constexpr uint32_t IDESC = idesc_bf16(kTileP, kTileN);
+    static_assert(HI % 32 == 0 && QPT >= 2, "index heads must be 32, 64 or 128");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sB = smem;
+    uint8_t* sA = smem + L::kOffA;
+    float* wtab_all = reinterpret_cast<float*>(smem + L::kOffW);
+    int* ntab_all = reinterpret_cast<int*>(smem + L::kOffN);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + S;
+    uint64_t* bfull = bars + 2 * S;
+    uint64_t* bempty = bfull + 1;
+    uint64_t* accfull = bempty + 1;   // [2]
+    uint64_t* accempty = accfull + 2; // [2]
+    uint64_t* drain = accempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init(bfull, 1);
+        mbar_init(bempty, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accfull + b, 1);
+            mbar_init(accempty + b, kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile(
+            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                smem_u32(tmem_slot)),
+            "r"(kTmemCols)
+            : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const long long units = (long long)a.qtiles * a.pchunks;
+
+    if (warp == 0) {
+        // ---- TMA producer ----
+        // Per unit: the first pool tiles (as many as there are stages), then the query
+        // tile once the previous unit's MMAs have released it, then the rest; so the
+        // reload of the query tile overlaps pool tiles already in flight.
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t sphase = 0;
+            bool armed[S];
+            uint32_t apar[S];
+            for (int s = 0; s < S; ++s) armed[s] = false, apar[s] = 0;
+            bool barmed = false;
+            uint32_t bpar = 0;
+            int uc = 0;
+            bool ok = true;
+            for (long long u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+                const int qt = (int)(u / a.pchunks), pc = (int)(u % a.pchunks);
+                const int t0 = pc * kTilesPerUnit, t1 = min(a.ptiles, t0 + kTilesPerUnit);
+                const int tb = min(t1, t0 + S);  // the query tile is loaded before tile tb
+                for (int t = t0; t <= t1 && ok; ++t) {
+                    if (t == tb) {
+                        if (!wait_or_abort(bempty, (uint32_t)(uc & 1) ^ 1u, abort_flag,
+                                           a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bfull, L::kBBytes);
+                        for (int ka = 0; ka < KA; ++ka)
+                            tma_load_2d(smem_u32(sB + ka * L::kBBox), &tmB, ka * 64,
+                                        qt * kTileN, bfull);
+                        barmed = true;
+                        bpar = (uint32_t)(uc & 1);
+                    }
+                    if (t == t1) break;
+                    if (!wait_or_abort(empty + stage, sphase ^ 1u, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full + stage, L::kABytes);
+                    const int y = (int)(a.prow0 + (long long)t * kTileP);
+                    for (int ka = 0; ka < KA; ++ka)
+                        tma_load_2d(smem_u32(sA + stage * L::kABytes + ka * L::kABox), &tmA,
+                                    ka * 64, y, full + stage);
+                    armed[stage] = true;
+                    apar[stage] = sphase;
+                    if (++stage == S) stage = 0, sphase ^= 1u;
+                }
+            }
+            // Drain: every copy this thread issued has landed before the CTA ends.
+            for (int s = 0; s < S; ++s)
+                if (armed[s]) mbar_wait(full + s, apar[s]);
+            if (barmed) mbar_wait(bfull, bpar);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer ----
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t sphase = 0;
+            int tc = 0, uc = 0;
+            bool ok = true;
+            for (long long u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+                const int pc = (int)(u % a.pchunks);
+                const int t0 = pc * kTilesPerUnit, t1 = min(a.ptiles, t0 + kTilesPerUnit);
+                if (!wait_or_abort(bfull, (uint32_t)(uc & 1), abort_flag, a.status)) break;
+                tc_fence_after();
+                for (int t = t0; t < t1; ++t, ++tc) {
+                    const int buf = tc & 1;
+                    if (!wait_or_abort(accempty + buf, (uint32_t)((tc >> 1) & 1) ^ 1u, abort_flag,
+                                       a.status) ||
+                        !wait_or_abort(full + stage, sphase, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(buf * kTileN);
+                    const uint32_t a0 = smem_u32(sA + stage * L::kABytes);
+                    const uint32_t b0 = smem_u32(sB);
+#pragma unroll
+                    for (int k = 0; k < KSTEPS; ++k) {
+                        const uint32_t off = (uint32_t)(k & 3) * 32u;  // K = 16 bf16 = 32 B
+                        const uint64_t ad = sw128_desc(a0 + (uint32_t)(k >> 2) * L::kABox + off);
+                        const uint64_t bd = sw128_desc(b0 + (uint32_t)(k >> 2) * L::kBBox + off);
+                        tc_mma(d, ad, bd, IDESC, k > 0 ? 1u : 0u);
+                    }
+                    tc_commit(empty + stage);
+                    tc_commit(accfull + buf);
+                    if (++stage == S) stage = 0, sphase ^= 1u;
+                }
+                if (ok) tc_commit(bempty);
+            }
+            // Drain: every MMA issued has completed before tensor memory is released.
+            tc_commit(drain);
+            mbar_wait(drain, 0);
+        }
+    } else {
+        // ---- epilogue ----
+        const int e = warp - 2;
+        const int quarter = warp & 3;   // tensor-memory lanes 32*quarter .. +31
+        const int half = e >> 2;        // columns 128*half .. +127
+        float* wtab = wtab_all + e * 128;
+        int* ntab = ntab_all + e * 8;
+        const float NEG_INF = __int_as_float(0xff800000);
+        const int Lseq = min(__ldg(a.seq_lens + a.seq), a.cap);
+        int tc = 0;
+        bool ok = true;
+        for (long long u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const int qt = (int)(u / a.pchunks), pc = (int)(u % a.pchunks);
+            const int t0 = pc * kTilesPerUnit, t1 = min(a.ptiles, t0 + kTilesPerUnit);
+            // This warp's weights (w * |scale|) and visible-pool counts for the unit.
+            const long long wbase = (long long)qt * kTileN + half * 128;
+            const long long wlim = (long long)a.rows * HI;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const long long idx = wbase + lane + 32 * i;
+                wtab[lane + 32 * i] = idx < wlim ? __ldg(a.w + idx) * a.wscale : 0.f;
+            }
+            if (lane < QPW) {
+                const int r = qt * QPT + half * QPW + lane;
+                int nv = 0;
+                if (r < a.rows) {
+                    const int ctx = a.row_ctx ? min(__ldg(a.row_ctx + r), Lseq) : Lseq;
+                    nv = ctx > a.first_key ? (ctx - a.first_key) / a.kpool : 0;
+                }
+                ntab[lane] = nv;
+            }
+            __syncwarp();
+            for (int t = t0; t < t1; ++t, ++tc) {
+                const int buf = tc & 1;
+                const int p = t * kTileP + 32 * quarter + lane;
+                const bool flag = p < a.pcap && __ldg(a.pv + p) != 0;
+                // One lane waits and the warp follows its verdict, so the warp-wide
+                // tensor-memory loads below are always reached by all lanes together.
+                int got = 1;
+                if (lane == 0)
+                    got = wait_or_abort(accfull + buf, (uint32_t)((tc >> 1) & 1), abort_flag,
+                                        a.status);
+                if (!__shfl_sync(0xffffffffu, got, 0)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tb =
+                    tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kTileN + half * 128);
+                uint32_t v[2][32];
+                tc_ld32(v[0], tb);
+                tc_wait_ld(v[0]);
+                float acc = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    if (ch + 1 < 4) tc_ld32(v[(ch + 1) & 1], tb + 32u * (ch + 1));
+                    const uint32_t* x = v[ch & 1];
+                    const float4* w4 = reinterpret_cast<const float4*>(wtab + 32 * ch);
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+                    if (a.neg) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 ww = w4[i];
+                            s0 = fmaf(fmaxf(-__uint_as_float(x[4 * i]), 0.f), ww.x, s0);
+                            s1 = fmaf(fmaxf(-__uint_as_float(x[4 * i + 1]), 0.f), ww.y, s1);
+                            s2 = fmaf(fmaxf(-__uint_as_float(x[4 * i + 2]), 0.f), ww.z, s2);
+                            s3 = fmaf(fmaxf(-__uint_as_float(x[4 * i + 3]), 0.f), ww.w, s3);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 ww = w4[i];
+                            s0 = fmaf(fmaxf(__uint_as_float(x[4 * i]), 0.f), ww.x, s0);
+                            s1 = fmaf(fmaxf(__uint_as_float(x[4 * i + 1]), 0.f), ww.y, s1);
+                            s2 = fmaf(fmaxf(__uint_as_float(x[4 * i + 2]), 0.f), ww.z, s2);
+                            s3 = fmaf(fmaxf(__uint_as_float(x[4 * i + 3]), 0.f), ww.w, s3);
+                        }
+                    }
+                    acc += (s0 + s1) + (s2 + s3);
+                    if ((32 * (ch + 1)) % HI == 0) {  // the chunk ends a query
+                        const int jl = (32 * ch) / HI;  // query within this warp's half
+                        const int r = qt * QPT + half * QPW + jl;
+                        if (r < a.rows && p < a.p_stride)
+                            a.scores[(long long)r * a.p_stride + p] =
+                                (flag && p < ntab[jl]) ? acc : NEG_INF;
+                        acc = 0.f;
+                    }
+                    if (ch + 1 < 4) tc_wait_ld(v[(ch + 1) & 1]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(accempty + buf);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+__global__ void fill_neg_inf_kernel(float* scores, long long n) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x)
+        scores[i] = __int_as_float(0xff800000);
+}
+
+template <int KA, int HI>
+int launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const PrefillArgs& a, int grid,
+           cudaStream_t st) {
+    constexpr uint32_t bytes = Layout<KA>::kDynBytes;
+    int rc = set_max_smem((const void*)prefill_score_kernel<KA, HI>, (int)bytes);
+    if (rc) return rc;
+    prefill_score_kernel<KA, HI><<<grid, kThreads, bytes, st>>>(tmA, tmB, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_score_prefill launch");
+    return DSA_OK;
+}
+
+template <int KA>
+int launch_heads(int heads, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                 const PrefillArgs& a, int grid, cudaStream_t st) {
+    switch (heads) {
+        case 32: return launch<KA, 32>(tmA, tmB, a, grid, st);
+        case 64: return launch<KA, 64>(tmA, tmB, a, grid, st);
+        default: return launch<KA, 128>(tmA, tmB, a, grid, st);
+    }
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" int dsa_score_prefill(const dsa_bf16* qidx, const float* w, int rows,
+                                 int index_heads, int ihd, int seq, const int32_t* row_ctx,
+                                 const dsa_bf16* kpool, const uint8_t* pool_valid,
+                                 const dsa_paging* pg, int first_key, int kpool_size,
+                                 float scale, float* scores, int p_stride, int32_t* status,
+                                 void* stream) {
+    if (rows < 0 || p_stride < 0 || first_key < 0)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_score_prefill: rows %d, p_stride %d, first_key %d",
+                    rows, p_stride, first_key);
+    if (kpool_size < 1 || kpool_size > DSA_MAX_KPOOL)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_score_prefill: kpool %d outside [1, %d]",
+                    kpool_size, DSA_MAX_KPOOL);
+    if (ihd != 64 && ihd != 128)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_score_prefill: index_head_dim %d not in {64, 128}",
+                    ihd);
+    if (index_heads != 32 && index_heads != 64 && index_heads != 128)
+        return fail(DSA_ERR_UNSUPPORTED,
+                    "dsa_score_prefill: index_heads %d not in {32, 64, 128}; dsa_score takes "
+                    "any head count",
+                    index_heads);
+    Paging P;
+    int rc = check_paging(pg, kpool_size, &P);
+    if (rc) return rc;
+    if (P.block_table)
+        return fail(DSA_ERR_UNSUPPORTED,
+                    "dsa_score_prefill: contiguous caches only; dsa_score takes paged caches");
+    if (seq < 0 || seq >= P.batch)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_score_prefill: seq %d outside [0, %d)", seq,
+                    P.batch);
+    if (rows == 0 || p_stride == 0) return DSA_OK;
+    if (!qidx || !w || !kpool || !pool_valid || !scores)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_score_prefill: NULL tensor");
+    if ((((uintptr_t)qidx) | ((uintptr_t)kpool)) & 15)
+        return fail(DSA_ERR_INVALID_ARG,
+                    "dsa_score_prefill: qidx and kpool must be 16-byte aligned");
+    if ((long long)rows * index_heads > 0x7fffffffLL)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_score_prefill: rows x index_heads too large");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int pcap = P.max_seq_len / kpool_size;
+    if (pcap == 0) {  // no pool fits a sequence: every score is -inf
+        const long long n = (long long)rows * p_stride;
+        fill_neg_inf_kernel<<<(int)std::min<long long>((n + 255) / 256, 4096), 256, 0, st>>>(
+            scores, n);
+        cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? DSA_OK : cuda_fail(e, "dsa_score_prefill launch");
+    }
+    const long long prows = (long long)P.batch * pcap;
+    if (prows + kTileP * 2LL > 0x7fffffffLL)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_score_prefill: pooled-key tensor too large");
+
+    PrefillArgs a;
+    a.w = w;
+    a.row_ctx = row_ctx;
+    a.seq_lens = P.seq_lens;
+    a.pv = pool_valid + (long long)seq * pcap;
+    a.scores = scores;
+    a.status = status;
+    a.rows = rows;
+    a.p_stride = p_stride;
+    a.first_key = first_key;
+    a.kpool = kpool_size;
+    a.seq = seq;
+    a.cap = P.max_seq_len;
+    a.pcap = pcap;
+    a.prow0 = (long long)seq * pcap;
+    const int qpt = kTileN / index_heads;
+    a.qtiles = (rows + qpt - 1) / qpt;
+    a.ptiles = (p_stride + kTileP - 1) / kTileP;
+    a.pchunks = (a.ptiles + kTilesPerUnit - 1) / kTilesPerUnit;
+    a.wscale = fabsf(scale);
+    a.neg = scale < 0.f ? 1 : 0;
+    const long long units = (long long)a.qtiles * a.pchunks;
+    if (a.prow0 + (long long)a.ptiles * kTileP > 0x7fffffffLL)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_score_prefill: pool coordinates exceed int32");
+    if (units > 0x7fffffffLL)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_score_prefill: too many tiles");
+
+    CUtensorMap tmA, tmB;
+    rc = make_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kpool, (uint64_t)ihd,
+                      (uint64_t)prows, (uint64_t)ihd * 2, 64, kTileP,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+    rc = make_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qidx, (uint64_t)ihd,
+                      (uint64_t)rows * index_heads, (uint64_t)ihd * 2, 64, kTileN,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    const int grid = (int)std::min<long long>(units, sms);
+    return ihd == 128 ? launch_heads<2>(index_heads, tmA, tmB, a, grid, st)
+                      : launch_heads<1>(index_heads, tmA, tmB, a, grid, st);
+}

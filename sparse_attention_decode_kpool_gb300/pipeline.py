@@ -18,7 +18,8 @@ from .workloads import Workload
 
 class DsaDecodeLayer:
     def __init__(self, wl: Workload, device: str = "cuda", keep_olat: bool = False,
-                 with_o_absorb: bool = True, use_drawn_kpool: bool = False):
+                 with_o_absorb: bool = True, use_drawn_kpool: bool = False,
+                 score_path: str = "auto"):
         g = wl.geom
         self.wl = wl
         self.geom = g
@@ -74,6 +75,19 @@ class DsaDecodeLayer:
         pws = api.dsa_latent_project_workspace(R, g.heads, hidden) if self.two_call else 0
         self.proj_workspace = torch.empty(max(pws, 1), dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # Scoring: a chunk of >= 64 query rows of one contiguous sequence goes to the
+        # tensor-core contraction (dsa_score_prefill); everything else to dsa_score.
+        one_seq = R > 0 and bool((wl.row_seq == wl.row_seq[0]).all())
+        gemm_ok = (one_seq and not wl.paged and g.index_heads in (32, 64, 128)
+                   and ihd in (64, 128))
+        if score_path not in ("auto", "decode", "prefill"):
+            raise ValueError(f"score_path {score_path!r}")
+        if score_path == "prefill" and not gemm_ok:
+            raise ValueError("score_path='prefill' needs one contiguous sequence and "
+                             "index_heads in {32, 64, 128}")
+        self.prefill_seq = int(wl.row_seq[0]) if R > 0 else 0
+        self.score_gemm = score_path == "prefill" or (score_path == "auto" and gemm_ok
+                                                      and R >= 64)
         self.graph: Optional[torch.cuda.CUDAGraph] = None
         self._fused_ws: Optional[torch.Tensor] = None
 
@@ -96,6 +110,11 @@ class DsaDecodeLayer:
 
     def score(self, stream=None) -> None:
         g = self.geom
+        if self.score_gemm:
+            api.dsa_score_prefill(self.qidx, self.w, self.prefill_seq, self.row_ctx, self.kpool,
+                                  self.pool_valid, self.pg, g.first_key, g.index_kpool,
+                                  g.index_scale, self.scores, status=self.status, stream=stream)
+            return
         api.dsa_score(self.qidx, self.w, self.row_seq, self.row_ctx, self.kpool, self.pool_valid,
                       self.pg, g.first_key, g.index_kpool, g.index_scale, self.scores,
                       status=self.status, stream=stream)

@@ -215,6 +215,7 @@ def make_workload(
     invalid_tail: int = 0,
     invalid_per_seq: int = 0,
     rows_ctx: Optional[Sequence[int]] = None,
+    prefill_seq: int = 0,
     sequences: Optional[Sequence[int]] = None,
     with_raw: bool = True,
     with_o_absorb: bool = True,
@@ -226,8 +227,9 @@ def make_workload(
     ``invalid_tail``: the last ``n`` tokens of every sequence are marked invalid.
     ``invalid_per_seq``: that many token positions per sequence, drawn uniformly
     without replacement, are marked invalid.
-    ``rows_ctx``: chunked prefill on sequence 0: one query row per entry, seeing
-    that many tokens; default is one decode row per sequence seeing all of it.
+    ``rows_ctx``: chunked prefill on sequence ``prefill_seq``: one query row per
+    entry, seeing that many tokens; default is one decode row per sequence seeing
+    all of it.
     ``sequences``: draw only these sequences' cache contents (others stay zero);
     values of a drawn sequence are identical to a full draw.
     ``direct_kpool``: also draw a pooled-key cache N(0, 0.5) with 0.2 % of pools
@@ -243,7 +245,7 @@ def make_workload(
         row_ctx = seq_lens.astype(np.int32)
     else:
         rows = len(rows_ctx)
-        row_seq = np.zeros(rows, dtype=np.int32)
+        row_seq = np.full(rows, prefill_seq, dtype=np.int32)
         row_ctx = np.asarray(rows_ctx, dtype=np.int32)
     want = set(range(B)) if sequences is None else set(int(s) for s in sequences)
     ihd, kvl, KP = g.index_head_dim, g.kv_lora_rank, g.index_kpool

@@ -104,6 +104,30 @@ def test_score_select_expand_argument_errors(lib):
     assert lib.dsa_expand(FAKE, 2, 64, -1, 4, 256, FAKE, None) == DSA_ERR_INVALID_ARG
 
 
+def test_score_prefill_argument_errors(lib):
+    pg = _paging(batch=2)
+
+    def pf(heads=32, ihd=128, seq=0, kp=4, pgp=None, rows=8, q=FAKE, fk=0):
+        return lib.dsa_score_prefill(q, FAKE, rows, heads, ihd, seq, None, FAKE, FAKE,
+                                     pgp or ctypes.byref(pg), fk, kp, 0.1, FAKE, 64, None, None)
+
+    assert pf(heads=20) == DSA_ERR_UNSUPPORTED
+    assert "dsa_score" in _err(lib)
+    assert pf(heads=256) == DSA_ERR_UNSUPPORTED
+    assert pf(ihd=96) == DSA_ERR_UNSUPPORTED
+    assert pf(kp=17) == DSA_ERR_UNSUPPORTED
+    assert pf(seq=2) == DSA_ERR_INVALID_ARG
+    assert pf(seq=-1) == DSA_ERR_INVALID_ARG
+    assert pf(rows=-1) == DSA_ERR_INVALID_ARG
+    assert pf(fk=-1) == DSA_ERR_INVALID_ARG
+    assert pf(q=FAKE + 8) == DSA_ERR_INVALID_ARG  # misaligned
+    assert pf(q=None) == DSA_ERR_INVALID_ARG
+    paged = _paging(block_table=FAKE, max_blocks=16, block_size=64, nb=8)
+    assert pf(pgp=ctypes.byref(paged)) == DSA_ERR_UNSUPPORTED
+    assert "paged" in _err(lib)
+    assert pf(rows=0) == DSA_OK  # nothing to do
+
+
 def test_sparse_mla_argument_errors(lib):
     pg = _paging()
 
