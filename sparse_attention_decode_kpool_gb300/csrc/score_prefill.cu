@@ -7,11 +7,12 @@
 // equation, with the candidate rule of dsa_score (pool flag set, last slot before the
 // row's context length).
 //
-// Tile: D[p, (q,h)] = <kpool[p,:], qidx[q,h,:]> for 128 pools (the MMA's M, one
-// tensor-memory lane each) by 256 (query, head) columns (N), K = ihd, bf16 operands,
-// f32 accumulation in tensor memory. A pool's row of D holds every head of the
-// tile's queries, so the head sum stays in one thread:
-//   score[q, p] = sum_h (w[q,h] * |scale|) * relu(sign(scale) * D[p, (q,h)]).
+// Tile: D[p, (q,h)] = sign(scale) * <kpool[p,:], qidx[q,h,:]> for 128 pools (the
+// MMA's M, one tensor-memory lane each) by 256 (query, head) columns (N), K = ihd,
+// bf16 operands (the sign applied by the MMA's negate-A bit), f32 accumulation in
+// tensor memory. A pool's row of D holds every head of the tile's queries, so the
+// head sum stays in one thread:
+//   score[q, p] = sum_h (w[q,h] * |scale|) * relu(D[p, (q,h)]).
 //
 // Roles (one CTA per SM, persistent over work units of one query tile x 32 pool
 // tiles):
@@ -19,8 +20,9 @@
 //               of shared-memory stages (128-byte swizzled K-major boxes);
 //   warp 1      owns the 512 tensor-memory columns (two 256-column accumulators) and
 //               issues tcgen05.mma from one thread;
-//   warps 2..9  epilogue: tcgen05.ld of their lane quarter and column half, the
-//               relu-weighted head sum, masking, and the f32 score stores.
+//   warps 2..   epilogue (16 warps, or 8 at 128 heads): tcgen05.ld of their lane
+//               quarter and column slice, the relu-weighted head sum (packed f32x2
+//               FMAs), masking, and the f32 score stores.
 // Every wait is bounded: a wait that runs out sets DSA_STATUS_TIMEOUT and a CTA-wide
 // abort flag, every role then leaves its loop, copies and MMAs in flight are drained,
 // and tensor memory is released.
@@ -33,9 +35,13 @@ namespace {
 
 constexpr int kTileP = 128;        // pools per tile
 constexpr int kTileN = 256;        // (query, head) columns per tile
-constexpr int kEpiWarps = 8;       // two per tensor-memory lane quarter
-constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTilesPerUnit = 32;  // pool tiles per work unit
+constexpr int kWTab = 1024;        // floats of per-warp weight tables, all warps together
+
+// Epilogue warps: four per tensor-memory lane quarter (64 columns each) when a
+// query's heads fit in 64 columns, else two (128 columns each).
+__host__ __device__ constexpr int epi_warps(int heads) { return heads <= 64 ? 16 : 8; }
+__host__ __device__ constexpr int block_threads(int heads) { return 64 + 32 * epi_warps(heads); }
 constexpr uint32_t kTmemCols = 2 * kTileN;
 
 struct PrefillArgs {
@@ -119,20 +125,75 @@ __device__ __forceinline__ void tc_wait_ld(uint32_t (&v)[32]) {
                  : "memory");
 }
 
-// Bounded wait that also gives up once another role has aborted.
+// Orders later uses of v after a tcgen05.wait::ld issued just before (no instruction).
+__device__ __forceinline__ void tc_tie(uint32_t (&v)[32]) {
+    asm volatile(""
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                   "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                   "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]),
+                   "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                   "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]),
+                   "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
+}
+
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+    float4 r;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "r"(addr));
+    return r;
+}
+__device__ __forceinline__ int lds_s32(uint32_t addr) {
+    int r;
+    asm volatile("ld.shared.s32 %0, [%1];\n" : "=r"(r) : "r"(addr));
+    return r;
+}
+
+// Per chunk c of NCH 32-column chunks: sum_i w[c][i] * relu(x[c][i]), the weights
+// read from shared memory at byte address waddr + 128 c. The chunks are interleaved,
+// four packed f32x2 FMA chains each, so that their work overlaps.
+template <int NCH>
+__device__ __forceinline__ void chunk_sums(const uint32_t (&x)[NCH][32], uint32_t waddr,
+                                           float (&out)[NCH]) {
+    float2 s[NCH][4];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s[c][k] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const float4 wa = lds_f4(waddr + 128u * c + 16u * i);
+            const float4 wb = lds_f4(waddr + 128u * c + 16u * (i + 1));
+            float r[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r[j] = fmaxf(__uint_as_float(x[c][4 * i + j]), 0.f);
+            s[c][0] = __ffma2_rn(make_float2(r[0], r[1]), make_float2(wa.x, wa.y), s[c][0]);
+            s[c][1] = __ffma2_rn(make_float2(r[2], r[3]), make_float2(wa.z, wa.w), s[c][1]);
+            s[c][2] = __ffma2_rn(make_float2(r[4], r[5]), make_float2(wb.x, wb.y), s[c][2]);
+            s[c][3] = __ffma2_rn(make_float2(r[6], r[7]), make_float2(wb.z, wb.w), s[c][3]);
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < NCH; ++c)
+        out[c] = ((s[c][0].x + s[c][0].y) + (s[c][1].x + s[c][1].y)) +
+                 ((s[c][2].x + s[c][2].y) + (s[c][3].x + s[c][3].y));
+}
+
+// Bounded wait that also gives up once another role has aborted. The thread sleeps
+// in the barrier between checks (about 1 ms at most per check).
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
                                               volatile int* abort_flag, int32_t* status) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0u) {
-            if (*abort_flag) return false;
-            if (global_ns() - t0 > 1000000000ull) {
-                *abort_flag = 1;
-                flag_status(status, DSA_STATUS_TIMEOUT);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > 1000000000ull) {
+            *abort_flag = 1;
+            flag_status(status, DSA_STATUS_TIMEOUT);
+            return false;
         }
     }
 }
@@ -146,9 +207,9 @@ struct Layout {
     static constexpr uint32_t kABytes = KA * kABox;                 // a stage
     static constexpr uint32_t kBBytes = KA * kBBox;
     static constexpr uint32_t kOffA = kBBytes;
-    static constexpr uint32_t kOffW = kOffA + kStages * kABytes;    // [warp][128] f32
-    static constexpr uint32_t kOffN = kOffW + kEpiWarps * 128 * 4;  // [warp][8] i32
-    static constexpr uint32_t kOffBar = kOffN + kEpiWarps * 8 * 4;
+    static constexpr uint32_t kOffW = kOffA + kStages * kABytes;    // per-warp weights, f32
+    static constexpr uint32_t kOffN = kOffW + kWTab * 4;            // [warp][8] i32
+    static constexpr uint32_t kOffBar = kOffN + 16 * 8 * 4;
     static constexpr int kBars = 2 * kStages + 2 + 4 + 1;
     static constexpr uint32_t kOffMisc = kOffBar + kBars * 8;
     static constexpr uint32_t kBytes = kOffMisc + 16;
@@ -156,16 +217,23 @@ struct Layout {
 };
 
 template <int KA, int HI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(block_threads(HI), 1)
     prefill_score_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB, PrefillArgs a) {
     using L = Layout<KA>;
     constexpr int S = L::kStages;
+    constexpr int EPW = epi_warps(HI);
+    constexpr int SLICES = EPW / 4;     // column slices per lane quarter
+    constexpr int CW = kTileN / SLICES; // columns per epilogue warp
+    constexpr int NCH = CW / 32;        // 32-column chunks per epilogue warp
     constexpr int QPT = kTileN / HI;    // queries per tile
-    constexpr int QPW = QPT / 2;        // queries per epilogue warp
+    constexpr int QPW = CW / HI;        // queries per epilogue warp
     constexpr int KSTEPS = KA * 4;      // MMAs of K = 16 per tile
-    constexpr uint32_t IDESC = idesc_bf16(kTileP, kTileN);
-    static_assert(HI % 32 == 0 && QPT >= 2, "index heads must be 32, 64 or 128");
+    // A negative scale negates the pooled keys inside the MMA (exact for bf16), so
+    // D = sign(scale) * <kpool, qidx> and the epilogue applies relu and |scale| only.
+    const uint32_t IDESC = idesc_bf16(kTileP, kTileN) | (a.neg ? (1u << 13) : 0u);
+    static_assert(HI % 32 == 0 && QPT >= 2 && QPW >= 1 && EPW * CW == kWTab,
+                  "index heads must be 32, 64 or 128");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -195,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bempty, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(accfull + b, 1);
-            mbar_init(accempty + b, kEpiWarps);
+            mbar_init(accempty + b, EPW);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -313,10 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---- epilogue ----
         const int e = warp - 2;
-        const int quarter = warp & 3;   // tensor-memory lanes 32*quarter .. +31
-        const int half = e >> 2;        // columns 128*half .. +127
-        float* wtab = wtab_all + e * 128;
+        const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
+        const int slice = e >> 2;      // columns CW*slice .. +CW-1
+        float* wtab = wtab_all + e * CW;
         int* ntab = ntab_all + e * 8;
+        const uint32_t wtab_s = smem_u32(wtab), ntab_s = smem_u32(ntab);
         const float NEG_INF = __int_as_float(0xff800000);
         const int Lseq = min(__ldg(a.seq_lens + a.seq), a.cap);
         int tc = 0;
@@ -325,15 +394,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qt = (int)(u / a.pchunks), pc = (int)(u % a.pchunks);
             const int t0 = pc * kTilesPerUnit, t1 = min(a.ptiles, t0 + kTilesPerUnit);
             // This warp's weights (w * |scale|) and visible-pool counts for the unit.
-            const long long wbase = (long long)qt * kTileN + half * 128;
+            const long long wbase = (long long)qt * kTileN + slice * CW;
             const long long wlim = (long long)a.rows * HI;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < NCH; ++i) {
                 const long long idx = wbase + lane + 32 * i;
                 wtab[lane + 32 * i] = idx < wlim ? __ldg(a.w + idx) * a.wscale : 0.f;
             }
             if (lane < QPW) {
-                const int r = qt * QPT + half * QPW + lane;
+                const int r = qt * QPT + slice * QPW + lane;
                 int nv = 0;
                 if (r < a.rows) {
                     const int ctx = a.row_ctx ? min(__ldg(a.row_ctx + r), Lseq) : Lseq;
@@ -342,10 +411,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ntab[lane] = nv;
             }
             __syncwarp();
+            // Pool flags are fetched one tile ahead, so their latency hides behind a
+            // tile of work.
+            const int prow = 32 * quarter + lane;
+            auto load_flag = [&](int t) -> int {
+                const int p = t * kTileP + prow;
+                return (t < t1 && p < a.pcap) ? (int)__ldg(a.pv + p) : 0;
+            };
+            int flag_next = load_flag(t0);
             for (int t = t0; t < t1; ++t, ++tc) {
                 const int buf = tc & 1;
-                const int p = t * kTileP + 32 * quarter + lane;
-                const bool flag = p < a.pcap && __ldg(a.pv + p) != 0;
+                const int p = t * kTileP + prow;
+                const bool flag = flag_next != 0;
+                flag_next = load_flag(t + 1);
                 // One lane waits and the warp follows its verdict, so the warp-wide
                 // tensor-memory loads below are always reached by all lanes together.
                 int got = 1;
@@ -357,47 +435,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tb =
-                    tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kTileN + half * 128);
-                uint32_t v[2][32];
-                tc_ld32(v[0], tb);
+                const uint32_t tb = tmem + ((uint32_t)(32 * quarter) << 16) +
+                                    (uint32_t)(buf * kTileN + slice * CW);
+                uint32_t v[NCH][32];
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) tc_ld32(v[ch], tb + 32u * ch);
                 tc_wait_ld(v[0]);
+#pragma unroll
+                for (int ch = 1; ch < NCH; ++ch) tc_tie(v[ch]);
+                float cs[NCH];
+                chunk_sums<NCH>(v, wtab_s, cs);
                 float acc = 0.f;
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    if (ch + 1 < 4) tc_ld32(v[(ch + 1) & 1], tb + 32u * (ch + 1));
-                    const uint32_t* x = v[ch & 1];
-                    const float4* w4 = reinterpret_cast<const float4*>(wtab + 32 * ch);
-                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-                    if (a.neg) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 ww = w4[i];
-                            s0 = fmaf(fmaxf(-__uint_as_float(x[4 * i]), 0.f), ww.x, s0);
-                            s1 = fmaf(fmaxf(-__uint_as_float(x[4 * i + 1]), 0.f), ww.y, s1);
-                            s2 = fmaf(fmaxf(-__uint_as_float(x[4 * i + 2]), 0.f), ww.z, s2);
-                            s3 = fmaf(fmaxf(-__uint_as_float(x[4 * i + 3]), 0.f), ww.w, s3);
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 ww = w4[i];
-                            s0 = fmaf(fmaxf(__uint_as_float(x[4 * i]), 0.f), ww.x, s0);
-                            s1 = fmaf(fmaxf(__uint_as_float(x[4 * i + 1]), 0.f), ww.y, s1);
-                            s2 = fmaf(fmaxf(__uint_as_float(x[4 * i + 2]), 0.f), ww.z, s2);
-                            s3 = fmaf(fmaxf(__uint_as_float(x[4 * i + 3]), 0.f), ww.w, s3);
-                        }
-                    }
-                    acc += (s0 + s1) + (s2 + s3);
+                for (int ch = 0; ch < NCH; ++ch) {
+                    acc += cs[ch];
                     if ((32 * (ch + 1)) % HI == 0) {  // the chunk ends a query
-                        const int jl = (32 * ch) / HI;  // query within this warp's half
-                        const int r = qt * QPT + half * QPW + jl;
+                        const int jl = (32 * ch) / HI;  // query within this warp's slice
+                        const int r = qt * QPT + slice * QPW + jl;
                         if (r < a.rows && p < a.p_stride)
                             a.scores[(long long)r * a.p_stride + p] =
-                                (flag && p < ntab[jl]) ? acc : NEG_INF;
+                                (flag && p < lds_s32(ntab_s + 4u * jl)) ? acc : NEG_INF;
                         acc = 0.f;
                     }
-                    if (ch + 1 < 4) tc_wait_ld(v[(ch + 1) & 1]);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -428,7 +487,7 @@ int launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const PrefillArgs& a,
     constexpr uint32_t bytes = Layout<KA>::kDynBytes;
     int rc = set_max_smem((const void*)prefill_score_kernel<KA, HI>, (int)bytes);
     if (rc) return rc;
-    prefill_score_kernel<KA, HI><<<grid, kThreads, bytes, st>>>(tmA, tmB, a);
+    prefill_score_kernel<KA, HI><<<grid, block_threads(HI), bytes, st>>>(tmA, tmB, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_score_prefill launch");
     return DSA_OK;

@@ -397,11 +397,14 @@ def long_262k(seed: int = 3, seq_len: Optional[int] = None, **kw) -> Workload:
                          invalid_per_seq=(S * 2621 + 131072) // 262144, **kw)
 
 
-def prefill_chunk(seed: int = 4, **kw) -> Workload:
+def prefill_chunk(seed: int = 4, rows: Optional[int] = None, **kw) -> Workload:
     """Chunked prefill: 4,096 query rows; row i sees the first 126,977 + i of
-    131,072 tokens."""
-    return make_workload("prefill-Q4096-S131072", seed, Geometry(**GLM53), [131072],
-                         rows_ctx=[126977 + i for i in range(4096)], **kw)
+    131,072 tokens. ``rows`` keeps only the last rows of the chunk (same context
+    lengths as in the full chunk) for profiling."""
+    n = rows or 4096
+    name = "prefill-Q4096-S131072" if rows is None else f"prefill-Q{n}-S131072"
+    return make_workload(name, seed, Geometry(**GLM53), [131072],
+                         rows_ctx=[126977 + i for i in range(4096 - n, 4096)], **kw)
 
 
 WORKLOADS = {0: tiny, 1: single_32k, 2: paged_batch, 3: long_262k, 4: prefill_chunk}
