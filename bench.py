@@ -38,6 +38,9 @@ sys.path.insert(0, ROOT)
 from sparse_attention_decode_kpool_gb300 import workloads as W  # noqa: E402
 
 METRIC = "DSA decode queries/s (select + sparse MLA) at 262K ctx; % of HBM roofline"
+PREFILL_METRIC = ("DSA chunked-prefill query rows/s (tensor-core index scores + select + expand "
+                  "+ sparse latent attention to olat); % of bf16 tensor peak")
+PREFILL_WORKLOAD = 4  # scored on the tensor cores; the o_absorb GEMM is not in its step
 FLUSH_BYTES = 256 << 20
 
 
@@ -174,6 +177,18 @@ def algorithmic_bytes(wl, layer) -> dict:
             "candidate_pools": cand}
 
 
+def algorithmic_flops(wl, layer) -> dict:
+    """Per step of the prefill chunk: the dense index-score contraction over every
+    pool of the row stride (2 * rows * heads * p_stride * ihd) and the sparse
+    attention over the selected tokens (QK and PV: 4 * heads * 512 per token)."""
+    g = wl.geom
+    sel_tokens = int((layer.token_ids >= 0).sum().item())
+    score = 2.0 * wl.rows * g.index_heads * wl.p_stride * g.index_head_dim
+    attend = 4.0 * g.heads * g.kv_lora_rank * sel_tokens
+    return {"score": score, "attend": attend, "total": score + attend,
+            "selected_tokens": sel_tokens}
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing (the cpu_baseline leg and the reference arm)
 
@@ -182,10 +197,11 @@ class OracleRunner:
     """Times the oracle's decode_row on rows of the workload. The oracle's own
     pooled-key cache of a sequence is built once, untimed (it is layer state)."""
 
-    def __init__(self, wl):
+    def __init__(self, wl, with_project: bool = True):
         from oracle import dsa_oracle as O
 
         self.O, self.wl = O, wl
+        self.with_project = with_project
         self._pools = {}
         self._A = None
 
@@ -209,7 +225,7 @@ class OracleRunner:
                                            self._tokens(wl.valid, b), wl.ape.numpy(), f(wl.ln_w),
                                            f(wl.ln_b), g.eps, g.first_key, g.index_kpool)
             self._pools[b] = (keys, pv, self._tokens(wl.ckv, b))
-        if self._A is None and wl.o_absorb is not None:
+        if self._A is None and wl.o_absorb is not None and self.with_project:
             self._A = wl.o_absorb.float().numpy()
         return b
 
@@ -228,7 +244,8 @@ class OracleRunner:
 
 
 def cpu_baseline(wl, budget_s: float = 12.0, max_rows: int = 2) -> dict:
-    runner = OracleRunner(wl)
+    prefill = wl.name.startswith("prefill")
+    runner = OracleRunner(wl, with_project=not prefill)
     times, rows = [], []
     for r in range(min(max_rows, wl.rows)):
         runner._prep(r)
@@ -238,14 +255,15 @@ def cpu_baseline(wl, budget_s: float = 12.0, max_rows: int = 2) -> dict:
             break
     # Repeat the prepared rows until the time budget is used.
     i = 0
-    while sum(times) < budget_s and i < 50:
+    while sum(times) < budget_s and i < 5000:
         times.append(runner.run_row(rows[i % len(rows)]))
         i += 1
     v = len(times) / sum(times)
+    tail = "olat (no o_absorb, as the GPU step)" if prefill else "o_absorb"
     return {"value": v, "unit": "queries/s", "cores": 1, "kind": "oracle",
-            "sample": f"{len(times)} decode rows (sequences {rows}) of {wl.name}: score over all "
+            "sample": f"{len(times)} query rows (rows {rows}) of {wl.name}: score over all "
                       f"{wl.p_stride} pools, top-k, expand, attention over the selected tokens, "
-                      f"o_absorb; float64 numpy, one thread; pooled-key cache built untimed",
+                      f"{tail}; float64 numpy, one thread; pooled-key cache built untimed",
             "seconds": sum(times)}
 
 
@@ -256,7 +274,8 @@ def run_reference(args, ws, rank):
     if rank != 0:
         return
     wl = W.WORKLOADS[args.workload]()
-    runner = OracleRunner(wl)
+    prefill = args.workload == PREFILL_WORKLOAD
+    runner = OracleRunner(wl, with_project=not prefill)
     rows = [r % wl.rows for r in range(min(2, wl.rows))]
     for r in rows:
         runner._prep(r)
@@ -266,13 +285,14 @@ def run_reference(args, ws, rank):
     total = sum(ts)
     v = args.steps / total
     line = {
-        "impl": "reference", "metric": METRIC, "value": v, "unit": "queries/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": PREFILL_METRIC if prefill else METRIC, "value": v,
+        "unit": "queries/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": workload_config(wl, args),
         "cpu_baseline": {"value": v, "unit": "queries/s", "cores": 1, "kind": "oracle",
-                         "sample": f"one decode query row per step (rows {rows}) of {wl.name}"},
+                         "sample": f"one query row per step (rows {rows}) of {wl.name}"},
         "e2e": {"value": v, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -320,7 +340,9 @@ def main():
 
     wl = (W.long_262k(seq_len=args.seq_len) if (args.seq_len and args.workload == 3)
           else W.WORKLOADS[args.workload]())
-    layer = DsaDecodeLayer(wl, device=str(dev))
+    prefill = args.workload == PREFILL_WORKLOAD
+    # The prefill chunk's step ends at olat (its o_absorb GEMM is not part of it).
+    layer = DsaDecodeLayer(wl, device=str(dev), with_o_absorb=not prefill, keep_olat=prefill)
     layer.compress()
     torch.cuda.synchronize()
 
@@ -363,9 +385,10 @@ def main():
         layer.step()
     # A second graph with timing event nodes at the stage boundaries (external
     # events when the installed torch supports them): per-stage times.
-    stage_names = ["score", "select", "expand", "attend", "project"]
+    stage_names = ["score", "select", "expand", "attend"] + ([] if prefill else ["project"])
+    ns = len(stage_names)
     try:
-        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(ns + 1)]
         graph_events = True
     except TypeError:
         ev, graph_events = None, False
@@ -374,11 +397,9 @@ def main():
         sgraph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(sgraph):
             ev[0].record()
-            layer.score(); ev[1].record()
-            layer.select(); ev[2].record()
-            layer.expand(); ev[3].record()
-            layer.attend(); ev[4].record()
-            layer.project(); ev[5].record()
+            for j, k in enumerate(stage_names):
+                getattr(layer, k)()
+                ev[j + 1].record()
 
     launches = layer.launches_per_step()
     for _ in range(args.warmup):
@@ -407,15 +428,16 @@ def main():
         flush.zero_()
         if graph_events:
             sgraph.replay()
-            ev[5].synchronize()
+            ev[ns].synchronize()
             for j, k in enumerate(stage_names):
                 stage_ms[k] += ev[j].elapsed_time(ev[j + 1])
         else:
-            ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-            ev2[0].record(); layer.score(); ev2[1].record(); layer.select(); ev2[2].record()
-            layer.expand(); ev2[3].record(); layer.attend(); ev2[4].record()
-            layer.project(); ev2[5].record()
-            ev2[5].synchronize()
+            ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)]
+            ev2[0].record()
+            for j, k in enumerate(stage_names):
+                getattr(layer, k)()
+                ev2[j + 1].record()
+            ev2[ns].synchronize()
             for j, k in enumerate(stage_names):
                 stage_ms[k] += ev2[j].elapsed_time(ev2[j + 1])
     stage_ms = {k: v / args.steps for k, v in stage_ms.items()}
@@ -430,7 +452,8 @@ def main():
         h_w = wl.w.pin_memory()
         h_qlat = wl.qlat.pin_memory()
         h_ctx = torch.from_numpy(wl.row_ctx).pin_memory()
-        h_y = torch.empty_like(layer.y, device="cpu").pin_memory()
+        result = layer.olat if prefill else layer.y
+        h_y = torch.empty_like(result, device="cpu").pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in (h_qidx, h_w, h_qlat, h_ctx))
         d2h = h_y.numel() * h_y.element_size()
         for _ in range(3):
@@ -447,13 +470,14 @@ def main():
             layer.qlat.copy_(h_qlat, non_blocking=True)
             layer.row_ctx.copy_(h_ctx, non_blocking=True)
             graph.replay()
-            h_y.copy_(layer.y, non_blocking=True)
+            h_y.copy_(result, non_blocking=True)
             torch.cuda.synchronize()
             t_e2e.append(time.perf_counter() - t0)
         e2e_ms = max_over_ranks(1e3 * sum(t_e2e) / len(t_e2e), ws)
         e2e = {"value": queries / (e2e_ms * 1e-3), "unit": "queries/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "path": "pinned host qidx/w/qlat/row_ctx -> device, graph replay, y -> host"}
+               "path": "pinned host qidx/w/qlat/row_ctx -> device, graph replay, "
+                       + ("olat" if prefill else "y") + " -> host"}
 
     if rank != 0:
         return
@@ -462,25 +486,42 @@ def main():
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk):
         peaks = json.load(open(pk))
-    hbm = peaks.get("hbm_gbs")
-    peak_src = "measured" if hbm else "fallback"
-    hbm = hbm or 6800.0
-    ab = algorithmic_bytes(wl, layer)
-    dom = max(("score", "attend", "project"), key=lambda k: stage_ms[k])
-    dom_bytes = ab[dom]
-    achieved = dom_bytes / (stage_ms[dom] * 1e-3) / 1e9
-    total_gbs = ab["total"] / (ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": None, "peak_source": peak_src,
-                "kernel": {"attend": "dsa_sparse_mla_decode (split attention + combine)",
-                           "project": "dsa_latent_project (TMA-pipelined o_absorb GEMM + "
-                                      "partial sum)",
-                           "score": "dsa_score"}[dom],
-                "algorithmic_bytes_per_launch": dom_bytes,
-                "step_algorithmic_bytes": ab["total"], "step_achieved_gbs": total_gbs,
-                "step_frac": total_gbs / hbm}
+    if prefill:
+        tf = peaks.get("bf16_tflops")
+        peak_src = "measured (bf16 dense burst)" if tf else "fallback"
+        tf = tf or 1900.0
+        fl = algorithmic_flops(wl, layer)
+        dom = max(("score", "attend"), key=lambda k: stage_ms[k])
+        achieved = fl[dom] / (stage_ms[dom] * 1e-3) / 1e12
+        step_tf = fl["total"] / (ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": tf, "unit": "TFLOP/s",
+                    "frac": achieved / tf, "traffic": None, "peak_source": peak_src,
+                    "kernel": {"score": "dsa_score_prefill (tcgen05 contraction, TMEM epilogue)",
+                               "attend": "dsa_sparse_mla_decode (split attention)"}[dom],
+                    "algorithmic_flops_per_launch": fl[dom], "step_algorithmic_flops": fl["total"],
+                    "step_achieved_tflops": step_tf, "step_frac": step_tf / tf,
+                    "stage_tflops": {k: fl[k] / (stage_ms[k] * 1e-3) / 1e12
+                                     for k in ("score", "attend")}}
+    else:
+        hbm = peaks.get("hbm_gbs")
+        peak_src = "measured" if hbm else "fallback"
+        hbm = hbm or 6800.0
+        ab = algorithmic_bytes(wl, layer)
+        dom = max(("score", "attend", "project"), key=lambda k: stage_ms[k])
+        dom_bytes = ab[dom]
+        achieved = dom_bytes / (stage_ms[dom] * 1e-3) / 1e9
+        total_gbs = ab["total"] / (ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                    "frac": achieved / hbm, "traffic": None, "peak_source": peak_src,
+                    "kernel": {"attend": "dsa_sparse_mla_decode (split attention + combine)",
+                               "project": "dsa_latent_project (TMA-pipelined o_absorb GEMM + "
+                                          "partial sum)",
+                               "score": "dsa_score"}[dom],
+                    "algorithmic_bytes_per_launch": dom_bytes,
+                    "step_algorithmic_bytes": ab["total"], "step_achieved_gbs": total_gbs,
+                    "step_frac": total_gbs / hbm}
     line = {
-        "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": ws, "steps": args.steps,
+        "metric": PREFILL_METRIC if prefill else METRIC, "value": value, "unit": "queries/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(wl, args),
