@@ -231,7 +231,8 @@ int dsa_expand(const int32_t* pool_ids, int rows, int sk, int first_key, int kpo
  * seq_lens of the row's sequence); o_absorb [hidden, heads*kv_lora_rank] bf16
  * (nullable: then y must be NULL and only olat is produced); y [rows, hidden]
  * bf16; olat [rows, heads, kv_lora_rank] f32 (nullable).
- * Limits: kv_lora_rank == 512; hidden % 32 == 0; heads >= 1.
+ * Limits: kv_lora_rank == 512; hidden % 32 == 0; heads >= 1; qlat, ckv, o_absorb,
+ * y, olat and workspace 16-byte aligned (DSA_ERR_INVALID_ARG otherwise).
  */
 int dsa_sparse_mla_decode_workspace(int rows, int heads, int kv_lora_rank, int out_width,
                                     int hidden, int with_o_absorb, size_t* bytes);
@@ -255,7 +256,8 @@ int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, int kv_lora
  * timed apart; the two-call form gives results identical to the one-call form.
  * olat [rows, heads*kv_lora_rank] f32 (rounded to bf16 as the MMA operand);
  * o_absorb [hidden, heads*kv_lora_rank] bf16; y [rows, hidden] bf16; status as
- * above (DSA_STATUS_TIMEOUT only). Limits: kv_lora_rank == 512; hidden % 64 == 0.
+ * above (DSA_STATUS_TIMEOUT only). Limits: kv_lora_rank == 512; hidden % 64 == 0;
+ * olat, o_absorb, y and workspace 16-byte aligned (DSA_ERR_INVALID_ARG otherwise).
  */
 int dsa_latent_project_workspace(int rows, int heads, int kv_lora_rank, int hidden,
                                  size_t* bytes);

@@ -2,6 +2,7 @@
 // dsa_expand (expand_selection).
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 
 #include <atomic>
 #include <mutex>
@@ -53,6 +54,14 @@ int set_max_smem(const void* kernel, int bytes) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     done.insert(key);
     return DSA_OK;
+}
+
+bool pdl_enabled() {
+    static const bool on = []() {
+        const char* v = getenv("DSA_PDL");
+        return !(v && v[0] == '0');
+    }();
+    return on;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -120,6 +129,7 @@ int check_paging(const dsa_paging* pg, int kpool, Paging* out) {
 __global__ void expand_kernel(const int32_t* __restrict__ pool_ids, int rows, int sk,
                               int first_key, int kpool, int out_width,
                               int32_t* __restrict__ token_ids) {
+    pdl_wait();
     long long n = (long long)rows * out_width;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
@@ -193,9 +203,10 @@ int dsa_expand(const int32_t* pool_ids, int rows, int sk, int first_key, int kpo
     int cap = sm_count() * 8;
     if (cap < 1) cap = 1024;
     if (blocks > cap) blocks = cap;
-    expand_kernel<<<(int)blocks, threads, 0, (cudaStream_t)stream>>>(
-        pool_ids, rows, sk, first_key, kpool, out_width, token_ids);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(expand_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+                               (cudaStream_t)stream, pool_ids, rows, sk, first_key, kpool,
+                               out_width, token_ids);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_expand launch");
     return DSA_OK;
 }

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "dsa.h"
 
 namespace dsa {
@@ -17,6 +19,30 @@ int fail(int code, const char* fmt, ...);  // records the message, returns code
 int cuda_fail(cudaError_t e, const char* what);
 int sm_count();                            // SMs of the current device (cached)
 int set_max_smem(const void* kernel, int bytes);  // once per (device, kernel)
+
+// Programmatic dependent launch. Every kernel of the library is launched as a
+// programmatic dependent of the work before it on the stream, and waits for that
+// work (pdl_wait) before it touches global memory, so only the launch and the
+// kernel's prologue overlap the predecessor's completion. No kernel triggers its
+// dependents early: blocks of a dependent waiting beside a running grid slowed it.
+// DSA_PDL=0 in the environment turns the attribute off (the wait then returns at
+// once).
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Kernel-side copy of dsa_paging.
 struct Paging {
@@ -111,6 +137,12 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
+
+// ---- programmatic dependent launch -------------------------------------------
+
+// Blocks until the grids this one depends on have completed and their memory is
+// visible (returns at once when launched without the attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 
 // ---- mbarrier + bulk async copy (TMA engine, non-tensor form) ----------------
 

@@ -38,6 +38,7 @@ constexpr int kThreads = 256;
 
 template <int IHD, int KPMAX>
 __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
+    pdl_wait();
     constexpr int LPP = IHD / 8;     // lanes per pool
     constexpr int PPW = 32 / LPP;    // pools per warp
     constexpr int PPC = PPW * (kThreads / 32);
@@ -189,7 +190,8 @@ int launch(const CompressArgs& a, int pmax, cudaStream_t st) {
     if (grid.x == 0) return DSA_OK;
     if (grid.x > 0x7fffffffu || grid.y > 65535u)
         return fail(DSA_ERR_UNSUPPORTED, "dsa_compress: grid too large");
-    compress_kernel<IHD, KPMAX><<<grid, kThreads, 0, st>>>(a);
+    cudaError_t le = launch_pdl(compress_kernel<IHD, KPMAX>, dim3(grid), dim3(kThreads), 0, st, a);
+    if (le != cudaSuccess) return cuda_fail(le, "dsa_compress launch");
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_compress launch");
     return DSA_OK;

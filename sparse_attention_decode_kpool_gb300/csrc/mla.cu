@@ -29,6 +29,7 @@ namespace {
 
 constexpr int KVL = DSA_KV_LORA_RANK;  // 512
 constexpr int CH = 64;                 // tokens per gathered chunk
+constexpr int kMaxSplits = 64;         // token splits per row (make_plan's bound)
 constexpr int ROWB = KVL * 2;          // bytes per latent row
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -66,6 +67,7 @@ constexpr int split_smem_bytes() {
 
 template <int MT>
 __global__ void __launch_bounds__(MT * 64, 1) mla_split_kernel(MlaArgs a) {
+    pdl_wait();
     constexpr int NW = 2 * MT;
     constexpr int NTH = NW * 32;
     constexpr int HP = 16 * MT;
@@ -319,32 +321,68 @@ __global__ void __launch_bounds__(MT * 64, 1) mla_split_kernel(MlaArgs a) {
     }
 }
 
-// One CTA per (head, row): merge the splits with log-sum-exp weights.
+// One CTA per (head, row): merge the splits with log-sum-exp weights. The splits'
+// (m, l) pairs are read once into shared memory as weights 2^(m_s - M); the partial
+// outputs are then summed in split order, eight independent 16-byte loads in flight
+// per thread.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restrict__ part_o,
                                                           const float* __restrict__ part_ml,
                                                           int heads, int ns, float* olat,
                                                           uint16_t* xbf) {
+    pdl_wait();
+    __shared__ float wsh[kMaxSplits];
+    __shared__ float lsum;
     const int h = blockIdx.x, r = blockIdx.y, t = threadIdx.x;
-    float M = -INFINITY;
-    for (int s = 0; s < ns; ++s)
-        M = fmaxf(M, __ldg(part_ml + (((long long)r * ns + s) * heads + h) * 2));
+    if (t < 32) {
+        float m[2], l[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int s = t + 32 * k;
+            m[k] = -INFINITY;
+            l[k] = 0.f;
+            if (s < ns) {
+                const float2 ml = __ldg(reinterpret_cast<const float2*>(part_ml) +
+                                        ((long long)r * ns + s) * heads + h);
+                m[k] = ml.x;
+                l[k] = ml.y;
+            }
+        }
+        float M = fmaxf(m[0], m[1]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = 0.f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float wgt = m[k] == -INFINITY ? 0.f : exp2f(m[k] - M);
+            L += wgt * l[k];
+            if (t + 32 * k < ns) wsh[t + 32 * k] = wgt;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        if (t == 0) lsum = L;
+    }
+    __syncthreads();
+    const long long stride = (long long)heads * (KVL / 4);  // float4s between splits
+    const float4* po = reinterpret_cast<const float4*>(part_o) +
+                       ((long long)r * ns * heads + h) * (KVL / 4) + t;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float Ls = 0.f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < ns; ++s) {
-            const long long idx = ((long long)r * ns + s) * heads + h;
-            const float m = __ldg(part_ml + idx * 2);
-            const float l = __ldg(part_ml + idx * 2 + 1);
-            const float wgt = exp2f(m - M);
-            Ls += wgt * l;
-            const float4 o = __ldg(reinterpret_cast<const float4*>(part_o + idx * KVL) + t);
-            acc.x += wgt * o.x;
-            acc.y += wgt * o.y;
-            acc.z += wgt * o.z;
-            acc.w += wgt * o.w;
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+        float4 o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            o[j] = s0 + j < ns ? __ldg(po + (s0 + j) * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (s0 + j < ns) {
+                const float wgt = wsh[s0 + j];
+                acc.x += wgt * o[j].x;
+                acc.y += wgt * o[j].y;
+                acc.z += wgt * o[j].z;
+                acc.w += wgt * o[j].w;
+            }
         }
     }
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     acc.x *= inv;
     acc.y *= inv;
     acc.z *= inv;
@@ -407,6 +445,7 @@ __device__ __forceinline__ void gemv_step(float (&acc)[kGemvMT][NT][4],
 
 template <int NT>
 __global__ void __launch_bounds__(kGemvWarps * 32) oabs_gemv_kernel(GemvArgs a) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -474,6 +513,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) oabs_gemv_kernel(GemvArgs a) 
 
 __global__ void ysum_kernel(const float* __restrict__ ypart, int KS, long long n,
                             uint16_t* __restrict__ y) {
+    pdl_wait();
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
         float s = 0.f;
@@ -508,7 +548,7 @@ Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms)
     long long ns = base > 0 ? (sms + base - 1) / base : 1;
     if (ns < 1) ns = 1;
     if (ns > max_ns) ns = max_ns;
-    if (ns > 64) ns = 64;
+    if (ns > kMaxSplits) ns = kMaxSplits;
     const int per = ow > 0 ? (int)((ow + ns - 1) / ns) : 0;
     p.tps = per > 0 ? ((per + CH - 1) / CH) * CH : CH;
     p.ns = ow > 0 ? (ow + p.tps - 1) / p.tps : 1;
@@ -562,14 +602,16 @@ int launch_split(const MlaArgs& a, const Plan& p, cudaStream_t st) {
     int rc = set_max_smem((const void*)mla_split_kernel<MT>, smem);
     if (rc) return rc;
     dim3 grid(p.ns, a.rows, p.hgroups);
-    mla_split_kernel<MT><<<grid, MT * 64, smem, st>>>(a);
+    cudaError_t e = launch_pdl(mla_split_kernel<MT>, grid, dim3(MT * 64), smem, st, a);
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_mla_decode split launch");
     return DSA_OK;
 }
 
 template <int NT>
 void launch_gemv(GemvArgs g, cudaStream_t st) {
     const int units = g.n_mg * g.KS;
-    oabs_gemv_kernel<NT><<<(units + kGemvWarps - 1) / kGemvWarps, kGemvWarps * 32, 0, st>>>(g);
+    launch_pdl(oabs_gemv_kernel<NT>, dim3((units + kGemvWarps - 1) / kGemvWarps),
+               dim3(kGemvWarps * 32), 0, st, g);
 }
 
 }  // namespace
@@ -609,7 +651,7 @@ extern "C" int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, 
     if (!qlat || !ckv || (out_width > 0 && !token_ids))
         return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_mla_decode: NULL tensor");
     if ((((uintptr_t)qlat) | ((uintptr_t)ckv) | ((uintptr_t)o_absorb) | ((uintptr_t)olat) |
-         ((uintptr_t)workspace)) & 15)
+         ((uintptr_t)y) | ((uintptr_t)workspace)) & 15)
         return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_mla_decode: tensors must be 16-byte aligned");
     const int sms = sm_count();
     if (sms <= 0) return fail(DSA_ERR_CUDA, "dsa_sparse_mla_decode: no CUDA device");
@@ -648,9 +690,9 @@ extern "C" int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_mla_decode split launch");
     if (p.ns > 1) {
-        mla_combine_kernel<<<dim3(heads, rows), 128, 0, st>>>(a.part_o, a.part_ml, heads, p.ns,
-                                                              olat, a.xbf);
-        e = cudaGetLastError();
+        e = launch_pdl(mla_combine_kernel, dim3(heads, rows), dim3(128), 0, st,
+                       (const float*)a.part_o, (const float*)a.part_ml, heads, p.ns, olat, a.xbf);
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_mla_decode combine launch");
     }
     if (p.tma_proj) {
@@ -682,8 +724,9 @@ extern "C" int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, 
         const long long n = (long long)rows * hidden;
         long long blocks = (n + 255) / 256;
         if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
-        ysum_kernel<<<(int)blocks, 256, 0, st>>>(g.ypart, p.KS, n, y);
-        e = cudaGetLastError();
+        e = launch_pdl(ysum_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                       (const float*)g.ypart, p.KS, n, (uint16_t*)y);
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_mla_decode ysum launch");
     }
     return DSA_OK;

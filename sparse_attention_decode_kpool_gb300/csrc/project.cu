@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NT))
     const long long G = gridDim.x;
     const long long u0 = unit_begin(blockIdx.x, a.U, G);
     const long long u1 = unit_begin(blockIdx.x + 1, a.U, G);
+    pdl_wait();
 
     if (tid == 0) {
         for (int s = 0; s < C::S; ++s) {
@@ -199,27 +200,53 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NT))
     if (cur_mb >= 0) flush(cur_mb);
 }
 
-// y[r, col] = bf16(sum over the CTAs that covered row block col/64 of their partial).
+// y[r, col] = bf16(sum over the CTAs that covered row block col/64 of their partial),
+// the CTAs in ascending order. One thread per 4 columns; the contributing CTAs are
+// read four at a time so their loads overlap.
 __global__ void project_reduce_kernel(const float* __restrict__ ypart, long long U, int KB, int G,
                                       int J, int R, int hidden, uint16_t* __restrict__ y) {
-    const long long n = (long long)R * hidden;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-         i += (long long)gridDim.x * blockDim.x) {
+    pdl_wait();
+    const long long n4 = (long long)R * hidden / 4;
+    for (long long i4 = blockIdx.x * (long long)blockDim.x + threadIdx.x; i4 < n4;
+         i4 += (long long)gridDim.x * blockDim.x) {
+        const long long i = 4 * i4;
         const int r = (int)(i / hidden);
         const int col = (int)(i % hidden);
         const long long mb = col / MROWS;
         const long long lo = mb * KB, hi = lo + KB;
         long long c = lo * G / U;
         while (c > 0 && unit_begin(c, U, G) > lo) --c;
-        float s = 0.f;
-        for (; c < G; ++c) {
-            const long long b0 = unit_begin(c, U, G), b1 = unit_begin(c + 1, U, G);
-            if (b0 >= hi) break;
-            if (b1 <= lo || b1 == b0) continue;
-            const int j = (int)(mb - b0 / KB);
-            s += __ldg(ypart + (((long long)c * J + j) * R + r) * MROWS + (col % MROWS));
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (; c < G; c += 4) {
+            float4 v[4];
+            bool use[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const long long cc = c + k;
+                const long long b0 = unit_begin(cc, U, G), b1 = unit_begin(cc + 1, U, G);
+                use[k] = cc < G && b0 < hi && b1 > lo && b1 > b0;
+                v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (use[k]) {
+                    const int j = (int)(mb - b0 / KB);
+                    v[k] = __ldg(reinterpret_cast<const float4*>(
+                        ypart + ((cc * J + j) * R + r) * MROWS + (col % MROWS)));
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (use[k]) {
+                    s.x += v[k].x;
+                    s.y += v[k].y;
+                    s.z += v[k].z;
+                    s.w += v[k].w;
+                }
+            }
+            if (c + 4 >= G || unit_begin(c + 4, U, G) >= hi) break;
         }
-        y[i] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+        uint2 o;
+        o.x = pack_bf16x2(s.x, s.y);
+        o.y = pack_bf16x2(s.z, s.w);
+        *reinterpret_cast<uint2*>(y + i) = o;
     }
 }
 
@@ -256,7 +283,9 @@ int launch_proj(const ProjArgs& a, int G, cudaStream_t st) {
     rc = make_tmap_2d(&tmX, XF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                       a.X, (uint64_t)a.K, (uint64_t)a.R, (uint64_t)a.K * C::XB, KT, 8 * NT);
     if (rc) return rc;
-    project_kernel<NT, XF32><<<G, kThreads, C::SMEM, st>>>(tmA, tmX, a);
+    cudaError_t e = launch_pdl(project_kernel<NT, XF32>, dim3(G), dim3(kThreads), C::SMEM, st,
+                               tmA, tmX, a);
+    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
     return DSA_OK;
 }
 
@@ -302,12 +331,12 @@ int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "projection launch");
-    const long long n = (long long)rows * hidden;
-    long long blocks = (n + 255) / 256;
+    const long long n4 = (long long)rows * hidden / 4;
+    long long blocks = (n4 + 255) / 256;
     if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
-    project_reduce_kernel<<<(int)blocks, 256, 0, st>>>(static_cast<float*>(ws), p.U, p.KB, p.G,
-                                                       p.J, rows, hidden, y);
-    e = cudaGetLastError();
+    e = launch_pdl(project_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                   (const float*)ws, p.U, p.KB, p.G, p.J, rows, hidden, (uint16_t*)y);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "projection reduce launch");
     return DSA_OK;
 }
@@ -347,7 +376,7 @@ extern "C" int dsa_latent_project(const float* olat, int rows, int heads, int kv
                     hidden);
     if (rows == 0) return DSA_OK;
     if (!olat || !o_absorb || !y) return fail(DSA_ERR_INVALID_ARG, "dsa_latent_project: NULL tensor");
-    if ((((uintptr_t)olat) | ((uintptr_t)o_absorb) | ((uintptr_t)workspace)) & 15)
+    if ((((uintptr_t)olat) | ((uintptr_t)o_absorb) | ((uintptr_t)y) | ((uintptr_t)workspace)) & 15)
         return fail(DSA_ERR_INVALID_ARG, "dsa_latent_project: tensors must be 16-byte aligned");
     return project_launch(olat, true, rows, heads * kv_lora_rank, o_absorb, hidden, y, status,
                           workspace, workspace_bytes, (cudaStream_t)stream);

@@ -47,6 +47,7 @@ constexpr int kWarps = 4;
 template <int IHD, int NT>
 __global__ void __launch_bounds__(kWarps * 32) score_kernel(ScoreArgs a) {
     constexpr int NV = IHD / 32;  // 16-byte vectors per row per lane
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int g = lane >> 2;
@@ -213,6 +214,7 @@ __global__ void __launch_bounds__(kTmaThreads, kCtasPerSm) score_tma_kernel(Scor
     const int spr = (a.p_stride + kStagePools - 1) / kStagePools;  // stages per row
     const long long U = (long long)a.rows * spr;
     const long long G = gridDim.x;
+    pdl_wait();
     const long long u0 = blockIdx.x * U / G, u1 = (blockIdx.x + 1) * U / G;
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -412,8 +414,8 @@ int launch_tma(const ScoreArgs& a0, cudaStream_t st) {
     const long long U = (long long)a.rows * spr;
     const long long slots = (long long)sm_count() * kCtasPerSm;
     const int G = (int)(U < slots ? U : slots);
-    score_tma_kernel<IHD, NT><<<G, kTmaThreads, smem, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(score_tma_kernel<IHD, NT>, dim3(G), dim3(kTmaThreads), smem, st, a);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_score launch");
     return DSA_OK;
 }
@@ -431,8 +433,8 @@ int launch(const ScoreArgs& a0, cudaStream_t st) {
     const long long warps_per_row = (ntiles + a.tiles_per_warp - 1) / a.tiles_per_warp;
     dim3 grid((unsigned)((warps_per_row + kWarps - 1) / kWarps), a.rows);
     if (grid.y > 65535u) return fail(DSA_ERR_UNSUPPORTED, "dsa_score: rows %d > 65535", a.rows);
-    score_kernel<IHD, NT><<<grid, kWarps * 32, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(score_kernel<IHD, NT>, grid, dim3(kWarps * 32), 0, st, a);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_score launch");
     return DSA_OK;
 }

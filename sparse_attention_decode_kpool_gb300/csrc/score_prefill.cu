@@ -254,6 +254,7 @@ __global__ void __launch_bounds__(block_threads(HI), 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full + s, 1);
@@ -476,6 +477,7 @@ __global__ void __launch_bounds__(block_threads(HI), 1)
 }
 
 __global__ void fill_neg_inf_kernel(float* scores, long long n) {
+    pdl_wait();
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x)
         scores[i] = __int_as_float(0xff800000);
@@ -487,8 +489,9 @@ int launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const PrefillArgs& a,
     constexpr uint32_t bytes = Layout<KA>::kDynBytes;
     int rc = set_max_smem((const void*)prefill_score_kernel<KA, HI>, (int)bytes);
     if (rc) return rc;
-    prefill_score_kernel<KA, HI><<<grid, block_threads(HI), bytes, st>>>(tmA, tmB, a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(prefill_score_kernel<KA, HI>, dim3(grid), dim3(block_threads(HI)),
+                               bytes, st, tmA, tmB, a);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_score_prefill launch");
     return DSA_OK;
 }
@@ -549,9 +552,10 @@ extern "C" int dsa_score_prefill(const dsa_bf16* qidx, const float* w, int rows,
     const int pcap = P.max_seq_len / kpool_size;
     if (pcap == 0) {  // no pool fits a sequence: every score is -inf
         const long long n = (long long)rows * p_stride;
-        fill_neg_inf_kernel<<<(int)std::min<long long>((n + 255) / 256, 4096), 256, 0, st>>>(
-            scores, n);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(fill_neg_inf_kernel,
+                                   dim3((unsigned)std::min<long long>((n + 255) / 256, 4096)),
+                                   dim3(256), 0, st, scores, n);
+        if (e == cudaSuccess) e = cudaGetLastError();
         return e == cudaSuccess ? DSA_OK : cuda_fail(e, "dsa_score_prefill launch");
     }
     const long long prows = (long long)P.batch * pcap;

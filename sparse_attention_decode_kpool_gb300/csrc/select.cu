@@ -375,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
     uint8_t* dyn = reinterpret_cast<uint8_t*>(keys);
     uint32_t* tbuf = reinterpret_cast<uint32_t*>(dyn + a.tbuf_off);
 
+    pdl_wait();
     const int begin = crank * a.chunk;
     const int n = max(0, min(a.chunk, a.p_stride - begin));
     const float* srow = a.scores + (long long)r * a.p_stride + begin;
@@ -533,13 +534,15 @@ extern "C" int dsa_select(const float* scores, int rows, int p_stride, int index
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = (size_t)sp.bytes;
     cfg.stream = (cudaStream_t)stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, select_kernel, a);
     if (e != cudaSuccess) return cuda_fail(e, "dsa_select launch");
     e = cudaGetLastError();
