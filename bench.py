@@ -41,6 +41,16 @@ METRIC = "DSA decode queries/s (select + sparse MLA) at 262K ctx; % of HBM roofl
 PREFILL_METRIC = ("DSA chunked-prefill query rows/s (tensor-core index scores + select + expand "
                   "+ sparse latent attention to olat); % of bf16 tensor peak")
 PREFILL_WORKLOAD = 4  # scored on the tensor cores; the o_absorb GEMM is not in its step
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a stage's
+# kernels, from one ncu capture of the current kernels (profiles/<file>); a stage
+# not listed, or whose kernels changed since the capture, reports null. The
+# projection reads all of o_absorb whatever the context length, so its capture at
+# S=32,768 holds for the 262,144-token workload.
+MEASURED_TRAFFIC = {
+    "project": (269.665536e6 + 3.664896e6 + 0.735488e6,
+                "project_decode_S32768_b8.md (project_kernel + project_reduce_kernel)"),
+}
 FLUSH_BYTES = 256 << 20
 
 
@@ -511,8 +521,10 @@ def main():
         dom_bytes = ab[dom]
         achieved = dom_bytes / (stage_ms[dom] * 1e-3) / 1e9
         total_gbs = ab["total"] / (ms * 1e-3) / 1e9
+        tr = MEASURED_TRAFFIC.get(dom) if wl.geom.hidden == 4096 and wl.rows == 8 else None
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                    "frac": achieved / hbm, "traffic": None, "peak_source": peak_src,
+                    "frac": achieved / hbm, "traffic": tr[0] if tr else None,
+                    "traffic_source": tr[1] if tr else None, "peak_source": peak_src,
                     "kernel": {"attend": "dsa_sparse_mla_decode (split attention + combine)",
                                "project": "dsa_latent_project (TMA-pipelined o_absorb GEMM + "
                                           "partial sum)",
