@@ -12,6 +12,9 @@
 // reduces over the pool's lane group with xor shuffles (two passes: mean, then the
 // centred second moment); the normalised key is rounded to bf16 in registers, the
 // storage point of the unfused pipeline, and pooled with the slot softmax in f32.
+// The softmax uses exp2 of log2(e)-scaled logits, the LayerNorm rsqrt and the final
+// ratio a fast divide: each is within a few f32 ulp, far below the bf16 rounding of
+// the stored key.
 #include "common.cuh"
 
 namespace dsa {
@@ -94,7 +97,10 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
         }
     }
 
-    // Pass 1: per-channel max of the slot logits.
+    // Pass 1: the slot logits gate + ape (kept in registers when kpool <= 4) and
+    // their per-channel max.
+    constexpr int KC = KPMAX <= 4 ? KPMAX : 1;  // cached slots
+    float lg[KC][8];
     float mx[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
@@ -107,11 +113,22 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
             const uint32_t gv[4] = {gr[s].x, gr[s].y, gr[s].z, gr[s].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                mx[2 * i] = fmaxf(mx[2 * i], bf16_lo(gv[i]) + ap[2 * i]);
-                mx[2 * i + 1] = fmaxf(mx[2 * i + 1], bf16_hi(gv[i]) + ap[2 * i + 1]);
+                const float l0 = bf16_lo(gv[i]) + ap[2 * i];
+                const float l1 = bf16_hi(gv[i]) + ap[2 * i + 1];
+                if (s < KC) {
+                    lg[s < KC ? s : 0][2 * i] = l0;
+                    lg[s < KC ? s : 0][2 * i + 1] = l1;
+                }
+                mx[2 * i] = fmaxf(mx[2 * i], l0);
+                mx[2 * i + 1] = fmaxf(mx[2 * i + 1], l1);
             }
         }
     }
+    // softmax weights as 2^(l*log2e - max*log2e)
+    constexpr float kLog2e = 1.4426950408889634f;
+    float mxs[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mxs[i] = mx[i] * kLog2e;
 
     // Pass 2: LayerNorm each slot, round to bf16, accumulate the softmax-weighted sum.
     float num[8], den[8];
@@ -137,28 +154,34 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 x[i] -= mean;
-                sq += x[i] * x[i];
+                sq = fmaf(x[i], x[i], sq);
             }
 #pragma unroll
             for (int off = LPP / 2; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-            const float rstd = 1.0f / sqrtf(sq * (1.0f / IHD) + a.eps);
+            const float rstd = rsqrtf(fmaf(sq, 1.0f / IHD, a.eps));
 
-            const float4 ap0 = __ldg(reinterpret_cast<const float4*>(a.ape + s * IHD + c0));
-            const float4 ap1 = __ldg(reinterpret_cast<const float4*>(a.ape + s * IHD + c0 + 4));
-            const float ap[8] = {ap0.x, ap0.y, ap0.z, ap0.w, ap1.x, ap1.y, ap1.z, ap1.w};
-            const uint32_t gv[4] = {gr[s].x, gr[s].y, gr[s].z, gr[s].w};
-            float gl[8];
+            float l[8];
+            if (s < KC) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                gl[2 * i] = bf16_lo(gv[i]);
-                gl[2 * i + 1] = bf16_hi(gv[i]);
+                for (int i = 0; i < 8; ++i) l[i] = lg[s < KC ? s : 0][i];
+            } else {
+                const float4 ap0 = __ldg(reinterpret_cast<const float4*>(a.ape + s * IHD + c0));
+                const float4 ap1 =
+                    __ldg(reinterpret_cast<const float4*>(a.ape + s * IHD + c0 + 4));
+                const float ap[8] = {ap0.x, ap0.y, ap0.z, ap0.w, ap1.x, ap1.y, ap1.z, ap1.w};
+                const uint32_t gv[4] = {gr[s].x, gr[s].y, gr[s].z, gr[s].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    l[2 * i] = bf16_lo(gv[i]) + ap[2 * i];
+                    l[2 * i + 1] = bf16_hi(gv[i]) + ap[2 * i + 1];
+                }
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float kn = round_bf16(x[i] * rstd * lw[i] + lb[i]);
-                const float e = expf(gl[i] + ap[i] - mx[i]);
+                const float kn = round_bf16(fmaf(x[i] * rstd, lw[i], lb[i]));
+                const float e = exp2f(fmaf(l[i], kLog2e, -mxs[i]));
                 den[i] += e;
-                num[i] += e * kn;
+                num[i] = fmaf(e, kn, num[i]);
             }
         }
     }
@@ -167,10 +190,10 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
     const bool pv = ok;
     uint4 o;
     if (pv) {
-        o.x = pack_bf16x2(num[0] / den[0], num[1] / den[1]);
-        o.y = pack_bf16x2(num[2] / den[2], num[3] / den[3]);
-        o.z = pack_bf16x2(num[4] / den[4], num[5] / den[5]);
-        o.w = pack_bf16x2(num[6] / den[6], num[7] / den[7]);
+        o.x = pack_bf16x2(__fdividef(num[0], den[0]), __fdividef(num[1], den[1]));
+        o.y = pack_bf16x2(__fdividef(num[2], den[2]), __fdividef(num[3], den[3]));
+        o.z = pack_bf16x2(__fdividef(num[4], den[4]), __fdividef(num[5], den[5]));
+        o.w = pack_bf16x2(__fdividef(num[6], den[6]), __fdividef(num[7], den[7]));
     } else {
         o = make_uint4(0, 0, 0, 0);
     }
