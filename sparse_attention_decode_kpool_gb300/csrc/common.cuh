@@ -70,6 +70,31 @@ size_t project_workspace_bytes(int rows, int K, int hidden, int sms);
 int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A, int hidden,
                    uint16_t* y, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st);
 
+// Sparse latent attention on the tensor cores (mla_tc.cu): the split kernel of
+// dsa_sparse_mla_decode for 64 heads when DSA_MLA_TC=1. Writes the splits' partials
+// (ns > 1) or olat / its bf16 copy (ns == 1) in the same layout as the mma.sync split
+// kernel.
+struct MlaTcParams {
+    const uint16_t* qlat;
+    const int32_t* row_seq;
+    const uint16_t* ckv;
+    const int32_t* token_ids;
+    float* part_o;
+    float* part_ml;
+    float* olat;
+    uint16_t* xbf;
+    int32_t* status;
+    Paging pg;
+    int rows;
+    int ow;
+    int ns;
+    int tps;
+    float sl2;  // softmax_scale * log2(e)
+};
+bool mla_tc_supported(int heads, int kv_lora_rank);
+int mla_tc_chunk();  // tokens per chunk: split sizes are rounded to it
+int mla_tc_launch(const MlaTcParams& a, long long ckv_rows, cudaStream_t st);
+
 // ---------------------------------------------------------------------------
 // Device side.
 

@@ -526,6 +526,7 @@ __global__ void ysum_kernel(const float* __restrict__ ypart, int KS, long long n
 // Launch plan (shared by the workspace query and the call).
 
 struct Plan {
+    bool tc;  // the tensor-core split kernel (mla_tc.cu) for 64 heads
     int mt;
     int hgroups;
     int ns;
@@ -541,16 +542,18 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms) {
     Plan p;
+    p.tc = mla_tc_supported(heads, KVL);
     p.mt = heads <= 16 ? 1 : heads <= 32 ? 2 : 4;
-    p.hgroups = (heads + 16 * p.mt - 1) / (16 * p.mt);
+    p.hgroups = p.tc ? 1 : (heads + 16 * p.mt - 1) / (16 * p.mt);
+    const int chunk = p.tc ? mla_tc_chunk() : CH;
     const long long base = (long long)rows * p.hgroups;
-    const int max_ns = ow > 0 ? (ow + CH - 1) / CH : 1;
+    const int max_ns = ow > 0 ? (ow + chunk - 1) / chunk : 1;
     long long ns = base > 0 ? (sms + base - 1) / base : 1;
     if (ns < 1) ns = 1;
     if (ns > max_ns) ns = max_ns;
     if (ns > kMaxSplits) ns = kMaxSplits;
     const int per = ow > 0 ? (int)((ow + ns - 1) / ns) : 0;
-    p.tps = per > 0 ? ((per + CH - 1) / CH) * CH : CH;
+    p.tps = per > 0 ? ((per + chunk - 1) / chunk) * chunk : chunk;
     p.ns = ow > 0 ? (ow + p.tps - 1) / p.tps : 1;
 
     const int nr = rows < 64 ? rows : 64;
@@ -681,10 +684,32 @@ extern "C" int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, 
     a.sl2 = softmax_scale * kLog2e;
 
     if (!olat && !with_oabs) return DSA_OK;  // nothing requested
-    switch (p.mt) {
-        case 1: rc = launch_split<1>(a, p, st); break;
-        case 2: rc = launch_split<2>(a, p, st); break;
-        default: rc = launch_split<4>(a, p, st); break;
+    if (p.tc) {
+        MlaTcParams t;
+        t.qlat = qlat;
+        t.row_seq = row_seq;
+        t.ckv = ckv;
+        t.token_ids = token_ids;
+        t.part_o = a.part_o;
+        t.part_ml = a.part_ml;
+        t.olat = olat;
+        t.xbf = a.xbf;
+        t.status = status;
+        t.pg = P;
+        t.rows = rows;
+        t.ow = out_width;
+        t.ns = p.ns;
+        t.tps = p.tps;
+        t.sl2 = a.sl2;
+        const long long ckv_rows = P.block_table ? (long long)P.num_blocks * P.block_size
+                                                 : (long long)P.batch * P.max_seq_len;
+        rc = mla_tc_launch(t, ckv_rows, st);
+    } else {
+        switch (p.mt) {
+            case 1: rc = launch_split<1>(a, p, st); break;
+            case 2: rc = launch_split<2>(a, p, st); break;
+            default: rc = launch_split<4>(a, p, st); break;
+        }
     }
     if (rc) return rc;
     cudaError_t e = cudaGetLastError();

@@ -250,6 +250,63 @@ __global__ void project_reduce_kernel(const float* __restrict__ ypart, long long
     }
 }
 
+// Row-block form of the same sum: one CTA per 64-row block of y and up to 128 of
+// its (row, 4-column) outputs. The first warp finds the CTAs whose unit ranges meet
+// the block (consecutive, at most 32: checked on the host) and stores their partial
+// offsets in shared memory; every thread then sums its output over them in CTA
+// order with all its loads issued together (eight at a time).
+__global__ void __launch_bounds__(128) project_reduce_rows_kernel(
+    const float* __restrict__ ypart, long long U, int KB, int G, int J, int R, int hidden,
+    uint16_t* __restrict__ y) {
+    pdl_wait();
+    __shared__ long long soff[32];
+    __shared__ int scount;
+    const int tid = threadIdx.x;
+    const long long mb = blockIdx.x;
+    if (tid < 32) {
+        const long long lo = mb * KB, hi = lo + KB;
+        long long c0 = lo * G / U;
+        while (c0 > 0 && unit_begin(c0, U, G) > lo) --c0;
+        while (c0 + 1 < G && unit_begin(c0 + 1, U, G) <= lo) ++c0;
+        const long long c = c0 + tid;
+        bool contrib = false;
+        if (c < G) {
+            const long long b0 = unit_begin(c, U, G), b1 = unit_begin(c + 1, U, G);
+            contrib = b0 < hi && b1 > lo && b1 > b0;
+            if (contrib) soff[tid] = ((c * J + (mb - b0 / KB)) * R) * MROWS;
+        }
+        const int n = __popc(__ballot_sync(0xffffffffu, contrib));
+        if (tid == 0) scount = n;
+    }
+    __syncthreads();
+    const int n = scount;
+    const int o = blockIdx.y * 128 + tid;
+    if (o >= R * (MROWS / 4)) return;
+    const int r = o / (MROWS / 4), c4 = o % (MROWS / 4);
+    const long long ro = (long long)r * MROWS + 4 * c4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < n; k += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            v[i] = k + i < n ? __ldg(reinterpret_cast<const float4*>(ypart + soff[k + i] + ro))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (k + i < n) {
+                acc.x += v[i].x;
+                acc.y += v[i].y;
+                acc.z += v[i].z;
+                acc.w += v[i].w;
+            }
+        }
+    }
+    uint2 out;
+    out.x = pack_bf16x2(acc.x, acc.y);
+    out.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(y + (long long)r * hidden + mb * MROWS + 4 * c4) = out;
+}
+
 struct ProjPlan {
     long long U;
     int KB, G, J, nt;
@@ -331,11 +388,29 @@ int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "projection launch");
-    const long long n4 = (long long)rows * hidden / 4;
-    long long blocks = (n4 + 255) / 256;
-    if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
-    e = launch_pdl(project_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
-                   (const float*)ws, p.U, p.KB, p.G, p.J, rows, hidden, (uint16_t*)y);
+    // Most CTAs meeting one row block: the row-block reduce takes up to 32.
+    int most = 0;
+    for (long long mb = 0; mb < hidden / MROWS; ++mb) {
+        const long long lo = mb * p.KB, hi = lo + p.KB;
+        long long c = lo * p.G / p.U;
+        while (c > 0 && unit_begin(c, p.U, p.G) > lo) --c;
+        int cnt = 0;
+        for (; c < p.G && unit_begin(c, p.U, p.G) < hi; ++c)
+            if (unit_begin(c + 1, p.U, p.G) > lo) ++cnt;
+        if (cnt > most) most = cnt;
+    }
+    if (most <= 32) {
+        const long long nmb = hidden / MROWS;
+        const unsigned yb = (unsigned)((rows * (MROWS / 4) + 127) / 128);
+        e = launch_pdl(project_reduce_rows_kernel, dim3((unsigned)nmb, yb), dim3(128), 0, st,
+                       (const float*)ws, p.U, p.KB, p.G, p.J, rows, hidden, (uint16_t*)y);
+    } else {
+        const long long n4 = (long long)rows * hidden / 4;
+        long long blocks = (n4 + 255) / 256;
+        if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+        e = launch_pdl(project_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                       (const float*)ws, p.U, p.KB, p.G, p.J, rows, hidden, (uint16_t*)y);
+    }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "projection reduce launch");
     return DSA_OK;

@@ -29,6 +29,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace dsa {
 namespace {
@@ -64,91 +65,6 @@ struct PrefillArgs {
     int neg;       // scale < 0
 };
 
-// ---- tcgen05 / tensor-memory helpers ---------------------------------------
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-}
-// Shared-memory matrix descriptor: K-major operand in 128-byte swizzle atoms (8
-// rows x 128 bytes, rows 128 bytes apart, atoms 1024 bytes apart).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
-           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive on `bar` once every tcgen05 operation this thread issued so far is done.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-// 32 consecutive f32 columns of this thread's lane.
-__device__ __forceinline__ void tc_ld32(uint32_t (&v)[32], uint32_t taddr) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
-          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
-          "=r"(v[31])
-        : "r"(taddr));
-}
-// Waits for this thread's tensor-memory loads; v is tied in so that no use of it is
-// scheduled before the wait.
-__device__ __forceinline__ void tc_wait_ld(uint32_t (&v)[32]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
-                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
-                   "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
-                   "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]),
-                   "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
-                   "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]),
-                   "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
-                 :
-                 : "memory");
-}
-
-// Orders later uses of v after a tcgen05.wait::ld issued just before (no instruction).
-__device__ __forceinline__ void tc_tie(uint32_t (&v)[32]) {
-    asm volatile(""
-                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
-                   "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
-                   "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]),
-                   "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
-                   "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]),
-                   "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
-}
-
-__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
-    float4 r;
-    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
-                 : "r"(addr));
-    return r;
-}
-__device__ __forceinline__ int lds_s32(uint32_t addr) {
-    int r;
-    asm volatile("ld.shared.s32 %0, [%1];\n" : "=r"(r) : "r"(addr));
-    return r;
-}
-
 // Per chunk c of NCH 32-column chunks: sum_i w[c][i] * relu(x[c][i]), the weights
 // read from shared memory at byte address waddr + 128 c. The chunks are interleaved,
 // four packed f32x2 FMA chains each, so that their work overlaps.
@@ -179,23 +95,6 @@ __device__ __forceinline__ void chunk_sums(const uint32_t (&x)[NCH][32], uint32_
     for (int c = 0; c < NCH; ++c)
         out[c] = ((s[c][0].x + s[c][0].y) + (s[c][1].x + s[c][1].y)) +
                  ((s[c][2].x + s[c][2].y) + (s[c][3].x + s[c][3].y));
-}
-
-// Bounded wait that also gives up once another role has aborted. The thread sleeps
-// in the barrier between checks (about 1 ms at most per check).
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
-                                              volatile int* abort_flag, int32_t* status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
-        if (*abort_flag) return false;
-        if (global_ns() - t0 > 1000000000ull) {
-            *abort_flag = 1;
-            flag_status(status, DSA_STATUS_TIMEOUT);
-            return false;
-        }
-    }
 }
 
 template <int KA>

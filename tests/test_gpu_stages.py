@@ -204,6 +204,7 @@ MLA_CASES = [
     ("h16-olat-only", 16, 0, [1500, 1500], None, 700, False),
     ("h96-two-groups", 96, 64, [800], None, 200, True),
     ("h64-b70-rows", 64, 64, [300] * 70, None, 64, True),
+    ("h64-r40-two-chunks", 64, 128, [3000] * 40, None, 1024, False),
     ("h8-hidden96-fallback", 8, 96, [600, 333], None, 128, True),
 ]
 
@@ -220,9 +221,19 @@ def _token_rows(rng, wl, ow, empty_row=True):
     return ids
 
 
+@pytest.fixture(params=["mma", "tcgen05"])
+def mla_kernel(request, monkeypatch):
+    """Both split-attention kernels: the default mma.sync one, and the opt-in tcgen05
+    one (64 heads only; other head counts keep the default)."""
+    monkeypatch.setenv("DSA_MLA_TC", "1" if request.param == "tcgen05" else "0")
+    return request.param
+
+
 @pytest.mark.parametrize("case", MLA_CASES, ids=[c[0] for c in MLA_CASES])
-def test_mla_parity(case):
+def test_mla_parity(case, mla_kernel):
     name, heads, hidden, lens, bs, ow, with_o = case
+    if mla_kernel == "tcgen05" and heads != 64:
+        pytest.skip("the tcgen05 split kernel serves 64 heads")
     g = _geom(heads=heads, hidden=max(hidden, 32), index_topk=ow)
     wl = W.make_workload(name, 300, g, lens, block_size=bs, with_raw=False,
                          with_o_absorb=with_o)
@@ -252,6 +263,38 @@ def test_mla_parity(case):
     H.check_attention(olat.t.cpu().numpy().reshape(wl.rows, -1), np.array(ro), f"{name} olat")
     if with_o:
         H.check_attention(y.t.float().cpu().numpy(), np.array(ry), f"{name} y")
+
+
+def test_mla_rescaled_running_max(mla_kernel):
+    """Latent rows whose norm grows with the token position: each 128-token chunk's
+    score maximum exceeds the last by far more than 2^8 (log2 units), so the
+    attention kernel's running maximum, output and sums are rescaled (64 heads)."""
+    g = _geom(heads=64, hidden=64, index_topk=2048)
+    wl = W.make_workload("rescale", 302, g, [4096, 2600], with_raw=False, with_o_absorb=False)
+    ck = wl.ckv.float()
+    flat = ck.view(-1, 512)
+    n = flat.shape[0]
+    # token row k of the cache gets factor 1 + 6 * (k mod 4096) / 4096
+    fac = 1.0 + 6.0 * (torch.arange(n, dtype=torch.float32) % 4096) / 4096.0
+    wl.ckv = (flat * fac[:, None]).to(torch.bfloat16).view(wl.ckv.shape)
+    layer = DsaDecodeLayer(wl, with_o_absorb=False, keep_olat=True)
+    rng = np.random.default_rng(11)
+    ids = _token_rows(rng, wl, 2048, empty_row=False)
+    for r in range(wl.rows):  # ascending token ids: later chunks hold the larger rows
+        v = np.sort(ids[r][ids[r] >= 0])
+        ids[r] = -1
+        ids[r, : v.size] = v
+    tok = torch.from_numpy(ids).cuda()
+    olat = H.Guarded((wl.rows, 64, 512), torch.float32, 555.0)
+    api.dsa_sparse_mla_decode(layer.qlat, layer.row_seq, layer.ckv, layer.pg, tok,
+                              g.softmax_scale, None, None, olat.t, layer.status, layer.workspace)
+    torch.cuda.synchronize()
+    olat.check()
+    assert int(layer.status.item()) == 0
+    oq = H.OracleSeq(wl)
+    ro = [O.sparse_mla_decode_row(H.f(wl.qlat[r]), oq.ckv(int(wl.row_seq[r])), ids[r],
+                                  g.softmax_scale, None)[0].reshape(-1) for r in range(wl.rows)]
+    H.check_attention(olat.t.cpu().numpy().reshape(wl.rows, -1), np.array(ro), "rescale olat")
 
 
 def test_mla_bad_ids_set_status_and_are_skipped():
