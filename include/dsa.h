@@ -216,6 +216,21 @@ int dsa_expand(const int32_t* pool_ids, int rows, int sk, int first_key, int kpo
                int out_width, int32_t* token_ids, void* stream);
 
 /*
+ * dsa_select_expand -- dsa_select then dsa_expand in one launch (the top-k kernel
+ * writes each chosen pool's token ids as it writes the pool id): pool_ids and
+ * token_ids are bit-identical to the two calls in sequence. No counterpart on the
+ * pages beyond the two steps it fuses (mod.rs "Shape of the pipeline", top-k and
+ * expand).
+ *
+ * scores [rows, p_stride] f32; pool_ids [rows, select_k] i32; token_ids
+ * [rows, out_width] i32 with out_width >= select_k * kpool.
+ * Limits: p_stride <= 327,680; 1 <= kpool <= 16; first_key >= 0.
+ */
+int dsa_select_expand(const float* scores, int rows, int p_stride, int index_topk, int kpool,
+                      int first_key, int out_width, int32_t* pool_ids, int32_t* token_ids,
+                      void* stream);
+
+/*
  * dsa_sparse_mla_decode -- NoPE MLA restricted to the selected tokens, in the
  * latent space (mod.rs "Shape of the pipeline", last stage; build.rs module
  * doc, transforms 1 and 3: Q is absorbed through kv_b_proj's K half, o_proj

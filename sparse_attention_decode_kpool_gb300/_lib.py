@@ -53,6 +53,7 @@ SIGNATURES = {
                                _P]),
     "dsa_select": (_I, [_P, _I, _I, _I, _I, _P, _P]),
     "dsa_expand": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
+    "dsa_select_expand": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "dsa_sparse_mla_decode_workspace": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "dsa_sparse_mla_decode": (_I, [_P, _I, _I, _I, _P, _P, _PG, _P, _I, _F, _P, _I, _P, _P, _P,
                                    _P, _SZ, _P]),

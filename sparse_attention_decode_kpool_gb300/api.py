@@ -14,6 +14,7 @@ from . import _lib
 from ._lib import DsaPaging, check
 
 __all__ = ["paging", "dsa_compress", "dsa_score", "dsa_score_prefill", "dsa_select", "dsa_expand",
+           "dsa_select_expand",
            "dsa_sparse_mla_decode_workspace", "dsa_sparse_mla_decode",
            "dsa_sparse_mla_decode_noalloc", "dsa_latent_project_workspace",
            "dsa_latent_project", "dsa_select_k",
@@ -128,6 +129,21 @@ def dsa_select(scores, index_topk: int, kpool: int, pool_ids, stream=None) -> No
     check(_lib.load().dsa_select(
         _ptr(scores, torch.float32, "scores"), rows, p_stride, int(index_topk), int(kpool),
         _ptr(pool_ids, torch.int32, "pool_ids"), _stream(stream)))
+
+
+def dsa_select_expand(scores, index_topk: int, kpool: int, first_key: int, pool_ids, token_ids,
+                      stream=None) -> None:
+    """dsa_select and dsa_expand in one launch (identical results)."""
+    rows, p_stride = (int(x) for x in scores.shape)
+    sk = dsa_select_k(index_topk, kpool, p_stride)
+    if tuple(pool_ids.shape) != (rows, max(sk, 0)):
+        raise ValueError(f"pool_ids must be [{rows}, {sk}]")
+    if token_ids.dim() != 2 or token_ids.shape[0] != rows:
+        raise ValueError("token_ids must be [rows, out_width]")
+    check(_lib.load().dsa_select_expand(
+        _ptr(scores, torch.float32, "scores"), rows, p_stride, int(index_topk), int(kpool),
+        int(first_key), int(token_ids.shape[1]), _ptr(pool_ids, torch.int32, "pool_ids"),
+        _ptr(token_ids, torch.int32, "token_ids"), _stream(stream)))
 
 
 def dsa_expand(pool_ids, first_key: int, kpool: int, token_ids, stream=None) -> None:

@@ -47,6 +47,10 @@ struct SelectArgs {
     int merge_off;  // byte offsets in dynamic shared memory: merge keys, then ids
     int tbuf_off;   // the threshold bin's scratch list
     int tcap;       // its capacity (keys)
+    int32_t* tok;   // nullable: token ids [rows, ow] (dsa_select_expand)
+    int first_key;
+    int kpool;
+    int ow;
 };
 
 __device__ __forceinline__ uint32_t score_key(float f) {
@@ -287,17 +291,31 @@ struct EmitTo {
     uint32_t* rkeys;
     uint32_t* rids;
     const uint32_t* ids;
+    int32_t* tok;  // nullable: also write the pool's token ids at rank*kpool (modes 0, 2)
+    int first_key;
+    int kpool;
 };
 
 __device__ __forceinline__ void emit_one(const EmitTo& e, const uint32_t* keys, int at, int i) {
-    if (e.mode == 0) {
-        e.out[at] = e.base + i;
-    } else if (e.mode == 1) {
+    if (e.mode == 1) {
         e.rkeys[at] = keys[i];
         e.rids[at] = (uint32_t)(e.base + i);
-    } else {
-        e.out[at] = (int)e.ids[i];
+        return;
     }
+    const int p = e.mode == 0 ? e.base + i : (int)e.ids[i];
+    e.out[at] = p;
+    if (e.tok) {
+        const int t0 = e.first_key + p * e.kpool;
+        for (int s = 0; s < e.kpool; ++s) e.tok[at * e.kpool + s] = t0 + s;
+    }
+}
+
+// -1 over the pool ids from rank kk on, and over the token ids from kk*kpool on.
+__device__ __forceinline__ void fill_tail(int32_t* out, int sk, int32_t* tok, int ow, int kpool,
+                                          int kk) {
+    for (int j = kk + threadIdx.x; j < sk; j += blockDim.x) out[j] = -1;
+    if (tok)
+        for (int j = kk * kpool + threadIdx.x; j < ow; j += blockDim.x) tok[j] = -1;
 }
 
 // Emits every chosen position, ranks ascending with position. Thread t owns the
@@ -419,16 +437,20 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
     const MinMax mm = block_minmax(kmn, kmx, kcnt, sc);  // also publishes keys[]
 
     int32_t* out = a.pool_ids + (long long)r * a.sk;
+    int32_t* tok = a.tok ? a.tok + (long long)r * a.ow : nullptr;
     EmitTo e;
     e.base = begin;
     e.out = out;
     e.rkeys = e.rids = nullptr;
     e.ids = nullptr;
+    e.tok = tok;
+    e.first_key = a.first_key;
+    e.kpool = a.kpool;
     Thr t;
     if (C == 1) {
         e.mode = 0;
         const int kk = block_topk(keys, n, a.sk, mm, sc, tbuf, a.tcap, e, &t);
-        for (int j = kk + threadIdx.x; j < a.sk; j += kThreads) out[j] = -1;
+        fill_tail(out, a.sk, tok, a.ow, a.kpool, kk);
         return;
     }
 
@@ -461,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
     e.base = 0;
     e.ids = mkeys + C * a.sk;
     const int kk = block_topk(mkeys, C * a.sk, a.sk, mg, sc, tbuf, a.tcap, e, &t);
-    for (int j = kk + threadIdx.x; j < a.sk; j += kThreads) out[j] = -1;
+    fill_tail(out, a.sk, tok, a.ow, a.kpool, kk);
 }
 
 // Dynamic shared memory: the slice's keys (4 B each); with C > 1 the merge area
@@ -486,16 +508,9 @@ SmemPlan smem_plan(int p_stride, int sk, int C) {
 
 using namespace dsa;
 
-extern "C" int dsa_select(const float* scores, int rows, int p_stride, int index_topk, int kpool,
-                          int32_t* pool_ids, void* stream) {
-    if (rows < 0 || p_stride < 0)
-        return fail(DSA_ERR_INVALID_ARG, "dsa_select: rows %d, p_stride %d", rows, p_stride);
-    if (index_topk < 1 || kpool < 1)
-        return fail(DSA_ERR_CONFIG, "dsa_select: index_topk %d and kpool %d must be > 0",
-                    index_topk, kpool);
-    const int sk = dsa_select_k(index_topk, kpool, p_stride);
-    if (rows == 0 || sk == 0) return DSA_OK;
-    if (!scores || !pool_ids) return fail(DSA_ERR_INVALID_ARG, "dsa_select: NULL tensor");
+namespace {
+int select_launch(const float* scores, int rows, int p_stride, int sk, int32_t* pool_ids,
+                  int32_t* tok, int first_key, int kpool, int ow, void* stream) {
     if ((long long)p_stride > (long long)kMaxChunk * kMaxCluster)
         return fail(DSA_ERR_UNSUPPORTED, "dsa_select: p_stride %d > %d", p_stride,
                     kMaxChunk * kMaxCluster);
@@ -526,6 +541,10 @@ extern "C" int dsa_select(const float* scores, int rows, int p_stride, int index
     a.merge_off = (int)sp.merge_off;
     a.tbuf_off = (int)sp.tbuf_off;
     a.tcap = (int)sp.tcap;
+    a.tok = tok;
+    a.first_key = first_key;
+    a.kpool = kpool;
+    a.ow = ow;
     int rc = set_max_smem((const void*)select_kernel, kMaxSmem);
     if (rc) return rc;
     if ((long long)rows * C > 0x7fffffffLL) return fail(DSA_ERR_UNSUPPORTED, "dsa_select: too many rows");
@@ -548,4 +567,44 @@ extern "C" int dsa_select(const float* scores, int rows, int p_stride, int index
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_select launch");
     return DSA_OK;
+}
+}  // namespace
+
+extern "C" int dsa_select(const float* scores, int rows, int p_stride, int index_topk, int kpool,
+                          int32_t* pool_ids, void* stream) {
+    if (rows < 0 || p_stride < 0)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_select: rows %d, p_stride %d", rows, p_stride);
+    if (index_topk < 1 || kpool < 1)
+        return fail(DSA_ERR_CONFIG, "dsa_select: index_topk %d and kpool %d must be > 0",
+                    index_topk, kpool);
+    const int sk = dsa_select_k(index_topk, kpool, p_stride);
+    if (rows == 0 || sk == 0) return DSA_OK;
+    if (!scores || !pool_ids) return fail(DSA_ERR_INVALID_ARG, "dsa_select: NULL tensor");
+    return select_launch(scores, rows, p_stride, sk, pool_ids, nullptr, 0, kpool, 0, stream);
+}
+
+extern "C" int dsa_select_expand(const float* scores, int rows, int p_stride, int index_topk,
+                                 int kpool, int first_key, int out_width, int32_t* pool_ids,
+                                 int32_t* token_ids, void* stream) {
+    if (rows < 0 || p_stride < 0 || first_key < 0 || out_width < 0)
+        return fail(DSA_ERR_INVALID_ARG,
+                    "dsa_select_expand: rows %d, p_stride %d, first_key %d, out_width %d", rows,
+                    p_stride, first_key, out_width);
+    if (index_topk < 1 || kpool < 1)
+        return fail(DSA_ERR_CONFIG, "dsa_select_expand: index_topk %d and kpool %d must be > 0",
+                    index_topk, kpool);
+    if (kpool > DSA_MAX_KPOOL)
+        return fail(DSA_ERR_UNSUPPORTED, "dsa_select_expand: kpool %d > %d", kpool,
+                    DSA_MAX_KPOOL);
+    const int sk = dsa_select_k(index_topk, kpool, p_stride);
+    if ((long long)sk * kpool > out_width)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_select_expand: out_width %d < sk*kpool %lld",
+                    out_width, (long long)sk * kpool);
+    if (rows == 0) return DSA_OK;
+    if (sk == 0)  // nothing to select: every token slot is -1
+        return dsa_expand(nullptr, rows, 0, first_key, kpool, out_width, token_ids, stream);
+    if (!scores || !pool_ids || (out_width > 0 && !token_ids))
+        return fail(DSA_ERR_INVALID_ARG, "dsa_select_expand: NULL tensor");
+    return select_launch(scores, rows, p_stride, sk, pool_ids, token_ids, first_key, kpool,
+                         out_width, stream);
 }

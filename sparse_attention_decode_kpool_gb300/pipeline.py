@@ -19,7 +19,7 @@ from .workloads import Workload
 class DsaDecodeLayer:
     def __init__(self, wl: Workload, device: str = "cuda", keep_olat: bool = False,
                  with_o_absorb: bool = True, use_drawn_kpool: bool = False,
-                 score_path: str = "auto"):
+                 score_path: str = "auto", fuse_expand: bool = True):
         g = wl.geom
         self.wl = wl
         self.geom = g
@@ -90,6 +90,8 @@ class DsaDecodeLayer:
                                                       and R >= 64)
         self.graph: Optional[torch.cuda.CUDAGraph] = None
         self._fused_ws: Optional[torch.Tensor] = None
+        # select() also expands (dsa_select_expand); expand() is then a no-op.
+        self.fuse_expand = bool(fuse_expand)
 
     def fused_workspace(self) -> torch.Tensor:
         """Workspace for the one-call form dsa_sparse_mla_decode(..., o_absorb, y)."""
@@ -120,10 +122,16 @@ class DsaDecodeLayer:
                       status=self.status, stream=stream)
 
     def select(self, stream=None) -> None:
-        api.dsa_select(self.scores, self.geom.index_topk, self.geom.index_kpool, self.pool_ids,
-                       stream=stream)
+        g = self.geom
+        if self.fuse_expand:
+            api.dsa_select_expand(self.scores, g.index_topk, g.index_kpool, g.first_key,
+                                  self.pool_ids, self.token_ids, stream=stream)
+            return
+        api.dsa_select(self.scores, g.index_topk, g.index_kpool, self.pool_ids, stream=stream)
 
     def expand(self, stream=None) -> None:
+        if self.fuse_expand:
+            return
         api.dsa_expand(self.pool_ids, self.geom.first_key, self.geom.index_kpool, self.token_ids,
                        stream=stream)
 
@@ -156,7 +164,7 @@ class DsaDecodeLayer:
     def launches_per_step(self) -> int:
         """Library kernel launches one step() makes."""
         R, g = self.wl.rows, self.geom
-        n = 4  # score, select, expand, split attention
+        n = 3 if self.fuse_expand else 4  # score, select(+expand), [expand], split attention
         if api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, 0, False) > 0:
             n += 1  # split combine
         if self.o_absorb is not None:

@@ -174,6 +174,49 @@ def test_select_parity(case):
                                       err_msg=f"row {r}")
 
 
+SELECT_EXPAND_CASES = [
+    # rows, P, topk, kpool, kind, first_key, out_width extra
+    (1, 1, 4, 4, "normal", 0, 0), (3, 5, 8, 4, "ties", 3, 5), (4, 511, 256, 4, "normal", 0, 0),
+    (8, 65536, 2048, 4, "positive", 0, 0), (2, 3000, 2048, 4, "sparse", 1, 17),
+    (2, 700, 256, 4, "allinf", 0, 0), (64, 16384, 2048, 4, "normal", 0, 0),
+    (300, 2048, 512, 4, "ties", 0, 0), (2, 40000, 64, 1, "ties", 2, 3),
+    (3, 2000, 128, 16, "normal", 16, 0), (2, 0, 256, 4, "allinf", 0, 9),
+]
+
+
+@pytest.mark.parametrize("case", SELECT_EXPAND_CASES,
+                         ids=[f"{c[0]}x{c[1]}-k{c[2]}/{c[3]}-{c[4]}-fk{c[5]}" for c in SELECT_EXPAND_CASES])
+def test_select_expand_parity(case):
+    """The fused call equals dsa_select then dsa_expand bit for bit, and the oracle's
+    top-k and expansion."""
+    rows, P, topk, kp, kind, fk, extra = case
+    rng = np.random.default_rng(rows * 31 + P + kp)
+    s = _tie_rows(rng, rows, P, kind) if P else np.zeros((rows, 0), np.float32)
+    sk = O.select_k(topk, kp, P)
+    width = sk * kp + extra
+    scores = torch.from_numpy(s).cuda()
+    ids = H.Guarded((rows, sk), torch.int32, -77)
+    tok = H.Guarded((rows, width), torch.int32, -88)
+    api.dsa_select_expand(scores, topk, kp, fk, ids.t, tok.t)
+    torch.cuda.synchronize()
+    ids.check()
+    tok.check()
+    got_ids, got_tok = ids.t.cpu().numpy(), tok.t.cpu().numpy()
+    if sk:
+        ref_ids = torch.empty((rows, sk), dtype=torch.int32, device="cuda")
+        api.dsa_select(scores, topk, kp, ref_ids)
+        ref_tok = torch.empty((rows, width), dtype=torch.int32, device="cuda")
+        api.dsa_expand(ref_ids, fk, kp, ref_tok)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(got_ids, ref_ids.cpu().numpy())
+        np.testing.assert_array_equal(got_tok, ref_tok.cpu().numpy())
+    for r in range(rows):
+        o_ids = O.topk_pools(s[r].astype(np.float64), sk)
+        np.testing.assert_array_equal(got_ids[r], o_ids, err_msg=f"row {r}")
+        np.testing.assert_array_equal(got_tok[r], O.expand_selection(o_ids, fk, kp, width),
+                                      err_msg=f"row {r}")
+
+
 def test_expand_parity():
     rng = np.random.default_rng(3)
     for kp, fk, sk, width, rows in [(4, 0, 64, 256, 5), (4, 3, 512, 2048, 3), (1, 0, 7, 9, 2),
