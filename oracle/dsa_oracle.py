@@ -209,6 +209,39 @@ def expand_selection(pool_ids_row, first_key: int, kpool: int, width: int) -> np
     return row
 
 
+def tail_tokens(ctx_len: int, first_key: int, kpool: int) -> np.ndarray:
+    """Tokens of the trailing partial pool a query row sees: ``[first_key + P*kpool,
+    ctx_len)`` with ``P = max(0, (ctx_len - first_key) // kpool)`` whole pools.
+
+    mod.rs "Checkpoint and kernel facts": pooling starts at ``first_key`` and a
+    trailing partial pool is not a pool, so these tokens are never a top-k
+    candidate. There are at most ``kpool - 1`` of them; none when ``ctx_len`` is
+    at most ``first_key`` or ends on a pool boundary.
+    """
+    if ctx_len <= first_key:
+        return np.zeros(0, dtype=np.int64)
+    P = (ctx_len - first_key) // kpool
+    return np.arange(first_key + P * kpool, ctx_len, dtype=np.int64)
+
+
+def expand_selection_tail(pool_ids_row, first_key: int, kpool: int, index_topk: int,
+                          ctx_len: int, width: Optional[int] = None) -> np.ndarray:
+    """``dsa_expand_selection`` with ``always_select_tail`` set, for one row.
+
+    ``Glm5NextDsaConfig::out_width`` widens the row by ``index_kpool - 1`` slots
+    when ``always_select_tail`` is set; the pages say no more. Reading taken: the
+    selected pools expand as without the flag into positions ``[0, index_topk)``,
+    and the extra slots, from position ``index_topk`` on, hold ``tail_tokens`` in
+    ascending order, then -1. The tail is taken by position alone (token validity
+    gates pool candidacy, and the tail is not a pool).
+    """
+    w = out_width(index_topk, kpool, True) if width is None else width
+    row = expand_selection(pool_ids_row, first_key, kpool, w)
+    tail = tail_tokens(ctx_len, first_key, kpool)
+    row[index_topk: index_topk + tail.size] = tail
+    return row
+
+
 # ---------------------------------------------------------------------------
 # (a5) NoPE MLA restricted to the selected tokens, in latent space
 
@@ -369,12 +402,15 @@ def sequence_pools(pcache, b: int, n_pools: int, block_table=None, pools_per_blo
 
 def decode_row(qidx_row, w_row, keys, pool_valid, ctx_len: int, first_key: int, kpool: int,
                index_scale: float, index_topk: int, p_stride: int, qlat_row, ckv_seq,
-               softmax_scale: float, o_absorb=None):
+               softmax_scale: float, o_absorb=None, always_select_tail: bool = False):
     """score -> top-k -> expand -> sparse latent MLA (-> o_absorb) for one row."""
     s = index_scores(qidx_row, w_row, keys, pool_valid, ctx_len, first_key, kpool,
                      index_scale, p_stride)
     sk = select_k(index_topk, kpool, p_stride)
     ids = topk_pools(s, sk)
-    tok = expand_selection(ids, first_key, kpool, out_width(index_topk, kpool))
+    if always_select_tail:
+        tok = expand_selection_tail(ids, first_key, kpool, index_topk, ctx_len)
+    else:
+        tok = expand_selection(ids, first_key, kpool, out_width(index_topk, kpool))
     olat, y, yb = sparse_mla_decode_row(qlat_row, ckv_seq, tok, softmax_scale, o_absorb)
     return dict(scores=s, pool_ids=ids, token_ids=tok, olat=olat, y=y, y_bf16=yb)

@@ -313,6 +313,67 @@ def test_expand_properties():
     assert (O.expand_selection([-1, -1], 0, 4, 8) == -1).all()
 
 
+def test_expand_tail_golden():
+    g = load_kv("expand_tail.txt")
+    assert len(g["case"]) == 6
+    for c, pools, toks in zip(g["case"], g["pools"], g["tokens"]):
+        ctx, fk, kp, topk = (int(v) for v in c)
+        got = O.expand_selection_tail(pools.astype(int), fk, kp, topk, ctx)
+        np.testing.assert_array_equal(got, toks)
+
+
+def test_expand_tail_covers_every_seen_token_once():
+    # Selecting every pool of a row: pools plus tail are exactly the tokens
+    # [first_key, ctx), each once, and the tail fits the kpool - 1 extra slots.
+    rng = np.random.default_rng(12)
+    for _ in range(300):
+        kp = int(rng.integers(1, 9))
+        fk = int(rng.integers(0, 6))
+        ctx = int(rng.integers(0, 60))
+        P = max(0, (ctx - fk) // kp)
+        topk = kp * (P + int(rng.integers(0, 3)))
+        if topk == 0:
+            topk = kp
+        sk = O.select_k(topk, kp, P)
+        ids = list(range(P))[:sk] + [-1] * (sk - min(sk, P))
+        row = O.expand_selection_tail(ids, fk, kp, topk, ctx)
+        assert row.shape == (O.out_width(topk, kp, True),)
+        seen = row[row >= 0]
+        assert sorted(seen.tolist()) == list(range(fk, max(fk, ctx)))
+        assert (np.diff(seen) > 0).all()
+        tail = row[topk:]
+        n_tail = (ctx - fk) % kp if ctx > fk else 0
+        assert (tail >= 0).sum() == n_tail
+    # Without a selection the tail still comes through, and nothing else does.
+    row = O.expand_selection_tail([-1, -1], 0, 4, 8, 7)
+    np.testing.assert_array_equal(row, [-1] * 8 + [4, 5, 6])
+
+
+def test_dense_equivalence_with_tail():
+    # With always_select_tail and index_topk covering every candidate pool, sparse
+    # attention equals dense masked attention over the tokens of candidate pools
+    # plus every token past the last whole pool.
+    g = W.Geometry(index_kpool=4, index_heads=4, index_head_dim=32, index_topk=4 * 64,
+                   heads=3, hidden=64, kv_lora_rank=32)
+    L, fk = 206, 3
+    wl = W.make_workload("t", 23, g, [L], invalid_per_seq=9)
+    k = wl.k_raw.float().numpy()[0]
+    keys, pv, _ = O.kpool_compress(k, wl.gate.float().numpy()[0], wl.valid.numpy()[0],
+                                   wl.ape.numpy(), wl.ln_w.float().numpy(),
+                                   wl.ln_b.float().numpy(), g.eps, fk, 4)
+    ckv = wl.ckv.float().numpy()[0]
+    r = O.decode_row(wl.qidx.float().numpy()[0], wl.w.numpy()[0], keys, pv, L, fk, 4,
+                     g.index_scale, g.index_topk, wl.p_stride, wl.qlat.float().numpy()[0],
+                     ckv, g.softmax_scale, always_select_tail=True)
+    mask = np.zeros(L, bool)
+    for t in range(fk, L):
+        p = (t - fk) // 4
+        mask[t] = p >= len(pv) or bool(pv[p])
+    assert len(pv) == 50 and mask[fk + 200:].all() and mask[fk + 200:].sum() == 3
+    dense = O.dense_masked_attention(wl.qlat.float().numpy()[0], ckv, mask, g.softmax_scale)
+    np.testing.assert_allclose(r["olat"], dense, rtol=1e-12, atol=1e-13)
+
+
 # ---------------------------------------------------------------------------
 # sparse latent MLA
 
