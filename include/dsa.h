@@ -93,7 +93,7 @@ const char* dsa_last_error(void);
 
 /* ABI version of this header (bumped on any signature change). */
 int dsa_abi_version(void);
-#define DSA_ABI_VERSION 1
+#define DSA_ABI_VERSION 2
 
 /*
  * Layer-geometry rules (mod.rs, Glm5NextDsaConfig::validate): index_kpool and
@@ -229,6 +229,36 @@ int dsa_expand(const int32_t* pool_ids, int rows, int sk, int first_key, int kpo
 int dsa_select_expand(const float* scores, int rows, int p_stride, int index_topk, int kpool,
                       int first_key, int out_width, int32_t* pool_ids, int32_t* token_ids,
                       void* stream);
+
+/*
+ * dsa_expand_tail -- dsa_expand_selection with always_select_tail set.
+ * Glm5NextDsaConfig::out_width (mod.rs) widens the index row by kpool - 1 slots
+ * for this flag; mod.rs "Checkpoint and kernel facts" says pooling starts at
+ * first_key and a trailing partial pool is not a pool. Reading implemented: the
+ * pools expand as in dsa_expand into positions [0, index_topk); from position
+ * index_topk on, row r holds the tokens of its trailing partial pool,
+ *   [first_key + kpool * floor((L_r - first_key) / kpool), L_r)   (L_r = row_ctx[r]),
+ * ascending, by position alone (token validity only gates pool candidacy), and
+ * every other slot is -1. Rows with L_r <= first_key have no tail.
+ *
+ * pool_ids [rows, sk] i32 with sk*kpool <= index_topk; row_ctx [rows] i32
+ * (device); token_ids [rows, out_width] i32, out_width >= index_topk + kpool - 1.
+ */
+int dsa_expand_tail(const int32_t* pool_ids, int rows, int sk, int first_key, int kpool,
+                    int index_topk, const int32_t* row_ctx, int out_width, int32_t* token_ids,
+                    void* stream);
+
+/*
+ * dsa_select_expand_tail -- dsa_select then dsa_expand_tail in one launch:
+ * pool_ids and token_ids are bit-identical to the two calls in sequence.
+ *
+ * scores [rows, p_stride] f32; row_ctx [rows] i32 (device, not NULL); pool_ids
+ * [rows, select_k] i32; token_ids [rows, out_width] i32 with
+ * out_width >= index_topk + kpool - 1. Limits as dsa_select_expand.
+ */
+int dsa_select_expand_tail(const float* scores, int rows, int p_stride, int index_topk,
+                           int kpool, int first_key, const int32_t* row_ctx, int out_width,
+                           int32_t* pool_ids, int32_t* token_ids, void* stream);
 
 /*
  * dsa_sparse_mla_decode -- NoPE MLA restricted to the selected tokens, in the

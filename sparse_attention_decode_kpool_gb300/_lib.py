@@ -20,7 +20,7 @@ DSA_ERR_CUDA = 4
 DSA_STATUS_BAD_TOKEN = 1
 DSA_STATUS_BAD_BLOCK = 2
 DSA_STATUS_TIMEOUT = 4
-DSA_ABI_VERSION = 1
+DSA_ABI_VERSION = 2
 
 
 class DsaPaging(ctypes.Structure):
@@ -54,6 +54,8 @@ SIGNATURES = {
     "dsa_select": (_I, [_P, _I, _I, _I, _I, _P, _P]),
     "dsa_expand": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "dsa_select_expand": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "dsa_expand_tail": (_I, [_P, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
+    "dsa_select_expand_tail": (_I, [_P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
     "dsa_sparse_mla_decode_workspace": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "dsa_sparse_mla_decode": (_I, [_P, _I, _I, _I, _P, _P, _PG, _P, _I, _F, _P, _I, _P, _P, _P,
                                    _P, _SZ, _P]),

@@ -14,7 +14,7 @@ from . import _lib
 from ._lib import DsaPaging, check
 
 __all__ = ["paging", "dsa_compress", "dsa_score", "dsa_score_prefill", "dsa_select", "dsa_expand",
-           "dsa_select_expand",
+           "dsa_select_expand", "dsa_expand_tail", "dsa_select_expand_tail",
            "dsa_sparse_mla_decode_workspace", "dsa_sparse_mla_decode",
            "dsa_sparse_mla_decode_noalloc", "dsa_latent_project_workspace",
            "dsa_latent_project", "dsa_select_k",
@@ -153,6 +153,39 @@ def dsa_expand(pool_ids, first_key: int, kpool: int, token_ids, stream=None) -> 
     check(_lib.load().dsa_expand(
         _ptr(pool_ids, torch.int32, "pool_ids"), rows, sk, int(first_key), int(kpool),
         int(token_ids.shape[1]), _ptr(token_ids, torch.int32, "token_ids"), _stream(stream)))
+
+
+def dsa_expand_tail(pool_ids, first_key: int, kpool: int, index_topk: int, row_ctx, token_ids,
+                    stream=None) -> None:
+    """dsa_expand with always_select_tail: the trailing partial pool's tokens of
+    each row (row_ctx [rows] i32) follow the pools from position index_topk on."""
+    rows, sk = (int(x) for x in pool_ids.shape)
+    if token_ids.dim() != 2 or token_ids.shape[0] != rows:
+        raise ValueError("token_ids must be [rows, out_width]")
+    if tuple(row_ctx.shape) != (rows,):
+        raise ValueError(f"row_ctx must be [{rows}]")
+    check(_lib.load().dsa_expand_tail(
+        _ptr(pool_ids, torch.int32, "pool_ids"), rows, sk, int(first_key), int(kpool),
+        int(index_topk), _ptr(row_ctx, torch.int32, "row_ctx"), int(token_ids.shape[1]),
+        _ptr(token_ids, torch.int32, "token_ids"), _stream(stream)))
+
+
+def dsa_select_expand_tail(scores, index_topk: int, kpool: int, first_key: int, row_ctx,
+                           pool_ids, token_ids, stream=None) -> None:
+    """dsa_select and dsa_expand_tail in one launch (identical results)."""
+    rows, p_stride = (int(x) for x in scores.shape)
+    sk = dsa_select_k(index_topk, kpool, p_stride)
+    if tuple(pool_ids.shape) != (rows, max(sk, 0)):
+        raise ValueError(f"pool_ids must be [{rows}, {sk}]")
+    if token_ids.dim() != 2 or token_ids.shape[0] != rows:
+        raise ValueError("token_ids must be [rows, out_width]")
+    if tuple(row_ctx.shape) != (rows,):
+        raise ValueError(f"row_ctx must be [{rows}]")
+    check(_lib.load().dsa_select_expand_tail(
+        _ptr(scores, torch.float32, "scores"), rows, p_stride, int(index_topk), int(kpool),
+        int(first_key), _ptr(row_ctx, torch.int32, "row_ctx"), int(token_ids.shape[1]),
+        _ptr(pool_ids, torch.int32, "pool_ids"), _ptr(token_ids, torch.int32, "token_ids"),
+        _stream(stream)))
 
 
 def dsa_sparse_mla_decode_workspace(rows: int, heads: int, out_width: int, hidden: int,

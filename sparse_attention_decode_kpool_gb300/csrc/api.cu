@@ -124,10 +124,13 @@ int check_paging(const dsa_paging* pg, int kpool, Paging* out) {
 }
 
 // ---------------------------------------------------------------------------
-// dsa_expand: one thread per output slot; each slot written exactly once.
+// dsa_expand / dsa_expand_tail: one thread per output slot; each slot written
+// exactly once. With row_ctx, positions tail_at + i hold the row's trailing
+// partial-pool tokens [t0, L), t0 = first_key + kpool * floor((L - first_key) / kpool).
 
 __global__ void expand_kernel(const int32_t* __restrict__ pool_ids, int rows, int sk,
                               int first_key, int kpool, int out_width,
+                              const int32_t* __restrict__ row_ctx, int tail_at,
                               int32_t* __restrict__ token_ids) {
     pdl_wait();
     long long n = (long long)rows * out_width;
@@ -140,9 +143,31 @@ __global__ void expand_kernel(const int32_t* __restrict__ pool_ids, int rows, in
         if (slot < sk) {
             int p = __ldg(pool_ids + (long long)r * sk + slot);
             if (p >= 0) v = first_key + p * kpool + (j - slot * kpool);
+        } else if (row_ctx && j >= tail_at) {
+            const int L = __ldg(row_ctx + r);
+            const int t0 = first_key + (L > first_key ? (L - first_key) / kpool * kpool : 0);
+            const int t = t0 + (j - tail_at);
+            if (t < L) v = t;
         }
         token_ids[i] = v;
     }
+}
+
+int expand_launch(const int32_t* pool_ids, int rows, int sk, int first_key, int kpool,
+                  int out_width, const int32_t* row_ctx, int tail_at, int32_t* token_ids,
+                  void* stream, const char* name) {
+    long long n = (long long)rows * out_width;
+    int threads = 256;
+    long long blocks = (n + threads - 1) / threads;
+    int cap = sm_count() * 8;
+    if (cap < 1) cap = 1024;
+    if (blocks > cap) blocks = cap;
+    cudaError_t e = launch_pdl(expand_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+                               (cudaStream_t)stream, pool_ids, rows, sk, first_key, kpool,
+                               out_width, row_ctx, tail_at, token_ids);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    return DSA_OK;
 }
 
 }  // namespace dsa
@@ -197,18 +222,30 @@ int dsa_expand(const int32_t* pool_ids, int rows, int sk, int first_key, int kpo
     if (rows == 0 || out_width == 0) return DSA_OK;
     if (!token_ids || (sk > 0 && !pool_ids))
         return fail(DSA_ERR_INVALID_ARG, "dsa_expand: NULL tensor");
-    long long n = (long long)rows * out_width;
-    int threads = 256;
-    long long blocks = (n + threads - 1) / threads;
-    int cap = sm_count() * 8;
-    if (cap < 1) cap = 1024;
-    if (blocks > cap) blocks = cap;
-    cudaError_t e = launch_pdl(expand_kernel, dim3((unsigned)blocks), dim3(threads), 0,
-                               (cudaStream_t)stream, pool_ids, rows, sk, first_key, kpool,
-                               out_width, token_ids);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "dsa_expand launch");
-    return DSA_OK;
+    return expand_launch(pool_ids, rows, sk, first_key, kpool, out_width, nullptr, out_width,
+                         token_ids, stream, "dsa_expand launch");
+}
+
+int dsa_expand_tail(const int32_t* pool_ids, int rows, int sk, int first_key, int kpool,
+                    int index_topk, const int32_t* row_ctx, int out_width, int32_t* token_ids,
+                    void* stream) {
+    if (rows < 0 || sk < 0 || first_key < 0 || kpool < 1 || index_topk < 0 || out_width < 0)
+        return fail(DSA_ERR_INVALID_ARG,
+                    "dsa_expand_tail: rows %d, sk %d, first_key %d, kpool %d, index_topk %d, "
+                    "out_width %d",
+                    rows, sk, first_key, kpool, index_topk, out_width);
+    if ((long long)sk * kpool > index_topk)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_expand_tail: sk*kpool %lld > index_topk %d",
+                    (long long)sk * kpool, index_topk);
+    if ((long long)index_topk + kpool - 1 > out_width)
+        return fail(DSA_ERR_INVALID_ARG,
+                    "dsa_expand_tail: out_width %d < index_topk + kpool - 1 = %lld", out_width,
+                    (long long)index_topk + kpool - 1);
+    if (rows == 0 || out_width == 0) return DSA_OK;
+    if (!token_ids || !row_ctx || (sk > 0 && !pool_ids))
+        return fail(DSA_ERR_INVALID_ARG, "dsa_expand_tail: NULL tensor");
+    return expand_launch(pool_ids, rows, sk, first_key, kpool, out_width, row_ctx, index_topk,
+                         token_ids, stream, "dsa_expand_tail launch");
 }
 
 }  // extern "C"

@@ -51,6 +51,8 @@ struct SelectArgs {
     int first_key;
     int kpool;
     int ow;
+    const int32_t* row_ctx;  // nullable: rows' context lengths, for the tail tokens
+    int tail_at;             // token-id position of the first tail slot (ow: no tail)
 };
 
 __device__ __forceinline__ uint32_t score_key(float f) {
@@ -310,12 +312,29 @@ __device__ __forceinline__ void emit_one(const EmitTo& e, const uint32_t* keys, 
     }
 }
 
-// -1 over the pool ids from rank kk on, and over the token ids from kk*kpool on.
+// -1 over the pool ids from rank kk on, and over the token ids from kk*kpool on,
+// except that token-id positions tail_at + i hold t0 + i while that is below tend
+// (the tokens of the row's trailing partial pool, with always_select_tail).
 __device__ __forceinline__ void fill_tail(int32_t* out, int sk, int32_t* tok, int ow, int kpool,
-                                          int kk) {
+                                          int kk, int tail_at, int t0, int tend) {
     for (int j = kk + threadIdx.x; j < sk; j += blockDim.x) out[j] = -1;
     if (tok)
-        for (int j = kk * kpool + threadIdx.x; j < ow; j += blockDim.x) tok[j] = -1;
+        for (int j = kk * kpool + threadIdx.x; j < ow; j += blockDim.x) {
+            const int t = t0 + (j - tail_at);
+            tok[j] = (j >= tail_at && t < tend) ? t : -1;
+        }
+}
+
+// The trailing partial pool of a row that sees the first L tokens: [t0, L) with
+// t0 = first_key + kpool * floor((L - first_key) / kpool); empty when L <= first_key.
+__device__ __forceinline__ void tail_range(const SelectArgs& a, int r, int* t0, int* tend) {
+    *t0 = 0;
+    *tend = 0;
+    if (a.row_ctx && a.tok) {
+        const int L = __ldg(a.row_ctx + r);
+        *t0 = a.first_key + (L > a.first_key ? (L - a.first_key) / a.kpool * a.kpool : 0);
+        *tend = L;
+    }
 }
 
 // Emits every chosen position, ranks ascending with position. Thread t owns the
@@ -450,7 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
     if (C == 1) {
         e.mode = 0;
         const int kk = block_topk(keys, n, a.sk, mm, sc, tbuf, a.tcap, e, &t);
-        fill_tail(out, a.sk, tok, a.ow, a.kpool, kk);
+        int t0, tend;
+        tail_range(a, r, &t0, &tend);
+        fill_tail(out, a.sk, tok, a.ow, a.kpool, kk, a.tail_at, t0, tend);
         return;
     }
 
@@ -483,7 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
     e.base = 0;
     e.ids = mkeys + C * a.sk;
     const int kk = block_topk(mkeys, C * a.sk, a.sk, mg, sc, tbuf, a.tcap, e, &t);
-    fill_tail(out, a.sk, tok, a.ow, a.kpool, kk);
+    int t0, tend;
+    tail_range(a, r, &t0, &tend);
+    fill_tail(out, a.sk, tok, a.ow, a.kpool, kk, a.tail_at, t0, tend);
 }
 
 // Dynamic shared memory: the slice's keys (4 B each); with C > 1 the merge area
@@ -510,7 +533,8 @@ using namespace dsa;
 
 namespace {
 int select_launch(const float* scores, int rows, int p_stride, int sk, int32_t* pool_ids,
-                  int32_t* tok, int first_key, int kpool, int ow, void* stream) {
+                  int32_t* tok, int first_key, int kpool, int ow, const int32_t* row_ctx,
+                  int tail_at, void* stream) {
     if ((long long)p_stride > (long long)kMaxChunk * kMaxCluster)
         return fail(DSA_ERR_UNSUPPORTED, "dsa_select: p_stride %d > %d", p_stride,
                     kMaxChunk * kMaxCluster);
@@ -545,6 +569,8 @@ int select_launch(const float* scores, int rows, int p_stride, int sk, int32_t* 
     a.first_key = first_key;
     a.kpool = kpool;
     a.ow = ow;
+    a.row_ctx = row_ctx;
+    a.tail_at = row_ctx ? tail_at : ow;
     int rc = set_max_smem((const void*)select_kernel, kMaxSmem);
     if (rc) return rc;
     if ((long long)rows * C > 0x7fffffffLL) return fail(DSA_ERR_UNSUPPORTED, "dsa_select: too many rows");
@@ -580,31 +606,57 @@ extern "C" int dsa_select(const float* scores, int rows, int p_stride, int index
     const int sk = dsa_select_k(index_topk, kpool, p_stride);
     if (rows == 0 || sk == 0) return DSA_OK;
     if (!scores || !pool_ids) return fail(DSA_ERR_INVALID_ARG, "dsa_select: NULL tensor");
-    return select_launch(scores, rows, p_stride, sk, pool_ids, nullptr, 0, kpool, 0, stream);
+    return select_launch(scores, rows, p_stride, sk, pool_ids, nullptr, 0, kpool, 0, nullptr, 0,
+                         stream);
 }
+
+namespace {
+// dsa_select_expand and dsa_select_expand_tail (row_ctx != nullptr).
+int select_expand_impl(const char* name, const float* scores, int rows, int p_stride,
+                       int index_topk, int kpool, int first_key, const int32_t* row_ctx,
+                       int out_width, int32_t* pool_ids, int32_t* token_ids, void* stream) {
+    if (rows < 0 || p_stride < 0 || first_key < 0 || out_width < 0)
+        return fail(DSA_ERR_INVALID_ARG, "%s: rows %d, p_stride %d, first_key %d, out_width %d",
+                    name, rows, p_stride, first_key, out_width);
+    if (index_topk < 1 || kpool < 1)
+        return fail(DSA_ERR_CONFIG, "%s: index_topk %d and kpool %d must be > 0", name,
+                    index_topk, kpool);
+    if (kpool > DSA_MAX_KPOOL)
+        return fail(DSA_ERR_UNSUPPORTED, "%s: kpool %d > %d", name, kpool, DSA_MAX_KPOOL);
+    const int sk = dsa_select_k(index_topk, kpool, p_stride);
+    if ((long long)sk * kpool > out_width)
+        return fail(DSA_ERR_INVALID_ARG, "%s: out_width %d < sk*kpool %lld", name, out_width,
+                    (long long)sk * kpool);
+    if (row_ctx && (long long)index_topk + kpool - 1 > out_width)
+        return fail(DSA_ERR_INVALID_ARG, "%s: out_width %d < index_topk + kpool - 1 = %lld",
+                    name, out_width, (long long)index_topk + kpool - 1);
+    if (rows == 0) return DSA_OK;
+    if (sk == 0) {  // nothing to select: token slots are -1 but for the tail
+        if (row_ctx)
+            return dsa_expand_tail(nullptr, rows, 0, first_key, kpool, index_topk, row_ctx,
+                                   out_width, token_ids, stream);
+        return dsa_expand(nullptr, rows, 0, first_key, kpool, out_width, token_ids, stream);
+    }
+    if (!scores || !pool_ids || (out_width > 0 && !token_ids))
+        return fail(DSA_ERR_INVALID_ARG, "%s: NULL tensor", name);
+    return select_launch(scores, rows, p_stride, sk, pool_ids, token_ids, first_key, kpool,
+                         out_width, row_ctx, index_topk, stream);
+}
+}  // namespace
 
 extern "C" int dsa_select_expand(const float* scores, int rows, int p_stride, int index_topk,
                                  int kpool, int first_key, int out_width, int32_t* pool_ids,
                                  int32_t* token_ids, void* stream) {
-    if (rows < 0 || p_stride < 0 || first_key < 0 || out_width < 0)
-        return fail(DSA_ERR_INVALID_ARG,
-                    "dsa_select_expand: rows %d, p_stride %d, first_key %d, out_width %d", rows,
-                    p_stride, first_key, out_width);
-    if (index_topk < 1 || kpool < 1)
-        return fail(DSA_ERR_CONFIG, "dsa_select_expand: index_topk %d and kpool %d must be > 0",
-                    index_topk, kpool);
-    if (kpool > DSA_MAX_KPOOL)
-        return fail(DSA_ERR_UNSUPPORTED, "dsa_select_expand: kpool %d > %d", kpool,
-                    DSA_MAX_KPOOL);
-    const int sk = dsa_select_k(index_topk, kpool, p_stride);
-    if ((long long)sk * kpool > out_width)
-        return fail(DSA_ERR_INVALID_ARG, "dsa_select_expand: out_width %d < sk*kpool %lld",
-                    out_width, (long long)sk * kpool);
-    if (rows == 0) return DSA_OK;
-    if (sk == 0)  // nothing to select: every token slot is -1
-        return dsa_expand(nullptr, rows, 0, first_key, kpool, out_width, token_ids, stream);
-    if (!scores || !pool_ids || (out_width > 0 && !token_ids))
-        return fail(DSA_ERR_INVALID_ARG, "dsa_select_expand: NULL tensor");
-    return select_launch(scores, rows, p_stride, sk, pool_ids, token_ids, first_key, kpool,
-                         out_width, stream);
+    return select_expand_impl("dsa_select_expand", scores, rows, p_stride, index_topk, kpool,
+                              first_key, nullptr, out_width, pool_ids, token_ids, stream);
+}
+
+extern "C" int dsa_select_expand_tail(const float* scores, int rows, int p_stride,
+                                      int index_topk, int kpool, int first_key,
+                                      const int32_t* row_ctx, int out_width, int32_t* pool_ids,
+                                      int32_t* token_ids, void* stream) {
+    if (!row_ctx && rows > 0)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_select_expand_tail: NULL row_ctx");
+    return select_expand_impl("dsa_select_expand_tail", scores, rows, p_stride, index_topk,
+                              kpool, first_key, row_ctx, out_width, pool_ids, token_ids, stream);
 }

@@ -123,6 +123,10 @@ class DsaDecodeLayer:
 
     def select(self, stream=None) -> None:
         g = self.geom
+        if self.fuse_expand and g.always_select_tail:
+            api.dsa_select_expand_tail(self.scores, g.index_topk, g.index_kpool, g.first_key,
+                                       self.row_ctx, self.pool_ids, self.token_ids, stream=stream)
+            return
         if self.fuse_expand:
             api.dsa_select_expand(self.scores, g.index_topk, g.index_kpool, g.first_key,
                                   self.pool_ids, self.token_ids, stream=stream)
@@ -130,10 +134,14 @@ class DsaDecodeLayer:
         api.dsa_select(self.scores, g.index_topk, g.index_kpool, self.pool_ids, stream=stream)
 
     def expand(self, stream=None) -> None:
+        g = self.geom
         if self.fuse_expand:
             return
-        api.dsa_expand(self.pool_ids, self.geom.first_key, self.geom.index_kpool, self.token_ids,
-                       stream=stream)
+        if g.always_select_tail:
+            api.dsa_expand_tail(self.pool_ids, g.first_key, g.index_kpool, g.index_topk,
+                                self.row_ctx, self.token_ids, stream=stream)
+            return
+        api.dsa_expand(self.pool_ids, g.first_key, g.index_kpool, self.token_ids, stream=stream)
 
     def attend(self, stream=None) -> None:
         """Sparse latent attention over the selected tokens -> olat (f32); in the

@@ -129,6 +129,7 @@ class Geometry:
     first_key: int = 0
     eps: float = 1e-6
     qk_head_dim: int = 256  # GLM-5.3: q_b_proj has 256 rows per head
+    always_select_tail: bool = False  # the trailing partial pool's tokens are always attended
 
     @property
     def index_scale(self) -> float:
@@ -140,7 +141,7 @@ class Geometry:
 
     @property
     def out_width(self) -> int:
-        return self.index_topk
+        return self.index_topk + (self.index_kpool - 1 if self.always_select_tail else 0)
 
 
 @dataclasses.dataclass

@@ -104,6 +104,25 @@ def test_score_select_expand_argument_errors(lib):
     assert lib.dsa_expand(FAKE, 2, 64, -1, 4, 256, FAKE, None) == DSA_ERR_INVALID_ARG
 
 
+def test_tail_entry_argument_errors(lib):
+    # dsa_expand_tail(pool_ids, rows, sk, first_key, kpool, index_topk, row_ctx,
+    #                 out_width, token_ids, stream): out_width >= index_topk + kpool - 1.
+    et = lib.dsa_expand_tail
+    assert et(FAKE, 2, 64, 0, 4, 256, FAKE, 258, FAKE, None) == DSA_ERR_INVALID_ARG
+    assert "index_topk + kpool - 1" in _err(lib)
+    assert et(FAKE, 2, 65, 0, 4, 256, FAKE, 259, FAKE, None) == DSA_ERR_INVALID_ARG
+    assert et(FAKE, 2, 64, 0, 4, 256, None, 259, FAKE, None) == DSA_ERR_INVALID_ARG
+    assert et(FAKE, 2, 64, 0, 0, 256, FAKE, 259, FAKE, None) == DSA_ERR_INVALID_ARG
+    assert et(FAKE, 0, 64, 0, 4, 256, FAKE, 259, FAKE, None) == DSA_OK
+    st = lib.dsa_select_expand_tail
+    assert st(FAKE, 1, 100, 256, 4, 0, FAKE, 258, FAKE, FAKE, None) == DSA_ERR_INVALID_ARG
+    assert st(FAKE, 1, 100, 256, 4, 0, None, 259, FAKE, FAKE, None) == DSA_ERR_INVALID_ARG
+    assert st(FAKE, 1, 100, 0, 4, 0, FAKE, 259, FAKE, FAKE, None) == DSA_ERR_CONFIG
+    assert st(FAKE, 1, 100, 256, 17, 0, FAKE, 400, FAKE, FAKE, None) == DSA_ERR_UNSUPPORTED
+    assert st(None, 1, 100, 256, 4, 0, FAKE, 259, FAKE, FAKE, None) == DSA_ERR_INVALID_ARG
+    assert st(FAKE, 0, 100, 256, 4, 0, FAKE, 259, FAKE, FAKE, None) == DSA_OK
+
+
 def test_score_prefill_argument_errors(lib):
     pg = _paging(batch=2)
 

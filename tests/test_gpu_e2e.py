@@ -55,7 +55,12 @@ def _run(wl, rows_to_check, with_o_absorb=True):
         # S3: against the oracle's scores, exact outside the near-tie band.
         kinds[H.check_selection(ids[r], ref_s, layer.sk)] += 1
         ref_ids = O.topk_pools(ref_s, layer.sk)
-        ref_tok = O.expand_selection(ref_ids, g.first_key, g.index_kpool, g.out_width)
+        if g.always_select_tail:
+            ref_tok = O.expand_selection_tail(ref_ids, g.first_key, g.index_kpool, g.index_topk,
+                                              int(wl.row_ctx[r]))
+        else:
+            ref_tok = O.expand_selection(ref_ids, g.first_key, g.index_kpool, g.out_width)
+        assert ref_tok.shape == (g.out_width,)
         if np.array_equal(ref_tok, tok[r]):
             o_, y_, _ = O.sparse_mla_decode_row(H.f(wl.qlat[r]), oq.ckv(b), ref_tok,
                                                 g.softmax_scale, A)
@@ -105,6 +110,29 @@ def test_tiny_graph_replay_matches_eager():
     torch.cuda.synchronize()
     assert torch.equal(layer.pool_ids, ids0)
     assert torch.equal(layer.y, y0)
+
+
+def _tail_workload():
+    # always_select_tail on a paged batch whose lengths leave every remainder mod
+    # kpool past first_key 3, plus a sequence with no whole pool (6 tokens) and one
+    # that ends before first_key (2 tokens: empty selection).
+    g = W.Geometry(**W.GLM53, first_key=3, always_select_tail=True)
+    return W.make_workload("tail-paged-fk3", 11, g, [4097, 5002, 1023, 6, 2050, 9000, 2],
+                           block_size=64, max_seq_len=9024, invalid_per_seq=5)
+
+
+@pytest.mark.parametrize("fuse", [True, False], ids=["fused", "two-call"])
+def test_always_select_tail_end_to_end(fuse, monkeypatch):
+    wl = _tail_workload()
+    assert wl.geom.out_width == 2048 + 3
+    orig = DsaDecodeLayer.__init__
+
+    def init(self, *a, **k):
+        k["fuse_expand"] = fuse
+        orig(self, *a, **k)
+
+    monkeypatch.setattr(DsaDecodeLayer, "__init__", init)
+    _run(wl, range(wl.rows))
 
 
 @pytest.mark.slow

@@ -234,6 +234,80 @@ def test_expand_parity():
             np.testing.assert_array_equal(got[r], O.expand_selection(ids[r], fk, kp, width))
 
 
+def _tail_ctx(rng, rows, P, kp, fk):
+    """Context lengths for the tail tests: every remainder mod kpool, rows at and
+    below first_key, and lengths past the last pool the scores cover."""
+    base = fk + P * kp
+    choices = [base + (r % kp) for r in range(rows)]
+    for r in range(rows):
+        pick = r % 5
+        if pick == 1:
+            choices[r] = int(rng.integers(0, fk + 1))
+        elif pick == 3:
+            choices[r] = int(rng.integers(fk, fk + 3 * kp + 5))
+        elif pick == 4:
+            choices[r] = base + int(rng.integers(0, 4 * kp))
+    return np.asarray(choices, dtype=np.int32)
+
+
+@pytest.mark.parametrize("case", SELECT_EXPAND_CASES,
+                         ids=[f"{c[0]}x{c[1]}-k{c[2]}/{c[3]}-{c[4]}-fk{c[5]}" for c in SELECT_EXPAND_CASES])
+def test_select_expand_tail_parity(case):
+    """always_select_tail: the fused call equals dsa_select then dsa_expand_tail bit
+    for bit, and the oracle's top-k and tail expansion."""
+    rows, P, topk, kp, kind, fk, extra = case
+    rng = np.random.default_rng(rows * 37 + P + kp)
+    s = _tie_rows(rng, rows, P, kind) if P else np.zeros((rows, 0), np.float32)
+    sk = O.select_k(topk, kp, P)
+    width = O.out_width(topk, kp, True) + extra
+    ctx = _tail_ctx(rng, rows, P, kp, fk)
+    scores = torch.from_numpy(s).cuda()
+    row_ctx = torch.from_numpy(ctx).cuda()
+    ids = H.Guarded((rows, sk), torch.int32, -77)
+    tok = H.Guarded((rows, width), torch.int32, -88)
+    api.dsa_select_expand_tail(scores, topk, kp, fk, row_ctx, ids.t, tok.t)
+    torch.cuda.synchronize()
+    ids.check()
+    tok.check()
+    got_ids, got_tok = ids.t.cpu().numpy(), tok.t.cpu().numpy()
+    ref_ids = torch.full((rows, sk), -1, dtype=torch.int32, device="cuda")
+    if sk:
+        api.dsa_select(scores, topk, kp, ref_ids)
+    ref_tok = torch.empty((rows, width), dtype=torch.int32, device="cuda")
+    api.dsa_expand_tail(ref_ids, fk, kp, topk, row_ctx, ref_tok)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(got_ids, ref_ids.cpu().numpy())
+    np.testing.assert_array_equal(got_tok, ref_tok.cpu().numpy())
+    for r in range(rows):
+        o_ids = O.topk_pools(s[r].astype(np.float64), sk)
+        np.testing.assert_array_equal(got_ids[r], o_ids, err_msg=f"row {r}")
+        want = O.expand_selection_tail(o_ids, fk, kp, topk, int(ctx[r]), width)
+        np.testing.assert_array_equal(got_tok[r], want, err_msg=f"row {r} ctx {ctx[r]}")
+
+
+def test_expand_tail_parity():
+    rng = np.random.default_rng(4)
+    for kp, fk, topk, extra, rows in [(4, 0, 256, 0, 7), (4, 3, 2048, 0, 5), (1, 0, 7, 2, 3),
+                                      (16, 16, 64, 5, 9), (3, 1, 30, 1, 8)]:
+        sk = topk // kp
+        ids = np.full((rows, sk), -1, dtype=np.int32)
+        for r in range(rows):
+            k = int(rng.integers(0, sk + 1))
+            ids[r, :k] = np.sort(rng.choice(10 * sk + 10, k, replace=False))
+        width = O.out_width(topk, kp, True) + extra
+        ctx = _tail_ctx(rng, rows, 10 * sk + 10, kp, fk)
+        out = H.Guarded((rows, width), torch.int32, -99)
+        api.dsa_expand_tail(torch.from_numpy(ids).cuda(), fk, kp, topk,
+                            torch.from_numpy(ctx).cuda(), out.t)
+        torch.cuda.synchronize()
+        out.check()
+        got = out.t.cpu().numpy()
+        for r in range(rows):
+            np.testing.assert_array_equal(
+                got[r], O.expand_selection_tail(ids[r], fk, kp, topk, int(ctx[r]), width),
+                err_msg=f"kp {kp} row {r} ctx {ctx[r]}")
+
+
 # ---------------------------------------------------------------------------
 # dsa_sparse_mla_decode (fed oracle-side token ids)
 
