@@ -112,18 +112,23 @@ def test_tiny_graph_replay_matches_eager():
     assert torch.equal(layer.y, y0)
 
 
-def _tail_workload():
-    # always_select_tail on a paged batch whose lengths leave every remainder mod
-    # kpool past first_key 3, plus a sequence with no whole pool (6 tokens) and one
-    # that ends before first_key (2 tokens: empty selection).
-    g = W.Geometry(**W.GLM53, first_key=3, always_select_tail=True)
-    return W.make_workload("tail-paged-fk3", 11, g, [4097, 5002, 1023, 6, 2050, 9000, 2],
-                           block_size=64, max_seq_len=9024, invalid_per_seq=5)
+def _tail_workload(paged: bool):
+    # always_select_tail on lengths that leave every remainder mod kpool past
+    # first_key, plus a sequence with no whole pool (6 tokens) and one that ends
+    # before first_key (2 tokens: empty selection). The paged layout wants
+    # first_key on a pool boundary, so it takes 4; the contiguous one takes 3.
+    fk = 4 if paged else 3
+    g = W.Geometry(**W.GLM53, first_key=fk, always_select_tail=True)
+    return W.make_workload(f"tail-{'paged' if paged else 'contig'}-fk{fk}", 11, g,
+                           [4097, 5002, 1023, 6, 2050, 9000, 2],
+                           block_size=64 if paged else None, max_seq_len=9024,
+                           invalid_per_seq=5)
 
 
+@pytest.mark.parametrize("paged", [False, True], ids=["contig", "paged"])
 @pytest.mark.parametrize("fuse", [True, False], ids=["fused", "two-call"])
-def test_always_select_tail_end_to_end(fuse, monkeypatch):
-    wl = _tail_workload()
+def test_always_select_tail_end_to_end(fuse, paged, monkeypatch):
+    wl = _tail_workload(paged)
     assert wl.geom.out_width == 2048 + 3
     orig = DsaDecodeLayer.__init__
 
