@@ -7,7 +7,7 @@ CUDA-graph replay of the four C-ABI calls. Inputs are resident in HBM; L2 is
 flushed (a 256 MiB write) between timed steps, outside the timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload 3] [--no-cpu-baseline] [--no-e2e]
+                  [--workload 3] [--no-cpu-baseline] [--no-e2e] [--always-select-tail]
 
 --impl reference times the CPU oracle (the plain float64 restatement of the
 method) on the host, one query row per step, single-threaded.
@@ -23,6 +23,7 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
 
 import argparse
 import ctypes
+import dataclasses
 import json
 import statistics
 import sys
@@ -249,7 +250,8 @@ class OracleRunner:
         ql = wl.qlat[r].float().numpy()
         t0 = time.perf_counter()
         O.decode_row(q, w, keys, pv, int(wl.row_ctx[r]), g.first_key, g.index_kpool,
-                     g.index_scale, g.index_topk, wl.p_stride, ql, ckv, g.softmax_scale, self._A)
+                     g.index_scale, g.index_topk, wl.p_stride, ql, ckv, g.softmax_scale, self._A,
+                     always_select_tail=g.always_select_tail)
         return time.perf_counter() - t0
 
 
@@ -280,10 +282,18 @@ def cpu_baseline(wl, budget_s: float = 12.0, max_rows: int = 2) -> dict:
 # ---------------------------------------------------------------------------
 
 
+def make_wl(args):
+    wl = (W.long_262k(seq_len=args.seq_len) if (args.seq_len and args.workload == 3)
+          else W.WORKLOADS[args.workload]())
+    if args.always_select_tail:
+        wl.geom = dataclasses.replace(wl.geom, always_select_tail=True)
+    return wl
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return
-    wl = W.WORKLOADS[args.workload]()
+    wl = make_wl(args)
     prefill = args.workload == PREFILL_WORKLOAD
     runner = OracleRunner(wl, with_project=not prefill)
     rows = [r % wl.rows for r in range(min(2, wl.rows))]
@@ -315,6 +325,7 @@ def workload_config(wl, args) -> dict:
             "index_head_dim": g.index_head_dim, "index_topk": g.index_topk, "heads": g.heads,
             "kv_lora_rank": g.kv_lora_rank, "hidden": g.hidden,
             "paged_block": wl.block_size, "seed": wl.seed,
+            "always_select_tail": bool(g.always_select_tail),
             "l2": "flushed between timed steps (256 MiB write, then a 256 MiB read so the dirty "
                   "lines are written back; both outside the timed events)",
             "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
@@ -331,6 +342,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="shrink the 262K workload's sequences (profiling runs only)")
+    ap.add_argument("--always-select-tail", action="store_true",
+                    help="index rows index_topk + kpool - 1 wide, the trailing partial "
+                         "pool's tokens always attended")
     args = ap.parse_args()
     ws, rank, local = dist_init(args.gpus)
     if args.impl == "reference":
@@ -348,8 +362,7 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
-    wl = (W.long_262k(seq_len=args.seq_len) if (args.seq_len and args.workload == 3)
-          else W.WORKLOADS[args.workload]())
+    wl = make_wl(args)
     prefill = args.workload == PREFILL_WORKLOAD
     # The prefill chunk's step ends at olat (its o_absorb GEMM is not part of it).
     layer = DsaDecodeLayer(wl, device=str(dev), with_o_absorb=not prefill, keep_olat=prefill)

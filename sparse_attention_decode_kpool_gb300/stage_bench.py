@@ -5,12 +5,14 @@
 
 Stages: compress, score, select, expand, attend, project, step. ``--rows`` shrinks
 the prefill chunk (workload 4), ``--seq-len`` the long-context sequences (workload
-3). Each iteration is preceded by a write-then-read of 256 MiB so that the stage
+3); ``--always-select-tail`` widens the index rows by the trailing partial pool.
+Each iteration is preceded by a write-then-read of 256 MiB so that the stage
 starts from a cold L2; the median of the CUDA-event times is printed as one JSON
 line. Meant for profiler runs (a fixed, small number of launches of one stage)."""
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 
 import torch
@@ -42,9 +44,12 @@ def main(argv=None) -> None:
     ap.add_argument("--stage", choices=STAGES, default="step")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=1)
+    ap.add_argument("--always-select-tail", action="store_true")
     args = ap.parse_args(argv)
 
     wl = make(args.workload, args.seq_len, args.rows)
+    if args.always_select_tail:
+        wl.geom = dataclasses.replace(wl.geom, always_select_tail=True)
     layer = DsaDecodeLayer(wl)
     layer.compress()
     layer.step()  # every stage's inputs exist from here on
