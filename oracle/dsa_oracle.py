@@ -369,6 +369,77 @@ def dense_masked_attention(qlat_row, ckv_seq, mask, softmax_scale: float) -> np.
 
 
 # ---------------------------------------------------------------------------
+# Decode-time append and the geometry derived from the live length (mod.rs,
+# ``Glm5NextDsaKernels`` fields ``indexer_store`` and ``write_geom``;
+# ``Glm5NextDsaConfig::max_context``)
+
+
+def max_dsa_context(max_context: int, kpool: int) -> int:
+    """Tokens a sequence's indexer cache holds: ``max_context`` rounded down to
+    whole pools (mod.rs, ``max_context`` field doc). Reading: a multiple of
+    ``kpool``."""
+    return (max_context // kpool) * kpool
+
+
+def indexer_store(k_seq, gate_seq, valid_seq, seq_len: int, k_row, gate_row, capacity: int,
+                  ckv_seq=None, ckv_row=None) -> int:
+    """``indexer_store`` for one sequence: the staged indexer row goes to position
+    ``seq_len`` of the sequence's caches, which is marked valid, and the length
+    grows by one (mod.rs: the kernel copies the staged indexer row to a device-side
+    position and marks it valid). The caches are the sequence's logical token-major
+    arrays, updated in place. A full cache (``seq_len >= capacity``) is left
+    unchanged. ``ckv_seq``/``ckv_row``: the layer's latent row for the same token,
+    stored alongside (no counterpart on the pages; the latent cache append).
+    Returns the new length."""
+    if seq_len >= capacity:
+        return seq_len
+    k_seq[seq_len] = k_row
+    gate_seq[seq_len] = gate_row
+    valid_seq[seq_len] = 1
+    if ckv_seq is not None:
+        ckv_seq[seq_len] = ckv_row
+    return seq_len + 1
+
+
+def pools_completed(prev_len: int, new_len: int, first_key: int, kpool: int) -> range:
+    """Pools that are whole at ``new_len`` tokens but were not at ``prev_len``:
+    pool p is whole once ``first_key + (p+1)*kpool <= length`` (mod.rs, "Checkpoint
+    and kernel facts": pooling starts at first_key; a trailing partial pool is not
+    a pool)."""
+    def whole(n):
+        return max(0, (n - first_key) // kpool) if n > first_key else 0
+    return range(whole(prev_len), whole(new_len))
+
+
+def compress_append(k_tok, gate_tok, valid_tok, ape, gamma, beta, eps: float, first_key: int,
+                    kpool: int, prev_len: int, new_len: int, keys_out, pool_valid_out):
+    """Compress only the pools that the tokens ``[prev_len, new_len)`` completed,
+    into the sequence's pooled cache (``keys_out [Pcap, ihd]``, ``pool_valid_out
+    [Pcap]``, updated in place); other pools are not touched. Each such pool is
+    ``kpool_compress`` of the first ``new_len`` tokens."""
+    rng = pools_completed(prev_len, new_len, first_key, kpool)
+    if len(rng) == 0:
+        return rng
+    keys, pv, _ = kpool_compress(np.asarray(k_tok)[:new_len], np.asarray(gate_tok)[:new_len],
+                                 np.asarray(valid_tok)[:new_len], ape, gamma, beta, eps,
+                                 first_key, kpool)
+    keys_out[rng.start:rng.stop] = keys[rng.start:rng.stop]
+    pool_valid_out[rng.start:rng.stop] = pv[rng.start:rng.stop]
+    return rng
+
+
+def write_geom(seq_lens, row_seq=None) -> np.ndarray:
+    """``write_geom``: the selector geometry derived from the live ``seq_len`` on
+    the device (mod.rs: so that a captured graph replays over the live context).
+    Reading: a decode row sees its whole sequence, so its context length is the
+    sequence's current length; the visible pools and the tail follow from it."""
+    seq_lens = np.asarray(seq_lens, dtype=np.int64)
+    if row_seq is None:
+        return seq_lens.copy()
+    return seq_lens[np.asarray(row_seq, dtype=np.int64)]
+
+
+# ---------------------------------------------------------------------------
 # Cache addressing (the oracle's own, independent of the kernels')
 
 

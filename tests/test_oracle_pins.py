@@ -375,6 +375,75 @@ def test_dense_equivalence_with_tail():
 
 
 # ---------------------------------------------------------------------------
+# decode-time append and geometry
+
+
+def test_append_geometry_golden():
+    g = load_kv("append_geom.txt")
+    assert len(g["completed"]) == 8
+    for v in g["completed"]:
+        prev, new, fk, kp, lo, hi = (int(x) for x in v)
+        assert O.pools_completed(prev, new, fk, kp) == range(lo, hi), v
+    for v in g["maxctx"]:
+        assert O.max_dsa_context(int(v[0]), int(v[1])) == int(v[2])
+    np.testing.assert_array_equal(
+        O.write_geom(g["geom_seq_lens"][0].astype(int), g["geom_row_seq"][0].astype(int)),
+        g["geom_row_ctx"][0])
+
+
+def test_pools_completed_partition_the_whole_pools():
+    # Over any sequence of appends the completed ranges are disjoint, contiguous,
+    # and together are exactly the pools whole at the final length.
+    rng = np.random.default_rng(13)
+    for _ in range(300):
+        kp = int(rng.integers(1, 9))
+        fk = int(rng.integers(0, 7))
+        lens = np.cumsum(rng.integers(0, 6, size=int(rng.integers(1, 12))))
+        seen = []
+        prev = 0
+        for L in lens:
+            r = O.pools_completed(prev, int(L), fk, kp)
+            assert r.start == (len(seen) if seen else 0) or len(r) == 0
+            seen.extend(r)
+            prev = int(L)
+        P = max(0, (prev - fk) // kp)
+        assert seen == list(range(P))
+
+
+def test_store_then_incremental_compress_equals_one_shot():
+    g = W.Geometry(index_kpool=4, index_heads=4, index_head_dim=32, index_topk=64, heads=2,
+                   hidden=32, kv_lora_rank=32)
+    wl = W.make_workload("t", 31, g, [61], invalid_per_seq=5)
+    k = wl.k_raw.float().numpy()[0]
+    gt = wl.gate.float().numpy()[0]
+    v = wl.valid.numpy()[0]
+    ln = (wl.ape.numpy(), wl.ln_w.float().numpy(), wl.ln_b.float().numpy(), g.eps)
+    for fk in (0, 3):
+        L0 = 17
+        kc, gc, vc = np.zeros_like(k), np.zeros_like(gt), np.zeros_like(v)
+        kc[:L0], gc[:L0], vc[:L0] = k[:L0], gt[:L0], v[:L0]
+        keys = np.full((64, k.shape[1]), np.nan)
+        pv = np.full(64, 7, dtype=np.uint8)
+        O.compress_append(kc, gc, vc, *ln, fk, 4, 0, L0, keys, pv)
+        L = L0
+        for t in range(L0, 61):
+            L = O.indexer_store(kc, gc, vc, L, k[t], gt[t], capacity=61)
+            if not v[t]:
+                vc[t] = 0  # the workload's own invalid tokens stay invalid
+            O.compress_append(kc, gc, vc, *ln, fk, 4, L - 1, L, keys, pv)
+        assert L == 61
+        ref_k, ref_v, _ = O.kpool_compress(k, gt, v, *ln, fk, 4)
+        P = ref_k.shape[0]
+        np.testing.assert_array_equal(keys[:P], ref_k)
+        np.testing.assert_array_equal(pv[:P], ref_v)
+        assert np.isnan(keys[P:]).all() and (pv[P:] == 7).all()  # untouched
+    # A full cache is left as it is.
+    kc = np.zeros((3, 2))
+    assert O.indexer_store(kc, kc.copy(), np.zeros(3), 3, [1, 1], [1, 1], capacity=3) == 3
+    assert (kc == 0).all()
+
+
+# ---------------------------------------------------------------------------
 # sparse latent MLA
 
 
