@@ -54,6 +54,7 @@ extern "C" {
 #define DSA_STATUS_BAD_TOKEN 1 /* token id < -1, or >= its sequence's length  */
 #define DSA_STATUS_BAD_BLOCK 2 /* block-table entry outside [0, num_blocks)    */
 #define DSA_STATUS_TIMEOUT 4   /* a pipeline wait gave up after ~1 s (results invalid) */
+#define DSA_STATUS_CACHE_FULL 8 /* dsa_indexer_store: a sequence's cache was full (not stored) */
 
 #define DSA_KV_LORA_RANK 512 /* latent width the attention kernels are built for */
 #define DSA_MAX_KPOOL 16     /* most slots per pool dsa_compress handles         */
@@ -93,7 +94,7 @@ const char* dsa_last_error(void);
 
 /* ABI version of this header (bumped on any signature change). */
 int dsa_abi_version(void);
-#define DSA_ABI_VERSION 2
+#define DSA_ABI_VERSION 3
 
 /*
  * Layer-geometry rules (mod.rs, Glm5NextDsaConfig::validate): index_kpool and
@@ -136,6 +137,66 @@ int dsa_compress(const dsa_bf16* k_raw, const dsa_bf16* gate, const uint8_t* tok
                  const dsa_paging* pg, int first_key, int kpool, int ihd,
                  dsa_bf16* kpool_out, uint8_t* pool_valid, int32_t* pool_idx,
                  int32_t* status, void* stream);
+
+/*
+ * dsa_compress_append -- dsa_compress for the pools that the last new_tokens
+ * tokens of each sequence completed (the decode-time form: only the newly whole
+ * pool is pooled). With L = seq_lens[b] read on the device and
+ * whole(n) = floor((n - first_key) / kpool) for n > first_key, else 0, the pools
+ * p in [whole(max(L - new_tokens, 0)), whole(L)) are written exactly as
+ * dsa_compress writes them (bit-identical); every other row is not touched.
+ * new_tokens >= 1 is a host constant, so a captured graph stays valid as the
+ * lengths grow. Arguments, limits and errors otherwise as dsa_compress.
+ */
+int dsa_compress_append(const dsa_bf16* k_raw, const dsa_bf16* gate, const uint8_t* token_valid,
+                        const float* ape, const dsa_bf16* ln_w, const dsa_bf16* ln_b, float eps,
+                        const dsa_paging* pg, int first_key, int kpool, int ihd, int new_tokens,
+                        dsa_bf16* kpool_out, uint8_t* pool_valid, int32_t* pool_idx,
+                        int32_t* status, void* stream);
+
+/*
+ * dsa_indexer_store -- the decode-time append. mod.rs, Glm5NextDsaKernels:
+ * indexer_store copies the staged indexer row to a device-side position and
+ * marks it valid. For each sequence b, with t = seq_lens[b] read on the device:
+ *
+ *   k_raw[b, t, :] = k_new[b, :]     gate[b, t, :] = gate_new[b, :]
+ *   token_valid[b, t] = 1            ckv[b, t, :] = ckv_new[b, :]  (when given)
+ *   seq_lens[b] = t + 1
+ *
+ * through pg's layout (for a paged cache the block table must already map block
+ * t / block_size). The latent row (ckv, ckv_new) is optional and has no
+ * counterpart on the pages: it is the layer's own cache append for the same
+ * token, done in the same launch. t at or past the capacity (max_seq_len, or
+ * max_blocks * block_size when paged) sets DSA_STATUS_CACHE_FULL and stores
+ * nothing; a bad block-table entry sets DSA_STATUS_BAD_BLOCK and stores nothing;
+ * in both cases seq_lens[b] is left as it was.
+ *
+ * k_new, gate_new [batch, ihd] bf16; ckv_new [batch, kv_lora_rank] bf16
+ * (nullable, with ckv); seq_lens must be pg->seq_lens, writable. k_raw, gate,
+ * ckv: token caches (bf16) of widths ihd, ihd, kv_lora_rank; token_valid: token
+ * cache of width 1 (u8). No host value depends on the lengths, so a captured
+ * graph appends one token per sequence per replay.
+ * Limits: ihd in {64, 128}; kv_lora_rank % 8 == 0; rows 16-byte aligned.
+ */
+int dsa_indexer_store(const dsa_bf16* k_new, const dsa_bf16* gate_new, const dsa_bf16* ckv_new,
+                      int ihd, int kv_lora_rank, const dsa_paging* pg, int32_t* seq_lens,
+                      dsa_bf16* k_raw, dsa_bf16* gate, uint8_t* token_valid, dsa_bf16* ckv,
+                      int32_t* status, void* stream);
+
+/*
+ * dsa_write_geom -- mod.rs, Glm5NextDsaKernels: write_geom derives the selector
+ * geometry on the device from seq_len, so a captured graph replays over the live
+ * context. A decode row sees its whole sequence:
+ *
+ *   row_ctx[r] = seq_lens[row_seq[r]]   (row_seq NULL: seq_lens[r])
+ *
+ * The other kernels take their candidate pools, tails and bounds from row_ctx
+ * (or seq_lens) on the device. A row_seq entry outside [0, batch) gives
+ * row_ctx[r] = 0 and sets DSA_STATUS_BAD_TOKEN.
+ * seq_lens [batch] i32, row_seq [rows] i32, row_ctx [rows] i32 (device).
+ */
+int dsa_write_geom(const int32_t* seq_lens, int batch, const int32_t* row_seq, int rows,
+                   int32_t* row_ctx, int32_t* status, void* stream);
 
 /*
  * dsa_score -- dsa_index_scores. tp.rs, "Why the indexer is replicated": the

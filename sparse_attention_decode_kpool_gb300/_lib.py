@@ -20,7 +20,8 @@ DSA_ERR_CUDA = 4
 DSA_STATUS_BAD_TOKEN = 1
 DSA_STATUS_BAD_BLOCK = 2
 DSA_STATUS_TIMEOUT = 4
-DSA_ABI_VERSION = 2
+DSA_STATUS_CACHE_FULL = 8
+DSA_ABI_VERSION = 3
 
 
 class DsaPaging(ctypes.Structure):
@@ -48,6 +49,10 @@ SIGNATURES = {
     "dsa_validate_config": (_I, [_I, _I, _I, _I]),
     "dsa_select_k": (_I, [_I, _I, _I]),
     "dsa_compress": (_I, [_P, _P, _P, _P, _P, _P, _F, _PG, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "dsa_compress_append": (_I, [_P, _P, _P, _P, _P, _P, _F, _PG, _I, _I, _I, _I, _P, _P, _P, _P,
+                                 _P]),
+    "dsa_indexer_store": (_I, [_P, _P, _P, _I, _I, _PG, _P, _P, _P, _P, _P, _P, _P]),
+    "dsa_write_geom": (_I, [_P, _I, _P, _I, _P, _P, _P]),
     "dsa_score": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _PG, _I, _I, _F, _P, _I, _P, _P]),
     "dsa_score_prefill": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _PG, _I, _I, _F, _P, _I, _P,
                                _P]),

@@ -13,7 +13,8 @@ import torch
 from . import _lib
 from ._lib import DsaPaging, check
 
-__all__ = ["paging", "dsa_compress", "dsa_score", "dsa_score_prefill", "dsa_select", "dsa_expand",
+__all__ = ["paging", "dsa_compress", "dsa_compress_append", "dsa_indexer_store",
+           "dsa_write_geom", "dsa_score", "dsa_score_prefill", "dsa_select", "dsa_expand",
            "dsa_select_expand", "dsa_expand_tail", "dsa_select_expand_tail",
            "dsa_sparse_mla_decode_workspace", "dsa_sparse_mla_decode",
            "dsa_sparse_mla_decode_noalloc", "dsa_latent_project_workspace",
@@ -83,6 +84,47 @@ def dsa_compress(k_raw, gate, token_valid, ape, ln_w, ln_b, eps: float, pg: DsaP
         ctypes.byref(pg), int(first_key), int(kpool), ihd,
         _ptr(kpool_out, torch.bfloat16, "kpool_out"), _ptr(pool_valid, torch.uint8, "pool_valid"),
         _ptr(pool_idx, torch.int32, "pool_idx"), _ptr(status, torch.int32, "status"),
+        _stream(stream)))
+
+
+def dsa_compress_append(k_raw, gate, token_valid, ape, ln_w, ln_b, eps: float, pg: DsaPaging,
+                        first_key: int, kpool: int, new_tokens: int, kpool_out, pool_valid,
+                        pool_idx=None, status=None, stream=None) -> None:
+    """dsa_compress for the pools the last ``new_tokens`` tokens of each sequence
+    completed (the lengths are read on the device)."""
+    ihd = int(k_raw.shape[-1])
+    check(_lib.load().dsa_compress_append(
+        _ptr(k_raw, torch.bfloat16, "k_raw"), _ptr(gate, torch.bfloat16, "gate"),
+        _ptr(token_valid, torch.uint8, "token_valid"), _ptr(ape, torch.float32, "ape"),
+        _ptr(ln_w, torch.bfloat16, "ln_w"), _ptr(ln_b, torch.bfloat16, "ln_b"), float(eps),
+        ctypes.byref(pg), int(first_key), int(kpool), ihd, int(new_tokens),
+        _ptr(kpool_out, torch.bfloat16, "kpool_out"), _ptr(pool_valid, torch.uint8, "pool_valid"),
+        _ptr(pool_idx, torch.int32, "pool_idx"), _ptr(status, torch.int32, "status"),
+        _stream(stream)))
+
+
+def dsa_indexer_store(k_new, gate_new, pg: DsaPaging, seq_lens, k_raw, gate, token_valid,
+                      ckv_new=None, ckv=None, status=None, stream=None) -> None:
+    """Append one staged token per sequence at its current length (read on the
+    device) and advance ``seq_lens`` (the tensor ``pg`` was built from)."""
+    batch, ihd = (int(x) for x in k_new.shape)
+    if tuple(gate_new.shape) != (batch, ihd):
+        raise ValueError(f"gate_new must be [{batch}, {ihd}]")
+    kvl = int(ckv_new.shape[-1]) if ckv_new is not None else 0
+    check(_lib.load().dsa_indexer_store(
+        _ptr(k_new, torch.bfloat16, "k_new"), _ptr(gate_new, torch.bfloat16, "gate_new"),
+        _ptr(ckv_new, torch.bfloat16, "ckv_new"), ihd, kvl, ctypes.byref(pg),
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(k_raw, torch.bfloat16, "k_raw"),
+        _ptr(gate, torch.bfloat16, "gate"), _ptr(token_valid, torch.uint8, "token_valid"),
+        _ptr(ckv, torch.bfloat16, "ckv"), _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def dsa_write_geom(seq_lens, row_seq, row_ctx, status=None, stream=None) -> None:
+    """row_ctx[r] = seq_lens[row_seq[r]] on the device (row_seq None: r)."""
+    check(_lib.load().dsa_write_geom(
+        _ptr(seq_lens, torch.int32, "seq_lens"), int(seq_lens.numel()),
+        _ptr(row_seq, torch.int32, "row_seq"), int(row_ctx.numel()),
+        _ptr(row_ctx, torch.int32, "row_ctx"), _ptr(status, torch.int32, "status"),
         _stream(stream)))
 
 

@@ -15,6 +15,8 @@
 // The softmax uses exp2 of log2(e)-scaled logits, the LayerNorm rsqrt and the final
 // ratio a fast divide: each is within a few f32 ulp, far below the bf16 rounding of
 // the stored key.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace dsa {
@@ -35,9 +37,15 @@ struct CompressArgs {
     float eps;
     int first_key;
     int kpool;
+    int append;  // > 0: only the pools completed by the last `append` tokens
 };
 
 constexpr int kThreads = 256;
+
+// Pools whole among the first n tokens.
+__device__ __forceinline__ int whole_pools(int n, int first_key, int kpool) {
+    return n > first_key ? (n - first_key) / kpool : 0;
+}
 
 template <int IHD, int KPMAX>
 __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
@@ -50,12 +58,13 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
     const int sub = lane % LPP;
     const int c0 = sub * 8;
     const int b = blockIdx.y;
-    const int p = blockIdx.x * PPC + warp * PPW + lane / LPP;
     const int KP = a.kpool;
 
     int L = __ldg(a.pg.seq_lens + b);
     L = min(L, seq_capacity(a.pg));
-    const int P = L > a.first_key ? (L - a.first_key) / KP : 0;
+    const int P = whole_pools(L, a.first_key, KP);
+    const int p0 = a.append > 0 ? whole_pools(max(L - a.append, 0), a.first_key, KP) : 0;
+    const int p = p0 + blockIdx.x * PPC + warp * PPW + lane / LPP;
     bool active = p < P;
     const int t0 = a.first_key + p * KP;
     long long trow = -1, orow = -1;
@@ -225,32 +234,35 @@ int launch(const CompressArgs& a, int pmax, cudaStream_t st) {
 
 using namespace dsa;
 
-extern "C" int dsa_compress(const dsa_bf16* k_raw, const dsa_bf16* gate,
-                            const uint8_t* token_valid, const float* ape, const dsa_bf16* ln_w,
-                            const dsa_bf16* ln_b, float eps, const dsa_paging* pg,
-                            int first_key, int kpool, int ihd, dsa_bf16* kpool_out,
-                            uint8_t* pool_valid, int32_t* pool_idx, int32_t* status,
-                            void* stream) {
+namespace {
+int compress_impl(const char* name, const dsa_bf16* k_raw, const dsa_bf16* gate,
+                  const uint8_t* token_valid, const float* ape, const dsa_bf16* ln_w,
+                  const dsa_bf16* ln_b, float eps, const dsa_paging* pg, int first_key, int kpool,
+                  int ihd, int append, dsa_bf16* kpool_out, uint8_t* pool_valid,
+                  int32_t* pool_idx, int32_t* status, void* stream) {
     if (kpool < 1 || kpool > DSA_MAX_KPOOL)
-        return fail(DSA_ERR_UNSUPPORTED, "dsa_compress: kpool %d outside [1, %d]", kpool,
+        return fail(DSA_ERR_UNSUPPORTED, "%s: kpool %d outside [1, %d]", name, kpool,
                     DSA_MAX_KPOOL);
     if (ihd != 64 && ihd != 128)
-        return fail(DSA_ERR_UNSUPPORTED, "dsa_compress: index_head_dim %d not in {64, 128}", ihd);
-    if (first_key < 0) return fail(DSA_ERR_INVALID_ARG, "dsa_compress: first_key %d < 0", first_key);
-    if (!(eps >= 0.f)) return fail(DSA_ERR_INVALID_ARG, "dsa_compress: eps must be >= 0");
+        return fail(DSA_ERR_UNSUPPORTED, "%s: index_head_dim %d not in {64, 128}", name, ihd);
+    if (first_key < 0) return fail(DSA_ERR_INVALID_ARG, "%s: first_key %d < 0", name, first_key);
+    if (!(eps >= 0.f)) return fail(DSA_ERR_INVALID_ARG, "%s: eps must be >= 0", name);
     Paging P;
     int rc = check_paging(pg, kpool, &P);
     if (rc) return rc;
     if (P.block_table && first_key % kpool != 0)
         return fail(DSA_ERR_UNSUPPORTED,
-                    "dsa_compress: paged layout needs first_key %% kpool == 0 (got %d, %d)",
+                    "%s: paged layout needs first_key %% kpool == 0 (got %d, %d)", name,
                     first_key, kpool);
     if (!k_raw || !gate || !token_valid || !ape || !ln_w || !ln_b || !kpool_out || !pool_valid)
-        return fail(DSA_ERR_INVALID_ARG, "dsa_compress: NULL tensor");
+        return fail(DSA_ERR_INVALID_ARG, "%s: NULL tensor", name);
     if ((((uintptr_t)k_raw) | ((uintptr_t)gate) | ((uintptr_t)kpool_out) | ((uintptr_t)ape) |
          ((uintptr_t)ln_w) | ((uintptr_t)ln_b)) & 15)
-        return fail(DSA_ERR_INVALID_ARG, "dsa_compress: tensors must be 16-byte aligned");
-    const int pmax = P.max_seq_len > first_key ? (P.max_seq_len - first_key) / kpool : 0;
+        return fail(DSA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", name);
+    const int full = P.max_seq_len > first_key ? (P.max_seq_len - first_key) / kpool : 0;
+    // At most ceil(append / kpool) pools become whole over `append` tokens.
+    const int pmax = append > 0 ? (int)std::min<long long>(full, (append + (long long)kpool - 1) / kpool)
+                                : full;
     CompressArgs a;
     a.k_raw = k_raw;
     a.gate = gate;
@@ -266,7 +278,33 @@ extern "C" int dsa_compress(const dsa_bf16* k_raw, const dsa_bf16* gate,
     a.eps = eps;
     a.first_key = first_key;
     a.kpool = kpool;
+    a.append = append;
     cudaStream_t st = (cudaStream_t)stream;
     if (ihd == 128) return kpool <= 4 ? launch<128, 4>(a, pmax, st) : launch<128, 16>(a, pmax, st);
     return kpool <= 4 ? launch<64, 4>(a, pmax, st) : launch<64, 16>(a, pmax, st);
+}
+}  // namespace
+
+extern "C" int dsa_compress(const dsa_bf16* k_raw, const dsa_bf16* gate,
+                            const uint8_t* token_valid, const float* ape, const dsa_bf16* ln_w,
+                            const dsa_bf16* ln_b, float eps, const dsa_paging* pg,
+                            int first_key, int kpool, int ihd, dsa_bf16* kpool_out,
+                            uint8_t* pool_valid, int32_t* pool_idx, int32_t* status,
+                            void* stream) {
+    return compress_impl("dsa_compress", k_raw, gate, token_valid, ape, ln_w, ln_b, eps, pg,
+                         first_key, kpool, ihd, 0, kpool_out, pool_valid, pool_idx, status,
+                         stream);
+}
+
+extern "C" int dsa_compress_append(const dsa_bf16* k_raw, const dsa_bf16* gate,
+                                   const uint8_t* token_valid, const float* ape,
+                                   const dsa_bf16* ln_w, const dsa_bf16* ln_b, float eps,
+                                   const dsa_paging* pg, int first_key, int kpool, int ihd,
+                                   int new_tokens, dsa_bf16* kpool_out, uint8_t* pool_valid,
+                                   int32_t* pool_idx, int32_t* status, void* stream) {
+    if (new_tokens < 1)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_compress_append: new_tokens %d < 1", new_tokens);
+    return compress_impl("dsa_compress_append", k_raw, gate, token_valid, ape, ln_w, ln_b, eps,
+                         pg, first_key, kpool, ihd, new_tokens, kpool_out, pool_valid, pool_idx,
+                         status, stream);
 }

@@ -10,6 +10,7 @@ from __future__ import annotations
 
 from typing import Optional
 
+import numpy as np
 import torch
 
 from . import api
@@ -19,7 +20,7 @@ from .workloads import Workload
 class DsaDecodeLayer:
     def __init__(self, wl: Workload, device: str = "cuda", keep_olat: bool = False,
                  with_o_absorb: bool = True, use_drawn_kpool: bool = False,
-                 score_path: str = "auto", fuse_expand: bool = True):
+                 score_path: str = "auto", fuse_expand: bool = True, decode_from=None):
         g = wl.geom
         self.wl = wl
         self.geom = g
@@ -92,6 +93,103 @@ class DsaDecodeLayer:
         self._fused_ws: Optional[torch.Tensor] = None
         # select() also expands (dsa_select_expand); expand() is then a no-op.
         self.fuse_expand = bool(fuse_expand)
+        # Decode-time append: the caches start at decode_from tokens per sequence and
+        # append_step() appends one staged token per sequence before the step.
+        self.decode_from: Optional[np.ndarray] = None
+        self.append_graph: Optional[torch.cuda.CUDAGraph] = None
+        if decode_from is not None:
+            self._init_append(decode_from)
+
+    # -- decode-time append -------------------------------------------------
+    def _token_rows(self, b: int, t0: int, t1: int) -> np.ndarray:
+        """Flat row numbers of tokens [t0, t1) of sequence b in a token cache."""
+        wl = self.wl
+        t = np.arange(t0, t1, dtype=np.int64)
+        if not wl.paged:
+            return b * wl.max_seq_len + t
+        blk = wl.block_table.numpy()[b, t // wl.block_size].astype(np.int64)
+        return blk * wl.block_size + t % wl.block_size
+
+    def _init_append(self, decode_from) -> None:
+        wl, g = self.wl, self.geom
+        if self.k_raw is None:
+            raise ValueError("decode-time append needs the raw indexer caches")
+        if wl.rows != wl.batch or not (wl.row_seq == np.arange(wl.batch)).all():
+            raise ValueError("decode-time append takes one decode row per sequence")
+        L0 = np.broadcast_to(np.asarray(decode_from, dtype=np.int64), (wl.batch,)).copy()
+        if (L0 < 0).any() or (L0 > wl.seq_lens).any():
+            raise ValueError("decode_from must lie in [0, seq_lens]")
+        self.decode_from = L0
+        # The caches hold only the first L0[b] tokens; later rows are staged one per
+        # step (the workload's own rows, so a step's result can be checked).
+        dev = self.device
+        for b in range(wl.batch):
+            rows = torch.from_numpy(self._token_rows(b, int(L0[b]), int(wl.seq_lens[b]))).to(dev)
+            if rows.numel():
+                self.k_raw.view(-1, g.index_head_dim)[rows] = 0
+                self.gate.view(-1, g.index_head_dim)[rows] = 0
+                self.valid.view(-1)[rows] = 0
+                self.ckv.view(-1, g.kv_lora_rank)[rows] = 0
+        self.seq_lens.copy_(torch.from_numpy(L0.astype(np.int32)))
+        B = wl.batch
+        self.k_new = torch.zeros((B, g.index_head_dim), dtype=torch.bfloat16, device=dev)
+        self.gate_new = torch.zeros_like(self.k_new)
+        self.ckv_new = torch.zeros((B, g.kv_lora_rank), dtype=torch.bfloat16, device=dev)
+        self.row_ctx.copy_(self.seq_lens)
+
+    def staged_rows(self, i: int):
+        """Host rows (k, gate, ckv) [batch, ...] of the token each sequence appends at
+        step i: the workload's token at position decode_from[b] + i (zeros past the
+        workload's own length)."""
+        wl, g = self.wl, self.geom
+        out = []
+        for name, width in (("k_raw", g.index_head_dim), ("gate", g.index_head_dim),
+                            ("ckv", g.kv_lora_rank)):
+            src = getattr(wl, name).reshape(-1, width)
+            rows = torch.zeros((wl.batch, width), dtype=torch.bfloat16)
+            for b in range(wl.batch):
+                t = int(self.decode_from[b]) + i
+                if t < int(wl.seq_lens[b]):
+                    rows[b] = src[int(self._token_rows(b, t, t + 1)[0])]
+            out.append(rows)
+        return tuple(out)
+
+    def stage(self, i: int) -> None:
+        """Copy step i's staged rows into the device buffers append_step() reads."""
+        k, gt, c = self.staged_rows(i)
+        self.k_new.copy_(k)
+        self.gate_new.copy_(gt)
+        self.ckv_new.copy_(c)
+
+    def append_step(self, stream=None) -> None:
+        """indexer_store -> write_geom -> compress of the newly whole pool -> step()."""
+        g = self.geom
+        api.dsa_indexer_store(self.k_new, self.gate_new, self.pg, self.seq_lens, self.k_raw,
+                              self.gate, self.valid, self.ckv_new, self.ckv, self.status,
+                              stream=stream)
+        api.dsa_write_geom(self.seq_lens, self.row_seq, self.row_ctx, self.status, stream=stream)
+        api.dsa_compress_append(self.k_raw, self.gate, self.valid, self.ape, self.ln_w, self.ln_b,
+                                g.eps, self.pg, g.first_key, g.index_kpool, 1, self.kpool,
+                                self.pool_valid, status=self.status, stream=stream)
+        self.step(stream)
+
+    def capture_append(self) -> torch.cuda.CUDAGraph:
+        """Capture append_step() into a CUDA graph. Each replay appends the staged
+        rows at the live lengths and runs the step over the grown context. step()
+        runs once eagerly first (it changes no cache or length)."""
+        if self.decode_from is None:
+            raise ValueError("the layer was not built with decode_from")
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            self.step()
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        torch.cuda.synchronize(self.device)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            self.append_step()
+        self.append_graph = gr
+        return gr
 
     def fused_workspace(self) -> torch.Tensor:
         """Workspace for the one-call form dsa_sparse_mla_decode(..., o_absorb, y)."""
@@ -178,6 +276,10 @@ class DsaDecodeLayer:
         if self.o_absorb is not None:
             n += (R + 63) // 64 + 1  # projection kernel(s) + reduction (either form)
         return n
+
+    def launches_per_append_step(self) -> int:
+        """Library kernel launches one append_step() makes."""
+        return self.launches_per_step() + 3  # store, write_geom, compress of the new pool
 
     # -- graphs ------------------------------------------------------------
     def capture(self) -> torch.cuda.CUDAGraph:

@@ -85,6 +85,33 @@ def test_compress_argument_errors(lib):
     assert "paging" in _err(lib)
 
 
+def test_append_entry_argument_errors(lib):
+    pg = _paging()
+    ca = lambda n, kp=4, ihd=128: lib.dsa_compress_append(
+        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1e-6, ctypes.byref(pg), 0, kp, ihd, n, FAKE, FAKE,
+        None, None, None)
+    assert ca(0) == DSA_ERR_INVALID_ARG and "new_tokens" in _err(lib)
+    assert ca(1, 17) == DSA_ERR_UNSUPPORTED
+    assert ca(1, 4, 96) == DSA_ERR_UNSUPPORTED
+    # dsa_indexer_store(k_new, gate_new, ckv_new, ihd, kvl, pg, seq_lens, k_raw, gate, valid,
+    #                   ckv, status, stream)
+    st = lambda ihd=128, kvl=512, ckv_new=FAKE, ckv=FAKE, sl=FAKE, pgp=ctypes.byref(pg): \
+        lib.dsa_indexer_store(FAKE, FAKE, ckv_new, ihd, kvl, pgp, sl, FAKE, FAKE, FAKE, ckv,
+                              None, None)
+    assert st(ihd=96) == DSA_ERR_UNSUPPORTED
+    assert st(ckv=None) == DSA_ERR_INVALID_ARG and "together" in _err(lib)
+    assert st(kvl=500) == DSA_ERR_INVALID_ARG
+    assert st(sl=FAKE + 64) == DSA_ERR_INVALID_ARG and "seq_lens" in _err(lib)
+    assert st(sl=None) == DSA_ERR_INVALID_ARG
+    assert st(pgp=None) == DSA_ERR_INVALID_ARG
+    assert lib.dsa_indexer_store(FAKE + 8, FAKE, None, 128, 0, ctypes.byref(pg), FAKE, FAKE,
+                                 FAKE, FAKE, None, None, None) == DSA_ERR_INVALID_ARG  # align
+    assert lib.dsa_write_geom(FAKE, 0, None, 4, FAKE, None, None) == DSA_ERR_INVALID_ARG
+    assert lib.dsa_write_geom(FAKE, 2, None, -1, FAKE, None, None) == DSA_ERR_INVALID_ARG
+    assert lib.dsa_write_geom(FAKE, 2, None, 0, None, None, None) == DSA_OK
+    assert lib.dsa_write_geom(None, 2, None, 3, FAKE, None, None) == DSA_ERR_INVALID_ARG
+
+
 def test_score_select_expand_argument_errors(lib):
     pg = _paging()
     score = lambda heads, ihd, kp=4: lib.dsa_score(FAKE, FAKE, 1, heads, ihd, None, None, FAKE,
