@@ -8,6 +8,7 @@ flushed (a 256 MiB write) between timed steps, outside the timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload 3] [--no-cpu-baseline] [--no-e2e] [--always-select-tail]
+                  [--decode-append]
 
 --impl reference times the CPU oracle (the plain float64 restatement of the
 method) on the host, one query row per step, single-threaded.
@@ -165,6 +166,7 @@ def algorithmic_bytes(wl, layer) -> dict:
     selected latent rows, absorbed Q, o_absorb once, the output."""
     g = wl.geom
     pv = layer.pool_valid
+    ctx = layer.row_ctx.cpu().numpy()  # the live context (it grows under --decode-append)
     # candidate pools of each row = valid pools among those visible to the row
     cand = 0
     if wl.paged:
@@ -172,9 +174,9 @@ def algorithmic_bytes(wl, layer) -> dict:
     else:
         for r in range(wl.rows):
             b = int(wl.row_seq[r])
-            nvis = max(0, (int(wl.row_ctx[r]) - g.first_key) // g.index_kpool)
+            nvis = max(0, (int(ctx[r]) - g.first_key) // g.index_kpool)
             cand += int(pv[b, :nvis].sum().item())
-    flags = sum(max(0, (int(wl.row_ctx[r]) - g.first_key) // g.index_kpool) for r in range(wl.rows))
+    flags = sum(max(0, (int(ctx[r]) - g.first_key) // g.index_kpool) for r in range(wl.rows))
     keys = cand * g.index_head_dim * 2
     q = wl.rows * g.index_heads * (g.index_head_dim * 2 + 4)
     sel_tokens = int((layer.token_ids >= 0).sum().item())
@@ -183,9 +185,18 @@ def algorithmic_bytes(wl, layer) -> dict:
     oabs = g.hidden * g.heads * g.kv_lora_rank * 2 if layer.o_absorb is not None else 0
     y = wl.rows * g.hidden * 2 if layer.o_absorb is not None else 0
     olat = wl.rows * g.heads * g.kv_lora_rank * 4 if layer.o_absorb is not None else 0
+    # --decode-append: per sequence the staged rows in and out, the valid byte, and
+    # at most one newly whole pool (kpool token rows of keys, gates and flags in,
+    # one pooled key and flag out).
+    app = 0
+    if layer.decode_from is not None:
+        ihd, kp = g.index_head_dim, g.index_kpool
+        app = wl.batch * (2 * (2 * ihd + g.kv_lora_rank) * 2 + 1
+                          + kp * (2 * ihd * 2 + 1) + ihd * 2 + 1)
     return {"score": keys + flags + q, "attend": latent + qlat, "project": oabs + olat + y,
-            "total": keys + flags + q + latent + qlat + oabs + y, "selected_tokens": sel_tokens,
-            "candidate_pools": cand}
+            "append": app,
+            "total": keys + flags + q + latent + qlat + oabs + y + app,
+            "selected_tokens": sel_tokens, "candidate_pools": cand}
 
 
 def algorithmic_flops(wl, layer) -> dict:
@@ -326,6 +337,7 @@ def workload_config(wl, args) -> dict:
             "kv_lora_rank": g.kv_lora_rank, "hidden": g.hidden,
             "paged_block": wl.block_size, "seed": wl.seed,
             "always_select_tail": bool(g.always_select_tail),
+            "decode_append": bool(getattr(args, "decode_append", False)),
             "l2": "flushed between timed steps (256 MiB write, then a 256 MiB read so the dirty "
                   "lines are written back; both outside the timed events)",
             "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
@@ -342,6 +354,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="shrink the 262K workload's sequences (profiling runs only)")
+    ap.add_argument("--decode-append", action="store_true",
+                    help="each step first appends one token per sequence (indexer store, "
+                         "device-side geometry, compress of the newly whole pool), replayed "
+                         "as one graph over the growing context")
     ap.add_argument("--always-select-tail", action="store_true",
                     help="index rows index_topk + kpool - 1 wide, the trailing partial "
                          "pool's tokens always attended")
@@ -365,7 +381,18 @@ def main():
     wl = make_wl(args)
     prefill = args.workload == PREFILL_WORKLOAD
     # The prefill chunk's step ends at olat (its o_absorb GEMM is not part of it).
-    layer = DsaDecodeLayer(wl, device=str(dev), with_o_absorb=not prefill, keep_olat=prefill)
+    append = bool(args.decode_append)
+    if append and prefill:
+        raise SystemExit("--decode-append applies to the decode workloads")
+    decode_from = None
+    if append:
+        # Room for every replay that appends (warm-up, timed, stage and e2e passes).
+        room = args.warmup + 3 * args.steps + 16
+        decode_from = np.maximum(wl.seq_lens.astype(np.int64) - room, 0)
+    layer = DsaDecodeLayer(wl, device=str(dev), with_o_absorb=not prefill, keep_olat=prefill,
+                           decode_from=decode_from)
+    if append:
+        layer.stage(0)  # the staged rows stay as they are for every replay
     layer.compress()
     torch.cuda.synchronize()
 
@@ -396,19 +423,24 @@ def main():
     torch.cuda.synchronize()
     assert int(layer.status.item()) == 0, "device status flagged during the first step"
 
-    # The timed graph: the step's library calls only.
-    s = torch.cuda.Stream(device=dev)
-    s.wait_stream(torch.cuda.current_stream(dev))
-    with torch.cuda.stream(s):
-        layer.step()
-    torch.cuda.current_stream(dev).wait_stream(s)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        layer.step()
+    # The timed graph: the step's library calls only (with --decode-append, the
+    # append of one token per sequence first: every replay grows the context).
+    if append:
+        graph = layer.capture_append()
+    else:
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            layer.step()
+        torch.cuda.current_stream(dev).wait_stream(s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layer.step()
     # A second graph with timing event nodes at the stage boundaries (external
     # events when the installed torch supports them): per-stage times.
-    stage_names = ["score", "select", "expand", "attend"] + ([] if prefill else ["project"])
+    stage_names = (["append"] if append else []) + ["score", "select", "expand", "attend"] + (
+        [] if prefill else ["project"])
     ns = len(stage_names)
     try:
         ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(ns + 1)]
@@ -424,7 +456,7 @@ def main():
                 getattr(layer, k)()
                 ev[j + 1].record()
 
-    launches = layer.launches_per_step()
+    launches = layer.launches_per_append_step() if append else layer.launches_per_step()
     for _ in range(args.warmup):
         flush.zero_()
         graph.replay()
@@ -477,7 +509,16 @@ def main():
         h_ctx = torch.from_numpy(wl.row_ctx).pin_memory()
         result = layer.olat if prefill else layer.y
         h_y = torch.empty_like(result, device="cpu").pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (h_qidx, h_w, h_qlat, h_ctx))
+        # The step's inputs: query tensors and the row contexts; with --decode-append
+        # the staged token rows instead of the contexts (those follow the lengths on
+        # the device).
+        ins = [(layer.qidx, h_qidx), (layer.w, h_w), (layer.qlat, h_qlat)]
+        if append:
+            ins += [(d, h.pin_memory()) for d, h in zip((layer.k_new, layer.gate_new,
+                                                        layer.ckv_new), layer.staged_rows(0))]
+        else:
+            ins.append((layer.row_ctx, h_ctx))
+        h2d = sum(h.numel() * h.element_size() for _, h in ins)
         d2h = h_y.numel() * h_y.element_size()
         for _ in range(3):
             layer.qidx.copy_(h_qidx, non_blocking=True)
@@ -488,10 +529,8 @@ def main():
             flush.zero_()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-            layer.qidx.copy_(h_qidx, non_blocking=True)
-            layer.w.copy_(h_w, non_blocking=True)
-            layer.qlat.copy_(h_qlat, non_blocking=True)
-            layer.row_ctx.copy_(h_ctx, non_blocking=True)
+            for d, h in ins:
+                d.copy_(h, non_blocking=True)
             graph.replay()
             h_y.copy_(result, non_blocking=True)
             torch.cuda.synchronize()
@@ -499,8 +538,8 @@ def main():
         e2e_ms = max_over_ranks(1e3 * sum(t_e2e) / len(t_e2e), ws)
         e2e = {"value": queries / (e2e_ms * 1e-3), "unit": "queries/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "path": "pinned host qidx/w/qlat/row_ctx -> device, graph replay, "
-                       + ("olat" if prefill else "y") + " -> host"}
+               "path": "pinned host qidx/w/qlat/" + ("staged token rows" if append else "row_ctx")
+                       + " -> device, graph replay, " + ("olat" if prefill else "y") + " -> host"}
 
     if rank != 0:
         return

@@ -199,6 +199,25 @@ int dsa_write_geom(const int32_t* seq_lens, int batch, const int32_t* row_seq, i
                    int32_t* row_ctx, int32_t* status, void* stream);
 
 /*
+ * dsa_decode_append -- dsa_indexer_store, then dsa_write_geom (row_seq NULL,
+ * rows = batch: one decode row per sequence), then dsa_compress_append with
+ * new_tokens = 1, in one launch: every output (caches, lengths, row_ctx, pooled
+ * keys, flags, pool_idx, status bits) is bit-identical to the three calls in
+ * sequence. One CTA per sequence stores the staged rows, advances the length and
+ * writes row_ctx[b]; when the stored token completes a pool, one warp of the same
+ * CTA pools it. No counterpart on the pages beyond the steps it joins.
+ *
+ * Arguments as in the three calls; row_ctx [batch] i32 (device, nullable).
+ * Limits: those of dsa_indexer_store and dsa_compress.
+ */
+int dsa_decode_append(const dsa_bf16* k_new, const dsa_bf16* gate_new, const dsa_bf16* ckv_new,
+                      const float* ape, const dsa_bf16* ln_w, const dsa_bf16* ln_b, float eps,
+                      const dsa_paging* pg, int32_t* seq_lens, int first_key, int kpool, int ihd,
+                      int kv_lora_rank, dsa_bf16* k_raw, dsa_bf16* gate, uint8_t* token_valid,
+                      dsa_bf16* ckv, dsa_bf16* kpool_out, uint8_t* pool_valid, int32_t* pool_idx,
+                      int32_t* row_ctx, int32_t* status, void* stream);
+
+/*
  * dsa_score -- dsa_index_scores. tp.rs, "Why the indexer is replicated": the
  * score adds weights[h] * relu(scale * dot) over the indexer heads; build.rs
  * transform 2: w arrives already multiplied by index_heads^-0.5.

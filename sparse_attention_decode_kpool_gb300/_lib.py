@@ -53,6 +53,8 @@ SIGNATURES = {
                                  _P]),
     "dsa_indexer_store": (_I, [_P, _P, _P, _I, _I, _PG, _P, _P, _P, _P, _P, _P, _P]),
     "dsa_write_geom": (_I, [_P, _I, _P, _I, _P, _P, _P]),
+    "dsa_decode_append": (_I, [_P, _P, _P, _P, _P, _P, _F, _PG, _P, _I, _I, _I, _I, _P, _P, _P,
+                               _P, _P, _P, _P, _P, _P, _P]),
     "dsa_score": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _PG, _I, _I, _F, _P, _I, _P, _P]),
     "dsa_score_prefill": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _PG, _I, _I, _F, _P, _I, _P,
                                _P]),

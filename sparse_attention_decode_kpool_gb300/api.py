@@ -14,7 +14,7 @@ from . import _lib
 from ._lib import DsaPaging, check
 
 __all__ = ["paging", "dsa_compress", "dsa_compress_append", "dsa_indexer_store",
-           "dsa_write_geom", "dsa_score", "dsa_score_prefill", "dsa_select", "dsa_expand",
+           "dsa_write_geom", "dsa_decode_append", "dsa_score", "dsa_score_prefill", "dsa_select", "dsa_expand",
            "dsa_select_expand", "dsa_expand_tail", "dsa_select_expand_tail",
            "dsa_sparse_mla_decode_workspace", "dsa_sparse_mla_decode",
            "dsa_sparse_mla_decode_noalloc", "dsa_latent_project_workspace",
@@ -126,6 +126,28 @@ def dsa_write_geom(seq_lens, row_seq, row_ctx, status=None, stream=None) -> None
         _ptr(row_seq, torch.int32, "row_seq"), int(row_ctx.numel()),
         _ptr(row_ctx, torch.int32, "row_ctx"), _ptr(status, torch.int32, "status"),
         _stream(stream)))
+
+
+def dsa_decode_append(k_new, gate_new, ape, ln_w, ln_b, eps: float, pg: DsaPaging, seq_lens,
+                      first_key: int, kpool: int, k_raw, gate, token_valid, kpool_out, pool_valid,
+                      ckv_new=None, ckv=None, pool_idx=None, row_ctx=None, status=None,
+                      stream=None) -> None:
+    """dsa_indexer_store + dsa_write_geom + dsa_compress_append(new_tokens=1) in one
+    launch (identical results)."""
+    batch, ihd = (int(x) for x in k_new.shape)
+    if tuple(gate_new.shape) != (batch, ihd):
+        raise ValueError(f"gate_new must be [{batch}, {ihd}]")
+    kvl = int(ckv_new.shape[-1]) if ckv_new is not None else 0
+    check(_lib.load().dsa_decode_append(
+        _ptr(k_new, torch.bfloat16, "k_new"), _ptr(gate_new, torch.bfloat16, "gate_new"),
+        _ptr(ckv_new, torch.bfloat16, "ckv_new"), _ptr(ape, torch.float32, "ape"),
+        _ptr(ln_w, torch.bfloat16, "ln_w"), _ptr(ln_b, torch.bfloat16, "ln_b"), float(eps),
+        ctypes.byref(pg), _ptr(seq_lens, torch.int32, "seq_lens"), int(first_key), int(kpool),
+        ihd, kvl, _ptr(k_raw, torch.bfloat16, "k_raw"), _ptr(gate, torch.bfloat16, "gate"),
+        _ptr(token_valid, torch.uint8, "token_valid"), _ptr(ckv, torch.bfloat16, "ckv"),
+        _ptr(kpool_out, torch.bfloat16, "kpool_out"), _ptr(pool_valid, torch.uint8, "pool_valid"),
+        _ptr(pool_idx, torch.int32, "pool_idx"), _ptr(row_ctx, torch.int32, "row_ctx"),
+        _ptr(status, torch.int32, "status"), _stream(stream)))
 
 
 def dsa_score(qidx, w, row_seq, row_ctx, kpool, pool_valid, pg: DsaPaging, first_key: int,

@@ -12,6 +12,7 @@
 //
 // dsa_write_geom: row r's context length is its sequence's current length.
 #include "common.cuh"
+#include "store.cuh"
 
 namespace dsa {
 namespace {
@@ -38,39 +39,12 @@ __global__ void __launch_bounds__(kStoreThreads) indexer_store_kernel(StoreArgs 
     __shared__ long long s_row;
     __shared__ int s_t;
     const int b = blockIdx.x;
-    if (threadIdx.x == 0) {
-        const int t = a.seq_lens[b];
-        long long row = -1;
-        if (t < 0 || t >= seq_capacity(a.pg)) {
-            flag_status(a.status, DSA_STATUS_CACHE_FULL);
-        } else {
-            row = token_row(a.pg, b, t);
-            if (row < 0) flag_status(a.status, DSA_STATUS_BAD_BLOCK);
-        }
-        s_row = row;
-        s_t = t;
-    }
+    if (threadIdx.x == 0) s_row = next_token_row(a.pg, a.seq_lens, b, &s_t, a.status);
     __syncthreads();
     const long long row = s_row;
     if (row < 0) return;
-    // 16-byte vectors: ihd / 8 of the key row, as many of the gate row, kvl / 8 of
-    // the latent row.
-    const int nk = a.ihd / 8, nl = a.ckv ? a.kvl / 8 : 0;
-    for (int i = threadIdx.x; i < 2 * nk + nl; i += kStoreThreads) {
-        if (i < nk) {
-            *reinterpret_cast<uint4*>(a.k_raw + row * a.ihd + 8 * i) =
-                ldg16(a.k_new + (long long)b * a.ihd + 8 * i);
-        } else if (i < 2 * nk) {
-            const int j = i - nk;
-            *reinterpret_cast<uint4*>(a.gate + row * a.ihd + 8 * j) =
-                ldg16(a.gate_new + (long long)b * a.ihd + 8 * j);
-        } else {
-            const int j = i - 2 * nk;
-            *reinterpret_cast<uint4*>(a.ckv + row * a.kvl + 8 * j) =
-                ldg16(a.ckv_new + (long long)b * a.kvl + 8 * j);
-        }
-    }
-    if (threadIdx.x == 0) a.valid[row] = 1;
+    store_token_rows(a.k_new, a.gate_new, a.ckv_new, a.k_raw, a.gate, a.valid, a.ckv, b, row,
+                     a.ihd, a.kvl);
     __syncthreads();  // every thread has used s_t's position before the length moves
     if (threadIdx.x == 0) a.seq_lens[b] = s_t + 1;
 }

@@ -18,6 +18,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "store.cuh"
 
 namespace dsa {
 namespace {
@@ -47,54 +48,21 @@ __device__ __forceinline__ int whole_pools(int n, int first_key, int kpool) {
     return n > first_key ? (n - first_key) / kpool : 0;
 }
 
+// The pooled key of one pool for the 8 channels [c0, c0 + 8) this lane owns, from
+// its kpool rows of raw keys (kr) and gate logits (gr): LayerNorm per slot (the
+// pool's IHD/8 lanes reduce together, so every lane of the warp must call this),
+// bf16 rounding of the normalised key, and the slot softmax in the log2 domain.
+// Returns the packed bf16 result (to be stored only for a valid pool).
 template <int IHD, int KPMAX>
-__global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
-    pdl_wait();
-    constexpr int LPP = IHD / 8;     // lanes per pool
-    constexpr int PPW = 32 / LPP;    // pools per warp
-    constexpr int PPC = PPW * (kThreads / 32);
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int sub = lane % LPP;
-    const int c0 = sub * 8;
-    const int b = blockIdx.y;
-    const int KP = a.kpool;
-
-    int L = __ldg(a.pg.seq_lens + b);
-    L = min(L, seq_capacity(a.pg));
-    const int P = whole_pools(L, a.first_key, KP);
-    const int p0 = a.append > 0 ? whole_pools(max(L - a.append, 0), a.first_key, KP) : 0;
-    const int p = p0 + blockIdx.x * PPC + warp * PPW + lane / LPP;
-    bool active = p < P;
-    const int t0 = a.first_key + p * KP;
-    long long trow = -1, orow = -1;
-    if (active) {
-        trow = token_row(a.pg, b, t0);  // all slots of a pool share one block
-        orow = pool_row(a.pg, b, p, KP);
-        if (trow < 0 || orow < 0) {
-            if (sub == 0) flag_status(a.status, DSA_STATUS_BAD_BLOCK);
-            active = false;
-        }
-    }
-
-    uint4 kr[KPMAX], gr[KPMAX];
-    bool ok = true;
-#pragma unroll
-    for (int s = 0; s < KPMAX; ++s) {
-        kr[s] = make_uint4(0, 0, 0, 0);
-        gr[s] = make_uint4(0, 0, 0, 0);
-        if (s < KP && active) {
-            const long long row = trow + s;
-            kr[s] = ldg16_stream(a.k_raw + row * IHD + c0);
-            gr[s] = ldg16_stream(a.gate + row * IHD + c0);
-            ok = ok && (__ldg(a.valid + row) != 0);
-        }
-    }
-
+__device__ __forceinline__ uint4 pool_lane(const uint4 (&kr)[KPMAX], const uint4 (&gr)[KPMAX],
+                                           int KP, const float* __restrict__ ape,
+                                           const uint16_t* __restrict__ ln_w,
+                                           const uint16_t* __restrict__ ln_b, float eps, int c0) {
+    constexpr int LPP = IHD / 8;
     float lw[8], lb[8];
     {
-        const uint4 w4 = ldg16(a.ln_w + c0);
-        const uint4 b4 = ldg16(a.ln_b + c0);
+        const uint4 w4 = ldg16(ln_w + c0);
+        const uint4 b4 = ldg16(ln_b + c0);
         const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
         const uint32_t bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
@@ -116,8 +84,8 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
 #pragma unroll
     for (int s = 0; s < KPMAX; ++s) {
         if (s < KP) {
-            const float4 ap0 = __ldg(reinterpret_cast<const float4*>(a.ape + s * IHD + c0));
-            const float4 ap1 = __ldg(reinterpret_cast<const float4*>(a.ape + s * IHD + c0 + 4));
+            const float4 ap0 = __ldg(reinterpret_cast<const float4*>(ape + s * IHD + c0));
+            const float4 ap1 = __ldg(reinterpret_cast<const float4*>(ape + s * IHD + c0 + 4));
             const float ap[8] = {ap0.x, ap0.y, ap0.z, ap0.w, ap1.x, ap1.y, ap1.z, ap1.w};
             const uint32_t gv[4] = {gr[s].x, gr[s].y, gr[s].z, gr[s].w};
 #pragma unroll
@@ -167,16 +135,16 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
             }
 #pragma unroll
             for (int off = LPP / 2; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-            const float rstd = rsqrtf(fmaf(sq, 1.0f / IHD, a.eps));
+            const float rstd = rsqrtf(fmaf(sq, 1.0f / IHD, eps));
 
             float l[8];
             if (s < KC) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) l[i] = lg[s < KC ? s : 0][i];
             } else {
-                const float4 ap0 = __ldg(reinterpret_cast<const float4*>(a.ape + s * IHD + c0));
+                const float4 ap0 = __ldg(reinterpret_cast<const float4*>(ape + s * IHD + c0));
                 const float4 ap1 =
-                    __ldg(reinterpret_cast<const float4*>(a.ape + s * IHD + c0 + 4));
+                    __ldg(reinterpret_cast<const float4*>(ape + s * IHD + c0 + 4));
                 const float ap[8] = {ap0.x, ap0.y, ap0.z, ap0.w, ap1.x, ap1.y, ap1.z, ap1.w};
                 const uint32_t gv[4] = {gr[s].x, gr[s].y, gr[s].z, gr[s].w};
 #pragma unroll
@@ -195,23 +163,159 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
         }
     }
 
+    uint4 o;
+    o.x = pack_bf16x2(__fdividef(num[0], den[0]), __fdividef(num[1], den[1]));
+    o.y = pack_bf16x2(__fdividef(num[2], den[2]), __fdividef(num[3], den[3]));
+    o.z = pack_bf16x2(__fdividef(num[4], den[4]), __fdividef(num[5], den[5]));
+    o.w = pack_bf16x2(__fdividef(num[6], den[6]), __fdividef(num[7], den[7]));
+    return o;
+}
+
+template <int IHD, int KPMAX>
+__global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
+    pdl_wait();
+    constexpr int LPP = IHD / 8;     // lanes per pool
+    constexpr int PPW = 32 / LPP;    // pools per warp
+    constexpr int PPC = PPW * (kThreads / 32);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int sub = lane % LPP;
+    const int c0 = sub * 8;
+    const int b = blockIdx.y;
+    const int KP = a.kpool;
+
+    int L = __ldg(a.pg.seq_lens + b);
+    L = min(L, seq_capacity(a.pg));
+    const int P = whole_pools(L, a.first_key, KP);
+    const int p0 = a.append > 0 ? whole_pools(max(L - a.append, 0), a.first_key, KP) : 0;
+    const int p = p0 + blockIdx.x * PPC + warp * PPW + lane / LPP;
+    bool active = p < P;
+    const int t0 = a.first_key + p * KP;
+    long long trow = -1, orow = -1;
+    if (active) {
+        trow = token_row(a.pg, b, t0);  // all slots of a pool share one block
+        orow = pool_row(a.pg, b, p, KP);
+        if (trow < 0 || orow < 0) {
+            if (sub == 0) flag_status(a.status, DSA_STATUS_BAD_BLOCK);
+            active = false;
+        }
+    }
+
+    uint4 kr[KPMAX], gr[KPMAX];
+    bool ok = true;
+#pragma unroll
+    for (int s = 0; s < KPMAX; ++s) {
+        kr[s] = make_uint4(0, 0, 0, 0);
+        gr[s] = make_uint4(0, 0, 0, 0);
+        if (s < KP && active) {
+            const long long row = trow + s;
+            kr[s] = ldg16_stream(a.k_raw + row * IHD + c0);
+            gr[s] = ldg16_stream(a.gate + row * IHD + c0);
+            ok = ok && (__ldg(a.valid + row) != 0);
+        }
+    }
+
+    const uint4 pooled = pool_lane<IHD, KPMAX>(kr, gr, KP, a.ape, a.ln_w, a.ln_b, a.eps, c0);
     if (!active) return;
     const bool pv = ok;
-    uint4 o;
-    if (pv) {
-        o.x = pack_bf16x2(__fdividef(num[0], den[0]), __fdividef(num[1], den[1]));
-        o.y = pack_bf16x2(__fdividef(num[2], den[2]), __fdividef(num[3], den[3]));
-        o.z = pack_bf16x2(__fdividef(num[4], den[4]), __fdividef(num[5], den[5]));
-        o.w = pack_bf16x2(__fdividef(num[6], den[6]), __fdividef(num[7], den[7]));
-    } else {
-        o = make_uint4(0, 0, 0, 0);
-    }
-    *reinterpret_cast<uint4*>(a.kout + orow * IHD + c0) = o;
+    *reinterpret_cast<uint4*>(a.kout + orow * IHD + c0) = pv ? pooled : make_uint4(0, 0, 0, 0);
     if (sub == 0) {
         a.pvalid[orow] = pv ? 1 : 0;
         if (a.pidx) {
             for (int s = 0; s < KP; ++s) a.pidx[orow * KP + s] = t0 + s;
         }
+    }
+}
+
+// dsa_decode_append: one CTA per sequence stores the staged token at the live
+// length, advances the length, writes the row context, and (warp 0) pools the pool
+// that token completed, with the same pool_lane arithmetic as compress_kernel.
+struct AppendArgs {
+    const uint16_t* k_new;
+    const uint16_t* gate_new;
+    const uint16_t* ckv_new;
+    uint16_t* k_raw;
+    uint16_t* gate;
+    uint8_t* valid;
+    uint16_t* ckv;
+    int32_t* seq_lens;
+    int32_t* row_ctx;
+    int32_t* status;
+    const float* ape;
+    const uint16_t* ln_w;
+    const uint16_t* ln_b;
+    uint16_t* kout;
+    uint8_t* pvalid;
+    int32_t* pidx;
+    Paging pg;
+    float eps;
+    int first_key;
+    int kpool;
+    int kvl;
+};
+
+constexpr int kAppendThreads = 128;
+
+template <int IHD, int KPMAX>
+__global__ void __launch_bounds__(kAppendThreads) decode_append_kernel(AppendArgs a) {
+    pdl_wait();
+    constexpr int LPP = IHD / 8;
+    __shared__ long long s_row;
+    __shared__ int s_t;
+    const int b = blockIdx.x;
+    if (threadIdx.x == 0) s_row = next_token_row(a.pg, a.seq_lens, b, &s_t, a.status);
+    __syncthreads();
+    const long long row = s_row;
+    const int t = s_t;
+    if (row >= 0)
+        store_token_rows(a.k_new, a.gate_new, a.ckv_new, a.k_raw, a.gate, a.valid, a.ckv, b, row,
+                         IHD, a.kvl);
+    __syncthreads();  // the stored rows are visible to the whole block from here on
+    const int L = row >= 0 ? t + 1 : t;
+    if (threadIdx.x == 0) {
+        if (row >= 0) a.seq_lens[b] = L;
+        if (a.row_ctx) a.row_ctx[b] = L;
+    }
+    const int KP = a.kpool;
+    const int Lc = min(L, seq_capacity(a.pg));
+    const int P = whole_pools(Lc, a.first_key, KP);
+    const int p = whole_pools(max(Lc - 1, 0), a.first_key, KP);  // the pool the token completed
+    if (p >= P || threadIdx.x >= 32) return;  // block-uniform, then warp 0 only
+
+    const int lane = threadIdx.x;
+    const int c0 = (lane % LPP) * 8;
+    bool active = lane < LPP;  // lanes past the pool's width join the shuffles with zeros
+    const int t0 = a.first_key + p * KP;
+    long long trow = -1, orow = -1;
+    if (active) {
+        trow = token_row(a.pg, b, t0);
+        orow = pool_row(a.pg, b, p, KP);
+        if (trow < 0 || orow < 0) {
+            if (lane == 0) flag_status(a.status, DSA_STATUS_BAD_BLOCK);
+            active = false;
+        }
+    }
+    uint4 kr[KPMAX], gr[KPMAX];
+    bool ok = true;
+#pragma unroll
+    for (int s = 0; s < KPMAX; ++s) {
+        kr[s] = make_uint4(0, 0, 0, 0);
+        gr[s] = make_uint4(0, 0, 0, 0);
+        if (s < KP && active) {
+            // Plain (coherent) loads: this block wrote the newest row.
+            const long long r = trow + s;
+            kr[s] = *reinterpret_cast<const uint4*>(a.k_raw + r * IHD + c0);
+            gr[s] = *reinterpret_cast<const uint4*>(a.gate + r * IHD + c0);
+            ok = ok && (a.valid[r] != 0);
+        }
+    }
+    const uint4 pooled = pool_lane<IHD, KPMAX>(kr, gr, KP, a.ape, a.ln_w, a.ln_b, a.eps, c0);
+    if (!active) return;
+    *reinterpret_cast<uint4*>(a.kout + orow * IHD + c0) = ok ? pooled : make_uint4(0, 0, 0, 0);
+    if (lane == 0) {
+        a.pvalid[orow] = ok ? 1 : 0;
+        if (a.pidx)
+            for (int s = 0; s < KP; ++s) a.pidx[orow * KP + s] = t0 + s;
     }
 }
 
@@ -307,4 +411,78 @@ extern "C" int dsa_compress_append(const dsa_bf16* k_raw, const dsa_bf16* gate,
     return compress_impl("dsa_compress_append", k_raw, gate, token_valid, ape, ln_w, ln_b, eps,
                          pg, first_key, kpool, ihd, new_tokens, kpool_out, pool_valid, pool_idx,
                          status, stream);
+}
+
+extern "C" int dsa_decode_append(const dsa_bf16* k_new, const dsa_bf16* gate_new,
+                                 const dsa_bf16* ckv_new, const float* ape, const dsa_bf16* ln_w,
+                                 const dsa_bf16* ln_b, float eps, const dsa_paging* pg,
+                                 int32_t* seq_lens, int first_key, int kpool, int ihd,
+                                 int kv_lora_rank, dsa_bf16* k_raw, dsa_bf16* gate,
+                                 uint8_t* token_valid, dsa_bf16* ckv, dsa_bf16* kpool_out,
+                                 uint8_t* pool_valid, int32_t* pool_idx, int32_t* row_ctx,
+                                 int32_t* status, void* stream) {
+    const char* name = "dsa_decode_append";
+    if (kpool < 1 || kpool > DSA_MAX_KPOOL)
+        return fail(DSA_ERR_UNSUPPORTED, "%s: kpool %d outside [1, %d]", name, kpool,
+                    DSA_MAX_KPOOL);
+    if (ihd != 64 && ihd != 128)
+        return fail(DSA_ERR_UNSUPPORTED, "%s: index_head_dim %d not in {64, 128}", name, ihd);
+    if (first_key < 0) return fail(DSA_ERR_INVALID_ARG, "%s: first_key %d < 0", name, first_key);
+    if (!(eps >= 0.f)) return fail(DSA_ERR_INVALID_ARG, "%s: eps must be >= 0", name);
+    if ((ckv == nullptr) != (ckv_new == nullptr))
+        return fail(DSA_ERR_INVALID_ARG, "%s: ckv and ckv_new go together", name);
+    if (ckv && (kv_lora_rank < 8 || kv_lora_rank % 8 != 0))
+        return fail(DSA_ERR_INVALID_ARG, "%s: kv_lora_rank %d not a multiple of 8", name,
+                    kv_lora_rank);
+    Paging P;
+    int rc = check_paging(pg, kpool, &P);
+    if (rc) return rc;
+    if (P.block_table && first_key % kpool != 0)
+        return fail(DSA_ERR_UNSUPPORTED,
+                    "%s: paged layout needs first_key %% kpool == 0 (got %d, %d)", name,
+                    first_key, kpool);
+    if (!seq_lens || seq_lens != pg->seq_lens)
+        return fail(DSA_ERR_INVALID_ARG, "%s: seq_lens must be the descriptor's (writable) lengths",
+                    name);
+    if (!k_new || !gate_new || !k_raw || !gate || !token_valid || !ape || !ln_w || !ln_b ||
+        !kpool_out || !pool_valid)
+        return fail(DSA_ERR_INVALID_ARG, "%s: NULL tensor", name);
+    if ((((uintptr_t)k_new) | ((uintptr_t)gate_new) | ((uintptr_t)ckv_new) | ((uintptr_t)k_raw) |
+         ((uintptr_t)gate) | ((uintptr_t)ckv) | ((uintptr_t)kpool_out) | ((uintptr_t)ape) |
+         ((uintptr_t)ln_w) | ((uintptr_t)ln_b)) & 15)
+        return fail(DSA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", name);
+    AppendArgs a;
+    a.k_new = k_new;
+    a.gate_new = gate_new;
+    a.ckv_new = ckv_new;
+    a.k_raw = k_raw;
+    a.gate = gate;
+    a.valid = token_valid;
+    a.ckv = ckv;
+    a.seq_lens = seq_lens;
+    a.row_ctx = row_ctx;
+    a.status = status;
+    a.ape = ape;
+    a.ln_w = ln_w;
+    a.ln_b = ln_b;
+    a.kout = kpool_out;
+    a.pvalid = pool_valid;
+    a.pidx = pool_idx;
+    a.pg = P;
+    a.eps = eps;
+    a.first_key = first_key;
+    a.kpool = kpool;
+    a.kvl = kv_lora_rank;
+    const dim3 grid((unsigned)P.batch), block(kAppendThreads);
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e;
+    if (ihd == 128)
+        e = kpool <= 4 ? launch_pdl(decode_append_kernel<128, 4>, grid, block, 0, st, a)
+                       : launch_pdl(decode_append_kernel<128, 16>, grid, block, 0, st, a);
+    else
+        e = kpool <= 4 ? launch_pdl(decode_append_kernel<64, 4>, grid, block, 0, st, a)
+                       : launch_pdl(decode_append_kernel<64, 16>, grid, block, 0, st, a);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_decode_append launch");
+    return DSA_OK;
 }

@@ -20,7 +20,8 @@ from .workloads import Workload
 class DsaDecodeLayer:
     def __init__(self, wl: Workload, device: str = "cuda", keep_olat: bool = False,
                  with_o_absorb: bool = True, use_drawn_kpool: bool = False,
-                 score_path: str = "auto", fuse_expand: bool = True, decode_from=None):
+                 score_path: str = "auto", fuse_expand: bool = True, decode_from=None,
+                 fuse_append: bool = True):
         g = wl.geom
         self.wl = wl
         self.geom = g
@@ -95,6 +96,8 @@ class DsaDecodeLayer:
         self.fuse_expand = bool(fuse_expand)
         # Decode-time append: the caches start at decode_from tokens per sequence and
         # append_step() appends one staged token per sequence before the step.
+        # append() is one dsa_decode_append launch, or the three calls it joins.
+        self.fuse_append = bool(fuse_append)
         self.decode_from: Optional[np.ndarray] = None
         self.append_graph: Optional[torch.cuda.CUDAGraph] = None
         if decode_from is not None:
@@ -162,8 +165,20 @@ class DsaDecodeLayer:
         self.ckv_new.copy_(c)
 
     def append_step(self, stream=None) -> None:
-        """indexer_store -> write_geom -> compress of the newly whole pool -> step()."""
+        """append() then step(): one decode step over the grown context."""
+        self.append(stream)
+        self.step(stream)
+
+    def append(self, stream=None) -> None:
+        """indexer_store -> write_geom -> compress of the newly whole pool."""
         g = self.geom
+        if self.fuse_append:
+            api.dsa_decode_append(self.k_new, self.gate_new, self.ape, self.ln_w, self.ln_b, g.eps,
+                                  self.pg, self.seq_lens, g.first_key, g.index_kpool, self.k_raw,
+                                  self.gate, self.valid, self.kpool, self.pool_valid,
+                                  ckv_new=self.ckv_new, ckv=self.ckv, row_ctx=self.row_ctx,
+                                  status=self.status, stream=stream)
+            return
         api.dsa_indexer_store(self.k_new, self.gate_new, self.pg, self.seq_lens, self.k_raw,
                               self.gate, self.valid, self.ckv_new, self.ckv, self.status,
                               stream=stream)
@@ -171,7 +186,6 @@ class DsaDecodeLayer:
         api.dsa_compress_append(self.k_raw, self.gate, self.valid, self.ape, self.ln_w, self.ln_b,
                                 g.eps, self.pg, g.first_key, g.index_kpool, 1, self.kpool,
                                 self.pool_valid, status=self.status, stream=stream)
-        self.step(stream)
 
     def capture_append(self) -> torch.cuda.CUDAGraph:
         """Capture append_step() into a CUDA graph. Each replay appends the staged
@@ -279,7 +293,8 @@ class DsaDecodeLayer:
 
     def launches_per_append_step(self) -> int:
         """Library kernel launches one append_step() makes."""
-        return self.launches_per_step() + 3  # store, write_geom, compress of the new pool
+        # store, write_geom, compress of the new pool (one launch when fused)
+        return self.launches_per_step() + (1 if self.fuse_append else 3)
 
     # -- graphs ------------------------------------------------------------
     def capture(self) -> torch.cuda.CUDAGraph:

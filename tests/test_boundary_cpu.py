@@ -106,6 +106,21 @@ def test_append_entry_argument_errors(lib):
     assert st(pgp=None) == DSA_ERR_INVALID_ARG
     assert lib.dsa_indexer_store(FAKE + 8, FAKE, None, 128, 0, ctypes.byref(pg), FAKE, FAKE,
                                  FAKE, FAKE, None, None, None) == DSA_ERR_INVALID_ARG  # align
+    # dsa_decode_append(k_new, gate_new, ckv_new, ape, ln_w, ln_b, eps, pg, seq_lens, fk,
+    #                   kpool, ihd, kvl, k_raw, gate, valid, ckv, kpool_out, pool_valid,
+    #                   pool_idx, row_ctx, status, stream)
+    da = lambda kp=4, ihd=128, kvl=512, ckv=FAKE, sl=FAKE, fk=0, pgp=ctypes.byref(pg): \
+        lib.dsa_decode_append(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1e-6, pgp, sl, fk, kp, ihd, kvl,
+                              FAKE, FAKE, FAKE, ckv, FAKE, FAKE, None, None, None, None)
+    assert da(kp=17) == DSA_ERR_UNSUPPORTED
+    assert da(ihd=96) == DSA_ERR_UNSUPPORTED
+    assert da(fk=-1) == DSA_ERR_INVALID_ARG
+    assert da(ckv=None) == DSA_ERR_INVALID_ARG and "together" in _err(lib)
+    assert da(kvl=12) == DSA_ERR_INVALID_ARG
+    assert da(sl=FAKE + 4) == DSA_ERR_INVALID_ARG and "seq_lens" in _err(lib)
+    assert da(pgp=None) == DSA_ERR_INVALID_ARG
+    paged = _paging(block_table=FAKE, max_blocks=16, block_size=64, nb=8)
+    assert da(fk=2, pgp=ctypes.byref(paged)) == DSA_ERR_UNSUPPORTED  # first_key % kpool
     assert lib.dsa_write_geom(FAKE, 0, None, 4, FAKE, None, None) == DSA_ERR_INVALID_ARG
     assert lib.dsa_write_geom(FAKE, 2, None, -1, FAKE, None, None) == DSA_ERR_INVALID_ARG
     assert lib.dsa_write_geom(FAKE, 2, None, 0, None, None, None) == DSA_OK

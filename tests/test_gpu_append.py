@@ -22,10 +22,11 @@ def _cuda():
 
 
 CASES = [
-    # name, seq_lens, block_size, first_key, steps, always_select_tail
-    ("contig", [300, 517, 77], None, 0, 9, False),
-    ("contig-fk3-tail", [300, 517, 77], None, 3, 9, True),
-    ("paged-fk4-tail", [300, 517, 130], 64, 4, 9, True),
+    # name, seq_lens, block_size, first_key, steps, always_select_tail, graph layer's append
+    # fused (the eager twin takes the other form, so the two forms are compared bit for bit)
+    ("contig", [300, 517, 77], None, 0, 9, False, True),
+    ("contig-fk3-tail", [300, 517, 77], None, 3, 9, True, False),
+    ("paged-fk4-tail", [300, 517, 130], 64, 4, 9, True, True),
 ]
 
 
@@ -47,14 +48,14 @@ def _snapshot(layer):
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_append_graph_replay(case):
-    name, lens, bs, fk, n, tail = case
+    name, lens, bs, fk, n, tail, fused = case
     g = W.Geometry(index_kpool=4, index_heads=32, index_head_dim=128, index_topk=256, heads=8,
                    hidden=256, first_key=fk, always_select_tail=tail)
     wl = W.make_workload(f"append-{name}", 41, g, lens, block_size=bs,
                          max_seq_len=576 if bs else None, invalid_per_seq=3)
     L0 = wl.seq_lens.astype(np.int64) - n
-    graph_layer = DsaDecodeLayer(wl, keep_olat=True, decode_from=L0)
-    twin = DsaDecodeLayer(wl, keep_olat=True, decode_from=L0)
+    graph_layer = DsaDecodeLayer(wl, keep_olat=True, decode_from=L0, fuse_append=fused)
+    twin = DsaDecodeLayer(wl, keep_olat=True, decode_from=L0, fuse_append=not fused)
     for lay in (graph_layer, twin):
         lay.status.zero_()
         lay.compress()
@@ -245,3 +246,27 @@ def test_write_geom_and_compress_append_ranges():
             assert (got_k[~inside].view(torch.int16) == torch.tensor(7, dtype=torch.bfloat16,
                                                                       device="cuda").view(torch.int16)).all()
             assert (got_v[~inside] == 9).all()
+
+
+def test_decode_append_full_cache_matches_separate_calls():
+    """At the capacity the fused append flags the status, stores nothing, keeps the
+    length and writes it to row_ctx, as the three separate calls do."""
+    g = W.Geometry(index_kpool=4, index_heads=4, index_head_dim=128, index_topk=64, heads=2,
+                   hidden=64)
+    wl = W.make_workload("append-full", 8, g, [128, 100], max_seq_len=128)
+    out = []
+    for fused in (True, False):
+        lay = DsaDecodeLayer(wl, decode_from=[127, 97], fuse_append=fused)
+        lay.compress()
+        lay.stage(0)
+        lay.status.zero_()
+        for _ in range(3):  # sequence 0 fills at the first append
+            lay.append()
+        torch.cuda.synchronize()
+        out.append((lay.seq_lens.clone(), lay.row_ctx.clone(), int(lay.status.item()),
+                    lay.k_raw.clone(), lay.kpool.clone(), lay.pool_valid.clone(), lay.valid.clone()))
+    (a, b) = out
+    assert a[0].tolist() == [128, 100] and a[1].tolist() == [128, 100] and a[2] == 8
+    assert b[2] == a[2]
+    for x, y in zip(a[:2] + a[3:], b[:2] + b[3:]):
+        assert torch.equal(x, y)
