@@ -369,6 +369,90 @@ def dense_masked_attention(qlat_row, ckv_seq, mask, softmax_scale: float) -> np.
 
 
 # ---------------------------------------------------------------------------
+# FP8 latent cache (mod.rs, ``MASKED_ATTN_MAX_KEYS`` doc: the serve's decode
+# kernel is ``glm5next_dsa_mla_decode_fp8``). The pages name the kernel and
+# nothing of its format; the format below is this layer's stated choice:
+# OCP FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+# largest finite 448, no infinities) with one power-of-two scale per token and
+# 128-channel group.
+
+E4M3_MAX = 448.0
+FP8_GROUP = 128
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Round float64 values to the nearest E4M3 value, ties to even; magnitudes
+    above 448 saturate to 448 (no infinities in the format)."""
+    v = np.asarray(v, dtype=F64)
+    a = np.abs(v)
+    _, E2 = np.frexp(np.where(a > 0, a, 1.0))  # a = f * 2^E2, f in [0.5, 1)
+    # Spacing of E4M3 values at a's binade: 2^(e - 3) for normals (e >= -6),
+    # 2^-9 throughout the subnormal range.
+    e = np.maximum(E2 - 1, -6)
+    q = np.ldexp(1.0, e - 3)
+    r = np.round(a / q) * q  # numpy rounds halves to even; a / q is exact
+    r = np.minimum(r, E4M3_MAX)
+    return np.where(a > 0, np.copysign(r, v), v * 0.0)
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Byte codes of values that are already E4M3 values (``e4m3_round`` output)."""
+    v = np.asarray(v, dtype=F64)
+    a = np.abs(v)
+    sign = np.where(np.signbit(v), 0x80, 0)
+    _, E2 = np.frexp(np.where(a > 0, a, 1.0))
+    e = E2 - 1
+    normal = a >= 2.0 ** -6
+    exp_field = np.where(normal, e + 7, 0)
+    mant = np.where(normal, (a / np.ldexp(1.0, e) - 1.0) * 8, a / 2.0 ** -9)
+    code = (exp_field << 3) | np.rint(mant).astype(np.int64)
+    return (sign | np.where(a > 0, code, 0)).astype(np.uint8)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of E4M3 byte codes (0x7F and 0xFF, the NaNs, decode to NaN)."""
+    c = np.asarray(codes, dtype=np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    ef = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(ef == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.ldexp(1.0, ef - 7))
+    val = np.where((c & 0x7F) == 0x7F, np.nan, val)
+    return s * val
+
+
+def fp8_scale_exponent(amax) -> np.ndarray:
+    """k of a group's scale 2^k: the smallest integer with amax <= 448 * 2^k, not
+    below -126 (so 2^k and 2^-k are normal float32 numbers); 0 for an all-zero
+    group."""
+    a = np.asarray(amax, dtype=F64)
+    f, E2 = np.frexp(np.where(a > 0, a, 1.0))  # a = (2f) * 2^(E2-1), 2f in [1, 2)
+    # a <= 448 * 2^k  <=>  (2f) * 2^(E2-1-k) <= 1.75 * 2^8
+    k = np.where(2 * f <= 1.75, E2 - 1 - 8, E2 - 1 - 7)
+    k = np.maximum(k, -126)
+    return np.where(a > 0, k, 0).astype(np.int64)
+
+
+def quantize_latent_fp8(rows):
+    """Latent rows ``[T, kvl]`` -> ``(codes uint8 [T, kvl], scales float64
+    [T, kvl/128])``: per 128-channel group, scale ``2^k`` (``fp8_scale_exponent``
+    of the group's largest magnitude) and codes ``E4M3(x / 2^k)``."""
+    x = np.asarray(rows, dtype=F64)
+    T, kvl = x.shape
+    g = x.reshape(T, kvl // FP8_GROUP, FP8_GROUP)
+    k = fp8_scale_exponent(np.abs(g).max(axis=2))  # [T, G]
+    q = e4m3_round(np.ldexp(g, -k[:, :, None]))
+    return e4m3_encode(q).reshape(T, kvl), np.ldexp(1.0, k)
+
+
+def dequantize_latent_fp8(codes, scales) -> np.ndarray:
+    """``x[t, c] = E4M3(codes[t, c]) * scales[t, c // 128]`` (float64)."""
+    c = np.asarray(codes)
+    T, kvl = c.shape
+    v = e4m3_decode(c).reshape(T, kvl // FP8_GROUP, FP8_GROUP)
+    return (v * np.asarray(scales, dtype=F64)[:, :, None]).reshape(T, kvl)
+
+
+# ---------------------------------------------------------------------------
 # Decode-time append and the geometry derived from the live length (mod.rs,
 # ``Glm5NextDsaKernels`` fields ``indexer_store`` and ``write_geom``;
 # ``Glm5NextDsaConfig::max_context``)

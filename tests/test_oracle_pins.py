@@ -375,6 +375,67 @@ def test_dense_equivalence_with_tail():
 
 
 # ---------------------------------------------------------------------------
+# FP8 latent cache
+
+
+def test_e4m3_golden():
+    g = load_kv("fp8_e4m3.txt")
+    for v, c in g["code"]:
+        assert O.e4m3_round(v) == v
+        assert int(O.e4m3_encode(np.array([v]))[0]) == int(c), v
+        assert O.e4m3_decode(np.array([int(c)]))[0] == v
+    for v, r in g["round"]:
+        assert O.e4m3_round(v) == r, v
+    for a, k in g["scale"]:
+        assert int(O.fp8_scale_exponent(a)) == int(k), a
+    assert int(O.fp8_scale_exponent(2.0 ** -130)) == -126
+
+
+def test_e4m3_matches_library_codec():
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    if f8 is None:
+        pytest.skip("torch without float8_e4m3fn")
+    codes = np.arange(256)
+    lib = torch.from_numpy(codes.astype(np.uint8)).view(f8).float().numpy().astype(np.float64)
+    mine = O.e4m3_decode(codes)
+    np.testing.assert_array_equal(np.isnan(mine), np.isnan(lib))
+    fin = ~np.isnan(mine)
+    np.testing.assert_array_equal(mine[fin], lib[fin])
+    np.testing.assert_array_equal(O.e4m3_encode(mine[fin]), codes[fin].astype(np.uint8))
+    rng = np.random.default_rng(14)
+    x = np.concatenate([rng.uniform(-448, 448, 20000), rng.normal(0, 1e-2, 20000),
+                        rng.normal(0, 3e-3, 5000), mine[fin],
+                        (mine[fin][1:] + mine[fin][:-1]) / 2]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    want = torch.from_numpy(x).to(f8)
+    got = O.e4m3_encode(O.e4m3_round(x.astype(np.float64)))
+    np.testing.assert_array_equal(got, want.view(torch.uint8).numpy())
+
+
+def test_fp8_scale_and_quantize_properties():
+    rng = np.random.default_rng(15)
+    amax = np.abs(rng.normal(0, 1, 5000)) * np.exp2(rng.integers(-40, 40, 5000))
+    k = O.fp8_scale_exponent(amax)
+    assert (amax <= 448 * np.exp2(k.astype(np.float64))).all()
+    assert ((k == -126) | (amax > 448 * np.exp2(k - 1.0))).all()
+    x = O.bf16_round(rng.normal(0, 1, (40, 512)) * np.exp2(rng.integers(-6, 6, (40, 1))))
+    x[3, 128:256] = 0.0  # an all-zero group
+    codes, scales = O.quantize_latent_fp8(x)
+    assert codes.dtype == np.uint8 and scales.shape == (40, 4)
+    assert scales[3, 1] == 1.0 and (codes[3, 128:256] == 0).all()
+    deq = O.dequantize_latent_fp8(codes, scales)
+    # each element within half an E4M3 spacing (at its binade) of the input, times the scale
+    g = np.abs(x).reshape(40, 4, 128).max(axis=2)
+    assert (np.abs(deq.reshape(40, 4, 128)).max(axis=2) <= 448 * scales).all()
+    rel = np.abs(deq - x) / np.maximum(np.abs(x), 2.0 ** -6 * np.repeat(scales, 128, axis=1))
+    assert rel.max() <= 2.0 ** -4 + 1e-12
+    assert (g <= 448 * scales).all()
+    # E4M3 values times a power of two come back exactly
+    back_codes, back_scales = O.quantize_latent_fp8(deq)
+    np.testing.assert_array_equal(O.dequantize_latent_fp8(back_codes, back_scales), deq)
+
+
+# ---------------------------------------------------------------------------
 # decode-time append and geometry
 
 
