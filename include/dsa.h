@@ -94,7 +94,7 @@ const char* dsa_last_error(void);
 
 /* ABI version of this header (bumped on any signature change). */
 int dsa_abi_version(void);
-#define DSA_ABI_VERSION 3
+#define DSA_ABI_VERSION 4
 
 /*
  * Layer-geometry rules (mod.rs, Glm5NextDsaConfig::validate): index_kpool and
@@ -368,6 +368,44 @@ int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, int kv_lora
                           const dsa_bf16* o_absorb, int hidden, dsa_bf16* y, float* olat,
                           int32_t* status, void* workspace, size_t workspace_bytes,
                           void* stream);
+
+/*
+ * dsa_quantize_latent -- encoder of the FP8 latent cache. mod.rs names the serve's
+ * FP8 decode kernel (glm5next_dsa_mla_decode_fp8) and nothing of its format; the
+ * format here is this library's stated choice: OCP FP8 E4M3 codes (largest finite
+ * 448, nearest rounding with ties to even) and one power-of-two scale per token and
+ * 128-channel group,
+ *
+ *   k = the smallest integer with amax_g <= 448 * 2^k, not below -126 (0 if amax_g = 0)
+ *   scales[r, g] = 2^k,   codes[r, c] = E4M3(x[r, c] / 2^k)   for c in group g
+ *
+ * so decoding (code value times 2^k) is exact in bf16.
+ * x [rows, kv_lora_rank] bf16 (any token cache viewed as rows); codes [rows,
+ * kv_lora_rank] u8; scales [rows, kv_lora_rank / 128] f32.
+ * Limits: kv_lora_rank a positive multiple of 128; 16-byte aligned tensors.
+ */
+int dsa_quantize_latent(const dsa_bf16* x, long long rows, int kv_lora_rank, uint8_t* codes,
+                        float* scales, void* stream);
+
+/*
+ * dsa_sparse_mla_decode_fp8 -- dsa_sparse_mla_decode over an FP8 latent cache
+ * (mod.rs: the serve's decode kernel glm5next_dsa_mla_decode_fp8 reads the selected
+ * tokens through the block table). The latent row of token t is the decoded
+ * E4M3 code times its group's scale (dsa_quantize_latent); everything else, the
+ * equations included, is dsa_sparse_mla_decode's. Each gathered row is 528 bytes
+ * (512 codes + 4 scales) instead of 1,024.
+ *
+ * ckv_codes: token cache of width kv_lora_rank (u8); ckv_scales: token cache of
+ * width kv_lora_rank / 128 (f32), both laid out as pg says. The workspace size is
+ * dsa_sparse_mla_decode_workspace's. Limits as dsa_sparse_mla_decode.
+ */
+int dsa_sparse_mla_decode_fp8(const dsa_bf16* qlat, int rows, int heads, int kv_lora_rank,
+                              const int32_t* row_seq, const uint8_t* ckv_codes,
+                              const float* ckv_scales, const dsa_paging* pg,
+                              const int32_t* token_ids, int out_width, float softmax_scale,
+                              const dsa_bf16* o_absorb, int hidden, dsa_bf16* y, float* olat,
+                              int32_t* status, void* workspace, size_t workspace_bytes,
+                              void* stream);
 
 /*
  * dsa_latent_project -- the absorbed output projection on its own (build.rs,

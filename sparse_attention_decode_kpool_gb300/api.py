@@ -17,7 +17,7 @@ __all__ = ["paging", "dsa_compress", "dsa_compress_append", "dsa_indexer_store",
            "dsa_write_geom", "dsa_decode_append", "dsa_score", "dsa_score_prefill", "dsa_select", "dsa_expand",
            "dsa_select_expand", "dsa_expand_tail", "dsa_select_expand_tail",
            "dsa_sparse_mla_decode_workspace", "dsa_sparse_mla_decode",
-           "dsa_sparse_mla_decode_noalloc", "dsa_latent_project_workspace",
+           "dsa_sparse_mla_decode_noalloc", "dsa_sparse_mla_decode_fp8", "dsa_quantize_latent", "dsa_latent_project_workspace",
            "dsa_latent_project", "dsa_select_k",
            "dsa_validate_config", "DsaPaging"]
 
@@ -281,6 +281,44 @@ def dsa_sparse_mla_decode(qlat, row_seq, ckv, pg: DsaPaging, token_ids, softmax_
         _ptr(o_absorb, torch.bfloat16, "o_absorb"), hidden, _ptr(y, torch.bfloat16, "y"),
         _ptr(olat, torch.float32, "olat"), _ptr(status, torch.int32, "status"),
         _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)))
+
+
+def dsa_sparse_mla_decode_fp8(qlat, row_seq, ckv_codes, ckv_scales, pg: DsaPaging, token_ids,
+                              softmax_scale: float, o_absorb=None, y=None, olat=None,
+                              status=None, workspace=None, stream=None) -> None:
+    """dsa_sparse_mla_decode over an FP8 latent cache (E4M3 codes + per-128-channel
+    power-of-two scales, see dsa_quantize_latent)."""
+    rows, heads, kvl = (int(x) for x in qlat.shape)
+    ow = int(token_ids.shape[1])
+    hidden = int(o_absorb.shape[0]) if o_absorb is not None else 0
+    if o_absorb is not None and tuple(o_absorb.shape) != (hidden, heads * kvl):
+        raise ValueError(f"o_absorb must be [hidden, {heads * kvl}]")
+    if y is not None and tuple(y.shape) != (rows, hidden):
+        raise ValueError(f"y must be [{rows}, {hidden}]")
+    if olat is not None and tuple(olat.shape) != (rows, heads, kvl):
+        raise ValueError(f"olat must be [{rows}, {heads}, {kvl}]")
+    if ckv_codes.shape[-1] != kvl or ckv_scales.shape[-1] != kvl // 128:
+        raise ValueError("ckv_codes must be [..., kvl] and ckv_scales [..., kvl/128]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check(_lib.load().dsa_sparse_mla_decode_fp8(
+        _ptr(qlat, torch.bfloat16, "qlat"), rows, heads, kvl,
+        _ptr(row_seq, torch.int32, "row_seq"), _ptr(ckv_codes, torch.uint8, "ckv_codes"),
+        _ptr(ckv_scales, torch.float32, "ckv_scales"), ctypes.byref(pg),
+        _ptr(token_ids, torch.int32, "token_ids"), ow, float(softmax_scale),
+        _ptr(o_absorb, torch.bfloat16, "o_absorb"), hidden, _ptr(y, torch.bfloat16, "y"),
+        _ptr(olat, torch.float32, "olat"), _ptr(status, torch.int32, "status"),
+        _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)))
+
+
+def dsa_quantize_latent(x, codes, scales, stream=None) -> None:
+    """FP8 latent cache from bf16 rows: codes [..., kvl] u8, scales [..., kvl/128] f32."""
+    kvl = int(x.shape[-1])
+    rows = x.numel() // kvl
+    if codes.numel() != x.numel() or scales.numel() != rows * (kvl // 128):
+        raise ValueError("codes must match x and scales hold kvl/128 per row")
+    check(_lib.load().dsa_quantize_latent(
+        _ptr(x, torch.bfloat16, "x"), rows, kvl, _ptr(codes, torch.uint8, "codes"),
+        _ptr(scales, torch.float32, "scales"), _stream(stream)))
 
 
 def dsa_latent_project_workspace(rows: int, heads: int, hidden: int,

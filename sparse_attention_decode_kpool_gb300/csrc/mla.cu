@@ -31,12 +31,16 @@ constexpr int KVL = DSA_KV_LORA_RANK;  // 512
 constexpr int CH = 64;                 // tokens per gathered chunk
 constexpr int kMaxSplits = 64;         // token splits per row (make_plan's bound)
 constexpr int ROWB = KVL * 2;          // bytes per latent row
+constexpr int kF8Groups = KVL / 128;   // FP8 cache: one scale per 128 channels
+constexpr int ROW8 = KVL + kF8Groups * 4;  // FP8 cache: codes + scales of one token (528 B)
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct MlaArgs {
     const uint16_t* qlat;
     const int32_t* row_seq;
     const uint16_t* ckv;
+    const uint8_t* ckv8;     // FP8 cache: E4M3 codes [.., KVL]
+    const float* ckv_scale;  // FP8 cache: power-of-two scales [.., KVL / 128]
     const int32_t* token_ids;
     float* part_o;
     float* part_ml;
@@ -56,16 +60,30 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in
     return (uint32_t)(row * ROWB + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int MT>
-constexpr int split_smem_bytes() {
-    return MT * 16 * ROWB            // Q
-           + 2 * CH * ROWB           // latent rows, double buffered
-           + MT * 16 * CH * 2        // P (bf16)
-           + 4 * MT * 16 * 4         // cross-warp max/sum exchange
-           + 2 * CH;                 // token validity
+// Two E4M3 codes (low byte first) times a power-of-two scale, as packed bf16: the
+// E4M3 -> f16 conversion, the f16 -> f32 widening and the scaling are exact, and so
+// is the bf16 rounding (an E4M3 value times 2^k has a 4-bit significand).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float scale) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)(two & 0xffffu)));
+    float f0, f1;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f0) : "h"((unsigned short)(h2 & 0xffffu)));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f1) : "h"((unsigned short)(h2 >> 16)));
+    return pack_bf16x2(f0 * scale, f1 * scale);
 }
 
-template <int MT>
+template <int MT, bool F8>
+constexpr int split_smem_bytes() {
+    return MT * 16 * ROWB                 // Q
+           + (F8 ? 1 : 2) * CH * ROWB     // latent rows as bf16: double buffered, or one
+                                          // tile converted from the FP8 stage
+           + (F8 ? 2 * CH * ROW8 : 0)     // FP8 codes + scales, double buffered
+           + MT * 16 * CH * 2             // P (bf16)
+           + 4 * MT * 16 * 4              // cross-warp max/sum exchange
+           + 2 * CH;                      // token validity
+}
+
+template <int MT, bool F8>
 __global__ void __launch_bounds__(MT * 64, 1) mla_split_kernel(MlaArgs a) {
     pdl_wait();
     constexpr int NW = 2 * MT;
@@ -76,7 +94,8 @@ __global__ void __launch_bounds__(MT * 64, 1) mla_split_kernel(MlaArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* Qs = smem;
     uint8_t* KV = Qs + HP * ROWB;
-    uint8_t* Ps = KV + 2 * CH * ROWB;
+    uint8_t* stage = KV + (F8 ? 1 : 2) * CH * ROWB;  // FP8 only
+    uint8_t* Ps = stage + (F8 ? 2 * CH * ROW8 : 0);
     float* red = reinterpret_cast<float*>(Ps + HP * CH * 2);  // [max|sum][half][HP]
     uint8_t* vmask = reinterpret_cast<uint8_t*>(red + 4 * HP);
 
@@ -137,15 +156,33 @@ __global__ void __launch_bounds__(MT * 64, 1) mla_split_kernel(MlaArgs a) {
             }
             vmask[buf * CH + j] = prow >= 0 ? 1 : 0;
         }
-        uint8_t* dst = KV + buf * CH * ROWB;
+        if constexpr (F8) {
+            // codes (32 lanes x 16 B) and the row's scales (16 B) into the stage
+            uint8_t* dst = stage + buf * CH * ROW8;
 #pragma unroll 4
-        for (int jj = 0; jj < RPW; ++jj) {
-            const long long pr = __shfl_sync(0xffffffffu, prow, jj);
-            const int row = warp * RPW + jj;
-            const uint16_t* src = pr >= 0 ? a.ckv + pr * KVL : a.ckv;
-            const int nb = pr >= 0 ? 16 : 0;
-            cp_async16(smem_u32(dst + swz(row, lane)), src + lane * 8, nb);
-            cp_async16(smem_u32(dst + swz(row, lane + 32)), src + (lane + 32) * 8, nb);
+            for (int jj = 0; jj < RPW; ++jj) {
+                const long long pr = __shfl_sync(0xffffffffu, prow, jj);
+                const int row = warp * RPW + jj;
+                const int nb = pr >= 0 ? 16 : 0;
+                const uint8_t* src = pr >= 0 ? a.ckv8 + pr * KVL : a.ckv8;
+                cp_async16(smem_u32(dst + row * ROW8 + lane * 16), src + lane * 16, nb);
+                if (lane == 0)
+                    cp_async16(smem_u32(dst + row * ROW8 + KVL),
+                               pr >= 0 ? (const void*)(a.ckv_scale + pr * kF8Groups)
+                                       : (const void*)a.ckv_scale,
+                               nb);
+            }
+        } else {
+            uint8_t* dst = KV + buf * CH * ROWB;
+#pragma unroll 4
+            for (int jj = 0; jj < RPW; ++jj) {
+                const long long pr = __shfl_sync(0xffffffffu, prow, jj);
+                const int row = warp * RPW + jj;
+                const uint16_t* src = pr >= 0 ? a.ckv + pr * KVL : a.ckv;
+                const int nb = pr >= 0 ? 16 : 0;
+                cp_async16(smem_u32(dst + swz(row, lane)), src + lane * 8, nb);
+                cp_async16(smem_u32(dst + swz(row, lane + 32)), src + (lane + 32) * 8, nb);
+            }
         }
     };
 
@@ -171,7 +208,24 @@ __global__ void __launch_bounds__(MT * 64, 1) mla_split_kernel(MlaArgs a) {
             cp_async_wait<0>();
         }
         __syncthreads();
-        const uint8_t* Kb = KV + buf * CH * ROWB;
+        if constexpr (F8) {
+            // Stage -> bf16 tile: each thread converts 8 codes into one 16-byte chunk
+            // (a quarter warp covers 8 consecutive chunks of a row: no bank conflicts).
+            const uint8_t* sb = stage + buf * CH * ROW8;
+            for (int u = tid; u < CH * 64; u += NTH) {
+                const int row = u >> 6, j = u & 63;
+                const uint2 cw = *reinterpret_cast<const uint2*>(sb + row * ROW8 + j * 8);
+                const float sc = *reinterpret_cast<const float*>(sb + row * ROW8 + KVL + (j >> 4) * 4);
+                uint4 o;
+                o.x = e4m3x2_to_bf16x2(cw.x, sc);
+                o.y = e4m3x2_to_bf16x2(cw.x >> 16, sc);
+                o.z = e4m3x2_to_bf16x2(cw.y, sc);
+                o.w = e4m3x2_to_bf16x2(cw.y >> 16, sc);
+                *reinterpret_cast<uint4*>(KV + swz(row, j)) = o;
+            }
+            __syncthreads();
+        }
+        const uint8_t* Kb = KV + (F8 ? 0 : buf) * CH * ROWB;
 
         // ---- S = Q K^T for 16 heads x 32 tokens
         float sacc[4][4];
@@ -540,9 +594,10 @@ struct Plan {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms) {
+Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms,
+               bool fp8 = false) {
     Plan p;
-    p.tc = mla_tc_supported(heads, KVL);
+    p.tc = !fp8 && mla_tc_supported(heads, KVL);
     p.mt = heads <= 16 ? 1 : heads <= 32 ? 2 : 4;
     p.hgroups = p.tc ? 1 : (heads + 16 * p.mt - 1) / (16 * p.mt);
     const int chunk = p.tc ? mla_tc_chunk() : CH;
@@ -599,13 +654,14 @@ int check_common(int rows, int heads, int kv_lora_rank, int out_width, int hidde
     return DSA_OK;
 }
 
-template <int MT>
+template <int MT, bool F8>
 int launch_split(const MlaArgs& a, const Plan& p, cudaStream_t st) {
-    constexpr int smem = split_smem_bytes<MT>();
-    int rc = set_max_smem((const void*)mla_split_kernel<MT>, smem);
+    constexpr int smem = split_smem_bytes<MT, F8>();
+    static_assert(smem <= 227 * 1024, "split kernel shared memory");
+    int rc = set_max_smem((const void*)mla_split_kernel<MT, F8>, smem);
     if (rc) return rc;
     dim3 grid(p.ns, a.rows, p.hgroups);
-    cudaError_t e = launch_pdl(mla_split_kernel<MT>, grid, dim3(MT * 64), smem, st, a);
+    cudaError_t e = launch_pdl(mla_split_kernel<MT, F8>, grid, dim3(MT * 64), smem, st, a);
     if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_mla_decode split launch");
     return DSA_OK;
 }
@@ -630,18 +686,23 @@ extern "C" int dsa_sparse_mla_decode_workspace(int rows, int heads, int kv_lora_
     if (rc) return rc;
     const int sms = sm_count();
     if (sms <= 0) return fail(DSA_ERR_CUDA, "dsa_sparse_mla_decode_workspace: no CUDA device");
-    *bytes = make_plan(rows, heads, out_width, hidden, with_o_absorb != 0, sms).bytes;
+    // Enough for either cache format (the FP8 path never takes the tensor-core plan).
+    const size_t b16 = make_plan(rows, heads, out_width, hidden, with_o_absorb != 0, sms).bytes;
+    const size_t b8 = make_plan(rows, heads, out_width, hidden, with_o_absorb != 0, sms, true).bytes;
+    *bytes = b16 > b8 ? b16 : b8;
     return DSA_OK;
 }
 
-extern "C" int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, int kv_lora_rank,
-                                     const int32_t* row_seq, const dsa_bf16* ckv,
-                                     const dsa_paging* pg, const int32_t* token_ids,
-                                     int out_width, float softmax_scale,
-                                     const dsa_bf16* o_absorb, int hidden, dsa_bf16* y,
-                                     float* olat, int32_t* status, void* workspace,
-                                     size_t workspace_bytes, void* stream) {
+namespace {
+// dsa_sparse_mla_decode (ckv) and dsa_sparse_mla_decode_fp8 (ckv8 + ckv_scale).
+int mla_decode_impl(const dsa_bf16* qlat, int rows, int heads, int kv_lora_rank,
+                    const int32_t* row_seq, const dsa_bf16* ckv, const uint8_t* ckv8,
+                    const float* ckv_scale, const dsa_paging* pg, const int32_t* token_ids,
+                    int out_width, float softmax_scale, const dsa_bf16* o_absorb, int hidden,
+                    dsa_bf16* y, float* olat, int32_t* status, void* workspace,
+                    size_t workspace_bytes, void* stream) {
     const bool with_oabs = o_absorb != nullptr;
+    const bool fp8 = ckv8 != nullptr;
     int rc = check_common(rows, heads, kv_lora_rank, out_width, hidden, with_oabs);
     if (rc) return rc;
     if (with_oabs != (y != nullptr))
@@ -651,14 +712,14 @@ extern "C" int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, 
     rc = check_paging(pg, 0, &P);
     if (rc) return rc;
     if (rows == 0) return DSA_OK;
-    if (!qlat || !ckv || (out_width > 0 && !token_ids))
+    if (!qlat || (fp8 ? !ckv_scale : !ckv) || (out_width > 0 && !token_ids))
         return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_mla_decode: NULL tensor");
-    if ((((uintptr_t)qlat) | ((uintptr_t)ckv) | ((uintptr_t)o_absorb) | ((uintptr_t)olat) |
-         ((uintptr_t)y) | ((uintptr_t)workspace)) & 15)
+    if ((((uintptr_t)qlat) | ((uintptr_t)ckv) | ((uintptr_t)ckv8) | ((uintptr_t)ckv_scale) |
+         ((uintptr_t)o_absorb) | ((uintptr_t)olat) | ((uintptr_t)y) | ((uintptr_t)workspace)) & 15)
         return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_mla_decode: tensors must be 16-byte aligned");
     const int sms = sm_count();
     if (sms <= 0) return fail(DSA_ERR_CUDA, "dsa_sparse_mla_decode: no CUDA device");
-    const Plan p = make_plan(rows, heads, out_width, hidden, with_oabs, sms);
+    const Plan p = make_plan(rows, heads, out_width, hidden, with_oabs, sms, fp8);
     if (p.bytes > 0 && (!workspace || workspace_bytes < p.bytes))
         return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_mla_decode: workspace %zu B < %zu B needed",
                     workspace_bytes, p.bytes);
@@ -669,6 +730,8 @@ extern "C" int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, 
     a.qlat = qlat;
     a.row_seq = row_seq;
     a.ckv = ckv;
+    a.ckv8 = ckv8;
+    a.ckv_scale = ckv_scale;
     a.token_ids = token_ids;
     a.part_o = p.ns > 1 ? reinterpret_cast<float*>(ws + p.off_part_o) : nullptr;
     a.part_ml = p.ns > 1 ? reinterpret_cast<float*>(ws + p.off_part_ml) : nullptr;
@@ -705,10 +768,13 @@ extern "C" int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, 
                                                  : (long long)P.batch * P.max_seq_len;
         rc = mla_tc_launch(t, ckv_rows, st);
     } else {
-        switch (p.mt) {
-            case 1: rc = launch_split<1>(a, p, st); break;
-            case 2: rc = launch_split<2>(a, p, st); break;
-            default: rc = launch_split<4>(a, p, st); break;
+        switch (p.mt * 2 + (fp8 ? 1 : 0)) {
+            case 2: rc = launch_split<1, false>(a, p, st); break;
+            case 3: rc = launch_split<1, true>(a, p, st); break;
+            case 4: rc = launch_split<2, false>(a, p, st); break;
+            case 5: rc = launch_split<2, true>(a, p, st); break;
+            case 9: rc = launch_split<4, true>(a, p, st); break;
+            default: rc = launch_split<4, false>(a, p, st); break;
         }
     }
     if (rc) return rc;
@@ -755,4 +821,31 @@ extern "C" int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, 
         if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_mla_decode ysum launch");
     }
     return DSA_OK;
+}
+}  // namespace
+
+extern "C" int dsa_sparse_mla_decode(const dsa_bf16* qlat, int rows, int heads, int kv_lora_rank,
+                                     const int32_t* row_seq, const dsa_bf16* ckv,
+                                     const dsa_paging* pg, const int32_t* token_ids,
+                                     int out_width, float softmax_scale,
+                                     const dsa_bf16* o_absorb, int hidden, dsa_bf16* y,
+                                     float* olat, int32_t* status, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+    return mla_decode_impl(qlat, rows, heads, kv_lora_rank, row_seq, ckv, nullptr, nullptr, pg,
+                           token_ids, out_width, softmax_scale, o_absorb, hidden, y, olat, status,
+                           workspace, workspace_bytes, stream);
+}
+
+extern "C" int dsa_sparse_mla_decode_fp8(const dsa_bf16* qlat, int rows, int heads,
+                                         int kv_lora_rank, const int32_t* row_seq,
+                                         const uint8_t* ckv_codes, const float* ckv_scales,
+                                         const dsa_paging* pg, const int32_t* token_ids,
+                                         int out_width, float softmax_scale,
+                                         const dsa_bf16* o_absorb, int hidden, dsa_bf16* y,
+                                         float* olat, int32_t* status, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+    if (!ckv_codes) return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_mla_decode_fp8: NULL codes");
+    return mla_decode_impl(qlat, rows, heads, kv_lora_rank, row_seq, nullptr, ckv_codes,
+                           ckv_scales, pg, token_ids, out_width, softmax_scale, o_absorb, hidden,
+                           y, olat, status, workspace, workspace_bytes, stream);
 }

@@ -21,7 +21,7 @@ class DsaDecodeLayer:
     def __init__(self, wl: Workload, device: str = "cuda", keep_olat: bool = False,
                  with_o_absorb: bool = True, use_drawn_kpool: bool = False,
                  score_path: str = "auto", fuse_expand: bool = True, decode_from=None,
-                 fuse_append: bool = True):
+                 fuse_append: bool = True, latent_fp8: bool = False):
         g = wl.geom
         self.wl = wl
         self.geom = g
@@ -38,6 +38,19 @@ class DsaDecodeLayer:
 
         # Resident state.
         self.ckv = up(wl.ckv)
+        # FP8 latent cache (E4M3 codes + power-of-two scales per 128 channels), encoded
+        # once from the bf16 cache; attention then gathers 528 instead of 1,024 bytes
+        # per token.
+        self.latent_fp8 = bool(latent_fp8)
+        self.ckv_codes = self.ckv_scales = None
+        if self.latent_fp8:
+            if decode_from is not None:
+                raise ValueError("decode-time append writes the bf16 latent cache only")
+            kvl = g.kv_lora_rank
+            self.ckv_codes = torch.empty(self.ckv.shape, dtype=torch.uint8, device=dev)
+            self.ckv_scales = torch.empty(self.ckv.shape[:-1] + (kvl // 128,),
+                                          dtype=torch.float32, device=dev)
+            api.dsa_quantize_latent(self.ckv, self.ckv_codes, self.ckv_scales)
         self.o_absorb = up(wl.o_absorb) if with_o_absorb else None
         KP, ihd = g.index_kpool, g.index_head_dim
         if wl.paged:
@@ -255,17 +268,24 @@ class DsaDecodeLayer:
             return
         api.dsa_expand(self.pool_ids, g.first_key, g.index_kpool, self.token_ids, stream=stream)
 
+    def _mla(self, o_absorb, y, workspace, stream) -> None:
+        if self.latent_fp8:
+            api.dsa_sparse_mla_decode_fp8(self.qlat, self.row_seq, self.ckv_codes, self.ckv_scales,
+                                          self.pg, self.token_ids, self.geom.softmax_scale,
+                                          o_absorb, y, self.olat, self.status, workspace,
+                                          stream=stream)
+        else:
+            api.dsa_sparse_mla_decode(self.qlat, self.row_seq, self.ckv, self.pg, self.token_ids,
+                                      self.geom.softmax_scale, o_absorb, y, self.olat,
+                                      self.status, workspace, stream=stream)
+
     def attend(self, stream=None) -> None:
         """Sparse latent attention over the selected tokens -> olat (f32); in the
         one-call form also y."""
         if self.o_absorb is not None and not self.two_call:
-            api.dsa_sparse_mla_decode(self.qlat, self.row_seq, self.ckv, self.pg, self.token_ids,
-                                      self.geom.softmax_scale, self.o_absorb, self.y, self.olat,
-                                      self.status, self.fused_workspace(), stream=stream)
+            self._mla(self.o_absorb, self.y, self.fused_workspace(), stream)
             return
-        api.dsa_sparse_mla_decode(self.qlat, self.row_seq, self.ckv, self.pg, self.token_ids,
-                                  self.geom.softmax_scale, None, None, self.olat, self.status,
-                                  self.workspace, stream=stream)
+        self._mla(None, None, self.workspace, stream)
 
     def project(self, stream=None) -> None:
         """y = o_absorb . olat (the absorbed output projection)."""
