@@ -421,6 +421,9 @@ int dsa_sparse_mla_decode_fp8(const dsa_bf16* qlat, int rows, int heads, int kv_
  * o_absorb [hidden, heads*kv_lora_rank] bf16; y [rows, hidden] bf16; status as
  * above (DSA_STATUS_TIMEOUT only). Limits: kv_lora_rank == 512; hidden % 64 == 0;
  * olat, o_absorb, y and workspace 16-byte aligned (DSA_ERR_INVALID_ARG otherwise).
+ * Ordering: the kernel may start reading o_absorb (weights) before the kernel just
+ * before it on the stream has finished (programmatic dependent launch), so that
+ * kernel must not write o_absorb; olat is read only after it has finished.
  */
 int dsa_latent_project_workspace(int rows, int heads, int kv_lora_rank, int hidden,
                                  size_t* bytes);

@@ -168,6 +168,11 @@ __device__ __forceinline__ void cp_async_wait() {
 // Blocks until the grids this one depends on have completed and their memory is
 // visible (returns at once when launched without the attribute).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Lets the next kernel on the stream (a programmatic dependent) start its blocks now;
+// it still waits in pdl_wait() until this grid has completed.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
 
 // ---- mbarrier + bulk async copy (TMA engine, non-tensor form) ----------------
 

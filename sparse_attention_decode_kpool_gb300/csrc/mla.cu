@@ -383,6 +383,9 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
                                                           const float* __restrict__ part_ml,
                                                           int heads, int ns, float* olat,
                                                           uint16_t* xbf) {
+    // The projection that follows streams weights it can fetch before olat exists:
+    // let its blocks start now (they wait for this grid before reading olat).
+    pdl_trigger();
     pdl_wait();
     __shared__ float wsh[kMaxSplits];
     __shared__ float lsum;

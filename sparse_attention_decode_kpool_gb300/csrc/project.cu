@@ -77,7 +77,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NT))
     const long long G = gridDim.x;
     const long long u0 = unit_begin(blockIdx.x, a.U, G);
     const long long u1 = unit_begin(blockIdx.x + 1, a.U, G);
-    pdl_wait();
 
     if (tid == 0) {
         for (int s = 0; s < C::S; ++s) {
@@ -88,6 +87,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NT))
     }
     if ((smem_u32(smem) & 127u) != 0u) {  // tensor copies need an aligned destination
         if (tid == 0) flag_status(a.status, DSA_STATUS_TIMEOUT);
+        pdl_wait();
         return;
     }
     __syncthreads();
@@ -97,8 +97,27 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NT))
         const uint32_t bytes = (uint32_t)C::STAGE;  // full boxes (zero fill counts too)
         long long i = 0;
         bool ok = true;
+        // o_absorb is not written by the kernels before this one: the first ring's
+        // worth of its boxes is requested before waiting for them, so it streams in
+        // while the preceding kernel finishes; the X (olat) boxes follow the wait.
+        const long long pre = (u1 - u0) < C::S ? (u1 - u0) : C::S;
         if (lane == 0) {
-            for (long long u = u0; u < u1; ++u, ++i) {
+            for (long long j = 0; j < pre; ++j) {
+                const long long u = u0 + j;
+                mbar_arrive_expect_tx(&full[j], bytes);
+                tma_load_2d(smem_u32(smem + j * C::STAGE), &tmA, (int)(u % a.KB) * KT,
+                            (int)(u / a.KB) * MROWS, &full[j]);
+            }
+        }
+        pdl_wait();
+        if (lane == 0) {
+            for (long long j = 0; j < pre; ++j) {
+                const long long u = u0 + j;
+                tma_load_2d(smem_u32(smem + j * C::STAGE) + C::A_BYTES, &tmX, (int)(u % a.KB) * KT,
+                            a.n0, &full[j]);
+            }
+            i = pre;
+            for (long long u = u0 + pre; u < u1; ++u, ++i) {
                 const int s = (int)(i % C::S);
                 const uint32_t ph = (uint32_t)((i / C::S) & 1);
                 if (!mbar_wait(&empty[s], ph ^ 1u)) {
@@ -124,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NT))
     }
 
     // ---------------- consumer warps: rows 16*warp .. +15 of the 64-row tile
+    pdl_wait();
     const int g = lane >> 2, q = lane & 3;
     const int rA = 16 * warp + g;
     float acc[NT][4];
