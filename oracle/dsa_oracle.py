@@ -524,6 +524,41 @@ def write_geom(seq_lens, row_seq=None) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# Projection front-end: the layer's inputs from the hidden state (build.rs, the
+# tensor table of ``DsaTpPlan::new`` and ``build_dsa_weights``). The pages give the
+# weights and their shapes; the order of the computation is the plain reading of
+# those shapes: q_a_proj, q_a_layernorm, then q_absorb (-> qlat) and indexer.wq_b
+# (-> qidx) on the normalised q_lora; kv_a_proj_with_mqa and kv_a_layernorm (-> the
+# token's latent row); indexer.wk (-> raw indexer key), the compress gate (-> gate
+# logits) and weights_proj (already scaled by index_heads^-0.5 at load, -> w) on
+# the hidden state. The two a-norms carry a weight and no bias (the pages single out
+# k_norm as the one norm with a bias): RMSNorm.
+
+
+def rms_norm(x, gamma, eps: float) -> np.ndarray:
+    """``x / sqrt(mean(x^2) + eps) * gamma`` over the last axis (float64)."""
+    x = np.asarray(x, dtype=F64)
+    ms = (x * x).mean(axis=-1, keepdims=True)
+    return x / np.sqrt(ms + F64(eps)) * np.asarray(gamma, dtype=F64)
+
+
+def frontend_row(x_row, q_a_proj, q_a_norm, kv_a_proj, kv_a_norm, wk, compress_gate,
+                 weights_proj, q_absorb, wq_b, eps: float, heads: int, index_heads: int) -> dict:
+    """One decode row's front-end. Storage points (bf16 unless noted): q_lora (the
+    normalised q_a), qlat ``[heads, kvl]``, qidx ``[index_heads, ihd]``, the latent
+    row ``ckv``, ``k_raw``, ``gate``; ``w`` stays float (f32 on the device)."""
+    x = np.asarray(x_row, dtype=F64)
+    mm = lambda W, v: np.asarray(W, dtype=F64) @ v
+    q_lora = bf16_round(rms_norm(mm(q_a_proj, x), q_a_norm, eps))
+    ckv = bf16_round(rms_norm(mm(kv_a_proj, x), kv_a_norm, eps))
+    qlat = bf16_round(mm(q_absorb, q_lora))
+    qidx = bf16_round(mm(wq_b, q_lora))
+    return dict(q_lora=q_lora, ckv=ckv, qlat=qlat.reshape(heads, -1),
+                qidx=qidx.reshape(index_heads, -1), k_raw=bf16_round(mm(wk, x)),
+                gate=bf16_round(mm(compress_gate, x)), w=mm(weights_proj, x))
+
+
+# ---------------------------------------------------------------------------
 # Cache addressing (the oracle's own, independent of the kernels')
 
 

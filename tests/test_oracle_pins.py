@@ -375,6 +375,52 @@ def test_dense_equivalence_with_tail():
 
 
 # ---------------------------------------------------------------------------
+# projection front-end
+
+
+def test_rms_norm_golden_and_closed_forms():
+    g = load_kv("rms_norm.txt")
+    x, gamma = g["x"][0], g["gamma"][0]
+    np.testing.assert_allclose(O.rms_norm(x, gamma, 0.0), g["eps0"][0], rtol=1e-15)
+    np.testing.assert_allclose(O.rms_norm(x, gamma, 0.5), g["eps05"][0], rtol=1e-15)
+    rng = np.random.default_rng(16)
+    v = rng.normal(size=(5, 33))
+    gm = rng.normal(size=33)
+    # constant row -> sign * gamma; positive scale invariance; unit mean square
+    np.testing.assert_allclose(O.rms_norm(np.full(33, -2.5), gm, 0.0), -gm, rtol=1e-14)
+    np.testing.assert_allclose(O.rms_norm(7.0 * v, gm, 0.0), O.rms_norm(v, gm, 0.0), rtol=1e-13)
+    np.testing.assert_allclose((O.rms_norm(v, np.ones(33), 0.0) ** 2).mean(axis=1), 1.0,
+                               rtol=1e-13)
+
+
+def test_frontend_row_on_basis_vectors():
+    # With x a scaled basis vector every projection picks one weight column, and with
+    # q_absorb and wq_b the identity qlat and qidx are q_lora itself: each output is
+    # fixed without retyping the composition.
+    rng = np.random.default_rng(17)
+    hidden, ql, kvl, ihd, Hi, H = 64, 96, 32, 16, 6, 3
+    W = lambda n, k: rng.normal(size=(n, k))
+    q_a, kv_a, wk, gate, wp = W(ql, hidden), W(kvl, hidden), W(ihd, hidden), W(ihd, hidden), W(Hi, hidden)
+    gq, gkv = rng.normal(size=ql), rng.normal(size=kvl)
+    eye = np.eye(ql)
+    for j, sc in ((5, 1.5), (63, -0.25)):
+        x = np.zeros(hidden)
+        x[j] = sc
+        out = O.frontend_row(x, q_a, gq, kv_a, gkv, wk, gate, wp, eye, eye, 1e-6, H, Hi)
+        np.testing.assert_array_equal(out["w"], sc * wp[:, j])
+        np.testing.assert_array_equal(out["k_raw"], O.bf16_round(sc * wk[:, j]))
+        np.testing.assert_array_equal(out["gate"], O.bf16_round(sc * gate[:, j]))
+        np.testing.assert_array_equal(out["ckv"], O.bf16_round(O.rms_norm(sc * kv_a[:, j], gkv, 1e-6)))
+        ql_ref = O.bf16_round(O.rms_norm(sc * q_a[:, j], gq, 1e-6))
+        np.testing.assert_array_equal(out["q_lora"], ql_ref)
+        np.testing.assert_array_equal(out["qlat"], ql_ref.reshape(H, kvl))
+        np.testing.assert_array_equal(out["qidx"], ql_ref.reshape(Hi, ihd))
+    # the norms are not interchangeable, and q uses q_lora, not x (distinct widths)
+    out = O.frontend_row(x, q_a, gq, kv_a, gkv, wk, gate, wp, eye, eye, 1e-6, H, Hi)
+    assert out["q_lora"].shape == (ql,) and out["ckv"].shape == (kvl,)
+
+
+# ---------------------------------------------------------------------------
 # FP8 latent cache
 
 
