@@ -21,7 +21,7 @@ DSA_STATUS_BAD_TOKEN = 1
 DSA_STATUS_BAD_BLOCK = 2
 DSA_STATUS_TIMEOUT = 4
 DSA_STATUS_CACHE_FULL = 8
-DSA_ABI_VERSION = 4
+DSA_ABI_VERSION = 5
 
 
 class DsaPaging(ctypes.Structure):
@@ -69,6 +69,9 @@ SIGNATURES = {
     "dsa_quantize_latent": (_I, [_P, ctypes.c_longlong, _I, _P, _P, _P]),
     "dsa_sparse_mla_decode_fp8": (_I, [_P, _I, _I, _I, _P, _P, _P, _PG, _P, _I, _F, _P, _I, _P,
                                        _P, _P, _P, _SZ, _P]),
+    "dsa_frontend_workspace": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
+    "dsa_frontend": (_I, [_P, _I, _I, _P, _I, _I, _I, _I, _I, _P, _P, _F, _P, _I, _P, _P, _P, _P,
+                          _P, _P, _P, _P, _P, _SZ, _P]),
     "dsa_latent_project_workspace": (_I, [_I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "dsa_latent_project": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P, _SZ, _P]),
     "dsa_sparse_mla_decode_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _PG, _P, _I, _F, _P, _I, _P,

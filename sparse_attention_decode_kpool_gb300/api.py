@@ -17,7 +17,8 @@ __all__ = ["paging", "dsa_compress", "dsa_compress_append", "dsa_indexer_store",
            "dsa_write_geom", "dsa_decode_append", "dsa_score", "dsa_score_prefill", "dsa_select", "dsa_expand",
            "dsa_select_expand", "dsa_expand_tail", "dsa_select_expand_tail",
            "dsa_sparse_mla_decode_workspace", "dsa_sparse_mla_decode",
-           "dsa_sparse_mla_decode_noalloc", "dsa_sparse_mla_decode_fp8", "dsa_quantize_latent", "dsa_latent_project_workspace",
+           "dsa_sparse_mla_decode_noalloc", "dsa_sparse_mla_decode_fp8", "dsa_quantize_latent",
+           "dsa_frontend_workspace", "dsa_frontend", "dsa_latent_project_workspace",
            "dsa_latent_project", "dsa_select_k",
            "dsa_validate_config", "DsaPaging"]
 
@@ -319,6 +320,40 @@ def dsa_quantize_latent(x, codes, scales, stream=None) -> None:
     check(_lib.load().dsa_quantize_latent(
         _ptr(x, torch.bfloat16, "x"), rows, kvl, _ptr(codes, torch.uint8, "codes"),
         _ptr(scales, torch.float32, "scales"), _stream(stream)))
+
+
+def dsa_frontend_workspace(rows: int, hidden: int, n_x: int, q_lora_rank: int, kv_lora_rank: int,
+                           ihd: int, index_heads: int, heads: int) -> int:
+    n = ctypes.c_size_t(0)
+    check(_lib.load().dsa_frontend_workspace(int(rows), int(hidden), int(n_x), int(q_lora_rank),
+                                             int(kv_lora_rank), int(ihd), int(index_heads),
+                                             int(heads), ctypes.byref(n)))
+    return int(n.value)
+
+
+def dsa_frontend(x, w_x, q_a_norm, kv_a_norm, eps: float, q_absorb, wq_b, qlat, qidx, w, k_new,
+                 gate_new, ckv_new, status=None, workspace=None, stream=None) -> None:
+    """The step's inputs from the hidden state (see dsa_frontend in include/dsa.h)."""
+    rows, hidden = (int(v) for v in x.shape)
+    n_x = int(w_x.shape[0])
+    ql, kvl = int(q_a_norm.numel()), int(kv_a_norm.numel())
+    _, heads, kvl2 = (int(v) for v in qlat.shape)
+    _, hi, ihd = (int(v) for v in qidx.shape)
+    if kvl2 != kvl or tuple(w_x.shape) != (n_x, hidden):
+        raise ValueError("qlat's width must be kv_lora_rank and w_x [n_x, hidden]")
+    if tuple(q_absorb.shape) != (heads * kvl, ql) or tuple(wq_b.shape) != (hi * ihd, ql):
+        raise ValueError("q_absorb must be [heads*kvl, q_lora] and wq_b [index_heads*ihd, q_lora]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check(_lib.load().dsa_frontend(
+        _ptr(x, torch.bfloat16, "x"), rows, hidden, _ptr(w_x, torch.bfloat16, "w_x"), n_x, ql, kvl,
+        ihd, hi, _ptr(q_a_norm, torch.bfloat16, "q_a_norm"),
+        _ptr(kv_a_norm, torch.bfloat16, "kv_a_norm"), float(eps),
+        _ptr(q_absorb, torch.bfloat16, "q_absorb"), heads, _ptr(wq_b, torch.bfloat16, "wq_b"),
+        _ptr(qlat, torch.bfloat16, "qlat"), _ptr(qidx, torch.bfloat16, "qidx"),
+        _ptr(w, torch.float32, "w"), _ptr(k_new, torch.bfloat16, "k_new"),
+        _ptr(gate_new, torch.bfloat16, "gate_new"), _ptr(ckv_new, torch.bfloat16, "ckv_new"),
+        _ptr(status, torch.int32, "status"), _ptr(workspace, None, "workspace"), ws_bytes,
+        _stream(stream)))
 
 
 def dsa_latent_project_workspace(rows: int, heads: int, hidden: int,

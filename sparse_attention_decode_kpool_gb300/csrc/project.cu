@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NT))
 // the CTAs in ascending order. One thread per 4 columns; the contributing CTAs are
 // read four at a time so their loads overlap.
 __global__ void project_reduce_kernel(const float* __restrict__ ypart, long long U, int KB, int G,
-                                      int J, int R, int hidden, uint16_t* __restrict__ y) {
+                                      int J, int R, int hidden, uint16_t* __restrict__ y,
+                                      float* __restrict__ yf) {
     pdl_wait();
     const long long n4 = (long long)R * hidden / 4;
     for (long long i4 = blockIdx.x * (long long)blockDim.x + threadIdx.x; i4 < n4;
@@ -263,10 +264,14 @@ __global__ void project_reduce_kernel(const float* __restrict__ ypart, long long
             }
             if (c + 4 >= G || unit_begin(c + 4, U, G) >= hi) break;
         }
-        uint2 o;
-        o.x = pack_bf16x2(s.x, s.y);
-        o.y = pack_bf16x2(s.z, s.w);
-        *reinterpret_cast<uint2*>(y + i) = o;
+        if (yf) {
+            *reinterpret_cast<float4*>(yf + i) = s;
+        } else {
+            uint2 o;
+            o.x = pack_bf16x2(s.x, s.y);
+            o.y = pack_bf16x2(s.z, s.w);
+            *reinterpret_cast<uint2*>(y + i) = o;
+        }
     }
 }
 
@@ -277,7 +282,7 @@ __global__ void project_reduce_kernel(const float* __restrict__ ypart, long long
 // order with all its loads issued together (eight at a time).
 __global__ void __launch_bounds__(128) project_reduce_rows_kernel(
     const float* __restrict__ ypart, long long U, int KB, int G, int J, int R, int hidden,
-    uint16_t* __restrict__ y) {
+    uint16_t* __restrict__ y, float* __restrict__ yf) {
     pdl_wait();
     __shared__ long long soff[32];
     __shared__ int scount;
@@ -321,10 +326,15 @@ __global__ void __launch_bounds__(128) project_reduce_rows_kernel(
             }
         }
     }
+    const long long oi = (long long)r * hidden + mb * MROWS + 4 * c4;
+    if (yf) {
+        *reinterpret_cast<float4*>(yf + oi) = acc;
+        return;
+    }
     uint2 out;
     out.x = pack_bf16x2(acc.x, acc.y);
     out.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(y + (long long)r * hidden + mb * MROWS + 4 * c4) = out;
+    *reinterpret_cast<uint2*>(y + oi) = out;
 }
 
 struct ProjPlan {
@@ -385,7 +395,8 @@ size_t project_workspace_bytes(int rows, int K, int hidden, int sms) {
 }
 
 int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A, int hidden,
-                   uint16_t* y, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st) {
+                   uint16_t* y, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st,
+                   float* yf) {
     const int sms = sm_count();
     if (sms <= 0) return fail(DSA_ERR_CUDA, "projection: no CUDA device");
     const ProjPlan p = plan_for(rows, K, hidden, sms);
@@ -423,13 +434,13 @@ int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A
         const long long nmb = hidden / MROWS;
         const unsigned yb = (unsigned)((rows * (MROWS / 4) + 127) / 128);
         e = launch_pdl(project_reduce_rows_kernel, dim3((unsigned)nmb, yb), dim3(128), 0, st,
-                       (const float*)ws, p.U, p.KB, p.G, p.J, rows, hidden, (uint16_t*)y);
+                       (const float*)ws, p.U, p.KB, p.G, p.J, rows, hidden, (uint16_t*)y, yf);
     } else {
         const long long n4 = (long long)rows * hidden / 4;
         long long blocks = (n4 + 255) / 256;
         if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
         e = launch_pdl(project_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
-                       (const float*)ws, p.U, p.KB, p.G, p.J, rows, hidden, (uint16_t*)y);
+                       (const float*)ws, p.U, p.KB, p.G, p.J, rows, hidden, (uint16_t*)y, yf);
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "projection reduce launch");

@@ -21,7 +21,7 @@ class DsaDecodeLayer:
     def __init__(self, wl: Workload, device: str = "cuda", keep_olat: bool = False,
                  with_o_absorb: bool = True, use_drawn_kpool: bool = False,
                  score_path: str = "auto", fuse_expand: bool = True, decode_from=None,
-                 fuse_append: bool = True, latent_fp8: bool = False):
+                 fuse_append: bool = True, latent_fp8: bool = False, frontend=None):
         g = wl.geom
         self.wl = wl
         self.geom = g
@@ -115,6 +115,43 @@ class DsaDecodeLayer:
         self.append_graph: Optional[torch.cuda.CUDAGraph] = None
         if decode_from is not None:
             self._init_append(decode_from)
+        # Projection front-end (dsa_frontend): the step's query inputs and the token's
+        # staged rows computed from a hidden state x on the device.
+        self.fe = None
+        if frontend is not None:
+            self._init_frontend(frontend)
+
+    def _init_frontend(self, fe) -> None:
+        g, dev, R = self.geom, self.device, self.wl.rows
+        up = lambda t: t.to(dev).contiguous()
+        self.fe = fe
+        self.x = up(fe.x)
+        self.w_x = up(fe.packed_x_weights())
+        self.q_a_norm, self.kv_a_norm = up(fe.q_a_norm), up(fe.kv_a_norm)
+        self.q_absorb, self.wq_b = up(fe.q_absorb), up(fe.wq_b)
+        if self.decode_from is None:  # the staged rows have nowhere to go: scratch
+            self.k_new = torch.zeros((R, g.index_head_dim), dtype=torch.bfloat16, device=dev)
+            self.gate_new = torch.zeros_like(self.k_new)
+            self.ckv_new = torch.zeros((R, g.kv_lora_rank), dtype=torch.bfloat16, device=dev)
+        n = api.dsa_frontend_workspace(R, g.hidden, int(self.w_x.shape[0]), fe.q_lora_rank,
+                                       g.kv_lora_rank, g.index_head_dim, g.index_heads, g.heads)
+        self.fe_workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+
+    def frontend(self, stream=None) -> None:
+        """x -> qlat, qidx, w (the step's inputs) and k_new, gate_new, ckv_new (the
+        token's rows that append() stores)."""
+        api.dsa_frontend(self.x, self.w_x, self.q_a_norm, self.kv_a_norm, self.fe.eps,
+                         self.q_absorb, self.wq_b, self.qlat, self.qidx, self.w, self.k_new,
+                         self.gate_new, self.ckv_new, self.status, self.fe_workspace,
+                         stream=stream)
+
+    def layer_step(self, stream=None) -> None:
+        """The whole decode layer: front-end, the token's append (when the layer was
+        built with decode_from), then the step."""
+        self.frontend(stream)
+        if self.decode_from is not None:
+            self.append(stream)
+        self.step(stream)
 
     # -- decode-time append -------------------------------------------------
     def _token_rows(self, b: int, t0: int, t1: int) -> np.ndarray:
@@ -310,6 +347,30 @@ class DsaDecodeLayer:
         if self.o_absorb is not None:
             n += (R + 63) // 64 + 1  # projection kernel(s) + reduction (either form)
         return n
+
+    def capture_layer(self) -> torch.cuda.CUDAGraph:
+        """Capture layer_step() into a CUDA graph. frontend() and step() run once
+        eagerly first (neither changes a cache or a length)."""
+        if self.fe is None:
+            raise ValueError("the layer was not built with a front-end")
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            self.frontend()
+            self.step()
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        torch.cuda.synchronize(self.device)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            self.layer_step()
+        self.layer_graph = gr
+        return gr
+
+    def launches_per_layer_step(self) -> int:
+        """Library kernel launches one layer_step() makes: the front-end's three
+        GEMMs with their reductions and the norm kernel, the append, the step."""
+        n = 7 + self.launches_per_step()
+        return n + (0 if self.decode_from is None else (1 if self.fuse_append else 3))
 
     def launches_per_append_step(self) -> int:
         """Library kernel launches one append_step() makes."""

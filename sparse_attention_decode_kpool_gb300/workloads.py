@@ -40,6 +40,8 @@ import torch
 _T_KRAW, _T_LNW, _T_LNB, _T_GATE, _T_APE, _T_VALID = 1, 2, 3, 4, 5, 6
 _T_QIDX, _T_W, _T_QLAT, _T_CKV, _T_OABS, _T_LENS, _T_PERM = 7, 8, 9, 10, 11, 12, 13
 _T_KPOOL = 14
+_T_FX, _T_FQA, _T_FKVA, _T_FWK, _T_FGATE, _T_FWP, _T_FQN, _T_FKVN, _T_FQABS, _T_FWQB = (
+    20, 21, 22, 23, 24, 25, 26, 27, 28, 29)
 
 
 def _rng(seed: int, tensor: int, seq: int = 0, chunk: Optional[int] = None) -> np.random.Generator:
@@ -358,6 +360,62 @@ def make_workload(
         k_raw=k_raw, gate=gate, valid=valid, ape=ape, ln_w=ln_w, ln_b=ln_b,
         qidx=qidx, w=w, qlat=qlat, ckv=ckv, o_absorb=o_absorb,
         kpool_keys=kpool_keys, kpool_valid=kpool_valid,
+    )
+
+
+# ---------------------------------------------------------------------------
+# Projection front-end inputs (the hidden state and the weights that turn it into
+# the step's inputs). Random weights with the checkpoint's shapes, scaled so every
+# projection output is O(1); q_absorb is drawn directly (it is a load-time product,
+# but only its shape and scale matter here).
+
+
+@dataclasses.dataclass
+class FrontEnd:
+    x: torch.Tensor              # [R, hidden] bf16
+    q_a_proj: torch.Tensor       # [q_lora, hidden]
+    kv_a_proj: torch.Tensor      # [kv_lora, hidden]
+    wk: torch.Tensor             # [ihd, hidden]
+    compress_gate: torch.Tensor  # [ihd, hidden]
+    weights_proj: torch.Tensor   # [index_heads, hidden], already x index_heads^-0.5
+    q_a_norm: torch.Tensor       # [q_lora]
+    kv_a_norm: torch.Tensor      # [kv_lora]
+    q_absorb: torch.Tensor       # [heads * kv_lora, q_lora]
+    wq_b: torch.Tensor           # [index_heads * ihd, q_lora]
+    eps: float
+
+    @property
+    def q_lora_rank(self) -> int:
+        return int(self.q_a_proj.shape[0])
+
+    def packed_x_weights(self) -> torch.Tensor:
+        """The five x projections as one [n_x, hidden] matrix (row concatenation in
+        the order q_a, kv_a, wk, gate, weights_proj, then zero rows to a multiple of
+        64): the layout the front-end streams."""
+        parts = [self.q_a_proj, self.kv_a_proj, self.wk, self.compress_gate, self.weights_proj]
+        n = sum(int(t.shape[0]) for t in parts)
+        pad = (-n) % 64
+        if pad:
+            parts.append(torch.zeros((pad, self.x.shape[1]), dtype=torch.bfloat16))
+        return torch.cat(parts, dim=0).contiguous()
+
+
+def make_frontend(g: "Geometry", rows: int, q_lora_rank: int = 1536, seed: int = 0,
+                  eps: float = 1e-6) -> FrontEnd:
+    hidden, kvl, ihd, hi = g.hidden, g.kv_lora_rank, g.index_head_dim, g.index_heads
+    mat = lambda t, n, k, std: _normal_bf16(seed, t, 0, n * k, 0.0, std).view(n, k)
+    return FrontEnd(
+        x=mat(_T_FX, rows, hidden, 1.0),
+        q_a_proj=mat(_T_FQA, q_lora_rank, hidden, hidden ** -0.5),
+        kv_a_proj=mat(_T_FKVA, kvl, hidden, hidden ** -0.5),
+        wk=mat(_T_FWK, ihd, hidden, hidden ** -0.5),
+        compress_gate=mat(_T_FGATE, ihd, hidden, hidden ** -0.5),
+        weights_proj=mat(_T_FWP, hi, hidden, hidden ** -0.5 * hi ** -0.5),
+        q_a_norm=_normal_bf16(seed, _T_FQN, 0, q_lora_rank, 1.0, 0.1),
+        kv_a_norm=_normal_bf16(seed, _T_FKVN, 0, kvl, 1.0, 0.1),
+        q_absorb=mat(_T_FQABS, g.heads * kvl, q_lora_rank, q_lora_rank ** -0.5),
+        wq_b=mat(_T_FWQB, hi * ihd, q_lora_rank, q_lora_rank ** -0.5),
+        eps=eps,
     )
 
 
