@@ -8,7 +8,7 @@ flushed (a 256 MiB write) between timed steps, outside the timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload 3] [--no-cpu-baseline] [--no-e2e] [--always-select-tail]
-                  [--decode-append]
+                  [--decode-append] [--latent-fp8] [--frontend [--q-lora-rank Q]]
 
 --impl reference times the CPU oracle (the plain float64 restatement of the
 method) on the host, one query row per step, single-threaded.
@@ -180,7 +180,10 @@ def algorithmic_bytes(wl, layer) -> dict:
     keys = cand * g.index_head_dim * 2
     q = wl.rows * g.index_heads * (g.index_head_dim * 2 + 4)
     sel_tokens = int((layer.token_ids >= 0).sum().item())
-    latent = sel_tokens * g.kv_lora_rank * 2
+    # a gathered latent row: bf16, or E4M3 codes plus one f32 scale per 128 channels
+    row_bytes = (g.kv_lora_rank + g.kv_lora_rank // 128 * 4 if layer.latent_fp8
+                 else g.kv_lora_rank * 2)
+    latent = sel_tokens * row_bytes
     qlat = wl.rows * g.heads * g.kv_lora_rank * 2
     oabs = g.hidden * g.heads * g.kv_lora_rank * 2 if layer.o_absorb is not None else 0
     y = wl.rows * g.hidden * 2 if layer.o_absorb is not None else 0
@@ -193,9 +196,17 @@ def algorithmic_bytes(wl, layer) -> dict:
         ihd, kp = g.index_head_dim, g.index_kpool
         app = wl.batch * (2 * (2 * ihd + g.kv_lora_rank) * 2 + 1
                           + kp * (2 * ihd * 2 + 1) + ihd * 2 + 1)
+    # --frontend: every front-end weight once, the hidden state in, and its outputs
+    # (qlat, qidx, w, the staged rows) out.
+    fe = 0
+    if layer.fe is not None:
+        wts = (layer.w_x, layer.w_q, layer.q_a_norm, layer.kv_a_norm)
+        fe = sum(t.numel() * t.element_size() for t in wts)
+        fe += layer.x.numel() * 2 + qlat + q
+        fe += wl.rows * (2 * g.index_head_dim + g.kv_lora_rank) * 2
     return {"score": keys + flags + q, "attend": latent + qlat, "project": oabs + olat + y,
-            "append": app,
-            "total": keys + flags + q + latent + qlat + oabs + y + app,
+            "append": app, "frontend": fe,
+            "total": keys + flags + q + latent + qlat + oabs + y + app + fe,
             "selected_tokens": sel_tokens, "candidate_pools": cand}
 
 
@@ -219,11 +230,12 @@ class OracleRunner:
     """Times the oracle's decode_row on rows of the workload. The oracle's own
     pooled-key cache of a sequence is built once, untimed (it is layer state)."""
 
-    def __init__(self, wl, with_project: bool = True):
+    def __init__(self, wl, with_project: bool = True, latent_fp8: bool = False):
         from oracle import dsa_oracle as O
 
         self.O, self.wl = O, wl
         self.with_project = with_project
+        self.latent_fp8 = latent_fp8
         self._pools = {}
         self._A = None
 
@@ -246,7 +258,10 @@ class OracleRunner:
             keys, pv, _ = O.kpool_compress(self._tokens(wl.k_raw, b), self._tokens(wl.gate, b),
                                            self._tokens(wl.valid, b), wl.ape.numpy(), f(wl.ln_w),
                                            f(wl.ln_b), g.eps, g.first_key, g.index_kpool)
-            self._pools[b] = (keys, pv, self._tokens(wl.ckv, b))
+            ckv = self._tokens(wl.ckv, b)
+            if self.latent_fp8:  # the FP8 cache, encoded and decoded once (layer state)
+                ckv = O.dequantize_latent_fp8(*O.quantize_latent_fp8(ckv))
+            self._pools[b] = (keys, pv, ckv)
         if self._A is None and wl.o_absorb is not None and self.with_project:
             self._A = wl.o_absorb.float().numpy()
         return b
@@ -266,9 +281,9 @@ class OracleRunner:
         return time.perf_counter() - t0
 
 
-def cpu_baseline(wl, budget_s: float = 12.0, max_rows: int = 2) -> dict:
+def cpu_baseline(wl, budget_s: float = 12.0, max_rows: int = 2, latent_fp8: bool = False) -> dict:
     prefill = wl.name.startswith("prefill")
-    runner = OracleRunner(wl, with_project=not prefill)
+    runner = OracleRunner(wl, with_project=not prefill, latent_fp8=latent_fp8)
     times, rows = [], []
     for r in range(min(max_rows, wl.rows)):
         runner._prep(r)
@@ -306,7 +321,7 @@ def run_reference(args, ws, rank):
         return
     wl = make_wl(args)
     prefill = args.workload == PREFILL_WORKLOAD
-    runner = OracleRunner(wl, with_project=not prefill)
+    runner = OracleRunner(wl, with_project=not prefill, latent_fp8=args.latent_fp8)
     rows = [r % wl.rows for r in range(min(2, wl.rows))]
     for r in rows:
         runner._prep(r)
@@ -338,6 +353,9 @@ def workload_config(wl, args) -> dict:
             "paged_block": wl.block_size, "seed": wl.seed,
             "always_select_tail": bool(g.always_select_tail),
             "decode_append": bool(getattr(args, "decode_append", False)),
+            "latent_cache": "fp8-e4m3" if getattr(args, "latent_fp8", False) else "bf16",
+            "frontend": ({"q_lora_rank": args.q_lora_rank}
+                         if getattr(args, "frontend", False) else None),
             "l2": "flushed between timed steps (256 MiB write, then a 256 MiB read so the dirty "
                   "lines are written back; both outside the timed events)",
             "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
@@ -358,6 +376,14 @@ def main():
                     help="each step first appends one token per sequence (indexer store, "
                          "device-side geometry, compress of the newly whole pool), replayed "
                          "as one graph over the growing context")
+    ap.add_argument("--frontend", action="store_true",
+                    help="each step starts from the hidden state: the projection front-end "
+                         "(q_a/kv_a/indexer projections, a-norms, q_absorb, wq_b) on the "
+                         "device, then the step")
+    ap.add_argument("--q-lora-rank", type=int, default=1536)
+    ap.add_argument("--latent-fp8", action="store_true",
+                    help="attention reads an FP8 latent cache (E4M3 codes + power-of-two "
+                         "scales per 128 channels) encoded once from the bf16 cache")
     ap.add_argument("--always-select-tail", action="store_true",
                     help="index rows index_topk + kpool - 1 wide, the trailing partial "
                          "pool's tokens always attended")
@@ -389,8 +415,13 @@ def main():
         # Room for every replay that appends (warm-up, timed, stage and e2e passes).
         room = args.warmup + 3 * args.steps + 16
         decode_from = np.maximum(wl.seq_lens.astype(np.int64) - room, 0)
+    fe = None
+    if args.frontend:
+        if prefill:
+            raise SystemExit("--frontend applies to the decode workloads")
+        fe = W.make_frontend(wl.geom, wl.rows, q_lora_rank=args.q_lora_rank, seed=wl.seed + 100)
     layer = DsaDecodeLayer(wl, device=str(dev), with_o_absorb=not prefill, keep_olat=prefill,
-                           decode_from=decode_from)
+                           decode_from=decode_from, latent_fp8=args.latent_fp8, frontend=fe)
     if append:
         layer.stage(0)  # the staged rows stay as they are for every replay
     layer.compress()
@@ -425,7 +456,9 @@ def main():
 
     # The timed graph: the step's library calls only (with --decode-append, the
     # append of one token per sequence first: every replay grows the context).
-    if append:
+    if fe is not None:
+        graph = layer.capture_layer()
+    elif append:
         graph = layer.capture_append()
     else:
         s = torch.cuda.Stream(device=dev)
@@ -439,8 +472,8 @@ def main():
             layer.step()
     # A second graph with timing event nodes at the stage boundaries (external
     # events when the installed torch supports them): per-stage times.
-    stage_names = (["append"] if append else []) + ["score", "select", "expand", "attend"] + (
-        [] if prefill else ["project"])
+    stage_names = (["frontend"] if fe is not None else []) + (["append"] if append else []) + [
+        "score", "select", "expand", "attend"] + ([] if prefill else ["project"])
     ns = len(stage_names)
     try:
         ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(ns + 1)]
@@ -456,7 +489,8 @@ def main():
                 getattr(layer, k)()
                 ev[j + 1].record()
 
-    launches = layer.launches_per_append_step() if append else layer.launches_per_step()
+    launches = (layer.launches_per_layer_step() if fe is not None else
+                layer.launches_per_append_step() if append else layer.launches_per_step())
     for _ in range(args.warmup):
         flush.zero_()
         graph.replay()
@@ -512,16 +546,21 @@ def main():
         # The step's inputs: query tensors and the row contexts; with --decode-append
         # the staged token rows instead of the contexts (those follow the lengths on
         # the device).
-        ins = [(layer.qidx, h_qidx), (layer.w, h_w), (layer.qlat, h_qlat)]
-        if append:
+        # With --frontend the hidden state replaces the query tensors and the staged
+        # rows (the front-end makes both on the device).
+        if fe is not None:
+            ins = [(layer.x, fe.x.pin_memory())]
+        else:
+            ins = [(layer.qidx, h_qidx), (layer.w, h_w), (layer.qlat, h_qlat)]
+        if append and fe is None:
             ins += [(d, h.pin_memory()) for d, h in zip((layer.k_new, layer.gate_new,
                                                         layer.ckv_new), layer.staged_rows(0))]
-        else:
+        elif not append:
             ins.append((layer.row_ctx, h_ctx))
         h2d = sum(h.numel() * h.element_size() for _, h in ins)
         d2h = h_y.numel() * h_y.element_size()
         for _ in range(3):
-            layer.qidx.copy_(h_qidx, non_blocking=True)
+            ins[0][0].copy_(ins[0][1], non_blocking=True)
             graph.replay()
         torch.cuda.synchronize()
         t_e2e = []
@@ -538,7 +577,9 @@ def main():
         e2e_ms = max_over_ranks(1e3 * sum(t_e2e) / len(t_e2e), ws)
         e2e = {"value": queries / (e2e_ms * 1e-3), "unit": "queries/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "path": "pinned host qidx/w/qlat/" + ("staged token rows" if append else "row_ctx")
+               "path": "pinned host " + ("x (hidden state)" if fe is not None else "qidx/w/qlat")
+                       + ("" if append and fe is not None else
+                          "/staged token rows" if append else "/row_ctx")
                        + " -> device, graph replay, " + ("olat" if prefill else "y") + " -> host"}
 
     if rank != 0:
@@ -569,7 +610,8 @@ def main():
         peak_src = "measured" if hbm else "fallback"
         hbm = hbm or 6800.0
         ab = algorithmic_bytes(wl, layer)
-        dom = max(("score", "attend", "project"), key=lambda k: stage_ms[k])
+        dom = max(("score", "attend", "project") + (("frontend",) if fe is not None else ()),
+                  key=lambda k: stage_ms[k])
         dom_bytes = ab[dom]
         achieved = dom_bytes / (stage_ms[dom] * 1e-3) / 1e9
         total_gbs = ab["total"] / (ms * 1e-3) / 1e9
@@ -580,7 +622,9 @@ def main():
                     "kernel": {"attend": "dsa_sparse_mla_decode (split attention + combine)",
                                "project": "dsa_latent_project (TMA-pipelined o_absorb GEMM + "
                                           "partial sum)",
-                               "score": "dsa_score"}[dom],
+                               "score": "dsa_score",
+                               "frontend": "dsa_frontend (x projections, a-norms, q_absorb and "
+                                           "wq_b skinny GEMMs)"}[dom],
                     "algorithmic_bytes_per_launch": dom_bytes,
                     "step_algorithmic_bytes": ab["total"], "step_achieved_gbs": total_gbs,
                     "step_frac": total_gbs / hbm}
@@ -600,7 +644,7 @@ def main():
     if e2e is not None:
         line["e2e"] = e2e
     if not args.no_cpu_baseline and ws == 1:
-        line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"] = cpu_baseline(wl, latent_fp8=args.latent_fp8)
     print(json.dumps(line), flush=True)
 
 

@@ -94,7 +94,7 @@ const char* dsa_last_error(void);
 
 /* ABI version of this header (bumped on any signature change). */
 int dsa_abi_version(void);
-#define DSA_ABI_VERSION 5
+#define DSA_ABI_VERSION 6
 
 /*
  * Layer-geometry rules (mod.rs, Glm5NextDsaConfig::validate): index_kpool and
@@ -417,16 +417,17 @@ int dsa_sparse_mla_decode_fp8(const dsa_bf16* qlat, int rows, int heads, int kv_
  *   [q_a | kv_a | k | g | wv] = w_x . x[r]                    (f32 sums)
  *   q_lora   = bf16(q_a / sqrt(mean(q_a^2) + eps) * q_a_norm)
  *   ckv_new  = bf16(kv_a / sqrt(mean(kv_a^2) + eps) * kv_a_norm)
- *   qlat     = bf16(q_absorb . q_lora)       qidx = bf16(wq_b . q_lora)
+ *   [qlat | qidx] = bf16(w_q . q_lora)
  *   k_new    = bf16(k)    gate_new = bf16(g)    w = wv (f32)
  *
  * w_x [n_x, hidden] bf16 is the load-time row concatenation of q_a_proj
  * [q_lora_rank], kv_a_proj_with_mqa [kv_lora_rank], indexer.wk [ihd], the compress
  * gate [ihd] and indexer.weights_proj [index_heads] (already scaled by
  * index_heads^-0.5, build.rs transform 2), then zero rows up to n_x, so the hidden
- * state is streamed once for all five. q_a_norm [q_lora_rank], kv_a_norm
- * [kv_lora_rank] bf16; q_absorb [heads * kv_lora_rank, q_lora_rank] (build.rs
- * absorb_q); wq_b [index_heads * ihd, q_lora_rank]. x [rows, hidden] bf16.
+ * state is streamed once for all five. w_q [heads * kv_lora_rank + index_heads *
+ * ihd, q_lora_rank] bf16 is likewise q_absorb (build.rs absorb_q) with indexer.wq_b
+ * below it. q_a_norm [q_lora_rank], kv_a_norm [kv_lora_rank] bf16. x [rows, hidden]
+ * bf16.
  * Outputs (row-major, one row per query): qlat [rows, heads, kv_lora_rank] bf16,
  * qidx [rows, index_heads, ihd] bf16, w [rows, index_heads] f32, and the token's
  * staged rows for dsa_indexer_store / dsa_decode_append: k_new, gate_new
@@ -442,7 +443,7 @@ int dsa_frontend_workspace(int rows, int hidden, int n_x, int q_lora_rank, int k
 int dsa_frontend(const dsa_bf16* x, int rows, int hidden, const dsa_bf16* w_x, int n_x,
                  int q_lora_rank, int kv_lora_rank, int ihd, int index_heads,
                  const dsa_bf16* q_a_norm, const dsa_bf16* kv_a_norm, float eps,
-                 const dsa_bf16* q_absorb, int heads, const dsa_bf16* wq_b, dsa_bf16* qlat,
+                 const dsa_bf16* w_q, int heads, dsa_bf16* qlat,
                  dsa_bf16* qidx, float* w, dsa_bf16* k_new, dsa_bf16* gate_new,
                  dsa_bf16* ckv_new, int32_t* status, void* workspace, size_t workspace_bytes,
                  void* stream);

@@ -21,7 +21,7 @@ DSA_STATUS_BAD_TOKEN = 1
 DSA_STATUS_BAD_BLOCK = 2
 DSA_STATUS_TIMEOUT = 4
 DSA_STATUS_CACHE_FULL = 8
-DSA_ABI_VERSION = 5
+DSA_ABI_VERSION = 6
 
 
 class DsaPaging(ctypes.Structure):
@@ -70,7 +70,7 @@ SIGNATURES = {
     "dsa_sparse_mla_decode_fp8": (_I, [_P, _I, _I, _I, _P, _P, _P, _PG, _P, _I, _F, _P, _I, _P,
                                        _P, _P, _P, _SZ, _P]),
     "dsa_frontend_workspace": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
-    "dsa_frontend": (_I, [_P, _I, _I, _P, _I, _I, _I, _I, _I, _P, _P, _F, _P, _I, _P, _P, _P, _P,
+    "dsa_frontend": (_I, [_P, _I, _I, _P, _I, _I, _I, _I, _I, _P, _P, _F, _P, _I, _P, _P, _P,
                           _P, _P, _P, _P, _P, _SZ, _P]),
     "dsa_latent_project_workspace": (_I, [_I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "dsa_latent_project": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P, _SZ, _P]),

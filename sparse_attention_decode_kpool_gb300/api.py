@@ -331,9 +331,10 @@ def dsa_frontend_workspace(rows: int, hidden: int, n_x: int, q_lora_rank: int, k
     return int(n.value)
 
 
-def dsa_frontend(x, w_x, q_a_norm, kv_a_norm, eps: float, q_absorb, wq_b, qlat, qidx, w, k_new,
-                 gate_new, ckv_new, status=None, workspace=None, stream=None) -> None:
-    """The step's inputs from the hidden state (see dsa_frontend in include/dsa.h)."""
+def dsa_frontend(x, w_x, q_a_norm, kv_a_norm, eps: float, w_q, qlat, qidx, w, k_new, gate_new,
+                 ckv_new, status=None, workspace=None, stream=None) -> None:
+    """The step's inputs from the hidden state (see dsa_frontend in include/dsa.h):
+    w_x packs the five x projections, w_q packs q_absorb over indexer.wq_b."""
     rows, hidden = (int(v) for v in x.shape)
     n_x = int(w_x.shape[0])
     ql, kvl = int(q_a_norm.numel()), int(kv_a_norm.numel())
@@ -341,14 +342,14 @@ def dsa_frontend(x, w_x, q_a_norm, kv_a_norm, eps: float, q_absorb, wq_b, qlat, 
     _, hi, ihd = (int(v) for v in qidx.shape)
     if kvl2 != kvl or tuple(w_x.shape) != (n_x, hidden):
         raise ValueError("qlat's width must be kv_lora_rank and w_x [n_x, hidden]")
-    if tuple(q_absorb.shape) != (heads * kvl, ql) or tuple(wq_b.shape) != (hi * ihd, ql):
-        raise ValueError("q_absorb must be [heads*kvl, q_lora] and wq_b [index_heads*ihd, q_lora]")
+    if tuple(w_q.shape) != (heads * kvl + hi * ihd, ql):
+        raise ValueError("w_q must be [heads*kvl + index_heads*ihd, q_lora]")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     check(_lib.load().dsa_frontend(
         _ptr(x, torch.bfloat16, "x"), rows, hidden, _ptr(w_x, torch.bfloat16, "w_x"), n_x, ql, kvl,
         ihd, hi, _ptr(q_a_norm, torch.bfloat16, "q_a_norm"),
         _ptr(kv_a_norm, torch.bfloat16, "kv_a_norm"), float(eps),
-        _ptr(q_absorb, torch.bfloat16, "q_absorb"), heads, _ptr(wq_b, torch.bfloat16, "wq_b"),
+        _ptr(w_q, torch.bfloat16, "w_q"), heads,
         _ptr(qlat, torch.bfloat16, "qlat"), _ptr(qidx, torch.bfloat16, "qidx"),
         _ptr(w, torch.float32, "w"), _ptr(k_new, torch.bfloat16, "k_new"),
         _ptr(gate_new, torch.bfloat16, "gate_new"), _ptr(ckv_new, torch.bfloat16, "ckv_new"),

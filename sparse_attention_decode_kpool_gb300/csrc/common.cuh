@@ -65,12 +65,14 @@ int make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, 
                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
 // The o_absorb projection (project.cu), a skinny GEMM: y[r] = bf16(A . x[r]), x bf16 or
-// f32, A [hidden, K] bf16; with yf the sums are stored as f32 there instead of y.
+// f32, A [hidden, K] bf16. With yf the sums are stored as f32 there instead of y; with
+// y2, output columns from `split` (a multiple of 64) on go to y2 [rows, hidden - split]
+// and y is [rows, split].
 bool project_supported(int K, int hidden);
 size_t project_workspace_bytes(int rows, int K, int hidden, int sms);
 int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A, int hidden,
                    uint16_t* y, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st,
-                   float* yf = nullptr);
+                   float* yf = nullptr, uint16_t* y2 = nullptr, int split = 0);
 
 // Sparse latent attention on the tensor cores (mla_tc.cu): the split kernel of
 // dsa_sparse_mla_decode for 64 heads when DSA_MLA_TC=1. Writes the splits' partials

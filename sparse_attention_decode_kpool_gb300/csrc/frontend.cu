@@ -8,7 +8,7 @@
 //   [q_a | kv_a | k | gate | w] = W_x . x        (one skinny GEMM over the x weights,
 //                                                 f32 results)
 //   q_lora = bf16(rms(q_a) * q_a_norm)           ckv = bf16(rms(kv_a) * kv_a_norm)
-//   qlat   = bf16(q_absorb . q_lora)             qidx = bf16(wq_b . q_lora)
+//   [qlat | qidx] = bf16(w_q . q_lora)            (w_q = [q_absorb ; wq_b], one GEMM)
 //   k_new  = bf16(k),  gate_new = bf16(gate),    w (f32)
 //
 // with rms(v) = v / sqrt(mean(v^2) + eps). At decode sizes each GEMM streams its
@@ -47,6 +47,9 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 __global__ void __launch_bounds__(kNormThreads) frontend_norm_kernel(NormArgs a) {
+    // The q GEMM after this kernel streams weights it can fetch before q_lora
+    // exists: let its blocks start now (they wait for this grid before reading it).
+    pdl_trigger();
     pdl_wait();
     __shared__ float red[kNormThreads / 32];
     const int r = blockIdx.x;
@@ -81,16 +84,14 @@ struct FrontPlan {
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-FrontPlan front_plan(int rows, int hidden, int n_x, int ql, int nq, int ni, int sms) {
+FrontPlan front_plan(int rows, int hidden, int n_x, int ql, int nq, int sms) {
     FrontPlan p;
     p.off_y1 = 0;
     p.off_qlora = al256((size_t)rows * n_x * 4);
     p.off_part = p.off_qlora + al256((size_t)rows * ql * 2);
     size_t part = project_workspace_bytes(rows, hidden, n_x, sms);
     const size_t b = project_workspace_bytes(rows, ql, nq, sms);
-    const size_t c = project_workspace_bytes(rows, ql, ni, sms);
     if (b > part) part = b;
-    if (c > part) part = c;
     p.bytes = p.off_part + al256(part);
     return p;
 }
@@ -106,7 +107,7 @@ int check_front(int rows, int hidden, int n_x, int ql, int kvl, int ihd, int hi,
         return fail(DSA_ERR_INVALID_ARG, "dsa_frontend: n_x %d < q_lora + kv_lora + 2*ihd + heads",
                     n_x);
     if (!project_supported(hidden, n_x) || !project_supported(ql, heads * kvl) ||
-        !project_supported(ql, hi * ihd))
+        !project_supported(ql, hi * ihd) || !project_supported(ql, heads * kvl + hi * ihd))
         return fail(DSA_ERR_UNSUPPORTED,
                     "dsa_frontend: hidden and q_lora_rank must be multiples of 256; n_x, "
                     "heads*kv_lora_rank and index_heads*ihd multiples of 64");
@@ -128,7 +129,7 @@ extern "C" int dsa_frontend_workspace(int rows, int hidden, int n_x, int q_lora_
     if (rc) return rc;
     const int sms = sm_count();
     if (sms <= 0) return fail(DSA_ERR_CUDA, "dsa_frontend_workspace: no CUDA device");
-    *bytes = front_plan(rows, hidden, n_x, q_lora_rank, heads * kv_lora_rank, index_heads * ihd,
+    *bytes = front_plan(rows, hidden, n_x, q_lora_rank, heads * kv_lora_rank + index_heads * ihd,
                         sms)
                  .bytes;
     return DSA_OK;
@@ -137,24 +138,24 @@ extern "C" int dsa_frontend_workspace(int rows, int hidden, int n_x, int q_lora_
 extern "C" int dsa_frontend(const dsa_bf16* x, int rows, int hidden, const dsa_bf16* w_x, int n_x,
                             int q_lora_rank, int kv_lora_rank, int ihd, int index_heads,
                             const dsa_bf16* q_a_norm, const dsa_bf16* kv_a_norm, float eps,
-                            const dsa_bf16* q_absorb, int heads, const dsa_bf16* wq_b,
-                            dsa_bf16* qlat, dsa_bf16* qidx, float* w, dsa_bf16* k_new,
-                            dsa_bf16* gate_new, dsa_bf16* ckv_new, int32_t* status,
+                            const dsa_bf16* w_q, int heads, dsa_bf16* qlat, dsa_bf16* qidx,
+                            float* w, dsa_bf16* k_new, dsa_bf16* gate_new, dsa_bf16* ckv_new,
+                            int32_t* status,
                             void* workspace, size_t workspace_bytes, void* stream) {
     int rc = check_front(rows, hidden, n_x, q_lora_rank, kv_lora_rank, ihd, index_heads, heads);
     if (rc) return rc;
     if (!(eps >= 0.f)) return fail(DSA_ERR_INVALID_ARG, "dsa_frontend: eps must be >= 0");
     if (rows == 0) return DSA_OK;
-    if (!x || !w_x || !q_a_norm || !kv_a_norm || !q_absorb || !wq_b || !qlat || !qidx || !w ||
+    if (!x || !w_x || !q_a_norm || !kv_a_norm || !w_q || !qlat || !qidx || !w ||
         !k_new || !gate_new || !ckv_new)
         return fail(DSA_ERR_INVALID_ARG, "dsa_frontend: NULL tensor");
-    if ((((uintptr_t)x) | ((uintptr_t)w_x) | ((uintptr_t)q_absorb) | ((uintptr_t)wq_b) |
-         ((uintptr_t)qlat) | ((uintptr_t)qidx) | ((uintptr_t)workspace)) & 15)
+    if ((((uintptr_t)x) | ((uintptr_t)w_x) | ((uintptr_t)w_q) | ((uintptr_t)qlat) |
+         ((uintptr_t)qidx) | ((uintptr_t)workspace)) & 15)
         return fail(DSA_ERR_INVALID_ARG, "dsa_frontend: tensors must be 16-byte aligned");
     const int sms = sm_count();
     if (sms <= 0) return fail(DSA_ERR_CUDA, "dsa_frontend: no CUDA device");
-    const FrontPlan p = front_plan(rows, hidden, n_x, q_lora_rank, heads * kv_lora_rank,
-                                   index_heads * ihd, sms);
+    const int nq = heads * kv_lora_rank + index_heads * ihd;
+    const FrontPlan p = front_plan(rows, hidden, n_x, q_lora_rank, nq, sms);
     if (!workspace || workspace_bytes < p.bytes)
         return fail(DSA_ERR_INVALID_ARG, "dsa_frontend: workspace %zu B < %zu B needed",
                     workspace_bytes, p.bytes);
@@ -187,9 +188,6 @@ extern "C" int dsa_frontend(const dsa_bf16* x, int rows, int hidden, const dsa_b
                                st, na);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_frontend norm launch");
-    rc = project_launch(q_lora, false, rows, q_lora_rank, q_absorb, heads * kv_lora_rank, qlat,
-                        status, part, part_bytes, st);
-    if (rc) return rc;
-    return project_launch(q_lora, false, rows, q_lora_rank, wq_b, index_heads * ihd, qidx, status,
-                          part, part_bytes, st);
+    return project_launch(q_lora, false, rows, q_lora_rank, w_q, nq, qlat, status, part,
+                          part_bytes, st, nullptr, qidx, heads * kv_lora_rank);
 }

@@ -223,9 +223,32 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NT))
 // y[r, col] = bf16(sum over the CTAs that covered row block col/64 of their partial),
 // the CTAs in ascending order. One thread per 4 columns; the contributing CTAs are
 // read four at a time so their loads overlap.
+// Where the sums go: f32 into yf [R, hidden] when it is set; else bf16, columns
+// below `split` into y [R, split] and the rest into y2 [R, hidden - split] (split is
+// hidden when y2 is NULL, and a multiple of 64).
+struct ProjOut {
+    uint16_t* y;
+    float* yf;
+    uint16_t* y2;
+    int split;
+};
+
+__device__ __forceinline__ void store_sum(const ProjOut& o, int r, int hidden, int col, float4 v) {
+    if (o.yf) {
+        *reinterpret_cast<float4*>(o.yf + (long long)r * hidden + col) = v;
+        return;
+    }
+    uint2 b;
+    b.x = pack_bf16x2(v.x, v.y);
+    b.y = pack_bf16x2(v.z, v.w);
+    if (col < o.split)
+        *reinterpret_cast<uint2*>(o.y + (long long)r * o.split + col) = b;
+    else
+        *reinterpret_cast<uint2*>(o.y2 + (long long)r * (hidden - o.split) + (col - o.split)) = b;
+}
+
 __global__ void project_reduce_kernel(const float* __restrict__ ypart, long long U, int KB, int G,
-                                      int J, int R, int hidden, uint16_t* __restrict__ y,
-                                      float* __restrict__ yf) {
+                                      int J, int R, int hidden, ProjOut out) {
     pdl_wait();
     const long long n4 = (long long)R * hidden / 4;
     for (long long i4 = blockIdx.x * (long long)blockDim.x + threadIdx.x; i4 < n4;
@@ -264,14 +287,7 @@ __global__ void project_reduce_kernel(const float* __restrict__ ypart, long long
             }
             if (c + 4 >= G || unit_begin(c + 4, U, G) >= hi) break;
         }
-        if (yf) {
-            *reinterpret_cast<float4*>(yf + i) = s;
-        } else {
-            uint2 o;
-            o.x = pack_bf16x2(s.x, s.y);
-            o.y = pack_bf16x2(s.z, s.w);
-            *reinterpret_cast<uint2*>(y + i) = o;
-        }
+        store_sum(out, r, hidden, col, s);
     }
 }
 
@@ -282,7 +298,7 @@ __global__ void project_reduce_kernel(const float* __restrict__ ypart, long long
 // order with all its loads issued together (eight at a time).
 __global__ void __launch_bounds__(128) project_reduce_rows_kernel(
     const float* __restrict__ ypart, long long U, int KB, int G, int J, int R, int hidden,
-    uint16_t* __restrict__ y, float* __restrict__ yf) {
+    ProjOut out) {
     pdl_wait();
     __shared__ long long soff[32];
     __shared__ int scount;
@@ -326,15 +342,7 @@ __global__ void __launch_bounds__(128) project_reduce_rows_kernel(
             }
         }
     }
-    const long long oi = (long long)r * hidden + mb * MROWS + 4 * c4;
-    if (yf) {
-        *reinterpret_cast<float4*>(yf + oi) = acc;
-        return;
-    }
-    uint2 out;
-    out.x = pack_bf16x2(acc.x, acc.y);
-    out.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(y + oi) = out;
+    store_sum(out, r, hidden, (int)(mb * MROWS) + 4 * c4, acc);
 }
 
 struct ProjPlan {
@@ -396,7 +404,12 @@ size_t project_workspace_bytes(int rows, int K, int hidden, int sms) {
 
 int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A, int hidden,
                    uint16_t* y, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st,
-                   float* yf) {
+                   float* yf, uint16_t* y2, int split) {
+    ProjOut out;
+    out.y = y;
+    out.yf = yf;
+    out.y2 = y2;
+    out.split = y2 ? split : hidden;
     const int sms = sm_count();
     if (sms <= 0) return fail(DSA_ERR_CUDA, "projection: no CUDA device");
     const ProjPlan p = plan_for(rows, K, hidden, sms);
@@ -434,13 +447,13 @@ int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A
         const long long nmb = hidden / MROWS;
         const unsigned yb = (unsigned)((rows * (MROWS / 4) + 127) / 128);
         e = launch_pdl(project_reduce_rows_kernel, dim3((unsigned)nmb, yb), dim3(128), 0, st,
-                       (const float*)ws, p.U, p.KB, p.G, p.J, rows, hidden, (uint16_t*)y, yf);
+                       (const float*)ws, p.U, p.KB, p.G, p.J, rows, hidden, out);
     } else {
         const long long n4 = (long long)rows * hidden / 4;
         long long blocks = (n4 + 255) / 256;
         if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
         e = launch_pdl(project_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
-                       (const float*)ws, p.U, p.KB, p.G, p.J, rows, hidden, (uint16_t*)y, yf);
+                       (const float*)ws, p.U, p.KB, p.G, p.J, rows, hidden, out);
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "projection reduce launch");

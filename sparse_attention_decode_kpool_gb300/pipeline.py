@@ -128,7 +128,7 @@ class DsaDecodeLayer:
         self.x = up(fe.x)
         self.w_x = up(fe.packed_x_weights())
         self.q_a_norm, self.kv_a_norm = up(fe.q_a_norm), up(fe.kv_a_norm)
-        self.q_absorb, self.wq_b = up(fe.q_absorb), up(fe.wq_b)
+        self.w_q = up(fe.packed_q_weights())
         if self.decode_from is None:  # the staged rows have nowhere to go: scratch
             self.k_new = torch.zeros((R, g.index_head_dim), dtype=torch.bfloat16, device=dev)
             self.gate_new = torch.zeros_like(self.k_new)
@@ -141,9 +141,8 @@ class DsaDecodeLayer:
         """x -> qlat, qidx, w (the step's inputs) and k_new, gate_new, ckv_new (the
         token's rows that append() stores)."""
         api.dsa_frontend(self.x, self.w_x, self.q_a_norm, self.kv_a_norm, self.fe.eps,
-                         self.q_absorb, self.wq_b, self.qlat, self.qidx, self.w, self.k_new,
-                         self.gate_new, self.ckv_new, self.status, self.fe_workspace,
-                         stream=stream)
+                         self.w_q, self.qlat, self.qidx, self.w, self.k_new, self.gate_new,
+                         self.ckv_new, self.status, self.fe_workspace, stream=stream)
 
     def layer_step(self, stream=None) -> None:
         """The whole decode layer: front-end, the token's append (when the layer was
@@ -367,9 +366,9 @@ class DsaDecodeLayer:
         return gr
 
     def launches_per_layer_step(self) -> int:
-        """Library kernel launches one layer_step() makes: the front-end's three
-        GEMMs with their reductions and the norm kernel, the append, the step."""
-        n = 7 + self.launches_per_step()
+        """Library kernel launches one layer_step() makes: the front-end's two GEMMs
+        with their reductions and the norm kernel, the append, the step."""
+        n = 5 + self.launches_per_step()
         return n + (0 if self.decode_from is None else (1 if self.fuse_append else 3))
 
     def launches_per_append_step(self) -> int:

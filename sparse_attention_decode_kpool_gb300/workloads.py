@@ -399,6 +399,11 @@ class FrontEnd:
             parts.append(torch.zeros((pad, self.x.shape[1]), dtype=torch.bfloat16))
         return torch.cat(parts, dim=0).contiguous()
 
+    def packed_q_weights(self) -> torch.Tensor:
+        """q_absorb with indexer.wq_b below it, [heads*kvl + index_heads*ihd, q_lora]:
+        one stream over q_lora's weights."""
+        return torch.cat([self.q_absorb, self.wq_b], dim=0).contiguous()
+
 
 def make_frontend(g: "Geometry", rows: int, q_lora_rank: int = 1536, seed: int = 0,
                   eps: float = 1e-6) -> FrontEnd:
