@@ -5,7 +5,8 @@
 
 Stages: compress, score, select, expand, attend, project, step. ``--rows`` shrinks
 the prefill chunk (workload 4), ``--seq-len`` the long-context sequences (workload
-3); ``--always-select-tail`` widens the index rows by the trailing partial pool.
+3); ``--always-select-tail`` widens the index rows by the trailing partial pool;
+``--latent-fp8`` gives attention the FP8 latent cache.
 Each iteration is preceded by a write-then-read of 256 MiB so that the stage
 starts from a cold L2; the median of the CUDA-event times is printed as one JSON
 line. Meant for profiler runs (a fixed, small number of launches of one stage)."""
@@ -45,12 +46,13 @@ def main(argv=None) -> None:
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--always-select-tail", action="store_true")
+    ap.add_argument("--latent-fp8", action="store_true")
     args = ap.parse_args(argv)
 
     wl = make(args.workload, args.seq_len, args.rows)
     if args.always_select_tail:
         wl.geom = dataclasses.replace(wl.geom, always_select_tail=True)
-    layer = DsaDecodeLayer(wl)
+    layer = DsaDecodeLayer(wl, latent_fp8=args.latent_fp8)
     layer.compress()
     layer.step()  # every stage's inputs exist from here on
     torch.cuda.synchronize()
