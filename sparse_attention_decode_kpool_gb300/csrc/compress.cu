@@ -39,6 +39,7 @@ struct CompressArgs {
     int first_key;
     int kpool;
     int append;  // > 0: only the pools completed by the last `append` tokens
+    int tiles;   // units of PPC pools per sequence
 };
 
 constexpr int kThreads = 256;
@@ -48,18 +49,27 @@ __device__ __forceinline__ int whole_pools(int n, int first_key, int kpool) {
     return n > first_key ? (n - first_key) / kpool : 0;
 }
 
+// 2^x on the special-function unit (x <= 0 here: softmax weights in (0, 1]).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // The pooled key of one pool for the 8 channels [c0, c0 + 8) this lane owns, from
-// its kpool rows of raw keys (kr) and gate logits (gr): LayerNorm per slot (the
-// pool's IHD/8 lanes reduce together, so every lane of the warp must call this),
-// bf16 rounding of the normalised key, and the slot softmax in the log2 domain.
+// its kpool rows of raw keys and gate logits (kr(s), gr(s): 16-byte vectors of slot
+// s): LayerNorm per slot (the pool's IHD/8 lanes reduce together, so every lane of
+// the warp must call this), bf16 rounding of the normalised key, and the slot softmax
+// in the log2 domain. Channels are processed in pairs with packed f32x2 arithmetic.
 // Returns the packed bf16 result (to be stored only for a valid pool).
-template <int IHD, int KPMAX>
-__device__ __forceinline__ uint4 pool_lane(const uint4 (&kr)[KPMAX], const uint4 (&gr)[KPMAX],
-                                           int KP, const float* __restrict__ ape,
+template <int IHD, int KPMAX, class KR, class GR>
+__device__ __forceinline__ uint4 pool_lane(KR kr, GR gr, int KP, const float* __restrict__ ape,
                                            const uint16_t* __restrict__ ln_w,
                                            const uint16_t* __restrict__ ln_b, float eps, int c0) {
     constexpr int LPP = IHD / 8;
-    float lw[8], lb[8];
+    constexpr float kLog2e = 1.4426950408889634f;
+    auto pair = [](uint32_t u) { return make_float2(bf16_lo(u), bf16_hi(u)); };
+    float2 lw[4], lb[4];
     {
         const uint4 w4 = ldg16(ln_w + c0);
         const uint4 b4 = ldg16(ln_b + c0);
@@ -67,113 +77,121 @@ __device__ __forceinline__ uint4 pool_lane(const uint4 (&kr)[KPMAX], const uint4
         const uint32_t bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            lw[2 * i] = bf16_lo(wv[i]);
-            lw[2 * i + 1] = bf16_hi(wv[i]);
-            lb[2 * i] = bf16_lo(bv[i]);
-            lb[2 * i + 1] = bf16_hi(bv[i]);
+            lw[i] = pair(wv[i]);
+            lb[i] = pair(bv[i]);
         }
     }
-
-    // Pass 1: the slot logits gate + ape (kept in registers when kpool <= 4) and
-    // their per-channel max.
-    constexpr int KC = KPMAX <= 4 ? KPMAX : 1;  // cached slots
-    float lg[KC][8];
-    float mx[8];
+    auto logits = [&](int s, float2 (&l)[4]) {  // gate + ape of slot s
+        const float4 ap0 = __ldg(reinterpret_cast<const float4*>(ape + s * IHD + c0));
+        const float4 ap1 = __ldg(reinterpret_cast<const float4*>(ape + s * IHD + c0 + 4));
+        const float2 ap[4] = {make_float2(ap0.x, ap0.y), make_float2(ap0.z, ap0.w),
+                              make_float2(ap1.x, ap1.y), make_float2(ap1.z, ap1.w)};
+        const uint4 g4 = gr(s);
+        const uint32_t gv[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+        for (int i = 0; i < 4; ++i) l[i] = __fadd2_rn(pair(gv[i]), ap[i]);
+    };
+
+    // Pass 1: the slot logits (kept in registers when kpool <= 4) and their
+    // per-channel max.
+    constexpr int KC = KPMAX <= 4 ? KPMAX : 1;  // cached slots
+    float2 lg[KC][4];
+    float2 mx[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mx[i] = make_float2(-INFINITY, -INFINITY);
 #pragma unroll
     for (int s = 0; s < KPMAX; ++s) {
         if (s < KP) {
-            const float4 ap0 = __ldg(reinterpret_cast<const float4*>(ape + s * IHD + c0));
-            const float4 ap1 = __ldg(reinterpret_cast<const float4*>(ape + s * IHD + c0 + 4));
-            const float ap[8] = {ap0.x, ap0.y, ap0.z, ap0.w, ap1.x, ap1.y, ap1.z, ap1.w};
-            const uint32_t gv[4] = {gr[s].x, gr[s].y, gr[s].z, gr[s].w};
+            float2 l[4];
+            logits(s, l);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float l0 = bf16_lo(gv[i]) + ap[2 * i];
-                const float l1 = bf16_hi(gv[i]) + ap[2 * i + 1];
-                if (s < KC) {
-                    lg[s < KC ? s : 0][2 * i] = l0;
-                    lg[s < KC ? s : 0][2 * i + 1] = l1;
-                }
-                mx[2 * i] = fmaxf(mx[2 * i], l0);
-                mx[2 * i + 1] = fmaxf(mx[2 * i + 1], l1);
+                if (s < KC) lg[s < KC ? s : 0][i] = l[i];
+                mx[i] = make_float2(fmaxf(mx[i].x, l[i].x), fmaxf(mx[i].y, l[i].y));
             }
         }
     }
     // softmax weights as 2^(l*log2e - max*log2e)
-    constexpr float kLog2e = 1.4426950408889634f;
-    float mxs[8];
+    const float2 log2e2 = make_float2(kLog2e, kLog2e);
+    float2 nmxs[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) mxs[i] = mx[i] * kLog2e;
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __fmul2_rn(mx[i], log2e2);
+        nmxs[i] = make_float2(-t.x, -t.y);
+    }
 
     // Pass 2: LayerNorm each slot, round to bf16, accumulate the softmax-weighted sum.
-    float num[8], den[8];
+    float2 num[4], den[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) num[i] = den[i] = 0.f;
+    for (int i = 0; i < 4; ++i) num[i] = den[i] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int s = 0; s < KPMAX; ++s) {
         if (s < KP) {  // KP is warp-uniform: the shuffles below see the whole warp
-            const uint32_t kv[4] = {kr[s].x, kr[s].y, kr[s].z, kr[s].w};
-            float x[8];
+            const uint4 k4 = kr(s);
+            const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
+            float2 x[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                x[2 * i] = bf16_lo(kv[i]);
-                x[2 * i + 1] = bf16_hi(kv[i]);
-            }
-            float sum = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) sum += x[i];
+            for (int i = 0; i < 4; ++i) x[i] = pair(kv[i]);
+            float2 s2 = __fadd2_rn(__fadd2_rn(x[0], x[1]), __fadd2_rn(x[2], x[3]));
+            float sum = s2.x + s2.y;
 #pragma unroll
             for (int off = LPP / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            const float mean = sum * (1.0f / IHD);
-            float sq = 0.f;
+            const float nm = -sum * (1.0f / IHD);
+            const float2 nm2 = make_float2(nm, nm);
+            float2 q2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                x[i] -= mean;
-                sq = fmaf(x[i], x[i], sq);
+            for (int i = 0; i < 4; ++i) {
+                x[i] = __fadd2_rn(x[i], nm2);
+                q2 = __ffma2_rn(x[i], x[i], q2);
             }
+            float sq = q2.x + q2.y;
 #pragma unroll
             for (int off = LPP / 2; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
             const float rstd = rsqrtf(fmaf(sq, 1.0f / IHD, eps));
+            const float2 r2 = make_float2(rstd, rstd);
 
-            float l[8];
+            float2 l[4];
             if (s < KC) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) l[i] = lg[s < KC ? s : 0][i];
+                for (int i = 0; i < 4; ++i) l[i] = lg[s < KC ? s : 0][i];
             } else {
-                const float4 ap0 = __ldg(reinterpret_cast<const float4*>(ape + s * IHD + c0));
-                const float4 ap1 =
-                    __ldg(reinterpret_cast<const float4*>(ape + s * IHD + c0 + 4));
-                const float ap[8] = {ap0.x, ap0.y, ap0.z, ap0.w, ap1.x, ap1.y, ap1.z, ap1.w};
-                const uint32_t gv[4] = {gr[s].x, gr[s].y, gr[s].z, gr[s].w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    l[2 * i] = bf16_lo(gv[i]) + ap[2 * i];
-                    l[2 * i + 1] = bf16_hi(gv[i]) + ap[2 * i + 1];
-                }
+                logits(s, l);
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float kn = round_bf16(fmaf(x[i] * rstd, lw[i], lb[i]));
-                const float e = exp2f(fmaf(l[i], kLog2e, -mxs[i]));
-                den[i] += e;
-                num[i] = fmaf(e, kn, num[i]);
+            for (int i = 0; i < 4; ++i) {
+                const float2 kn2 = __ffma2_rn(__fmul2_rn(x[i], r2), lw[i], lb[i]);
+                const uint32_t kb = pack_bf16x2(kn2.x, kn2.y);  // the bf16 storage point
+                const float2 kn = pair(kb);
+                const float2 a = __ffma2_rn(l[i], log2e2, nmxs[i]);
+                const float2 e = make_float2(ex2(a.x), ex2(a.y));
+                den[i] = __fadd2_rn(den[i], e);
+                num[i] = __ffma2_rn(e, kn, num[i]);
             }
         }
     }
 
     uint4 o;
-    o.x = pack_bf16x2(__fdividef(num[0], den[0]), __fdividef(num[1], den[1]));
-    o.y = pack_bf16x2(__fdividef(num[2], den[2]), __fdividef(num[3], den[3]));
-    o.z = pack_bf16x2(__fdividef(num[4], den[4]), __fdividef(num[5], den[5]));
-    o.w = pack_bf16x2(__fdividef(num[6], den[6]), __fdividef(num[7], den[7]));
+    o.x = pack_bf16x2(__fdividef(num[0].x, den[0].x), __fdividef(num[0].y, den[0].y));
+    o.y = pack_bf16x2(__fdividef(num[1].x, den[1].x), __fdividef(num[1].y, den[1].y));
+    o.z = pack_bf16x2(__fdividef(num[2].x, den[2].x), __fdividef(num[2].y, den[2].y));
+    o.w = pack_bf16x2(__fdividef(num[3].x, den[3].x), __fdividef(num[3].y, den[3].y));
     return o;
 }
 
 template <int IHD, int KPMAX>
+__device__ __forceinline__ void compress_unit(const CompressArgs& a, int b, int tile);
+
+template <int IHD, int KPMAX>
 __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
     pdl_wait();
+    // A persistent grid: CTA units (sequence b, PPC consecutive pools) are taken in
+    // turn, so the per-CTA start-up is paid once per CTA, not once per 16 pools.
+    for (long long u = blockIdx.x; u < (long long)a.tiles * a.pg.batch; u += gridDim.x)
+        compress_unit<IHD, KPMAX>(a, (int)(u / a.tiles), (int)(u % a.tiles));
+}
+
+template <int IHD, int KPMAX>
+__device__ __forceinline__ void compress_unit(const CompressArgs& a, int b, int tile) {
     constexpr int LPP = IHD / 8;     // lanes per pool
     constexpr int PPW = 32 / LPP;    // pools per warp
     constexpr int PPC = PPW * (kThreads / 32);
@@ -181,14 +199,13 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
     const int warp = threadIdx.x >> 5;
     const int sub = lane % LPP;
     const int c0 = sub * 8;
-    const int b = blockIdx.y;
     const int KP = a.kpool;
 
     int L = __ldg(a.pg.seq_lens + b);
     L = min(L, seq_capacity(a.pg));
     const int P = whole_pools(L, a.first_key, KP);
     const int p0 = a.append > 0 ? whole_pools(max(L - a.append, 0), a.first_key, KP) : 0;
-    const int p = p0 + blockIdx.x * PPC + warp * PPW + lane / LPP;
+    const int p = p0 + tile * PPC + warp * PPW + lane / LPP;
     bool active = p < P;
     const int t0 = a.first_key + p * KP;
     long long trow = -1, orow = -1;
@@ -215,7 +232,9 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
         }
     }
 
-    const uint4 pooled = pool_lane<IHD, KPMAX>(kr, gr, KP, a.ape, a.ln_w, a.ln_b, a.eps, c0);
+    const uint4 pooled = pool_lane<IHD, KPMAX>([&](int q) { return kr[q]; },
+                                               [&](int q) { return gr[q]; }, KP, a.ape, a.ln_w,
+                                               a.ln_b, a.eps, c0);
     if (!active) return;
     const bool pv = ok;
     *reinterpret_cast<uint4*>(a.kout + orow * IHD + c0) = pv ? pooled : make_uint4(0, 0, 0, 0);
@@ -309,7 +328,9 @@ __global__ void __launch_bounds__(kAppendThreads) decode_append_kernel(AppendArg
             ok = ok && (a.valid[r] != 0);
         }
     }
-    const uint4 pooled = pool_lane<IHD, KPMAX>(kr, gr, KP, a.ape, a.ln_w, a.ln_b, a.eps, c0);
+    const uint4 pooled = pool_lane<IHD, KPMAX>([&](int q) { return kr[q]; },
+                                               [&](int q) { return gr[q]; }, KP, a.ape, a.ln_w,
+                                               a.ln_b, a.eps, c0);
     if (!active) return;
     *reinterpret_cast<uint4*>(a.kout + orow * IHD + c0) = ok ? pooled : make_uint4(0, 0, 0, 0);
     if (lane == 0) {
@@ -320,13 +341,15 @@ __global__ void __launch_bounds__(kAppendThreads) decode_append_kernel(AppendArg
 }
 
 template <int IHD, int KPMAX>
-int launch(const CompressArgs& a, int pmax, cudaStream_t st) {
+int launch(CompressArgs a, int pmax, cudaStream_t st) {
     constexpr int PPC = (32 / (IHD / 8)) * (kThreads / 32);
-    dim3 grid((pmax + PPC - 1) / PPC, a.pg.batch);
-    if (grid.x == 0) return DSA_OK;
-    if (grid.x > 0x7fffffffu || grid.y > 65535u)
-        return fail(DSA_ERR_UNSUPPORTED, "dsa_compress: grid too large");
-    cudaError_t le = launch_pdl(compress_kernel<IHD, KPMAX>, dim3(grid), dim3(kThreads), 0, st, a);
+    a.tiles = (pmax + PPC - 1) / PPC;
+    const long long units = (long long)a.tiles * a.pg.batch;
+    if (units == 0) return DSA_OK;
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    const long long grid = units < 2LL * sms ? units : 2LL * sms;  // two CTAs fit per SM
+    cudaError_t le = launch_pdl(compress_kernel<IHD, KPMAX>, dim3((unsigned)grid), dim3(kThreads),
+                                0, st, a);
     if (le != cudaSuccess) return cuda_fail(le, "dsa_compress launch");
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_compress launch");

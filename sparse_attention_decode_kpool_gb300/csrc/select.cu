@@ -308,7 +308,12 @@ __device__ __forceinline__ void emit_one(const EmitTo& e, const uint32_t* keys, 
     e.out[at] = p;
     if (e.tok) {
         const int t0 = e.first_key + p * e.kpool;
-        for (int s = 0; s < e.kpool; ++s) e.tok[at * e.kpool + s] = t0 + s;
+        int32_t* dst = e.tok + at * e.kpool;
+        if (e.kpool == 4 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0u) {
+            *reinterpret_cast<int4*>(dst) = make_int4(t0, t0 + 1, t0 + 2, t0 + 3);
+        } else {
+            for (int s = 0; s < e.kpool; ++s) dst[s] = t0 + s;
+        }
     }
 }
 
