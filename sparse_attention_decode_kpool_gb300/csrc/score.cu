@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kWarps * 32) score_kernel(ScoreArgs a) {
 // CTA per SM. Pool flags are read by the consumers while the keys are in flight.
 
 constexpr int kStagePools = 64;
-constexpr int kStages = 4;
+constexpr int kStages = 3;  // deeper rings measured slower (less L1 beside them)
 constexpr int kCtasPerSm = 3;  // 12 consumer warps per SM hide the MMA and shuffle latency
 constexpr int kTmaThreads = 5 * 32;
 
