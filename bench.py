@@ -50,7 +50,7 @@ PREFILL_WORKLOAD = 4  # scored on the tensor cores; the o_absorb GEMM is not in 
 # projection reads all of o_absorb whatever the context length, so its capture at
 # S=32,768 holds for the 262,144-token workload.
 MEASURED_TRAFFIC = {
-    "project": (269.678848e6 + 3.427072e6 + 0.732672e6,
+    "project": (269.730816e6 + 3.598336e6 + 0.733184e6,
                 "project_decode_S32768_b8.md (project_kernel + project_reduce_rows_kernel)"),
 }
 FLUSH_BYTES = 256 << 20
