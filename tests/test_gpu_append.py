@@ -270,3 +270,27 @@ def test_decode_append_full_cache_matches_separate_calls():
     assert b[2] == a[2]
     for x, y in zip(a[:2] + a[3:], b[:2] + b[3:]):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "three-call"])
+def test_append_bad_block_entry_sets_status(fused):
+    """A block-table entry outside [0, num_blocks) at the append position: the token is
+    not stored, the length stays, DSA_STATUS_BAD_BLOCK is set; other sequences append."""
+    g = W.Geometry(index_kpool=4, index_heads=4, index_head_dim=128, index_topk=64, heads=2,
+                   hidden=64)
+    wl = W.make_workload("append-badblock", 9, g, [300, 200], block_size=64, max_seq_len=320)
+    lay = DsaDecodeLayer(wl, decode_from=[290, 190], fuse_append=fused)
+    lay.compress()
+    lay.stage(0)
+    blk = 290 // 64
+    lay.block_table[0, blk] = -1
+    k0 = lay.k_raw.clone()
+    lay.status.zero_()
+    lay.append()
+    torch.cuda.synchronize()
+    assert int(lay.status.item()) & 2
+    assert lay.seq_lens.tolist() == [290, 191]
+    row = int(lay._token_rows(1, 190, 191)[0])
+    changed = (lay.k_raw.view(-1, 128) != k0.view(-1, 128)).any(dim=1).nonzero().flatten()
+    assert set(changed.tolist()) <= {row}
+    assert torch.equal(lay.k_raw.view(-1, 128)[row], lay.k_new[1])
