@@ -537,10 +537,6 @@ def main():
     # e2e: per-step query inputs from pinned host memory, result read back.
     e2e = None
     if not args.no_e2e:
-        h_qidx = wl.qidx.pin_memory()
-        h_w = wl.w.pin_memory()
-        h_qlat = wl.qlat.pin_memory()
-        h_ctx = torch.from_numpy(wl.row_ctx).pin_memory()
         result = layer.olat if prefill else layer.y
         h_y = torch.empty_like(result, device="cpu").pin_memory()
         # The step's inputs: query tensors and the row contexts; with --decode-append
@@ -550,25 +546,31 @@ def main():
         # rows (the front-end makes both on the device).
         if fe is not None:
             ins = [(layer.x, fe.x.pin_memory())]
-        else:
-            ins = [(layer.qidx, h_qidx), (layer.w, h_w), (layer.qlat, h_qlat)]
+        else:  # qidx, w, qlat and row_ctx share one buffer: one transfer
+            ins = [(layer.step_inputs, layer.host_step_inputs())]
         if append and fe is None:
             ins += [(d, h.pin_memory()) for d, h in zip((layer.k_new, layer.gate_new,
                                                         layer.ckv_new), layer.staged_rows(0))]
-        elif not append:
-            ins.append((layer.row_ctx, h_ctx))
         h2d = sum(h.numel() * h.element_size() for _, h in ins)
         d2h = h_y.numel() * h_y.element_size()
         # One graph per step: the pinned-host copies in, the step's library calls,
-        # the result's copy out; the host waits for it and reads the clock.
+        # the result out; the host waits for it and reads the clock. The projection
+        # stores y straight into pinned host memory (unified addressing), so the
+        # result needs no copy node.
         step_fn = (layer.layer_step if fe is not None else
                    layer.append_step if append else layer.step)
+        direct_out = not prefill and layer.two_call
         io_graph = torch.cuda.CUDAGraph()
+        y_dev = layer.y
+        if direct_out:
+            layer.y = h_y
         with torch.cuda.graph(io_graph):
             for d, h in ins:
                 d.copy_(h, non_blocking=True)
             step_fn()
-            h_y.copy_(result, non_blocking=True)
+            if not direct_out:
+                h_y.copy_(result, non_blocking=True)
+        layer.y = y_dev
         for _ in range(3):
             io_graph.replay()
         torch.cuda.synchronize()
@@ -583,12 +585,13 @@ def main():
         e2e_ms = max_over_ranks(1e3 * sum(t_e2e) / len(t_e2e), ws)
         e2e = {"value": queries / (e2e_ms * 1e-3), "unit": "queries/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "path": "pinned host " + ("x (hidden state)" if fe is not None else "qidx/w/qlat")
-                       + ("" if append and fe is not None else
-                          "/staged token rows" if append else "/row_ctx")
+               "path": "pinned host " + ("x (hidden state)" if fe is not None else
+                                         "qidx/w/qlat/row_ctx (one buffer)")
+                       + ("/staged token rows" if append and fe is None else "")
                        + " -> device, the step, " + ("olat" if prefill else "y")
-                       + " -> host, as one CUDA graph replayed per step, host-timed to "
-                         "completion"}
+                       + (" stored by the projection straight into pinned host memory"
+                          if direct_out else " -> host")
+                       + ", as one CUDA graph replayed per step, host-timed to completion"}
 
     if rank != 0:
         return

@@ -465,6 +465,8 @@ int dsa_frontend(const dsa_bf16* x, int rows, int hidden, const dsa_bf16* w_x, i
  * Ordering: the kernel may start reading o_absorb (weights) before the kernel just
  * before it on the stream has finished (programmatic dependent launch), so that
  * kernel must not write o_absorb; olat is read only after it has finished.
+ * y may be pinned host memory (under unified addressing its address is valid on
+ * the device): the final sums are then stored straight into it, with no copy.
  */
 int dsa_latent_project_workspace(int rows, int heads, int kv_lora_rank, int hidden,
                                  size_t* bytes);

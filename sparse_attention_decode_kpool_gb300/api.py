@@ -23,11 +23,15 @@ __all__ = ["paging", "dsa_compress", "dsa_compress_append", "dsa_indexer_store",
            "dsa_validate_config", "DsaPaging"]
 
 
-def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "tensor") -> Optional[int]:
+def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "tensor",
+         host_ok: bool = False) -> Optional[int]:
+    """Device address of t. With host_ok, pinned host memory is accepted too: under
+    unified addressing its address is valid in kernels, which then read or write it
+    directly (no copy)."""
     if t is None:
         return None
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or pinned host memory" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -374,7 +378,7 @@ def dsa_latent_project(olat, o_absorb, y, status=None, workspace=None, stream=No
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     check(_lib.load().dsa_latent_project(
         _ptr(olat, torch.float32, "olat"), rows, heads, kvl, _ptr(o_absorb, torch.bfloat16, "o_absorb"),
-        hidden, _ptr(y, torch.bfloat16, "y"), _ptr(status, torch.int32, "status"),
+        hidden, _ptr(y, torch.bfloat16, "y", host_ok=True), _ptr(status, torch.int32, "status"),
         _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)))
 
 

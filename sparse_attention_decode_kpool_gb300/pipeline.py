@@ -34,7 +34,15 @@ class DsaDecodeLayer:
         self.pg = api.paging(self.seq_lens, wl.max_seq_len, self.block_table,
                              wl.block_size or 0, wl.num_blocks)
         self.row_seq = torch.from_numpy(wl.row_seq).to(dev)
-        self.row_ctx = torch.from_numpy(wl.row_ctx).to(dev)
+        # The per-step query inputs (qidx, w, qlat, row_ctx) are views of one device
+        # buffer, so that a host copy of the step's inputs is a single transfer.
+        R0, g0 = wl.rows, wl.geom
+        self._in_specs = [("qidx", (R0, g0.index_heads, g0.index_head_dim), torch.bfloat16),
+                          ("w", (R0, g0.index_heads), torch.float32),
+                          ("qlat", (R0, g0.heads, g0.kv_lora_rank), torch.bfloat16),
+                          ("row_ctx", (R0,), torch.int32)]
+        self.step_inputs = self._carve(dev, pinned=False)
+        self.row_ctx.copy_(torch.from_numpy(wl.row_ctx))
 
         # Resident state.
         self.ckv = up(wl.ckv)
@@ -68,9 +76,9 @@ class DsaDecodeLayer:
         self.ape, self.ln_w, self.ln_b = up(wl.ape), up(wl.ln_w), up(wl.ln_b)
 
         # Per-step inputs (device copies) and buffers.
-        self.qidx = up(wl.qidx)
-        self.w = up(wl.w)
-        self.qlat = up(wl.qlat)
+        self.qidx.copy_(wl.qidx)
+        self.w.copy_(wl.w)
+        self.qlat.copy_(wl.qlat)
         R = wl.rows
         self.p_stride = wl.p_stride
         self.sk = api.dsa_select_k(g.index_topk, KP, self.p_stride)
@@ -151,6 +159,33 @@ class DsaDecodeLayer:
         if self.decode_from is not None:
             self.append(stream)
         self.step(stream)
+
+    def _carve(self, device, pinned: bool, names: bool = True) -> torch.Tensor:
+        """One byte buffer holding the step inputs at 256-byte aligned offsets; on the
+        device the layer's qidx, w, qlat and row_ctx become views of it."""
+        offs, off = [], 0
+        for _, shape, dt in self._in_specs:
+            n = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+            offs.append((off, n))
+            off = (off + n + 255) & ~255
+        buf = (torch.empty(off, dtype=torch.uint8).pin_memory() if pinned
+               else torch.empty(off, dtype=torch.uint8, device=device))
+        self._in_offs = offs
+        if names:
+            for (name, shape, dt), (o, n) in zip(self._in_specs, offs):
+                setattr(self, name, buf[o:o + n].view(dt).view(shape))
+        return buf
+
+    def host_step_inputs(self) -> torch.Tensor:
+        """A pinned host buffer with the device step-input layout, filled with the
+        workload's inputs: one copy_ into step_inputs uploads a step's queries."""
+        buf = self._carve(None, pinned=True, names=False)
+        wl = self.wl
+        src = {"qidx": wl.qidx, "w": wl.w, "qlat": wl.qlat,
+               "row_ctx": torch.from_numpy(wl.row_ctx)}
+        for (name, shape, dt), (o, n) in zip(self._in_specs, self._in_offs):
+            buf[o:o + n].view(dt).view(shape).copy_(src[name])
+        return buf
 
     # -- decode-time append -------------------------------------------------
     def _token_rows(self, b: int, t0: int, t1: int) -> np.ndarray:
