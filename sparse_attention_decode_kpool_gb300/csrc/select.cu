@@ -22,6 +22,8 @@
 // slices' top-k, and slot order keeps the ids ascending.
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace cg = cooperative_groups;
@@ -406,18 +408,35 @@ __device__ __noinline__ int block_topk(const uint32_t* keys, int n, int k, MinMa
     return t.kk;
 }
 
+__device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_group& cluster,
+                                           int r, uint32_t* keys, BlockScratch& sc);
+
+// ROWS: single-CTA rows (C == 1) taken in turn by a grid of at most one CTA per SM,
+// so the start-up of a CTA is paid once per SM rather than once per row. Otherwise
+// one row per CTA or cluster.
+template <bool ROWS>
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
     cg::cluster_group cluster = cg::this_cluster();
     const int C = (int)cluster.num_blocks();
-    const int crank = (int)cluster.block_rank();
-    const int r = blockIdx.x / C;
-
     extern __shared__ __align__(16) uint32_t keys[];
     __shared__ BlockScratch sc;
+    pdl_wait();
+    if (!ROWS) {
+        select_row(a, cluster, (int)blockIdx.x / C, keys, sc);
+        return;
+    }
+    for (int r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        select_row(a, cluster, r, keys, sc);
+        __syncthreads();  // the next row reuses keys[] and the scratch
+    }
+}
+
+__device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_group& cluster,
+                                           int r, uint32_t* keys, BlockScratch& sc) {
+    const int C = (int)cluster.num_blocks();
+    const int crank = (int)cluster.block_rank();
     uint8_t* dyn = reinterpret_cast<uint8_t*>(keys);
     uint32_t* tbuf = reinterpret_cast<uint32_t*>(dyn + a.tbuf_off);
-
-    pdl_wait();
     const int begin = crank * a.chunk;
     const int n = max(0, min(a.chunk, a.p_stride - begin));
     const float* srow = a.scores + (long long)r * a.p_stride + begin;
@@ -576,11 +595,14 @@ int select_launch(const float* scores, int rows, int p_stride, int sk, int32_t* 
     a.ow = ow;
     a.row_ctx = row_ctx;
     a.tail_at = row_ctx ? tail_at : ow;
-    int rc = set_max_smem((const void*)select_kernel, kMaxSmem);
+    const bool by_rows = C == 1 && rows > sms;
+    auto kernel = by_rows ? select_kernel<true> : select_kernel<false>;
+    int rc = set_max_smem((const void*)kernel, kMaxSmem);
     if (rc) return rc;
     if ((long long)rows * C > 0x7fffffffLL) return fail(DSA_ERR_UNSUPPORTED, "dsa_select: too many rows");
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(rows * C));
+    // single-CTA rows: a grid of at most one CTA per SM walks the rows
+    cfg.gridDim = dim3((unsigned)(by_rows ? sms : rows * C));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = (size_t)sp.bytes;
     cfg.stream = (cudaStream_t)stream;
@@ -593,7 +615,7 @@ int select_launch(const float* scores, int rows, int p_stride, int sk, int32_t* 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, select_kernel, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a);
     if (e != cudaSuccess) return cuda_fail(e, "dsa_select launch");
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_select launch");
