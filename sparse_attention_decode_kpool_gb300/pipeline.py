@@ -91,12 +91,12 @@ class DsaDecodeLayer:
         self.olat = (torch.empty((R, g.heads, g.kv_lora_rank), dtype=torch.float32, device=dev)
                      if (keep_olat or self.o_absorb is not None) else None)
         ws = api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, 0, False)
-        self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+        self.workspace = torch.zeros(max(ws, 1), dtype=torch.uint8, device=dev)
         # Two-call form (attention, then dsa_latent_project) where the projection
         # kernel supports the shape (hidden % 64 == 0); else the one-call form.
         self.two_call = bool(hidden) and hidden % 64 == 0
         pws = api.dsa_latent_project_workspace(R, g.heads, hidden) if self.two_call else 0
-        self.proj_workspace = torch.empty(max(pws, 1), dtype=torch.uint8, device=dev)
+        self.proj_workspace = torch.zeros(max(pws, 1), dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         # Scoring: a chunk of >= 64 query rows of one contiguous sequence goes to the
         # tensor-core contraction (dsa_score_prefill); everything else to dsa_score.
@@ -143,7 +143,7 @@ class DsaDecodeLayer:
             self.ckv_new = torch.zeros((R, g.kv_lora_rank), dtype=torch.bfloat16, device=dev)
         n = api.dsa_frontend_workspace(R, g.hidden, int(self.w_x.shape[0]), fe.q_lora_rank,
                                        g.kv_lora_rank, g.index_head_dim, g.index_heads, g.heads)
-        self.fe_workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        self.fe_workspace = torch.zeros(max(n, 1), dtype=torch.uint8, device=dev)
 
     def frontend(self, stream=None) -> None:
         """x -> qlat, qidx, w (the step's inputs) and k_new, gate_new, ckv_new (the
@@ -296,7 +296,7 @@ class DsaDecodeLayer:
             hidden = g.hidden if self.o_absorb is not None else 0
             n = api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, hidden,
                                                     self.o_absorb is not None)
-            self._fused_ws = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
+            self._fused_ws = torch.zeros(max(n, 1), dtype=torch.uint8, device=self.device)
         return self._fused_ws
 
     # -- stages ------------------------------------------------------------

@@ -472,7 +472,7 @@ def test_latent_project_parity(rows, heads, hidden):
     olat = torch.from_numpy(rng.standard_normal((rows, heads, 512)).astype(np.float32))
     A = torch.from_numpy((rng.standard_normal((hidden, heads * 512)) * 0.02).astype(np.float32)
                          ).to(torch.bfloat16)
-    ws = torch.empty(max(1, api.dsa_latent_project_workspace(rows, heads, hidden)),
+    ws = torch.zeros(max(1, api.dsa_latent_project_workspace(rows, heads, hidden)),
                      dtype=torch.uint8, device="cuda")
     y = H.Guarded((rows, hidden), torch.bfloat16, 5.0)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
