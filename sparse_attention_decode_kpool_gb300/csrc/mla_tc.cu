@@ -1,5 +1,6 @@
 // Sparse latent attention on the tensor cores (tcgen05) for 64 heads: the split
-// kernel of dsa_sparse_mla_decode when heads == 64.
+// kernel of dsa_sparse_mla_decode when heads == 64 and the batch holds enough
+// 128-token chunks to keep a persistent grid busy (prefill chunks).
 //
 // Page: metrale_model_arch/glm5next_dsa/mod.rs, "Shape of the pipeline" (last stage)
 // and build.rs module doc, transforms 1 and 3 (absorbed Q; each latent row is both
@@ -7,23 +8,29 @@
 //   s[t,h] = softmax_scale * <ckv[t,:], qlat[r,h,:]>;  O[h,:] = sum_t p[t,h] ckv[t,:]
 // with p = 2^(s*log2e - m_h) against a running per-head maximum m_h.
 //
-// A CTA takes one (split, row) and walks its tokens in chunks of 128:
-//   - warp 0 resolves the chunk's token rows, and it and the four softmax warps
-//     gather the 128 latent rows with cp.async (512 contiguous bytes per warp
-//     instruction) into eight 128-byte-swizzled atoms of 64 latent columns
-//     ([atom][token][64 c]); the row's Q (64 heads x 512) is loaded once by TMA;
-//   - warp 1 owns the tensor memory and issues the MMAs:
-//       S^T = K Q^T   M = 128 tokens, N = 64 heads, K = 512 (the atoms are K-major);
-//       O^T += V^T P^T  M = 512 latent (4 tiles of 128), N = 64 heads, K = 128 tokens,
-//     where the same atoms are read MN-major for V^T and P^T is written by the
-//     softmax warps as [token][64 heads] (MN-major);
-//   - warps 2..5 (one tensor-memory lane per token) take S^T, find each head's chunk
-//     maximum (warp max, then across the four warps through shared memory), update
-//     the running maximum only when it grows by more than 2^8 (then O^T and the
-//     partial sums are rescaled), write P^T in bf16, keep per-thread partial sums,
-//     and at the end write the split's partial (or, with one split, olat).
+// The grid is persistent: CTA b takes the (row, split) units b, b + G, b + 2G, ...
+// and walks each unit's tokens in chunks of 128. Shared memory holds the unit's Q
+// (64 heads x 512, 64 KB), one 128-token latent tile (128 KB) and P^T (16 KB); there
+// is no room for a second tile, so the tile is refilled a quarter (two 64-column
+// atoms, the rows of one O^T tile) at a time, as soon as the MMAs of the previous
+// chunk are done with that quarter. Roles (eight warps):
+//   - warp 0 resolves each chunk's token ids to cache rows, two chunks ahead, into a
+//     double buffer, and loads each unit's Q by TMA once the last unit's QK is done;
+//   - warps 6-7 gather: per quarter, 128 tokens x 256 bytes with cp.async into the
+//     128-byte-swizzled atoms, each thread's copies completing on the quarter's
+//     mbarrier (cp.async.mbarrier.arrive.noinc), so the warps run ahead freely;
+//   - warp 1 (one lane) issues the MMAs, accumulators in tensor memory:
+//       S^T = K Q^T   M = 128 tokens, N = 64 heads, K = 512, quarter by quarter;
+//       O^T += V^T P^T  M = 512 latent (four tiles of 128, tile i = quarter i read
+//       MN-major), N = 64 heads, K = 128 tokens; each tile's completion frees its
+//       quarter for the next chunk's gather;
+//   - warps 2-5 (one tensor-memory lane, i.e. one token, per thread) take S^T, find
+//     each head's chunk maximum (redux.sync, then across the four warps through
+//     shared memory), move the running maximum only when it grows by more than 2^8
+//     (then O^T and the partial sums are rescaled), write P^T in bf16, and at the end
+//     of a unit write its partial (or, with one split, olat) and free O^T.
 // All waits are bounded; a timeout sets DSA_STATUS_TIMEOUT, every role leaves its
-// loop, copies and MMAs in flight are drained, and the tensor memory is released.
+// loops, copies and MMAs in flight are drained, and the tensor memory is released.
 #include <stdlib.h>
 
 #include "common.cuh"
@@ -36,191 +43,296 @@ constexpr int kT = 128;                        // tokens per chunk
 constexpr int kH = 64;                         // heads
 constexpr int kKVL = 512;                      // latent width
 constexpr int kAtoms = kKVL / 64;              // 128-byte atoms per latent row
+constexpr int kQuarters = 4;                   // two atoms each
 constexpr uint32_t kLatAtom = kT * 128;        // one atom of the token tile
 constexpr uint32_t kQAtom = kH * 128;          // one atom of the Q tile
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffLat = kOffQ + kAtoms * kQAtom;
 constexpr uint32_t kOffP = kOffLat + kAtoms * kLatAtom;
-constexpr uint32_t kOffRed = kOffP + kT * 128;          // [2][4 warps][kH] f32
-constexpr uint32_t kOffM = kOffRed + 2 * 4 * kH * 4;    // [2][kH] running maxima
-constexpr uint32_t kOffRows = kOffM + 2 * kH * 4;       // [kT] cache row per token
-constexpr uint32_t kOffMask = kOffRows + kT * 4;        // [kT] token valid
-constexpr uint32_t kOffBar = kOffMask + kT;
-constexpr int kBars = 11;
+constexpr uint32_t kOffRed = kOffP + kT * 128;          // [2][4 warps][kH] f32 chunk maxima
+constexpr uint32_t kOffSums = kOffRed + 2 * 4 * kH * 4; // [4 warps][kH] f32 head sums
+constexpr uint32_t kOffM = kOffSums + 4 * kH * 4;       // [2][kH] running maxima
+constexpr uint32_t kOffRows = kOffM + 2 * kH * 4;       // [2][kT] cache row per token
+constexpr uint32_t kOffMask = kOffRows + 2 * kT * 4;    // [2][kT] token valid
+constexpr uint32_t kOffBar = kOffMask + 2 * kT;
+// mbarriers
+constexpr int Q_FULL = 0;         // Q landed (TMA bytes)
+constexpr int Q_EMPTY = 1;        // the unit's last QK is done with Q (commit)
+constexpr int ROWS_FULL = 2;      // [2] token rows of a chunk resolved (warp 0)
+constexpr int ROWS_EMPTY = 4;     // [2] rows and mask read (2 gather + 4 softmax warps)
+constexpr int LAT_FULL = 6;       // [4] a quarter gathered (64 gather threads' copies)
+constexpr int LAT_EMPTY = 10;     // [4] a quarter's PV tile done (commit)
+constexpr int S_FULL = 14;        // S^T of a chunk complete (commit)
+constexpr int P_FULL = 15;        // P^T written, S^T read (4 softmax warps)
+constexpr int O_DONE = 16;        // the unit's last PV done (commit)
+constexpr int O_FREE = 17;        // the unit's O^T read out (4 softmax warps)
+constexpr int RED = 18;           // [2] chunk maxima of all four warps in place
+constexpr int SUM_IN = 20;        // head sums of all four warps in place
+constexpr int SUM_OUT = 21;       // head sums read by all four warps
+constexpr int DRAIN = 22;         // every MMA issued has completed
+constexpr int kBars = 23;
 constexpr uint32_t kOffMisc = kOffBar + kBars * 8;
 constexpr uint32_t kBytes = kOffMisc + 16;
 constexpr uint32_t kDyn = kBytes + 1024;
 constexpr uint32_t kTmemCols = 512;  // S^T: columns [0, 64); O^T tile i: [64 + 64 i, +64)
-constexpr int kThreads = 192;
-constexpr int kGatherWarps = 5;  // warp 0 and the four softmax warps
-constexpr float kLazy = 8.f;     // log2 units the running max may lag behind
+constexpr int kThreads = 256;
+constexpr int kGatherThreads = 64;   // warps 6 and 7
+constexpr float kLazy = 8.f;         // log2 units the running max may lag behind
+static_assert(kDyn <= 227 * 1024, "tcgen05 attention shared memory");
+static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;\n" ::: "memory");
 }
+// Arrive on bar once every cp.async this thread issued so far has landed (the
+// arrival counts against the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar))
+                 : "memory");
+}
 
-// Rows j of the chunk with j % kGatherWarps == gw: two warp instructions of 512
-// contiguous bytes per token row, into the row's place in each 128-byte atom.
-__device__ __forceinline__ void gather_rows(uint8_t* sLat, const int* rows, const uint16_t* ckv,
-                                            int gw, int lane) {
-    const uint32_t lat = smem_u32(sLat);
-    for (int j = gw; j < kT; j += kGatherWarps) {
-        const long long row = rows[j];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int at = 4 * half + (lane >> 3), q = lane & 7;
-            const uint16_t* src = ckv + row * kKVL + at * 64 + q * 8;
-            const uint32_t dst = lat + at * kLatAtom + j * 128 + ((q ^ (j & 7)) << 4);
-            cp_async16(dst, src, 16);
-        }
+// Token range of a unit: split `split` of its row, in chunks of kT.
+struct Unit {
+    int r, split, t_begin, t_end, nch;
+};
+__device__ __forceinline__ Unit unit_of(const MlaTcParams& a, int u) {
+    Unit w;
+    w.r = u / a.ns;
+    w.split = u - w.r * a.ns;
+    w.t_begin = w.split * a.tps;
+    w.t_end = min(w.t_begin + a.tps, a.ow);
+    w.nch = w.t_end > w.t_begin ? (w.t_end - w.t_begin + kT - 1) / kT : 0;
+    return w;
+}
+
+// Quarter q of a chunk (atoms 2q, 2q+1: latent columns 128q .. 128q+127 of every
+// token): 2048 copies of 16 bytes, thread g of the 64 gather threads taking g, g+64,
+// ...; a warp's 32 copies are two tokens' 256 contiguous bytes.
+__device__ __forceinline__ void gather_quarter(uint32_t lat, const int* rows, const uint16_t* ckv,
+                                               int q, int g) {
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) {
+        const int idx = g + kGatherThreads * m;
+        const int j = idx >> 4, at = 2 * q + ((idx >> 3) & 1), c = idx & 7;
+        const uint16_t* src = ckv + (long long)rows[j] * kKVL + at * 64 + c * 8;
+        cp_async16(lat + at * kLatAtom + j * 128 + ((c ^ (j & 7)) << 4), src, 16);
     }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     mla_tc_kernel(const __grid_constant__ CUtensorMap tmQ, MlaTcParams a) {
-    pdl_wait();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sQ = smem + kOffQ;
     uint8_t* sLat = smem + kOffLat;
     uint8_t* sP = smem + kOffP;
     float* red = reinterpret_cast<float*>(smem + kOffRed);
-    int* rows = reinterpret_cast<int*>(smem + kOffRows);
+    float* sums = reinterpret_cast<float*>(smem + kOffSums);
     float* msm = reinterpret_cast<float*>(smem + kOffM);
+    int* rows = reinterpret_cast<int*>(smem + kOffRows);
     uint8_t* mask = smem + kOffMask;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    uint64_t* q_full = bars + 0;
-    uint64_t* lat_full = bars + 1;
-    uint64_t* lat_empty = bars + 2;
-    uint64_t* s_full = bars + 3;
-    uint64_t* p_full = bars + 4;
-    uint64_t* o_done = bars + 5;
-    uint64_t* red_bar = bars + 6;  // [2]
-    uint64_t* sum_bar = bars + 8;
-    uint64_t* drain = bars + 9;
-    uint64_t* rows_ready = bars + 10;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x, r = blockIdx.y;
-    int seq = a.row_seq ? __ldg(a.row_seq + r) : r;
-    int L = 0;
-    if (seq >= 0 && seq < a.pg.batch) {
-        L = min(__ldg(a.pg.seq_lens + seq), seq_capacity(a.pg));
-    } else {
-        if (threadIdx.x == 0 && split == 0) flag_status(a.status, DSA_STATUS_BAD_TOKEN);
-        seq = 0;
-    }
-    const int t_begin = split * a.tps;
-    const int t_end = min(t_begin + a.tps, a.ow);
-    const int nch = t_end > t_begin ? (t_end - t_begin + kT - 1) / kT : 0;
+    const int units = a.rows * a.ns;
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        mbar_init(lat_full, kGatherWarps);
-        mbar_init(lat_empty, 1);
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 4);
-        mbar_init(o_done, 1);
-        mbar_init(red_bar + 0, 4);
-        mbar_init(red_bar + 1, 4);
-        mbar_init(sum_bar, 4);
-        mbar_init(drain, 1);
-        mbar_init(rows_ready, 1);
+        mbar_init(bars + Q_FULL, 1);
+        mbar_init(bars + Q_EMPTY, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bars + ROWS_FULL + b, 1);
+            mbar_init(bars + ROWS_EMPTY + b, 6);
+            mbar_init(bars + RED + b, 4);
+        }
+        for (int q = 0; q < kQuarters; ++q) {
+            mbar_init(bars + LAT_FULL + q, kGatherThreads);
+            mbar_init(bars + LAT_EMPTY + q, 1);
+        }
+        mbar_init(bars + S_FULL, 1);
+        mbar_init(bars + P_FULL, 4);
+        mbar_init(bars + O_DONE, 1);
+        mbar_init(bars + O_FREE, 4);
+        mbar_init(bars + SUM_IN, 4);
+        mbar_init(bars + SUM_OUT, 4);
+        mbar_init(bars + DRAIN, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (threadIdx.x < kH) msm[threadIdx.x] = __int_as_float(0xff800000);
     if (warp == 1) tc_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // token ids, qlat and the caches come from the kernels before this one
+    pdl_wait();
+
     // one lane waits, the warp follows its verdict
-    auto bwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    auto bwait = [&](int bar, uint32_t parity) -> bool {
         int got = 1;
-        if (lane == 0) got = wait_or_abort(bar, parity, abort_flag, a.status);
+        if (lane == 0) got = wait_or_abort(bars + bar, parity, abort_flag, a.status);
         return __shfl_sync(0xffffffffu, got, 0) != 0;
-    };
-    // this warp's share of chunk c's gather, then its arrival on lat_full
-    auto gather_and_arrive = [&](int gw) {
-        gather_rows(sLat, rows, a.ckv, gw, lane);
-        cp_async_wait_all();
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(lat_full);
     };
 
     if (warp == 0) {
-        // ---- Q once (TMA), then per chunk: token rows, rows_ready, a share of the gather
-        if (lane == 0 && nch > 0) {
-            mbar_arrive_expect_tx(q_full, kAtoms * kQAtom);
-            for (int at = 0; at < kAtoms; ++at)
-                tma_load_2d(smem_u32(sQ + at * kQAtom), &tmQ, 64 * at, r * kH, q_full);
-        }
-        for (int c = 0; c < nch; ++c) {
-            if (!bwait(lat_empty, (uint32_t)(c & 1) ^ 1u)) break;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int j = 4 * lane + k;
-                const int pos = t_begin + c * kT + j;
-                long long prow = -1;
-                if (pos < t_end) {
-                    const int t = __ldg(a.token_ids + (long long)r * a.ow + pos);
-                    if (t >= 0) {
-                        if (t >= L) {
-                            flag_status(a.status, DSA_STATUS_BAD_TOKEN);
-                        } else {
-                            prow = token_row(a.pg, seq, t);
-                            if (prow < 0) flag_status(a.status, DSA_STATUS_BAD_BLOCK);
-                        }
-                    } else if (t < -1) {
-                        flag_status(a.status, DSA_STATUS_BAD_TOKEN);
-                    }
-                }
-                mask[j] = prow >= 0 ? 1 : 0;
-                rows[j] = prow >= 0 ? (int)prow : 0;  // a real row; masked in the softmax
+        // ---- token rows (two chunks ahead) and each unit's Q ----
+        int n = 0, k = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const Unit w = unit_of(a, u);
+            if (w.nch == 0) continue;
+            int seq = a.row_seq ? __ldg(a.row_seq + w.r) : w.r;
+            int L = 0;
+            if (seq >= 0 && seq < a.pg.batch) {
+                L = min(__ldg(a.pg.seq_lens + seq), seq_capacity(a.pg));
+            } else {
+                if (lane == 0 && w.split == 0) flag_status(a.status, DSA_STATUS_BAD_TOKEN);
+                seq = 0;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(rows_ready);
-            gather_and_arrive(0);
+            for (int c = 0; c < w.nch; ++c, ++n) {
+                const int b = n & 1;
+                if (!bwait(ROWS_EMPTY + b, (uint32_t)((n >> 1) & 1) ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int j = 4 * lane + kk;
+                    const int pos = w.t_begin + c * kT + j;
+                    long long prow = -1;
+                    if (pos < w.t_end) {
+                        const int t = __ldg(a.token_ids + (long long)w.r * a.ow + pos);
+                        if (t >= 0) {
+                            if (t >= L) {
+                                flag_status(a.status, DSA_STATUS_BAD_TOKEN);
+                            } else {
+                                prow = token_row(a.pg, seq, t);
+                                if (prow < 0) flag_status(a.status, DSA_STATUS_BAD_BLOCK);
+                            }
+                        } else if (t < -1) {
+                            flag_status(a.status, DSA_STATUS_BAD_TOKEN);
+                        }
+                    }
+                    mask[b * kT + j] = prow >= 0 ? 1 : 0;
+                    rows[b * kT + j] = prow >= 0 ? (int)prow : 0;  // a real row; masked later
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars + ROWS_FULL + b);
+                if (c == 0) {
+                    // Q of this unit, once the last unit's QK is done with the buffer
+                    int got = 1;
+                    if (lane == 0) {
+                        got = k == 0 || wait_or_abort(bars + Q_EMPTY, (uint32_t)((k - 1) & 1),
+                                                      abort_flag, a.status);
+                        if (got) {
+                            mbar_arrive_expect_tx(bars + Q_FULL, kAtoms * kQAtom);
+                            for (int at = 0; at < kAtoms; ++at)
+                                tma_load_2d(smem_u32(sQ + at * kQAtom), &tmQ, 64 * at, w.r * kH,
+                                            bars + Q_FULL);
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, got, 0)) {
+                        ok = false;
+                        ++n;
+                        break;
+                    }
+                    ++k;
+                }
+            }
         }
-        if (lane == 0 && nch > 0) mbar_wait(q_full, 0);  // drain the Q copy
+        // drain: the last Q copy issued has landed before the CTA may exit
+        if (lane == 0 && k > 0) mbar_wait(bars + Q_FULL, (uint32_t)((k - 1) & 1));
+    } else if (warp >= 6) {
+        // ---- gather: quarters of each chunk as the previous chunk's PV frees them ----
+        const int g = threadIdx.x - 6 * 32;
+        const uint32_t lat = smem_u32(sLat);
+        int n = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const Unit w = unit_of(a, u);
+            for (int c = 0; c < w.nch; ++c, ++n) {
+                const int b = n & 1;
+                if (!bwait(ROWS_FULL + b, (uint32_t)((n >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                for (int q = 0; q < kQuarters && ok; ++q) {
+                    if (!bwait(LAT_EMPTY + q, (uint32_t)(n & 1) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    gather_quarter(lat, rows + b * kT, a.ckv, q, g);
+                    cp_async_arrive_noinc(bars + LAT_FULL + q);
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars + ROWS_EMPTY + b);
+            }
+        }
+        cp_async_wait_all();  // drain
     } else if (warp == 1) {
         // ---- MMA issuer ----
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16(kT, kH);
             constexpr uint32_t IDESC_PV = idesc_bf16(128, kH) | (1u << 15) | (1u << 16);
-            bool ok = nch == 0 || wait_or_abort(q_full, 0, abort_flag, a.status);
             const uint32_t q0 = smem_u32(sQ), l0 = smem_u32(sLat), p0 = smem_u32(sP);
-            for (int c = 0; c < nch && ok; ++c) {
-                if (!wait_or_abort(lat_full, (uint32_t)(c & 1), abort_flag, a.status)) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int at = 0; at < kAtoms; ++at)
+            int n = 0, k = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const Unit w = unit_of(a, u);
+                if (w.nch == 0) continue;
+                if (!wait_or_abort(bars + Q_FULL, (uint32_t)(k & 1), abort_flag, a.status)) break;
+                for (int c = 0; c < w.nch; ++c, ++n) {
+                    // S^T = K Q^T, quarter by quarter as the gather lands
+                    for (int q = 0; q < kQuarters && ok; ++q) {
+                        if (!wait_or_abort(bars + LAT_FULL + q, (uint32_t)(n & 1), abort_flag,
+                                           a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma(tmem, sw128_desc(l0 + at * kLatAtom + 32 * kk),
-                               sw128_desc(q0 + at * kQAtom + 32 * kk), IDESC_QK,
-                               (at | kk) != 0 ? 1u : 0u);
-                tc_commit(s_full);
-                if (!wait_or_abort(p_full, (uint32_t)(c & 1), abort_flag, a.status)) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int i = 0; i < 4; ++i)
+                        for (int h = 0; h < 2; ++h) {
+                            const int at = 2 * q + h;
 #pragma unroll
-                    for (int kk = 0; kk < kT / 16; ++kk)
-                        tc_mma(tmem + 64 + 64 * i,
-                               sw128_desc_mn(l0 + 2 * i * kLatAtom + kk * 2048, kLatAtom, 1024),
-                               sw128_desc_mn(p0 + kk * 2048, kQAtom, 1024), IDESC_PV,
-                               (c > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(lat_empty);
-                tc_commit(o_done);
+                            for (int kk = 0; kk < 4; ++kk)
+                                tc_mma(tmem, sw128_desc(l0 + at * kLatAtom + 32 * kk),
+                                       sw128_desc(q0 + at * kQAtom + 32 * kk), IDESC_QK,
+                                       (at | kk) != 0 ? 1u : 0u);
+                        }
+                    }
+                    if (!ok) break;
+                    if (c == w.nch - 1) tc_commit(bars + Q_EMPTY);
+                    tc_commit(bars + S_FULL);
+                    if (!wait_or_abort(bars + P_FULL, (uint32_t)(n & 1), abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (c == 0 && k > 0 &&
+                        !wait_or_abort(bars + O_FREE, (uint32_t)((k - 1) & 1), abort_flag,
+                                       a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // O^T += V^T P^T, tile by tile; each frees its quarter
+                    for (int i = 0; i < kQuarters; ++i) {
+#pragma unroll
+                        for (int kk = 0; kk < kT / 16; ++kk)
+                            tc_mma(tmem + 64 + 64 * i,
+                                   sw128_desc_mn(l0 + 2 * i * kLatAtom + kk * 2048, kLatAtom, 1024),
+                                   sw128_desc_mn(p0 + kk * 2048, kQAtom, 1024), IDESC_PV,
+                                   (c > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(bars + LAT_EMPTY + i);
+                    }
+                    if (c == w.nch - 1) tc_commit(bars + O_DONE);
+                }
+                ++k;
             }
             // Drain: every MMA issued has completed before tensor memory is released.
-            tc_commit(drain);
-            mbar_wait(drain, 0);
+            tc_commit(bars + DRAIN);
+            mbar_wait(bars + DRAIN, 0);
         }
     } else {
         // ---- softmax and epilogue: thread j owns token j of a chunk (tensor lane j) ----
@@ -228,209 +340,237 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = 32 * qd + lane;
         const uint32_t lrow = (uint32_t)(32 * qd) << 16;
         const float NEG_INF = __int_as_float(0xff800000);
-        // Running maxima (identical in every thread) live in msm[c & 1] during chunk c;
-        // the chunk's new ones go to msm[(c + 1) & 1].
-        float lacc[kH];
-#pragma unroll
-        for (int h = 0; h < kH; ++h) lacc[h] = 0.f;
+        int n = 0, k = 0;
         bool ok = true;
-        for (int c = 0; c < nch; ++c) {
-            // a share of this chunk's gather
-            if (!bwait(rows_ready, (uint32_t)(c & 1))) {
-                ok = false;
-                break;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const Unit w = unit_of(a, u);
+            const long long pbase = ((long long)w.r * a.ns + w.split) * kH;
+            if (w.nch == 0) {
+                // no tokens: zero output, (m, l) = (-inf, 0)
+                if (a.ns > 1 && j < kH)
+                    *reinterpret_cast<float2*>(a.part_ml + (pbase + j) * 2) = make_float2(NEG_INF, 0.f);
+                for (int h = 0; h < kH; ++h)
+                    for (int i = 0; i < kQuarters; ++i) {
+                        const int cidx = 128 * i + j;
+                        if (a.ns > 1) {
+                            a.part_o[(pbase + h) * kKVL + cidx] = 0.f;
+                        } else {
+                            const long long oi = ((long long)w.r * kH + h) * kKVL + cidx;
+                            if (a.olat) a.olat[oi] = 0.f;
+                            if (a.xbf) a.xbf[oi] = 0;
+                        }
+                    }
+                continue;
             }
-            gather_and_arrive(1 + (warp - 2));
-            if (!bwait(s_full, (uint32_t)(c & 1))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const bool valid = mask[j] != 0;
-            // chunk maximum per head: over the warp, then over the four warps
-            const int b = c & 1;
-            float* rb = red + b * 4 * kH;
-            {
-                uint32_t sv[2][32];
-                tc_ld32(sv[0], tmem + lrow);
-                tc_ld32(sv[1], tmem + lrow + 32);
-                tc_wait_ld(sv[0]);
-                tc_tie(sv[1]);
-                float4* dst = reinterpret_cast<float4*>(rb + qd * kH);
+            // Running maxima (identical in every thread) live in msm[n & 1] during
+            // chunk n; the chunk's new ones go to msm[(n + 1) & 1].
+            float lacc[kH];
 #pragma unroll
-                for (int i = 0; i < kH / 4; ++i) {
-                    float4 m4;
-                    m4.x = warp_max(valid ? __uint_as_float(sv[i >> 3][(4 * i) & 31]) * a.sl2 : NEG_INF);
-                    m4.y = warp_max(valid ? __uint_as_float(sv[i >> 3][(4 * i + 1) & 31]) * a.sl2
-                                          : NEG_INF);
-                    m4.z = warp_max(valid ? __uint_as_float(sv[i >> 3][(4 * i + 2) & 31]) * a.sl2
-                                          : NEG_INF);
-                    m4.w = warp_max(valid ? __uint_as_float(sv[i >> 3][(4 * i + 3) & 31]) * a.sl2
-                                          : NEG_INF);
-                    if (lane == 0) dst[i] = m4;
+            for (int h = 0; h < kH; ++h) lacc[h] = 0.f;
+            for (int c = 0; c < w.nch; ++c, ++n) {
+                const int b = n & 1;
+                if (!bwait(ROWS_FULL + b, (uint32_t)((n >> 1) & 1))) {
+                    ok = false;
+                    break;
                 }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(red_bar + b);
-            if (!bwait(red_bar + b, (uint32_t)((c >> 1) & 1))) {
-                ok = false;
-                break;
-            }
-            // new running maxima (lagging by at most kLazy) into cm
-            float cm[kH];
-            {
-                const float4* r4 = reinterpret_cast<const float4*>(rb);
-#pragma unroll
-                for (int i = 0; i < kH / 4; ++i) {
-                    const float4 w0 = r4[i], w1 = r4[kH / 4 + i], w2 = r4[2 * (kH / 4) + i],
-                                 w3 = r4[3 * (kH / 4) + i];
-                    cm[4 * i] = fmaxf(fmaxf(w0.x, w1.x), fmaxf(w2.x, w3.x));
-                    cm[4 * i + 1] = fmaxf(fmaxf(w0.y, w1.y), fmaxf(w2.y, w3.y));
-                    cm[4 * i + 2] = fmaxf(fmaxf(w0.z, w1.z), fmaxf(w2.z, w3.z));
-                    cm[4 * i + 3] = fmaxf(fmaxf(w0.w, w1.w), fmaxf(w2.w, w3.w));
-                }
-            }
-            const float* mold = msm + b * kH;
-            bool resc = false;
-#pragma unroll
-            for (int h = 0; h < kH; ++h) {
-                const float mo = mold[h];
-                const bool up = mo != NEG_INF && cm[h] > mo + kLazy;
-                resc = resc || up;
-                cm[h] = (mo == NEG_INF || up) ? cm[h] : mo;
-            }
-            if (resc) {
-                // O^T through the previous chunk is complete before it is rescaled
-                if (!bwait(o_done, (uint32_t)((c - 1) & 1))) {
+                const bool valid = mask[b * kT + j] != 0;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars + ROWS_EMPTY + b);
+                if (!bwait(S_FULL, (uint32_t)(n & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                // chunk maximum per head: over the warp, then over the four warps
+                float* rb = red + b * 4 * kH;
+                {
+                    uint32_t sv[2][32];
+                    tc_ld32(sv[0], tmem + lrow);
+                    tc_ld32(sv[1], tmem + lrow + 32);
+                    tc_wait_ld(sv[0]);
+                    tc_tie(sv[1]);
+                    float4* dst = reinterpret_cast<float4*>(rb + qd * kH);
+#pragma unroll
+                    for (int i = 0; i < kH / 4; ++i) {
+                        float4 m4;
+                        m4.x = warp_max(valid ? __uint_as_float(sv[i >> 3][(4 * i) & 31]) * a.sl2
+                                              : NEG_INF);
+                        m4.y = warp_max(valid ? __uint_as_float(sv[i >> 3][(4 * i + 1) & 31]) * a.sl2
+                                              : NEG_INF);
+                        m4.z = warp_max(valid ? __uint_as_float(sv[i >> 3][(4 * i + 2) & 31]) * a.sl2
+                                              : NEG_INF);
+                        m4.w = warp_max(valid ? __uint_as_float(sv[i >> 3][(4 * i + 3) & 31]) * a.sl2
+                                              : NEG_INF);
+                        if (lane == 0) dst[i] = m4;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars + RED + b);
+                if (!bwait(RED + b, (uint32_t)((n >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                // new running maxima (lagging by at most kLazy) into cm
+                float cm[kH];
+                {
+                    const float4* r4 = reinterpret_cast<const float4*>(rb);
+#pragma unroll
+                    for (int i = 0; i < kH / 4; ++i) {
+                        const float4 w0 = r4[i], w1 = r4[kH / 4 + i], w2 = r4[2 * (kH / 4) + i],
+                                     w3 = r4[3 * (kH / 4) + i];
+                        cm[4 * i] = fmaxf(fmaxf(w0.x, w1.x), fmaxf(w2.x, w3.x));
+                        cm[4 * i + 1] = fmaxf(fmaxf(w0.y, w1.y), fmaxf(w2.y, w3.y));
+                        cm[4 * i + 2] = fmaxf(fmaxf(w0.z, w1.z), fmaxf(w2.z, w3.z));
+                        cm[4 * i + 3] = fmaxf(fmaxf(w0.w, w1.w), fmaxf(w2.w, w3.w));
+                    }
+                }
+                const float* mold = msm + b * kH;  // read only when c > 0
+                bool resc = false;
+#pragma unroll
+                for (int h = 0; h < kH; ++h) {
+                    const float mo = c > 0 ? mold[h] : NEG_INF;
+                    const bool up = mo != NEG_INF && cm[h] > mo + kLazy;
+                    resc = resc || up;
+                    cm[h] = (mo == NEG_INF || up) ? cm[h] : mo;
+                }
+                if (resc) {
+                    // O^T through the previous chunk is complete: S_FULL of this chunk
+                    // was committed after that chunk's PV.
 #pragma unroll 1
-                for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < kQuarters; ++i) {
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        uint32_t v[32];
-                        const uint32_t addr = tmem + lrow + 64 + 64 * i + 32 * hh;
-                        tc_ld32(v, addr);
-                        tc_wait_ld(v);
+                        for (int hh = 0; hh < 2; ++hh) {
+                            uint32_t v[32];
+                            const uint32_t addr = tmem + lrow + 64 + 64 * i + 32 * hh;
+                            tc_ld32(v, addr);
+                            tc_wait_ld(v);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            const int h = 32 * hh + k;
-                            const float f = mold[h] == NEG_INF ? 1.f : exp2f(mold[h] - cm[h]);
-                            v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
+                            for (int kk = 0; kk < 32; ++kk) {
+                                const int h = 32 * hh + kk;
+                                const float f = mold[h] == NEG_INF ? 1.f : exp2f(mold[h] - cm[h]);
+                                v[kk] = __float_as_uint(__uint_as_float(v[kk]) * f);
+                            }
+                            tc_st32(addr, v);
                         }
-                        tc_st32(addr, v);
+                    }
+                    tc_wait_st();
+                }
+                if (c > 0) {
+#pragma unroll
+                    for (int h = 0; h < kH; ++h)
+                        if (mold[h] != NEG_INF && cm[h] != mold[h]) lacc[h] *= exp2f(mold[h] - cm[h]);
+                }
+                if (lane == 0) {  // every warp writes the same values
+                    float4* mn4 = reinterpret_cast<float4*>(msm + (b ^ 1) * kH);
+#pragma unroll
+                    for (int i = 0; i < kH / 4; ++i)
+                        mn4[i] = make_float4(cm[4 * i], cm[4 * i + 1], cm[4 * i + 2], cm[4 * i + 3]);
+                }
+                // probabilities (scores read again from tensor memory) as P^T row j in bf16
+                {
+                    uint32_t sv[2][32];
+                    tc_ld32(sv[0], tmem + lrow);
+                    tc_ld32(sv[1], tmem + lrow + 32);
+                    tc_wait_ld(sv[0]);
+                    tc_tie(sv[1]);
+                    uint4* prow = reinterpret_cast<uint4*>(sP + j * 128);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {  // heads 8q .. 8q+7 -> one 16-byte chunk
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int h = 8 * q + 2 * e;
+                            const float x0 = __uint_as_float(sv[h >> 5][h & 31]) * a.sl2;
+                            const float x1 = __uint_as_float(sv[(h + 1) >> 5][(h + 1) & 31]) * a.sl2;
+                            const float p0 = (valid && cm[h] != NEG_INF) ? exp2f(x0 - cm[h]) : 0.f;
+                            const float p1 =
+                                (valid && cm[h + 1] != NEG_INF) ? exp2f(x1 - cm[h + 1]) : 0.f;
+                            lacc[h] += p0;
+                            lacc[h + 1] += p1;
+                            pk[e] = pack_bf16x2(p0, p1);
+                        }
+                        prow[q ^ (j & 7)] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     }
                 }
-                tc_wait_st();
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars + P_FULL);
             }
-#pragma unroll
-            for (int h = 0; h < kH; ++h)
-                if (mold[h] != NEG_INF && cm[h] != mold[h]) lacc[h] *= exp2f(mold[h] - cm[h]);
-            if (lane == 0) {  // every warp writes the same values
-                float4* mn4 = reinterpret_cast<float4*>(msm + (b ^ 1) * kH);
-#pragma unroll
-                for (int i = 0; i < kH / 4; ++i)
-                    mn4[i] = make_float4(cm[4 * i], cm[4 * i + 1], cm[4 * i + 2], cm[4 * i + 3]);
-            }
-            // probabilities (scores read again from tensor memory) as P^T row j in bf16
-            {
-                uint32_t sv[2][32];
-                tc_ld32(sv[0], tmem + lrow);
-                tc_ld32(sv[1], tmem + lrow + 32);
-                tc_wait_ld(sv[0]);
-                tc_tie(sv[1]);
-                uint4* prow = reinterpret_cast<uint4*>(sP + j * 128);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {  // heads 8q .. 8q+7 -> one 16-byte chunk
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int h = 8 * q + 2 * e;
-                        const float x0 = __uint_as_float(sv[h >> 5][h & 31]) * a.sl2;
-                        const float x1 = __uint_as_float(sv[(h + 1) >> 5][(h + 1) & 31]) * a.sl2;
-                        const float p0 = (valid && cm[h] != NEG_INF) ? exp2f(x0 - cm[h]) : 0.f;
-                        const float p1 =
-                            (valid && cm[h + 1] != NEG_INF) ? exp2f(x1 - cm[h + 1]) : 0.f;
-                        lacc[h] += p0;
-                        lacc[h + 1] += p1;
-                        pk[e] = pack_bf16x2(p0, p1);
-                    }
-                    prow[q ^ (j & 7)] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
-        }
+            if (!ok) break;
 
-        // ---- epilogue ----
-        if (ok && nch > 0 && !bwait(o_done, (uint32_t)((nch - 1) & 1))) ok = false;
-        // head sums: reduce-scatter over the warp (lane l ends with heads 2l, 2l+1),
-        // then over the four warps through shared memory
-        float v64[kH];
-#pragma unroll
-        for (int h = 0; h < kH; ++h) v64[h] = lacc[h];
-#pragma unroll
-        for (int w = kH / 2, m = 16; m >= 1; w >>= 1, m >>= 1) {
-#pragma unroll
-            for (int i = 0; i < w; ++i) {
-                const bool hi = (lane & m) != 0;
-                const float send = hi ? v64[i] : v64[w + i];
-                const float recv = __shfl_xor_sync(0xffffffffu, send, m);
-                v64[i] = (hi ? v64[w + i] : v64[i]) + recv;
+            // ---- epilogue of the unit ----
+            if (!bwait(O_DONE, (uint32_t)(k & 1))) {
+                ok = false;
+                break;
             }
-        }
-        // [4 warps][kH] in the buffer the last chunk did not use: every warp finished
-        // its reads of that one before the last chunk's scores existed
-        float* sums = red + (nch & 1) * 4 * kH;
-        sums[qd * kH + 2 * lane] = v64[0];
-        sums[qd * kH + 2 * lane + 1] = v64[1];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sum_bar);
-        if (!bwait(sum_bar, 0)) ok = false;
-        if (ok) {
+            tc_fence_after();
+            // head sums: reduce-scatter over the warp (lane l ends with heads 2l, 2l+1),
+            // then over the four warps through shared memory
+            float v64[kH];
+#pragma unroll
+            for (int h = 0; h < kH; ++h) v64[h] = lacc[h];
+#pragma unroll
+            for (int ww = kH / 2, m = 16; m >= 1; ww >>= 1, m >>= 1) {
+#pragma unroll
+                for (int i = 0; i < ww; ++i) {
+                    const bool hi = (lane & m) != 0;
+                    const float send = hi ? v64[i] : v64[ww + i];
+                    const float recv = __shfl_xor_sync(0xffffffffu, send, m);
+                    v64[i] = (hi ? v64[ww + i] : v64[i]) + recv;
+                }
+            }
+            // the sums buffer is free once every warp has read the last unit's sums
+            if (k > 0 && !bwait(SUM_OUT, (uint32_t)((k - 1) & 1))) {
+                ok = false;
+                break;
+            }
+            sums[qd * kH + 2 * lane] = v64[0];
+            sums[qd * kH + 2 * lane + 1] = v64[1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + SUM_IN);
+            if (!bwait(SUM_IN, (uint32_t)(k & 1))) {
+                ok = false;
+                break;
+            }
             if (a.ns > 1 && j < kH) {  // thread j writes head j's (m, l)
-                const float mj = msm[(nch & 1) * kH + j];  // the last chunk's new maxima
+                const float mj = msm[(n & 1) * kH + j];  // the last chunk's new maxima
                 const float ls = (sums[j] + sums[kH + j]) + (sums[2 * kH + j] + sums[3 * kH + j]);
-                *reinterpret_cast<float2*>(a.part_ml + (((long long)r * a.ns + split) * kH + j) * 2) =
-                    make_float2(mj, ls);
+                *reinterpret_cast<float2*>(a.part_ml + (pbase + j) * 2) = make_float2(mj, ls);
             }
-            const long long pbase = ((long long)r * a.ns + split) * kH;
-            if (nch > 0) tc_fence_after();
 #pragma unroll 1
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < kQuarters; ++i) {
                 const int cidx = 128 * i + j;  // latent column = tensor lane of tile i
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t v[32];
-                    if (nch > 0) {
-                        tc_ld32(v, tmem + lrow + 64 + 64 * i + 32 * hh);
-                        tc_wait_ld(v);
-                    } else {
+                    tc_ld32(v, tmem + lrow + 64 + 64 * i + 32 * hh);
+                    tc_wait_ld(v);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) v[k] = 0u;
-                    }
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const int h = 32 * hh + k;
-                        const float o = __uint_as_float(v[k]);
+                    for (int kk = 0; kk < 32; ++kk) {
+                        const int h = 32 * hh + kk;
+                        const float o = __uint_as_float(v[kk]);
                         if (a.ns > 1) {
                             a.part_o[(pbase + h) * kKVL + cidx] = o;
                         } else {
                             const float ls = (sums[h] + sums[kH + h]) +
                                              (sums[2 * kH + h] + sums[3 * kH + h]);
                             const float val = ls > 0.f ? o / ls : 0.f;
-                            const long long oi = ((long long)r * kH + h) * kKVL + cidx;
+                            const long long oi = ((long long)w.r * kH + h) * kKVL + cidx;
                             if (a.olat) a.olat[oi] = val;
-                            if (a.xbf)
-                                a.xbf[oi] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+                            if (a.xbf) a.xbf[oi] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
                         }
                     }
                 }
             }
+            // O^T is read: the next unit's first PV may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bars + O_FREE);
+                mbar_arrive(bars + SUM_OUT);
+            }
+            ++k;
         }
     }
 
@@ -444,10 +584,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-// Opt-in (DSA_MLA_TC=1): at the sizes measured so far it is not faster than the
-// mma.sync split kernel. At decode size each CTA runs its single chunk once and
-// waits on instruction fetch; at prefill size its gather, QK, softmax and PV of a
-// chunk run back to back (one latent buffer fits next to Q).
+// Opt-in (DSA_MLA_TC=1, 64 heads). Not faster than the mma.sync split kernel at the
+// sizes measured: a phase probe at 4,096 rows x 2,048 tokens shows about 11.6 us per
+// chunk, of which the gather of the 128 KB tile takes 5.7 us (cp.async reaches about
+// 25 GB/s per SM) and the softmax 4.8 us, with the tensor pipe busy about 1.5 us;
+// with one tile in shared memory the gather cannot overlap the softmax.
 bool mla_tc_supported(int heads, int kv_lora_rank) {
     if (heads != kH || kv_lora_rank != kKVL) return false;
     const char* v = getenv("DSA_MLA_TC");
@@ -460,16 +601,20 @@ int mla_tc_launch(const MlaTcParams& a, long long ckv_rows, cudaStream_t st) {
     if (ckv_rows < 1 || ckv_rows > 0x7fffffffLL)
         return fail(DSA_ERR_UNSUPPORTED, "dsa_sparse_mla_decode: latent cache rows %lld",
                     ckv_rows);
-    if ((long long)a.rows * kH > 0x7fffffffLL)
+    if ((long long)a.rows * kH > 0x7fffffffLL || (long long)a.rows * a.ns > 0x7fffffffLL)
         return fail(DSA_ERR_UNSUPPORTED, "dsa_sparse_mla_decode: too many rows");
+    const int sms = sm_count();
+    if (sms <= 0) return fail(DSA_ERR_CUDA, "dsa_sparse_mla_decode: no CUDA device");
+    const long long units = (long long)a.rows * a.ns;
+    if (units == 0) return DSA_OK;
+    const int grid = (int)(units < sms ? units : sms);
     CUtensorMap tmQ;
     int rc = make_tmap_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.qlat, kKVL,
                           (uint64_t)a.rows * kH, kKVL * 2, 64, kH, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
     rc = set_max_smem((const void*)mla_tc_kernel, (int)kDyn);
     if (rc) return rc;
-    cudaError_t e = launch_pdl(mla_tc_kernel, dim3((unsigned)a.ns, (unsigned)a.rows), dim3(kThreads),
-                               kDyn, st, tmQ, a);
+    cudaError_t e = launch_pdl(mla_tc_kernel, dim3((unsigned)grid), dim3(kThreads), kDyn, st, tmQ, a);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_mla_decode tensor-core launch");
     return DSA_OK;

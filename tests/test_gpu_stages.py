@@ -414,6 +414,50 @@ def test_mla_rescaled_running_max(mla_kernel):
     H.check_attention(olat.t.cpu().numpy().reshape(wl.rows, -1), np.array(ro), "rescale olat")
 
 
+PERSISTENT_CASES = [
+    # name, query rows, sequence lengths, the rows' sequence, block_size, out_width,
+    # rescale. More (row, split) units than SMs: the tcgen05 kernel's persistent CTAs
+    # walk several units each, many 128-token chunks per unit, a ragged last chunk,
+    # and rows with no tokens at all.
+    ("r400-ow1000-paged", 400, [3100, 6000], 1, 64, 1000, False),
+    ("r320-ow2048-rescale", 320, [4096, 2600], 0, None, 2048, True),
+]
+
+
+@pytest.mark.parametrize("case", PERSISTENT_CASES, ids=[c[0] for c in PERSISTENT_CASES])
+def test_mla_persistent_many_units(case, mla_kernel):
+    name, rows, lens, seq, bs, ow, rescale = case
+    g = _geom(heads=64, hidden=64, index_topk=ow)
+    wl = W.make_workload(name, 303, g, lens, block_size=bs, with_raw=False, with_o_absorb=False,
+                         rows_ctx=[lens[seq]] * rows, prefill_seq=seq)
+    if rescale:
+        # token row k gets factor 1 + 6 * (k mod 4096) / 4096: later chunks of a row
+        # with ascending ids score far above the earlier ones (running-max rescales)
+        flat = wl.ckv.float().view(-1, 512)
+        fac = 1.0 + 6.0 * (torch.arange(flat.shape[0], dtype=torch.float32) % 4096) / 4096.0
+        wl.ckv = (flat * fac[:, None]).to(torch.bfloat16).view(wl.ckv.shape)
+    layer = DsaDecodeLayer(wl, with_o_absorb=False, keep_olat=True)
+    rng = np.random.default_rng(ow + len(lens))
+    ids = _token_rows(rng, wl, ow)
+    ids[7] = -1  # another row with no tokens
+    if rescale:
+        for r in range(wl.rows):
+            v = np.sort(ids[r][ids[r] >= 0])
+            ids[r] = -1
+            ids[r, : v.size] = v
+    tok = torch.from_numpy(ids).cuda()
+    olat = H.Guarded((wl.rows, 64, 512), torch.float32, 555.0)
+    api.dsa_sparse_mla_decode(layer.qlat, layer.row_seq, layer.ckv, layer.pg, tok,
+                              g.softmax_scale, None, None, olat.t, layer.status, layer.workspace)
+    torch.cuda.synchronize()
+    olat.check()
+    assert int(layer.status.item()) == 0
+    oq = H.OracleSeq(wl)
+    ro = [O.sparse_mla_decode_row(H.f(wl.qlat[r]), oq.ckv(int(wl.row_seq[r])), ids[r],
+                                  g.softmax_scale, None)[0].reshape(-1) for r in range(wl.rows)]
+    H.check_attention(olat.t.cpu().numpy().reshape(wl.rows, -1), np.array(ro), f"{name} olat")
+
+
 def test_mla_bad_ids_set_status_and_are_skipped():
     g = _geom(heads=8, hidden=64, index_topk=128)
     wl = W.make_workload("bad", 301, g, [500, 200], block_size=64, with_raw=False)
