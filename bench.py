@@ -26,7 +26,9 @@ import argparse
 import ctypes
 import dataclasses
 import json
+import platform
 import statistics
+import subprocess
 import sys
 import threading
 import time
@@ -210,6 +212,38 @@ def algorithmic_bytes(wl, layer) -> dict:
             "selected_tokens": sel_tokens, "candidate_pools": cand}
 
 
+def compress_bytes(wl, seq_lens) -> int:
+    """dsa_compress over the given context lengths: raw keys, gate logits and validity
+    of every token in; one pooled key and flag per whole pool out."""
+    g = wl.geom
+    ihd, kp = g.index_head_dim, g.index_kpool
+    toks = int(np.sum(seq_lens))
+    pools = int(sum(max(0, (int(L) - g.first_key) // kp) for L in seq_lens))
+    return toks * (2 * ihd * 2 + 1) + pools * (ihd * 2 + 1)
+
+
+def cpu_info() -> dict:
+    """The host's CPU model and thread count (for the CPU baseline's label)."""
+    model = None
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.strip().lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return {"cpu_model": model or platform.machine(), "nproc": os.cpu_count()}
+
+
 def algorithmic_flops(wl, layer) -> dict:
     """Per step of the prefill chunk: the dense index-score contraction over every
     pool of the row stride (2 * rows * heads * p_stride * ihd) and the sparse
@@ -284,6 +318,19 @@ class OracleRunner:
 def cpu_baseline(wl, budget_s: float = 12.0, max_rows: int = 2, latent_fp8: bool = False) -> dict:
     prefill = wl.name.startswith("prefill")
     runner = OracleRunner(wl, with_project=not prefill, latent_fp8=latent_fp8)
+    # one thread, held on one core for the timed rows
+    old_aff = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    core = min(old_aff) if old_aff else None
+    if core is not None:
+        os.sched_setaffinity(0, {core})
+    try:
+        return _cpu_baseline(runner, wl, budget_s, max_rows, prefill, core)
+    finally:
+        if old_aff:
+            os.sched_setaffinity(0, old_aff)
+
+
+def _cpu_baseline(runner, wl, budget_s, max_rows, prefill, core) -> dict:
     times, rows = [], []
     for r in range(min(max_rows, wl.rows)):
         runner._prep(r)
@@ -302,7 +349,7 @@ def cpu_baseline(wl, budget_s: float = 12.0, max_rows: int = 2, latent_fp8: bool
             "sample": f"{len(times)} query rows (rows {rows}) of {wl.name}: score over all "
                       f"{wl.p_stride} pools, top-k, expand, attention over the selected tokens, "
                       f"{tail}; float64 numpy, one thread; pooled-key cache built untimed",
-            "seconds": sum(times)}
+            "seconds": sum(times), "pinned_core": core, **cpu_info()}
 
 
 # ---------------------------------------------------------------------------
@@ -325,9 +372,17 @@ def run_reference(args, ws, rank):
     rows = [r % wl.rows for r in range(min(2, wl.rows))]
     for r in rows:
         runner._prep(r)
-    for i in range(args.warmup):
-        runner.run_row(rows[i % len(rows)])
-    ts = [runner.run_row(rows[i % len(rows)]) for i in range(args.steps)]
+    old_aff = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    core = min(old_aff) if old_aff else None
+    if core is not None:
+        os.sched_setaffinity(0, {core})  # one thread on one core, as the CPU baseline
+    try:
+        for i in range(args.warmup):
+            runner.run_row(rows[i % len(rows)])
+        ts = [runner.run_row(rows[i % len(rows)]) for i in range(args.steps)]
+    finally:
+        if old_aff:
+            os.sched_setaffinity(0, old_aff)
     total = sum(ts)
     v = args.steps / total
     line = {
@@ -338,7 +393,8 @@ def run_reference(args, ws, rank):
         "data": "synthetic",
         "config": workload_config(wl, args),
         "cpu_baseline": {"value": v, "unit": "queries/s", "cores": 1, "kind": "oracle",
-                         "sample": f"one query row per step (rows {rows}) of {wl.name}"},
+                         "sample": f"one query row per step (rows {rows}) of {wl.name}",
+                         "pinned_core": core, **cpu_info()},
         "e2e": {"value": v, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -442,6 +498,7 @@ def main():
 
     flush = _Flush()
     ct = []
+    comp_bytes = compress_bytes(wl, layer.seq_lens.cpu().numpy())
     for _ in range(3):
         flush.zero_()
         e0.record()
@@ -600,6 +657,7 @@ def main():
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk):
         peaks = json.load(open(pk))
+    hbm_peak = peaks.get("hbm_gbs") or 6800.0
     if prefill:
         tf = peaks.get("bf16_tflops")
         peak_src = "measured (bf16 dense burst)" if tf else "fallback"
@@ -639,6 +697,13 @@ def main():
                     "algorithmic_bytes_per_launch": dom_bytes,
                     "step_algorithmic_bytes": ab["total"], "step_achieved_gbs": total_gbs,
                     "step_frac": total_gbs / hbm}
+        # the step without the o_absorb projection: index scores, top-k (+ token ids)
+        # and the sparse attention to olat, timed by their stages
+        core_b = ab["score"] + ab["attend"]
+        core_ms = sum(stage_ms[k] for k in ("score", "select", "expand", "attend"))
+        roofline["attention_core"] = {"bytes": core_b, "ms": core_ms,
+                                      "achieved_gbs": core_b / (core_ms * 1e-3) / 1e9,
+                                      "frac": core_b / (core_ms * 1e-3) / 1e9 / hbm}
     line = {
         "metric": PREFILL_METRIC if prefill else METRIC, "value": value, "unit": "queries/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -649,6 +714,11 @@ def main():
         "stage_timing": ("separate pass, graph with event nodes" if graph_events
                          else "separate eager pass"),
         "compress_ms": min(ct),
+        "compress": {"bytes": comp_bytes, "ms": min(ct),
+                     "achieved_gbs": comp_bytes / (min(ct) * 1e-3) / 1e9,
+                     "frac": comp_bytes / (min(ct) * 1e-3) / 1e9 / hbm_peak,
+                     "note": "dsa_compress alone (setup, not in the step): raw keys, gates "
+                             "and flags in, pooled keys and flags out; L2 flushed before"},
         "gpu_launches": launches * args.steps,
         "clocks": clocks.summary(),
     }
