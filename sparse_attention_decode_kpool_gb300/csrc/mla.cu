@@ -390,6 +390,16 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
     __shared__ float wsh[kMaxSplits];
     __shared__ float lsum;
     const int h = blockIdx.x, r = blockIdx.y, t = threadIdx.x;
+    const long long stride = (long long)heads * (KVL / 4);  // float4s between splits
+    const float4* po = reinterpret_cast<const float4*>(part_o) +
+                       ((long long)r * ns * heads + h) * (KVL / 4) + t;
+    // The first 16 splits' partials are requested before the weights are known, so
+    // the two round trips to L2 overlap.
+    constexpr int kEarly = 16;
+    float4 oe[kEarly];
+#pragma unroll
+    for (int j = 0; j < kEarly; ++j)
+        oe[j] = j < ns ? __ldg(po + j * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (t < 32) {
         float m[2], l[2];
 #pragma unroll
@@ -419,11 +429,18 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
         if (t == 0) lsum = L;
     }
     __syncthreads();
-    const long long stride = (long long)heads * (KVL / 4);  // float4s between splits
-    const float4* po = reinterpret_cast<const float4*>(part_o) +
-                       ((long long)r * ns * heads + h) * (KVL / 4) + t;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < ns; s0 += 8) {
+#pragma unroll
+    for (int j = 0; j < kEarly; ++j) {
+        if (j < ns) {
+            const float wgt = wsh[j];
+            acc.x += wgt * oe[j].x;
+            acc.y += wgt * oe[j].y;
+            acc.z += wgt * oe[j].z;
+            acc.w += wgt * oe[j].w;
+        }
+    }
+    for (int s0 = kEarly; s0 < ns; s0 += 8) {
         float4 o[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
