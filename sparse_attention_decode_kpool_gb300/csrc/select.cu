@@ -15,11 +15,13 @@
 // shared-memory histograms) resolves the exact key and how many equal keys to take.
 // A ballot-prefix pass then emits the chosen positions in ascending order.
 //
-// With C > 1 every CTA pushes its chosen (key, id) pairs through distributed shared
-// memory into its own slot of CTA 0's merge area (unused slot entries get key 0),
-// one cluster barrier publishes them, and CTA 0 selects the row's top-k among the
-// C x k candidates the same way: the row's top-k is contained in the union of the
-// slices' top-k, and slot order keeps the ids ascending.
+// With C > 1 every CTA stages its chosen (key, id) pairs in its own slot of its merge
+// area (unused slot entries get key 0) and moves the slot to the same place in CTA 0
+// with bulk copies that complete on an mbarrier there; CTA 0 then selects the row's
+// top-k among the C x k candidates the same way: the row's top-k is contained in the
+// union of the slices' top-k, and slot order keeps the ids ascending. Two cluster
+// barrier phases order the rest: CTA 0's mbarrier exists before any push, and no CTA
+// leaves before CTA 0 has received its slot.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -56,6 +58,31 @@ struct SelectArgs {
     const int32_t* row_ctx;  // nullable: rows' context lengths, for the tail tokens
     int tail_at;             // token-id position of the first tail slot (ow: no tail)
 };
+
+// Orders this thread's shared-memory writes before later bulk (async proxy) copies.
+__device__ __forceinline__ void fence_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+// Cluster barrier halves (every thread of every CTA of the cluster arrives).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// bytes (a multiple of 16) from this CTA's shared memory at src to dst in CTA
+// `rank`'s shared memory (same offsets), completing on that CTA's mbarrier bar.
+__device__ __forceinline__ void bulk_to_peer(const void* src, const void* dst, uint32_t bytes,
+                                             const uint64_t* bar, uint32_t rank) {
+    uint32_t d, b;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(d) : "r"(smem_u32(dst)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(b) : "r"(smem_u32(bar)), "r"(rank));
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];\n" ::"r"(d),
+        "r"(smem_u32(src)), "r"(bytes), "r"(b)
+        : "memory");
+}
 
 __device__ __forceinline__ uint32_t score_key(float f) {
     uint32_t u = __float_as_uint(f);
@@ -440,6 +467,19 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
     const int begin = crank * a.chunk;
     const int n = max(0, min(a.chunk, a.p_stride - begin));
     const float* srow = a.scores + (long long)r * a.p_stride + begin;
+    // Merge area (used in CTA 0; the other CTAs stage their own slot there first):
+    // keys [C][sk4], ids [C][sk4], bounds [C][4], then the mbarrier the pushes
+    // complete on. sk4 = select_k rounded up to whole 16-byte rows.
+    const int sk4 = (a.sk + 3) & ~3;
+    uint32_t* mloc = reinterpret_cast<uint32_t*>(dyn + a.merge_off);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(mloc + 2 * C * sk4 + 4 * C);
+    if (C > 1) {
+        if (crank == 0 && threadIdx.x == 0) {
+            mbar_init(mbar, 1);
+            fence_mbar_init();
+        }
+        cluster_arrive();  // phase 1: CTA 0's mbarrier exists (waited on before the push)
+    }
     uint32_t kmx = 0u, kmn = 0xffffffffu;
     int kcnt = 0;
     auto put = [&](int i, float f) {
@@ -499,43 +539,74 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
         return;
     }
 
-    // This slice's top-k, pushed into slot crank of CTA 0's merge area, with bounds
-    // (chosen keys are >= the slice threshold and <= the slice maximum) and count.
-    uint32_t* m0 = cluster.map_shared_rank(reinterpret_cast<uint32_t*>(dyn + a.merge_off), 0);
+    // This slice's top-k, staged in slot crank of this CTA's merge area, with bounds
+    // (chosen keys are >= the slice threshold and <= the slice maximum) and count;
+    // one bulk copy per part then moves the slot to the same place in CTA 0.
     e.mode = 1;
-    e.rkeys = m0 + crank * a.sk;
-    e.rids = m0 + C * a.sk + crank * a.sk;
+    e.rkeys = mloc + crank * sk4;
+    e.rids = mloc + C * sk4 + crank * sk4;
     const int kc = block_topk(keys, n, a.sk, mm, sc, tbuf, a.tcap, e, &t);
-    for (int j = kc + threadIdx.x; j < a.sk; j += kThreads) e.rkeys[j] = 0u;
+    for (int j = kc + threadIdx.x; j < sk4; j += kThreads) e.rkeys[j] = 0u;
+    uint32_t* st = mloc + 2 * C * sk4;
     if (threadIdx.x == 0) {
-        uint32_t* st = m0 + 2 * C * a.sk + 3 * crank;
-        st[0] = kc > 0 ? t.T : 0xffffffffu;
-        st[1] = kc > 0 ? mm.kmax : 0u;
-        st[2] = (uint32_t)kc;
+        st[4 * crank] = kc > 0 ? t.T : 0xffffffffu;
+        st[4 * crank + 1] = kc > 0 ? mm.kmax : 0u;
+        st[4 * crank + 2] = (uint32_t)kc;
+        st[4 * crank + 3] = 0u;
     }
-    cluster.sync();  // publishes the pushed lists; no remote access happens after it
-    if (crank != 0) return;
+    cluster_wait();  // phase 1 (long complete: CTA 0 arrived before its slice work)
+    const uint32_t slot = (uint32_t)sk4 * 4u;
+    if (crank != 0) {
+        fence_async_shared();  // the staged slot, written by this CTA's threads ...
+        __syncthreads();       // ... is visible to the bulk copies
+        if (threadIdx.x == 0) {
+            bulk_to_peer(e.rkeys, e.rkeys, slot, mbar, 0);
+            bulk_to_peer(e.rids, e.rids, slot, mbar, 0);
+            bulk_to_peer(st + 4 * crank, st + 4 * crank, 16, mbar, 0);
+        }
+        // phase 2: CTA 0 arrives once every push has landed, so this CTA's shared
+        // memory is no longer read when it leaves
+        cluster_arrive();
+        cluster_wait();
+        return;
+    }
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(mbar, (uint32_t)(C - 1) * (2u * slot + 16u));
+        // bounded: a push that never lands leaves the row unselected (all -1)
+        sc.pick[0] = mbar_wait(mbar, 0) ? 1 : 0;
+    }
+    __syncthreads();
+    const bool landed = sc.pick[0] != 0;
+    __syncthreads();  // pick[] is scratch of the merge below
+    cluster_arrive();  // phase 2: the pushed slots are in; the other CTAs may leave
+    if (!landed) {
+        int t0, tend;
+        tail_range(a, r, &t0, &tend);
+        fill_tail(out, a.sk, tok, a.ow, a.kpool, 0, a.tail_at, t0, tend);
+        cluster_wait();
+        return;
+    }
 
-    const uint32_t* mkeys = reinterpret_cast<const uint32_t*>(dyn + a.merge_off);
-    const uint32_t* st = mkeys + 2 * C * a.sk;
+    const uint32_t* mkeys = mloc;
     MinMax mg{0xffffffffu, 0u, 0};
     for (int c = 0; c < C; ++c) {
-        mg.kmin = min(mg.kmin, st[3 * c]);
-        mg.kmax = max(mg.kmax, st[3 * c + 1]);
-        mg.count += (int)st[3 * c + 2];
+        mg.kmin = min(mg.kmin, st[4 * c]);
+        mg.kmax = max(mg.kmax, st[4 * c + 1]);
+        mg.count += (int)st[4 * c + 2];
     }
     e.mode = 2;
     e.base = 0;
-    e.ids = mkeys + C * a.sk;
-    const int kk = block_topk(mkeys, C * a.sk, a.sk, mg, sc, tbuf, a.tcap, e, &t);
+    e.ids = mkeys + C * sk4;
+    const int kk = block_topk(mkeys, C * sk4, a.sk, mg, sc, tbuf, a.tcap, e, &t);
     int t0, tend;
     tail_range(a, r, &t0, &tend);
     fill_tail(out, a.sk, tok, a.ow, a.kpool, kk, a.tail_at, t0, tend);
+    cluster_wait();  // phase 2 (complete: every CTA arrived)
 }
 
 // Dynamic shared memory: the slice's keys (4 B each); with C > 1 the merge area
-// (C x select_k keys and ids plus 3 words of bounds per slice, used in CTA 0); the
-// threshold bin's list.
+// (C x sk4 keys and ids, 4 words of bounds per slice and an mbarrier; sk4 = select_k
+// rounded up to a multiple of 4); the threshold bin's list.
 struct SmemPlan {
     long long merge_off, tbuf_off, tcap, bytes;
 };
@@ -543,7 +614,8 @@ SmemPlan smem_plan(int p_stride, int sk, int C) {
     const long long chunk = (p_stride + C - 1) / C;
     SmemPlan p;
     p.merge_off = (chunk * 4 + 15) & ~15LL;
-    p.tbuf_off = p.merge_off + (C > 1 ? ((long long)C * sk * 8 + 12LL * C + 15) & ~15LL : 0);
+    const long long sk4 = (sk + 3) & ~3LL;
+    p.tbuf_off = p.merge_off + (C > 1 ? (long long)C * sk4 * 8 + 16LL * C + 16 : 0);
     const long long room = (kMaxSmem - p.tbuf_off) / 4;
     p.tcap = room > 2048 ? 2048 : room;
     p.bytes = p.tbuf_off + 4 * (p.tcap > 0 ? p.tcap : 0);
