@@ -154,6 +154,8 @@ SELECT_CASES = [
     (3, 100003, 2048, 4, "normal"), (2, 3000, 2048, 4, "sparse"), (2, 700, 256, 4, "allinf"),
     (5, 16384, 2048, 4, "positive"), (64, 16384, 2048, 4, "normal"), (300, 2048, 512, 4, "ties"),
     (1, 327680, 2048, 4, "positive"), (2, 40000, 64, 1, "ties"),
+    # select_k not a multiple of 4 on clustered rows (padded merge slots)
+    (3, 60000, 2044, 4, "ties"), (2, 50000, 1026, 1, "normal"),
 ]
 
 
@@ -181,6 +183,7 @@ SELECT_EXPAND_CASES = [
     (2, 700, 256, 4, "allinf", 0, 0), (64, 16384, 2048, 4, "normal", 0, 0),
     (300, 2048, 512, 4, "ties", 0, 0), (2, 40000, 64, 1, "ties", 2, 3),
     (3, 2000, 128, 16, "normal", 16, 0), (2, 0, 256, 4, "allinf", 0, 9),
+    (2, 70001, 2042, 2, "positive", 1, 3),
 ]
 
 
