@@ -22,11 +22,13 @@ int set_max_smem(const void* kernel, int bytes);  // once per (device, kernel)
 
 // Programmatic dependent launch. Every kernel of the library is launched as a
 // programmatic dependent of the work before it on the stream, and waits for that
-// work (pdl_wait) before it touches global memory, so only the launch and the
-// kernel's prologue overlap the predecessor's completion. No kernel triggers its
-// dependents early: blocks of a dependent waiting beside a running grid slowed it.
-// DSA_PDL=0 in the environment turns the attribute off (the wait then returns at
-// once).
+// work (pdl_wait) before it reads anything that work may have written; the only
+// earlier reads are of weights (the projection's first ring of o_absorb boxes).
+// Two kernels let their dependents start early (pdl_trigger): the split combine, so
+// that the projection fetches o_absorb meanwhile, and the front-end norm kernel,
+// ahead of the q GEMM. Elsewhere, dependent blocks waiting beside a running grid
+// slowed it. DSA_PDL=0 in the environment turns the attribute off (the wait then
+// returns at once).
 bool pdl_enabled();
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,

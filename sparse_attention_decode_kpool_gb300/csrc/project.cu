@@ -9,12 +9,13 @@
 // At decode sizes this is a skinny GEMM: every element of o_absorb (268 MB at
 // 4096 x 64 x 512) is used by only the few query rows of the step, so the kernel is
 // an HBM stream. It is built so the number of bytes in flight does not depend on
-// registers: one producer warp per CTA issues bulk async copies (the TMA engine's
-// non-tensor form, one 512-byte row segment per copy) into a ring of shared-memory
-// stages guarded by mbarriers; four consumer warps turn each stage into m16n8k16
-// MMAs (o_absorb rows on M, query rows on N, f32 accumulation). The grid is one CTA
-// per SM and the (row block, k block) units are split evenly over the CTAs in
-// row-block-major order ("stream-K"), so every SM streams the same number of bytes;
+// registers: one producer lane per CTA issues 2-D tensor copies (a 256 x 64 box of
+// o_absorb and the matching 256 x 8 box of the queries per stage) into a ring of
+// shared-memory stages guarded by mbarriers; four consumer warps turn each stage into
+// m16n8k16 MMAs (o_absorb rows on M, query rows on N, f32 accumulation). The grid is
+// two CTAs per SM at decode sizes and the (row block, k block) units are split evenly
+// over the CTAs in row-block-major order ("stream-K"), so every SM streams the same
+// number of bytes;
 // a CTA whose range crosses a row block writes one partial per row block, and a
 // small reduction adds the partials of each row block in a fixed order.
 //
