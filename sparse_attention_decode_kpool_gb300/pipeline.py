@@ -176,6 +176,15 @@ class DsaDecodeLayer:
                 setattr(self, name, buf[o:o + n].view(dt).view(shape))
         return buf
 
+    def use_step_inputs(self, buf: torch.Tensor) -> None:
+        """Point qidx, w, qlat and row_ctx at device buffer buf (the step_inputs
+        layout), e.g. a second buffer so that the next step's inputs can be uploaded
+        while this step runs. Graphs captured afterwards read from buf."""
+        if buf.numel() != self.step_inputs.numel() or buf.device != self.step_inputs.device:
+            raise ValueError("buf must match step_inputs in size and device")
+        for (name, shape, dt), (o, n) in zip(self._in_specs, self._in_offs):
+            setattr(self, name, buf[o:o + n].view(dt).view(shape))
+
     def host_step_inputs(self) -> torch.Tensor:
         """A pinned host buffer with the device step-input layout, filled with the
         workload's inputs: one copy_ into step_inputs uploads a step's queries."""
