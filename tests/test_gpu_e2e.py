@@ -112,6 +112,29 @@ def test_tiny_graph_replay_matches_eager():
     assert torch.equal(layer.y, y0)
 
 
+def test_second_step_input_buffer_matches():
+    # use_step_inputs: a graph captured over a second input buffer (holding the same
+    # inputs) gives the same outputs bit for bit, and writing the first buffer does
+    # not reach it.
+    wl = W.tiny()
+    layer = DsaDecodeLayer(wl)
+    layer.compress()
+    layer.step()
+    torch.cuda.synchronize()
+    y0, tok0 = layer.y.clone(), layer.token_ids.clone()
+    first = layer.step_inputs
+    second = first.clone()
+    layer.use_step_inputs(second)
+    layer.capture()
+    first.zero_()  # the captured graph reads the second buffer only
+    layer.y.zero_()
+    layer.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(layer.y, y0) and torch.equal(layer.token_ids, tok0)
+    with pytest.raises(ValueError):
+        layer.use_step_inputs(second[:-1])
+
+
 def _tail_workload(paged: bool):
     # always_select_tail on lengths that leave every remainder mod kpool past
     # first_key, plus a sequence with no whole pool (6 tokens) and one that ends
