@@ -659,21 +659,36 @@ def main():
         # is already queued. No flush: a step streams over three times the L2's size.
         # For the plain decode step the inputs go through a second device buffer on a
         # copy stream, so step i+1's upload overlaps step i.
-        overlap = fe is None and not append and not prefill and direct_out
+        # (the front-end's hidden state the same way)
+        # (the staged token rows and the front-end's hidden state the same way)
+        overlap = direct_out
         done = [torch.cuda.Event(), torch.cuda.Event()]
         if overlap:
-            dbufs = [layer.step_inputs, torch.empty_like(layer.step_inputs)]
+            # device input sets in the order of `ins`; point(b) makes the layer read set b
+            if fe is None:
+                names = ["k_new", "gate_new", "ckv_new"] if append else []
+                dsets = [[layer.step_inputs] + [getattr(layer, n) for n in names]]
+
+                def point(b: int) -> None:
+                    layer.use_step_inputs(dsets[b][0])
+                    for n, t in zip(names, dsets[b][1:]):
+                        setattr(layer, n, t)
+            else:
+                dsets = [[layer.x]]
+
+                def point(b: int) -> None:
+                    layer.x = dsets[b][0]
+            dsets.append([torch.empty_like(t) for t in dsets[0]])
             sgraphs = []
             for b in range(2):
-                layer.use_step_inputs(dbufs[b])
+                point(b)
                 layer.y = h_ys[b]
                 gr = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(gr):
                     step_fn()
                 sgraphs.append(gr)
-            layer.use_step_inputs(dbufs[0])
+            point(0)
             layer.y = y_dev
-            hsrc = h_ins[0][0], h_ins[1][0]
             cs = torch.cuda.Stream()
             main = torch.cuda.current_stream()
             up = [torch.cuda.Event(), torch.cuda.Event()]
@@ -681,8 +696,9 @@ def main():
             def upload(b: int, after_step: bool) -> None:
                 with torch.cuda.stream(cs):
                     if after_step:
-                        cs.wait_event(done[b])  # the step that last read dbufs[b]
-                    dbufs[b].copy_(hsrc[b], non_blocking=True)
+                        cs.wait_event(done[b])  # the step that last read set b
+                    for d, h in zip(dsets[b], h_ins[b]):
+                        d.copy_(h, non_blocking=True)
                     up[b].record(cs)
 
             def launch(i: int) -> None:
