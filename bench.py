@@ -661,8 +661,11 @@ def main():
         # copy stream, so step i+1's upload overlaps step i.
         # (the front-end's hidden state the same way)
         # (the staged token rows and the front-end's hidden state the same way)
-        overlap = direct_out
+        # With a result that has to be copied out (the prefill chunk's olat) the result
+        # is double-buffered too and read back on a third stream.
+        overlap = True
         done = [torch.cuda.Event(), torch.cuda.Event()]
+        got = [torch.cuda.Event(), torch.cuda.Event()]  # result in host memory
         if overlap:
             # device input sets in the order of `ins`; point(b) makes the layer read set b
             if fe is None:
@@ -679,17 +682,24 @@ def main():
                 def point(b: int) -> None:
                     layer.x = dsets[b][0]
             dsets.append([torch.empty_like(t) for t in dsets[0]])
+            obufs = None if direct_out else [layer.olat, torch.empty_like(layer.olat)]
             sgraphs = []
             for b in range(2):
                 point(b)
-                layer.y = h_ys[b]
+                if direct_out:
+                    layer.y = h_ys[b]
+                else:
+                    layer.olat = obufs[b]
                 gr = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(gr):
                     step_fn()
                 sgraphs.append(gr)
             point(0)
             layer.y = y_dev
+            if obufs is not None:
+                layer.olat = obufs[0]
             cs = torch.cuda.Stream()
+            rs = torch.cuda.Stream()
             main = torch.cuda.current_stream()
             up = [torch.cuda.Event(), torch.cuda.Event()]
 
@@ -704,8 +714,17 @@ def main():
             def launch(i: int) -> None:
                 b = i % 2
                 main.wait_event(up[b])
+                if obufs is not None and i >= 2:
+                    main.wait_event(got[b])  # step i-2's result has left obufs[b]
                 sgraphs[b].replay()
                 done[b].record(main)
+                if obufs is None:
+                    got[b].record(main)  # the step stored it in pinned memory itself
+                else:
+                    with torch.cuda.stream(rs):
+                        rs.wait_event(done[b])
+                        h_ys[b].copy_(obufs[b], non_blocking=True)
+                        got[b].record(rs)
 
             for b in range(2):  # warm both graphs once
                 upload(b, False)
@@ -721,7 +740,7 @@ def main():
                 if i + 1 < args.steps:
                     upload((i + 1) % 2, i >= 1)
                     launch(i + 1)
-                done[i % 2].synchronize()
+                got[i % 2].synchronize()
                 _ = int(views[i % 2].flat[0])
         else:
             io_graphs[0].replay()
@@ -747,7 +766,9 @@ def main():
                          "back to back, two in flight, every result waited for and read on "
                          "the host (no L2 flush: each step streams over 3x L2)"
                        + ("; inputs double-buffered on the device, each step's upload on a "
-                          "copy stream overlapping the step before" if overlap else "")
+                          "copy stream overlapping the step before"
+                          + ("" if direct_out else ", olat double-buffered and read back "
+                             "on a second copy stream") if overlap else "")
                        + "; latency_*: one step at a time from an idle GPU and a flushed L2"}
 
     if rank != 0:
