@@ -13,10 +13,10 @@
 // (64 heads x 512, 64 KB), one 128-token latent tile (128 KB) and P^T (16 KB); there
 // is no room for a second tile, so the tile is refilled a quarter (two 64-column
 // atoms, the rows of one O^T tile) at a time, as soon as the MMAs of the previous
-// chunk are done with that quarter. Roles (eight warps):
+// chunk are done with that quarter. Roles (sixteen warps):
 //   - warp 0 resolves each chunk's token ids to cache rows, two chunks ahead, into a
 //     double buffer, and loads each unit's Q by TMA once the last unit's QK is done;
-//   - warps 6-7 gather: per quarter, 128 tokens x 256 bytes with cp.async into the
+//   - warps 2-3 and 12-15 gather: per quarter, 128 tokens x 256 bytes with cp.async into the
 //     128-byte-swizzled atoms, each thread's copies completing on the quarter's
 //     mbarrier (cp.async.mbarrier.arrive.noinc), so the warps run ahead freely;
 //   - warp 1 (one lane) issues the MMAs, accumulators in tensor memory:
@@ -24,9 +24,9 @@
 //       O^T += V^T P^T  M = 512 latent (four tiles of 128, tile i = quarter i read
 //       MN-major), N = 64 heads, K = 128 tokens; each tile's completion frees its
 //       quarter for the next chunk's gather;
-//   - warps 2-5 (one tensor-memory lane, i.e. one token, per thread) take S^T, find
-//     each head's chunk maximum (redux.sync, then across the four warps through
-//     shared memory), move the running maximum only when it grows by more than 2^8
+//   - warps 4-11 (one tensor-memory lane, i.e. one token, and half of the heads per
+//     thread: two warps per lane quarter) take S^T, find each head's chunk maximum
+//     (redux.sync, then across the four lane quarters through shared memory), move the running maximum only when it grows by more than 2^8
 //     (then O^T and the partial sums are rescaled), write P^T in bf16, and at the end
 //     of a unit write its partial (or, with one split, olat) and free O^T.
 // All waits are bounded; a timeout sets DSA_STATUS_TIMEOUT, every role leaves its
@@ -75,8 +75,18 @@ constexpr uint32_t kOffMisc = kOffBar + kBars * 8;
 constexpr uint32_t kBytes = kOffMisc + 16;
 constexpr uint32_t kDyn = kBytes + 1024;
 constexpr uint32_t kTmemCols = 512;  // S^T: columns [0, 64); O^T tile i: [64 + 64 i, +64)
-constexpr int kThreads = 256;
-constexpr int kGatherThreads = 64;   // warps 6 and 7
+// Four warpgroups. 0: warp 0 token rows and Q, warp 1 MMA issue, warps 2-3 gather;
+// 1 and 2: softmax (warps 4-11, two per tensor-memory lane quarter); 3: gather
+// (warps 12-15). Launched at 128 registers a thread; the softmax warpgroups raise
+// theirs to 192 and the others lower theirs to 64 (setmaxnreg), which adds up to
+// the launch's 512 x 128 exactly, in every SM sub-partition too (one warp of each
+// warpgroup per sub-partition).
+constexpr int kSoftWarps = 8;
+constexpr int kGatherWarps = 6;
+constexpr int kThreads = 16 * 32;
+constexpr int kGatherThreads = kGatherWarps * 32;
+constexpr int kRegLow = 64, kRegHigh = 192;
+static_assert(2 * kRegLow + 2 * kRegHigh == 4 * 128, "register split");
 constexpr float kLazy = 8.f;         // log2 units the running max may lag behind
 static_assert(kDyn <= 227 * 1024, "tcgen05 attention shared memory");
 static_assert(kOffBar % 8 == 0, "mbarrier alignment");
@@ -111,8 +121,9 @@ __device__ __forceinline__ Unit unit_of(const MlaTcParams& a, int u) {
 __device__ __forceinline__ void gather_quarter(uint32_t lat, const int* rows, const uint16_t* ckv,
                                                int q, int g) {
 #pragma unroll 8
-    for (int m = 0; m < 32; ++m) {
+    for (int m = 0; m < (2048 + kGatherThreads - 1) / kGatherThreads; ++m) {
         const int idx = g + kGatherThreads * m;
+        if (idx >= 2048) break;
         const int j = idx >> 4, at = 2 * q + ((idx >> 3) & 1), c = idx & 7;
         const uint16_t* src = ckv + (long long)rows[j] * kKVL + at * 64 + c * 8;
         cp_async16(lat + at * kLatAtom + j * 128 + ((c ^ (j & 7)) << 4), src, 16);
@@ -143,19 +154,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bars + Q_EMPTY, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bars + ROWS_FULL + b, 1);
-            mbar_init(bars + ROWS_EMPTY + b, 6);
-            mbar_init(bars + RED + b, 4);
+            mbar_init(bars + ROWS_EMPTY + b, kGatherWarps + kSoftWarps);
+            mbar_init(bars + RED + b, kSoftWarps);
         }
         for (int q = 0; q < kQuarters; ++q) {
             mbar_init(bars + LAT_FULL + q, kGatherThreads);
             mbar_init(bars + LAT_EMPTY + q, 1);
         }
         mbar_init(bars + S_FULL, 1);
-        mbar_init(bars + P_FULL, 4);
+        mbar_init(bars + P_FULL, kSoftWarps);
         mbar_init(bars + O_DONE, 1);
-        mbar_init(bars + O_FREE, 4);
-        mbar_init(bars + SUM_IN, 4);
-        mbar_init(bars + SUM_OUT, 4);
+        mbar_init(bars + O_FREE, kSoftWarps);
+        mbar_init(bars + SUM_IN, kSoftWarps);
+        mbar_init(bars + SUM_OUT, kSoftWarps);
         mbar_init(bars + DRAIN, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -175,7 +186,239 @@ __global__ void __launch_bounds__(kThreads, 1)
         return __shfl_sync(0xffffffffu, got, 0) != 0;
     };
 
-    if (warp == 0) {
+    // Register split by warpgroup: the softmax warpgroups (warps 4-11) raise their
+    // registers, the other two lower theirs; each instruction is executed by whole
+    // warpgroups.
+    if (warp >= 4 && warp < 12) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegHigh));
+        // ---- softmax and epilogue: thread j owns token j of a chunk (tensor lane j)
+        // and one half of the heads (h0 .. h0 + 31); two warps share each lane quarter ----
+        const int qd = warp & 3;
+        const int h0 = 32 * ((warp - 4) >> 2);
+        const int j = 32 * qd + lane;
+        const uint32_t lrow = (uint32_t)(32 * qd) << 16;
+        const float NEG_INF = __int_as_float(0xff800000);
+        int n = 0, k = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const Unit w = unit_of(a, u);
+            const long long pbase = ((long long)w.r * a.ns + w.split) * kH;
+            if (w.nch == 0) {
+                // no tokens: zero output, (m, l) = (-inf, 0)
+                if (a.ns > 1 && qd == 0)
+                    *reinterpret_cast<float2*>(a.part_ml + (pbase + h0 + lane) * 2) =
+                        make_float2(NEG_INF, 0.f);
+                for (int h = h0; h < h0 + 32; ++h)
+                    for (int i = 0; i < kQuarters; ++i) {
+                        const int cidx = 128 * i + j;
+                        if (a.ns > 1) {
+                            a.part_o[(pbase + h) * kKVL + cidx] = 0.f;
+                        } else {
+                            const long long oi = ((long long)w.r * kH + h) * kKVL + cidx;
+                            if (a.olat) a.olat[oi] = 0.f;
+                            if (a.xbf) a.xbf[oi] = 0;
+                        }
+                    }
+                continue;
+            }
+            // Running maxima (identical in every thread) live in msm[n & 1] during
+            // chunk n; the chunk's new ones go to msm[(n + 1) & 1].
+            float lacc[32];
+#pragma unroll
+            for (int h = 0; h < 32; ++h) lacc[h] = 0.f;
+            for (int c = 0; c < w.nch; ++c, ++n) {
+                const int b = n & 1;
+                if (!bwait(ROWS_FULL + b, (uint32_t)((n >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const bool valid = mask[b * kT + j] != 0;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars + ROWS_EMPTY + b);
+                if (!bwait(S_FULL, (uint32_t)(n & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // chunk maximum per head: over the warp, then over the four lane quarters
+                float* rb = red + b * 4 * kH;
+                {
+                    uint32_t sv[32];
+                    tc_ld32(sv, tmem + lrow + h0);
+                    tc_wait_ld(sv);
+                    float4* dst = reinterpret_cast<float4*>(rb + qd * kH + h0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float4 m4;
+                        m4.x = warp_max(valid ? __uint_as_float(sv[4 * i]) * a.sl2 : NEG_INF);
+                        m4.y = warp_max(valid ? __uint_as_float(sv[4 * i + 1]) * a.sl2 : NEG_INF);
+                        m4.z = warp_max(valid ? __uint_as_float(sv[4 * i + 2]) * a.sl2 : NEG_INF);
+                        m4.w = warp_max(valid ? __uint_as_float(sv[4 * i + 3]) * a.sl2 : NEG_INF);
+                        if (lane == 0) dst[i] = m4;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars + RED + b);
+                if (!bwait(RED + b, (uint32_t)((n >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                // new running maxima of this half (lagging by at most kLazy) into cm
+                float cm[32];
+                {
+                    const float4* r4 = reinterpret_cast<const float4*>(rb + h0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 w0 = r4[i], w1 = r4[kH / 4 + i], w2 = r4[2 * (kH / 4) + i],
+                                     w3 = r4[3 * (kH / 4) + i];
+                        cm[4 * i] = fmaxf(fmaxf(w0.x, w1.x), fmaxf(w2.x, w3.x));
+                        cm[4 * i + 1] = fmaxf(fmaxf(w0.y, w1.y), fmaxf(w2.y, w3.y));
+                        cm[4 * i + 2] = fmaxf(fmaxf(w0.z, w1.z), fmaxf(w2.z, w3.z));
+                        cm[4 * i + 3] = fmaxf(fmaxf(w0.w, w1.w), fmaxf(w2.w, w3.w));
+                    }
+                }
+                const float* mold = msm + b * kH + h0;  // read only when c > 0
+                bool resc = false;
+#pragma unroll
+                for (int h = 0; h < 32; ++h) {
+                    const float mo = c > 0 ? mold[h] : NEG_INF;
+                    const bool up = mo != NEG_INF && cm[h] > mo + kLazy;
+                    resc = resc || up;
+                    cm[h] = (mo == NEG_INF || up) ? cm[h] : mo;
+                }
+                if (resc) {
+                    // O^T through the previous chunk is complete: S_FULL of this chunk
+                    // was committed after that chunk's PV.
+#pragma unroll 1
+                    for (int i = 0; i < kQuarters; ++i) {
+                        uint32_t v[32];
+                        const uint32_t addr = tmem + lrow + 64 + 64 * i + h0;
+                        tc_ld32(v, addr);
+                        tc_wait_ld(v);
+#pragma unroll
+                        for (int kk = 0; kk < 32; ++kk) {
+                            const float f = mold[kk] == NEG_INF ? 1.f : exp2f(mold[kk] - cm[kk]);
+                            v[kk] = __float_as_uint(__uint_as_float(v[kk]) * f);
+                        }
+                        tc_st32(addr, v);
+                    }
+                    tc_wait_st();
+                }
+                if (c > 0) {
+#pragma unroll
+                    for (int h = 0; h < 32; ++h)
+                        if (mold[h] != NEG_INF && cm[h] != mold[h]) lacc[h] *= exp2f(mold[h] - cm[h]);
+                }
+                if (lane == 0) {  // both warps of a half write the same values
+                    float4* mn4 = reinterpret_cast<float4*>(msm + (b ^ 1) * kH + h0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        mn4[i] = make_float4(cm[4 * i], cm[4 * i + 1], cm[4 * i + 2], cm[4 * i + 3]);
+                }
+                // probabilities (scores read again from tensor memory) into row j of P^T
+                {
+                    uint32_t sv[32];
+                    tc_ld32(sv, tmem + lrow + h0);
+                    tc_wait_ld(sv);
+                    uint4* prow = reinterpret_cast<uint4*>(sP + j * 128);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {  // heads h0 + 8q .. +7 -> one 16-byte chunk
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int h = 8 * q + 2 * e;
+                            const float x0 = __uint_as_float(sv[h]) * a.sl2;
+                            const float x1 = __uint_as_float(sv[h + 1]) * a.sl2;
+                            const float p0 = (valid && cm[h] != NEG_INF) ? exp2f(x0 - cm[h]) : 0.f;
+                            const float p1 =
+                                (valid && cm[h + 1] != NEG_INF) ? exp2f(x1 - cm[h + 1]) : 0.f;
+                            lacc[h] += p0;
+                            lacc[h + 1] += p1;
+                            pk[e] = pack_bf16x2(p0, p1);
+                        }
+                        prow[((h0 >> 3) + q) ^ (j & 7)] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars + P_FULL);
+            }
+            if (!ok) break;
+
+            // ---- epilogue of the unit ----
+            if (!bwait(O_DONE, (uint32_t)(k & 1))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // head sums: reduce-scatter over the warp (lane l ends with head h0 + l),
+            // then over the four lane quarters through shared memory
+            float v32[32];
+#pragma unroll
+            for (int h = 0; h < 32; ++h) v32[h] = lacc[h];
+#pragma unroll
+            for (int ww = 16, m = 16; m >= 1; ww >>= 1, m >>= 1) {
+#pragma unroll
+                for (int i = 0; i < ww; ++i) {
+                    const bool hi = (lane & m) != 0;
+                    const float send = hi ? v32[i] : v32[ww + i];
+                    const float recv = __shfl_xor_sync(0xffffffffu, send, m);
+                    v32[i] = (hi ? v32[ww + i] : v32[i]) + recv;
+                }
+            }
+            // the sums buffer is free once every warp has read the last unit's sums
+            if (k > 0 && !bwait(SUM_OUT, (uint32_t)((k - 1) & 1))) {
+                ok = false;
+                break;
+            }
+            sums[qd * kH + h0 + lane] = v32[0];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + SUM_IN);
+            if (!bwait(SUM_IN, (uint32_t)(k & 1))) {
+                ok = false;
+                break;
+            }
+            if (a.ns > 1 && qd == 0) {  // lane l writes head h0 + l's (m, l)
+                const int hd = h0 + lane;
+                const float mj = msm[(n & 1) * kH + hd];  // the last chunk's new maxima
+                const float ls = (sums[hd] + sums[kH + hd]) + (sums[2 * kH + hd] + sums[3 * kH + hd]);
+                *reinterpret_cast<float2*>(a.part_ml + (pbase + hd) * 2) = make_float2(mj, ls);
+            }
+#pragma unroll 1
+            for (int i = 0; i < kQuarters; ++i) {
+                const int cidx = 128 * i + j;  // latent column = tensor lane of tile i
+                uint32_t v[32];
+                tc_ld32(v, tmem + lrow + 64 + 64 * i + h0);
+                tc_wait_ld(v);
+#pragma unroll
+                for (int kk = 0; kk < 32; ++kk) {
+                    const int h = h0 + kk;
+                    const float o = __uint_as_float(v[kk]);
+                    if (a.ns > 1) {
+                        a.part_o[(pbase + h) * kKVL + cidx] = o;
+                    } else {
+                        const float ls =
+                            (sums[h] + sums[kH + h]) + (sums[2 * kH + h] + sums[3 * kH + h]);
+                        const float val = ls > 0.f ? o / ls : 0.f;
+                        const long long oi = ((long long)w.r * kH + h) * kKVL + cidx;
+                        if (a.olat) a.olat[oi] = val;
+                        if (a.xbf) a.xbf[oi] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+                    }
+                }
+            }
+            // O^T is read: the next unit's first PV may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bars + O_FREE);
+                mbar_arrive(bars + SUM_OUT);
+            }
+            ++k;
+        }
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegLow));
+        if (warp == 0) {
         // ---- token rows (two chunks ahead) and each unit's Q ----
         int n = 0, k = 0;
         bool ok = true;
@@ -243,35 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // drain: the last Q copy issued has landed before the CTA may exit
         if (lane == 0 && k > 0) mbar_wait(bars + Q_FULL, (uint32_t)((k - 1) & 1));
-    } else if (warp >= 6) {
-        // ---- gather: quarters of each chunk as the previous chunk's PV frees them ----
-        const int g = threadIdx.x - 6 * 32;
-        const uint32_t lat = smem_u32(sLat);
-        int n = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            const Unit w = unit_of(a, u);
-            for (int c = 0; c < w.nch; ++c, ++n) {
-                const int b = n & 1;
-                if (!bwait(ROWS_FULL + b, (uint32_t)((n >> 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                for (int q = 0; q < kQuarters && ok; ++q) {
-                    if (!bwait(LAT_EMPTY + q, (uint32_t)(n & 1) ^ 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    gather_quarter(lat, rows + b * kT, a.ckv, q, g);
-                    cp_async_arrive_noinc(bars + LAT_FULL + q);
-                }
-                if (!ok) break;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars + ROWS_EMPTY + b);
-            }
-        }
-        cp_async_wait_all();  // drain
-    } else if (warp == 1) {
+        } else if (warp == 1) {
         // ---- MMA issuer ----
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16(kT, kH);
@@ -334,243 +549,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(bars + DRAIN);
             mbar_wait(bars + DRAIN, 0);
         }
-    } else {
-        // ---- softmax and epilogue: thread j owns token j of a chunk (tensor lane j) ----
-        const int qd = warp & 3;
-        const int j = 32 * qd + lane;
-        const uint32_t lrow = (uint32_t)(32 * qd) << 16;
-        const float NEG_INF = __int_as_float(0xff800000);
-        int n = 0, k = 0;
+        } else {
+        // ---- gather: quarters of each chunk as the previous chunk's PV frees them ----
+        const int g = (warp < 4 ? warp - 2 : warp - 10) * 32 + lane;
+        const uint32_t lat = smem_u32(sLat);
+        int n = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const Unit w = unit_of(a, u);
-            const long long pbase = ((long long)w.r * a.ns + w.split) * kH;
-            if (w.nch == 0) {
-                // no tokens: zero output, (m, l) = (-inf, 0)
-                if (a.ns > 1 && j < kH)
-                    *reinterpret_cast<float2*>(a.part_ml + (pbase + j) * 2) = make_float2(NEG_INF, 0.f);
-                for (int h = 0; h < kH; ++h)
-                    for (int i = 0; i < kQuarters; ++i) {
-                        const int cidx = 128 * i + j;
-                        if (a.ns > 1) {
-                            a.part_o[(pbase + h) * kKVL + cidx] = 0.f;
-                        } else {
-                            const long long oi = ((long long)w.r * kH + h) * kKVL + cidx;
-                            if (a.olat) a.olat[oi] = 0.f;
-                            if (a.xbf) a.xbf[oi] = 0;
-                        }
-                    }
-                continue;
-            }
-            // Running maxima (identical in every thread) live in msm[n & 1] during
-            // chunk n; the chunk's new ones go to msm[(n + 1) & 1].
-            float lacc[kH];
-#pragma unroll
-            for (int h = 0; h < kH; ++h) lacc[h] = 0.f;
             for (int c = 0; c < w.nch; ++c, ++n) {
                 const int b = n & 1;
                 if (!bwait(ROWS_FULL + b, (uint32_t)((n >> 1) & 1))) {
                     ok = false;
                     break;
                 }
-                const bool valid = mask[b * kT + j] != 0;
+                for (int q = 0; q < kQuarters && ok; ++q) {
+                    if (!bwait(LAT_EMPTY + q, (uint32_t)(n & 1) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    gather_quarter(lat, rows + b * kT, a.ckv, q, g);
+                    cp_async_arrive_noinc(bars + LAT_FULL + q);
+                }
+                if (!ok) break;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars + ROWS_EMPTY + b);
-                if (!bwait(S_FULL, (uint32_t)(n & 1))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // chunk maximum per head: over the warp, then over the four warps
-                float* rb = red + b * 4 * kH;
-                {
-                    uint32_t sv[2][32];
-                    tc_ld32(sv[0], tmem + lrow);
-                    tc_ld32(sv[1], tmem + lrow + 32);
-                    tc_wait_ld(sv[0]);
-                    tc_tie(sv[1]);
-                    float4* dst = reinterpret_cast<float4*>(rb + qd * kH);
-#pragma unroll
-                    for (int i = 0; i < kH / 4; ++i) {
-                        float4 m4;
-                        m4.x = warp_max(valid ? __uint_as_float(sv[i >> 3][(4 * i) & 31]) * a.sl2
-                                              : NEG_INF);
-                        m4.y = warp_max(valid ? __uint_as_float(sv[i >> 3][(4 * i + 1) & 31]) * a.sl2
-                                              : NEG_INF);
-                        m4.z = warp_max(valid ? __uint_as_float(sv[i >> 3][(4 * i + 2) & 31]) * a.sl2
-                                              : NEG_INF);
-                        m4.w = warp_max(valid ? __uint_as_float(sv[i >> 3][(4 * i + 3) & 31]) * a.sl2
-                                              : NEG_INF);
-                        if (lane == 0) dst[i] = m4;
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars + RED + b);
-                if (!bwait(RED + b, (uint32_t)((n >> 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                // new running maxima (lagging by at most kLazy) into cm
-                float cm[kH];
-                {
-                    const float4* r4 = reinterpret_cast<const float4*>(rb);
-#pragma unroll
-                    for (int i = 0; i < kH / 4; ++i) {
-                        const float4 w0 = r4[i], w1 = r4[kH / 4 + i], w2 = r4[2 * (kH / 4) + i],
-                                     w3 = r4[3 * (kH / 4) + i];
-                        cm[4 * i] = fmaxf(fmaxf(w0.x, w1.x), fmaxf(w2.x, w3.x));
-                        cm[4 * i + 1] = fmaxf(fmaxf(w0.y, w1.y), fmaxf(w2.y, w3.y));
-                        cm[4 * i + 2] = fmaxf(fmaxf(w0.z, w1.z), fmaxf(w2.z, w3.z));
-                        cm[4 * i + 3] = fmaxf(fmaxf(w0.w, w1.w), fmaxf(w2.w, w3.w));
-                    }
-                }
-                const float* mold = msm + b * kH;  // read only when c > 0
-                bool resc = false;
-#pragma unroll
-                for (int h = 0; h < kH; ++h) {
-                    const float mo = c > 0 ? mold[h] : NEG_INF;
-                    const bool up = mo != NEG_INF && cm[h] > mo + kLazy;
-                    resc = resc || up;
-                    cm[h] = (mo == NEG_INF || up) ? cm[h] : mo;
-                }
-                if (resc) {
-                    // O^T through the previous chunk is complete: S_FULL of this chunk
-                    // was committed after that chunk's PV.
-#pragma unroll 1
-                    for (int i = 0; i < kQuarters; ++i) {
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            uint32_t v[32];
-                            const uint32_t addr = tmem + lrow + 64 + 64 * i + 32 * hh;
-                            tc_ld32(v, addr);
-                            tc_wait_ld(v);
-#pragma unroll
-                            for (int kk = 0; kk < 32; ++kk) {
-                                const int h = 32 * hh + kk;
-                                const float f = mold[h] == NEG_INF ? 1.f : exp2f(mold[h] - cm[h]);
-                                v[kk] = __float_as_uint(__uint_as_float(v[kk]) * f);
-                            }
-                            tc_st32(addr, v);
-                        }
-                    }
-                    tc_wait_st();
-                }
-                if (c > 0) {
-#pragma unroll
-                    for (int h = 0; h < kH; ++h)
-                        if (mold[h] != NEG_INF && cm[h] != mold[h]) lacc[h] *= exp2f(mold[h] - cm[h]);
-                }
-                if (lane == 0) {  // every warp writes the same values
-                    float4* mn4 = reinterpret_cast<float4*>(msm + (b ^ 1) * kH);
-#pragma unroll
-                    for (int i = 0; i < kH / 4; ++i)
-                        mn4[i] = make_float4(cm[4 * i], cm[4 * i + 1], cm[4 * i + 2], cm[4 * i + 3]);
-                }
-                // probabilities (scores read again from tensor memory) as P^T row j in bf16
-                {
-                    uint32_t sv[2][32];
-                    tc_ld32(sv[0], tmem + lrow);
-                    tc_ld32(sv[1], tmem + lrow + 32);
-                    tc_wait_ld(sv[0]);
-                    tc_tie(sv[1]);
-                    uint4* prow = reinterpret_cast<uint4*>(sP + j * 128);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {  // heads 8q .. 8q+7 -> one 16-byte chunk
-                        uint32_t pk[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int h = 8 * q + 2 * e;
-                            const float x0 = __uint_as_float(sv[h >> 5][h & 31]) * a.sl2;
-                            const float x1 = __uint_as_float(sv[(h + 1) >> 5][(h + 1) & 31]) * a.sl2;
-                            const float p0 = (valid && cm[h] != NEG_INF) ? exp2f(x0 - cm[h]) : 0.f;
-                            const float p1 =
-                                (valid && cm[h + 1] != NEG_INF) ? exp2f(x1 - cm[h + 1]) : 0.f;
-                            lacc[h] += p0;
-                            lacc[h + 1] += p1;
-                            pk[e] = pack_bf16x2(p0, p1);
-                        }
-                        prow[q ^ (j & 7)] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    }
-                }
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars + P_FULL);
             }
-            if (!ok) break;
-
-            // ---- epilogue of the unit ----
-            if (!bwait(O_DONE, (uint32_t)(k & 1))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // head sums: reduce-scatter over the warp (lane l ends with heads 2l, 2l+1),
-            // then over the four warps through shared memory
-            float v64[kH];
-#pragma unroll
-            for (int h = 0; h < kH; ++h) v64[h] = lacc[h];
-#pragma unroll
-            for (int ww = kH / 2, m = 16; m >= 1; ww >>= 1, m >>= 1) {
-#pragma unroll
-                for (int i = 0; i < ww; ++i) {
-                    const bool hi = (lane & m) != 0;
-                    const float send = hi ? v64[i] : v64[ww + i];
-                    const float recv = __shfl_xor_sync(0xffffffffu, send, m);
-                    v64[i] = (hi ? v64[ww + i] : v64[i]) + recv;
-                }
-            }
-            // the sums buffer is free once every warp has read the last unit's sums
-            if (k > 0 && !bwait(SUM_OUT, (uint32_t)((k - 1) & 1))) {
-                ok = false;
-                break;
-            }
-            sums[qd * kH + 2 * lane] = v64[0];
-            sums[qd * kH + 2 * lane + 1] = v64[1];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars + SUM_IN);
-            if (!bwait(SUM_IN, (uint32_t)(k & 1))) {
-                ok = false;
-                break;
-            }
-            if (a.ns > 1 && j < kH) {  // thread j writes head j's (m, l)
-                const float mj = msm[(n & 1) * kH + j];  // the last chunk's new maxima
-                const float ls = (sums[j] + sums[kH + j]) + (sums[2 * kH + j] + sums[3 * kH + j]);
-                *reinterpret_cast<float2*>(a.part_ml + (pbase + j) * 2) = make_float2(mj, ls);
-            }
-#pragma unroll 1
-            for (int i = 0; i < kQuarters; ++i) {
-                const int cidx = 128 * i + j;  // latent column = tensor lane of tile i
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t v[32];
-                    tc_ld32(v, tmem + lrow + 64 + 64 * i + 32 * hh);
-                    tc_wait_ld(v);
-#pragma unroll
-                    for (int kk = 0; kk < 32; ++kk) {
-                        const int h = 32 * hh + kk;
-                        const float o = __uint_as_float(v[kk]);
-                        if (a.ns > 1) {
-                            a.part_o[(pbase + h) * kKVL + cidx] = o;
-                        } else {
-                            const float ls = (sums[h] + sums[kH + h]) +
-                                             (sums[2 * kH + h] + sums[3 * kH + h]);
-                            const float val = ls > 0.f ? o / ls : 0.f;
-                            const long long oi = ((long long)w.r * kH + h) * kKVL + cidx;
-                            if (a.olat) a.olat[oi] = val;
-                            if (a.xbf) a.xbf[oi] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-                        }
-                    }
-                }
-            }
-            // O^T is read: the next unit's first PV may overwrite it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bars + O_FREE);
-                mbar_arrive(bars + SUM_OUT);
-            }
-            ++k;
+        }
+        cp_async_wait_all();  // drain
         }
     }
 
