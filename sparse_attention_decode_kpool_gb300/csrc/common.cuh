@@ -98,6 +98,7 @@ struct MlaTcParams {
     float sl2;  // softmax_scale * log2(e)
 };
 bool mla_tc_supported(int heads, int kv_lora_rank);
+int mla_tc_mode();  // 1 / 0: forced on / off by DSA_MLA_TC; -1: by size
 int mla_tc_chunk();  // tokens per chunk: split sizes are rounded to it
 int mla_tc_launch(const MlaTcParams& a, long long ckv_rows, cudaStream_t st);
 

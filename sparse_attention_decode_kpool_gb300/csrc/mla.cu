@@ -600,7 +600,7 @@ __global__ void ysum_kernel(const float* __restrict__ ypart, int KS, long long n
 // Launch plan (shared by the workspace query and the call).
 
 struct Plan {
-    bool tc;  // the tensor-core split kernel (mla_tc.cu) for 64 heads
+    bool tc;  // the tensor-core split kernel (mla_tc.cu): 64 heads, large batches
     int mt;
     int hgroups;
     int ns;
@@ -617,7 +617,12 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms,
                bool fp8 = false) {
     Plan p;
-    p.tc = !fp8 && mla_tc_supported(heads, KVL);
+    // The tensor-core kernel for 64 heads when the batch holds at least 16 of its
+    // 128-token chunks per SM (a prefill chunk), the mma.sync kernel otherwise.
+    const int tc_mode = mla_tc_mode();
+    const long long tc_chunks = (long long)rows * ((ow + mla_tc_chunk() - 1) / mla_tc_chunk());
+    p.tc = !fp8 && mla_tc_supported(heads, KVL) &&
+           (tc_mode == 1 || (tc_mode < 0 && tc_chunks >= 16LL * sms));
     p.mt = heads <= 16 ? 1 : heads <= 32 ? 2 : 4;
     p.hgroups = p.tc ? 1 : (heads + 16 * p.mt - 1) / (16 * p.mt);
     const int chunk = p.tc ? mla_tc_chunk() : CH;

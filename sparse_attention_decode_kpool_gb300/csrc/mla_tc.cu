@@ -590,15 +590,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-// Opt-in (DSA_MLA_TC=1, 64 heads). Not faster than the mma.sync split kernel at the
-// sizes measured: a phase probe at 4,096 rows x 2,048 tokens shows about 11.6 us per
-// chunk, of which the gather of the 128 KB tile takes 5.7 us (cp.async reaches about
-// 25 GB/s per SM) and the softmax 4.8 us, with the tensor pipe busy about 1.5 us;
-// with one tile in shared memory the gather cannot overlap the softmax.
-bool mla_tc_supported(int heads, int kv_lora_rank) {
-    if (heads != kH || kv_lora_rank != kKVL) return false;
+// The tensor-core kernel serves 64 heads of a 512-wide latent. It is chosen for
+// large batches (see make_plan): with many 128-token chunks per SM (a prefill chunk
+// of 4,096 rows: 3.52 ms against 3.96 ms for the mma.sync kernel) its gather and
+// softmax overlap its MMAs; at decode sizes (one or a few chunks per CTA) the
+// mma.sync kernel is faster (8 rows: 34.1 against 23.8 us).
+bool mla_tc_supported(int heads, int kv_lora_rank) { return heads == kH && kv_lora_rank == kKVL; }
+
+// DSA_MLA_TC=1 forces the tensor-core kernel where supported, 0 the mma.sync one;
+// unset: chosen by size.
+int mla_tc_mode() {
     const char* v = getenv("DSA_MLA_TC");
-    return v && v[0] == '1';
+    if (v && v[0] == '1') return 1;
+    if (v && v[0] == '0') return 0;
+    return -1;
 }
 
 int mla_tc_chunk() { return kT; }
