@@ -54,7 +54,8 @@ constexpr uint32_t kOffSums = kOffRed + 2 * 4 * kH * 4; // [4 warps][kH] f32 hea
 constexpr uint32_t kOffM = kOffSums + 4 * kH * 4;       // [2][kH] running maxima
 constexpr uint32_t kOffRows = kOffM + 2 * kH * 4;       // [2][kT] cache row per token
 constexpr uint32_t kOffMask = kOffRows + 2 * kT * 4;    // [2][kT] token valid
-constexpr uint32_t kOffBar = kOffMask + 2 * kT;
+constexpr uint32_t kOffFlag = kOffMask + 2 * kT;      // [2][8 softmax warps] maxima written
+constexpr uint32_t kOffBar = kOffFlag + 2 * 8 * 4;
 // mbarriers
 constexpr int Q_FULL = 0;         // Q landed (TMA bytes)
 constexpr int Q_EMPTY = 1;        // the unit's last QK is done with Q (commit)
@@ -139,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sP = smem + kOffP;
     float* red = reinterpret_cast<float*>(smem + kOffRed);
     float* sums = reinterpret_cast<float*>(smem + kOffSums);
+    uint32_t* wflag = reinterpret_cast<uint32_t*>(smem + kOffFlag);
     float* msm = reinterpret_cast<float*>(smem + kOffM);
     int* rows = reinterpret_cast<int*>(smem + kOffRows);
     uint8_t* mask = smem + kOffMask;
@@ -240,12 +242,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                // chunk maximum per head: over the warp, then over the four lane quarters
+                uint32_t sv[32];  // this token's scores for heads h0 .. h0 + 31
+                tc_ld32(sv, tmem + lrow + h0);
+                tc_wait_ld(sv);
+                const float* mold = msm + b * kH + h0;  // running maxima (read when c > 0)
+                // Does any score of this warp move a running maximum (lag above kLazy,
+                // or none yet)? Only such warps publish their chunk maxima: a warp with
+                // no such score cannot change the new maximum of any head.
+                bool mine = c == 0;
+                if (!mine && valid) {
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) {
+                        const float mo = mold[h];
+                        mine = mine || mo == NEG_INF || __uint_as_float(sv[h]) * a.sl2 > mo + kLazy;
+                    }
+                }
+                const bool pub = __any_sync(0xffffffffu, mine);
                 float* rb = red + b * 4 * kH;
-                {
-                    uint32_t sv[32];
-                    tc_ld32(sv, tmem + lrow + h0);
-                    tc_wait_ld(sv);
+                const int sw = warp - 4;  // softmax warp 0..7: lane quarter sw & 3, half sw >> 2
+                if (pub) {
                     float4* dst = reinterpret_cast<float4*>(rb + qd * kH + h0);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
@@ -257,34 +272,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lane == 0) dst[i] = m4;
                     }
                 }
+                if (lane == 0) wflag[b * 8 + sw] = pub ? 1u : 0u;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars + RED + b);
                 if (!bwait(RED + b, (uint32_t)((n >> 1) & 1))) {
                     ok = false;
                     break;
                 }
-                // new running maxima of this half (lagging by at most kLazy) into cm
+                // new running maxima of this half (lagging by at most kLazy) into cm,
+                // from the lane quarters that published
+                const int hw = (sw >> 2) * 4;
+                const bool any = (wflag[b * 8 + hw] | wflag[b * 8 + hw + 1] | wflag[b * 8 + hw + 2] |
+                                  wflag[b * 8 + hw + 3]) != 0u;
                 float cm[32];
-                {
-                    const float4* r4 = reinterpret_cast<const float4*>(rb + h0);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float4 w0 = r4[i], w1 = r4[kH / 4 + i], w2 = r4[2 * (kH / 4) + i],
-                                     w3 = r4[3 * (kH / 4) + i];
-                        cm[4 * i] = fmaxf(fmaxf(w0.x, w1.x), fmaxf(w2.x, w3.x));
-                        cm[4 * i + 1] = fmaxf(fmaxf(w0.y, w1.y), fmaxf(w2.y, w3.y));
-                        cm[4 * i + 2] = fmaxf(fmaxf(w0.z, w1.z), fmaxf(w2.z, w3.z));
-                        cm[4 * i + 3] = fmaxf(fmaxf(w0.w, w1.w), fmaxf(w2.w, w3.w));
-                    }
-                }
-                const float* mold = msm + b * kH + h0;  // read only when c > 0
                 bool resc = false;
+                if (!any) {
 #pragma unroll
-                for (int h = 0; h < 32; ++h) {
-                    const float mo = c > 0 ? mold[h] : NEG_INF;
-                    const bool up = mo != NEG_INF && cm[h] > mo + kLazy;
-                    resc = resc || up;
-                    cm[h] = (mo == NEG_INF || up) ? cm[h] : mo;
+                    for (int h = 0; h < 32; ++h) cm[h] = mold[h];  // c > 0 here
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) cm[h] = NEG_INF;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (wflag[b * 8 + hw + q] == 0u) continue;
+                        const float4* r4 = reinterpret_cast<const float4*>(rb + q * kH + h0);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 w4 = r4[i];
+                            cm[4 * i] = fmaxf(cm[4 * i], w4.x);
+                            cm[4 * i + 1] = fmaxf(cm[4 * i + 1], w4.y);
+                            cm[4 * i + 2] = fmaxf(cm[4 * i + 2], w4.z);
+                            cm[4 * i + 3] = fmaxf(cm[4 * i + 3], w4.w);
+                        }
+                    }
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) {
+                        const float mo = c > 0 ? mold[h] : NEG_INF;
+                        const bool up = mo != NEG_INF && cm[h] > mo + kLazy;
+                        resc = resc || up;
+                        cm[h] = (mo == NEG_INF || up) ? cm[h] : mo;
+                    }
                 }
                 if (resc) {
                     // O^T through the previous chunk is complete: S_FULL of this chunk
@@ -304,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_wait_st();
                 }
-                if (c > 0) {
+                if (any && c > 0) {
 #pragma unroll
                     for (int h = 0; h < 32; ++h)
                         if (mold[h] != NEG_INF && cm[h] != mold[h]) lacc[h] *= exp2f(mold[h] - cm[h]);
@@ -315,11 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 8; ++i)
                         mn4[i] = make_float4(cm[4 * i], cm[4 * i + 1], cm[4 * i + 2], cm[4 * i + 3]);
                 }
-                // probabilities (scores read again from tensor memory) into row j of P^T
+                // probabilities into row j of P^T (bf16)
                 {
-                    uint32_t sv[32];
-                    tc_ld32(sv, tmem + lrow + h0);
-                    tc_wait_ld(sv);
                     uint4* prow = reinterpret_cast<uint4*>(sP + j * 128);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {  // heads h0 + 8q .. +7 -> one 16-byte chunk
