@@ -353,9 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int h = 8 * q + 2 * e;
                             const float x0 = __uint_as_float(sv[h]) * a.sl2;
                             const float x1 = __uint_as_float(sv[h + 1]) * a.sl2;
-                            const float p0 = (valid && cm[h] != NEG_INF) ? exp2f(x0 - cm[h]) : 0.f;
+                            const float p0 = (valid && cm[h] != NEG_INF) ? ex2_sfu(x0 - cm[h]) : 0.f;
                             const float p1 =
-                                (valid && cm[h + 1] != NEG_INF) ? exp2f(x1 - cm[h + 1]) : 0.f;
+                                (valid && cm[h + 1] != NEG_INF) ? ex2_sfu(x1 - cm[h + 1]) : 0.f;
                             lacc[h] += p0;
                             lacc[h + 1] += p1;
                             pk[e] = pack_bf16x2(p0, p1);

@@ -124,6 +124,12 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
         "r"(smem_u32(bar))
         : "memory");
 }
+// 2^x on the special-function unit (one instruction; results below 2^-126 flush to 0).
+__device__ __forceinline__ float ex2_sfu(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float warp_max(float x) {
     float r;
     asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(x));
