@@ -79,14 +79,14 @@ constexpr uint32_t kTmemCols = 512;  // S^T: columns [0, 64); O^T tile i: [64 + 
 // Four warpgroups. 0: warp 0 token rows and Q, warp 1 MMA issue, warps 2-3 gather;
 // 1 and 2: softmax (warps 4-11, two per tensor-memory lane quarter); 3: gather
 // (warps 12-15). Launched at 128 registers a thread; the softmax warpgroups raise
-// theirs to 192 and the others lower theirs to 64 (setmaxnreg), which adds up to
+// theirs to 176 and the others lower theirs to 80 (setmaxnreg), which adds up to
 // the launch's 512 x 128 exactly, in every SM sub-partition too (one warp of each
 // warpgroup per sub-partition).
 constexpr int kSoftWarps = 8;
 constexpr int kGatherWarps = 6;
 constexpr int kThreads = 16 * 32;
 constexpr int kGatherThreads = kGatherWarps * 32;
-constexpr int kRegLow = 64, kRegHigh = 192;
+constexpr int kRegLow = 80, kRegHigh = 176;
 static_assert(2 * kRegLow + 2 * kRegHigh == 4 * 128, "register split");
 constexpr float kLazy = 8.f;         // log2 units the running max may lag behind
 static_assert(kDyn <= 227 * 1024, "tcgen05 attention shared memory");
