@@ -117,18 +117,19 @@ __device__ __forceinline__ Unit unit_of(const MlaTcParams& a, int u) {
 }
 
 // Quarter q of a chunk (atoms 2q, 2q+1: latent columns 128q .. 128q+127 of every
-// token): 2048 copies of 16 bytes, thread g of the 64 gather threads taking g, g+64,
-// ...; a warp's 32 copies are two tokens' 256 contiguous bytes.
+// token): 2048 copies of 16 bytes. The gather threads' count is a multiple of 16, so
+// thread g keeps one (atom, 16-byte chunk) pair, g & 15, and steps over the tokens
+// g / 16, + kGatherThreads / 16, ...; a warp's 32 copies are two tokens' 256
+// contiguous bytes.
+static_assert(kGatherThreads % 16 == 0, "gather threads");
 __device__ __forceinline__ void gather_quarter(uint32_t lat, const int* rows, const uint16_t* ckv,
                                                int q, int g) {
-#pragma unroll 8
-    for (int m = 0; m < (2048 + kGatherThreads - 1) / kGatherThreads; ++m) {
-        const int idx = g + kGatherThreads * m;
-        if (idx >= 2048) break;
-        const int j = idx >> 4, at = 2 * q + ((idx >> 3) & 1), c = idx & 7;
-        const uint16_t* src = ckv + (long long)rows[j] * kKVL + at * 64 + c * 8;
-        cp_async16(lat + at * kLatAtom + j * 128 + ((c ^ (j & 7)) << 4), src, 16);
-    }
+    const int c = g & 7, at = 2 * q + ((g >> 3) & 1);
+    const uint32_t dst0 = lat + at * kLatAtom;
+    const uint16_t* src0 = ckv + at * 64 + c * 8;
+#pragma unroll 4
+    for (int j = g >> 4; j < kT; j += kGatherThreads / 16)
+        cp_async16(dst0 + j * 128 + ((c ^ (j & 7)) << 4), src0 + (long long)rows[j] * kKVL, 16);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
