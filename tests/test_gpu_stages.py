@@ -343,8 +343,9 @@ def _token_rows(rng, wl, ow, empty_row=True):
 
 @pytest.fixture(params=["mma", "tcgen05"])
 def mla_kernel(request, monkeypatch):
-    """Both split-attention kernels: the default mma.sync one, and the opt-in tcgen05
-    one (64 heads only; other head counts keep the default)."""
+    """Both split-attention kernels, each forced: the mma.sync one, and the tcgen05
+    one (64 heads only; other head counts keep the mma.sync kernel). Without the
+    variable the library picks by batch size."""
     monkeypatch.setenv("DSA_MLA_TC", "1" if request.param == "tcgen05" else "0")
     return request.param
 
