@@ -453,6 +453,17 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
         return;
     }
     for (int r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        // this CTA's next row streams into L2 while this one is selected
+        const int rn = r + (int)gridDim.x;
+        if (threadIdx.x == 0 && rn < a.rows) {
+            const float* nxt = a.scores + (long long)rn * a.p_stride;
+            const uintptr_t lo = ((uintptr_t)nxt + 15u) & ~(uintptr_t)15u;
+            const uintptr_t hi = ((uintptr_t)(nxt + a.p_stride)) & ~(uintptr_t)15u;
+            if (hi > lo)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo),
+                             "r"((uint32_t)(hi - lo))
+                             : "memory");
+        }
         select_row(a, cluster, r, keys, sc);
         __syncthreads();  // the next row reuses keys[] and the scratch
     }
