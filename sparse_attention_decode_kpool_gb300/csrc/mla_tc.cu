@@ -127,9 +127,14 @@ __device__ __forceinline__ void gather_quarter(uint32_t lat, const int* rows, co
     const int c = g & 7, at = 2 * q + ((g >> 3) & 1);
     const uint32_t dst0 = lat + at * kLatAtom;
     const uint16_t* src0 = ckv + at * 64 + c * 8;
-#pragma unroll 4
-    for (int j = g >> 4; j < kT; j += kGatherThreads / 16)
-        cp_async16(dst0 + j * 128 + ((c ^ (j & 7)) << 4), src0 + (long long)rows[j] * kKVL, 16);
+    constexpr int kStep = kGatherThreads / 16;
+    const int j0 = g >> 4;
+#pragma unroll
+    for (int m = 0; m < (kT + kStep - 1) / kStep; ++m) {
+        const int j = j0 + kStep * m;
+        if (j < kT)
+            cp_async16(dst0 + j * 128 + ((c ^ (j & 7)) << 4), src0 + (long long)rows[j] * kKVL, 16);
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
