@@ -16,7 +16,9 @@
 // chunk are done with that quarter. Roles (sixteen warps):
 //   - warp 0 resolves each chunk's token ids to cache rows, two chunks ahead, into a
 //     double buffer, and loads each unit's Q by TMA once the last unit's QK is done;
-//   - warps 2-3 and 12-15 gather: per quarter, 128 tokens x 256 bytes with cp.async into the
+//   - warps 2-3 and 12-15 gather (and so do the softmax warps, each chunk's share
+//     right after their softmax of the chunk before): per quarter, 128 tokens x 256
+//     bytes with cp.async into the
 //     128-byte-swizzled atoms, each thread's copies completing on the quarter's
 //     mbarrier (cp.async.mbarrier.arrive.noinc), so the warps run ahead freely;
 //   - warp 1 (one lane) issues the MMAs, accumulators in tensor memory:
@@ -86,6 +88,9 @@ constexpr int kSoftWarps = 8;
 constexpr int kGatherWarps = 6;
 constexpr int kThreads = 16 * 32;
 constexpr int kGatherThreads = kGatherWarps * 32;
+// The softmax warps gather too: each chunk's share right after their softmax of the
+// chunk before, while the PV that frees the tile runs.
+constexpr int kCopyThreads = (kGatherWarps + kSoftWarps) * 32;
 constexpr int kRegLow = 80, kRegHigh = 176;
 static_assert(2 * kRegLow + 2 * kRegHigh == 4 * 128, "register split");
 constexpr float kLazy = 8.f;         // log2 units the running max may lag behind
@@ -121,13 +126,13 @@ __device__ __forceinline__ Unit unit_of(const MlaTcParams& a, int u) {
 // thread g keeps one (atom, 16-byte chunk) pair, g & 15, and steps over the tokens
 // g / 16, + kGatherThreads / 16, ...; a warp's 32 copies are two tokens' 256
 // contiguous bytes.
-static_assert(kGatherThreads % 16 == 0, "gather threads");
+static_assert(kCopyThreads % 16 == 0, "gather threads");
 __device__ __forceinline__ void gather_quarter(uint32_t lat, const int* rows, const uint16_t* ckv,
                                                int q, int g) {
     const int c = g & 7, at = 2 * q + ((g >> 3) & 1);
     const uint32_t dst0 = lat + at * kLatAtom;
     const uint16_t* src0 = ckv + at * 64 + c * 8;
-    constexpr int kStep = kGatherThreads / 16;
+    constexpr int kStep = kCopyThreads / 16;
     const int j0 = g >> 4;
 #pragma unroll
     for (int m = 0; m < (kT + kStep - 1) / kStep; ++m) {
@@ -166,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bars + RED + b, kSoftWarps);
         }
         for (int q = 0; q < kQuarters; ++q) {
-            mbar_init(bars + LAT_FULL + q, kGatherThreads);
+            mbar_init(bars + LAT_FULL + q, kCopyThreads);
             mbar_init(bars + LAT_EMPTY + q, 1);
         }
         mbar_init(bars + S_FULL, 1);
@@ -241,6 +246,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const bool valid = mask[b * kT + j] != 0;
+                // this warp's share of the chunk's gather, quarter by quarter as the
+                // previous chunk's PV frees them
+                for (int q = 0; q < kQuarters && ok; ++q) {
+                    if (!bwait(LAT_EMPTY + q, (uint32_t)(n & 1) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    gather_quarter(smem_u32(sLat), rows + b * kT, a.ckv, q,
+                                   kGatherThreads + (warp - 4) * 32 + lane);
+                    cp_async_arrive_noinc(bars + LAT_FULL + q);
+                }
+                if (!ok) break;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars + ROWS_EMPTY + b);
                 if (!bwait(S_FULL, (uint32_t)(n & 1))) {
@@ -446,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++k;
         }
+        cp_async_wait_all();  // drain this warp's copies
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegLow));
         if (warp == 0) {
