@@ -13,24 +13,25 @@
 // (64 heads x 512, 64 KB), one 128-token latent tile (128 KB) and P^T (16 KB); there
 // is no room for a second tile, so the tile is refilled a quarter (two 64-column
 // atoms, the rows of one O^T tile) at a time, as soon as the MMAs of the previous
-// chunk are done with that quarter. Roles (sixteen warps):
+// chunk are done with that quarter. Roles (sixteen warps, four warpgroups):
 //   - warp 0 resolves each chunk's token ids to cache rows, two chunks ahead, into a
 //     double buffer, and loads each unit's Q by TMA once the last unit's QK is done;
-//   - warps 2-3 and 12-15 gather (and so do the softmax warps, each chunk's share
+//   - warps 2-3 and 12-15 gather, and so do the softmax warps (each chunk's share
 //     right after their softmax of the chunk before): per quarter, 128 tokens x 256
-//     bytes with cp.async into the
-//     128-byte-swizzled atoms, each thread's copies completing on the quarter's
-//     mbarrier (cp.async.mbarrier.arrive.noinc), so the warps run ahead freely;
+//     bytes with cp.async into the 128-byte-swizzled atoms, each thread's copies
+//     completing on the quarter's mbarrier (cp.async.mbarrier.arrive.noinc);
 //   - warp 1 (one lane) issues the MMAs, accumulators in tensor memory:
 //       S^T = K Q^T   M = 128 tokens, N = 64 heads, K = 512, quarter by quarter;
 //       O^T += V^T P^T  M = 512 latent (four tiles of 128, tile i = quarter i read
 //       MN-major), N = 64 heads, K = 128 tokens; each tile's completion frees its
 //       quarter for the next chunk's gather;
 //   - warps 4-11 (one tensor-memory lane, i.e. one token, and half of the heads per
-//     thread: two warps per lane quarter) take S^T, find each head's chunk maximum
-//     (redux.sync, then across the four lane quarters through shared memory), move the running maximum only when it grows by more than 2^8
-//     (then O^T and the partial sums are rescaled), write P^T in bf16, and at the end
-//     of a unit write its partial (or, with one split, olat) and free O^T.
+//     thread: two warps per lane quarter) take S^T and keep a lazy running maximum
+//     per head: a warp vote asks whether any score moves a maximum by more than 2^8
+//     (or there is none yet); only such warps publish chunk maxima (redux.sync, then
+//     shared memory), and only then are the maxima moved and O^T and the partial sums
+//     rescaled. They write P^T in bf16 (ex2 on the special-function unit) and, at the
+//     end of a unit, its partial (or, with one split, olat), then free O^T.
 // All waits are bounded; a timeout sets DSA_STATUS_TIMEOUT, every role leaves its
 // loops, copies and MMAs in flight are drained, and the tensor memory is released.
 #include <stdlib.h>
