@@ -462,6 +462,25 @@ def test_mla_persistent_many_units(case, mla_kernel):
     H.check_attention(olat.t.cpu().numpy().reshape(wl.rows, -1), np.array(ro), f"{name} olat")
 
 
+def test_mla_empty_token_lists(mla_kernel):
+    """out_width 0: no unit has a chunk; olat and y are exactly zero (R16)."""
+    g = _geom(heads=64, hidden=64, index_topk=64)
+    wl = W.make_workload("empty", 304, g, [3000, 700], with_raw=False)
+    layer = DsaDecodeLayer(wl, keep_olat=True)
+    tok = torch.empty((wl.rows, 0), dtype=torch.int32, device="cuda")
+    olat = H.Guarded((wl.rows, 64, 512), torch.float32, 555.0)
+    y = H.Guarded((wl.rows, g.hidden), torch.bfloat16, 3.0)
+    ws = torch.zeros(max(1, api.dsa_sparse_mla_decode_workspace(wl.rows, 64, 0, g.hidden, True)),
+                     dtype=torch.uint8, device="cuda")
+    api.dsa_sparse_mla_decode(layer.qlat, layer.row_seq, layer.ckv, layer.pg, tok,
+                              g.softmax_scale, layer.o_absorb, y.t, olat.t, layer.status, ws)
+    torch.cuda.synchronize()
+    olat.check()
+    y.check()
+    assert int(layer.status.item()) == 0
+    assert not olat.t.any() and not y.t.float().any()
+
+
 def test_mla_bad_ids_set_status_and_are_skipped():
     g = _geom(heads=8, hidden=64, index_topk=128)
     wl = W.make_workload("bad", 301, g, [500, 200], block_size=64, with_raw=False)
