@@ -358,8 +358,8 @@ int dsa_select_expand_tail(const float* scores, int rows, int p_stride, int inde
  * bf16; olat [rows, heads, kv_lora_rank] f32 (nullable).
  * Limits: kv_lora_rank == 512; hidden % 32 == 0; heads >= 1; qlat, ckv, o_absorb,
  * y, olat and workspace 16-byte aligned (DSA_ERR_INVALID_ARG otherwise).
- * Kernels: with 64 heads and at least 16 chunks of 128 tokens per SM
- * (rows * ceil(out_width / 128) >= 16 * SMs: a prefill chunk) a persistent
+ * Kernels: with 64 heads and at least 4 chunks of 128 tokens per SM
+ * (rows * ceil(out_width / 128) >= 4 * SMs: 64 rows of 2,048 tokens) a persistent
  * tensor-core (tcgen05) kernel runs; otherwise a split kernel on mma.sync and a
  * combine. Each is deterministic; their results agree within rounding, not bit for
  * bit. DSA_MLA_TC=1 / DSA_MLA_TC=0 in the environment forces one or the other (read

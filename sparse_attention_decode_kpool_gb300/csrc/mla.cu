@@ -617,12 +617,13 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms,
                bool fp8 = false) {
     Plan p;
-    // The tensor-core kernel for 64 heads when the batch holds at least 16 of its
-    // 128-token chunks per SM (a prefill chunk), the mma.sync kernel otherwise.
+    // The tensor-core kernel for 64 heads when the batch holds at least 4 of its
+    // 128-token chunks per SM (64 rows of 2,048 tokens, a prefill chunk), the
+    // mma.sync kernel otherwise (decode batches of a few rows).
     const int tc_mode = mla_tc_mode();
     const long long tc_chunks = (long long)rows * ((ow + mla_tc_chunk() - 1) / mla_tc_chunk());
     p.tc = !fp8 && mla_tc_supported(heads, KVL) &&
-           (tc_mode == 1 || (tc_mode < 0 && tc_chunks >= 16LL * sms));
+           (tc_mode == 1 || (tc_mode < 0 && tc_chunks >= 4LL * sms));
     p.mt = heads <= 16 ? 1 : heads <= 32 ? 2 : 4;
     p.hgroups = p.tc ? 1 : (heads + 16 * p.mt - 1) / (16 * p.mt);
     const int chunk = p.tc ? mla_tc_chunk() : CH;

@@ -640,10 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 // The tensor-core kernel serves 64 heads of a 512-wide latent. It is chosen for
-// large batches (see make_plan): with many 128-token chunks per SM (a prefill chunk
-// of 4,096 rows: 3.52 ms against 3.96 ms for the mma.sync kernel) its gather and
-// softmax overlap its MMAs; at decode sizes (one or a few chunks per CTA) the
-// mma.sync kernel is faster (8 rows: 34.1 against 23.8 us).
+// batches with at least 4 of its 128-token chunks per SM (see make_plan): 64 paged
+// rows of 2,048 tokens, 117.4 against 127.4 us for the mma.sync kernel; a prefill
+// chunk of 4,096 rows, 2.79 against 3.96 ms. With one chunk per CTA (decode batches
+// of a few rows) the mma.sync kernel is faster (1 row: 18.0 against 32.4 us).
 bool mla_tc_supported(int heads, int kv_lora_rank) { return heads == kH && kv_lora_rank == kKVL; }
 
 // DSA_MLA_TC=1 forces the tensor-core kernel where supported, 0 the mma.sync one;
