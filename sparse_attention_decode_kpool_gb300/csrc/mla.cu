@@ -636,6 +636,25 @@ Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms,
     const int per = ow > 0 ? (int)((ow + ns - 1) / ns) : 0;
     p.tps = per > 0 ? ((per + chunk - 1) / chunk) * chunk : chunk;
     p.ns = ow > 0 ? (ow + p.tps - 1) / p.tps : 1;
+    if (p.tc && ow > 0) {
+        // Persistent grid: the busiest CTA walks ceil(units / sms) units of
+        // ceil(chunks per row / ns) chunks, plus about a chunk's time per unit (Q,
+        // the epilogue, the partials); take the split count that makes this smallest
+        // (the fewest splits on ties: less to combine).
+        const long long cpr = (ow + chunk - 1) / chunk;
+        long long best = -1;
+        for (long long t = 1; t <= cpr && t <= kMaxSplits; ++t) {
+            const long long tps = ((cpr + t - 1) / t) * chunk;
+            const long long nst = (ow + tps - 1) / tps;
+            const long long cost =
+                ((long long)rows * nst + sms - 1) / sms * ((cpr + nst - 1) / nst + 1);
+            if (best < 0 || cost < best) {
+                best = cost;
+                p.tps = (int)tps;
+                p.ns = (int)nst;
+            }
+        }
+    }
 
     const int nr = rows < 64 ? rows : 64;
     p.gemv_nt = nr <= 8 ? 1 : nr <= 16 ? 2 : nr <= 32 ? 4 : 8;
