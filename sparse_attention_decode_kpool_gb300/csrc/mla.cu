@@ -629,7 +629,8 @@ Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms,
     const int chunk = p.tc ? mla_tc_chunk() : CH;
     const long long base = (long long)rows * p.hgroups;
     const int max_ns = ow > 0 ? (ow + chunk - 1) / chunk : 1;
-    long long ns = base > 0 ? (sms + base - 1) / base : 1;
+    // one CTA per SM: at most sms / base splits keeps the grid to one wave
+    long long ns = base > 0 ? sms / base : 1;
     if (ns < 1) ns = 1;
     if (ns > max_ns) ns = max_ns;
     if (ns > kMaxSplits) ns = kMaxSplits;
