@@ -47,13 +47,14 @@ PREFILL_METRIC = ("DSA chunked-prefill query rows/s (tensor-core index scores + 
 PREFILL_WORKLOAD = 4  # scored on the tensor cores; the o_absorb GEMM is not in its step
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a stage's
-# kernels, from one ncu capture of the current kernels (profiles/<file>); a stage
-# not listed, or whose kernels changed since the capture, reports null. The
-# projection reads all of o_absorb whatever the context length, so its capture at
-# S=32,768 holds for the 262,144-token workload.
+# kernels, from one ncu capture of the current kernels; a stage not listed, or whose
+# kernels changed since the capture, reports null. The projection reads all of
+# o_absorb whatever the context length, so its capture at 8 rows of a 32,768-token
+# context holds for the 262,144-token workload.
 MEASURED_TRAFFIC = {
     "project": (269.730816e6 + 3.598336e6 + 0.733184e6,
-                "project_decode_S32768_b8.md (project_kernel + project_reduce_rows_kernel)"),
+                "ncu: project_kernel + project_reduce_rows_kernel, 8 rows, o_absorb "
+                "4096 x 32768 bf16"),
 }
 FLUSH_BYTES = 256 << 20
 

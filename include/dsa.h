@@ -94,7 +94,36 @@ const char* dsa_last_error(void);
 
 /* ABI version of this header (bumped on any signature change). */
 int dsa_abi_version(void);
-#define DSA_ABI_VERSION 6
+#define DSA_ABI_VERSION 7
+
+/*
+ * Process-wide launch options (no counterpart on the pages: they choose between
+ * equivalent launch forms, for profiling and for tests that pin one kernel). They
+ * are plain values read at each call; the library reads no environment variable.
+ * Set them before enqueueing work that depends on them, and keep
+ * DSA_OPT_MLA_KERNEL fixed between a *_workspace query and the calls that use
+ * that workspace (the kernel choice sizes the workspace).
+ *
+ *   DSA_OPT_PDL         1 (default): every kernel is launched as a programmatic
+ *                       dependent of the work before it on the stream (it still
+ *                       waits for that work before reading its outputs);
+ *                       0: ordinary stream-ordered launches.
+ *   DSA_OPT_MLA_KERNEL  which split kernel the sparse latent attention uses:
+ *                       DSA_MLA_KERNEL_AUTO (default, chosen by size),
+ *                       DSA_MLA_KERNEL_TCGEN05 (the tensor-core kernels wherever
+ *                       they support the shape), DSA_MLA_KERNEL_MMA (the mma.sync
+ *                       split kernel).
+ *
+ * dsa_set_option returns DSA_ERR_INVALID_ARG for an unknown option or value;
+ * dsa_get_option returns the current value, or -1 for an unknown option.
+ */
+#define DSA_OPT_PDL 0
+#define DSA_OPT_MLA_KERNEL 1
+#define DSA_MLA_KERNEL_AUTO 0
+#define DSA_MLA_KERNEL_TCGEN05 1
+#define DSA_MLA_KERNEL_MMA 2
+int dsa_set_option(int option, int value);
+int dsa_get_option(int option);
 
 /*
  * Layer-geometry rules (mod.rs, Glm5NextDsaConfig::validate): index_kpool and
@@ -155,9 +184,10 @@ int dsa_compress_append(const dsa_bf16* k_raw, const dsa_bf16* gate, const uint8
                         int32_t* status, void* stream);
 
 /*
- * dsa_indexer_store -- the decode-time append. mod.rs, Glm5NextDsaKernels:
- * indexer_store copies the staged indexer row to a device-side position and
- * marks it valid. For each sequence b, with t = seq_lens[b] read on the device:
+ * dsa_indexer_store -- the decode-time append (mod.rs, Glm5NextDsaKernels,
+ * indexer_store): the staged row lands at the position the device holds for the
+ * sequence and is flagged valid. For each sequence b, with t = seq_lens[b] read
+ * on the device:
  *
  *   k_raw[b, t, :] = k_new[b, :]     gate[b, t, :] = gate_new[b, :]
  *   token_valid[b, t] = 1            ckv[b, t, :] = ckv_new[b, :]  (when given)
@@ -184,9 +214,10 @@ int dsa_indexer_store(const dsa_bf16* k_new, const dsa_bf16* gate_new, const dsa
                       int32_t* status, void* stream);
 
 /*
- * dsa_write_geom -- mod.rs, Glm5NextDsaKernels: write_geom derives the selector
- * geometry on the device from seq_len, so a captured graph replays over the live
- * context. A decode row sees its whole sequence:
+ * dsa_write_geom -- mod.rs, Glm5NextDsaKernels, write_geom: the selector's
+ * per-row geometry is recomputed on the device from the current lengths, which
+ * keeps one captured graph valid as the sequences grow. A decode row sees its
+ * whole sequence:
  *
  *   row_ctx[r] = seq_lens[row_seq[r]]   (row_seq NULL: seq_lens[r])
  *
@@ -218,9 +249,9 @@ int dsa_decode_append(const dsa_bf16* k_new, const dsa_bf16* gate_new, const dsa
                       int32_t* row_ctx, int32_t* status, void* stream);
 
 /*
- * dsa_score -- dsa_index_scores. tp.rs, "Why the indexer is replicated": the
- * score adds weights[h] * relu(scale * dot) over the indexer heads; build.rs
- * transform 2: w arrives already multiplied by index_heads^-0.5.
+ * dsa_score -- dsa_index_scores (tp.rs, "Why the indexer is replicated": a sum
+ * over the indexer heads of weighted, rectified, scaled dot products; build.rs
+ * transform 2: w arrives already multiplied by index_heads^-0.5).
  *
  *   scores[r, p] = sum_h w[r,h] * relu(scale * <qidx[r,h,:], kpool[p,:]>)
  *
@@ -362,8 +393,7 @@ int dsa_select_expand_tail(const float* scores, int rows, int p_stride, int inde
  * (rows * ceil(out_width / 128) >= 4 * SMs: 64 rows of 2,048 tokens) a persistent
  * tensor-core (tcgen05) kernel runs; otherwise a split kernel on mma.sync and a
  * combine. Each is deterministic; their results agree within rounding, not bit for
- * bit. DSA_MLA_TC=1 / DSA_MLA_TC=0 in the environment forces one or the other (read
- * at each call and at each workspace query: keep it fixed between the two).
+ * bit. The option DSA_OPT_MLA_KERNEL (dsa_set_option) forces one or the other.
  */
 int dsa_sparse_mla_decode_workspace(int rows, int heads, int kv_lora_rank, int out_width,
                                     int hidden, int with_o_absorb, size_t* bytes);

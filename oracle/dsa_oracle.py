@@ -127,10 +127,10 @@ def index_scores(qidx_row, w_row, keys, pool_valid, ctx_len: int, first_key: int
                  kpool: int, scale: float, p_stride: Optional[int] = None) -> np.ndarray:
     """Scores of one query row over one sequence's pools (``dsa_index_scores``).
 
-    tp.rs, "Why the indexer is replicated": ``index_scores`` adds
-    ``weights[h] * relu(scale * dot)`` over the indexer heads; scores are
-    ``[q_rows, n_pools]``. build.rs, transform 2: the kernel does not apply
-    ``index_heads^-0.5``; ``w`` arrives with it folded in.
+    tp.rs, "Why the indexer is replicated": the score of a pool is a sum over the
+    indexer heads of each head's weight times the rectified, scaled dot product,
+    one score per (query row, pool). build.rs, transform 2: ``w`` already carries
+    the ``index_heads^-0.5`` factor, so the score does not apply it again.
 
     ``score[p] = sum_h w[h] * relu(scale * <qidx[h], keys[p]>)`` when pool p is a
     candidate: flagged valid, and visible to this row (its last slot
@@ -195,8 +195,9 @@ def out_width(index_topk: int, kpool: int, always_select_tail: bool = False) -> 
 def expand_selection(pool_ids_row, first_key: int, kpool: int, width: int) -> np.ndarray:
     """``dsa_expand_selection`` for one row: pool ids -> token ids.
 
-    mod.rs "Checkpoint and kernel facts": ``dsa_expand_selection`` writes -1 over
-    the whole index row before it stores any index, so every slot is written.
+    mod.rs "Checkpoint and kernel facts": the expansion first fills the entire
+    index row with -1 and only then stores token ids, so no slot keeps a stale
+    value.
     Pool id ``p`` at position ``j`` becomes tokens ``first_key + p*kpool + s`` at
     positions ``j*kpool + s``.
     """
@@ -298,11 +299,14 @@ def latent_project(olat, o_absorb):
 
 
 def absorb_q(q_b, kv_b, heads: int, nope: int, vd: int, kvl: int, ql: int) -> np.ndarray:
-    """build.rs ``absorb_q``:
-    ``q_absorb[h*kvl + c][k] = sum_r kv_b[h*(nope+vd) + r][c] * q_b[h*nope + r][k]``.
+    """Load-time Q absorption (build.rs module doc, transform 1; ``absorb_q``).
 
-    ``q_b [heads*nope, ql]`` (NoPE: ``qk_head_dim == nope``), ``kv_b
-    [heads*(nope+vd), kvl]``. Returns ``[heads*kvl, ql]``.
+    Head h owns ``nope`` rows of ``q_b`` (Q_h, ``[nope, ql]``) and a block of
+    ``nope + vd`` rows of ``kv_b`` whose first ``nope`` rows form its K half (K_h,
+    ``[nope, kvl]``). The absorbed block of head h is K_h^T Q_h (``[kvl, ql]``), so
+    that ``<q, K_h c> = <K_h^T q, c>`` for a latent row c; the blocks are stacked
+    over heads. ``q_b [heads*nope, ql]`` (NoPE: ``qk_head_dim == nope``),
+    ``kv_b [heads*(nope+vd), kvl]``. Returns ``[heads*kvl, ql]``.
     """
     q_b = np.asarray(q_b, dtype=F64).reshape(heads, nope, ql)
     kv_b = np.asarray(kv_b, dtype=F64).reshape(heads, nope + vd, kvl)
@@ -314,11 +318,13 @@ def absorb_q(q_b, kv_b, heads: int, nope: int, vd: int, kvl: int, ql: int) -> np
 
 
 def absorb_o(o_proj, kv_b, heads: int, nope: int, vd: int, kvl: int, hidden: int) -> np.ndarray:
-    """build.rs ``absorb_o``:
-    ``o_absorb[i][h*kvl + c] = sum_r o_proj[i][h*vd + r] * kv_b[h*(nope+vd) + nope + r][c]``.
+    """Load-time output absorption (build.rs module doc, transform 3; ``absorb_o``).
 
-    ``o_proj [hidden, heads*vd]``; each head's V half starts at row ``nope`` of
-    its ``kv_b`` block. Returns ``[hidden, heads*kvl]``.
+    The V half of head h's ``kv_b`` block (its last ``vd`` rows, V_h ``[vd, kvl]``)
+    maps a latent vector to that head's value; ``o_proj``'s columns of head h (O_h,
+    ``[hidden, vd]``) map the value to the hidden state. The absorbed columns of
+    head h are O_h V_h (``[hidden, kvl]``), placed side by side over heads.
+    ``o_proj [hidden, heads*vd]``. Returns ``[hidden, heads*kvl]``.
     """
     o = np.asarray(o_proj, dtype=F64).reshape(hidden, heads, vd)
     kv_b = np.asarray(kv_b, dtype=F64).reshape(heads, nope + vd, kvl)
@@ -469,8 +475,8 @@ def indexer_store(k_seq, gate_seq, valid_seq, seq_len: int, k_row, gate_row, cap
                   ckv_seq=None, ckv_row=None) -> int:
     """``indexer_store`` for one sequence: the staged indexer row goes to position
     ``seq_len`` of the sequence's caches, which is marked valid, and the length
-    grows by one (mod.rs: the kernel copies the staged indexer row to a device-side
-    position and marks it valid). The caches are the sequence's logical token-major
+    grows by one (mod.rs, Glm5NextDsaKernels: the position comes from the device,
+    and the slot is flagged valid). The caches are the sequence's logical token-major
     arrays, updated in place. A full cache (``seq_len >= capacity``) is left
     unchanged. ``ckv_seq``/``ckv_row``: the layer's latent row for the same token,
     stored alongside (no counterpart on the pages; the latent cache append).
@@ -513,8 +519,9 @@ def compress_append(k_tok, gate_tok, valid_tok, ape, gamma, beta, eps: float, fi
 
 
 def write_geom(seq_lens, row_seq=None) -> np.ndarray:
-    """``write_geom``: the selector geometry derived from the live ``seq_len`` on
-    the device (mod.rs: so that a captured graph replays over the live context).
+    """``write_geom``: the selector's per-row geometry recomputed on the device
+    from the current lengths (mod.rs, Glm5NextDsaKernels: this is what keeps one
+    captured graph valid while the sequences grow).
     Reading: a decode row sees its whole sequence, so its context length is the
     sequence's current length; the visible pools and the tail follow from it."""
     seq_lens = np.asarray(seq_lens, dtype=np.int64)

@@ -21,7 +21,12 @@ DSA_STATUS_BAD_TOKEN = 1
 DSA_STATUS_BAD_BLOCK = 2
 DSA_STATUS_TIMEOUT = 4
 DSA_STATUS_CACHE_FULL = 8
-DSA_ABI_VERSION = 6
+DSA_ABI_VERSION = 7
+DSA_OPT_PDL = 0
+DSA_OPT_MLA_KERNEL = 1
+DSA_MLA_KERNEL_AUTO = 0
+DSA_MLA_KERNEL_TCGEN05 = 1
+DSA_MLA_KERNEL_MMA = 2
 
 
 class DsaPaging(ctypes.Structure):
@@ -46,6 +51,8 @@ _PG = ctypes.POINTER(DsaPaging)
 SIGNATURES = {
     "dsa_last_error": (ctypes.c_char_p, []),
     "dsa_abi_version": (_I, []),
+    "dsa_set_option": (_I, [_I, _I]),
+    "dsa_get_option": (_I, [_I]),
     "dsa_validate_config": (_I, [_I, _I, _I, _I]),
     "dsa_select_k": (_I, [_I, _I, _I]),
     "dsa_compress": (_I, [_P, _P, _P, _P, _P, _P, _F, _PG, _I, _I, _I, _P, _P, _P, _P, _P]),

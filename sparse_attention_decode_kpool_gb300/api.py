@@ -20,7 +20,8 @@ __all__ = ["paging", "dsa_compress", "dsa_compress_append", "dsa_indexer_store",
            "dsa_sparse_mla_decode_noalloc", "dsa_sparse_mla_decode_fp8", "dsa_quantize_latent",
            "dsa_frontend_workspace", "dsa_frontend", "dsa_latent_project_workspace",
            "dsa_latent_project", "dsa_select_k",
-           "dsa_validate_config", "DsaPaging"]
+           "dsa_validate_config", "dsa_set_option", "dsa_get_option", "mla_kernel",
+           "DsaPaging"]
 
 
 def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "tensor",
@@ -37,6 +38,40 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "tensor",
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     return t.data_ptr()
+
+
+def dsa_set_option(option: int, value: int) -> None:
+    """Set a process-wide launch option (DSA_OPT_* in include/dsa.h)."""
+    check(_lib.load().dsa_set_option(int(option), int(value)))
+
+
+def dsa_get_option(option: int) -> int:
+    """Current value of a launch option (-1 for an unknown option)."""
+    return int(_lib.load().dsa_get_option(int(option)))
+
+
+class mla_kernel:
+    """Context manager pinning the sparse-attention split kernel: "auto", "tcgen05"
+    (the tensor-core kernels where they support the shape) or "mma" (the mma.sync
+    kernel); the previous choice is restored on exit."""
+
+    _VALUES = {"auto": _lib.DSA_MLA_KERNEL_AUTO, "tcgen05": _lib.DSA_MLA_KERNEL_TCGEN05,
+               "mma": _lib.DSA_MLA_KERNEL_MMA}
+
+    def __init__(self, which: str):
+        if which not in self._VALUES:
+            raise ValueError(f"kernel {which!r}: one of {sorted(self._VALUES)}")
+        self.value = self._VALUES[which]
+        self.prev = None
+
+    def __enter__(self):
+        self.prev = dsa_get_option(_lib.DSA_OPT_MLA_KERNEL)
+        dsa_set_option(_lib.DSA_OPT_MLA_KERNEL, self.value)
+        return self
+
+    def __exit__(self, *exc):
+        dsa_set_option(_lib.DSA_OPT_MLA_KERNEL, self.prev)
+        return False
 
 
 def _stream(stream) -> int:

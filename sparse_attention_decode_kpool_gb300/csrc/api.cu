@@ -56,13 +56,14 @@ int set_max_smem(const void* kernel, int bytes) {
     return DSA_OK;
 }
 
-bool pdl_enabled() {
-    static const bool on = []() {
-        const char* v = getenv("DSA_PDL");
-        return !(v && v[0] == '0');
-    }();
-    return on;
-}
+// Process-wide launch options (dsa_set_option); read by the launch code, never from
+// the environment.
+static std::atomic<int> g_opt_pdl{1};
+static std::atomic<int> g_opt_mla_kernel{DSA_MLA_KERNEL_AUTO};
+
+bool pdl_enabled() { return g_opt_pdl.load(std::memory_order_relaxed) != 0; }
+
+int mla_kernel_choice() { return g_opt_mla_kernel.load(std::memory_order_relaxed); }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -179,6 +180,34 @@ extern "C" {
 const char* dsa_last_error(void) { return g_err; }
 
 int dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+int dsa_set_option(int option, int value) {
+    switch (option) {
+        case DSA_OPT_PDL:
+            if (value != 0 && value != 1)
+                return fail(DSA_ERR_INVALID_ARG, "dsa_set_option: DSA_OPT_PDL takes 0 or 1, not %d",
+                            value);
+            g_opt_pdl.store(value, std::memory_order_relaxed);
+            return DSA_OK;
+        case DSA_OPT_MLA_KERNEL:
+            if (value != DSA_MLA_KERNEL_AUTO && value != DSA_MLA_KERNEL_TCGEN05 &&
+                value != DSA_MLA_KERNEL_MMA)
+                return fail(DSA_ERR_INVALID_ARG,
+                            "dsa_set_option: DSA_OPT_MLA_KERNEL takes 0, 1 or 2, not %d", value);
+            g_opt_mla_kernel.store(value, std::memory_order_relaxed);
+            return DSA_OK;
+        default:
+            return fail(DSA_ERR_INVALID_ARG, "dsa_set_option: unknown option %d", option);
+    }
+}
+
+int dsa_get_option(int option) {
+    switch (option) {
+        case DSA_OPT_PDL: return g_opt_pdl.load(std::memory_order_relaxed);
+        case DSA_OPT_MLA_KERNEL: return g_opt_mla_kernel.load(std::memory_order_relaxed);
+        default: return -1;
+    }
+}
 
 int dsa_validate_config(int index_kpool, int index_topk, int kv_lora_rank, int local_heads) {
     if (index_kpool <= 0 || index_topk <= 0)

@@ -1,9 +1,10 @@
 // Decode-time append and the geometry derived from the live sequence lengths.
 //
-// Page: metrale_model_arch/glm5next_dsa/mod.rs, Glm5NextDsaKernels: `indexer_store`
-// copies the staged indexer row to a device-side position and marks it valid;
-// `write_geom` derives the selector geometry on the device from seq_len, so that a
-// captured graph replays over the live context.
+// Page: metrale_model_arch/glm5next_dsa/mod.rs, Glm5NextDsaKernels (`indexer_store`,
+// `write_geom`). The new token's indexer row is placed at a position the device
+// reads (the live length), flagged valid, and the selector's per-row geometry is
+// recomputed on the device from the lengths: no host value changes between steps,
+// which is what lets one captured graph serve every step.
 //
 // dsa_indexer_store: one CTA per sequence. The position is the sequence's current
 // length, read on the device; the rows go there through the cache layout, the

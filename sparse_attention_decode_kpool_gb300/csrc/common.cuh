@@ -27,9 +27,10 @@ int set_max_smem(const void* kernel, int bytes);  // once per (device, kernel)
 // Two kernels let their dependents start early (pdl_trigger): the split combine, so
 // that the projection fetches o_absorb meanwhile, and the front-end norm kernel,
 // ahead of the q GEMM. Elsewhere, dependent blocks waiting beside a running grid
-// slowed it. DSA_PDL=0 in the environment turns the attribute off (the wait then
+// slowed it. dsa_set_option(DSA_OPT_PDL, 0) turns the attribute off (the wait then
 // returns at once).
 bool pdl_enabled();
+int mla_kernel_choice();  // DSA_OPT_MLA_KERNEL
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t st, Args&&... args) {
@@ -77,7 +78,7 @@ int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A
                    float* yf = nullptr, uint16_t* y2 = nullptr, int split = 0);
 
 // Sparse latent attention on the tensor cores (mla_tc.cu): the split kernel of
-// dsa_sparse_mla_decode for 64 heads when DSA_MLA_TC=1. Writes the splits' partials
+// dsa_sparse_mla_decode for 64 heads (large batches, or forced by DSA_OPT_MLA_KERNEL). Writes the splits' partials
 // (ns > 1) or olat / its bf16 copy (ns == 1) in the same layout as the mma.sync split
 // kernel.
 struct MlaTcParams {
@@ -98,7 +99,7 @@ struct MlaTcParams {
     float sl2;  // softmax_scale * log2(e)
 };
 bool mla_tc_supported(int heads, int kv_lora_rank);
-int mla_tc_mode();  // 1 / 0: forced on / off by DSA_MLA_TC; -1: by size
+int mla_tc_mode();  // 1 / 0: forced on / off by DSA_OPT_MLA_KERNEL; -1: by size
 int mla_tc_chunk();  // tokens per chunk: split sizes are rounded to it
 int mla_tc_launch(const MlaTcParams& a, long long ckv_rows, cudaStream_t st);
 

@@ -9,7 +9,8 @@
 //
 // Set-up: the first call on each device, with that device current, looks up the
 // array's device address with cudaGetSymbolAddress and caches it; later calls on
-// that device reuse it. Make that first call before any stream capture begins.
+// that device reuse it. Make that first call before any stream capture begins (if
+// the lookup fails, the call returns DSA_ERR_CUDA and a later call looks again).
 //
 // Sharing: every call uses the same array, which keeps the previous call's
 // contents. Nothing in it needs to start at zero (each call writes every scratch
@@ -28,12 +29,11 @@ static __device__ __align__(256) uint8_t g_scratch[kNoAllocScratchBytes];
 namespace dsa {
 namespace {
 
-struct DevScratch {
-    std::once_flag once;
-    void* ptr = nullptr;
-    cudaError_t err = cudaSuccess;
-};
-DevScratch g_dev[64];
+// Device address of g_scratch per device, filled by the first call on that device
+// whose lookup succeeds. A failed lookup (for instance a first call made during a
+// stream capture) is not remembered: the next call tries again.
+std::mutex g_mu;
+void* g_ptr[64] = {};
 
 int scratch_for_current_device(void** out) {
     int dev = 0;
@@ -41,15 +41,19 @@ int scratch_for_current_device(void** out) {
     if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_mla_decode_noalloc: cudaGetDevice");
     if (dev < 0 || dev >= 64)
         return fail(DSA_ERR_UNSUPPORTED, "dsa_sparse_mla_decode_noalloc: device %d >= 64", dev);
-    DevScratch& d = g_dev[dev];
-    std::call_once(d.once, [&d]() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_ptr[dev]) {
         // Host code sees g_scratch only as a stand-in symbol; the device address of
         // this device's copy comes from the runtime.
-        d.err = cudaGetSymbolAddress(&d.ptr, g_scratch);
-    });
-    if (d.err != cudaSuccess)
-        return cuda_fail(d.err, "dsa_sparse_mla_decode_noalloc: cudaGetSymbolAddress");
-    *out = d.ptr;
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_scratch);
+        if (e != cudaSuccess) {
+            cudaGetLastError();  // leave no sticky launch error behind
+            return cuda_fail(e, "dsa_sparse_mla_decode_noalloc: cudaGetSymbolAddress");
+        }
+        g_ptr[dev] = p;
+    }
+    *out = g_ptr[dev];
     return DSA_OK;
 }
 

@@ -34,8 +34,6 @@
 //     end of a unit, its partial (or, with one split, olat), then free O^T.
 // All waits are bounded; a timeout sets DSA_STATUS_TIMEOUT, every role leaves its
 // loops, copies and MMAs in flight are drained, and the tensor memory is released.
-#include <stdlib.h>
-
 #include "common.cuh"
 #include "tc.cuh"
 
@@ -641,18 +639,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // The tensor-core kernel serves 64 heads of a 512-wide latent. It is chosen for
 // batches with at least 4 of its 128-token chunks per SM (see make_plan): 64 paged
-// rows of 2,048 tokens, 117.4 against 127.4 us for the mma.sync kernel; a prefill
-// chunk of 4,096 rows, 2.79 against 3.96 ms. With one chunk per CTA (decode batches
-// of a few rows) the mma.sync kernel is faster (1 row: 18.0 against 32.4 us).
+// rows of 2,048 tokens (two splits per row) and prefill chunks of thousands of rows
+// run faster on it than on the mma.sync kernel; with one chunk per CTA (decode
+// batches of a few rows) the mma.sync kernel is faster.
 bool mla_tc_supported(int heads, int kv_lora_rank) { return heads == kH && kv_lora_rank == kKVL; }
 
-// DSA_MLA_TC=1 forces the tensor-core kernel where supported, 0 the mma.sync one;
-// unset: chosen by size.
+// DSA_OPT_MLA_KERNEL: the tensor-core kernel forced where supported, the mma.sync one
+// forced, or chosen by size.
 int mla_tc_mode() {
-    const char* v = getenv("DSA_MLA_TC");
-    if (v && v[0] == '1') return 1;
-    if (v && v[0] == '0') return 0;
-    return -1;
+    const int v = mla_kernel_choice();
+    return v == DSA_MLA_KERNEL_TCGEN05 ? 1 : v == DSA_MLA_KERNEL_MMA ? 0 : -1;
 }
 
 int mla_tc_chunk() { return kT; }

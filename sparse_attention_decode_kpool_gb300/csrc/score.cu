@@ -1,8 +1,9 @@
 // dsa_score: index scores of query rows against their sequence's pooled keys.
 //
-// Page: metrale_model_arch/glm5next_dsa/tp.rs, "Why the indexer is replicated": the
-// score adds weights[h] * relu(scale * dot) over the indexer heads; scores are
-// [q_rows, n_pools]. build.rs, transform 2: weights already carry index_heads^-0.5.
+// Page: metrale_model_arch/glm5next_dsa/tp.rs, "Why the indexer is replicated":
+//   score[r, p] = sum_h w[r, h] * max(0, scale * <qidx[r, h, :], kpool[p, :]>)
+// for every (query row, pool). build.rs, transform 2: w already carries the
+// index_heads^-0.5 factor.
 //
 // Per pooled key (ihd bf16 = 256 B at ihd 128) the row does index_heads * ihd MACs:
 // 16 MAC per byte at 32 x 128, more than the f32 pipes sustain at HBM speed. So the

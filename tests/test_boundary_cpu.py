@@ -55,6 +55,33 @@ def test_validate_config_rules(lib, args, code):
         assert _err(lib)
 
 
+def test_launch_options(lib):
+    from sparse_attention_decode_kpool_gb300._lib import (DSA_MLA_KERNEL_AUTO,
+                                                           DSA_MLA_KERNEL_MMA,
+                                                           DSA_MLA_KERNEL_TCGEN05,
+                                                           DSA_OPT_MLA_KERNEL, DSA_OPT_PDL)
+    assert lib.dsa_get_option(DSA_OPT_PDL) == 1
+    assert lib.dsa_get_option(DSA_OPT_MLA_KERNEL) == DSA_MLA_KERNEL_AUTO
+    assert lib.dsa_get_option(99) == -1
+    try:
+        for v in (DSA_MLA_KERNEL_TCGEN05, DSA_MLA_KERNEL_MMA, DSA_MLA_KERNEL_AUTO):
+            assert lib.dsa_set_option(DSA_OPT_MLA_KERNEL, v) == DSA_OK
+            assert lib.dsa_get_option(DSA_OPT_MLA_KERNEL) == v
+        assert lib.dsa_set_option(DSA_OPT_MLA_KERNEL, 3) == DSA_ERR_INVALID_ARG
+        assert "DSA_OPT_MLA_KERNEL" in _err(lib)
+        assert lib.dsa_set_option(DSA_OPT_PDL, 0) == DSA_OK
+        assert lib.dsa_get_option(DSA_OPT_PDL) == 0
+        assert lib.dsa_set_option(DSA_OPT_PDL, 2) == DSA_ERR_INVALID_ARG
+        assert lib.dsa_set_option(7, 0) == DSA_ERR_INVALID_ARG
+    finally:
+        lib.dsa_set_option(DSA_OPT_PDL, 1)
+        lib.dsa_set_option(DSA_OPT_MLA_KERNEL, DSA_MLA_KERNEL_AUTO)
+    # nothing in the library reads the environment
+    src = os.path.join(ROOT, "sparse_attention_decode_kpool_gb300", "csrc")
+    for f in os.listdir(src):
+        assert "getenv" not in open(os.path.join(src, f)).read(), f
+
+
 def test_select_k(lib):
     assert lib.dsa_select_k(2048, 4, 65536) == 512
     assert lib.dsa_select_k(256, 4, 50) == 50

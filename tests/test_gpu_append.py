@@ -1,4 +1,4 @@
-"""Decode-time append and graph replay over the live context: dsa_indexer_store ->
+"""Decode-time append and graph replay while the sequences grow: dsa_indexer_store ->
 dsa_write_geom -> dsa_compress_append -> the step, captured once and replayed while
 the sequences grow. Each step is checked against the oracle at the grown length,
 the replayed graph against an eager twin bit for bit, and the incrementally built

@@ -22,8 +22,9 @@ def _cuda():
 
 
 @pytest.fixture(autouse=True)
-def _mma_kernel(monkeypatch):
-    monkeypatch.setenv("DSA_MLA_TC", "0")  # the bf16 twin runs the same split kernel
+def _mma_kernel():
+    with api.mla_kernel("mma"):  # the bf16 twin runs the same split kernel
+        yield
 
 
 def _host_quant(x_bf16: torch.Tensor):

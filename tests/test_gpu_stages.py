@@ -342,12 +342,12 @@ def _token_rows(rng, wl, ow, empty_row=True):
 
 
 @pytest.fixture(params=["mma", "tcgen05"])
-def mla_kernel(request, monkeypatch):
-    """Both split-attention kernels, each forced: the mma.sync one, and the tcgen05
-    one (64 heads only; other head counts keep the mma.sync kernel). Without the
-    variable the library picks by batch size."""
-    monkeypatch.setenv("DSA_MLA_TC", "1" if request.param == "tcgen05" else "0")
-    return request.param
+def mla_kernel(request):
+    """Both split-attention kernels, each forced through DSA_OPT_MLA_KERNEL: the
+    mma.sync one, and the tcgen05 one (64 heads only; other head counts keep the
+    mma.sync kernel). By default the library picks by batch size."""
+    with api.mla_kernel(request.param):
+        yield request.param
 
 
 @pytest.mark.parametrize("case", MLA_CASES, ids=[c[0] for c in MLA_CASES])

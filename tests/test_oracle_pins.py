@@ -630,6 +630,24 @@ def test_absorption_equivalence():
     np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-12)
 
 
+def test_absorb_golden():
+    # absorb_q / absorb_o against values worked by hand from the build.rs index
+    # expressions (tests/golden/absorb.txt): a K/V half swap, a transposed operand
+    # or a head offset error changes them.
+    G = load_kv("absorb.txt")
+    q_b, kv_b, o_proj = (np.vstack(G[k]) for k in ("q_b", "kv_b", "o_proj"))
+    qa = O.absorb_q(q_b, kv_b, heads=2, nope=2, vd=1, kvl=2, ql=2)
+    oa = O.absorb_o(o_proj, kv_b, heads=2, nope=2, vd=1, kvl=2, hidden=2)
+    np.testing.assert_array_equal(qa, np.vstack(G["q_absorb"]))
+    np.testing.assert_array_equal(oa, np.vstack(G["o_absorb"]))
+    # the unabsorbed form with the same weights distinguishes the halves too: one
+    # latent row, so the softmax weight is 1 and y = o_proj . V_h(ckv) per head
+    ckv = np.array([[1.0, 2.0]])
+    y = O.mla_unabsorbed(np.array([1.0, 1.0]), q_b, kv_b, o_proj, ckv, 2, 2, 1, 2, 0.5)
+    # V_0(ckv) = 0*1 + 3*2 = 6, V_1(ckv) = 2*1 - 2*2 = -2; y = o_proj . (6, -2)
+    np.testing.assert_array_equal(y, [1 * 6 + 2 * -2, -1 * 6 + 3 * -2])
+
+
 def test_unabsorbed_reduces_to_plain_attention():
     # kv_b halves = identity, o_proj = identity: MLA is plain attention with
     # keys = values = latent rows.
