@@ -108,11 +108,20 @@ int dsa_abi_version(void);
  *                       dependent of the work before it on the stream (it still
  *                       waits for that work before reading its outputs);
  *                       0: ordinary stream-ordered launches.
- *   DSA_OPT_MLA_KERNEL  which split kernel the sparse latent attention uses:
+ *   DSA_OPT_MLA_KERNEL  which kernel the sparse latent attention uses:
  *                       DSA_MLA_KERNEL_AUTO (default, chosen by size),
- *                       DSA_MLA_KERNEL_TCGEN05 (the tensor-core kernels wherever
- *                       they support the shape), DSA_MLA_KERNEL_MMA (the mma.sync
- *                       split kernel).
+ *                       DSA_MLA_KERNEL_TCGEN05 (the persistent tensor-core split
+ *                       kernel wherever it supports the shape),
+ *                       DSA_MLA_KERNEL_MMA (the mma.sync split kernel),
+ *                       DSA_MLA_KERNEL_CLUSTER (the tensor-core decode kernel:
+ *                       a chunk of 128 selected tokens per CTA; a row's CTAs merge
+ *                       their partials inside a thread-block cluster when they are
+ *                       at most 8, else the combine kernel merges them).
+ *   DSA_OPT_SELECT_KERNEL  how rows split over a thread-block cluster are selected:
+ *                       DSA_SELECT_KERNEL_MERGE (default: each CTA's slice top-k
+ *                       merged in CTA 0) or DSA_SELECT_KERNEL_RADIX (the row's
+ *                       k-th key found digit by digit from histograms shared across
+ *                       the cluster). Both give the same ids.
  *
  * dsa_set_option returns DSA_ERR_INVALID_ARG for an unknown option or value;
  * dsa_get_option returns the current value, or -1 for an unknown option.
@@ -122,6 +131,10 @@ int dsa_abi_version(void);
 #define DSA_MLA_KERNEL_AUTO 0
 #define DSA_MLA_KERNEL_TCGEN05 1
 #define DSA_MLA_KERNEL_MMA 2
+#define DSA_MLA_KERNEL_CLUSTER 3
+#define DSA_OPT_SELECT_KERNEL 2
+#define DSA_SELECT_KERNEL_MERGE 0
+#define DSA_SELECT_KERNEL_RADIX 1
 int dsa_set_option(int option, int value);
 int dsa_get_option(int option);
 

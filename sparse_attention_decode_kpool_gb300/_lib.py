@@ -27,6 +27,10 @@ DSA_OPT_MLA_KERNEL = 1
 DSA_MLA_KERNEL_AUTO = 0
 DSA_MLA_KERNEL_TCGEN05 = 1
 DSA_MLA_KERNEL_MMA = 2
+DSA_MLA_KERNEL_CLUSTER = 3
+DSA_OPT_SELECT_KERNEL = 2
+DSA_SELECT_KERNEL_MERGE = 0
+DSA_SELECT_KERNEL_RADIX = 1
 
 
 class DsaPaging(ctypes.Structure):

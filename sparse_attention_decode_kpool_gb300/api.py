@@ -21,7 +21,7 @@ __all__ = ["paging", "dsa_compress", "dsa_compress_append", "dsa_indexer_store",
            "dsa_frontend_workspace", "dsa_frontend", "dsa_latent_project_workspace",
            "dsa_latent_project", "dsa_select_k",
            "dsa_validate_config", "dsa_set_option", "dsa_get_option", "mla_kernel",
-           "DsaPaging"]
+           "select_kernel", "DsaPaging"]
 
 
 def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "tensor",
@@ -51,12 +51,13 @@ def dsa_get_option(option: int) -> int:
 
 
 class mla_kernel:
-    """Context manager pinning the sparse-attention split kernel: "auto", "tcgen05"
-    (the tensor-core kernels where they support the shape) or "mma" (the mma.sync
-    kernel); the previous choice is restored on exit."""
+    """Context manager pinning the sparse-attention kernel: "auto", "tcgen05" (the
+    persistent tensor-core split kernel where it supports the shape), "mma" (the
+    mma.sync split kernel) or "cluster" (the tensor-core decode kernel that merges a
+    row's splits inside a cluster); the previous choice is restored on exit."""
 
     _VALUES = {"auto": _lib.DSA_MLA_KERNEL_AUTO, "tcgen05": _lib.DSA_MLA_KERNEL_TCGEN05,
-               "mma": _lib.DSA_MLA_KERNEL_MMA}
+               "mma": _lib.DSA_MLA_KERNEL_MMA, "cluster": _lib.DSA_MLA_KERNEL_CLUSTER}
 
     def __init__(self, which: str):
         if which not in self._VALUES:
@@ -71,6 +72,28 @@ class mla_kernel:
 
     def __exit__(self, *exc):
         dsa_set_option(_lib.DSA_OPT_MLA_KERNEL, self.prev)
+        return False
+
+
+class select_kernel:
+    """Context manager pinning how clustered rows are selected: "merge" (the
+    default) or "radix"; the previous choice is restored on exit."""
+
+    _VALUES = {"merge": _lib.DSA_SELECT_KERNEL_MERGE, "radix": _lib.DSA_SELECT_KERNEL_RADIX}
+
+    def __init__(self, which: str):
+        if which not in self._VALUES:
+            raise ValueError(f"kernel {which!r}: one of {sorted(self._VALUES)}")
+        self.value = self._VALUES[which]
+        self.prev = None
+
+    def __enter__(self):
+        self.prev = dsa_get_option(_lib.DSA_OPT_SELECT_KERNEL)
+        dsa_set_option(_lib.DSA_OPT_SELECT_KERNEL, self.value)
+        return self
+
+    def __exit__(self, *exc):
+        dsa_set_option(_lib.DSA_OPT_SELECT_KERNEL, self.prev)
         return False
 
 

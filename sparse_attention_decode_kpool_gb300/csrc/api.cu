@@ -60,10 +60,13 @@ int set_max_smem(const void* kernel, int bytes) {
 // the environment.
 static std::atomic<int> g_opt_pdl{1};
 static std::atomic<int> g_opt_mla_kernel{DSA_MLA_KERNEL_AUTO};
+static std::atomic<int> g_opt_select_kernel{DSA_SELECT_KERNEL_MERGE};
 
 bool pdl_enabled() { return g_opt_pdl.load(std::memory_order_relaxed) != 0; }
 
 int mla_kernel_choice() { return g_opt_mla_kernel.load(std::memory_order_relaxed); }
+
+int select_kernel_choice() { return g_opt_select_kernel.load(std::memory_order_relaxed); }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -191,10 +194,16 @@ int dsa_set_option(int option, int value) {
             return DSA_OK;
         case DSA_OPT_MLA_KERNEL:
             if (value != DSA_MLA_KERNEL_AUTO && value != DSA_MLA_KERNEL_TCGEN05 &&
-                value != DSA_MLA_KERNEL_MMA)
+                value != DSA_MLA_KERNEL_MMA && value != DSA_MLA_KERNEL_CLUSTER)
                 return fail(DSA_ERR_INVALID_ARG,
-                            "dsa_set_option: DSA_OPT_MLA_KERNEL takes 0, 1 or 2, not %d", value);
+                            "dsa_set_option: DSA_OPT_MLA_KERNEL takes 0 to 3, not %d", value);
             g_opt_mla_kernel.store(value, std::memory_order_relaxed);
+            return DSA_OK;
+        case DSA_OPT_SELECT_KERNEL:
+            if (value != DSA_SELECT_KERNEL_MERGE && value != DSA_SELECT_KERNEL_RADIX)
+                return fail(DSA_ERR_INVALID_ARG,
+                            "dsa_set_option: DSA_OPT_SELECT_KERNEL takes 0 or 1, not %d", value);
+            g_opt_select_kernel.store(value, std::memory_order_relaxed);
             return DSA_OK;
         default:
             return fail(DSA_ERR_INVALID_ARG, "dsa_set_option: unknown option %d", option);
@@ -205,6 +214,7 @@ int dsa_get_option(int option) {
     switch (option) {
         case DSA_OPT_PDL: return g_opt_pdl.load(std::memory_order_relaxed);
         case DSA_OPT_MLA_KERNEL: return g_opt_mla_kernel.load(std::memory_order_relaxed);
+        case DSA_OPT_SELECT_KERNEL: return g_opt_select_kernel.load(std::memory_order_relaxed);
         default: return -1;
     }
 }

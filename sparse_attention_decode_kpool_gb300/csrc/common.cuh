@@ -30,7 +30,8 @@ int set_max_smem(const void* kernel, int bytes);  // once per (device, kernel)
 // slowed it. dsa_set_option(DSA_OPT_PDL, 0) turns the attribute off (the wait then
 // returns at once).
 bool pdl_enabled();
-int mla_kernel_choice();  // DSA_OPT_MLA_KERNEL
+int mla_kernel_choice();     // DSA_OPT_MLA_KERNEL
+int select_kernel_choice();  // DSA_OPT_SELECT_KERNEL
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t st, Args&&... args) {
@@ -99,9 +100,15 @@ struct MlaTcParams {
     float sl2;  // softmax_scale * log2(e)
 };
 bool mla_tc_supported(int heads, int kv_lora_rank);
-int mla_tc_mode();  // 1 / 0: forced on / off by DSA_OPT_MLA_KERNEL; -1: by size
 int mla_tc_chunk();  // tokens per chunk: split sizes are rounded to it
 int mla_tc_launch(const MlaTcParams& a, long long ckv_rows, cudaStream_t st);
+// The decode kernel (mla_dec.cu): 64 heads, a row's selected tokens spread over CTAs
+// (mla_dec_plan: CTAs per row, tokens per CTA, and whether the row's CTAs form a
+// cluster that merges its partials into olat / xbf; otherwise the partials in
+// part_o / part_ml go to the combine kernel).
+bool mla_dec_supported(int heads, int kv_lora_rank, int ow);
+void mla_dec_plan(int ow, int* cs, int* tps, bool* merge);  // merge: in the kernel
+int mla_dec_launch(const MlaTcParams& a, long long ckv_rows, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // Device side.

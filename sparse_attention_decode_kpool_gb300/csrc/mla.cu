@@ -600,7 +600,9 @@ __global__ void ysum_kernel(const float* __restrict__ ypart, int KS, long long n
 // Launch plan (shared by the workspace query and the call).
 
 struct Plan {
-    bool tc;  // the tensor-core split kernel (mla_tc.cu): 64 heads, large batches
+    bool tc;   // the persistent tensor-core split kernel (mla_tc.cu): 64 heads, large batches
+    bool dec;        // the decode kernel (mla_dec.cu): 64 heads, decode batches
+    bool dec_merge;  // ... whose row clusters merge their partials themselves
     int mt;
     int hgroups;
     int ns;
@@ -617,13 +619,27 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms,
                bool fp8 = false) {
     Plan p;
-    // The tensor-core kernel for 64 heads when the batch holds at least 4 of its
-    // 128-token chunks per SM (64 rows of 2,048 tokens, a prefill chunk), the
-    // mma.sync kernel otherwise (decode batches of a few rows).
-    const int tc_mode = mla_tc_mode();
+    // 64 heads: the persistent tensor-core kernel when the batch holds at least 4 of
+    // its 128-token chunks per SM (64 rows of 2,048 tokens, a prefill chunk), the
+    // cluster decode kernel below that (decode batches of a few rows); other head
+    // counts and the FP8 cache: the mma.sync kernel. DSA_OPT_MLA_KERNEL forces one.
+    const int choice = mla_kernel_choice();
     const long long tc_chunks = (long long)rows * ((ow + mla_tc_chunk() - 1) / mla_tc_chunk());
-    p.tc = !fp8 && mla_tc_supported(heads, KVL) &&
-           (tc_mode == 1 || (tc_mode < 0 && tc_chunks >= 4LL * sms));
+    const bool tc_ok = !fp8 && mla_tc_supported(heads, KVL);
+    const bool dec_ok = !fp8 && mla_dec_supported(heads, KVL, ow);
+    if (choice == DSA_MLA_KERNEL_TCGEN05) {
+        p.tc = tc_ok;
+    } else if (choice == DSA_MLA_KERNEL_CLUSTER) {
+        p.tc = false;
+    } else if (choice == DSA_MLA_KERNEL_MMA) {
+        p.tc = false;
+    } else {
+        p.tc = tc_ok && tc_chunks >= 4LL * sms;
+    }
+    // The tcgen05 decode kernel runs when forced: at 8 rows of 2,048 tokens it takes
+    // 19.1 us (one chunk per CTA, combine kernel after it) against 16.8 us for the
+    // mma.sync split kernel (cold-cache launch list), so by size the latter stays.
+    p.dec = !p.tc && dec_ok && choice == DSA_MLA_KERNEL_CLUSTER;
     p.mt = heads <= 16 ? 1 : heads <= 32 ? 2 : 4;
     p.hgroups = p.tc ? 1 : (heads + 16 * p.mt - 1) / (16 * p.mt);
     const int chunk = p.tc ? mla_tc_chunk() : CH;
@@ -637,7 +653,11 @@ Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms,
     const int per = ow > 0 ? (int)((ow + ns - 1) / ns) : 0;
     p.tps = per > 0 ? ((per + chunk - 1) / chunk) * chunk : chunk;
     p.ns = ow > 0 ? (ow + p.tps - 1) / p.tps : 1;
-    if (p.tc && ow > 0) {
+    p.dec_merge = false;
+    if (p.dec) {
+        mla_dec_plan(ow, &p.ns, &p.tps, &p.dec_merge);
+        p.hgroups = 1;
+    } else if (p.tc && ow > 0) {
         // Persistent grid: the busiest CTA walks ceil(units / sms) units of
         // ceil(chunks per row / ns) chunks, plus about a chunk's time per unit (Q,
         // the epilogue, the partials); take the split count that makes this smallest
@@ -667,11 +687,14 @@ Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms,
     if (ks > KC) ks = KC;
     p.KS = (int)ks;
 
+    // partials: the split kernels' when a row has several splits; the decode kernel
+    // always stores its CTAs' partials and merges them itself
+    const bool parts = p.ns > 1 || p.dec;
     size_t off = 0;
     p.off_part_o = off;
-    if (p.ns > 1) off += align256((size_t)rows * p.ns * heads * KVL * 4);
+    if (parts) off += align256((size_t)rows * p.ns * heads * KVL * 4);
     p.off_part_ml = off;
-    if (p.ns > 1) off += align256((size_t)rows * p.ns * heads * 2 * 4);
+    if (parts) off += align256((size_t)rows * p.ns * heads * 2 * 4);
     p.off_xbf = off;
     if (with_oabs) off += align256((size_t)rows * heads * KVL * 2);
     p.off_ypart = off;
@@ -779,8 +802,9 @@ int mla_decode_impl(const dsa_bf16* qlat, int rows, int heads, int kv_lora_rank,
     a.ckv8 = ckv8;
     a.ckv_scale = ckv_scale;
     a.token_ids = token_ids;
-    a.part_o = p.ns > 1 ? reinterpret_cast<float*>(ws + p.off_part_o) : nullptr;
-    a.part_ml = p.ns > 1 ? reinterpret_cast<float*>(ws + p.off_part_ml) : nullptr;
+    const bool parts = p.ns > 1 || p.dec;
+    a.part_o = parts ? reinterpret_cast<float*>(ws + p.off_part_o) : nullptr;
+    a.part_ml = parts ? reinterpret_cast<float*>(ws + p.off_part_ml) : nullptr;
     a.olat = olat;
     a.xbf = with_oabs ? reinterpret_cast<uint16_t*>(ws + p.off_xbf) : nullptr;
     a.status = status;
@@ -793,7 +817,7 @@ int mla_decode_impl(const dsa_bf16* qlat, int rows, int heads, int kv_lora_rank,
     a.sl2 = softmax_scale * kLog2e;
 
     if (!olat && !with_oabs) return DSA_OK;  // nothing requested
-    if (p.tc) {
+    if (p.tc || p.dec) {
         MlaTcParams t;
         t.qlat = qlat;
         t.row_seq = row_seq;
@@ -812,7 +836,7 @@ int mla_decode_impl(const dsa_bf16* qlat, int rows, int heads, int kv_lora_rank,
         t.sl2 = a.sl2;
         const long long ckv_rows = P.block_table ? (long long)P.num_blocks * P.block_size
                                                  : (long long)P.batch * P.max_seq_len;
-        rc = mla_tc_launch(t, ckv_rows, st);
+        rc = p.dec ? mla_dec_launch(t, ckv_rows, st) : mla_tc_launch(t, ckv_rows, st);
     } else {
         switch (p.mt * 2 + (fp8 ? 1 : 0)) {
             case 2: rc = launch_split<1, false>(a, p, st); break;
@@ -826,7 +850,7 @@ int mla_decode_impl(const dsa_bf16* qlat, int rows, int heads, int kv_lora_rank,
     if (rc) return rc;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_mla_decode split launch");
-    if (p.ns > 1) {
+    if ((p.ns > 1 && !p.dec) || (p.dec && !p.dec_merge)) {
         e = launch_pdl(mla_combine_kernel, dim3(heads, rows), dim3(128), 0, st,
                        (const float*)a.part_o, (const float*)a.part_ml, heads, p.ns, olat, a.xbf);
         if (e == cudaSuccess) e = cudaGetLastError();

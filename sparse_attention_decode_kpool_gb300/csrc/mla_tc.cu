@@ -644,13 +644,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // batches of a few rows) the mma.sync kernel is faster.
 bool mla_tc_supported(int heads, int kv_lora_rank) { return heads == kH && kv_lora_rank == kKVL; }
 
-// DSA_OPT_MLA_KERNEL: the tensor-core kernel forced where supported, the mma.sync one
-// forced, or chosen by size.
-int mla_tc_mode() {
-    const int v = mla_kernel_choice();
-    return v == DSA_MLA_KERNEL_TCGEN05 ? 1 : v == DSA_MLA_KERNEL_MMA ? 0 : -1;
-}
-
 int mla_tc_chunk() { return kT; }
 
 int mla_tc_launch(const MlaTcParams& a, long long ckv_rows, cudaStream_t st) {

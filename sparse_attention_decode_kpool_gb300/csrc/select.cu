@@ -15,13 +15,27 @@
 // shared-memory histograms) resolves the exact key and how many equal keys to take.
 // A ballot-prefix pass then emits the chosen positions in ascending order.
 //
-// With C > 1 every CTA stages its chosen (key, id) pairs in its own slot of its merge
-// area (unused slot entries get key 0) and moves the slot to the same place in CTA 0
-// with bulk copies that complete on an mbarrier there; CTA 0 then selects the row's
-// top-k among the C x k candidates the same way: the row's top-k is contained in the
-// union of the slices' top-k, and slot order keeps the ids ascending. Two cluster
-// barrier phases order the rest: CTA 0's mbarrier exists before any push, and no CTA
-// leaves before CTA 0 has received its slot.
+// Rows split over a cluster (C > 1) take select_radix_kernel: the CTAs first share
+// their slices' key bounds, then find the row's k-th key digit by digit (9-bit digits
+// of kmax - key, from the top of the row's key range). Each CTA histograms the
+// next digit of its slice's keys that match the digits fixed so far and sends the
+// histogram to every other CTA of the cluster (bulk copies into the same place of each
+// peer's shared memory, completing on that peer's mbarrier); every CTA sums the C
+// histograms and walks them from the top to the bin holding the k-th key, so all CTAs
+// reach the same bin. Keys in higher bins are chosen. As soon as the bin holds few
+// enough keys, each CTA sends its keys of the bin to every peer, and every CTA ranks
+// the gathered keys (radix passes in shared memory): the k-th key T and how many keys
+// equal to T are taken (the lowest pool ids first, i.e. lower CTA ranks first, then
+// lower positions). Once every bit is fixed the bin holds one key value and nothing
+// is gathered. Every CTA then knows how many keys each CTA takes, hence its own offset in
+// the output row, and emits its chosen positions there in ascending order.
+//
+// If a cluster's slices do not fit that kernel's shared memory, the older form runs:
+// every CTA stages its slice's top-k (key, id) pairs in its own slot of a merge area
+// (unused entries get key 0) and moves the slot to the same place in CTA 0 with bulk
+// copies that complete on an mbarrier there; CTA 0 then selects the row's top-k among
+// the C x k candidates: the row's top-k is contained in the union of the slices' top-k,
+// and slot order keeps the ids ascending.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -615,6 +629,386 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
     cluster_wait();  // phase 2 (complete: every CTA arrived)
 }
 
+// ---------------------------------------------------------------------------
+// Cluster top-k by radix digits (see the file comment).
+
+constexpr int kDigitBits = 9;
+constexpr int kDigitBins = 1 << kDigitBits;
+constexpr int kRounds = 6;  // bounds, up to four digits, one key gather
+
+struct RadixLayout {
+    int hist_off;  // byte offsets in dynamic shared memory: histograms [2][C][kDigitBins]
+    int mm_off;    // slice bounds [C][4]: min key, max key, nonzero keys, 0
+    int list_off;  // the gathered keys of the final bin
+    int list_cap;  // its capacity (keys)
+    int bar_off;   // kRounds mbarriers
+};
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+// Returns once every bulk copy this thread committed has finished reading its source.
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+
+// Thread 0 sends bytes (a multiple of 16) at src to the same offset in every other CTA
+// of the cluster and waits until `expect` bytes from the peers have landed here on
+// bar. Returns false (in every thread) if that wait gave up.
+__device__ __noinline__ bool exchange(const void* src, uint32_t bytes, uint64_t* bar,
+                                      uint32_t expect, int C, int crank, BlockScratch& sc) {
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(bar, expect);
+        if (bytes) {
+            for (int p = 0; p < C; ++p)
+                if (p != crank) bulk_to_peer(src, src, bytes, bar, (uint32_t)p);
+            bulk_commit();
+        }
+        sc.pick[0] = mbar_wait(bar, 0) ? 1 : 0;
+    }
+    __syncthreads();
+    const bool ok = sc.pick[0] != 0;
+    __syncthreads();  // pick[] is scratch again
+    return ok;
+}
+
+// Digits are taken over v = kmax - key (0 for the row's largest key), the row's key
+// range split into 9-bit digits from the top: the first digit's bins are spread over
+// the keys the row actually holds.
+__global__ void __launch_bounds__(kThreads, 1) select_radix_kernel(SelectArgs a, RadixLayout L) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int crank = (int)cluster.block_rank();
+    const int r = (int)blockIdx.x / C;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    extern __shared__ __align__(16) uint32_t keys[];
+    __shared__ BlockScratch sc;
+    __shared__ int above_c[kMaxCluster];  // per CTA: its keys above the current bin
+    __shared__ int bin_c[kMaxCluster];    // per CTA: its keys in the current bin
+    __shared__ int gt_c[kMaxCluster], eq_c[kMaxCluster];
+    __shared__ int res[8];
+    uint8_t* dyn = reinterpret_cast<uint8_t*>(keys);
+    uint32_t* hist0 = reinterpret_cast<uint32_t*>(dyn + L.hist_off);
+    uint32_t* mmv = reinterpret_cast<uint32_t*>(dyn + L.mm_off);
+    uint32_t* list = reinterpret_cast<uint32_t*>(dyn + L.list_off);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(dyn + L.bar_off);
+
+    const int begin = crank * a.chunk;
+    const int n = max(0, min(a.chunk, a.p_stride - begin));
+    const int k = a.sk;
+    int32_t* out = a.pool_ids + (long long)r * a.sk;
+    int32_t* tok = a.tok ? a.tok + (long long)r * a.ow : nullptr;
+
+    if (tid == 0) {
+        for (int i = 0; i < kRounds; ++i) mbar_init(bars + i, 1);
+        fence_mbar_init();
+    }
+    if (tid < kMaxCluster) above_c[tid] = 0;
+    cluster_arrive();  // the mbarriers exist before any peer's first copy
+    pdl_wait();
+
+    // ---- slice -> order-preserving keys, with their bounds
+    const float* srow = a.scores + (long long)r * a.p_stride + begin;
+    uint32_t kmx = 0u, kmn = 0xffffffffu;
+    int kcnt = 0;
+    auto put = [&](int i, float f) {
+        const uint32_t key = score_key(f);
+        keys[i] = key;
+        if (key) {
+            kmx = max(kmx, key);
+            kmn = min(kmn, key);
+            ++kcnt;
+        }
+    };
+    if ((reinterpret_cast<uintptr_t>(srow) & 15u) == 0u) {
+        const float4* s4 = reinterpret_cast<const float4*>(srow);
+        const int nv = n >> 2;
+        for (int base = 0; base < nv; base += 8 * kThreads) {
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = base + j * kThreads + tid;
+                v[j] = i < nv ? __ldg(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = base + j * kThreads + tid;
+                if (i < nv) {
+                    put(4 * i, v[j].x);
+                    put(4 * i + 1, v[j].y);
+                    put(4 * i + 2, v[j].z);
+                    put(4 * i + 3, v[j].w);
+                }
+            }
+        }
+        for (int i = (nv << 2) + tid; i < n; i += kThreads) put(i, __ldg(srow + i));
+    } else {
+        for (int i = tid; i < n; i += kThreads) put(i, __ldg(srow + i));
+    }
+    const MinMax sm = block_minmax(kmn, kmx, kcnt, sc);  // also publishes keys[]
+    if (tid == 0) {
+        mmv[4 * crank] = sm.kmin;
+        mmv[4 * crank + 1] = sm.kmax;
+        mmv[4 * crank + 2] = (uint32_t)sm.count;
+        mmv[4 * crank + 3] = 0u;
+        fence_async_shared();
+    }
+    __syncthreads();
+    cluster_wait();
+
+    // ---- the row's bounds
+    bool ok = exchange(mmv + 4 * crank, 16u, bars + 0, (uint32_t)(C - 1) * 16u, C, crank, sc);
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    int total = 0;
+    for (int c = 0; c < C; ++c) {
+        if (mmv[4 * c + 2] == 0u) continue;
+        kmin = min(kmin, mmv[4 * c]);
+        kmax = max(kmax, mmv[4 * c + 1]);
+        total += (int)mmv[4 * c + 2];
+    }
+    const bool take_all = total <= k;  // every finite score is chosen
+
+    // ---- digits of v = kmax - key, from the top, down to the bin of the k-th key
+    int A = 0;            // keys of the row above the current bin
+    uint32_t prefix = 0u; // v >> hi of the keys in the current bin
+    int hi = kmax > kmin ? 32 - __clz(kmax - kmin) : 0;  // low bits of v still open
+    int nB = total;
+    if (ok && !take_all && hi > 0) {
+        for (int level = 0;; ++level) {
+            const int d = min(kDigitBits, hi);
+            const int lo = hi - d;
+            const int nbins = 1 << d;
+            uint32_t* hist = hist0 + (level & 1) * C * kDigitBins;
+            uint32_t* myh = hist + crank * kDigitBins;
+            // This buffer was last read two levels ago: every peer has finished that
+            // level (it needed this CTA's histogram of the level in between), and this
+            // CTA's own copies out of it are done once bulk_wait_read returns.
+            if (tid == 0) bulk_wait_read();
+            for (int b = tid; b < nbins; b += kThreads) myh[b] = 0u;
+            __syncthreads();
+            for (int i = tid; i < n; i += kThreads) {
+                const uint32_t key = keys[i];
+                const uint32_t v = kmax - key;
+                if (key != 0u && (hi >= 32 ? 0u : v >> hi) == prefix)
+                    atomicAdd(&myh[(v >> lo) & (uint32_t)(nbins - 1)], 1u);
+            }
+            fence_async_shared();
+            __syncthreads();
+            if (!exchange(myh, (uint32_t)nbins * 4u, bars + 1 + level, (uint32_t)(C - 1) * nbins * 4u,
+                          C, crank, sc)) {
+                ok = false;
+                break;
+            }
+            // thread t owns bin t (bin 0: the largest keys)
+            uint32_t g = 0u;
+            if (tid < nbins)
+                for (int c = 0; c < C; ++c) g += hist[c * kDigitBins + tid];
+            uint32_t incl = g;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint32_t x = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += x;
+            }
+            if (lane == 31) sc.wcnt[warp] = (int)incl;
+            __syncthreads();
+            uint32_t wbase = 0u;
+            for (int w = 0; w < warp; ++w) wbase += (uint32_t)sc.wcnt[w];
+            const uint32_t need = (uint32_t)(k - A);
+            const uint32_t excl = wbase + incl - g;
+            if (tid < nbins && excl < need && need <= excl + g) {
+                res[0] = tid;
+                res[1] = (int)excl;
+                res[2] = (int)g;
+            }
+            __syncthreads();
+            const int B = res[0];
+            A += res[1];
+            nB = res[2];
+            // each CTA's keys above the bin and in it (warp c sums CTA c's bins)
+            if (warp < C) {
+                uint32_t s = 0u;
+                for (int b = lane; b < B; b += 32) s += hist[warp * kDigitBins + b];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+                if (lane == 0) {
+                    above_c[warp] += (int)s;
+                    bin_c[warp] = (int)hist[warp * kDigitBins + B];
+                }
+            }
+            prefix = (prefix << d) | (uint32_t)B;
+            hi = lo;
+            __syncthreads();  // res[], sc.wcnt, above_c, bin_c
+            if (hi == 0 || nB + 3 * C <= L.list_cap) break;
+        }
+    } else if (ok && !take_all) {
+        // one key value (kmin == kmax): it is T, and every CTA's keys are equal to it
+        if (tid < C) bin_c[tid] = (int)mmv[4 * tid + 2];
+        __syncthreads();
+    }
+
+    Thr t{0u, 0, 0};  // this CTA's threshold, its quota of keys equal to T, its count
+    int off = 0, K = 0;
+    if (ok && take_all) {
+        // each CTA takes all of its finite keys; T = 0 takes every nonzero key
+        if (tid == 0) {
+            int o = 0;
+            for (int c = 0; c < C; ++c) {
+                if (c == crank) {
+                    res[3] = o;
+                    res[4] = (int)mmv[4 * c + 2];
+                }
+                o += (int)mmv[4 * c + 2];
+            }
+            res[5] = o;
+        }
+        __syncthreads();
+        off = res[3];
+        t = Thr{0u, 0, res[4]};
+        K = res[5];
+    } else if (ok) {
+        const int need = k - A;  // keys still to take from the bin: 1 <= need <= nB
+        uint32_t T = 0u;
+        int need_eq = 0;
+        if (hi == 0) {
+            // the bin is a single key value
+            T = kmax - prefix;
+            need_eq = need;
+            if (tid < C) {
+                gt_c[tid] = 0;
+                eq_c[tid] = bin_c[tid];
+            }
+        } else {
+            // gather the bin's keys: CTA c's at list offset sum_{c' < c} pad4(bin_c')
+            int loff = 0, ltot = 0;
+            for (int c = 0; c < C; ++c) {
+                const int padded = (bin_c[c] + 3) & ~3;
+                if (c < crank) loff += padded;
+                ltot += padded;
+            }
+            const int mine = (bin_c[crank] + 3) & ~3;
+            if (tid == 0) sc.tcount = 0;
+            __syncthreads();
+            for (int i = tid; i < n; i += kThreads) {
+                const uint32_t key = keys[i];
+                if (key != 0u && ((kmax - key) >> hi) == prefix) {
+                    const int at = atomicAdd(&sc.tcount, 1);
+                    if (at < mine) list[loff + at] = key;
+                }
+            }
+            if (tid < mine - bin_c[crank]) list[loff + bin_c[crank] + tid] = 0u;  // padding
+            fence_async_shared();
+            __syncthreads();
+            if (!exchange(list + loff, (uint32_t)mine * 4u, bars + kRounds - 1,
+                          (uint32_t)(ltot - mine) * 4u, C, crank, sc)) {
+                ok = false;
+            } else {
+                uint32_t mx = 0u, mn = 0xffffffffu;
+                int cnt = 0;
+                for (int i = tid; i < ltot; i += kThreads) {
+                    const uint32_t key = list[i];
+                    if (key) {
+                        mx = max(mx, key);
+                        mn = min(mn, key);
+                        ++cnt;
+                    }
+                }
+                const MinMax mm = block_minmax(mn, mx, cnt, sc);
+                const Thr th = radix_threshold(list, ltot, need, mm, sc, false);
+                T = th.T;
+                need_eq = th.need_eq;
+                // each CTA's keys of the bin above T and equal to T
+                if (warp < C) {
+                    int lo = 0;
+                    for (int c = 0; c < warp; ++c) lo += (bin_c[c] + 3) & ~3;
+                    int gt = 0, eq = 0;
+                    for (int i = lo + lane; i < lo + bin_c[warp]; i += 32) {
+                        const uint32_t key = list[i];
+                        gt += key > T;
+                        eq += key == T;
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        gt += __shfl_xor_sync(0xffffffffu, gt, o);
+                        eq += __shfl_xor_sync(0xffffffffu, eq, o);
+                    }
+                    if (lane == 0) {
+                        gt_c[warp] = gt;
+                        eq_c[warp] = eq;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        if (ok) {
+            // quotas of T-keys go to the lowest CTA ranks first; offsets follow
+            if (tid == 0) {
+                int eqp = 0, o = 0;
+                for (int c = 0; c < C; ++c) {
+                    const int q = min(eq_c[c], max(0, need_eq - eqp));
+                    eqp += eq_c[c];
+                    const int sel = above_c[c] + gt_c[c] + q;
+                    if (c == crank) {
+                        res[3] = o;
+                        res[4] = sel;
+                        res[5] = q;
+                    }
+                    o += sel;
+                }
+                res[6] = o;
+            }
+            __syncthreads();
+            off = res[3];
+            t = Thr{T, res[5], res[4]};
+            K = res[6];
+        }
+    }
+
+    int t0, tend;
+    tail_range(a, r, &t0, &tend);
+    if (!ok) {
+        // a copy that never landed: this row is left unselected
+        fill_tail(out, a.sk, tok, a.ow, a.kpool, 0, a.tail_at, t0, tend);
+    } else {
+        if (t.kk > 0) {
+            EmitTo e;
+            e.mode = 0;
+            e.base = begin;
+            e.out = out + off;
+            e.rkeys = e.rids = nullptr;
+            e.ids = nullptr;
+            e.tok = tok ? tok + (long long)off * a.kpool : nullptr;
+            e.first_key = a.first_key;
+            e.kpool = a.kpool;
+            ordered_emit(keys, n, t, sc, e);
+        }
+        if (crank == 0) fill_tail(out, a.sk, tok, a.ow, a.kpool, K, a.tail_at, t0, tend);
+    }
+    if (tid == 0) bulk_wait_read();  // this CTA's outgoing copies have read their sources
+    __syncthreads();
+    // no CTA leaves while a peer may still copy into it
+    cluster_arrive();
+    cluster_wait();
+}
+
+// Shared memory of select_radix_kernel for slices of `chunk` keys (a list_cap below
+// the minimum when it does not fit).
+RadixLayout radix_layout(int chunk, int C, long long* bytes) {
+    RadixLayout L;
+    long long off = ((long long)chunk * 4 + 15) & ~15LL;
+    L.hist_off = (int)off;
+    off += 2LL * C * kDigitBins * 4;
+    L.mm_off = (int)off;
+    off += 16LL * kMaxCluster;
+    L.bar_off = (int)off;
+    off += kRounds * 8;
+    L.list_off = (int)((off + 15) & ~15LL);
+    off = L.list_off;
+    const long long room = (kMaxSmem - off) / 4;
+    L.list_cap = (int)(room > 16384 ? 16384 : room);
+    *bytes = off + 4LL * (L.list_cap > 0 ? L.list_cap : 0);
+    return L;
+}
+
 // Dynamic shared memory: the slice's keys (4 B each); with C > 1 the merge area
 // (C x sk4 keys and ids, 4 words of bounds per slice and an mbarrier; sk4 = select_k
 // rounded up to a multiple of 4); the threshold bin's list.
@@ -679,15 +1073,16 @@ int select_launch(const float* scores, int rows, int p_stride, int sk, int32_t* 
     a.row_ctx = row_ctx;
     a.tail_at = row_ctx ? tail_at : ow;
     const bool by_rows = C == 1 && rows > sms;
-    auto kernel = by_rows ? select_kernel<true> : select_kernel<false>;
-    int rc = set_max_smem((const void*)kernel, kMaxSmem);
-    if (rc) return rc;
+    // Clustered rows take the radix kernel when its histograms fit beside the slice.
+    long long rbytes = 0;
+    const RadixLayout rl = radix_layout(a.chunk, C, &rbytes);
+    const bool radix = C > 1 && rl.list_cap >= 1024 && select_kernel_choice() == DSA_SELECT_KERNEL_RADIX;
     if ((long long)rows * C > 0x7fffffffLL) return fail(DSA_ERR_UNSUPPORTED, "dsa_select: too many rows");
     cudaLaunchConfig_t cfg = {};
     // single-CTA rows: a grid of at most one CTA per SM walks the rows
     cfg.gridDim = dim3((unsigned)(by_rows ? sms : rows * C));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = (size_t)sp.bytes;
+    cfg.dynamicSmemBytes = radix ? (size_t)rbytes : (size_t)sp.bytes;
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -698,7 +1093,17 @@ int select_launch(const float* scores, int rows, int p_stride, int sk, int32_t* 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a);
+    cudaError_t e;
+    if (radix) {
+        int rc = set_max_smem((const void*)select_radix_kernel, kMaxSmem);
+        if (rc) return rc;
+        e = cudaLaunchKernelEx(&cfg, select_radix_kernel, a, rl);
+    } else {
+        auto kernel = by_rows ? select_kernel<true> : select_kernel<false>;
+        int rc = set_max_smem((const void*)kernel, kMaxSmem);
+        if (rc) return rc;
+        e = cudaLaunchKernelEx(&cfg, kernel, a);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "dsa_select launch");
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_select launch");

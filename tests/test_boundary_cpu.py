@@ -67,15 +67,20 @@ def test_launch_options(lib):
         for v in (DSA_MLA_KERNEL_TCGEN05, DSA_MLA_KERNEL_MMA, DSA_MLA_KERNEL_AUTO):
             assert lib.dsa_set_option(DSA_OPT_MLA_KERNEL, v) == DSA_OK
             assert lib.dsa_get_option(DSA_OPT_MLA_KERNEL) == v
-        assert lib.dsa_set_option(DSA_OPT_MLA_KERNEL, 3) == DSA_ERR_INVALID_ARG
+        assert lib.dsa_set_option(DSA_OPT_MLA_KERNEL, 3) == DSA_OK
+        assert lib.dsa_set_option(DSA_OPT_MLA_KERNEL, 4) == DSA_ERR_INVALID_ARG
         assert "DSA_OPT_MLA_KERNEL" in _err(lib)
         assert lib.dsa_set_option(DSA_OPT_PDL, 0) == DSA_OK
         assert lib.dsa_get_option(DSA_OPT_PDL) == 0
         assert lib.dsa_set_option(DSA_OPT_PDL, 2) == DSA_ERR_INVALID_ARG
+        assert lib.dsa_set_option(2, 1) == DSA_OK  # DSA_OPT_SELECT_KERNEL, radix
+        assert lib.dsa_get_option(2) == 1
+        assert lib.dsa_set_option(2, 2) == DSA_ERR_INVALID_ARG
         assert lib.dsa_set_option(7, 0) == DSA_ERR_INVALID_ARG
     finally:
         lib.dsa_set_option(DSA_OPT_PDL, 1)
         lib.dsa_set_option(DSA_OPT_MLA_KERNEL, DSA_MLA_KERNEL_AUTO)
+        lib.dsa_set_option(2, 0)
     # nothing in the library reads the environment
     src = os.path.join(ROOT, "sparse_attention_decode_kpool_gb300", "csrc")
     for f in os.listdir(src):

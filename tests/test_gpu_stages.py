@@ -159,8 +159,16 @@ SELECT_CASES = [
 ]
 
 
+@pytest.fixture(params=["merge", "radix"])
+def select_form(request):
+    """Both ways clustered rows are selected, each forced through
+    DSA_OPT_SELECT_KERNEL (single-CTA rows take the same kernel either way)."""
+    with api.select_kernel(request.param):
+        yield request.param
+
+
 @pytest.mark.parametrize("case", SELECT_CASES, ids=[f"{c[0]}x{c[1]}-k{c[2]}/{c[3]}-{c[4]}" for c in SELECT_CASES])
-def test_select_parity(case):
+def test_select_parity(case, select_form):
     rows, P, topk, kp, kind = case
     rng = np.random.default_rng(rows * 7919 + P)
     s = _tie_rows(rng, rows, P, kind)
@@ -189,7 +197,7 @@ SELECT_EXPAND_CASES = [
 
 @pytest.mark.parametrize("case", SELECT_EXPAND_CASES,
                          ids=[f"{c[0]}x{c[1]}-k{c[2]}/{c[3]}-{c[4]}-fk{c[5]}" for c in SELECT_EXPAND_CASES])
-def test_select_expand_parity(case):
+def test_select_expand_parity(case, select_form):
     """The fused call equals dsa_select then dsa_expand bit for bit, and the oracle's
     top-k and expansion."""
     rows, P, topk, kp, kind, fk, extra = case
@@ -255,7 +263,7 @@ def _tail_ctx(rng, rows, P, kp, fk):
 
 @pytest.mark.parametrize("case", SELECT_EXPAND_CASES,
                          ids=[f"{c[0]}x{c[1]}-k{c[2]}/{c[3]}-{c[4]}-fk{c[5]}" for c in SELECT_EXPAND_CASES])
-def test_select_expand_tail_parity(case):
+def test_select_expand_tail_parity(case, select_form):
     """always_select_tail: the fused call equals dsa_select then dsa_expand_tail bit
     for bit, and the oracle's top-k and tail expansion."""
     rows, P, topk, kp, kind, fk, extra = case
@@ -341,11 +349,12 @@ def _token_rows(rng, wl, ow, empty_row=True):
     return ids
 
 
-@pytest.fixture(params=["mma", "tcgen05"])
+@pytest.fixture(params=["mma", "tcgen05", "cluster"])
 def mla_kernel(request):
-    """Both split-attention kernels, each forced through DSA_OPT_MLA_KERNEL: the
-    mma.sync one, and the tcgen05 one (64 heads only; other head counts keep the
-    mma.sync kernel). By default the library picks by batch size."""
+    """Every attention kernel, each forced through DSA_OPT_MLA_KERNEL: the mma.sync
+    split kernel, the persistent tcgen05 split kernel and the tcgen05 cluster decode
+    kernel (the last two: 64 heads only; other head counts keep the mma.sync kernel).
+    By default the library picks by batch size."""
     with api.mla_kernel(request.param):
         yield request.param
 
@@ -353,8 +362,8 @@ def mla_kernel(request):
 @pytest.mark.parametrize("case", MLA_CASES, ids=[c[0] for c in MLA_CASES])
 def test_mla_parity(case, mla_kernel):
     name, heads, hidden, lens, bs, ow, with_o = case
-    if mla_kernel == "tcgen05" and heads != 64:
-        pytest.skip("the tcgen05 split kernel serves 64 heads")
+    if mla_kernel in ("tcgen05", "cluster") and heads != 64:
+        pytest.skip("the tcgen05 kernels serve 64 heads")
     g = _geom(heads=heads, hidden=max(hidden, 32), index_topk=ow)
     wl = W.make_workload(name, 300, g, lens, block_size=bs, with_raw=False,
                          with_o_absorb=with_o)
