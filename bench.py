@@ -51,11 +51,7 @@ PREFILL_WORKLOAD = 4  # scored on the tensor cores; the o_absorb GEMM is not in 
 # kernels changed since the capture, reports null. The projection reads all of
 # o_absorb whatever the context length, so its capture at 8 rows of a 32,768-token
 # context holds for the 262,144-token workload.
-MEASURED_TRAFFIC = {
-    "project": (269.730816e6 + 3.598336e6 + 0.733184e6,
-                "ncu: project_kernel + project_reduce_rows_kernel, 8 rows, o_absorb "
-                "4096 x 32768 bf16"),
-}
+MEASURED_TRAFFIC = {}
 FLUSH_BYTES = 256 << 20
 
 
@@ -617,7 +613,7 @@ def main():
         # result needs no copy node.
         step_fn = (layer.layer_step if fe is not None else
                    layer.append_step if append else layer.step)
-        direct_out = not prefill and layer.two_call
+        direct_out = not prefill and layer.o_absorb is not None
         # Two graphs with their own pinned inputs and result buffers, so that the host
         # can queue step i+1 before it reads step i's result.
         h_ys = [h_y, torch.empty_like(h_y).pin_memory()]
@@ -811,8 +807,8 @@ def main():
                     "frac": achieved / hbm, "traffic": tr[0] if tr else None,
                     "traffic_source": tr[1] if tr else None, "peak_source": peak_src,
                     "kernel": {"attend": "dsa_sparse_mla_decode (split attention + combine)",
-                               "project": "dsa_latent_project (TMA-pipelined o_absorb GEMM + "
-                                          "partial sum)",
+                               "project": "dsa_latent_project (tcgen05 o_absorb GEMM, TMA "
+                                          "ring, K shares summed in a thread-block cluster)",
                                "score": "dsa_score",
                                "frontend": "dsa_frontend (x projections, a-norms, q_absorb and "
                                            "wq_b skinny GEMMs)"}[dom],
@@ -834,7 +830,10 @@ def main():
         "roofline": roofline,
         "stages_ms": stage_ms,
         "stage_timing": ("separate pass, graph with event nodes" if graph_events
-                         else "separate eager pass"),
+                         else "separate eager pass")
+                        + ("; attention and projection timed as two calls (dsa_sparse_mla_decode "
+                           "to olat, dsa_latent_project), the step makes them one"
+                           if layer.o_absorb is not None and layer.two_call and not prefill else ""),
         "compress_ms": min(ct),
         "compress": {"bytes": comp_bytes, "ms": min(ct),
                      "achieved_gbs": comp_bytes / (min(ct) * 1e-3) / 1e9,

@@ -122,6 +122,12 @@ int dsa_abi_version(void);
  *                       merged in CTA 0) or DSA_SELECT_KERNEL_RADIX (the row's
  *                       k-th key found digit by digit from histograms shared across
  *                       the cluster). Both give the same ids.
+ *   DSA_OPT_PROJECT_KERNEL  the o_absorb projection (and the front-end GEMMs):
+ *                       DSA_PROJECT_KERNEL_AUTO (default: the tensor-core form
+ *                       wherever the shape allows it, i.e. hidden a multiple of 128
+ *                       and K of 512), DSA_PROJECT_KERNEL_TCGEN05 (the same),
+ *                       DSA_PROJECT_KERNEL_MMA (the mma.sync stream-K form with
+ *                       its partial-sum reduction).
  *
  * dsa_set_option returns DSA_ERR_INVALID_ARG for an unknown option or value;
  * dsa_get_option returns the current value, or -1 for an unknown option.
@@ -135,6 +141,10 @@ int dsa_abi_version(void);
 #define DSA_OPT_SELECT_KERNEL 2
 #define DSA_SELECT_KERNEL_MERGE 0
 #define DSA_SELECT_KERNEL_RADIX 1
+#define DSA_OPT_PROJECT_KERNEL 3
+#define DSA_PROJECT_KERNEL_AUTO 0
+#define DSA_PROJECT_KERNEL_TCGEN05 1
+#define DSA_PROJECT_KERNEL_MMA 2
 int dsa_set_option(int option, int value);
 int dsa_get_option(int option);
 
@@ -401,7 +411,10 @@ int dsa_select_expand_tail(const float* scores, int rows, int p_stride, int inde
  * (nullable: then y must be NULL and only olat is produced); y [rows, hidden]
  * bf16; olat [rows, heads, kv_lora_rank] f32 (nullable).
  * Limits: kv_lora_rank == 512; hidden % 32 == 0; heads >= 1; qlat, ckv, o_absorb,
- * y, olat and workspace 16-byte aligned (DSA_ERR_INVALID_ARG otherwise).
+ * y, olat and workspace 16-byte aligned (DSA_ERR_INVALID_ARG otherwise). y may be
+ * pinned host memory (its sums are then stored straight into it).
+ * Projection: with hidden % 128 == 0 the tensor-core form (see dsa_latent_project)
+ * takes the bf16 copy of olat this call makes; else the mma.sync stream-K form.
  * Kernels: with 64 heads and at least 4 chunks of 128 tokens per SM
  * (rows * ceil(out_width / 128) >= 4 * SMs: 64 rows of 2,048 tokens) a persistent
  * tensor-core (tcgen05) kernel runs; otherwise a split kernel on mma.sync and a
@@ -508,6 +521,12 @@ int dsa_frontend(const dsa_bf16* x, int rows, int hidden, const dsa_bf16* w_x, i
  * attention (o_absorb = NULL, olat output) and the projection can be scheduled and
  * timed apart; the two-call form gives results identical to the one-call form.
  * olat [rows, heads*kv_lora_rank] f32 (rounded to bf16 as the MMA operand);
+ * Kernel: with hidden % 128 == 0 (and DSA_OPT_PROJECT_KERNEL not forcing mma.sync)
+ * olat is first rounded to a bf16 copy in the workspace, then 128-row tiles of
+ * o_absorb stream through a TMA ring into tcgen05 MMAs (query rows as N, 16 to 64 per
+ * launch), K split over the CTAs of a thread-block cluster whose partials are added
+ * through distributed shared memory in rank order; else the mma.sync stream-K kernel
+ * and its partial-sum reduction. Both are deterministic; they agree within rounding.
  * o_absorb [hidden, heads*kv_lora_rank] bf16; y [rows, hidden] bf16; status as
  * above (DSA_STATUS_TIMEOUT only). Limits: kv_lora_rank == 512; hidden % 64 == 0;
  * olat, o_absorb, y and workspace 16-byte aligned (DSA_ERR_INVALID_ARG otherwise).

@@ -31,6 +31,10 @@ DSA_MLA_KERNEL_CLUSTER = 3
 DSA_OPT_SELECT_KERNEL = 2
 DSA_SELECT_KERNEL_MERGE = 0
 DSA_SELECT_KERNEL_RADIX = 1
+DSA_OPT_PROJECT_KERNEL = 3
+DSA_PROJECT_KERNEL_AUTO = 0
+DSA_PROJECT_KERNEL_TCGEN05 = 1
+DSA_PROJECT_KERNEL_MMA = 2
 
 
 class DsaPaging(ctypes.Structure):

@@ -21,7 +21,7 @@ __all__ = ["paging", "dsa_compress", "dsa_compress_append", "dsa_indexer_store",
            "dsa_frontend_workspace", "dsa_frontend", "dsa_latent_project_workspace",
            "dsa_latent_project", "dsa_select_k",
            "dsa_validate_config", "dsa_set_option", "dsa_get_option", "mla_kernel",
-           "select_kernel", "DsaPaging"]
+           "select_kernel", "project_kernel", "DsaPaging"]
 
 
 def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "tensor",
@@ -94,6 +94,29 @@ class select_kernel:
 
     def __exit__(self, *exc):
         dsa_set_option(_lib.DSA_OPT_SELECT_KERNEL, self.prev)
+        return False
+
+
+class project_kernel:
+    """Context manager pinning the projection kernel: "auto" (the default),
+    "tcgen05" or "mma"; the previous choice is restored on exit."""
+
+    _VALUES = {"auto": _lib.DSA_PROJECT_KERNEL_AUTO, "tcgen05": _lib.DSA_PROJECT_KERNEL_TCGEN05,
+               "mma": _lib.DSA_PROJECT_KERNEL_MMA}
+
+    def __init__(self, which: str):
+        if which not in self._VALUES:
+            raise ValueError(f"kernel {which!r}: one of {sorted(self._VALUES)}")
+        self.value = self._VALUES[which]
+        self.prev = None
+
+    def __enter__(self):
+        self.prev = dsa_get_option(_lib.DSA_OPT_PROJECT_KERNEL)
+        dsa_set_option(_lib.DSA_OPT_PROJECT_KERNEL, self.value)
+        return self
+
+    def __exit__(self, *exc):
+        dsa_set_option(_lib.DSA_OPT_PROJECT_KERNEL, self.prev)
         return False
 
 
@@ -341,7 +364,8 @@ def dsa_sparse_mla_decode(qlat, row_seq, ckv, pg: DsaPaging, token_ids, softmax_
         _ptr(qlat, torch.bfloat16, "qlat"), rows, heads, kvl,
         _ptr(row_seq, torch.int32, "row_seq"), _ptr(ckv, torch.bfloat16, "ckv"),
         ctypes.byref(pg), _ptr(token_ids, torch.int32, "token_ids"), ow, float(softmax_scale),
-        _ptr(o_absorb, torch.bfloat16, "o_absorb"), hidden, _ptr(y, torch.bfloat16, "y"),
+        _ptr(o_absorb, torch.bfloat16, "o_absorb"), hidden,
+        _ptr(y, torch.bfloat16, "y", host_ok=True),
         _ptr(olat, torch.float32, "olat"), _ptr(status, torch.int32, "status"),
         _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)))
 
@@ -368,7 +392,7 @@ def dsa_sparse_mla_decode_fp8(qlat, row_seq, ckv_codes, ckv_scales, pg: DsaPagin
         _ptr(row_seq, torch.int32, "row_seq"), _ptr(ckv_codes, torch.uint8, "ckv_codes"),
         _ptr(ckv_scales, torch.float32, "ckv_scales"), ctypes.byref(pg),
         _ptr(token_ids, torch.int32, "token_ids"), ow, float(softmax_scale),
-        _ptr(o_absorb, torch.bfloat16, "o_absorb"), hidden, _ptr(y, torch.bfloat16, "y"),
+        _ptr(o_absorb, torch.bfloat16, "o_absorb"), hidden, _ptr(y, torch.bfloat16, "y", host_ok=True),
         _ptr(olat, torch.float32, "olat"), _ptr(status, torch.int32, "status"),
         _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)))
 
@@ -453,6 +477,6 @@ def dsa_sparse_mla_decode_noalloc(qlat, row_seq, ckv, pg: DsaPaging, token_ids,
         _ptr(qlat, torch.bfloat16, "qlat"), rows, heads, kvl,
         _ptr(row_seq, torch.int32, "row_seq"), _ptr(ckv, torch.bfloat16, "ckv"),
         ctypes.byref(pg), _ptr(token_ids, torch.int32, "token_ids"), ow, float(softmax_scale),
-        _ptr(o_absorb, torch.bfloat16, "o_absorb"), hidden, _ptr(y, torch.bfloat16, "y"),
+        _ptr(o_absorb, torch.bfloat16, "o_absorb"), hidden, _ptr(y, torch.bfloat16, "y", host_ok=True),
         _ptr(olat, torch.float32, "olat"), _ptr(status, torch.int32, "status"),
         _stream(stream)))

@@ -61,12 +61,15 @@ int set_max_smem(const void* kernel, int bytes) {
 static std::atomic<int> g_opt_pdl{1};
 static std::atomic<int> g_opt_mla_kernel{DSA_MLA_KERNEL_AUTO};
 static std::atomic<int> g_opt_select_kernel{DSA_SELECT_KERNEL_MERGE};
+static std::atomic<int> g_opt_project_kernel{DSA_PROJECT_KERNEL_AUTO};
 
 bool pdl_enabled() { return g_opt_pdl.load(std::memory_order_relaxed) != 0; }
 
 int mla_kernel_choice() { return g_opt_mla_kernel.load(std::memory_order_relaxed); }
 
 int select_kernel_choice() { return g_opt_select_kernel.load(std::memory_order_relaxed); }
+
+int project_kernel_choice() { return g_opt_project_kernel.load(std::memory_order_relaxed); }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -205,6 +208,13 @@ int dsa_set_option(int option, int value) {
                             "dsa_set_option: DSA_OPT_SELECT_KERNEL takes 0 or 1, not %d", value);
             g_opt_select_kernel.store(value, std::memory_order_relaxed);
             return DSA_OK;
+        case DSA_OPT_PROJECT_KERNEL:
+            if (value != DSA_PROJECT_KERNEL_AUTO && value != DSA_PROJECT_KERNEL_TCGEN05 &&
+                value != DSA_PROJECT_KERNEL_MMA)
+                return fail(DSA_ERR_INVALID_ARG,
+                            "dsa_set_option: DSA_OPT_PROJECT_KERNEL takes 0, 1 or 2, not %d", value);
+            g_opt_project_kernel.store(value, std::memory_order_relaxed);
+            return DSA_OK;
         default:
             return fail(DSA_ERR_INVALID_ARG, "dsa_set_option: unknown option %d", option);
     }
@@ -215,6 +225,7 @@ int dsa_get_option(int option) {
         case DSA_OPT_PDL: return g_opt_pdl.load(std::memory_order_relaxed);
         case DSA_OPT_MLA_KERNEL: return g_opt_mla_kernel.load(std::memory_order_relaxed);
         case DSA_OPT_SELECT_KERNEL: return g_opt_select_kernel.load(std::memory_order_relaxed);
+        case DSA_OPT_PROJECT_KERNEL: return g_opt_project_kernel.load(std::memory_order_relaxed);
         default: return -1;
     }
 }

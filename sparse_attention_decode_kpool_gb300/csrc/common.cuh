@@ -32,6 +32,7 @@ int set_max_smem(const void* kernel, int bytes);  // once per (device, kernel)
 bool pdl_enabled();
 int mla_kernel_choice();     // DSA_OPT_MLA_KERNEL
 int select_kernel_choice();  // DSA_OPT_SELECT_KERNEL
+int project_kernel_choice();  // DSA_OPT_PROJECT_KERNEL
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t st, Args&&... args) {
@@ -73,6 +74,13 @@ int make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, 
 // y2, output columns from `split` (a multiple of 64) on go to y2 [rows, hidden - split]
 // and y is [rows, split].
 bool project_supported(int K, int hidden);
+// The tensor-core form (project_tc.cu): hidden a multiple of 128, K of 512.
+bool project_tc_supported(int K, int hidden);
+// f32 x is rounded to bf16 into the workspace first (project_tc_convert_bytes).
+size_t project_tc_convert_bytes(int rows, int K);
+int project_tc_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A, int hidden,
+                      uint16_t* y, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st,
+                      float* yf, uint16_t* y2, int split);
 size_t project_workspace_bytes(int rows, int K, int hidden, int sms);
 int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A, int hidden,
                    uint16_t* y, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st,

@@ -400,7 +400,10 @@ int dispatch(const ProjArgs& a, int nt, int G, cudaStream_t st) {
 bool project_supported(int K, int hidden) { return hidden > 0 && hidden % MROWS == 0 && K % KT == 0; }
 
 size_t project_workspace_bytes(int rows, int K, int hidden, int sms) {
-    return plan_for(rows, K, hidden, sms).bytes;
+    // the stream-K partials, or the tensor-core form's bf16 copy of an f32 x
+    const size_t part = plan_for(rows, K, hidden, sms).bytes;
+    const size_t conv = project_tc_supported(K, hidden) ? project_tc_convert_bytes(rows, K) : 0;
+    return part > conv ? part : conv;
 }
 
 int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A, int hidden,
@@ -413,6 +416,11 @@ int project_launch(const void* x, bool x_f32, int rows, int K, const uint16_t* A
     out.split = y2 ? split : hidden;
     const int sms = sm_count();
     if (sms <= 0) return fail(DSA_ERR_CUDA, "projection: no CUDA device");
+    // The tensor-core form where the shape allows it (128-row tiles of A, K in eight
+    // equal shares of 64-column stages); no reduction launch follows it.
+    if (project_kernel_choice() != DSA_PROJECT_KERNEL_MMA && project_tc_supported(K, hidden))
+        return project_tc_launch(x, x_f32, rows, K, A, hidden, y, status, ws, ws_bytes, st, yf, y2,
+                                 split);
     const ProjPlan p = plan_for(rows, K, hidden, sms);
     if (ws_bytes < p.bytes) return fail(DSA_ERR_INVALID_ARG, "projection: workspace too small");
     ProjArgs a;

@@ -92,8 +92,11 @@ class DsaDecodeLayer:
                      if (keep_olat or self.o_absorb is not None) else None)
         ws = api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, 0, False)
         self.workspace = torch.zeros(max(ws, 1), dtype=torch.uint8, device=dev)
-        # Two-call form (attention, then dsa_latent_project) where the projection
-        # kernel supports the shape (hidden % 64 == 0); else the one-call form.
+        # The stages attend() and project() are the two-call form (attention to olat,
+        # then dsa_latent_project) where the projection kernels support the shape
+        # (hidden % 64 == 0); else attend() makes the one call. step() makes the one
+        # call (attention and projection, olat as bf16 straight into the projection)
+        # whenever o_absorb is present.
         self.two_call = bool(hidden) and hidden % 64 == 0
         pws = api.dsa_latent_project_workspace(R, g.heads, hidden) if self.two_call else 0
         self.proj_workspace = torch.zeros(max(pws, 1), dtype=torch.uint8, device=dev)
@@ -373,13 +376,21 @@ class DsaDecodeLayer:
             api.dsa_latent_project(self.olat, self.o_absorb, self.y, self.status,
                                    self.proj_workspace, stream=stream)
 
+    def attend_project(self, stream=None) -> None:
+        """Sparse latent attention and the o_absorb projection in one call (olat f32
+        and y); without o_absorb, the attention alone."""
+        if self.o_absorb is not None:
+            self._mla(self.o_absorb, self.y, self.fused_workspace(), stream)
+        else:
+            self._mla(None, None, self.workspace, stream)
+
     def step(self, stream=None) -> None:
-        """One decode step over the whole batch: score, select, expand, attend, project."""
+        """One decode step over the whole batch: score, select (with the token ids),
+        attention and projection."""
         self.score(stream)
         self.select(stream)
         self.expand(stream)
-        self.attend(stream)
-        self.project(stream)
+        self.attend_project(stream)
 
     def launches_per_step(self) -> int:
         """Library kernel launches one step() makes."""
@@ -388,7 +399,12 @@ class DsaDecodeLayer:
         if api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, 0, False) > 0:
             n += 1  # split combine
         if self.o_absorb is not None:
-            n += (R + 63) // 64 + 1  # projection kernel(s) + reduction (either form)
+            # tensor-core projection: one launch per 64 query rows; else the stream-K
+            # kernel(s) and the partial-sum reduction
+            tc = (api.dsa_get_option(api._lib.DSA_OPT_PROJECT_KERNEL)
+                  != api._lib.DSA_PROJECT_KERNEL_MMA and g.hidden % 128 == 0
+                  and (g.heads * g.kv_lora_rank) % 512 == 0)
+            n += (R + 63) // 64 + (0 if tc else 1)
         return n
 
     def capture_layer(self) -> torch.cuda.CUDAGraph:

@@ -539,11 +539,21 @@ def test_bad_block_table_entry_sets_status():
     assert (layer.olat[1].abs().sum().item() == 0.0)  # all of row 1's tokens skipped
 
 
-PROJECT_CASES = [(8, 64, 4096), (1, 64, 4096), (3, 4, 1024), (70, 16, 256), (20, 8, 128)]
+PROJECT_CASES = [(8, 64, 4096), (1, 64, 4096), (3, 4, 1024), (70, 16, 256), (20, 8, 128),
+                 (64, 64, 4096), (128, 8, 512), (16, 64, 1024), (33, 8, 384)]
+
+
+@pytest.fixture(params=["tcgen05", "mma"])
+def proj_kernel(request):
+    """Both projection kernels, forced through DSA_OPT_PROJECT_KERNEL (shapes the
+    tensor-core form does not take, hidden not a multiple of 128, run the mma.sync
+    form either way)."""
+    with api.project_kernel(request.param):
+        yield request.param
 
 
 @pytest.mark.parametrize("rows,heads,hidden", PROJECT_CASES)
-def test_latent_project_parity(rows, heads, hidden):
+def test_latent_project_parity(rows, heads, hidden, proj_kernel):
     rng = np.random.default_rng(rows * 100 + heads)
     olat = torch.from_numpy(rng.standard_normal((rows, heads, 512)).astype(np.float32))
     A = torch.from_numpy((rng.standard_normal((hidden, heads * 512)) * 0.02).astype(np.float32)
