@@ -47,7 +47,7 @@ struct PL {  // shared-memory layout of one CTA (offsets from a 1024-aligned bas
     // Bytes of A in flight are what keep the stream at HBM speed (about 160 KB per
     // SM): two CTAs per SM with 16 query rows, one otherwise.
     static constexpr int CTAS_PER_SM = (MT == 1 && N <= 16 && KS == 8) ? 2 : 1;
-    static constexpr int S_FIT = (int)((200u * 1024u / CTAS_PER_SM) / STAGE);
+    static constexpr int S_FIT = (int)(((CTAS_PER_SM == 2 ? 220u : 200u) * 1024u / CTAS_PER_SM) / STAGE);
     static constexpr int S = S_FIT > kMaxStages ? kMaxStages : S_FIT;  // ring stages
     static constexpr uint32_t RED = MT * BM * N * 4;            // the partial, f32 [MT*BM][N]
     static constexpr uint32_t RING = S * STAGE;
