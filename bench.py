@@ -193,7 +193,10 @@ def algorithmic_bytes(wl, layer) -> dict:
     app = 0
     if layer.decode_from is not None:
         ihd, kp = g.index_head_dim, g.index_kpool
-        app = wl.batch * (2 * (2 * ihd + g.kv_lora_rank) * 2 + 1
+        # the latent row goes out as bf16, or (FP8 cache) as codes and scales
+        ckv_out = (g.kv_lora_rank + g.kv_lora_rank // 128 * 4 if layer.latent_fp8
+                   else g.kv_lora_rank * 2)
+        app = wl.batch * ((2 * ihd + g.kv_lora_rank) * 2 + 2 * ihd * 2 + ckv_out + 1
                           + kp * (2 * ihd * 2 + 1) + ihd * 2 + 1)
     # --frontend: every front-end weight once, the hidden state in, and its outputs
     # (qlat, qidx, w, the staged rows) out.
@@ -409,6 +412,7 @@ def workload_config(wl, args) -> dict:
             "latent_cache": "fp8-e4m3" if getattr(args, "latent_fp8", False) else "bf16",
             "frontend": ({"q_lora_rank": args.q_lora_rank}
                          if getattr(args, "frontend", False) else None),
+            "o_absorb_l2_prefetch_mib": getattr(args, "l2_prefetch_mib_used", 0.0),
             "l2": "flushed between timed steps (256 MiB write, then a 256 MiB read so the dirty "
                   "lines are written back; both outside the timed events)",
             "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
@@ -437,6 +441,10 @@ def main():
     ap.add_argument("--latent-fp8", action="store_true",
                     help="attention reads an FP8 latent cache (E4M3 codes + power-of-two "
                          "scales per 128 channels) encoded once from the bf16 cache")
+    ap.add_argument("--l2-prefetch-mb", type=float, default=None,
+                    help="MiB of o_absorb prefetched into L2 on a second graph branch "
+                         "while top-k and the gather run (default: the layer's choice, "
+                         "64 MiB for the GLM-5.3 o_absorb; 0 turns it off)")
     ap.add_argument("--always-select-tail", action="store_true",
                     help="index rows index_topk + kpool - 1 wide, the trailing partial "
                          "pool's tokens always attended")
@@ -474,7 +482,10 @@ def main():
             raise SystemExit("--frontend applies to the decode workloads")
         fe = W.make_frontend(wl.geom, wl.rows, q_lora_rank=args.q_lora_rank, seed=wl.seed + 100)
     layer = DsaDecodeLayer(wl, device=str(dev), with_o_absorb=not prefill, keep_olat=prefill,
-                           decode_from=decode_from, latent_fp8=args.latent_fp8, frontend=fe)
+                           decode_from=decode_from, latent_fp8=args.latent_fp8, frontend=fe,
+                           l2_prefetch_bytes=(None if args.l2_prefetch_mb is None
+                                              else int(args.l2_prefetch_mb * (1 << 20))))
+    args.l2_prefetch_mib_used = layer.l2_prefetch_bytes / (1 << 20)
     if append:
         layer.stage(0)  # the staged rows stay as they are for every replay
     layer.compress()
@@ -833,7 +844,9 @@ def main():
                          else "separate eager pass")
                         + ("; attention and projection timed as two calls (dsa_sparse_mla_decode "
                            "to olat, dsa_latent_project), the step makes them one"
-                           if layer.o_absorb is not None and layer.two_call and not prefill else ""),
+                           if layer.o_absorb is not None and layer.two_call and not prefill else "")
+                        + ("; no o_absorb L2 prefetch branch in this pass (the projection "
+                           "streams all of o_absorb from HBM)" if layer.l2_prefetch_bytes else ""),
         "compress_ms": min(ct),
         "compress": {"bytes": comp_bytes, "ms": min(ct),
                      "achieved_gbs": comp_bytes / (min(ct) * 1e-3) / 1e9,

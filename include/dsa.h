@@ -94,7 +94,7 @@ const char* dsa_last_error(void);
 
 /* ABI version of this header (bumped on any signature change). */
 int dsa_abi_version(void);
-#define DSA_ABI_VERSION 7
+#define DSA_ABI_VERSION 8
 
 /*
  * Process-wide launch options (no counterpart on the pages: they choose between
@@ -147,6 +147,17 @@ int dsa_abi_version(void);
 #define DSA_PROJECT_KERNEL_MMA 2
 int dsa_set_option(int option, int value);
 int dsa_get_option(int option);
+
+/*
+ * dsa_prefetch_l2 -- ask the memory system to bring the device range
+ * [ptr, ptr + bytes) into L2 (bulk prefetch, 16 KB per request; the tail below 16
+ * bytes is ignored). Meant for read-only data needed soon, such as o_absorb, issued
+ * on a second stream or graph branch beside latency-bound stages so that the
+ * projection finds part of its weights in L2. A hint: nothing is written, nothing
+ * waits for it, and results never depend on it. ptr must be 16-byte aligned;
+ * bytes == 0 is a no-op. The range should stay well below the L2's 126 MB.
+ */
+int dsa_prefetch_l2(const void* ptr, size_t bytes, void* stream);
 
 /*
  * Layer-geometry rules (mod.rs, Glm5NextDsaConfig::validate): index_kpool and
@@ -270,6 +281,24 @@ int dsa_decode_append(const dsa_bf16* k_new, const dsa_bf16* gate_new, const dsa
                       int kv_lora_rank, dsa_bf16* k_raw, dsa_bf16* gate, uint8_t* token_valid,
                       dsa_bf16* ckv, dsa_bf16* kpool_out, uint8_t* pool_valid, int32_t* pool_idx,
                       int32_t* row_ctx, int32_t* status, void* stream);
+
+/*
+ * dsa_decode_append_fp8 -- dsa_decode_append for a layer with the FP8 latent cache
+ * (see dsa_quantize_latent): the staged latent row ckv_new is also encoded into
+ * ckv_codes [.., kv_lora_rank] u8 and ckv_scales [.., kv_lora_rank / 128] f32 at the
+ * token's cache row, with the same codec, so the bytes equal what
+ * dsa_quantize_latent makes of that row. ckv (the bf16 latent cache) is nullable
+ * here; ckv_new is required. Limits: those of dsa_decode_append, kv_lora_rank % 128
+ * == 0, FP8 caches 16-byte aligned. No counterpart on the pages (their FP8 kernel's
+ * format is not given; this library's is stated at dsa_quantize_latent).
+ */
+int dsa_decode_append_fp8(const dsa_bf16* k_new, const dsa_bf16* gate_new,
+                          const dsa_bf16* ckv_new, const float* ape, const dsa_bf16* ln_w,
+                          const dsa_bf16* ln_b, float eps, const dsa_paging* pg, int32_t* seq_lens,
+                          int first_key, int kpool, int ihd, int kv_lora_rank, dsa_bf16* k_raw,
+                          dsa_bf16* gate, uint8_t* token_valid, dsa_bf16* ckv, uint8_t* ckv_codes,
+                          float* ckv_scales, dsa_bf16* kpool_out, uint8_t* pool_valid,
+                          int32_t* pool_idx, int32_t* row_ctx, int32_t* status, void* stream);
 
 /*
  * dsa_score -- dsa_index_scores (tp.rs, "Why the indexer is replicated": a sum

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdsa.so")
-SOURCES = ["api.cu", "compress.cu", "score.cu", "score_prefill.cu", "select.cu", "mla.cu", "mla_tc.cu", "mla_dec.cu", "project.cu", "project_tc.cu", "mla_noalloc.cu", "append.cu", "fp8.cu", "frontend.cu"]
+SOURCES = ["api.cu", "compress.cu", "score.cu", "score_prefill.cu", "select.cu", "mla.cu", "mla_tc.cu", "mla_dec.cu", "project.cu", "project_tc.cu", "prefetch.cu", "mla_noalloc.cu", "append.cu", "fp8.cu", "frontend.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -21,7 +21,7 @@ DSA_STATUS_BAD_TOKEN = 1
 DSA_STATUS_BAD_BLOCK = 2
 DSA_STATUS_TIMEOUT = 4
 DSA_STATUS_CACHE_FULL = 8
-DSA_ABI_VERSION = 7
+DSA_ABI_VERSION = 8
 DSA_OPT_PDL = 0
 DSA_OPT_MLA_KERNEL = 1
 DSA_MLA_KERNEL_AUTO = 0
@@ -60,6 +60,7 @@ SIGNATURES = {
     "dsa_last_error": (ctypes.c_char_p, []),
     "dsa_abi_version": (_I, []),
     "dsa_set_option": (_I, [_I, _I]),
+    "dsa_prefetch_l2": (_I, [_P, _SZ, _P]),
     "dsa_get_option": (_I, [_I]),
     "dsa_validate_config": (_I, [_I, _I, _I, _I]),
     "dsa_select_k": (_I, [_I, _I, _I]),
@@ -70,6 +71,8 @@ SIGNATURES = {
     "dsa_write_geom": (_I, [_P, _I, _P, _I, _P, _P, _P]),
     "dsa_decode_append": (_I, [_P, _P, _P, _P, _P, _P, _F, _PG, _P, _I, _I, _I, _I, _P, _P, _P,
                                _P, _P, _P, _P, _P, _P, _P]),
+    "dsa_decode_append_fp8": (_I, [_P, _P, _P, _P, _P, _P, _F, _PG, _P, _I, _I, _I, _I, _P, _P,
+                                   _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dsa_score": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _PG, _I, _I, _F, _P, _I, _P, _P]),
     "dsa_score_prefill": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _PG, _I, _I, _F, _P, _I, _P,
                                _P]),

@@ -14,13 +14,13 @@ from . import _lib
 from ._lib import DsaPaging, check
 
 __all__ = ["paging", "dsa_compress", "dsa_compress_append", "dsa_indexer_store",
-           "dsa_write_geom", "dsa_decode_append", "dsa_score", "dsa_score_prefill", "dsa_select", "dsa_expand",
+           "dsa_write_geom", "dsa_decode_append", "dsa_decode_append_fp8", "dsa_score", "dsa_score_prefill", "dsa_select", "dsa_expand",
            "dsa_select_expand", "dsa_expand_tail", "dsa_select_expand_tail",
            "dsa_sparse_mla_decode_workspace", "dsa_sparse_mla_decode",
            "dsa_sparse_mla_decode_noalloc", "dsa_sparse_mla_decode_fp8", "dsa_quantize_latent",
            "dsa_frontend_workspace", "dsa_frontend", "dsa_latent_project_workspace",
            "dsa_latent_project", "dsa_select_k",
-           "dsa_validate_config", "dsa_set_option", "dsa_get_option", "mla_kernel",
+           "dsa_validate_config", "dsa_prefetch_l2", "dsa_set_option", "dsa_get_option", "mla_kernel",
            "select_kernel", "project_kernel", "DsaPaging"]
 
 
@@ -231,6 +231,31 @@ def dsa_decode_append(k_new, gate_new, ape, ln_w, ln_b, eps: float, pg: DsaPagin
         ctypes.byref(pg), _ptr(seq_lens, torch.int32, "seq_lens"), int(first_key), int(kpool),
         ihd, kvl, _ptr(k_raw, torch.bfloat16, "k_raw"), _ptr(gate, torch.bfloat16, "gate"),
         _ptr(token_valid, torch.uint8, "token_valid"), _ptr(ckv, torch.bfloat16, "ckv"),
+        _ptr(kpool_out, torch.bfloat16, "kpool_out"), _ptr(pool_valid, torch.uint8, "pool_valid"),
+        _ptr(pool_idx, torch.int32, "pool_idx"), _ptr(row_ctx, torch.int32, "row_ctx"),
+        _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def dsa_decode_append_fp8(k_new, gate_new, ckv_new, ape, ln_w, ln_b, eps: float, pg: DsaPaging,
+                          seq_lens, first_key: int, kpool: int, k_raw, gate, token_valid,
+                          ckv_codes, ckv_scales, kpool_out, pool_valid, ckv=None, pool_idx=None,
+                          row_ctx=None, status=None, stream=None) -> None:
+    """dsa_decode_append that also encodes the staged latent row into the FP8 cache
+    (same codec and bytes as dsa_quantize_latent); the bf16 cache ``ckv`` is optional."""
+    batch, ihd = (int(x) for x in k_new.shape)
+    if tuple(gate_new.shape) != (batch, ihd):
+        raise ValueError(f"gate_new must be [{batch}, {ihd}]")
+    kvl = int(ckv_new.shape[-1])
+    if int(ckv_codes.shape[-1]) != kvl or int(ckv_scales.shape[-1]) != kvl // 128:
+        raise ValueError(f"ckv_codes must be [.., {kvl}] and ckv_scales [.., {kvl // 128}]")
+    check(_lib.load().dsa_decode_append_fp8(
+        _ptr(k_new, torch.bfloat16, "k_new"), _ptr(gate_new, torch.bfloat16, "gate_new"),
+        _ptr(ckv_new, torch.bfloat16, "ckv_new"), _ptr(ape, torch.float32, "ape"),
+        _ptr(ln_w, torch.bfloat16, "ln_w"), _ptr(ln_b, torch.bfloat16, "ln_b"), float(eps),
+        ctypes.byref(pg), _ptr(seq_lens, torch.int32, "seq_lens"), int(first_key), int(kpool),
+        ihd, kvl, _ptr(k_raw, torch.bfloat16, "k_raw"), _ptr(gate, torch.bfloat16, "gate"),
+        _ptr(token_valid, torch.uint8, "token_valid"), _ptr(ckv, torch.bfloat16, "ckv"),
+        _ptr(ckv_codes, torch.uint8, "ckv_codes"), _ptr(ckv_scales, torch.float32, "ckv_scales"),
         _ptr(kpool_out, torch.bfloat16, "kpool_out"), _ptr(pool_valid, torch.uint8, "pool_valid"),
         _ptr(pool_idx, torch.int32, "pool_idx"), _ptr(row_ctx, torch.int32, "row_ctx"),
         _ptr(status, torch.int32, "status"), _stream(stream)))
@@ -449,6 +474,14 @@ def dsa_latent_project_workspace(rows: int, heads: int, hidden: int,
     check(_lib.load().dsa_latent_project_workspace(int(rows), int(heads), int(kv_lora_rank),
                                                    int(hidden), ctypes.byref(n)))
     return int(n.value)
+
+
+def dsa_prefetch_l2(t: torch.Tensor, nbytes: Optional[int] = None, stream=None) -> None:
+    """Bring the first nbytes of device tensor t (all of it by default) into L2: a hint
+    issued beside latency-bound work, e.g. on a second stream."""
+    total = t.numel() * t.element_size()
+    n = total if nbytes is None else min(int(nbytes), total)
+    check(_lib.load().dsa_prefetch_l2(_ptr(t, None, "t"), n, _stream(stream)))
 
 
 def dsa_latent_project(olat, o_absorb, y, status=None, workspace=None, stream=None) -> None:

@@ -29,6 +29,9 @@ int set_max_smem(const void* kernel, int bytes);  // once per (device, kernel)
 // ahead of the q GEMM. Elsewhere, dependent blocks waiting beside a running grid
 // slowed it. dsa_set_option(DSA_OPT_PDL, 0) turns the attribute off (the wait then
 // returns at once).
+// Bytes of [p, p + bytes), from p on, that the last dsa_prefetch_l2 on this device
+// staged in L2 at evict_last priority (0 if p is outside that range).
+size_t l2_staged_overlap(const void* p, size_t bytes);
 bool pdl_enabled();
 int mla_kernel_choice();     // DSA_OPT_MLA_KERNEL
 int select_kernel_choice();  // DSA_OPT_SELECT_KERNEL
@@ -178,6 +181,14 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int sr
                  "r"(src_bytes)
                  : "memory");
 }
+// L2 eviction-priority policy for the cache_hint copy forms below: data read once
+// per call (the o_absorb stream) is loaded evict_first, so it does not push out
+// lines staged in L2 for later use.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+    return p;
+}
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
@@ -272,6 +283,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+// tma_load_2d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 __device__ __forceinline__ uint4 lds16(uint32_t addr) {

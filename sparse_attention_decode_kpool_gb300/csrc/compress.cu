@@ -18,6 +18,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "fp8.cuh"
 #include "store.cuh"
 
 namespace dsa {
@@ -257,6 +258,8 @@ struct AppendArgs {
     uint16_t* gate;
     uint8_t* valid;
     uint16_t* ckv;
+    uint8_t* ckv8;      // nullable: the FP8 latent cache's codes ...
+    float* ckv_scale;   // ... and scales, written from ckv_new
     int32_t* seq_lens;
     int32_t* row_ctx;
     int32_t* status;
@@ -286,9 +289,19 @@ __global__ void __launch_bounds__(kAppendThreads) decode_append_kernel(AppendArg
     __syncthreads();
     const long long row = s_row;
     const int t = s_t;
-    if (row >= 0)
+    if (row >= 0) {
         store_token_rows(a.k_new, a.gate_new, a.ckv_new, a.k_raw, a.gate, a.valid, a.ckv, b, row,
                          IHD, a.kvl);
+        if (a.ckv8) {
+            // the FP8 cache: warp w encodes 128-channel groups w, w + 4, ... of the
+            // staged latent row, with the same codec as dsa_quantize_latent
+            const int G = a.kvl / 128;
+            for (int gi = threadIdx.x >> 5; gi < G; gi += kAppendThreads / 32)
+                fp8_encode_group(a.ckv_new + (long long)b * a.kvl + gi * 128,
+                                 a.ckv8 + row * a.kvl + gi * 128, a.ckv_scale + row * G + gi,
+                                 threadIdx.x & 31);
+        }
+    }
     __syncthreads();  // the stored rows are visible to the whole block from here on
     const int L = row >= 0 ? t + 1 : t;
     if (threadIdx.x == 0) {
@@ -436,15 +449,15 @@ extern "C" int dsa_compress_append(const dsa_bf16* k_raw, const dsa_bf16* gate,
                          status, stream);
 }
 
-extern "C" int dsa_decode_append(const dsa_bf16* k_new, const dsa_bf16* gate_new,
-                                 const dsa_bf16* ckv_new, const float* ape, const dsa_bf16* ln_w,
-                                 const dsa_bf16* ln_b, float eps, const dsa_paging* pg,
-                                 int32_t* seq_lens, int first_key, int kpool, int ihd,
-                                 int kv_lora_rank, dsa_bf16* k_raw, dsa_bf16* gate,
-                                 uint8_t* token_valid, dsa_bf16* ckv, dsa_bf16* kpool_out,
-                                 uint8_t* pool_valid, int32_t* pool_idx, int32_t* row_ctx,
-                                 int32_t* status, void* stream) {
-    const char* name = "dsa_decode_append";
+namespace {
+// dsa_decode_append and dsa_decode_append_fp8 (ckv8 / ckv_scale set).
+int decode_append_impl(const char* name, const dsa_bf16* k_new, const dsa_bf16* gate_new,
+                       const dsa_bf16* ckv_new, const float* ape, const dsa_bf16* ln_w,
+                       const dsa_bf16* ln_b, float eps, const dsa_paging* pg, int32_t* seq_lens,
+                       int first_key, int kpool, int ihd, int kv_lora_rank, dsa_bf16* k_raw,
+                       dsa_bf16* gate, uint8_t* token_valid, dsa_bf16* ckv, uint8_t* ckv8,
+                       float* ckv_scale, dsa_bf16* kpool_out, uint8_t* pool_valid,
+                       int32_t* pool_idx, int32_t* row_ctx, int32_t* status, void* stream) {
     if (kpool < 1 || kpool > DSA_MAX_KPOOL)
         return fail(DSA_ERR_UNSUPPORTED, "%s: kpool %d outside [1, %d]", name, kpool,
                     DSA_MAX_KPOOL);
@@ -452,10 +465,16 @@ extern "C" int dsa_decode_append(const dsa_bf16* k_new, const dsa_bf16* gate_new
         return fail(DSA_ERR_UNSUPPORTED, "%s: index_head_dim %d not in {64, 128}", name, ihd);
     if (first_key < 0) return fail(DSA_ERR_INVALID_ARG, "%s: first_key %d < 0", name, first_key);
     if (!(eps >= 0.f)) return fail(DSA_ERR_INVALID_ARG, "%s: eps must be >= 0", name);
-    if ((ckv == nullptr) != (ckv_new == nullptr))
-        return fail(DSA_ERR_INVALID_ARG, "%s: ckv and ckv_new go together", name);
-    if (ckv && (kv_lora_rank < 8 || kv_lora_rank % 8 != 0))
+    const bool fp8 = ckv8 != nullptr;
+    if (fp8 != (ckv_scale != nullptr))
+        return fail(DSA_ERR_INVALID_ARG, "%s: ckv_codes and ckv_scales go together", name);
+    if (fp8 ? !ckv_new : (ckv == nullptr) != (ckv_new == nullptr))
+        return fail(DSA_ERR_INVALID_ARG, "%s: ckv_new and the latent cache go together", name);
+    if (ckv_new && (kv_lora_rank < 8 || kv_lora_rank % 8 != 0))
         return fail(DSA_ERR_INVALID_ARG, "%s: kv_lora_rank %d not a multiple of 8", name,
+                    kv_lora_rank);
+    if (fp8 && kv_lora_rank % 128 != 0)
+        return fail(DSA_ERR_INVALID_ARG, "%s: kv_lora_rank %d not a multiple of 128", name,
                     kv_lora_rank);
     Paging P;
     int rc = check_paging(pg, kpool, &P);
@@ -472,7 +491,7 @@ extern "C" int dsa_decode_append(const dsa_bf16* k_new, const dsa_bf16* gate_new
         return fail(DSA_ERR_INVALID_ARG, "%s: NULL tensor", name);
     if ((((uintptr_t)k_new) | ((uintptr_t)gate_new) | ((uintptr_t)ckv_new) | ((uintptr_t)k_raw) |
          ((uintptr_t)gate) | ((uintptr_t)ckv) | ((uintptr_t)kpool_out) | ((uintptr_t)ape) |
-         ((uintptr_t)ln_w) | ((uintptr_t)ln_b)) & 15)
+         ((uintptr_t)ln_w) | ((uintptr_t)ln_b) | ((uintptr_t)ckv8) | ((uintptr_t)ckv_scale)) & 15)
         return fail(DSA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", name);
     AppendArgs a;
     a.k_new = k_new;
@@ -482,6 +501,8 @@ extern "C" int dsa_decode_append(const dsa_bf16* k_new, const dsa_bf16* gate_new
     a.gate = gate;
     a.valid = token_valid;
     a.ckv = ckv;
+    a.ckv8 = ckv8;
+    a.ckv_scale = ckv_scale;
     a.seq_lens = seq_lens;
     a.row_ctx = row_ctx;
     a.status = status;
@@ -508,4 +529,36 @@ extern "C" int dsa_decode_append(const dsa_bf16* k_new, const dsa_bf16* gate_new
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_decode_append launch");
     return DSA_OK;
+}
+}  // namespace
+
+extern "C" int dsa_decode_append(const dsa_bf16* k_new, const dsa_bf16* gate_new,
+                                 const dsa_bf16* ckv_new, const float* ape, const dsa_bf16* ln_w,
+                                 const dsa_bf16* ln_b, float eps, const dsa_paging* pg,
+                                 int32_t* seq_lens, int first_key, int kpool, int ihd,
+                                 int kv_lora_rank, dsa_bf16* k_raw, dsa_bf16* gate,
+                                 uint8_t* token_valid, dsa_bf16* ckv, dsa_bf16* kpool_out,
+                                 uint8_t* pool_valid, int32_t* pool_idx, int32_t* row_ctx,
+                                 int32_t* status, void* stream) {
+    return decode_append_impl("dsa_decode_append", k_new, gate_new, ckv_new, ape, ln_w, ln_b, eps,
+                              pg, seq_lens, first_key, kpool, ihd, kv_lora_rank, k_raw, gate,
+                              token_valid, ckv, nullptr, nullptr, kpool_out, pool_valid, pool_idx,
+                              row_ctx, status, stream);
+}
+
+extern "C" int dsa_decode_append_fp8(const dsa_bf16* k_new, const dsa_bf16* gate_new,
+                                     const dsa_bf16* ckv_new, const float* ape,
+                                     const dsa_bf16* ln_w, const dsa_bf16* ln_b, float eps,
+                                     const dsa_paging* pg, int32_t* seq_lens, int first_key,
+                                     int kpool, int ihd, int kv_lora_rank, dsa_bf16* k_raw,
+                                     dsa_bf16* gate, uint8_t* token_valid, dsa_bf16* ckv,
+                                     uint8_t* ckv_codes, float* ckv_scales, dsa_bf16* kpool_out,
+                                     uint8_t* pool_valid, int32_t* pool_idx, int32_t* row_ctx,
+                                     int32_t* status, void* stream) {
+    if (!ckv_codes || !ckv_scales)
+        return fail(DSA_ERR_INVALID_ARG, "dsa_decode_append_fp8: NULL FP8 cache");
+    return decode_append_impl("dsa_decode_append_fp8", k_new, gate_new, ckv_new, ape, ln_w, ln_b,
+                              eps, pg, seq_lens, first_key, kpool, ihd, kv_lora_rank, k_raw, gate,
+                              token_valid, ckv, ckv_codes, ckv_scales, kpool_out, pool_valid,
+                              pool_idx, row_ctx, status, stream);
 }

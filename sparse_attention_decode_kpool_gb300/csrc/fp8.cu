@@ -9,32 +9,13 @@
 //
 // One warp per latent row; for each 128-channel group every lane takes 4 channels,
 // the group's largest magnitude comes from a warp max, and the scale exponent from
-// its float bits.
-#include "common.cuh"
+// its float bits (fp8.cuh).
+#include "fp8.cuh"
 
 namespace dsa {
 namespace {
 
 constexpr int kQuantWarps = 8;
-
-// k for a group's largest magnitude (amax >= 0, finite).
-__device__ __forceinline__ int fp8_scale_exp(float amax) {
-    const uint32_t bits = __float_as_uint(amax);
-    if (bits == 0u) return 0;
-    const int E = (int)(bits >> 23);
-    if (E == 0) return -126;  // below 2^-126: the clamp
-    const uint32_t mant = bits & 0x7fffffu;
-    // amax = m * 2^e with m in [1, 2): amax <= 448 * 2^k  <=>  m * 2^(e-k) <= 1.75 * 2^8
-    const int e = E - 127;
-    const int k = mant <= 0x600000u ? e - 8 : e - 7;
-    return k < -126 ? -126 : k;
-}
-
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    unsigned short r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
 
 __global__ void __launch_bounds__(kQuantWarps * 32) quantize_latent_kernel(
     const uint16_t* __restrict__ x, long long rows, int kvl, uint8_t* __restrict__ codes,
@@ -44,19 +25,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_latent_kernel(
     const long long r = (long long)blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
     if (r >= rows) return;
     const int G = kvl / 128;
-    for (int gi = 0; gi < G; ++gi) {
-        const long long off = r * kvl + gi * 128 + lane * 4;
-        const uint2 v = __ldg(reinterpret_cast<const uint2*>(x + off));
-        const float f0 = bf16_lo(v.x), f1 = bf16_hi(v.x), f2 = bf16_lo(v.y), f3 = bf16_hi(v.y);
-        float m = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const int k = fp8_scale_exp(m);
-        const float inv = __uint_as_float((uint32_t)(127 - k) << 23);  // 2^-k, exact
-        const uint32_t c = e4m3x2(f0 * inv, f1 * inv) | (e4m3x2(f2 * inv, f3 * inv) << 16);
-        *reinterpret_cast<uint32_t*>(codes + off) = c;
-        if (lane == 0) scales[r * G + gi] = __uint_as_float((uint32_t)(k + 127) << 23);
-    }
+    for (int gi = 0; gi < G; ++gi)
+        fp8_encode_group(x + r * kvl + gi * 128, codes + r * kvl + gi * 128, scales + r * G + gi, lane);
 }
 
 }  // namespace

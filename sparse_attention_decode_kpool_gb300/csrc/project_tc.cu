@@ -108,6 +108,8 @@ struct TcProjArgs {
     int n0;         // first query row of this launch
     int nrows;      // query rows of this launch (<= N)
     int kper;       // K per CTA (a multiple of BK)
+    const uint8_t* A;  // o_absorb, for the demotion below
+    int demote_rows;   // A rows [0, demote_rows) were staged in L2 at evict_last
 };
 
 template <int N, int MT, int KS>
@@ -131,10 +133,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nst = a.kper / BK;
     const int k0 = rank * a.kper;
 
+    // Staged rows of A (see the demotion warp below): how many of this CTA's.
+    const int row0 = mt * MT * BM;
+    const int nstaged = max(0, min(MT * BM, a.demote_rows - row0));
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, 1);
+            mbar_init(empty + s, nstaged > 0 ? 2 : 1);  // + the demotion warp
         }
         mbar_init(done, 1);
         *abort_flag = 0;
@@ -153,13 +158,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t bytes = L::STAGE;  // A boxes and the x box (zero fill counts too)
             // A (o_absorb) is not written by the kernels before this one: the first
             // ring's A boxes are requested before waiting for them; x follows the wait.
+            // A is read once per call: evict_first, so that the stream does not push
+            // out A lines a prefetch staged in L2 before the other CTAs reach them.
+            const uint64_t ef = l2_evict_first();
             const int pre = nst < kStages ? nst : kStages;
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(full + i, bytes);
 #pragma unroll
                 for (int t = 0; t < MT; ++t)
-                    tma_load_2d(smem_u32(smem + i * L::STAGE + t * kABytes), &tmA, k0 + i * BK,
-                                (mt * MT + t) * BM, full + i);
+                    tma_load_2d_hint(smem_u32(smem + i * L::STAGE + t * kABytes), &tmA,
+                                     k0 + i * BK, (mt * MT + t) * BM, full + i, ef);
             }
             pdl_wait();
             for (int i = 0; i < pre; ++i)
@@ -174,7 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dst = smem_u32(smem + s * L::STAGE);
 #pragma unroll
                 for (int t = 0; t < MT; ++t)
-                    tma_load_2d(dst + t * kABytes, &tmA, k0 + i * BK, (mt * MT + t) * BM, full + s);
+                    tma_load_2d_hint(dst + t * kABytes, &tmA, k0 + i * BK, (mt * MT + t) * BM,
+                                     full + s, ef);
                 tma_load_2d(dst + L::AB, &tmX, k0 + i * BK, a.n0, full + s);
             }
             // the copies issued have landed before the CTA may reuse or leave its memory
@@ -211,6 +220,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_commit(done);  // every MMA issued (all of them, or those before an abort)
         }
+    } else if (warp == 2 && nstaged > 0) {
+        // ---------------- demotion of staged A lines ----------------
+        // Rows of A that dsa_prefetch_l2 staged at evict_last go back to normal L2
+        // priority as soon as their box has landed in shared memory: one 128-byte
+        // line per row and stage. The warp is the second arrival on each empty
+        // barrier, so the ring never runs a phase ahead of it.
+        const long long rb = (long long)a.kper * kKS * 2;  // bytes per A row
+        for (int i = 0; i < nst; ++i) {
+            const int s = i % kStages;
+            int ok = 1;
+            if (lane == 0) ok = poll_wait(full + s, (uint32_t)((i / kStages) & 1), abort_flag, a.status);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            const uint8_t* col = a.A + ((long long)k0 + (long long)i * BK) * 2;
+            for (int r = lane; r < nstaged; r += 32)
+                asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(col + (row0 + r) * rb)
+                             : "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + s);
+        }
+        pdl_wait();
     } else {
         pdl_wait();
     }
@@ -410,9 +439,18 @@ int project_tc_launch(const void* x, bool x_f32, int rows, int K, const uint16_t
     a.hidden = hidden;
     a.R = rows;
     a.kper = 0;  // set per launch form
+    a.A = reinterpret_cast<const uint8_t*>(A);
+    // o_absorb rows staged in L2 by dsa_prefetch_l2 (the last launch demotes them)
+    const size_t row_bytes = (size_t)K * 2;
+    // (applypriority acts on whole 128-byte lines: only for a line-aligned o_absorb)
+    const size_t staged = (reinterpret_cast<uintptr_t>(A) & 127u)
+                              ? 0
+                              : l2_staged_overlap(A, (size_t)hidden * row_bytes);
+    const int staged_rows = (int)((staged + row_bytes - 1) / row_bytes);
     for (int n0 = 0; n0 < rows; n0 += 64) {
         a.n0 = n0;
         a.nrows = rows - n0 < 64 ? rows - n0 : 64;
+        a.demote_rows = n0 + 64 >= rows ? staged_rows : 0;
         int rc = dispatch_tc(xb, rows, K, A, hidden, a, a.nrows, st);
         if (rc) return rc;
     }

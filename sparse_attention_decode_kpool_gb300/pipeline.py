@@ -21,7 +21,8 @@ class DsaDecodeLayer:
     def __init__(self, wl: Workload, device: str = "cuda", keep_olat: bool = False,
                  with_o_absorb: bool = True, use_drawn_kpool: bool = False,
                  score_path: str = "auto", fuse_expand: bool = True, decode_from=None,
-                 fuse_append: bool = True, latent_fp8: bool = False, frontend=None):
+                 fuse_append: bool = True, latent_fp8: bool = False, frontend=None,
+                 l2_prefetch_bytes: Optional[int] = None):
         g = wl.geom
         self.wl = wl
         self.geom = g
@@ -52,14 +53,24 @@ class DsaDecodeLayer:
         self.latent_fp8 = bool(latent_fp8)
         self.ckv_codes = self.ckv_scales = None
         if self.latent_fp8:
-            if decode_from is not None:
-                raise ValueError("decode-time append writes the bf16 latent cache only")
+            if decode_from is not None and not fuse_append:
+                raise ValueError("the FP8 latent cache is appended by dsa_decode_append_fp8 "
+                                 "only (fuse_append=True)")
             kvl = g.kv_lora_rank
             self.ckv_codes = torch.empty(self.ckv.shape, dtype=torch.uint8, device=dev)
             self.ckv_scales = torch.empty(self.ckv.shape[:-1] + (kvl // 128,),
                                           dtype=torch.float32, device=dev)
             api.dsa_quantize_latent(self.ckv, self.ckv_codes, self.ckv_scales)
         self.o_absorb = up(wl.o_absorb) if with_o_absorb else None
+        # The step prefetches the first l2_prefetch_bytes of o_absorb into L2 on a
+        # second stream while top-k and the gather run (they leave HBM mostly idle);
+        # None: a quarter of o_absorb, at most 64 MiB (half of L2; the gathered
+        # latent rows pass through the rest).
+        if l2_prefetch_bytes is None:
+            l2_prefetch_bytes = (min(64 << 20, self.o_absorb.numel() * 2 // 4)
+                                 if self.o_absorb is not None else 0)
+        self.l2_prefetch_bytes = int(l2_prefetch_bytes) if self.o_absorb is not None else 0
+        self._side = torch.cuda.Stream(device=dev) if self.l2_prefetch_bytes > 0 else None
         KP, ihd = g.index_kpool, g.index_head_dim
         if wl.paged:
             pshape = (wl.num_blocks, wl.block_size // KP)
@@ -235,6 +246,8 @@ class DsaDecodeLayer:
         self.gate_new = torch.zeros_like(self.k_new)
         self.ckv_new = torch.zeros((B, g.kv_lora_rank), dtype=torch.bfloat16, device=dev)
         self.row_ctx.copy_(self.seq_lens)
+        if self.latent_fp8:  # the FP8 cache of the cut-back bf16 cache
+            api.dsa_quantize_latent(self.ckv, self.ckv_codes, self.ckv_scales)
 
     def staged_rows(self, i: int):
         """Host rows (k, gate, ckv) [batch, ...] of the token each sequence appends at
@@ -268,6 +281,14 @@ class DsaDecodeLayer:
     def append(self, stream=None) -> None:
         """indexer_store -> write_geom -> compress of the newly whole pool."""
         g = self.geom
+        if self.latent_fp8:  # the token's latent row goes to the FP8 cache only
+            api.dsa_decode_append_fp8(self.k_new, self.gate_new, self.ckv_new, self.ape, self.ln_w,
+                                      self.ln_b, g.eps, self.pg, self.seq_lens, g.first_key,
+                                      g.index_kpool, self.k_raw, self.gate, self.valid,
+                                      self.ckv_codes, self.ckv_scales, self.kpool,
+                                      self.pool_valid, row_ctx=self.row_ctx, status=self.status,
+                                      stream=stream)
+            return
         if self.fuse_append:
             api.dsa_decode_append(self.k_new, self.gate_new, self.ape, self.ln_w, self.ln_b, g.eps,
                                   self.pg, self.seq_lens, g.first_key, g.index_kpool, self.k_raw,
@@ -388,9 +409,15 @@ class DsaDecodeLayer:
         """One decode step over the whole batch: score, select (with the token ids),
         attention and projection."""
         self.score(stream)
+        if self._side is not None:  # fork: the o_absorb prefetch beside the middle stages
+            main = stream if stream is not None else torch.cuda.current_stream(self.device)
+            self._side.wait_stream(main)
+            api.dsa_prefetch_l2(self.o_absorb, self.l2_prefetch_bytes, stream=self._side)
         self.select(stream)
         self.expand(stream)
         self.attend_project(stream)
+        if self._side is not None:  # join (the prefetch is long done by now)
+            main.wait_stream(self._side)
 
     def launches_per_step(self) -> int:
         """Library kernel launches one step() makes."""
@@ -405,7 +432,7 @@ class DsaDecodeLayer:
                   != api._lib.DSA_PROJECT_KERNEL_MMA and g.hidden % 128 == 0
                   and (g.heads * g.kv_lora_rank) % 512 == 0)
             n += (R + 63) // 64 + (0 if tc else 1)
-        return n
+        return n + (1 if self._side is not None else 0)  # the o_absorb L2 prefetch
 
     def capture_layer(self) -> torch.cuda.CUDAGraph:
         """Capture layer_step() into a CUDA graph. frontend() and step() run once

@@ -55,6 +55,15 @@ def test_validate_config_rules(lib, args, code):
         assert _err(lib)
 
 
+def test_prefetch_l2_argument_errors(lib):
+    assert lib.dsa_prefetch_l2(None, 0, None) == DSA_OK  # nothing to do: no launch
+    assert lib.dsa_prefetch_l2(FAKE, 0, None) == DSA_OK
+    assert lib.dsa_prefetch_l2(FAKE, 8, None) == DSA_OK  # below one 16-byte unit
+    assert lib.dsa_prefetch_l2(None, 1 << 20, None) == DSA_ERR_INVALID_ARG
+    assert lib.dsa_prefetch_l2(FAKE + 8, 1 << 20, None) == DSA_ERR_INVALID_ARG
+    assert "aligned" in _err(lib)
+
+
 def test_launch_options(lib):
     from sparse_attention_decode_kpool_gb300._lib import (DSA_MLA_KERNEL_AUTO,
                                                            DSA_MLA_KERNEL_MMA,
@@ -153,6 +162,17 @@ def test_append_entry_argument_errors(lib):
     assert da(pgp=None) == DSA_ERR_INVALID_ARG
     paged = _paging(block_table=FAKE, max_blocks=16, block_size=64, nb=8)
     assert da(fk=2, pgp=ctypes.byref(paged)) == DSA_ERR_UNSUPPORTED  # first_key % kpool
+    # dsa_decode_append_fp8: as dsa_decode_append plus ckv_codes, ckv_scales after ckv
+    d8 = lambda kvl=512, codes=FAKE, scales=FAKE, ckv_new=FAKE, ckv=None: \
+        lib.dsa_decode_append_fp8(FAKE, FAKE, ckv_new, FAKE, FAKE, FAKE, 1e-6, ctypes.byref(pg),
+                                  FAKE, 0, 4, 128, kvl, FAKE, FAKE, FAKE, ckv, codes, scales,
+                                  FAKE, FAKE, None, None, None, None)
+    assert d8(codes=None) == DSA_ERR_INVALID_ARG and "FP8" in _err(lib)
+    assert d8(scales=None) == DSA_ERR_INVALID_ARG
+    assert d8(ckv_new=None) == DSA_ERR_INVALID_ARG and "together" in _err(lib)
+    assert d8(kvl=196) == DSA_ERR_INVALID_ARG and "multiple of 8" in _err(lib)
+    assert d8(kvl=192) == DSA_ERR_INVALID_ARG and "multiple of 128" in _err(lib)
+    assert d8(codes=FAKE + 8) == DSA_ERR_INVALID_ARG and "aligned" in _err(lib)
     assert lib.dsa_write_geom(FAKE, 0, None, 4, FAKE, None, None) == DSA_ERR_INVALID_ARG
     assert lib.dsa_write_geom(FAKE, 2, None, -1, FAKE, None, None) == DSA_ERR_INVALID_ARG
     assert lib.dsa_write_geom(FAKE, 2, None, 0, None, None, None) == DSA_OK

@@ -153,3 +153,69 @@ def test_fp8_decode_step_equals_bf16_step_on_decoded_cache(make):
     assert torch.equal(fp8.pool_ids, ref.pool_ids)
     assert torch.equal(fp8.olat, ref.olat)
     assert torch.equal(fp8.y, ref.y)
+
+
+@pytest.mark.parametrize("paged", [False, True], ids=["contig", "paged"])
+def test_fp8_decode_append(paged):
+    """dsa_decode_append_fp8 grows the FP8 cache one token per sequence (eager, then a
+    replayed graph). Afterwards every cache row's codes and scales equal the oracle's
+    encoding of the workload's bf16 row, and the last step equals, bit for bit, the
+    step of a layer whose FP8 cache was encoded in one piece at the full length."""
+    g = W.Geometry(index_kpool=4, index_heads=32, index_head_dim=128, index_topk=256, heads=8,
+                   hidden=256)
+    n = 7
+    wl = W.make_workload(f"fp8-append-{int(paged)}", 43, g, [300, 517, 130],
+                         block_size=64 if paged else None, max_seq_len=576 if paged else None,
+                         invalid_per_seq=3)
+    L0 = wl.seq_lens.astype(np.int64) - n
+    grow = DsaDecodeLayer(wl, keep_olat=True, decode_from=L0, latent_fp8=True)
+    grow.compress()
+    for i in range(n):
+        grow.stage(i)
+        if i == 0:
+            grow.append_step()
+        else:
+            if grow.append_graph is None:
+                grow.capture_append()
+            grow.append_graph.replay()
+    torch.cuda.synchronize()
+    assert int(grow.status.item()) == 0
+    np.testing.assert_array_equal(grow.seq_lens.cpu().numpy(), wl.seq_lens)
+
+    codes = grow.ckv_codes.view(-1, g.kv_lora_rank).cpu().numpy()
+    scales = grow.ckv_scales.view(-1, g.kv_lora_rank // 128).cpu().numpy()
+    src = wl.ckv.reshape(-1, g.kv_lora_rank)
+    for b in range(wl.batch):
+        rows = grow._token_rows(b, 0, int(wl.seq_lens[b]))
+        c, sc = _host_quant(src[torch.from_numpy(rows)])
+        np.testing.assert_array_equal(codes[rows], c, err_msg=f"seq {b} codes")
+        np.testing.assert_array_equal(scales[rows], sc, err_msg=f"seq {b} scales")
+
+    # The one-piece twin: appended tokens count as valid, as the append marks them.
+    whole = DsaDecodeLayer(wl, keep_olat=True, latent_fp8=True)
+    for b in range(wl.batch):
+        rows = torch.from_numpy(whole._token_rows(b, int(L0[b]), int(wl.seq_lens[b])))
+        whole.valid.view(-1)[rows.to(whole.valid.device)] = 1
+    whole.compress()
+    whole.step()
+    torch.cuda.synchronize()
+    assert int(whole.status.item()) == 0
+    assert torch.equal(grow.kpool, whole.kpool)
+    for k in ("scores", "pool_ids", "token_ids", "olat", "y"):
+        assert torch.equal(getattr(grow, k), getattr(whole, k)), k
+
+
+def test_fp8_decode_append_rejects_bad_rank():
+    """kv_lora_rank must be a multiple of 128 for the FP8 cache (no launch)."""
+    g = W.Geometry(index_kpool=4, index_heads=32, index_head_dim=128, index_topk=256, heads=8,
+                   hidden=256)
+    wl = W.make_workload("fp8-append-bad", 44, g, [300], invalid_per_seq=0)
+    lay = DsaDecodeLayer(wl, decode_from=[290], latent_fp8=True)
+    ckv_new = torch.zeros((1, 200), dtype=torch.bfloat16, device="cuda")
+    codes = torch.zeros((wl.max_seq_len, 200), dtype=torch.uint8, device="cuda")
+    scales = torch.zeros((wl.max_seq_len, 1), dtype=torch.float32, device="cuda")
+    with pytest.raises(Exception, match="multiple of"):
+        api.dsa_decode_append_fp8(lay.k_new, lay.gate_new, ckv_new, lay.ape, lay.ln_w, lay.ln_b,
+                                  g.eps, lay.pg, lay.seq_lens, g.first_key, g.index_kpool,
+                                  lay.k_raw, lay.gate, lay.valid, codes, scales, lay.kpool,
+                                  lay.pool_valid, status=lay.status)

@@ -569,3 +569,49 @@ def test_latent_project_parity(rows, heads, hidden, proj_kernel):
     ref = np.array([O.latent_project(olat[r].numpy().astype(np.float64), H.f(A))[0]
                     for r in range(rows)])
     H.check_attention(y.t.float().cpu().numpy(), ref, "y")
+
+
+@pytest.mark.parametrize("rows,heads,hidden,frac", [(8, 64, 4096, 0.25), (64, 64, 4096, 0.25),
+                                                    (70, 16, 256, 1.0), (20, 8, 128, 0.4)])
+def test_project_after_l2_prefetch_is_identical(rows, heads, hidden, frac, proj_kernel):
+    """Staging part of o_absorb in L2 (dsa_prefetch_l2) changes nothing in y: the
+    tensor-core projection then also returns the staged lines to normal priority
+    (an extra arrival on its ring), over one or several 64-row launches."""
+    rng = np.random.default_rng(rows + heads + hidden)
+    olat = torch.from_numpy(rng.standard_normal((rows, heads, 512)).astype(np.float32)).cuda()
+    A = torch.from_numpy((rng.standard_normal((hidden, heads * 512)) * 0.02).astype(np.float32)
+                         ).to(torch.bfloat16).cuda()
+    ws = torch.zeros(max(1, api.dsa_latent_project_workspace(rows, heads, hidden)),
+                     dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y0 = torch.zeros((rows, hidden), dtype=torch.bfloat16, device="cuda")
+    api.dsa_latent_project(olat, A, y0, status, ws)
+    y1 = torch.zeros_like(y0)
+    api.dsa_prefetch_l2(A, int(A.numel() * 2 * frac))
+    api.dsa_latent_project(olat, A, y1, status, ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(y0, y1)
+
+
+def _paged_small_wl():
+    return W.make_workload("paged-small-pf", 6, W.Geometry(**W.GLM53), [3000, 5000, 700, 4096],
+                           block_size=64, max_seq_len=5120, invalid_per_seq=7)
+
+
+@pytest.mark.parametrize("make", [W.tiny, _paged_small_wl], ids=["tiny", "paged"])
+def test_step_with_l2_prefetch_branch_is_identical(make):
+    """The step graph with the o_absorb prefetch on a forked branch equals the plain
+    step bit for bit."""
+    wl = make()
+    plain = DsaDecodeLayer(wl, keep_olat=True, l2_prefetch_bytes=0)
+    pf = DsaDecodeLayer(wl, keep_olat=True, l2_prefetch_bytes=wl.o_absorb.numel())  # half
+    assert pf.l2_prefetch_bytes > 0 and pf.launches_per_step() == plain.launches_per_step() + 1
+    for lay in (plain, pf):
+        lay.compress()
+        lay.capture()
+        lay.graph.replay()
+    torch.cuda.synchronize()
+    assert int(pf.status.item()) == 0
+    for k in ("pool_ids", "token_ids", "olat", "y"):
+        assert torch.equal(getattr(pf, k), getattr(plain, k)), k
