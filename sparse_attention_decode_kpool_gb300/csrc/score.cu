@@ -227,34 +227,52 @@ __global__ void __launch_bounds__(kTmaThreads, kCtasPerSm) score_tma_kernel(Scor
     __syncthreads();
 
     if (warp == 4) {
-        // ---------------- producer
-        if (lane == 0) {
-            int cur_r = -1;
-            RowInfo ri{};
-            long long i = 0;
-            bool ok = true;
-            int r = (int)(u0 / spr), st = (int)(u0 % spr);
-            for (long long u = u0; u < u1; ++u, ++i) {
-                const int s = (int)(i % kStages);
-                const uint32_t ph = (uint32_t)((i / kStages) & 1);
-                if (!mbar_wait(&empty[s], ph ^ 1u)) {
-                    ok = false;
-                    break;
+        // ---------------- producer (lane 0 owns the ring; on a paged cache the whole
+        // warp resolves the stage's block-table entries, one block per lane, ahead of
+        // the slot wait, and each lane copies its block's run of pools)
+        const bool paged = a.pg.block_table != nullptr;
+        const int ppb = paged ? a.pg.block_size / a.kpool : 1;
+        int cur_r = -1;
+        RowInfo ri{};
+        long long i = 0;
+        bool ok = true;
+        int r = (int)(u0 / spr), st = (int)(u0 % spr);
+        for (long long u = u0; u < u1; ++u, ++i) {
+            const int s = (int)(i % kStages);
+            const uint32_t ph = (uint32_t)((i / kStages) & 1);
+            if (st == spr) {
+                st = 0;
+                ++r;
+            }
+            const int p0 = st++ * kStagePools;
+            if (r != cur_r) {
+                ri = row_info(a, r);
+                if (lane == 0 && ri.seq < 0 && u == u0) flag_status(a.status, DSA_STATUS_BAD_TOKEN);
+                cur_r = r;
+            }
+            const int nvalid = ri.seq < 0 ? 0 : max(0, min(kStagePools, ri.nvis - p0));
+            // blocks b0 .. b0 + nb - 1 hold the stage's pools; lane j looks up j and j + 32
+            const int b0 = p0 / ppb;
+            const int nb = paged && nvalid > 0 ? (p0 + nvalid - 1) / ppb - b0 + 1 : 0;
+            long long brow[2] = {-1, -1};  // first pool row of the lane's blocks, -1: bad
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int j = lane + 32 * t;
+                if (j < nb) {
+                    const int blk = __ldg(a.pg.block_table + (long long)ri.seq * a.pg.max_blocks + b0 + j);
+                    brow[t] = blk >= 0 && blk < a.pg.num_blocks ? (long long)blk * ppb : -1;
                 }
-                if (st == spr) {
-                    st = 0;
-                    ++r;
-                }
-                const int p0 = st++ * kStagePools;
-                if (r != cur_r) {
-                    ri = row_info(a, r);
-                    if (ri.seq < 0 && u == u0) flag_status(a.status, DSA_STATUS_BAD_TOKEN);
-                    cur_r = r;
-                }
-                const int nvalid = ri.seq < 0 ? 0 : max(0, min(kStagePools, ri.nvis - p0));
-                const uint32_t dst = smem_u32(smem + s * STAGE);
-                const uint32_t fdst = smem_u32(flags + s * kStagePools);
-                if (a.pg.block_table == nullptr) {
+            }
+            int got = 1;
+            if (lane == 0) got = mbar_wait(&empty[s], ph ^ 1u) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, got, 0)) {
+                ok = false;
+                break;
+            }
+            const uint32_t dst = smem_u32(smem + s * STAGE);
+            const uint32_t fdst = smem_u32(flags + s * kStagePools);
+            if (!paged) {
+                if (lane == 0) {
                     const long long prow0 = (long long)ri.seq * (a.pg.max_seq_len / a.kpool) + p0;
                     const uint32_t kbytes = (uint32_t)(nvalid * ROWB);
                     const uint32_t fbytes = a.flags_tma ? (uint32_t)((nvalid + 15) & ~15) : 0u;
@@ -262,40 +280,51 @@ __global__ void __launch_bounds__(kTmaThreads, kCtasPerSm) score_tma_kernel(Scor
                     mbar_arrive_expect_tx(&full[s], kbytes + fbytes);
                     if (kbytes) bulk_g2s(dst, a.kp + prow0 * IHD, kbytes, &full[s]);
                     if (fbytes) bulk_g2s(fdst, a.pv + prow0, fbytes, &full[s]);
+                }
+                continue;
+            }
+            // Pools of one block are contiguous: one copy per block run.
+            uint32_t bytes = 0;
+            unsigned long long badm = 0ull;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int j = lane + 32 * t;
+                if (j >= nb) continue;
+                const int pb = (b0 + j) * ppb;
+                const int ps = max(p0, pb), run = min(p0 + nvalid, pb + ppb) - ps;
+                if (brow[t] >= 0) {
+                    bytes += (uint32_t)(run * ROWB);
+                    if (a.flags_tma) bytes += (uint32_t)((run + 15) & ~15);
                 } else {
-                    // Pools of one block are contiguous: one copy per block run.
-                    const int ppb = a.pg.block_size / a.kpool;
-                    uint32_t bytes = 0;
-                    unsigned long long badm = 0ull;
-                    for (int p = p0; p < p0 + nvalid;) {
-                        const int run = min(ppb - p % ppb, p0 + nvalid - p);
-                        const long long row = pool_row(a.pg, ri.seq, p, a.kpool);
-                        if (row >= 0) {
-                            bytes += (uint32_t)(run * ROWB);
-                            if (a.flags_tma) bytes += (uint32_t)((run + 15) & ~15);
-                        } else {
-                            badm |= ((run >= 64) ? ~0ull : ((1ull << run) - 1ull)) << (p - p0);
-                            flag_status(a.status, DSA_STATUS_BAD_BLOCK);
-                        }
-                        p += run;
-                    }
-                    bad[s] = badm;
-                    mbar_arrive_expect_tx(&full[s], bytes);
-                    for (int p = p0; p < p0 + nvalid;) {
-                        const int run = min(ppb - p % ppb, p0 + nvalid - p);
-                        const long long row = pool_row(a.pg, ri.seq, p, a.kpool);
-                        if (row >= 0) {
-                            bulk_g2s(dst + (p - p0) * ROWB, a.kp + row * IHD, (uint32_t)(run * ROWB),
-                                     &full[s]);
-                            if (a.flags_tma)
-                                bulk_g2s(fdst + (p - p0), a.pv + row, (uint32_t)((run + 15) & ~15),
-                                         &full[s]);
-                        }
-                        p += run;
-                    }
+                    badm |= ((run >= 64) ? ~0ull : ((1ull << run) - 1ull)) << (ps - p0);
+                    flag_status(a.status, DSA_STATUS_BAD_BLOCK);
                 }
             }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+                badm |= __shfl_xor_sync(0xffffffffu, badm, o);
+            }
+            if (lane == 0) {
+                bad[s] = badm;
+                mbar_arrive_expect_tx(&full[s], bytes);
+            }
+            __syncwarp();  // the stage's bytes are expected before any copy lands
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int j = lane + 32 * t;
+                if (j >= nb || brow[t] < 0) continue;
+                const int pb = (b0 + j) * ppb;
+                const int ps = max(p0, pb), run = min(p0 + nvalid, pb + ppb) - ps;
+                const long long row = brow[t] + (ps - pb);
+                bulk_g2s(dst + (ps - p0) * ROWB, a.kp + row * IHD, (uint32_t)(run * ROWB), &full[s]);
+                if (a.flags_tma)
+                    bulk_g2s(fdst + (ps - p0), a.pv + row, (uint32_t)((run + 15) & ~15), &full[s]);
+            }
+        }
+        if (lane == 0) {
             if (!ok) flag_status(a.status, DSA_STATUS_TIMEOUT);
+            // the copies issued have landed before the CTA leaves
             const long long first = i > kStages ? i - kStages : 0;
             for (long long j = first; j < i; ++j)
                 if (!mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1))) break;
