@@ -46,7 +46,7 @@ struct PL {  // shared-memory layout of one CTA (offsets from a 1024-aligned bas
     static constexpr uint32_t STAGE = AB + XB;                  // multiple of 1 KB
     // Bytes of A in flight are what keep the stream at HBM speed (about 160 KB per
     // SM): two CTAs per SM with 16 query rows, one otherwise.
-    static constexpr int CTAS_PER_SM = (MT == 1 && N <= 16 && KS == 8) ? 2 : 1;
+    static constexpr int CTAS_PER_SM = (MT == 1 && N <= 16) ? 2 : 1;
     static constexpr int S_FIT = (int)(((CTAS_PER_SM == 2 ? 220u : 200u) * 1024u / CTAS_PER_SM) / STAGE);
     static constexpr int S = S_FIT > kMaxStages ? kMaxStages : S_FIT;  // ring stages
     static constexpr uint32_t RED = MT * BM * N * 4;            // the partial, f32 [MT*BM][N]
@@ -379,14 +379,45 @@ int launch_tc(const uint16_t* x, int R, int K, const uint16_t* A, int hidden, co
     return DSA_OK;
 }
 
+// K shares per 128-row tile: the most (up to `most`) that keep the grid within one wave
+// of `slots` CTAs and give each share at least eight 64-wide stages.
+int pick_ks(int tiles, int K, int slots, int most) {
+    int ks = most;
+    while (ks > 1 && ((long long)tiles * ks > slots || K / ks < 8 * BK || K % (ks * BK) != 0))
+        ks >>= 1;
+    return ks;
+}
+
 int dispatch_tc(const uint16_t* x, int R, int K, const uint16_t* A, int hidden, const TcProjArgs& a,
                 int n, cudaStream_t st) {
-    // Up to 16 query rows: clusters of 8 K shares, two CTAs per SM. More rows: a larger
-    // ring per CTA (one per SM) and clusters of 4 K shares, so that the grid of 128-row
-    // tiles stays one wave of clusters (eight-CTA clusters of one-CTA SMs do not all fit).
-    if (n <= 16) return launch_tc<16, 1, 8>(x, R, K, A, hidden, a, st);
-    if (n <= 32) return launch_tc<32, 1, 4>(x, R, K, A, hidden, a, st);
-    return launch_tc<64, 1, 4>(x, R, K, A, hidden, a, st);
+    // Up to 16 query rows: two CTAs per SM, clusters of up to 8 K shares. More rows: a
+    // larger ring per CTA (one per SM) and clusters of up to 4 K shares, so that the
+    // grid of 128-row tiles stays one wave of clusters (eight-CTA clusters of one-CTA
+    // SMs do not all fit). Many tiles (a tall weight with a short K, such as the
+    // front-end's q projection) take fewer shares: each CTA then streams a longer run.
+    const int tiles = hidden / BM;
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    if (n <= 16) {
+        switch (pick_ks(tiles, K, 2 * sms, 8)) {
+            case 8: return launch_tc<16, 1, 8>(x, R, K, A, hidden, a, st);
+            case 4: return launch_tc<16, 1, 4>(x, R, K, A, hidden, a, st);
+            case 2: return launch_tc<16, 1, 2>(x, R, K, A, hidden, a, st);
+            default: return launch_tc<16, 1, 1>(x, R, K, A, hidden, a, st);
+        }
+    }
+    const int ks = pick_ks(tiles, K, sms, 4);
+    if (n <= 32) {
+        switch (ks) {
+            case 4: return launch_tc<32, 1, 4>(x, R, K, A, hidden, a, st);
+            case 2: return launch_tc<32, 1, 2>(x, R, K, A, hidden, a, st);
+            default: return launch_tc<32, 1, 1>(x, R, K, A, hidden, a, st);
+        }
+    }
+    switch (ks) {
+        case 4: return launch_tc<64, 1, 4>(x, R, K, A, hidden, a, st);
+        case 2: return launch_tc<64, 1, 2>(x, R, K, A, hidden, a, st);
+        default: return launch_tc<64, 1, 1>(x, R, K, A, hidden, a, st);
+    }
 }
 
 // x f32 -> bf16 (round to nearest even), for the projection's bf16 x tiles.
