@@ -1047,7 +1047,11 @@ int select_launch(const float* scores, int rows, int p_stride, int sk, int32_t* 
     int C = 1;
     while (C < kMaxCluster) {
         const long long chunk = (p_stride + C - 1) / C;
-        const bool underfilled = (long long)rows * C < 2LL * sms && chunk > 2048;
+        // A slice of about 8,192 keys per CTA: a CTA's passes over its keys cost about
+        // the same up to there, while each further CTA of a cluster adds k keys to
+        // the merge (64 rows of 16,384 pools: two CTAs per row take 20.8 us, eight
+        // take 43.4 us; 8 rows of 65,536 pools: eight per row 20.8, four 22.9).
+        const bool underfilled = (long long)rows * C < 2LL * sms && chunk > 8192;
         if (fits(C) && !underfilled) break;
         if (fits(C) && !fits(2 * C)) break;
         C *= 2;
