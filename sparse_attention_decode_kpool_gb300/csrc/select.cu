@@ -243,9 +243,21 @@ __device__ __noinline__ Thr bin_threshold(const uint32_t* keys, int n, int k, Mi
     for (int b = threadIdx.x; b < kBins; b += kThreads) sc.hist[b] = 0u;
     if (threadIdx.x == 0) sc.tcount = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-        const uint32_t key = keys[i];
-        if (key) atomicAdd(&sc.hist[(mm.kmax - key) >> shift], 1u);
+    {
+        // four independent loads per step (the pass is bound by their latency)
+        int i = threadIdx.x;
+        for (; i + 3 * kThreads < n; i += 4 * kThreads) {
+            uint32_t k4[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) k4[t] = keys[i + t * kThreads];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                if (k4[t]) atomicAdd(&sc.hist[(mm.kmax - k4[t]) >> shift], 1u);
+        }
+        for (; i < n; i += kThreads) {
+            const uint32_t key = keys[i];
+            if (key) atomicAdd(&sc.hist[(mm.kmax - key) >> shift], 1u);
+        }
     }
     __syncthreads();
     // Thread t owns bins 8t .. 8t+7 (bin 0 holds the largest keys).
@@ -291,14 +303,24 @@ __device__ __noinline__ Thr bin_threshold(const uint32_t* keys, int n, int k, Mi
     // Collect the bin's keys (order is irrelevant to ranking). Exactly nb keys match,
     // so the slot index stays below nb <= tcap.
     uint32_t bmx = 0u, bmn = 0xffffffffu;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-        const uint32_t key = keys[i];
+    auto collect = [&](uint32_t key) {
         if (key != 0u && ((mm.kmax - key) >> shift) == bstar) {
             const int at = atomicAdd(&sc.tcount, 1);
             if (at < tcap) tbuf[at] = key;
             bmx = max(bmx, key);
             bmn = min(bmn, key);
         }
+    };
+    {
+        int i = threadIdx.x;
+        for (; i + 3 * kThreads < n; i += 4 * kThreads) {
+            uint32_t k4[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) k4[t] = keys[i + t * kThreads];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) collect(k4[t]);
+        }
+        for (; i < n; i += kThreads) collect(keys[i]);
     }
     if (nb > kRankMax) {
         const MinMax bm = block_minmax(bmn, bmx, 0, sc);  // syncs: tbuf complete after it
@@ -398,6 +420,7 @@ __device__ __noinline__ void ordered_emit(const uint32_t* keys, int n, Thr t, Bl
     const int i0 = threadIdx.x * per;
     const int i1 = min(n, i0 + per);
     uint32_t gt = 0u, eq = 0u;
+#pragma unroll 4
     for (int i = i0; i < i1; i += 4) {
         const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
         const uint32_t k4[4] = {v.x, v.y, v.z, v.w};
