@@ -190,7 +190,8 @@ def algorithmic_bytes(wl, layer) -> dict:
     qlat = wl.rows * g.heads * g.kv_lora_rank * 2
     oabs = g.hidden * g.heads * g.kv_lora_rank * 2 if layer.o_absorb is not None else 0
     y = wl.rows * g.hidden * 2 if layer.o_absorb is not None else 0
-    olat = wl.rows * g.heads * g.kv_lora_rank * 4 if layer.o_absorb is not None else 0
+    # the projection's input: the bf16 copy of olat the combine writes for it
+    olat = wl.rows * g.heads * g.kv_lora_rank * 2 if layer.o_absorb is not None else 0
     # --decode-append: per sequence the staged rows in and out, the valid byte, and
     # at most one newly whole pool (kpool token rows of keys, gates and flags in,
     # one pooled key and flag out).

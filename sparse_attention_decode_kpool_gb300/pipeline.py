@@ -99,6 +99,7 @@ class DsaDecodeLayer:
         hidden = g.hidden if self.o_absorb is not None else 0
         self.y = torch.empty((R, hidden), dtype=torch.bfloat16, device=dev) if hidden else None
         # olat feeds the projection, so it always exists when o_absorb does.
+        self.keep_olat = bool(keep_olat)
         self.olat = (torch.empty((R, g.heads, g.kv_lora_rank), dtype=torch.float32, device=dev)
                      if (keep_olat or self.o_absorb is not None) else None)
         ws = api.dsa_sparse_mla_decode_workspace(R, g.heads, g.out_width, 0, False)
@@ -372,24 +373,24 @@ class DsaDecodeLayer:
             return
         api.dsa_expand(self.pool_ids, g.first_key, g.index_kpool, self.token_ids, stream=stream)
 
-    def _mla(self, o_absorb, y, workspace, stream) -> None:
+    def _mla(self, o_absorb, y, workspace, stream, olat=None) -> None:
         if self.latent_fp8:
             api.dsa_sparse_mla_decode_fp8(self.qlat, self.row_seq, self.ckv_codes, self.ckv_scales,
                                           self.pg, self.token_ids, self.geom.softmax_scale,
-                                          o_absorb, y, self.olat, self.status, workspace,
+                                          o_absorb, y, olat, self.status, workspace,
                                           stream=stream)
         else:
             api.dsa_sparse_mla_decode(self.qlat, self.row_seq, self.ckv, self.pg, self.token_ids,
-                                      self.geom.softmax_scale, o_absorb, y, self.olat,
+                                      self.geom.softmax_scale, o_absorb, y, olat,
                                       self.status, workspace, stream=stream)
 
     def attend(self, stream=None) -> None:
         """Sparse latent attention over the selected tokens -> olat (f32); in the
         one-call form also y."""
         if self.o_absorb is not None and not self.two_call:
-            self._mla(self.o_absorb, self.y, self.fused_workspace(), stream)
+            self._mla(self.o_absorb, self.y, self.fused_workspace(), stream, self.olat)
             return
-        self._mla(None, None, self.workspace, stream)
+        self._mla(None, None, self.workspace, stream, self.olat)
 
     def project(self, stream=None) -> None:
         """y = o_absorb . olat (the absorbed output projection)."""
@@ -401,9 +402,12 @@ class DsaDecodeLayer:
         """Sparse latent attention and the o_absorb projection in one call (olat f32
         and y); without o_absorb, the attention alone."""
         if self.o_absorb is not None:
-            self._mla(self.o_absorb, self.y, self.fused_workspace(), stream)
+            # the f32 olat is written only when the layer keeps it (the projection reads
+            # the bf16 copy the combine writes for it)
+            self._mla(self.o_absorb, self.y, self.fused_workspace(), stream,
+                      self.olat if self.keep_olat else None)
         else:
-            self._mla(None, None, self.workspace, stream)
+            self._mla(None, None, self.workspace, stream, self.olat)
 
     def step(self, stream=None) -> None:
         """One decode step over the whole batch: score, select (with the token ids),
