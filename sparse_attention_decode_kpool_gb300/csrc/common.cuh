@@ -97,6 +97,8 @@ struct MlaTcParams {
     const uint16_t* qlat;
     const int32_t* row_seq;
     const uint16_t* ckv;
+    const uint8_t* ckv8;     // non-null: the FP8 cache (E4M3 codes [.., 512]) is read instead
+    const float* ckv_scale;  // ... with its power-of-two scales [.., 4]
     const int32_t* token_ids;
     float* part_o;
     float* part_ml;

@@ -1,6 +1,7 @@
 // The FP8 latent cache's codec on the device: OCP E4M3 codes with one power-of-two
 // scale 2^k per token and 128-channel group (see dsa_quantize_latent in dsa.h). Shared
-// by the cache encoder and the decode-time append, so both store the same bytes.
+// by the cache encoder and the decode-time append, so both store the same bytes, and
+// by the attention kernels that decode the cache.
 #pragma once
 
 #include "common.cuh"
@@ -19,6 +20,18 @@ __device__ __forceinline__ int fp8_scale_exp(float amax) {
     const int e = E - 127;
     const int k = mant <= 0x600000u ? e - 8 : e - 7;
     return k < -126 ? -126 : k;
+}
+
+// Two E4M3 codes (low byte first) times a power-of-two scale, as packed bf16: the
+// E4M3 -> f16 conversion, the f16 -> f32 widening and the scaling are exact, and so
+// is the bf16 rounding (an E4M3 value times 2^k has a 4-bit significand).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float scale) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)(two & 0xffffu)));
+    float f0, f1;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f0) : "h"((unsigned short)(h2 & 0xffffu)));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f1) : "h"((unsigned short)(h2 >> 16)));
+    return pack_bf16x2(f0 * scale, f1 * scale);
 }
 
 // Two values to E4M3 codes (nearest, ties to even, saturating), low byte first.

@@ -23,6 +23,7 @@
 //    trick as the score kernel), query rows on the MMA N axis.
 // 4. ysum_kernel -- adds the k-range partials and rounds y to bf16.
 #include "common.cuh"
+#include "fp8.cuh"
 
 namespace dsa {
 namespace {
@@ -58,18 +59,6 @@ struct MlaArgs {
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in a 1 KiB-row tile
     return (uint32_t)(row * ROWB + ((chunk ^ (row & 7)) << 4));
-}
-
-// Two E4M3 codes (low byte first) times a power-of-two scale, as packed bf16: the
-// E4M3 -> f16 conversion, the f16 -> f32 widening and the scaling are exact, and so
-// is the bf16 rounding (an E4M3 value times 2^k has a 4-bit significand).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float scale) {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)(two & 0xffffu)));
-    float f0, f1;
-    asm("cvt.f32.f16 %0, %1;" : "=f"(f0) : "h"((unsigned short)(h2 & 0xffffu)));
-    asm("cvt.f32.f16 %0, %1;" : "=f"(f1) : "h"((unsigned short)(h2 >> 16)));
-    return pack_bf16x2(f0 * scale, f1 * scale);
 }
 
 template <int MT, bool F8>
@@ -625,7 +614,7 @@ Plan make_plan(int rows, int heads, int ow, int hidden, bool with_oabs, int sms,
     // counts and the FP8 cache: the mma.sync kernel. DSA_OPT_MLA_KERNEL forces one.
     const int choice = mla_kernel_choice();
     const long long tc_chunks = (long long)rows * ((ow + mla_tc_chunk() - 1) / mla_tc_chunk());
-    const bool tc_ok = !fp8 && mla_tc_supported(heads, KVL);
+    const bool tc_ok = mla_tc_supported(heads, KVL);  // bf16 or FP8 cache
     const bool dec_ok = !fp8 && mla_dec_supported(heads, KVL, ow);
     if (choice == DSA_MLA_KERNEL_TCGEN05) {
         p.tc = tc_ok;
@@ -822,6 +811,8 @@ int mla_decode_impl(const dsa_bf16* qlat, int rows, int heads, int kv_lora_rank,
         t.qlat = qlat;
         t.row_seq = row_seq;
         t.ckv = ckv;
+        t.ckv8 = ckv8;
+        t.ckv_scale = ckv_scale;
         t.token_ids = token_ids;
         t.part_o = a.part_o;
         t.part_ml = a.part_ml;

@@ -35,6 +35,7 @@
 // All waits are bounded; a timeout sets DSA_STATUS_TIMEOUT, every role leaves its
 // loops, copies and MMAs in flight are drained, and the tensor memory is released.
 #include "common.cuh"
+#include "fp8.cuh"
 #include "tc.cuh"
 
 namespace dsa {
@@ -141,6 +142,54 @@ __device__ __forceinline__ void gather_quarter(uint32_t lat, const int* rows, co
     }
 }
 
+// FP8 cache: quarter q of a chunk decoded into the swizzled bf16 atoms by the six
+// gather warps. Unit u = (token u >> 3, 16-column group u & 7 of the quarter's 128
+// columns); gather thread g takes units g, g + kGatherThreads, ...: its 16 E4M3 codes
+// and the token's scale for this quarter (one 128-channel group) are loaded into
+// registers first (f8_load), and once the quarter is free decoded (exact: an E4M3
+// value times 2^k fits bf16) and stored as two 16-byte chunks of the atom (f8_store).
+constexpr int kF8Units = (kT * 8 + kGatherThreads - 1) / kGatherThreads;
+struct F8Quarter {
+    uint4 c[kF8Units];
+    float sc[kF8Units];
+};
+__device__ __forceinline__ void f8_load(F8Quarter& L, const int* rows, const uint8_t* ckv8,
+                                        const float* scl, int q, int g) {
+#pragma unroll
+    for (int m = 0; m < kF8Units; ++m) {
+        const int u = g + m * kGatherThreads;
+        if (u < kT * 8) {
+            const long long r = rows[u >> 3];
+            L.c[m] = __ldg(reinterpret_cast<const uint4*>(ckv8 + r * kKVL + q * 128 + (u & 7) * 16));
+            L.sc[m] = __ldg(scl + r * (kKVL / 128) + q);
+        }
+    }
+}
+__device__ __forceinline__ void f8_store(const F8Quarter& L, uint32_t lat, int q, int g) {
+#pragma unroll
+    for (int m = 0; m < kF8Units; ++m) {
+        const int u = g + m * kGatherThreads;
+        if (u < kT * 8) {
+            const int j = u >> 3, grp = u & 7;
+            const int c0 = 2 * (grp & 3);
+            const uint32_t row = lat + (2 * q + (grp >> 2)) * kLatAtom + j * 128;
+            const float sc = L.sc[m];
+            const uint4 c = L.c[m];
+            const uint4 lo = make_uint4(e4m3x2_to_bf16x2(c.x, sc), e4m3x2_to_bf16x2(c.x >> 16, sc),
+                                        e4m3x2_to_bf16x2(c.y, sc), e4m3x2_to_bf16x2(c.y >> 16, sc));
+            const uint4 hi = make_uint4(e4m3x2_to_bf16x2(c.z, sc), e4m3x2_to_bf16x2(c.z >> 16, sc),
+                                        e4m3x2_to_bf16x2(c.w, sc), e4m3x2_to_bf16x2(c.w >> 16, sc));
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(row + ((c0 ^ (j & 7)) << 4)),
+                         "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w)
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(row + (((c0 + 1) ^ (j & 7)) << 4)),
+                         "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                         : "memory");
+        }
+    }
+}
+
+template <bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_tc_kernel(const __grid_constant__ CUtensorMap tmQ, MlaTcParams a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -160,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = a.rows * a.ns;
+    constexpr bool f8 = F8;  // the FP8 cache: only the gather warps decode it
 
     if (threadIdx.x == 0) {
         mbar_init(bars + Q_FULL, 1);
@@ -170,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bars + RED + b, kSoftWarps);
         }
         for (int q = 0; q < kQuarters; ++q) {
-            mbar_init(bars + LAT_FULL + q, kCopyThreads);
+            mbar_init(bars + LAT_FULL + q, f8 ? kGatherThreads : kCopyThreads);
             mbar_init(bars + LAT_EMPTY + q, 1);
         }
         mbar_init(bars + S_FULL, 1);
@@ -246,8 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const bool valid = mask[b * kT + j] != 0;
                 // this warp's share of the chunk's gather, quarter by quarter as the
-                // previous chunk's PV frees them
-                for (int q = 0; q < kQuarters && ok; ++q) {
+                // previous chunk's PV frees them (the bf16 cache only)
+                for (int q = 0; q < kQuarters && ok && !f8; ++q) {
                     if (!bwait(LAT_EMPTY + q, (uint32_t)(n & 1) ^ 1u)) {
                         ok = false;
                         break;
@@ -610,7 +660,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                for (int q = 0; q < kQuarters && ok; ++q) {
+                if constexpr (F8) {
+                    // quarter q + 1's codes are requested while quarter q is decoded
+                    F8Quarter L;
+                    f8_load(L, rows + b * kT, a.ckv8, a.ckv_scale, 0, g);
+                    for (int q = 0; q < kQuarters && ok; ++q) {
+                        if (!bwait(LAT_EMPTY + q, (uint32_t)(n & 1) ^ 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        f8_store(L, lat, q, g);
+                        fence_async_smem();  // the tile's bytes are visible to the MMAs
+                        mbar_arrive(bars + LAT_FULL + q);
+                        if (q + 1 < kQuarters) f8_load(L, rows + b * kT, a.ckv8, a.ckv_scale, q + 1, g);
+                    }
+                }
+                for (int q = 0; q < kQuarters && ok && !f8; ++q) {
                     if (!bwait(LAT_EMPTY + q, (uint32_t)(n & 1) ^ 1u)) {
                         ok = false;
                         break;
@@ -661,9 +726,10 @@ int mla_tc_launch(const MlaTcParams& a, long long ckv_rows, cudaStream_t st) {
     int rc = make_tmap_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.qlat, kKVL,
                           (uint64_t)a.rows * kH, kKVL * 2, 64, kH, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
-    rc = set_max_smem((const void*)mla_tc_kernel, (int)kDyn);
+    auto kernel = a.ckv8 ? mla_tc_kernel<true> : mla_tc_kernel<false>;
+    rc = set_max_smem((const void*)kernel, (int)kDyn);
     if (rc) return rc;
-    cudaError_t e = launch_pdl(mla_tc_kernel, dim3((unsigned)grid), dim3(kThreads), kDyn, st, tmQ, a);
+    cudaError_t e = launch_pdl(kernel, dim3((unsigned)grid), dim3(kThreads), kDyn, st, tmQ, a);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_mla_decode tensor-core launch");
     return DSA_OK;

@@ -64,8 +64,19 @@ FP8_CASES = [
 ]
 
 
+@pytest.mark.parametrize("form", ["mma", "tcgen05"])
 @pytest.mark.parametrize("case", FP8_CASES, ids=[c[0] for c in FP8_CASES])
-def test_fp8_attention_parity(case):
+def test_fp8_attention_parity(case, form):
+    """Both attention kernels on the FP8 cache (the tcgen05 one, 64 heads, decodes in its
+    gather warps) equal the same kernel on the decoded cache stored as bf16, bit for bit."""
+    name, heads, hidden, lens, bs, ow, with_o = case
+    if form == "tcgen05" and heads != 64:
+        pytest.skip("the tcgen05 attention serves 64 heads")
+    with api.mla_kernel(form):
+        _fp8_attention_parity(case)
+
+
+def _fp8_attention_parity(case):
     name, heads, hidden, lens, bs, ow, with_o = case
     g = W.Geometry(index_kpool=4, index_heads=32, index_head_dim=128, index_topk=ow, heads=heads,
                    hidden=max(hidden, 32))
