@@ -15,8 +15,8 @@
 // shared-memory histograms) resolves the exact key and how many equal keys to take.
 // A ballot-prefix pass then emits the chosen positions in ascending order.
 //
-// Rows split over a cluster (C > 1) take select_radix_kernel: the CTAs first share
-// their slices' key bounds, then find the row's k-th key digit by digit (9-bit digits
+// With the radix option, rows split over a cluster (C > 1) take select_radix_kernel:
+// the CTAs first share their slices' key bounds, then find the row's k-th key digit by digit (9-bit digits
 // of kmax - key, from the top of the row's key range). Each CTA histograms the
 // next digit of its slice's keys that match the digits fixed so far and sends the
 // histogram to every other CTA of the cluster (bulk copies into the same place of each
@@ -30,12 +30,15 @@
 // is gathered. Every CTA then knows how many keys each CTA takes, hence its own offset in
 // the output row, and emits its chosen positions there in ascending order.
 //
-// If a cluster's slices do not fit that kernel's shared memory, the older form runs:
-// every CTA stages its slice's top-k (key, id) pairs in its own slot of a merge area
+// The default form for clustered rows merges instead: every CTA stages its slice's
+// top-kt (key, id) pairs, kt = min(k, 2 ceil(k / C)), in its own slot of a merge area
 // (unused entries get key 0) and moves the slot to the same place in CTA 0 with bulk
 // copies that complete on an mbarrier there; CTA 0 then selects the row's top-k among
-// the C x k candidates: the row's top-k is contained in the union of the slices' top-k,
-// and slot order keeps the ids ascending.
+// the C x kt candidates, slot order keeping the ids ascending. That is exact when each
+// slice that left keys out has its threshold below the candidates' k-th key; when one
+// does not (the row's top keys crowd into few slices), CTA 0 tells the other CTAs and
+// the exchange is repeated with every slice's full top-k, whose union always holds the
+// row's top-k.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -587,69 +590,104 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
         return;
     }
 
-    // This slice's top-k, staged in slot crank of this CTA's merge area, with bounds
-    // (chosen keys are >= the slice threshold and <= the slice maximum) and count;
-    // one bulk copy per part then moves the slot to the same place in CTA 0.
-    e.mode = 1;
-    e.rkeys = mloc + crank * sk4;
-    e.rids = mloc + C * sk4 + crank * sk4;
-    const int kc = block_topk(keys, n, a.sk, mm, sc, tbuf, a.tcap, e, &t);
-    for (int j = kc + threadIdx.x; j < sk4; j += kThreads) e.rkeys[j] = 0u;
+    // Round 0: this slice's top-kt, kt = min(k, 2 ceil(k / C)) (twice a slice's share
+    // of the row's top-k), staged in slot crank of this CTA's merge area with bounds
+    // (chosen keys are >= the slice threshold and <= the slice maximum), count and
+    // whether keys were left out; one bulk copy per part moves the slot to the same
+    // place in CTA 0, which finds the top-k threshold T of the C x kt candidates. The
+    // candidates hold the row's top-k whenever every slice that left keys out has a
+    // threshold below T: each left-out key is then below T, so every key >= T is a
+    // candidate, and slot order keeps equal keys in id order. Otherwise (a row whose
+    // top keys crowd into one slice) round 1 repeats the exchange with every slice's
+    // full top-k, whose union always holds the row's top-k.
+    const int kt = min(a.sk, 2 * ((a.sk + C - 1) / C));
+    const bool trim = kt < a.sk;
     uint32_t* st = mloc + 2 * C * sk4;
-    if (threadIdx.x == 0) {
-        st[4 * crank] = kc > 0 ? t.T : 0xffffffffu;
-        st[4 * crank + 1] = kc > 0 ? mm.kmax : 0u;
-        st[4 * crank + 2] = (uint32_t)kc;
-        st[4 * crank + 3] = 0u;
-    }
-    cluster_wait();  // phase 1 (long complete: CTA 0 arrived before its slice work)
-    const uint32_t slot = (uint32_t)sk4 * 4u;
-    if (crank != 0) {
-        fence_async_shared();  // the staged slot, written by this CTA's threads ...
-        __syncthreads();       // ... is visible to the bulk copies
+    uint32_t* again_flag = reinterpret_cast<uint32_t*>(mbar + 1);  // written by CTA 0
+    for (int round = 0;; ++round) {
+        const int kr = round == 0 ? kt : a.sk;
+        const int w = (kr + 3) & ~3;  // slot stride (keys)
+        e.mode = 1;
+        e.base = begin;
+        e.rkeys = mloc + crank * w;
+        e.rids = mloc + C * w + crank * w;
+        const int kc = block_topk(keys, n, kr, mm, sc, tbuf, a.tcap, e, &t);
+        for (int j = kc + threadIdx.x; j < w; j += kThreads) e.rkeys[j] = 0u;
         if (threadIdx.x == 0) {
-            bulk_to_peer(e.rkeys, e.rkeys, slot, mbar, 0);
-            bulk_to_peer(e.rids, e.rids, slot, mbar, 0);
-            bulk_to_peer(st + 4 * crank, st + 4 * crank, 16, mbar, 0);
+            st[4 * crank] = kc > 0 ? t.T : 0xffffffffu;
+            st[4 * crank + 1] = kc > 0 ? mm.kmax : 0u;
+            st[4 * crank + 2] = (uint32_t)kc;
+            st[4 * crank + 3] = mm.count > kr ? 1u : 0u;
         }
-        // phase 2: CTA 0 arrives once every push has landed, so this CTA's shared
-        // memory is no longer read when it leaves
+        // phase 1 (long complete: CTA 0 arrived before its slice work)
+        if (round == 0) cluster_wait();
+        const uint32_t slot = (uint32_t)w * 4u;
+        if (crank != 0) {
+            fence_async_shared();  // the staged slot, written by this CTA's threads ...
+            __syncthreads();       // ... is visible to the bulk copies
+            if (threadIdx.x == 0) {
+                bulk_to_peer(e.rkeys, e.rkeys, slot, mbar, 0);
+                bulk_to_peer(e.rids, e.rids, slot, mbar, 0);
+                bulk_to_peer(st + 4 * crank, st + 4 * crank, 16, mbar, 0);
+            }
+            // phase 2 (3 in round 1): CTA 0 arrives once every push has landed, so
+            // this CTA's shared memory is no longer read when it goes on; in round 0
+            // it has written again_flag here before it arrives
+            cluster_arrive();
+            cluster_wait();
+            if (round == 1 || *reinterpret_cast<volatile uint32_t*>(again_flag) == 0u) return;
+            continue;
+        }
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(mbar, (uint32_t)(C - 1) * (2u * slot + 16u));
+            // bounded: a push that never lands leaves the row unselected (all -1)
+            sc.pick[0] = mbar_wait(mbar, (uint32_t)round) ? 1 : 0;
+        }
+        __syncthreads();
+        const bool landed = sc.pick[0] != 0;
+        __syncthreads();  // pick[] is scratch of the threshold below
+        const uint32_t* mkeys = mloc;
+        MinMax mg{0xffffffffu, 0u, 0};
+        bool again = false;
+        Thr tm{0xffffffffu, 0, 0};
+        if (landed) {
+            for (int c = 0; c < C; ++c) {
+                mg.kmin = min(mg.kmin, st[4 * c]);
+                mg.kmax = max(mg.kmax, st[4 * c + 1]);
+                mg.count += (int)st[4 * c + 2];
+            }
+            tm = bin_threshold(mkeys, C * w, a.sk, mg, sc, tbuf, a.tcap);
+            if (round == 0 && trim)
+                for (int c = 0; c < C; ++c) again |= st[4 * c + 3] != 0u && !(st[4 * c] < tm.T);
+        }
+        if (round == 0 && threadIdx.x > 0 && threadIdx.x < C) {
+            uint32_t d;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n"
+                         : "=r"(d)
+                         : "r"(smem_u32(again_flag)), "r"((uint32_t)threadIdx.x));
+            asm volatile("st.shared::cluster.u32 [%0], %1;\n" ::"r"(d), "r"(again ? 1u : 0u)
+                         : "memory");
+        }
+        // phase 2 (3 in round 1): the pushed slots are in; the other CTAs may go on
+        __syncwarp();
         cluster_arrive();
-        cluster_wait();
-        return;
+        if (!again) {
+            int kk = 0;
+            if (landed && tm.kk > 0) {
+                e.mode = 2;
+                e.base = 0;
+                e.ids = mkeys + C * w;
+                ordered_emit(mkeys, C * w, tm, sc, e);
+                kk = tm.kk;
+            }
+            int t0, tend;
+            tail_range(a, r, &t0, &tend);
+            fill_tail(out, a.sk, tok, a.ow, a.kpool, kk, a.tail_at, t0, tend);
+            cluster_wait();
+            return;
+        }
+        cluster_wait();  // phase 2 (complete) before round 1's arrive
     }
-    if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(mbar, (uint32_t)(C - 1) * (2u * slot + 16u));
-        // bounded: a push that never lands leaves the row unselected (all -1)
-        sc.pick[0] = mbar_wait(mbar, 0) ? 1 : 0;
-    }
-    __syncthreads();
-    const bool landed = sc.pick[0] != 0;
-    __syncthreads();  // pick[] is scratch of the merge below
-    cluster_arrive();  // phase 2: the pushed slots are in; the other CTAs may leave
-    if (!landed) {
-        int t0, tend;
-        tail_range(a, r, &t0, &tend);
-        fill_tail(out, a.sk, tok, a.ow, a.kpool, 0, a.tail_at, t0, tend);
-        cluster_wait();
-        return;
-    }
-
-    const uint32_t* mkeys = mloc;
-    MinMax mg{0xffffffffu, 0u, 0};
-    for (int c = 0; c < C; ++c) {
-        mg.kmin = min(mg.kmin, st[4 * c]);
-        mg.kmax = max(mg.kmax, st[4 * c + 1]);
-        mg.count += (int)st[4 * c + 2];
-    }
-    e.mode = 2;
-    e.base = 0;
-    e.ids = mkeys + C * sk4;
-    const int kk = block_topk(mkeys, C * sk4, a.sk, mg, sc, tbuf, a.tcap, e, &t);
-    int t0, tend;
-    tail_range(a, r, &t0, &tend);
-    fill_tail(out, a.sk, tok, a.ow, a.kpool, kk, a.tail_at, t0, tend);
-    cluster_wait();  // phase 2 (complete: every CTA arrived)
 }
 
 // ---------------------------------------------------------------------------

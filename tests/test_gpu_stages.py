@@ -145,6 +145,21 @@ def _tie_rows(rng, rows, P, kind):
         return np.full((rows, P), -np.inf, dtype=np.float32)
     if kind == "positive":
         return (rng.random((rows, P)) * 3).astype(np.float32)
+    if kind == "ramp":
+        # scores rise with the pool id (fall on odd rows): a row's top-k sits in the
+        # last (first) slice of a clustered row, whose trimmed candidates cannot hold it
+        x = np.tile(np.arange(P, dtype=np.float32) / max(P, 1), (rows, 1))
+        x[1::2] = x[1::2, ::-1]
+        return np.ascontiguousarray(x)
+    if kind == "crowd":
+        # noise with one raised window of P/16 pools per row, some of it tied
+        x = rng.standard_normal((rows, P)).astype(np.float32)
+        for r in range(rows):
+            w = max(1, P // 16)
+            a = int(rng.integers(0, max(1, P - w)))
+            x[r, a:a + w] += 4.0
+            x[r, a:a + w:3] = 5.0
+        return x
     raise ValueError(kind)
 
 
@@ -156,6 +171,9 @@ SELECT_CASES = [
     (1, 327680, 2048, 4, "positive"), (2, 40000, 64, 1, "ties"),
     # select_k not a multiple of 4 on clustered rows (padded merge slots)
     (3, 60000, 2044, 4, "ties"), (2, 50000, 1026, 1, "normal"),
+    # top keys crowded into one slice (the merge's second, full-top-k round)
+    (8, 65536, 2048, 4, "ramp"), (4, 65536, 2048, 4, "crowd"), (3, 100003, 2044, 4, "crowd"),
+    (2, 16384, 2048, 4, "ramp"),
 ]
 
 
@@ -192,6 +210,7 @@ SELECT_EXPAND_CASES = [
     (300, 2048, 512, 4, "ties", 0, 0), (2, 40000, 64, 1, "ties", 2, 3),
     (3, 2000, 128, 16, "normal", 16, 0), (2, 0, 256, 4, "allinf", 0, 9),
     (2, 70001, 2042, 2, "positive", 1, 3),
+    (8, 65536, 2048, 4, "ramp", 0, 0), (4, 65536, 2048, 4, "crowd", 2, 5),
 ]
 
 
