@@ -128,6 +128,14 @@ int dsa_abi_version(void);
  *                       and K of 512), DSA_PROJECT_KERNEL_TCGEN05 (the same),
  *                       DSA_PROJECT_KERNEL_MMA (the mma.sync stream-K form with
  *                       its partial-sum reduction).
+ *   DSA_OPT_INJECT_STALL  fault injection for tests of the bounded pipeline waits
+ *                       (default 0, off). 1 arms it for the next launch of the
+ *                       tensor-core projection: that launch's copy warp stops before
+ *                       its last stage, so the MMA warp's bounded wait gives up after
+ *                       about 1 s; the launch ORs DSA_STATUS_TIMEOUT into its status
+ *                       word, winds down (the copies it issued have landed, its
+ *                       tensor memory is freed, every cluster barrier is passed) and
+ *                       leaves y invalid. The launch that takes it resets it to 0.
  *
  * dsa_set_option returns DSA_ERR_INVALID_ARG for an unknown option or value;
  * dsa_get_option returns the current value, or -1 for an unknown option.
@@ -145,6 +153,7 @@ int dsa_abi_version(void);
 #define DSA_PROJECT_KERNEL_AUTO 0
 #define DSA_PROJECT_KERNEL_TCGEN05 1
 #define DSA_PROJECT_KERNEL_MMA 2
+#define DSA_OPT_INJECT_STALL 4
 int dsa_set_option(int option, int value);
 int dsa_get_option(int option);
 

@@ -35,6 +35,7 @@ DSA_OPT_PROJECT_KERNEL = 3
 DSA_PROJECT_KERNEL_AUTO = 0
 DSA_PROJECT_KERNEL_TCGEN05 = 1
 DSA_PROJECT_KERNEL_MMA = 2
+DSA_OPT_INJECT_STALL = 4
 
 
 class DsaPaging(ctypes.Structure):

@@ -62,6 +62,7 @@ static std::atomic<int> g_opt_pdl{1};
 static std::atomic<int> g_opt_mla_kernel{DSA_MLA_KERNEL_AUTO};
 static std::atomic<int> g_opt_select_kernel{DSA_SELECT_KERNEL_MERGE};
 static std::atomic<int> g_opt_project_kernel{DSA_PROJECT_KERNEL_AUTO};
+static std::atomic<int> g_opt_inject_stall{0};
 
 bool pdl_enabled() { return g_opt_pdl.load(std::memory_order_relaxed) != 0; }
 
@@ -70,6 +71,8 @@ int mla_kernel_choice() { return g_opt_mla_kernel.load(std::memory_order_relaxed
 int select_kernel_choice() { return g_opt_select_kernel.load(std::memory_order_relaxed); }
 
 int project_kernel_choice() { return g_opt_project_kernel.load(std::memory_order_relaxed); }
+
+int take_inject_stall() { return g_opt_inject_stall.exchange(0, std::memory_order_relaxed); }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -215,6 +218,12 @@ int dsa_set_option(int option, int value) {
                             "dsa_set_option: DSA_OPT_PROJECT_KERNEL takes 0, 1 or 2, not %d", value);
             g_opt_project_kernel.store(value, std::memory_order_relaxed);
             return DSA_OK;
+        case DSA_OPT_INJECT_STALL:
+            if (value != 0 && value != 1)
+                return fail(DSA_ERR_INVALID_ARG,
+                            "dsa_set_option: DSA_OPT_INJECT_STALL takes 0 or 1, not %d", value);
+            g_opt_inject_stall.store(value, std::memory_order_relaxed);
+            return DSA_OK;
         default:
             return fail(DSA_ERR_INVALID_ARG, "dsa_set_option: unknown option %d", option);
     }
@@ -226,6 +235,7 @@ int dsa_get_option(int option) {
         case DSA_OPT_MLA_KERNEL: return g_opt_mla_kernel.load(std::memory_order_relaxed);
         case DSA_OPT_SELECT_KERNEL: return g_opt_select_kernel.load(std::memory_order_relaxed);
         case DSA_OPT_PROJECT_KERNEL: return g_opt_project_kernel.load(std::memory_order_relaxed);
+        case DSA_OPT_INJECT_STALL: return g_opt_inject_stall.load(std::memory_order_relaxed);
         default: return -1;
     }
 }

@@ -36,6 +36,7 @@ bool pdl_enabled();
 int mla_kernel_choice();     // DSA_OPT_MLA_KERNEL
 int select_kernel_choice();  // DSA_OPT_SELECT_KERNEL
 int project_kernel_choice();  // DSA_OPT_PROJECT_KERNEL
+int take_inject_stall();      // DSA_OPT_INJECT_STALL, reset to 0 by the taking
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t st, Args&&... args) {

@@ -110,6 +110,7 @@ struct TcProjArgs {
     int kper;       // K per CTA (a multiple of BK)
     const uint8_t* A;  // o_absorb, for the demotion below
     int demote_rows;   // A rows [0, demote_rows) were staged in L2 at evict_last
+    int stall_at;      // >= 0: the copies stop before this stage (DSA_OPT_INJECT_STALL)
 };
 
 template <int N, int MT, int KS>
@@ -161,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // A is read once per call: evict_first, so that the stream does not push
             // out A lines a prefetch staged in L2 before the other CTAs reach them.
             const uint64_t ef = l2_evict_first();
-            const int pre = nst < kStages ? nst : kStages;
+            int pre = nst < kStages ? nst : kStages;
+            if (a.stall_at >= 0 && a.stall_at < pre) pre = a.stall_at;
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(full + i, bytes);
 #pragma unroll
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(smem_u32(smem + i * L::STAGE + L::AB), &tmX, k0 + i * BK, a.n0, full + i);
             int i = pre;
             for (; i < nst; ++i) {
+                if (i == a.stall_at) break;  // injected stall: nothing more is copied
                 const int s = i % kStages;
                 if (!poll_wait(empty + s, (uint32_t)(((i / kStages) & 1) ^ 1), abort_flag,
                                    a.status))
@@ -350,6 +353,7 @@ int launch_tc(const uint16_t* x, int R, int K, const uint16_t* A, int hidden, co
     constexpr int kKS = KS;
     TcProjArgs a = a0;
     a.kper = K / KS;
+    if (a.stall_at >= 0) a.stall_at = a.kper / BK - 1;  // before the last stage
     int rc = set_max_smem((const void*)project_tc_kernel<N, MT, KS>, (int)L::DYN);
     if (rc) return rc;
     CUtensorMap tmA, tmX;
@@ -478,7 +482,9 @@ int project_tc_launch(const void* x, bool x_f32, int rows, int K, const uint16_t
                               ? 0
                               : l2_staged_overlap(A, (size_t)hidden * row_bytes);
     const int staged_rows = (int)((staged + row_bytes - 1) / row_bytes);
+    const bool stall = take_inject_stall() != 0;
     for (int n0 = 0; n0 < rows; n0 += 64) {
+        a.stall_at = stall && n0 == 0 ? 0 : -1;
         a.n0 = n0;
         a.nrows = rows - n0 < 64 ? rows - n0 : 64;
         a.demote_rows = n0 + 64 >= rows ? staged_rows : 0;

@@ -86,6 +86,12 @@ def test_launch_options(lib):
         assert lib.dsa_get_option(2) == 1
         assert lib.dsa_set_option(2, 2) == DSA_ERR_INVALID_ARG
         assert lib.dsa_set_option(7, 0) == DSA_ERR_INVALID_ARG
+        # DSA_OPT_INJECT_STALL: off by default, 0 or 1 only
+        assert lib.dsa_get_option(4) == 0
+        assert lib.dsa_set_option(4, 2) == DSA_ERR_INVALID_ARG
+        assert lib.dsa_set_option(4, 1) == DSA_OK
+        assert lib.dsa_get_option(4) == 1
+        assert lib.dsa_set_option(4, 0) == DSA_OK
     finally:
         lib.dsa_set_option(DSA_OPT_PDL, 1)
         lib.dsa_set_option(DSA_OPT_MLA_KERNEL, DSA_MLA_KERNEL_AUTO)

@@ -592,6 +592,45 @@ def test_latent_project_parity(rows, heads, hidden, proj_kernel):
     H.check_attention(y.t.float().cpu().numpy(), ref, "y")
 
 
+@pytest.mark.parametrize("rows,heads,hidden", [(8, 8, 1024), (40, 16, 512), (3, 64, 4096)])
+def test_projection_wait_timeout_flags_status(rows, heads, hidden):
+    """A bounded pipeline wait that runs out: DSA_OPT_INJECT_STALL stops the next
+    tensor-core projection's copies before their last stage, so its MMA warp waits on
+    a stage that nothing fills. After about a second that launch ORs
+    DSA_STATUS_TIMEOUT into its status word and returns (no fault, no hang); the
+    option is taken by that launch, and the next launch on the same context is
+    bit-identical to one before it."""
+    rng = np.random.default_rng(rows * 3 + hidden)
+    olat = torch.from_numpy(rng.standard_normal((rows, heads, 512)).astype(np.float32)).cuda()
+    A = torch.from_numpy((rng.standard_normal((hidden, heads * 512)) * 0.02).astype(np.float32)
+                         ).to(torch.bfloat16).cuda()
+    ws = torch.zeros(max(1, api.dsa_latent_project_workspace(rows, heads, hidden)),
+                     dtype=torch.uint8, device="cuda")
+    with api.project_kernel("tcgen05"):
+        st0 = torch.zeros(1, dtype=torch.int32, device="cuda")
+        y0 = torch.zeros((rows, hidden), dtype=torch.bfloat16, device="cuda")
+        api.dsa_latent_project(olat, A, y0, st0, ws)
+        torch.cuda.synchronize()
+        assert int(st0.item()) == 0
+        st1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+        y1 = torch.zeros_like(y0)
+        api.dsa_set_option(api._lib.DSA_OPT_INJECT_STALL, 1)
+        try:
+            api.dsa_latent_project(olat, A, y1, st1, ws)
+        finally:
+            taken = api.dsa_get_option(api._lib.DSA_OPT_INJECT_STALL)
+            api.dsa_set_option(api._lib.DSA_OPT_INJECT_STALL, 0)
+        torch.cuda.synchronize()
+        assert taken == 0
+        assert int(st1.item()) & api._lib.DSA_STATUS_TIMEOUT
+        st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+        y2 = torch.zeros_like(y0)
+        api.dsa_latent_project(olat, A, y2, st2, ws)
+        torch.cuda.synchronize()
+        assert int(st2.item()) == 0
+        assert torch.equal(y0, y2)
+
+
 @pytest.mark.parametrize("rows,heads,hidden,frac", [(8, 64, 4096, 0.25), (64, 64, 4096, 0.25),
                                                     (70, 16, 256, 1.0), (20, 8, 128, 0.4)])
 def test_project_after_l2_prefetch_is_identical(rows, heads, hidden, frac, proj_kernel):
