@@ -385,6 +385,40 @@ __device__ __forceinline__ void emit_one(const EmitTo& e, const uint32_t* keys, 
     }
 }
 
+// The emit loop of ordered_emit for mode 0, with the per-key work written so that it
+// needs no branch: a warp's threads rarely agree on which of their four keys are
+// chosen, and a divergent branch per key makes the pass issue-bound. KIND 0: pool
+// ids; KIND 2: pool ids and four token ids per pool, 16-byte stores (kpool 4, an
+// aligned token row). Used by the kernel that walks single-CTA rows, where the
+// pass repeats per row; elsewhere the generic loop below runs (there each CTA runs
+// the emit once, and a second loop's instructions cost more to fetch than they save
+// under the step's concurrent L2 prefetch).
+template <int KIND>
+__device__ __forceinline__ void emit_runs(const uint32_t* keys, int i0, int i1, uint32_t T,
+                                          int need_eq, int kk, int pos, int eqr, const EmitTo& e) {
+    for (int i = i0; i < i1 && pos < kk; i += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
+        const uint32_t k4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t key = i + j < i1 ? k4[j] : 0u;
+            const bool eq = key == T;
+            const bool sel = (key > T || (eq && eqr < need_eq)) && pos < kk;
+            eqr += eq ? 1 : 0;
+            const int at = pos;
+            pos += sel ? 1 : 0;
+            if (sel) {
+                const int p = e.base + i + j;
+                e.out[at] = p;
+                if (KIND == 2) {
+                    const int t0 = e.first_key + 4 * p;
+                    *reinterpret_cast<int4*>(e.tok + 4 * at) = make_int4(t0, t0 + 1, t0 + 2, t0 + 3);
+                }
+            }
+        }
+    }
+}
+
 // -1 over the pool ids from rank kk on, and over the token ids from kk*kpool on,
 // except that token-id positions tail_at + i hold t0 + i while that is below tend
 // (the tokens of the row's trailing partial pool, with always_select_tail).
@@ -415,6 +449,7 @@ __device__ __forceinline__ void tail_range(const SelectArgs& a, int r, int* t0, 
 // loads of a quarter warp hit distinct banks; one block scan of its (#greater,
 // #equal) counts, packed in 16-bit halves (n <= 65535), gives the rank of its first
 // chosen key.
+template <bool RUNS>
 __device__ __noinline__ void ordered_emit(const uint32_t* keys, int n, Thr t, BlockScratch& sc,
                                           EmitTo e) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -447,15 +482,22 @@ __device__ __noinline__ void ordered_emit(const uint32_t* keys, int n, Thr t, Bl
     for (int w = 0; w < warp; ++w) excl += (uint32_t)sc.wcnt[w];
     int eqr = (int)(excl >> 16);
     int pos = (int)(excl & 0xffffu) + min(eqr, t.need_eq);
-    for (int i = i0; i < i1 && pos < t.kk; i += 4) {
-        const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
-        const uint32_t k4[4] = {v.x, v.y, v.z, v.w};
+    if (RUNS && e.mode == 0 && !e.tok) {
+        emit_runs<0>(keys, i0, i1, T, t.need_eq, t.kk, pos, eqr, e);
+    } else if (RUNS && e.mode == 0 && e.kpool == 4 &&
+               (reinterpret_cast<uintptr_t>(e.tok) & 15u) == 0u) {
+        emit_runs<2>(keys, i0, i1, T, t.need_eq, t.kk, pos, eqr, e);
+    } else {
+        for (int i = i0; i < i1 && pos < t.kk; i += 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
+            const uint32_t k4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t key = i + j < i1 ? k4[j] : 0u;
-            bool sel = key > T;
-            if (key == T) sel = eqr++ < t.need_eq;
-            if (sel && pos < t.kk) emit_one(e, keys, pos++, i + j);
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t key = i + j < i1 ? k4[j] : 0u;
+                bool sel = key > T;
+                if (key == T) sel = eqr++ < t.need_eq;
+                if (sel && pos < t.kk) emit_one(e, keys, pos++, i + j);
+            }
         }
     }
     __syncthreads();
@@ -465,16 +507,18 @@ __device__ __noinline__ void ordered_emit(const uint32_t* keys, int n, Thr t, Bl
 // nonzero keys have min, max and count mm (bounds may be loose): emits the chosen
 // positions ascending and returns how many, min(k, #nonzero keys); *thr gets the
 // threshold (every chosen key is >= thr->T).
+template <bool RUNS>
 __device__ __noinline__ int block_topk(const uint32_t* keys, int n, int k, MinMax mm,
                                        BlockScratch& sc, uint32_t* tbuf, int tcap, EmitTo e,
                                        Thr* thr) {
     const Thr t = bin_threshold(keys, n, k, mm, sc, tbuf, tcap);
     *thr = t;
     if (t.kk == 0) return 0;
-    ordered_emit(keys, n, t, sc, e);
+    ordered_emit<RUNS>(keys, n, t, sc, e);
     return t.kk;
 }
 
+template <bool RUNS>
 __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_group& cluster,
                                            int r, uint32_t* keys, BlockScratch& sc);
 
@@ -489,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
     __shared__ BlockScratch sc;
     pdl_wait();
     if (!ROWS) {
-        select_row(a, cluster, (int)blockIdx.x / C, keys, sc);
+        select_row<false>(a, cluster, (int)blockIdx.x / C, keys, sc);
         return;
     }
     for (int r = blockIdx.x; r < a.rows; r += gridDim.x) {
@@ -504,11 +548,12 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a) {
                              "r"((uint32_t)(hi - lo))
                              : "memory");
         }
-        select_row(a, cluster, r, keys, sc);
+        select_row<true>(a, cluster, r, keys, sc);
         __syncthreads();  // the next row reuses keys[] and the scratch
     }
 }
 
+template <bool RUNS>
 __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_group& cluster,
                                            int r, uint32_t* keys, BlockScratch& sc) {
     const int C = (int)cluster.num_blocks();
@@ -583,7 +628,7 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
     Thr t;
     if (C == 1) {
         e.mode = 0;
-        const int kk = block_topk(keys, n, a.sk, mm, sc, tbuf, a.tcap, e, &t);
+        const int kk = block_topk<RUNS>(keys, n, a.sk, mm, sc, tbuf, a.tcap, e, &t);
         int t0, tend;
         tail_range(a, r, &t0, &tend);
         fill_tail(out, a.sk, tok, a.ow, a.kpool, kk, a.tail_at, t0, tend);
@@ -611,7 +656,7 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
         e.base = begin;
         e.rkeys = mloc + crank * w;
         e.rids = mloc + C * w + crank * w;
-        const int kc = block_topk(keys, n, kr, mm, sc, tbuf, a.tcap, e, &t);
+        const int kc = block_topk<false>(keys, n, kr, mm, sc, tbuf, a.tcap, e, &t);
         for (int j = kc + threadIdx.x; j < w; j += kThreads) e.rkeys[j] = 0u;
         if (threadIdx.x == 0) {
             st[4 * crank] = kc > 0 ? t.T : 0xffffffffu;
@@ -677,7 +722,7 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
                 e.mode = 2;
                 e.base = 0;
                 e.ids = mkeys + C * w;
-                ordered_emit(mkeys, C * w, tm, sc, e);
+                ordered_emit<false>(mkeys, C * w, tm, sc, e);
                 kk = tm.kk;
             }
             int t0, tend;
@@ -1040,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_radix_kernel(SelectArgs a,
             e.tok = tok ? tok + (long long)off * a.kpool : nullptr;
             e.first_key = a.first_key;
             e.kpool = a.kpool;
-            ordered_emit(keys, n, t, sc, e);
+            ordered_emit<false>(keys, n, t, sc, e);
         }
         if (crank == 0) fill_tail(out, a.sk, tok, a.ow, a.kpool, K, a.tail_at, t0, tend);
     }
