@@ -181,6 +181,13 @@ constexpr int kStagePools = 64;
 constexpr int kStages = 3;  // deeper rings measured slower (less L1 beside them)
 constexpr int kCtasPerSm = 3;  // 12 consumer warps per SM hide the MMA and shuffle latency
 constexpr int kTmaThreads = 5 * 32;
+// Paged caches with up to this many rows: the units are the rows' visible stages only,
+// split evenly over the CTAs (a CTA finds its first unit by a scan over the rows), and
+// the pools past a row's visible stages are filled with -inf afterwards by every CTA.
+// A batch of unequal lengths would otherwise leave the CTAs that cover long rows with
+// all the copies. (A contiguous cache keeps every stage of every row a unit: its rows
+// are usually equal, and the scan would delay the first copy.)
+constexpr int kBalRows = 256;
 
 struct RowInfo {
     int seq;
@@ -201,7 +208,48 @@ __device__ __forceinline__ RowInfo row_info(const ScoreArgs& a, int r) {
     return ri;
 }
 
-template <int IHD, int NT>
+// 64-pool stages of a row that hold visible pools.
+__device__ __forceinline__ int vis_stages(const RowInfo& ri, int spr) {
+    return ri.seq < 0 ? 0 : min(spr, (ri.nvis + kStagePools - 1) / kStagePools);
+}
+
+// Moves (r, st) to the unit to process next and refreshes the row's info when the row
+// changes (returns true then). Balanced: rows' stages from their visible count on are
+// skipped; otherwise every stage of every row is a unit.
+template <bool BAL>
+__device__ __forceinline__ bool next_unit(const ScoreArgs& a, int spr, int& r, int& st, int& cur_r,
+                                          RowInfo& ri, int& vs) {
+    bool changed = false;
+    if (BAL) {
+        if (r != cur_r) {
+            ri = row_info(a, r);
+            vs = vis_stages(ri, spr);
+            cur_r = r;
+            changed = true;
+        }
+        while (st >= vs && r + 1 < a.rows) {
+            ++r;
+            st = 0;
+            ri = row_info(a, r);
+            vs = vis_stages(ri, spr);
+            cur_r = r;
+            changed = true;
+        }
+    } else {
+        if (st == spr) {
+            st = 0;
+            ++r;
+        }
+        if (r != cur_r) {
+            ri = row_info(a, r);
+            cur_r = r;
+            changed = true;
+        }
+    }
+    return changed;
+}
+
+template <int IHD, int NT, bool BAL>
 __global__ void __launch_bounds__(kTmaThreads, kCtasPerSm) score_tma_kernel(ScoreArgs a) {
     constexpr int NV = IHD / 32;
     constexpr int ROWB = IHD * 2;                    // bytes per pooled key
@@ -211,12 +259,13 @@ __global__ void __launch_bounds__(kTmaThreads, kCtasPerSm) score_tma_kernel(Scor
     unsigned long long* bad = reinterpret_cast<unsigned long long*>(flags + kStages * kStagePools);
     uint64_t* full = reinterpret_cast<uint64_t*>(bad + kStages);
     uint64_t* empty = full + kStages;
+    long long* s_unit = reinterpret_cast<long long*>(empty + kStages);  // BAL: [u0, u1)
+    int* s_first = reinterpret_cast<int*>(s_unit + 2);                  // and u0's (row, stage)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int spr = (a.p_stride + kStagePools - 1) / kStagePools;  // stages per row
     const long long U = (long long)a.rows * spr;
     const long long G = gridDim.x;
     pdl_wait();
-    const long long u0 = blockIdx.x * U / G, u1 = (blockIdx.x + 1) * U / G;
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -224,7 +273,54 @@ __global__ void __launch_bounds__(kTmaThreads, kCtasPerSm) score_tma_kernel(Scor
         }
         fence_mbar_init();
     }
+    if (BAL && warp == 0) {
+        // visible stages of rows 32k + lane, their total, and the row holding unit u0
+        int vsl[kBalRows / 32];
+        long long tot = 0;
+#pragma unroll
+        for (int k = 0; k < kBalRows / 32; ++k) {
+            const int rr = 32 * k + lane;
+            vsl[k] = rr < a.rows ? vis_stages(row_info(a, rr), spr) : 0;
+            tot += vsl[k];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        const long long b0 = blockIdx.x * tot / G, b1 = (blockIdx.x + 1) * tot / G;
+        long long base = 0;
+        int r0 = 0, st0 = 0;
+        bool found = false;
+#pragma unroll
+        for (int k = 0; k < kBalRows / 32; ++k) {
+            int incl = vsl[k];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const long long end = base + incl;  // units up to the end of row 32k + lane
+            const unsigned m = __ballot_sync(0xffffffffu, !found && end > b0);
+            if (m != 0u) {
+                const int l = __ffs(m) - 1;
+                const long long endl = __shfl_sync(0xffffffffu, end, l);
+                const int vl = __shfl_sync(0xffffffffu, vsl[k], l);
+                r0 = 32 * k + l;
+                st0 = (int)(b0 - (endl - vl));
+                found = true;
+            }
+            base += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            s_unit[0] = b0;
+            s_unit[1] = b1;
+            s_first[0] = r0;
+            s_first[1] = st0;
+        }
+    }
     __syncthreads();
+    const long long u0 = BAL ? s_unit[0] : blockIdx.x * U / G;
+    const long long u1 = BAL ? s_unit[1] : (blockIdx.x + 1) * U / G;
+    const int r_first = BAL ? s_first[0] : (int)(u0 / spr);
+    const int st_first = BAL ? s_first[1] : (int)(u0 % spr);
 
     if (warp == 4) {
         // ---------------- producer (lane 0 owns the ring; on a paged cache the whole
@@ -232,24 +328,17 @@ __global__ void __launch_bounds__(kTmaThreads, kCtasPerSm) score_tma_kernel(Scor
         // the slot wait, and each lane copies its block's run of pools)
         const bool paged = a.pg.block_table != nullptr;
         const int ppb = paged ? a.pg.block_size / a.kpool : 1;
-        int cur_r = -1;
+        int cur_r = -1, vs = 0;
         RowInfo ri{};
         long long i = 0;
         bool ok = true;
-        int r = (int)(u0 / spr), st = (int)(u0 % spr);
+        int r = r_first, st = st_first;
         for (long long u = u0; u < u1; ++u, ++i) {
             const int s = (int)(i % kStages);
             const uint32_t ph = (uint32_t)((i / kStages) & 1);
-            if (st == spr) {
-                st = 0;
-                ++r;
-            }
+            if (next_unit<BAL>(a, spr, r, st, cur_r, ri, vs) && lane == 0 && ri.seq < 0 && u == u0)
+                flag_status(a.status, DSA_STATUS_BAD_TOKEN);
             const int p0 = st++ * kStagePools;
-            if (r != cur_r) {
-                ri = row_info(a, r);
-                if (lane == 0 && ri.seq < 0 && u == u0) flag_status(a.status, DSA_STATUS_BAD_TOKEN);
-                cur_r = r;
-            }
             const int nvalid = ri.seq < 0 ? 0 : max(0, min(kStagePools, ri.nvis - p0));
             // blocks b0 .. b0 + nb - 1 hold the stage's pools; lane j looks up j and j + 32
             const int b0 = p0 / ppb;
@@ -336,20 +425,16 @@ __global__ void __launch_bounds__(kTmaThreads, kCtasPerSm) score_tma_kernel(Scor
     const int g = lane >> 2, q = lane & 3;
     uint32_t bq[NT][NV][4];
     float wv[NT][2];
-    int cur_r = -1;
+    int cur_r = -1, vs = 0;
     RowInfo ri{};
     long long i = 0;
-    int r = (int)(u0 / spr), st = (int)(u0 % spr);
+    int r = r_first, st = st_first;
     for (long long u = u0; u < u1; ++u, ++i) {
         const int s = (int)(i % kStages);
         const uint32_t ph = (uint32_t)((i / kStages) & 1);
-        if (st == spr) {
-            st = 0;
-            ++r;
-        }
+        const bool new_row = next_unit<BAL>(a, spr, r, st, cur_r, ri, vs);
         const int p0 = st++ * kStagePools + 16 * warp;
-        if (r != cur_r) {
-            ri = row_info(a, r);
+        if (new_row) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int h = nt * 8 + g;
@@ -369,7 +454,6 @@ __global__ void __launch_bounds__(kTmaThreads, kCtasPerSm) score_tma_kernel(Scor
                     wv[nt][j] = hh < a.heads ? __ldg(a.w + (long long)r * a.heads + hh) : 0.f;
                 }
             }
-            cur_r = r;
         }
         const int pA = p0 + g, pB = pA + 8;
         bool cA = false, cB = false;
@@ -427,24 +511,44 @@ __global__ void __launch_bounds__(kTmaThreads, kCtasPerSm) score_tma_kernel(Scor
         if (q == 0 && pA < a.p_stride) srow[pA] = cA ? sA : -INFINITY;
         if (q == 1 && pB < a.p_stride) srow[pB] = cB ? sB : -INFINITY;
     }
+    if (BAL) {
+        // -inf over each row's pools past its visible stages (no unit covers them):
+        // CTA b writes the b-th of G equal runs of that tail, thread t rows t, t + 128, ...
+        for (int rr = tid; rr < a.rows; rr += 4 * 32) {
+            const RowInfo rj = row_info(a, rr);
+            if (rj.seq < 0 && blockIdx.x == 0) flag_status(a.status, DSA_STATUS_BAD_TOKEN);
+            const long long t0 = (long long)vis_stages(rj, spr) * kStagePools;
+            const long long len = (long long)a.p_stride - t0;
+            if (len <= 0) continue;
+            const long long per = (len + G - 1) / G;
+            const long long lo = t0 + (long long)blockIdx.x * per;
+            const long long hi = min(lo + per, (long long)a.p_stride);
+            float* srow = a.scores + (long long)rr * a.p_stride;
+            for (long long p = lo; p < hi; ++p) srow[p] = -INFINITY;
+        }
+    }
 }
 
 template <int IHD, int NT>
 int launch_tma(const ScoreArgs& a0, cudaStream_t st) {
-    constexpr int smem = kStages * kStagePools * IHD * 2 + kStages * kStagePools + 3 * kStages * 8;
+    // ring, flags, bad masks, full and empty barriers, the balanced split's unit range
+    constexpr int smem =
+        kStages * kStagePools * IHD * 2 + kStages * kStagePools + 3 * kStages * 8 + 32;
     ScoreArgs a = a0;
     // 16-byte flag copies need 16-byte aligned runs: whole 16-pool groups per row.
     const bool al = (reinterpret_cast<uintptr_t>(a.pv) & 15u) == 0u;
     a.flags_tma = al && (a.pg.block_table == nullptr
                              ? (a.pg.max_seq_len / a.kpool) % 16 == 0
                              : (a.pg.block_size / a.kpool) % 16 == 0);
-    int rc = set_max_smem((const void*)score_tma_kernel<IHD, NT>, smem);
+    const bool bal = a.pg.block_table != nullptr && a.rows <= kBalRows;
+    auto kernel = bal ? score_tma_kernel<IHD, NT, true> : score_tma_kernel<IHD, NT, false>;
+    int rc = set_max_smem((const void*)kernel, smem);
     if (rc) return rc;
     const int spr = (a.p_stride + kStagePools - 1) / kStagePools;
     const long long U = (long long)a.rows * spr;
     const long long slots = (long long)sm_count() * kCtasPerSm;
     const int G = (int)(U < slots ? U : slots);
-    cudaError_t e = launch_pdl(score_tma_kernel<IHD, NT>, dim3(G), dim3(kTmaThreads), smem, st, a);
+    cudaError_t e = launch_pdl(kernel, dim3(G), dim3(kTmaThreads), smem, st, a);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "dsa_score launch");
     return DSA_OK;

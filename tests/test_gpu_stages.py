@@ -98,6 +98,11 @@ SCORE_CASES = [
     ("h4-d64", dict(index_heads=4, index_head_dim=64), [2048], None, None, 0),
     ("h20-d128", dict(index_heads=20), [1234, 99], None, None, 0),
     ("h32-paged", dict(), [4000, 1000, 65], 64, None, 0),
+    # paged rows of very unequal length (the CTAs split the visible stages only; the
+    # rest of each row is filled with -inf): an empty and a 3-token sequence among them
+    ("h32-paged-ragged", dict(), [9000, 64, 3, 20000, 0, 777, 4096, 12345], 64, None, 0),
+    ("h32-paged-ctx", dict(), [6000], 64, [1, 3, 4, 5, 5999, 6000, 2000, 17], 0),
+    ("h8-paged-b16", dict(index_heads=8), [700, 5000, 1, 2048], 16, None, 0),
     ("h32-prefill-ctx", dict(), [2000], None, [1, 3, 4, 5, 1999, 2000, 1500, 17], 0),
     ("h32-fk3", dict(first_key=3), [701, 40], None, None, 0),
     ("h8-kp8", dict(index_heads=8, index_kpool=8, index_topk=64), [1601, 3], None, None, 0),
