@@ -635,7 +635,7 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
         return;
     }
 
-    // Round 0: this slice's top-kt, kt = min(k, 2 ceil(k / C)) (twice a slice's share
+    // Exchange 0: this slice's top-kt, kt = min(k, 2 ceil(k / C)) (twice a slice's share
     // of the row's top-k), staged in slot crank of this CTA's merge area with bounds
     // (chosen keys are >= the slice threshold and <= the slice maximum), count and
     // whether keys were left out; one bulk copy per part moves the slot to the same
@@ -643,14 +643,14 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
     // candidates hold the row's top-k whenever every slice that left keys out has a
     // threshold below T: each left-out key is then below T, so every key >= T is a
     // candidate, and slot order keeps equal keys in id order. Otherwise (a row whose
-    // top keys crowd into one slice) round 1 repeats the exchange with every slice's
+    // top keys crowd into one slice) exchange 1 repeats it with every slice's
     // full top-k, whose union always holds the row's top-k.
     const int kt = min(a.sk, 2 * ((a.sk + C - 1) / C));
     const bool trim = kt < a.sk;
     uint32_t* st = mloc + 2 * C * sk4;
     uint32_t* again_flag = reinterpret_cast<uint32_t*>(mbar + 1);  // written by CTA 0
-    for (int round = 0;; ++round) {
-        const int kr = round == 0 ? kt : a.sk;
+    for (int xg = 0;; ++xg) {
+        const int kr = xg == 0 ? kt : a.sk;
         const int w = (kr + 3) & ~3;  // slot stride (keys)
         e.mode = 1;
         e.base = begin;
@@ -665,7 +665,7 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
             st[4 * crank + 3] = mm.count > kr ? 1u : 0u;
         }
         // phase 1 (long complete: CTA 0 arrived before its slice work)
-        if (round == 0) cluster_wait();
+        if (xg == 0) cluster_wait();
         const uint32_t slot = (uint32_t)w * 4u;
         if (crank != 0) {
             fence_async_shared();  // the staged slot, written by this CTA's threads ...
@@ -675,18 +675,18 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
                 bulk_to_peer(e.rids, e.rids, slot, mbar, 0);
                 bulk_to_peer(st + 4 * crank, st + 4 * crank, 16, mbar, 0);
             }
-            // phase 2 (3 in round 1): CTA 0 arrives once every push has landed, so
-            // this CTA's shared memory is no longer read when it goes on; in round 0
+            // phase 2 (3 in exchange 1): CTA 0 arrives once every push has landed, so
+            // this CTA's shared memory is no longer read when it goes on; in exchange 0
             // it has written again_flag here before it arrives
             cluster_arrive();
             cluster_wait();
-            if (round == 1 || *reinterpret_cast<volatile uint32_t*>(again_flag) == 0u) return;
+            if (xg == 1 || *reinterpret_cast<volatile uint32_t*>(again_flag) == 0u) return;
             continue;
         }
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(mbar, (uint32_t)(C - 1) * (2u * slot + 16u));
             // bounded: a push that never lands leaves the row unselected (all -1)
-            sc.pick[0] = mbar_wait(mbar, (uint32_t)round) ? 1 : 0;
+            sc.pick[0] = mbar_wait(mbar, (uint32_t)xg) ? 1 : 0;
         }
         __syncthreads();
         const bool landed = sc.pick[0] != 0;
@@ -702,10 +702,10 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
                 mg.count += (int)st[4 * c + 2];
             }
             tm = bin_threshold(mkeys, C * w, a.sk, mg, sc, tbuf, a.tcap);
-            if (round == 0 && trim)
+            if (xg == 0 && trim)
                 for (int c = 0; c < C; ++c) again |= st[4 * c + 3] != 0u && !(st[4 * c] < tm.T);
         }
-        if (round == 0 && threadIdx.x > 0 && threadIdx.x < C) {
+        if (xg == 0 && threadIdx.x > 0 && threadIdx.x < C) {
             uint32_t d;
             asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n"
                          : "=r"(d)
@@ -713,7 +713,7 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
             asm volatile("st.shared::cluster.u32 [%0], %1;\n" ::"r"(d), "r"(again ? 1u : 0u)
                          : "memory");
         }
-        // phase 2 (3 in round 1): the pushed slots are in; the other CTAs may go on
+        // phase 2 (3 in exchange 1): the pushed slots are in; the other CTAs may go on
         __syncwarp();
         cluster_arrive();
         if (!again) {
@@ -731,7 +731,7 @@ __device__ __forceinline__ void select_row(const SelectArgs& a, cg::cluster_grou
             cluster_wait();
             return;
         }
-        cluster_wait();  // phase 2 (complete) before round 1's arrive
+        cluster_wait();  // phase 2 (complete) before exchange 1's arrive
     }
 }
 

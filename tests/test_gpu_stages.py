@@ -176,7 +176,7 @@ SELECT_CASES = [
     (1, 327680, 2048, 4, "positive"), (2, 40000, 64, 1, "ties"),
     # select_k not a multiple of 4 on clustered rows (padded merge slots)
     (3, 60000, 2044, 4, "ties"), (2, 50000, 1026, 1, "normal"),
-    # top keys crowded into one slice (the merge's second, full-top-k round)
+    # top keys crowded into one slice (the merge's second exchange, with full slice lists)
     (8, 65536, 2048, 4, "ramp"), (4, 65536, 2048, 4, "crowd"), (3, 100003, 2044, 4, "crowd"),
     (2, 16384, 2048, 4, "ramp"),
 ]
