@@ -118,8 +118,11 @@ int dsa_abi_version(void);
  *                       their partials inside a thread-block cluster when they are
  *                       at most 8, else the combine kernel merges them).
  *   DSA_OPT_SELECT_KERNEL  how rows split over a thread-block cluster are selected:
- *                       DSA_SELECT_KERNEL_MERGE (default: each CTA's slice top-k
- *                       merged in CTA 0) or DSA_SELECT_KERNEL_RADIX (the row's
+ *                       DSA_SELECT_KERNEL_MERGE (default: each CTA's slice
+ *                       candidates merged in CTA 0; a slice first sends its top
+ *                       2 ceil(k / C) and all slices send their full top-k only
+ *                       when those cannot hold the row's top-k) or
+ *                       DSA_SELECT_KERNEL_RADIX (the row's
  *                       k-th key found digit by digit from histograms shared across
  *                       the cluster). Both give the same ids.
  *   DSA_OPT_PROJECT_KERNEL  the o_absorb projection (and the front-end GEMMs):
