@@ -566,7 +566,9 @@ def test_bad_block_table_entry_sets_status():
 PROJECT_CASES = [(8, 64, 4096), (1, 64, 4096), (3, 4, 1024), (70, 16, 256), (20, 8, 128),
                  (64, 64, 4096), (128, 8, 512), (16, 64, 1024), (33, 8, 384),
                  # tall A with a short K (1,536): fewer K shares per tile (2, then 1)
-                 (8, 3, 12800), (8, 3, 36864), (40, 3, 19456)]
+                 (8, 3, 12800), (8, 3, 36864), (40, 3, 19456),
+                 # short and wide: 128 CTAs share each 64-row block (the many-CTA reduce)
+                 (8, 64, 128)]
 
 
 @pytest.fixture(params=["tcgen05", "mma"])
