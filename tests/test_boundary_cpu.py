@@ -37,6 +37,20 @@ def test_exports_every_declared_symbol(lib):
     assert lib.dsa_abi_version() == _lib.DSA_ABI_VERSION
 
 
+def test_header_constants_match_the_binding():
+    """Every integer DSA_* macro of include/dsa.h that the Python binding names has the
+    same value there, and the binding names no DSA_* constant the header lacks."""
+    import re
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    header = {m.group(1): int(m.group(2))
+              for m in re.finditer(r"^#define\s+(DSA_[A-Z0-9_]+)\s+(-?\d+)\b", text, re.M)}
+    binding = {k: v for k, v in vars(_lib).items() if k.startswith("DSA_") and isinstance(v, int)}
+    assert len(binding) >= 20
+    assert not set(binding) - set(header), sorted(set(binding) - set(header))
+    wrong = {k: (binding[k], header[k]) for k in binding if binding[k] != header[k]}
+    assert not wrong, wrong
+
+
 @pytest.mark.parametrize("args,code", [
     ((4, 2048, 512, 64), DSA_OK),
     ((0, 2048, 512, 64), DSA_ERR_CONFIG),
